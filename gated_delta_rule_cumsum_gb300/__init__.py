@@ -1,0 +1,264 @@
+"""GB300 (sm_103a) KDA forward: Python binding over the C ABI of libkda_gb300.so.
+
+Argument marshalling only.  Every step of the forward runs in the library's CUDA
+kernels; torch provides device memory and streams.  There is no CPU fallback:
+`load()` raises when the library has not been built.
+
+Binding functions carry the C names (`kda_chunk_fwd`, `kda_recurrent_fwd`,
+`kda_gate_cumsum`, ...) and take preallocated tensors exactly like the C calls.
+`chunk_kda`, `recurrent_kda` and `gate_cumsum` allocate the outputs and call
+them, mirroring kernel-fun 0.2.0.dev1 wheel, kda/ops.py `chunk_kda` and
+attention-gym PR #317 `recurrent_kda` (forward only).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+__all__ = [
+    "KDA_OK", "KDA_ERR_INVALID_ARG", "KDA_ERR_UNSUPPORTED", "KDA_ERR_BAD_CU_SEQLENS",
+    "KDA_ERR_CUDA", "KDA_ERR_TIMEOUT", "KDA_FLAG_QK_L2NORM", "KDA_FLAG_G_IS_CUMSUM",
+    "KdaError", "KdaShape", "load", "library_path", "make_shape",
+    "kda_gate_cumsum", "kda_chunk_fwd", "kda_recurrent_fwd", "kda_chunk_workspace_size",
+    "kda_read_device_status", "kda_clear_device_status", "kda_status_string",
+    "kda_last_error_message", "kda_version", "kda_profile_enable", "kda_profile_report",
+    "kda_profile_reset",
+    "chunk_kda", "recurrent_kda", "gate_cumsum",
+]
+
+KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED = 0, 1, 2
+KDA_ERR_BAD_CU_SEQLENS, KDA_ERR_CUDA, KDA_ERR_TIMEOUT = 3, 4, 5
+KDA_DTYPE_F32, KDA_DTYPE_BF16 = 0, 1
+KDA_FLAG_QK_L2NORM, KDA_FLAG_G_IS_CUMSUM = 1 << 0, 1 << 1
+KDA_DEVICE_BAD_CU_SEQLENS, KDA_DEVICE_TIMEOUT = 1 << 0, 1 << 1
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "_build", "libkda_gb300.so")
+_LIB = None
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{_STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+_STATUS_NAMES = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED",
+                 3: "KDA_ERR_BAD_CU_SEQLENS", 4: "KDA_ERR_CUDA", 5: "KDA_ERR_TIMEOUT"}
+
+
+class KdaShape(ctypes.Structure):
+    """Mirror of `kda_shape` in include/kda.h."""
+    _fields_ = [("B", ctypes.c_int32), ("T", ctypes.c_int32), ("H", ctypes.c_int32),
+                ("HV", ctypes.c_int32), ("K", ctypes.c_int32), ("V", ctypes.c_int32),
+                ("num_seqs", ctypes.c_int32), ("dtype", ctypes.c_int),
+                ("scale", ctypes.c_float), ("g_scale", ctypes.c_float),
+                ("flags", ctypes.c_uint32)]
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+# Exported symbols and their signatures (the whole C ABI).
+_VP, _SZ, _I32, _ST = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32, ctypes.c_int
+_SIGNATURES = {
+    "kda_gate_cumsum": (_ST, [_VP, _VP, _VP, ctypes.POINTER(KdaShape), _I32, _VP, _VP]),
+    "kda_chunk_fwd": (_ST, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.POINTER(KdaShape), _VP,
+                            _VP, _VP, _SZ, _VP, _VP]),
+    "kda_chunk_workspace_size": (_SZ, [ctypes.POINTER(KdaShape)]),
+    "kda_recurrent_fwd": (_ST, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.POINTER(KdaShape),
+                                _VP, _VP, _VP, _VP]),
+    "kda_read_device_status": (_ST, [_VP, ctypes.POINTER(ctypes.c_int32), _VP]),
+    "kda_clear_device_status": (_ST, [_VP, _VP]),
+    "kda_status_string": (ctypes.c_char_p, [_ST]),
+    "kda_last_error_message": (ctypes.c_char_p, []),
+    "kda_version": (ctypes.c_char_p, []),
+    "kda_profile_enable": (_ST, [ctypes.c_int]),
+    "kda_profile_report": (ctypes.c_int, [ctypes.c_char_p, _SZ, ctypes.POINTER(ctypes.c_double),
+                                          ctypes.POINTER(ctypes.c_int64), ctypes.c_int]),
+    "kda_profile_reset": (None, []),
+}
+
+
+def load() -> ctypes.CDLL:
+    """Load libkda_gb300.so (built by `gated_delta_rule_cumsum_gb300.build.build()`)."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                f"CUDA library not built: {_LIB_PATH} is missing "
+                "(run `python -c 'import __graft_entry__ as g; g.build()'`)")
+        lib = ctypes.CDLL(_LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype, fn.argtypes = res, args
+        _LIB = lib
+    return _LIB
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> Optional[ctypes.c_void_p]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(status: int):
+    if status != KDA_OK:
+        raise KdaError(status, load().kda_last_error_message().decode())
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return KDA_DTYPE_BF16
+    if t.dtype == torch.float32:
+        return KDA_DTYPE_F32
+    raise KdaError(KDA_ERR_UNSUPPORTED, f"dtype {t.dtype} (supported: bfloat16, float32)")
+
+
+def make_shape(q: torch.Tensor, v: torch.Tensor, cu_seqlens: Optional[torch.Tensor] = None,
+               scale: Optional[float] = None, g_scale: float = 1.0, flags: int = 0) -> KdaShape:
+    B, T, H, K = q.shape
+    HV, V = v.shape[2], v.shape[3]
+    N = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    return KdaShape(B, T, H, HV, K, V, N, _dtype_code(q), -1.0 if scale is None else float(scale),
+                    float(g_scale), int(flags))
+
+
+# ------------------------------------------------------------------ the C calls
+def kda_gate_cumsum(g, g_cum, cu_seqlens, shape: KdaShape, chunk_size: int, dev_status=None,
+                    stream=None):
+    _check(load().kda_gate_cumsum(_ptr(g), _ptr(g_cum), _ptr(cu_seqlens), ctypes.byref(shape),
+                                  int(chunk_size), _ptr(dev_status), _stream(stream)))
+
+
+def kda_chunk_fwd(q, k, v, g, beta, h0, cu_seqlens, shape: KdaShape, o, ht, workspace,
+                  dev_status=None, stream=None):
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().kda_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0),
+                                _ptr(cu_seqlens), ctypes.byref(shape), _ptr(o), _ptr(ht),
+                                _ptr(workspace), nbytes, _ptr(dev_status), _stream(stream)))
+
+
+def kda_chunk_workspace_size(shape: KdaShape) -> int:
+    return int(load().kda_chunk_workspace_size(ctypes.byref(shape)))
+
+
+def kda_recurrent_fwd(q, k, v, g, beta, h0, cu_seqlens, shape: KdaShape, o, ht, dev_status=None,
+                      stream=None):
+    _check(load().kda_recurrent_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0),
+                                    _ptr(cu_seqlens), ctypes.byref(shape), _ptr(o), _ptr(ht),
+                                    _ptr(dev_status), _stream(stream)))
+
+
+def kda_read_device_status(dev_status, stream=None):
+    """Synchronises the stream; returns (status, bits)."""
+    bits = ctypes.c_int32(0)
+    st = load().kda_read_device_status(_ptr(dev_status), ctypes.byref(bits), _stream(stream))
+    return int(st), int(bits.value)
+
+
+def kda_clear_device_status(dev_status, stream=None):
+    _check(load().kda_clear_device_status(_ptr(dev_status), _stream(stream)))
+
+
+def kda_status_string(status: int) -> str:
+    return load().kda_status_string(int(status)).decode()
+
+
+def kda_last_error_message() -> str:
+    return load().kda_last_error_message().decode()
+
+
+def kda_version() -> str:
+    return load().kda_version().decode()
+
+
+def kda_profile_enable(enable: bool = True):
+    _check(load().kda_profile_enable(int(bool(enable))))
+
+
+def kda_profile_reset():
+    load().kda_profile_reset()
+
+
+def kda_profile_report(max_entries: int = 32) -> dict:
+    """{kernel name: (total ms, launches)} of the kernels timed since the last reset."""
+    names = ctypes.create_string_buffer(4096)
+    ms = (ctypes.c_double * max_entries)()
+    cnt = (ctypes.c_int64 * max_entries)()
+    n = load().kda_profile_report(names, len(names), ms, cnt, max_entries)
+    if n < 0:
+        raise KdaError(KDA_ERR_CUDA, "kda_profile_report failed")
+    labels = names.raw.split(b"\0")[:n]
+    return {labels[i].decode(): (ms[i], int(cnt[i])) for i in range(n)}
+
+
+# ------------------------------------------------------- allocating wrappers
+def _prep(*ts):
+    for t in ts:
+        if t is not None:
+            if t.requires_grad:
+                raise KdaError(KDA_ERR_UNSUPPORTED,
+                               "forward only: inputs requiring grad are rejected")
+            if not t.is_cuda:
+                raise KdaError(KDA_ERR_INVALID_ARG, "tensors must be on a CUDA device")
+    return [None if t is None else t.contiguous() for t in ts]
+
+
+def new_status(device=None) -> torch.Tensor:
+    """A zeroed device status word."""
+    return torch.zeros(1, dtype=torch.int32, device=device or "cuda")
+
+
+def gate_cumsum(g, cu_seqlens=None, chunk_size: int = 64, g_scale: float = 1.0, dev_status=None,
+                stream=None):
+    """Chunk-local cumsum of g [B,T,HV,K] fp32; rows outside every sequence are zero."""
+    g, cu_seqlens = _prep(g, cu_seqlens)
+    B, T, HV, K = g.shape
+    shape = KdaShape(B, T, 1, HV, K, 1, B if cu_seqlens is None else cu_seqlens.numel() - 1,
+                     KDA_DTYPE_F32, -1.0, float(g_scale), 0)
+    out = torch.zeros_like(g)
+    kda_gate_cumsum(g, out, cu_seqlens, shape, chunk_size, dev_status, stream)
+    return out
+
+
+def chunk_kda(q, k, v, g, beta, scale=None, initial_state=None, output_final_state=False,
+              cu_seqlens=None, use_qk_l2norm_in_kernel=False, g_scale=1.0, g_is_cumsum=False,
+              workspace=None, dev_status=None, stream=None):
+    """Chunked forward; returns (o, ht or None).  `g` is the per-token log2 gate."""
+    q, k, v, g, beta, h0, cu = _prep(q, k, v, g, beta, initial_state, cu_seqlens)
+    flags = (KDA_FLAG_QK_L2NORM if use_qk_l2norm_in_kernel else 0) | (
+        KDA_FLAG_G_IS_CUMSUM if g_is_cumsum else 0)
+    shape = make_shape(q, v, cu, scale, g_scale, flags)
+    o = torch.empty(v.shape, dtype=q.dtype, device=q.device)
+    ht = (torch.empty(shape.num_seqs, shape.HV, shape.K, shape.V, dtype=torch.float32,
+                      device=q.device) if output_final_state else None)
+    if workspace is None:
+        workspace = torch.empty(max(kda_chunk_workspace_size(shape), 256), dtype=torch.uint8,
+                                device=q.device)
+    kda_chunk_fwd(q, k, v, g, beta, h0, cu, shape, o, ht, workspace, dev_status, stream)
+    return o, ht
+
+
+def recurrent_kda(q, k, v, gate, beta, initial_state=None, *, cu_seqlens=None,
+                  output_final_state=False, scale=None, use_qk_l2norm_in_kernel=False,
+                  g_scale=1.0, dev_status=None, stream=None, final_state_out=None):
+    """Token-by-token forward; returns (o, ht or None).  `gate` is the per-token log2 gate."""
+    q, k, v, g, beta, h0, cu = _prep(q, k, v, gate, beta, initial_state, cu_seqlens)
+    flags = KDA_FLAG_QK_L2NORM if use_qk_l2norm_in_kernel else 0
+    shape = make_shape(q, v, cu, scale, g_scale, flags)
+    o = torch.empty(v.shape, dtype=q.dtype, device=q.device)
+    ht = final_state_out
+    if ht is None and output_final_state:
+        ht = torch.empty(shape.num_seqs, shape.HV, shape.K, shape.V, dtype=torch.float32,
+                         device=q.device)
+    kda_recurrent_fwd(q, k, v, g, beta, h0, cu, shape, o, ht, dev_status, stream)
+    return o, ht

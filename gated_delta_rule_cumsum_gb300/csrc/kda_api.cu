@@ -1,0 +1,253 @@
+// kda_api.cu -- the extern "C" entry points declared in include/kda.h:
+// host-side argument checks, workspace carving and kernel launches.
+#include <climits>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <string>
+
+#include "kda_internal.cuh"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+kda_status fail(kda_status st, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return st;
+}
+
+kda_status cuda_fail(cudaError_t e, const char *where) {
+    return fail(KDA_ERR_CUDA, "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+constexpr uint32_t kKnownFlags = KDA_FLAG_QK_L2NORM | KDA_FLAG_G_IS_CUMSUM;
+
+// Checks shared by the three operations.  `need_h` also checks H and HV % H.
+kda_status check_common(const char *op, const kda_shape *s, const int32_t *cu) {
+    if (!s) return fail(KDA_ERR_INVALID_ARG, "%s: shape is NULL", op);
+    if (s->B <= 0 || s->T < 0 || s->H <= 0 || s->HV <= 0 || s->K <= 0 || s->V <= 0)
+        return fail(KDA_ERR_INVALID_ARG,
+                    "%s: sizes must be positive (B=%d T=%d H=%d HV=%d K=%d V=%d)", op, s->B, s->T,
+                    s->H, s->HV, s->K, s->V);
+    if (s->HV % s->H != 0)
+        return fail(KDA_ERR_INVALID_ARG, "%s: HV=%d must be divisible by H=%d", op, s->HV, s->H);
+    if (s->HV > 65535) return fail(KDA_ERR_UNSUPPORTED, "%s: HV=%d > 65535", op, s->HV);
+    if (cu) {
+        if (s->B != 1)
+            return fail(KDA_ERR_INVALID_ARG, "%s: packed sequences (cu_seqlens) need B == 1, got %d",
+                        op, s->B);
+        if (s->num_seqs < 0)
+            return fail(KDA_ERR_INVALID_ARG, "%s: num_seqs=%d < 0", op, s->num_seqs);
+    } else if (s->num_seqs != s->B) {
+        return fail(KDA_ERR_INVALID_ARG, "%s: num_seqs=%d must equal B=%d without cu_seqlens", op,
+                    s->num_seqs, s->B);
+    }
+    if (s->dtype != KDA_DTYPE_F32 && s->dtype != KDA_DTYPE_BF16)
+        return fail(KDA_ERR_INVALID_ARG, "%s: unknown dtype %d", op, (int)s->dtype);
+    if (s->flags & ~kKnownFlags)
+        return fail(KDA_ERR_UNSUPPORTED, "%s: unknown flag bits 0x%x", op, s->flags & ~kKnownFlags);
+    if (!std::isfinite(s->g_scale))
+        return fail(KDA_ERR_INVALID_ARG, "%s: g_scale is not finite", op);
+    // Element counts must fit comfortably in 64-bit index arithmetic and rows in int32.
+    const double elems = (double)s->B * s->T * s->HV * (s->K > s->V ? s->K : s->V);
+    if (elems > 4e18 || (double)s->B * s->T > INT_MAX)
+        return fail(KDA_ERR_UNSUPPORTED, "%s: tensor too large", op);
+    return KDA_OK;
+}
+
+float resolve_scale(const kda_shape *s) {
+    return s->scale > 0.f ? s->scale : 1.0f / std::sqrt((float)s->K);
+}
+
+kda_status check_fwd_pointers(const char *op, const kda_shape *s, const void *q, const void *k,
+                              const void *v, const float *g, const void *beta, const void *o,
+                              const int32_t *cu) {
+    const bool has_rows = (int64_t)s->B * s->T > 0;
+    if (has_rows && (!q || !k || !v || !g || !beta || !o))
+        return fail(KDA_ERR_INVALID_ARG, "%s: q, k, v, g, beta and o must be non-NULL", op);
+    if (cu == nullptr && s->num_seqs != s->B)
+        return fail(KDA_ERR_INVALID_ARG, "%s: num_seqs must equal B", op);
+    return KDA_OK;
+}
+
+struct ChunkWs {
+    size_t ctrl, chunk_start, units, total, unit_bytes;
+    int64_t slots;
+};
+
+ChunkWs chunk_ws_layout(const kda_shape *s, bool packed) {
+    ChunkWs L;
+    L.slots = kda::chunk_slots(*s, packed);
+    L.unit_bytes = kda::chunk_simt_unit_bytes(s->K, s->V);
+    L.ctrl = 0;
+    L.chunk_start = 256;
+    L.units = L.chunk_start + kda::align_up(sizeof(int32_t) * ((size_t)s->num_seqs + 1), 256);
+    L.total = L.units + (size_t)L.slots * s->HV * L.unit_bytes;
+    return L;
+}
+
+kda_status check_chunk_support(const char *op, const kda_shape *s) {
+    if (s->K != 64 && s->K != 128)
+        return fail(KDA_ERR_UNSUPPORTED, "%s: K=%d (supported: 64, 128)", op, s->K);
+    if (s->V > 256) return fail(KDA_ERR_UNSUPPORTED, "%s: V=%d > 256", op, s->V);
+    return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *kda_version(void) { return "0.1.0"; }
+
+const char *kda_status_string(kda_status st) {
+    switch (st) {
+        case KDA_OK: return "KDA_OK";
+        case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG";
+        case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED";
+        case KDA_ERR_BAD_CU_SEQLENS: return "KDA_ERR_BAD_CU_SEQLENS";
+        case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
+        case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT";
+    }
+    return "KDA_ERR_UNKNOWN";
+}
+
+const char *kda_last_error_message(void) { return g_last_error.c_str(); }
+
+kda_status kda_gate_cumsum(const float *g, float *g_cum, const int32_t *cu_seqlens,
+                           const kda_shape *shape, int32_t chunk_size, int32_t *dev_status,
+                           kda_stream_t stream) {
+    const char *op = "kda_gate_cumsum";
+    kda_status st = check_common(op, shape, cu_seqlens);
+    if (st != KDA_OK) return st;
+    if (chunk_size < 1 || chunk_size > 64)
+        return fail(KDA_ERR_UNSUPPORTED, "%s: chunk_size=%d (supported: 1..64)", op, chunk_size);
+    if ((int64_t)shape->B * shape->T > 0) {
+        if (!g || !g_cum) return fail(KDA_ERR_INVALID_ARG, "%s: g and g_cum must be non-NULL", op);
+        if (g == g_cum) return fail(KDA_ERR_INVALID_ARG, "%s: g_cum must not alias g", op);
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (cu_seqlens) {
+        e = kda::launch_validate_offsets(cu_seqlens, shape->num_seqs, shape->T, dev_status, nullptr,
+                                         nullptr, s);
+        if (e != cudaSuccess) return cuda_fail(e, op);
+    }
+    e = kda::launch_gate_cumsum(g, g_cum, cu_seqlens, *shape, chunk_size, s);
+    if (e != cudaSuccess) return cuda_fail(e, op);
+    g_last_error.clear();
+    return KDA_OK;
+}
+
+kda_status kda_recurrent_fwd(const void *q, const void *k, const void *v, const float *g,
+                             const void *beta, const float *h0, const int32_t *cu_seqlens,
+                             const kda_shape *shape, void *o, float *ht, int32_t *dev_status,
+                             kda_stream_t stream) {
+    const char *op = "kda_recurrent_fwd";
+    kda_status st = check_common(op, shape, cu_seqlens);
+    if (st != KDA_OK) return st;
+    if ((st = check_fwd_pointers(op, shape, q, k, v, g, beta, o, cu_seqlens)) != KDA_OK) return st;
+    if (shape->flags & KDA_FLAG_G_IS_CUMSUM)
+        return fail(KDA_ERR_UNSUPPORTED, "%s: g is the per-token gate; KDA_FLAG_G_IS_CUMSUM is "
+                    "for kda_chunk_fwd", op);
+    if (shape->K > 256) return fail(KDA_ERR_UNSUPPORTED, "%s: K=%d > 256", op, shape->K);
+    const int64_t blocks = (int64_t)shape->num_seqs * shape->HV * ((shape->V + 127) / 128);
+    if (blocks > INT_MAX) return fail(KDA_ERR_UNSUPPORTED, "%s: grid too large", op);
+    kda::RecurrentArgs a;
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.h0 = h0; a.cu = cu_seqlens;
+    a.o = o; a.ht = ht; a.status = dev_status;
+    a.B = shape->B; a.T = shape->T; a.H = shape->H; a.HV = shape->HV; a.K = shape->K;
+    a.V = shape->V; a.N = shape->num_seqs;
+    a.scale = resolve_scale(shape);
+    a.g_scale = shape->g_scale;
+    a.l2norm = (shape->flags & KDA_FLAG_QK_L2NORM) ? 1 : 0;
+    cudaError_t e = kda::launch_recurrent(a, shape->dtype, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, op);
+    g_last_error.clear();
+    return KDA_OK;
+}
+
+size_t kda_chunk_workspace_size(const kda_shape *shape) {
+    if (!shape || shape->K <= 0 || shape->V <= 0 || shape->HV <= 0 || shape->B <= 0 ||
+        shape->T < 0 || shape->num_seqs < 0)
+        return 0;
+    const bool packed = shape->num_seqs != shape->B || shape->B == 1;
+    return chunk_ws_layout(shape, packed).total;
+}
+
+kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const float *g,
+                         const void *beta, const float *h0, const int32_t *cu_seqlens,
+                         const kda_shape *shape, void *o, float *ht, void *workspace,
+                         size_t workspace_bytes, int32_t *dev_status, kda_stream_t stream) {
+    const char *op = "kda_chunk_fwd";
+    kda_status st = check_common(op, shape, cu_seqlens);
+    if (st != KDA_OK) return st;
+    if ((st = check_fwd_pointers(op, shape, q, k, v, g, beta, o, cu_seqlens)) != KDA_OK) return st;
+    if ((st = check_chunk_support(op, shape)) != KDA_OK) return st;
+    const bool packed = cu_seqlens != nullptr;
+    const ChunkWs L = chunk_ws_layout(shape, packed);
+    if (L.slots > INT_MAX) return fail(KDA_ERR_UNSUPPORTED, "%s: too many chunks", op);
+    const size_t need = kda_chunk_workspace_size(shape);
+    if (!workspace || workspace_bytes < need)
+        return fail(KDA_ERR_INVALID_ARG, "%s: workspace of %zu bytes needed, %zu given", op, need,
+                    workspace_bytes);
+    if ((uintptr_t)workspace % 256 != 0)
+        return fail(KDA_ERR_INVALID_ARG, "%s: workspace must be 256-byte aligned", op);
+
+    char *ws = static_cast<char *>(workspace);
+    kda::ChunkArgs a;
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.h0 = h0; a.cu = cu_seqlens;
+    a.o = o; a.ht = ht; a.status = dev_status;
+    a.B = shape->B; a.T = shape->T; a.H = shape->H; a.HV = shape->HV; a.K = shape->K;
+    a.V = shape->V; a.N = shape->num_seqs;
+    a.scale = resolve_scale(shape);
+    a.g_scale = shape->g_scale;
+    a.l2norm = (shape->flags & KDA_FLAG_QK_L2NORM) ? 1 : 0;
+    a.g_is_cumsum = (shape->flags & KDA_FLAG_G_IS_CUMSUM) ? 1 : 0;
+    a.ctrl = reinterpret_cast<kda::ChunkCtrl *>(ws + L.ctrl);
+    a.chunk_start = reinterpret_cast<int32_t *>(ws + L.chunk_start);
+    a.units = ws + L.units;
+    a.slots = L.slots;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (packed) {
+        e = kda::launch_validate_offsets(cu_seqlens, a.N, a.T, dev_status, a.ctrl, a.chunk_start, s);
+        if (e != cudaSuccess) return cuda_fail(e, op);
+    }
+    e = kda::launch_chunk_simt(a, shape->dtype, s);
+    if (e != cudaSuccess) return cuda_fail(e, op);
+    g_last_error.clear();
+    return KDA_OK;
+}
+
+kda_status kda_read_device_status(const int32_t *dev_status, int32_t *host_bits,
+                                  kda_stream_t stream) {
+    if (!dev_status) return fail(KDA_ERR_INVALID_ARG, "kda_read_device_status: NULL status word");
+    int32_t bits = 0;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(&bits, dev_status, sizeof(bits), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "kda_read_device_status");
+    if (host_bits) *host_bits = bits;
+    if (bits & KDA_DEVICE_BAD_CU_SEQLENS)
+        return fail(KDA_ERR_BAD_CU_SEQLENS, "device reported invalid cu_seqlens");
+    if (bits & KDA_DEVICE_TIMEOUT)
+        return fail(KDA_ERR_TIMEOUT, "a bounded device-side wait timed out");
+    return KDA_OK;
+}
+
+kda_status kda_clear_device_status(int32_t *dev_status, kda_stream_t stream) {
+    if (!dev_status) return fail(KDA_ERR_INVALID_ARG, "kda_clear_device_status: NULL status word");
+    cudaError_t e = cudaMemsetAsync(dev_status, 0, sizeof(int32_t),
+                                    reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "kda_clear_device_status");
+    return KDA_OK;
+}
+
+}  // extern "C"

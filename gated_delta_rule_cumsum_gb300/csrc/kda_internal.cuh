@@ -1,0 +1,116 @@
+// kda_internal.cuh -- device helpers and launcher declarations shared by the
+// translation units of the KDA library.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kda.h"
+
+namespace kda {
+
+// Chunk length of the chunked form (kernel-fun 0.2.0.dev1 sdist, ALGORITHM.md,
+// preamble: BT = 64).
+constexpr int kBT = 64;
+
+// ----------------------------------------------------------------- scalar I/O
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T>
+__device__ __forceinline__ T from_f32(float x);
+template <>
+__device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+
+__device__ __forceinline__ void report(int32_t *status, int bits) {
+    if (status) atomicOr(status, bits);
+}
+
+// Largest index i in [0, n) with a[i] <= x (a non-decreasing); 0 if none.
+// Stays in bounds for any contents of a.
+__device__ __forceinline__ int upper_bound_minus_one(const int32_t *a, int n, int x) {
+    int lo = 0, hi = n;  // first index with a[i] > x lies in [lo, hi]
+    while (lo < hi) {
+        int mid = (lo + hi) >> 1;
+        if (a[mid] <= x)
+            lo = mid + 1;
+        else
+            hi = mid;
+    }
+    return lo > 0 ? lo - 1 : 0;
+}
+
+// ----------------------------------------------------------- workspace layout
+// Control block at the start of the chunk workspace, written every call by the
+// offsets pre-pass and read by the later kernels of the same call.
+struct ChunkCtrl {
+    int32_t valid;         // 1 when the offsets passed validation
+    int32_t total_chunks;  // sum over sequences of ceil(len / BT)
+    int32_t pad[62];       // 256 bytes
+};
+
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Upper bound on the number of BT-row chunks of a call (host and device).
+__host__ __device__ inline int64_t chunk_slots(const kda_shape &s, bool packed) {
+    const int64_t ntc = (s.T + kBT - 1) / kBT;
+    return packed ? ntc + s.num_seqs : (int64_t)s.B * ntc;
+}
+
+// ------------------------------------------------------------- stage timing
+// When enabled (kda_profile_enable), every kernel the library enqueues is
+// bracketed by a pair of CUDA events on its stream; kda_profile_report sums
+// the elapsed times per kernel name.  No-ops when disabled.
+void prof_begin(const char *name, cudaStream_t st);
+void prof_end(cudaStream_t st);
+
+// --------------------------------------------------------------- launchers
+// Each returns the launch error (cudaSuccess when enqueued).
+cudaError_t launch_validate_offsets(const int32_t *cu, int N, int T, int32_t *dev_status,
+                                    ChunkCtrl *ctrl, int32_t *chunk_start, cudaStream_t st);
+
+cudaError_t launch_gate_cumsum(const float *g, float *out, const int32_t *cu, const kda_shape &s,
+                               int chunk, cudaStream_t st);
+
+struct RecurrentArgs {
+    const void *q, *k, *v;
+    const float *g;
+    const void *beta;
+    const float *h0;
+    const int32_t *cu;
+    void *o;
+    float *ht;
+    int32_t *status;
+    int B, T, H, HV, K, V, N;
+    float scale, g_scale;
+    int l2norm;
+};
+cudaError_t launch_recurrent(const RecurrentArgs &a, kda_dtype dt, cudaStream_t st);
+
+struct ChunkArgs {
+    const void *q, *k, *v;
+    const float *g;
+    const void *beta;
+    const float *h0;
+    const int32_t *cu;
+    void *o;
+    float *ht;
+    int32_t *status;
+    int B, T, H, HV, K, V, N;
+    float scale, g_scale;
+    int l2norm, g_is_cumsum;
+    // workspace, carved by the host
+    ChunkCtrl *ctrl;
+    int32_t *chunk_start;  // [N + 1] (packed only)
+    void *units;           // per-(chunk, value head) intermediates
+    int64_t slots;         // chunk slots (upper bound)
+};
+size_t chunk_simt_unit_bytes(int K, int V);
+cudaError_t launch_chunk_simt(const ChunkArgs &a, kda_dtype dt, cudaStream_t st);
+
+}  // namespace kda

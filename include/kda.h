@@ -1,0 +1,204 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) library for the KDA forward pass.
+ *
+ * KDA (Kimi Delta Attention) is a gated delta rule with a per-channel diagonal
+ * decay.  Per (sequence n, value head hv), with q/k taken from head
+ * h = hv / (HV / H), an fp32 state S of shape [K, V] evolves as
+ *
+ *     S_t = (I - beta_t k_t k_t^T) Diag(2^{g_t}) S_{t-1} + beta_t k_t v_t^T
+ *     o_t = scale * S_t^T q_t,            scale = K^{-1/2} unless given,
+ *
+ * with g_t <= 0 a base-2 log decay per channel (kernel-fun 0.2.0.dev1 sdist,
+ * ALGORITHM.md, preamble; attention-gym PR #317 "Add fused recurrent_kda for
+ * decode and inference prefill", PR description).
+ *
+ * Three operations:
+ *   kda_gate_cumsum    chunk-local gate cumsum (ALGORITHM.md, Stage 1)
+ *   kda_chunk_fwd      chunked forward, BT = 64 (ALGORITHM.md, Stages 1-4)
+ *   kda_recurrent_fwd  token-by-token forward for decode (PR #317)
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Memory.  Every tensor pointer is a DEVICE pointer owned by the caller, on
+ * the current CUDA device.  The library allocates no memory and keeps no
+ * global state beyond a per-process cache of device attributes.  All work is
+ * enqueued on `stream` (NULL = the legacy default stream); calls return
+ * without synchronising, except kda_read_device_status.
+ *
+ * Layouts (all C-contiguous, row-major):
+ *   q, k        [B, T, H, K]     dtype `shape->dtype`
+ *   v, o        [B, T, HV, V]    dtype `shape->dtype`  (o has q's dtype)
+ *   g, g_cum    [B, T, HV, K]    fp32 (the gate is per VALUE head)
+ *   beta        [B, T, HV]       dtype `shape->dtype`
+ *   h0, ht      [N, HV, K, V]    fp32, K-major state, one entry per sequence
+ *   cu_seqlens  [N + 1]          int32, device resident
+ * With cu_seqlens == NULL the batch is dense: N = B and row b is one sequence
+ * of T tokens.  With cu_seqlens != NULL the batch is packed: B must be 1, T is
+ * the physical capacity, and sequence n occupies rows [cu[n], cu[n+1]).
+ * Packed-sequence contract (attention-gym PR #317, PR description; review
+ * comments on offset validation): offsets must satisfy cu[0] == 0,
+ * cu[n] <= cu[n+1] and cu[N] <= T.  Repeated offsets are empty slots whose
+ * final state is h0 copied bit for bit (+0.0 when h0 is NULL).  Rows at or
+ * beyond cu[N] are outside the contract: never written, and their input values
+ * (NaN included) never reach any output.
+ *
+ * Errors.  Arguments the host can check are checked before anything is
+ * enqueued; a failing call returns KDA_ERR_INVALID_ARG or KDA_ERR_UNSUPPORTED,
+ * enqueues nothing, and kda_last_error_message() says why.  Offsets live on
+ * the device and are validated there on every call (graph replay included):
+ * invalid offsets never trap and never cause an out-of-bounds access; the
+ * work they govern is skipped and bit KDA_DEVICE_BAD_CU_SEQLENS is OR-ed into
+ * *dev_status (when dev_status is not NULL).  Outputs are unspecified for a
+ * call whose status word reports an error.  The status word is only written
+ * by OR; clear it with kda_clear_device_status.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Binary-compatible with cudaStream_t. */
+typedef struct CUstream_st *kda_stream_t;
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1,      /* malformed arguments (host-detected)         */
+    KDA_ERR_UNSUPPORTED = 2,      /* well-formed but outside the supported set    */
+    KDA_ERR_BAD_CU_SEQLENS = 3,   /* reported via the device status word          */
+    KDA_ERR_CUDA = 4,             /* a CUDA runtime call or a launch failed        */
+    KDA_ERR_TIMEOUT = 5           /* a bounded on-device wait gave up              */
+} kda_status;
+
+typedef enum {
+    KDA_DTYPE_F32 = 0,            /* q, k, v, beta, o in fp32                     */
+    KDA_DTYPE_BF16 = 1            /* q, k, v, beta, o in bf16                     */
+} kda_dtype;
+
+/* shape->flags */
+#define KDA_FLAG_QK_L2NORM   (1u << 0)  /* L2-normalise q and k rows inside the op:
+                                           x / sqrt(sum x^2 + 1e-6)  (kernel-fun
+                                           0.2.0.dev1 wheel, kda/autograd.py,
+                                           use_qk_l2norm)                          */
+#define KDA_FLAG_G_IS_CUMSUM (1u << 1)  /* kda_chunk_fwd only: g already holds the
+                                           chunk-local cumsum (kda_gate_cumsum
+                                           output with chunk_size 64)             */
+
+/* Bits of the device status word. */
+#define KDA_DEVICE_BAD_CU_SEQLENS (1 << 0)
+#define KDA_DEVICE_TIMEOUT        (1 << 1)
+
+typedef struct {
+    int32_t B, T, H, HV, K, V;  /* see Layouts; HV % H == 0                         */
+    int32_t num_seqs;           /* N: B when dense, len(cu_seqlens) - 1 when packed  */
+    kda_dtype dtype;            /* of q, k, v, beta and o                           */
+    float scale;                /* readout scale; <= 0 selects K^{-1/2}             */
+    float g_scale;              /* multiplier applied to g before use: 1 for base-2
+                                   log gates, 1/ln 2 for natural-log gates          */
+    uint32_t flags;             /* KDA_FLAG_*                                       */
+} kda_shape;
+
+/*
+ * kda_gate_cumsum -- chunk-local inclusive cumsum of the gate.
+ * Defined in kernel-fun 0.2.0.dev1 sdist, ALGORITHM.md, "Stage 1 -- cumsum":
+ *     g_cum[t, hv, d] = g_scale * sum_{s = c(t)}^{t} g[s, hv, d]
+ * where c(t) is the first row of t's chunk, chunks of `chunk_size` rows being
+ * counted from the first row of t's own sequence.  chunk_size == 1 is the
+ * identity (times g_scale), as with attention-gym's bounded_gate_cumsum with
+ * chunk_size=1 (PR #317, PR description).
+ *   g, g_cum   [B, T, HV, K] fp32; must not alias; rows outside every sequence
+ *              of g_cum are not written.
+ *   chunk_size 1 <= chunk_size <= 64.
+ *   Only B, T, H, HV, K, num_seqs and g_scale of *shape are used (H >= 1).
+ */
+kda_status kda_gate_cumsum(const float *g, float *g_cum, const int32_t *cu_seqlens,
+                           const kda_shape *shape, int32_t chunk_size, int32_t *dev_status,
+                           kda_stream_t stream);
+
+/*
+ * kda_chunk_fwd -- the chunked forward with chunks of BT = 64 rows.
+ * Defined in kernel-fun 0.2.0.dev1 sdist, ALGORITHM.md, "Forward" (Stage 1
+ * cumsum, Stage 2 intra/WY, Stage 3+4 scan + o); arguments and return contract
+ * of kernel-fun 0.2.0.dev1 wheel, kda/ops.py, chunk_kda (o in q's dtype, ht
+ * only when asked for, a NULL initial state meaning zeros).  Reaches the
+ * result of the token recurrence above up to rounding.
+ *   q, k, v, g, beta   inputs (Layouts).  g is the per-token log decay unless
+ *                      KDA_FLAG_G_IS_CUMSUM is set.
+ *   h0                 [N, HV, K, V] fp32 or NULL (zeros).
+ *   o                  [B, T, HV, V] output, dtype of q.
+ *   ht                 [N, HV, K, V] fp32 final state, or NULL (not stored).
+ *                      May alias h0.
+ *   workspace          device scratch of at least kda_chunk_workspace_size()
+ *                      bytes, 256-byte aligned; its contents on entry do not
+ *                      matter and on return are unspecified.  Calls that share
+ *                      one workspace must be ordered on the GPU.
+ * Supported: K in {64, 128}; 1 <= V <= 256; K, V multiples of 16 for bf16.
+ */
+kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const float *g,
+                         const void *beta, const float *h0, const int32_t *cu_seqlens,
+                         const kda_shape *shape, void *o, float *ht, void *workspace,
+                         size_t workspace_bytes, int32_t *dev_status, kda_stream_t stream);
+
+/* Bytes of workspace kda_chunk_fwd needs for *shape (0 on invalid shapes). */
+size_t kda_chunk_workspace_size(const kda_shape *shape);
+
+/*
+ * kda_recurrent_fwd -- token-by-token forward for decode and inference prefill.
+ * Defined in attention-gym PR #317, PR description: one sequential scan over
+ * the tokens of each (sequence, head, value block) with the [K, BV] fp32 state
+ * held in registers, fp32 arithmetic whatever the input dtype, queries scaled
+ * by 1/sqrt(K); work flattened onto grid x so that N * HV beyond 65535 works
+ * (PR #317, review comment on grid Y).
+ *   g         per-token log decay (KDA_FLAG_G_IS_CUMSUM is rejected).
+ *   h0, ht    as for kda_chunk_fwd; ht == h0 (in-place decode) is allowed.
+ * Supported: 1 <= K <= 256, 1 <= V (any size; value blocks of 128 columns).
+ */
+kda_status kda_recurrent_fwd(const void *q, const void *k, const void *v, const float *g,
+                             const void *beta, const float *h0, const int32_t *cu_seqlens,
+                             const kda_shape *shape, void *o, float *ht, int32_t *dev_status,
+                             kda_stream_t stream);
+
+/*
+ * kda_read_device_status -- synchronise `stream`, copy the status word to
+ * *host_bits (may be NULL) and map it to a status: KDA_OK when no bit is set,
+ * KDA_ERR_BAD_CU_SEQLENS or KDA_ERR_TIMEOUT otherwise.  Does not clear it.
+ */
+kda_status kda_read_device_status(const int32_t *dev_status, int32_t *host_bits,
+                                  kda_stream_t stream);
+
+/* kda_clear_device_status -- enqueue a reset of the status word to 0. */
+kda_status kda_clear_device_status(int32_t *dev_status, kda_stream_t stream);
+
+/*
+ * Stage timing for benchmarks (not needed for correct use).  While enabled,
+ * every kernel the library enqueues is bracketed by two CUDA events recorded
+ * on the caller's stream; do not enable it around stream capture.
+ * kda_profile_report synchronises the recorded events and writes up to
+ * max_entries rows: the kernel's name (NUL-separated into names, at most
+ * names_len bytes), its summed duration in milliseconds and its launch count.
+ * It returns the number of rows (or -1 on a CUDA error).  Reset clears the
+ * totals.  Process-wide, guarded by a mutex.
+ */
+kda_status kda_profile_enable(int enable);
+int kda_profile_report(char *names, size_t names_len, double *total_ms, int64_t *launches,
+                       int max_entries);
+void kda_profile_reset(void);
+
+/* Static text for a status code. */
+const char *kda_status_string(kda_status status);
+
+/* Reason for the most recent non-OK return on the calling host thread. */
+const char *kda_last_error_message(void);
+
+/* Library version, "major.minor.patch". */
+const char *kda_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

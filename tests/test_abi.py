@@ -1,0 +1,145 @@
+"""The C ABI without a GPU: the library loads, exports every symbol include/kda.h
+declares, and rejects malformed arguments on the host before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kda.h")
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z_0-9]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from gated_delta_rule_cumsum_gb300 import build as b
+
+    b.build()
+    import gated_delta_rule_cumsum_gb300 as kda
+
+    return kda.load()
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for must in ("kda_gate_cumsum", "kda_chunk_fwd", "kda_recurrent_fwd",
+                 "kda_chunk_workspace_size", "kda_read_device_status", "kda_status_string"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), f"{name} declared in kda.h but not exported"
+
+
+def test_binding_covers_every_declared_symbol():
+    import gated_delta_rule_cumsum_gb300 as kda
+
+    for name in _declared_functions():
+        assert hasattr(kda, name), f"binding lacks {name}"
+
+
+def test_status_strings(lib):
+    import gated_delta_rule_cumsum_gb300 as kda
+
+    assert kda.kda_status_string(0) == "KDA_OK"
+    assert kda.kda_status_string(3) == "KDA_ERR_BAD_CU_SEQLENS"
+    assert kda.kda_version().count(".") == 2
+
+
+def _shape(**kw):
+    import gated_delta_rule_cumsum_gb300 as kda
+
+    d = dict(B=1, T=128, H=2, HV=4, K=64, V=64, num_seqs=1, dtype=1, scale=-1.0, g_scale=1.0,
+             flags=0)
+    d.update(kw)
+    return kda.KdaShape(**d)
+
+
+FAKE = ctypes.c_void_p(0x1000)  # never dereferenced: the host checks fail first
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(HV=3), 1),              # HV % H != 0
+    (dict(K=0), 1),
+    (dict(num_seqs=2), 1),        # dense: num_seqs must equal B
+    (dict(dtype=7), 1),
+    (dict(flags=1 << 9), 2),      # unknown flag
+    (dict(K=96), 2),              # chunk path: K in {64, 128}
+    (dict(V=512), 2),
+])
+def test_chunk_fwd_rejects_on_host(lib, kw, status):
+    s = _shape(**kw)
+    st = lib.kda_chunk_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, None, None, ctypes.byref(s), FAKE, None,
+                           FAKE, 1 << 30, None, None)
+    assert st == status, lib.kda_last_error_message()
+    assert lib.kda_last_error_message()
+
+
+def test_chunk_fwd_rejects_small_or_misaligned_workspace(lib):
+    s = _shape()
+    need = lib.kda_chunk_workspace_size(ctypes.byref(s))
+    assert need > 0
+    st = lib.kda_chunk_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, None, None, ctypes.byref(s), FAKE, None,
+                           ctypes.c_void_p(0x100000), need - 1, None, None)
+    assert st == 1 and b"workspace" in lib.kda_last_error_message()
+    st = lib.kda_chunk_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, None, None, ctypes.byref(s), FAKE, None,
+                           ctypes.c_void_p(0x100010), need + 64, None, None)
+    assert st == 1 and b"aligned" in lib.kda_last_error_message()
+
+
+def test_packed_requires_batch_one(lib):
+    s = _shape(B=2, num_seqs=3)
+    st = lib.kda_recurrent_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, ctypes.byref(s), FAKE,
+                               None, None, None)
+    assert st == 1
+
+
+def test_recurrent_rejects_cumsum_flag_and_large_k(lib):
+    s = _shape(flags=2)
+    assert lib.kda_recurrent_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, None, None, ctypes.byref(s), FAKE,
+                                 None, None, None) == 2
+    s = _shape(K=300)
+    assert lib.kda_recurrent_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, None, None, ctypes.byref(s), FAKE,
+                                 None, None, None) == 2
+
+
+def test_null_tensors_rejected(lib):
+    s = _shape()
+    assert lib.kda_recurrent_fwd(None, FAKE, FAKE, FAKE, FAKE, None, None, ctypes.byref(s), FAKE,
+                                 None, None, None) == 1
+    assert lib.kda_gate_cumsum(FAKE, FAKE, None, None, 64, None, None) == 1
+
+
+def test_gate_cumsum_rejects_alias_and_chunk(lib):
+    s = _shape()
+    assert lib.kda_gate_cumsum(FAKE, FAKE, None, ctypes.byref(s), 64, None, None) == 1
+    assert lib.kda_gate_cumsum(FAKE, ctypes.c_void_p(0x2000), None, ctypes.byref(s), 65, None,
+                               None) == 2
+
+
+def test_workspace_size_scales_with_chunks(lib):
+    a = lib.kda_chunk_workspace_size(ctypes.byref(_shape(T=64)))
+    b = lib.kda_chunk_workspace_size(ctypes.byref(_shape(T=640)))
+    assert b > a > 0
+    assert lib.kda_chunk_workspace_size(None) == 0
+
+
+def test_product_never_imports_the_oracle():
+    """The product path has no CPU fallback: neither the binding nor the CUDA
+    sources mention the oracle."""
+    pkg = os.path.join(ROOT, "gated_delta_rule_cumsum_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        if "_build" in dirpath:
+            continue
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "kda_oracle" not in text, f
