@@ -25,6 +25,7 @@ SOURCES = [
     "kda_recurrent.cu",
     "kda_cumsum.cu",
     "kda_chunk_simt.cu",
+    "kda_chunk_tc.cu",
     "kda_profile.cu",
 ]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -81,10 +81,17 @@ struct ChunkWs {
     int64_t slots;
 };
 
+// The tensor-core path serves bf16 inputs whose K and V it supports; fp32
+// inputs (and bf16 shapes outside that set) take the fp32 SIMT path.
+bool use_tc(const kda_shape *s) {
+    return s->dtype == KDA_DTYPE_BF16 && kda::chunk_tc_supported(s->K, s->V);
+}
+
 ChunkWs chunk_ws_layout(const kda_shape *s, bool packed) {
     ChunkWs L;
     L.slots = kda::chunk_slots(*s, packed);
-    L.unit_bytes = kda::chunk_simt_unit_bytes(s->K, s->V);
+    L.unit_bytes = use_tc(s) ? kda::chunk_tc_unit_bytes(s->K, s->V)
+                             : kda::chunk_simt_unit_bytes(s->K, s->V);
     L.ctrl = 0;
     L.chunk_start = 256;
     L.units = L.chunk_start + kda::align_up(sizeof(int32_t) * ((size_t)s->num_seqs + 1), 256);
@@ -220,7 +227,16 @@ kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const floa
         e = kda::launch_validate_offsets(cu_seqlens, a.N, a.T, dev_status, a.ctrl, a.chunk_start, s);
         if (e != cudaSuccess) return cuda_fail(e, op);
     }
-    e = kda::launch_chunk_simt(a, shape->dtype, s);
+    if (use_tc(shape)) {
+        const void *ptrs[] = {q, k, v, g, h0, ht, o};
+        for (const void *ptr : ptrs)
+            if ((uintptr_t)ptr % 16 != 0)
+                return fail(KDA_ERR_INVALID_ARG, "%s: bf16 tensors, g, h0 and ht must be 16-byte "
+                            "aligned", op);
+        e = kda::launch_chunk_tc(a, s);
+    } else {
+        e = kda::launch_chunk_simt(a, shape->dtype, s);
+    }
     if (e != cudaSuccess) return cuda_fail(e, op);
     g_last_error.clear();
     return KDA_OK;

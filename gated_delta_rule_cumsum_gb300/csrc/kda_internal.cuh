@@ -113,4 +113,9 @@ struct ChunkArgs {
 size_t chunk_simt_unit_bytes(int K, int V);
 cudaError_t launch_chunk_simt(const ChunkArgs &a, kda_dtype dt, cudaStream_t st);
 
+// Tensor-core path (bf16 inputs): K in {64, 128}, V a multiple of 32 up to 256.
+bool chunk_tc_supported(int K, int V);
+size_t chunk_tc_unit_bytes(int K, int V);
+cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st);
+
 }  // namespace kda

@@ -1,0 +1,76 @@
+// tc_probe.cu -- a single-tile tcgen05 GEMM built from the library's own
+// wrappers (kda_tc.cuh), used by tests/test_gpu_tc_probe.py to check the
+// operand layouts, descriptors and TMEM read-back against a plain matmul.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "kda_tc.cuh"
+
+using namespace kda::tc;
+
+// D[128][N] = A[128][Kd] * B[Kd][N]; mode bit 0: B MN-major, bit 1: A MN-major.
+__global__ void __launch_bounds__(128) tc_probe_kernel(const __nv_bfloat16 *A,
+                                                       const __nv_bfloat16 *B, float *D, int N,
+                                                       int Kd, int mode, int *err) {
+    extern __shared__ __align__(1024) unsigned char sm[];
+    unsigned char *sA = sm;
+    unsigned char *sB = sm + 128 * Kd * 2;
+    __shared__ uint64_t bar;
+    __shared__ uint32_t slot;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool a_mn = mode & 2, b_mn = mode & 1;
+    if (warp == 0) {
+        tmem_alloc(&slot, 256);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        mbar_init(&bar, 1);
+        mbar_fence_init();
+    }
+    for (int idx = tid; idx < 128 * Kd; idx += 128) {
+        const int m = idx / Kd, k = idx % Kd;
+        const uint32_t off = a_mn ? tile_off(k, m, 128) : tile_off(m, k, Kd);
+        *reinterpret_cast<__nv_bfloat16 *>(sA + off) = A[idx];
+    }
+    for (int idx = tid; idx < Kd * N; idx += 128) {
+        const int k = idx / N, n = idx % N;
+        const uint32_t off = b_mn ? tile_off(k, n, N) : tile_off(n, k, Kd);
+        *reinterpret_cast<__nv_bfloat16 *>(sB + off) = B[idx];
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = slot;
+    if (tid == 0) {
+        const uint32_t a_lbo = a_mn ? 128 * 16 : 128, a_sbo = a_mn ? 128 : Kd * 16;
+        const uint32_t b_lbo = b_mn ? N * 16 : 128, b_sbo = b_mn ? 128 : Kd * 16;
+        mma_bf16_k(tmem, smem_addr(sA), a_lbo, a_sbo, smem_addr(sB), b_lbo, b_sbo,
+                   idesc_bf16(128, N, a_mn, b_mn), Kd / 16, 0);
+        mma_commit(&bar);
+    }
+    if (!mbar_wait(&bar, 0) && tid == 0) atomicExch(err, 1);
+    tc_fence_after();
+    for (int c0 = 0; c0 < N; c0 += 16) {
+        float v[16];
+        tmem_ld16(tmem_at(tmem, warp * 32, c0), v);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) D[(warp * 32 + lane) * N + c0 + j] = v[j];
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
+extern "C" int tc_probe(const void *A, const void *B, float *D, int N, int Kd, int mode, int *err,
+                        cudaStream_t st) {
+    if (N < 16 || N > 256 || N % 16 || Kd < 16 || Kd > 128 || Kd % 16) return -1;
+    // Room for the tiles read with either descriptor interpretation.
+    const int smem = 200 * 1024;
+    cudaFuncSetAttribute(tc_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    tc_probe_kernel<<<1, 128, smem, st>>>(static_cast<const __nv_bfloat16 *>(A),
+                                          static_cast<const __nv_bfloat16 *>(B), D, N, Kd, mode,
+                                          err);
+    return (int)cudaGetLastError();
+}

@@ -1,0 +1,46 @@
+"""The tensor-core building blocks (operand tile layout, shared-memory
+descriptors, instruction descriptor, TMEM read-back) on one tile, against a
+plain fp32 matmul of the same bf16 values (GPU)."""
+import ctypes
+import os
+import subprocess
+import tempfile
+
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "tests", "csrc", "tc_probe.cu")
+CSRC = os.path.join(ROOT, "gated_delta_rule_cumsum_gb300", "csrc")
+
+
+@pytest.fixture(scope="module")
+def probe():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    tmp = tempfile.mkdtemp()
+    so = os.path.join(tmp, "tc_probe.so")
+    subprocess.run(["nvcc", "-O2", "-std=c++17", "-gencode", "arch=compute_103a,code=sm_103a",
+                    "-Xcompiler", "-fPIC", "-shared", "-cudart", "shared", "-I", CSRC, SRC,
+                    "-o", so], check=True)
+    lib = ctypes.CDLL(so)
+    lib.tc_probe.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 3 + [ctypes.c_void_p] * 2
+    return lib
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2, 3], ids=["Ak_Bk", "Ak_Bmn", "Amn_Bk", "Amn_Bmn"])
+@pytest.mark.parametrize("N,Kd", [(16, 16), (32, 64), (64, 128), (128, 128), (256, 64)])
+def test_single_tile_gemm(probe, mode, N, Kd):
+    g = torch.Generator(device="cuda").manual_seed(N * 1000 + Kd + mode)
+    A = torch.randn(128, Kd, device="cuda", generator=g).to(torch.bfloat16)
+    B = torch.randn(Kd, N, device="cuda", generator=g).to(torch.bfloat16)
+    D = torch.full((128, N), float("nan"), device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = probe.tc_probe(A.data_ptr(), B.data_ptr(), D.data_ptr(), N, Kd, mode, err.data_ptr(),
+                        torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert rc == 0 and int(err) == 0
+    want = A.float() @ B.float()
+    assert torch.allclose(D, want, rtol=1e-4, atol=1e-3), (D - want).abs().max()
