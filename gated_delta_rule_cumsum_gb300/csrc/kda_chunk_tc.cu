@@ -37,20 +37,21 @@ namespace {
 
 using namespace tc;
 
-constexpr int kBV = 32;               // value columns per scan CTA
+constexpr int kSBV = 16;              // value columns per scan CTA
 constexpr int kStages = 3;            // scan pipeline depth
 constexpr float kSafeRange = 60.f;    // max |g2| (log2) for the split grams
 constexpr uint64_t kWaitNs = 1000000000ull;
 
-// Byte layout of one workspace unit (chunk, value head).
+// Byte layout of one workspace unit (chunk c, value head).
 struct TcLayout {
-    uint32_t aw;      // [128][dk] tile: rows 0..63 w, rows 64..127 scale * qg
-    uint32_t kgt;     // [128][64] tile: kg^T (rows >= dk zero)
-    uint32_t aqk;     // [64][64] tile: Aqk (scale inside)
-    uint32_t u;       // [dv / 32][64][32] bf16 row-major blocks
-    uint32_t dec;     // [128] fp32: 2^G (0 beyond dk)
+    uint32_t aw;      // [128][dk] tile: rows 0..63 W~_c = W_c Diag(2^G_{c-1}) (W_0 for a
+                      // sequence's first chunk), rows 64..127 scale * qg_c
+    uint32_t kgt;     // [128][64] tile: kg_c^T (rows >= dk zero)
+    uint32_t mt;      // [64][64] tile: M_c = W_c kg_{c-1}^T (unused for a first chunk)
+    uint32_t aqk;     // [64][64] tile: Aqk_c (scale inside)
+    uint32_t u;       // [dv / 16][64][16] bf16 row-major blocks: u_c
+    uint32_t dec;     // [128] fp32: 2^G_c (0 beyond dk)
     uint32_t stride;  // unit size, 256-byte multiple
-    uint32_t head;    // bytes of aw + kgt + aqk (one contiguous copy)
 };
 
 __host__ __device__ inline TcLayout tc_layout(int K, int V) {
@@ -58,27 +59,30 @@ __host__ __device__ inline TcLayout tc_layout(int K, int V) {
     uint32_t off = 0;
     L.aw = off;  off += 128u * K * 2;
     L.kgt = off; off += 128u * 64 * 2;
+    L.mt = off;  off += 64u * 64 * 2;
     L.aqk = off; off += 64u * 64 * 2;
-    L.head = off;
     L.u = off;   off += 64u * V * 2;
     L.dec = off; off += 128u * 4;
     L.stride = (uint32_t)align_up(off, 256);
     return L;
 }
 
+// Maps a chunk slot to its rows and its index within the sequence.  Returns
+// false for slots past the last chunk or when the offsets failed validation.
 __device__ __forceinline__ bool locate_chunk(const ChunkArgs &p, int64_t gc, int &b, int &r0,
-                                             int &nr) {
+                                             int &nr, int &cl) {
     if (p.cu) {
         if (!p.ctrl->valid || gc >= p.ctrl->total_chunks) return false;
         const int n = upper_bound_minus_one(p.chunk_start, p.N + 1, (int)gc);
-        const int c = (int)gc - p.chunk_start[n];
+        cl = (int)gc - p.chunk_start[n];
         b = 0;
-        r0 = p.cu[n] + kBT * c;
+        r0 = p.cu[n] + kBT * cl;
         nr = min(kBT, p.cu[n + 1] - r0);
     } else {
         const int ntc = (p.T + kBT - 1) / kBT;
         b = (int)(gc / ntc);
-        r0 = (int)(gc % ntc) * kBT;
+        cl = (int)(gc % ntc);
+        r0 = cl * kBT;
         nr = min(kBT, p.T - r0);
     }
     return nr > 0;
@@ -119,69 +123,75 @@ __device__ __forceinline__ uint4 pack8_at(const float *f) {
 // ============================================================== prep kernel
 template <int KK, int VV>
 struct PrepSmem {
-    static constexpr int kGStride = KK + 4;                       // padded fp32 row of g2
-    static constexpr uint32_t ag = 0;                             // [128][KK] bf16 tile
-    static constexpr uint32_t kb = ag + 128 * KK * 2;             // [64][KK] tile / scratch
-    static constexpr uint32_t kb_bytes = (64 * KK * 2 > 16384) ? 64 * KK * 2 : 16384;
-    static constexpr uint32_t ab = kb + kb_bytes;                 // [64][64] tile Akk diag(beta)
-    static constexpr uint32_t v = ab + 64 * 64 * 2;               // [64][VV] tile
-    static constexpr uint32_t g = v + 64 * VV * 2;                // g2 fp32, later L and Akk
-    static constexpr uint32_t g_bytes0 = 64 * kGStride * 4;
-    static constexpr uint32_t g_bytes = g_bytes0 > 2 * 64 * 65 * 4 ? g_bytes0 : 2 * 64 * 65 * 4;
-    static constexpr uint32_t used = g + g_bytes;
-    // Floor so that at most two CTAs (256 TMEM columns each) or one (512) share an SM.
-    static constexpr uint32_t floor_bytes = (KK + VV <= 256) ? 80 * 1024 : 120 * 1024;
-    static constexpr uint32_t total = used > floor_bytes ? used : floor_bytes;
+    static constexpr uint32_t ag = 0;                           // [128][KK]: q->qg, k->kg; Akk fp32 later
+    static constexpr uint32_t kbx = ag + 128 * KK * 2;          // [128][KK]: kb; kg of the previous chunk
+    // L (fp32 [64][64]) and the solve scratch: over the kb rows for dk = 128, after
+    // the tile for dk = 64 (so the previous chunk's kg survives the exact grams).
+    static constexpr uint32_t lbuf = (KK == 128) ? kbx : kbx + 128 * KK * 2;
+    static constexpr uint32_t kbx_bytes = (KK == 128) ? 128 * KK * 2 : 128 * KK * 2 + 64 * 64 * 4 + 4096;
+    static constexpr uint32_t ab = kbx + kbx_bytes;             // [64][64]: Akk diag(beta) (8 KB before it valid)
+    static constexpr uint32_t pb = ab + 64 * 64 * 2;            // [64][64]: P = kg_c kgp^T
+    static constexpr uint32_t v = pb + 64 * 64 * 2;             // [64][VV]
+    static constexpr uint32_t akk = (64 * KK * 2 >= 64 * 64 * 4) ? ag : v + 64 * VV * 2;  // fp32 [64][64]
+    static constexpr uint32_t used = (akk == ag) ? v + 64 * VV * 2 : akk + 64 * 64 * 4;
+    // Floor so that at most two CTAs (256 TMEM columns each) share an SM.
+    static constexpr uint32_t total = used > 80 * 1024 ? used : 80 * 1024;
 };
-constexpr int kLS = 65;  // padded row stride of L and Akk (fp32)
+
+// L (fp32 64 x 64) with an XOR swizzle: row-per-lane writes and the solve's
+// broadcast reads both stay free of bank conflicts.
+__device__ __forceinline__ int lidx(int i, int j) { return i * 64 + (j ^ (i & 31)); }
 
 template <int KK, int VV>
-__global__ void __launch_bounds__(128) chunk_prep_tc_kernel(ChunkArgs p) {
+__global__ void __launch_bounds__(256) chunk_prep_tc_kernel(ChunkArgs p) {
     using S = PrepSmem<KK, VV>;
     extern __shared__ __align__(1024) unsigned char sm[];
     __shared__ float sBeta[64];
-    __shared__ float sGlast[128];
+    __shared__ float sDprev[128];
     __shared__ uint64_t bar;
     __shared__ uint32_t tslot;
-    __shared__ float sRange;
+    __shared__ int sRangeBits;
 
     const int64_t gc = blockIdx.x;
     const int hv = blockIdx.y;
-    int b, r0, nr;
-    if (!locate_chunk(p, gc, b, r0, nr)) return;
+    int b, r0, nr, cl;
+    if (!locate_chunk(p, gc, b, r0, nr, cl)) return;
+    const bool halo = cl > 0;  // the previous chunk of the same sequence exists
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int h = hv / (p.HV / p.H);
-    constexpr uint32_t kTmemCols = (KK + VV <= 256) ? 256 : 512;
+    constexpr uint32_t kCols = 256;
 
     unsigned char *sAG = sm + S::ag;
-    unsigned char *sKB = sm + S::kb;
+    unsigned char *sKB = sm + S::kbx;
     unsigned char *sAB = sm + S::ab;
+    unsigned char *sPB = sm + S::pb;
     unsigned char *sV = sm + S::v;
-    float *sG = reinterpret_cast<float *>(sm + S::g);
-    float *sL = sG;                 // after the elementwise phase: L [64][kLS]
-    float *sA = sG + 64 * kLS;      //                             Akk [64][kLS]
-    float *sT = reinterpret_cast<float *>(sKB);  // solve scratch (after the grams)
+    float *sL = reinterpret_cast<float *>(sm + S::lbuf);
+    float *sT = sL + 64 * 64;                                      // solve scratch (3 KB)
+    float *sA = reinterpret_cast<float *>(sm + S::akk);            // Akk, row stride 64
 
     const TcLayout Lo = tc_layout(KK, VV);
     unsigned char *U = static_cast<unsigned char *>(p.units) + (gc * p.HV + hv) * Lo.stride;
 
     if (warp == 0) {
-        tmem_alloc(&tslot, kTmemCols);
+        tmem_alloc(&tslot, kCols);
         tmem_relinquish();
     }
     if (tid == 0) {
         mbar_init(&bar, 1);
         mbar_fence_init();
+        sRangeBits = 0;
     }
+    __syncthreads();
 
-    // ---- 1. inputs -> shared memory (q, k, v as operand tiles; g row-major)
+    // ---- 1. async loads: q, k (and the previous chunk's k) and v as operand tiles
     const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(p.q);
     const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(p.k);
     const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(p.v);
     const __nv_bfloat16 *beta = static_cast<const __nv_bfloat16 *>(p.beta);
     const size_t row0 = (size_t)b * p.T + r0;
-    constexpr int KG8 = KK / 8, VG8 = VV / 8, KG4 = KK / 4;
-    for (int idx = tid; idx < 64 * KG8; idx += 128) {
+    constexpr int KG8 = KK / 8, VG8 = VV / 8;
+    for (int idx = tid; idx < 64 * KG8; idx += 256) {
         const int i = idx / KG8, c = (idx % KG8) * 8;
         void *dq = sAG + tile_off(i, c, KK);
         void *dk = sAG + tile_off(64 + i, c, KK);
@@ -193,8 +203,10 @@ __global__ void __launch_bounds__(128) chunk_prep_tc_kernel(ChunkArgs p) {
             *reinterpret_cast<uint4 *>(dq) = make_uint4(0, 0, 0, 0);
             *reinterpret_cast<uint4 *>(dk) = make_uint4(0, 0, 0, 0);
         }
+        if (halo)
+            cp_async16(sKB + tile_off(64 + i, c, KK), k + ((row0 - 64 + i) * p.H + h) * KK + c);
     }
-    for (int idx = tid; idx < 64 * VG8; idx += 128) {
+    for (int idx = tid; idx < 64 * VG8; idx += 256) {
         const int i = idx / VG8, c = (idx % VG8) * 8;
         void *dv = sV + tile_off(i, c, VV);
         if (i < nr)
@@ -202,76 +214,101 @@ __global__ void __launch_bounds__(128) chunk_prep_tc_kernel(ChunkArgs p) {
         else
             *reinterpret_cast<uint4 *>(dv) = make_uint4(0, 0, 0, 0);
     }
-    for (int idx = tid; idx < 64 * KG4; idx += 128) {
-        const int i = idx / KG4, c = (idx % KG4) * 4;
-        float *dg = sG + i * S::kGStride + c;
-        if (i < nr)
-            cp_async16(dg, p.g + ((row0 + i) * p.HV + hv) * KK + c);
-        else
-            *reinterpret_cast<float4 *>(dg) = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
     if (tid < 64) sBeta[tid] = tid < nr ? to_f32(beta[(row0 + tid) * p.HV + hv]) : 0.f;
-    cp_async_wait_all();
-    __syncthreads();
 
-    // ---- optional L2 normalisation of the q and k rows (thread r: row r of [q; k])
-    if (p.l2norm) {
-        float ss = 0.f;
-        for (int c = 0; c < KK; c += 8) {
-            float f[8];
-            unpack8(*reinterpret_cast<const uint4 *>(sAG + tile_off(tid, c, KK)), f);
+    // ---- 2. gate cumsums in registers: thread d < KK owns channel d of this
+    // chunk; thread 128 + d owns channel d of the previous chunk (suffix sums).
+    float gam[64];
+    const int d = tid & 127;
+    const bool own = d < KK && (tid < 128 || halo);
+    if (own) {
+        const float *gp = p.g + ((tid < 128 ? row0 : row0 - 64) * p.HV + hv) * KK + d;
+        const size_t rs = (size_t)p.HV * KK;
+        const int lim = tid < 128 ? nr : 64;
+        // Unpredicated loads of clamped rows (one batch in flight), then masking.
 #pragma unroll
-            for (int j = 0; j < 8; ++j) ss = fmaf(f[j], f[j], ss);
-        }
-        const float rs = 1.f / sqrtf(ss + 1e-6f);
-        for (int c = 0; c < KK; c += 8) {
-            uint4 *ptr = reinterpret_cast<uint4 *>(sAG + tile_off(tid, c, KK));
-            float f[8];
-            unpack8(*ptr, f);
+        for (int i = 0; i < 64; ++i) gam[i] = __ldg(gp + (size_t)min(i, lim - 1) * rs);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) f[j] *= rs;
-            *ptr = pack8(f);
-        }
-    }
-
-    // ---- 2. Stage 1: chunk-local cumsum, thread d owns channel d
-    {
-        float rng = 0.f;
-        if (tid < KK) {
-            float acc = 0.f;
-            for (int i = 0; i < nr; ++i) {
-                const float gv = sG[i * S::kGStride + tid];
-                acc = p.g_is_cumsum ? gv : fmaf(p.g_scale, gv, acc);
-                sG[i * S::kGStride + tid] = acc;
+        for (int i = 0; i < 64; ++i) gam[i] = i < lim ? gam[i] : 0.f;
+        if (tid < 128) {  // inclusive prefix sums; rows past the end keep G
+            float acc = 0.f, rng = 0.f;
+#pragma unroll
+            for (int i = 0; i < 64; ++i) {
+                acc = p.g_is_cumsum ? (i < lim ? gam[i] : acc) : fmaf(p.g_scale, gam[i], acc);
+                gam[i] = acc;
                 rng = fmaxf(rng, fabsf(acc));
             }
-            for (int i = nr; i < 64; ++i) sG[i * S::kGStride + tid] = acc;
-            sGlast[tid] = acc;
-        }
+            atomicMax(&sRangeBits, __float_as_int(rng));
+        } else {  // gam[j] <- 2^(G' - g2'_j) for the previous chunk; sDprev <- 2^G'
+            float Gp;
+            if (p.g_is_cumsum) {
+                Gp = gam[63];
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) rng = fmaxf(rng, __shfl_xor_sync(0xffffffffu, rng, off));
-        if (tid == 0) sRange = 0.f;
-        __syncthreads();
-        if (lane == 0) atomicMax(reinterpret_cast<int *>(&sRange), __float_as_int(rng));
+                for (int j = 0; j < 64; ++j) gam[j] = exp2f(Gp - gam[j]);
+            } else {
+                float acc = 0.f;
+#pragma unroll
+                for (int j = 63; j >= 0; --j) {
+                    const float gj = gam[j];
+                    gam[j] = exp2f(acc);
+                    acc = fmaf(p.g_scale, gj, acc);
+                }
+                Gp = acc;
+            }
+            sDprev[d] = exp2f(Gp);
+        }
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
+    const bool fast = __int_as_float(sRangeBits) <= kSafeRange;
+
+    // ---- optional L2 normalisation of q, k and the previous chunk's k rows
+    if (p.l2norm) {
+        unsigned char *tileb = tid < 128 ? sAG : sKB;
+        const int row = tid < 128 ? tid : tid - 64;  // threads 128..191: rows 64..127 of sKB
+        if (tid < 128 || (halo && row < 128)) {
+            float ss = 0.f;
+            for (int c = 0; c < KK; c += 8) {
+                float f[8];
+                unpack8(*reinterpret_cast<const uint4 *>(tileb + tile_off(row, c, KK)), f);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) ss = fmaf(f[j], f[j], ss);
+            }
+            const float rsn = 1.f / sqrtf(ss + 1e-6f);
+            for (int c = 0; c < KK; c += 8) {
+                uint4 *ptr = reinterpret_cast<uint4 *>(tileb + tile_off(row, c, KK));
+                float f[8];
+                unpack8(*ptr, f);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) f[j] *= rsn;
+                *ptr = pack8(f);
+            }
+        }
         __syncthreads();
     }
-    const bool fast = sRange <= kSafeRange;
-    uint32_t phase = 0;  // completed phases of `bar`
 
-    // ---- exact grams for chunks whose gate range is too wide to split
+    // ---- exact grams for chunks whose gate range is too wide to split.  g2 goes
+    // through this unit's own (not yet written) output slot as fp32 scratch.
     if (!fast) {
-        float *sLx = reinterpret_cast<float *>(sKB);  // [64][64] fp32 L (16 KB)
-        for (int i = warp; i < 64; i += 4) {
+        float *gs = reinterpret_cast<float *>(U + Lo.aw);  // [64][KK] fp32
+        if (tid < KK) {
+#pragma unroll
+            for (int i = 0; i < 64; ++i) gs[i * KK + tid] = gam[i];
+        }
+        __threadfence_block();
+        __syncthreads();
+        for (int i = warp; i < 64; i += 8) {
             for (int j = 0; j <= i; ++j) {
                 float aq = 0.f, ak = 0.f;
-                for (int d = lane; d < KK; d += 32) {
-                    const float e = exp2f(sG[i * S::kGStride + d] - sG[j * S::kGStride + d]);
+                for (int dd = lane; dd < KK; dd += 32) {
+                    const float e = exp2f(gs[i * KK + dd] - gs[j * KK + dd]);
                     const float qi = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
-                        sAG + tile_off(i, d, KK)));
+                        sAG + tile_off(i, dd, KK)));
                     const float ki = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
-                        sAG + tile_off(64 + i, d, KK)));
+                        sAG + tile_off(64 + i, dd, KK)));
                     const float kj = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
-                        sAG + tile_off(64 + j, d, KK))) * e;
+                        sAG + tile_off(64 + j, dd, KK))) * e;
                     aq = fmaf(qi, kj, aq);
                     ak = fmaf(ki, kj, ak);
                 }
@@ -283,98 +320,124 @@ __global__ void __launch_bounds__(128) chunk_prep_tc_kernel(ChunkArgs p) {
                 if (lane == 0) {
                     *reinterpret_cast<__nv_bfloat16 *>(U + Lo.aqk + tile_off(i, j, 64)) =
                         __float2bfloat16_rn(p.scale * aq);
-                    sLx[i * 64 + j] = (i > j) ? sBeta[i] * ak : 0.f;
+                    sL[lidx(i, j)] = (i > j) ? sBeta[i] * ak : 0.f;
                 }
             }
             for (int j = i + 1 + lane; j < 64; j += 32) {
                 *reinterpret_cast<__nv_bfloat16 *>(U + Lo.aqk + tile_off(i, j, 64)) =
                     __float2bfloat16_rn(0.f);
-                sLx[i * 64 + j] = 0.f;
+                sL[lidx(i, j)] = 0.f;
             }
         }
+        __syncthreads();
     }
-    __syncthreads();
 
-    // ---- 3. elementwise: qg, kg (in place), kb, scale*qg -> workspace, kg^T -> workspace
-    // idx -> (row i = idx % 64, 8-column group): a warp covers 32 rows of one group.
-    for (int idx = tid; idx < 64 * KG8; idx += 128) {
-        const int i = idx & 63, c = (idx >> 6) * 8;
-        uint4 *pq = reinterpret_cast<uint4 *>(sAG + tile_off(i, c, KK));
-        uint4 *pk = reinterpret_cast<uint4 *>(sAG + tile_off(64 + i, c, KK));
-        float fq[8], fk[8], qg[8], kgm[8], kb[8], kg[8], qs[8];
-        unpack8(*pq, fq);
-        unpack8(*pk, fk);
-        const float *gr = sG + i * S::kGStride + c;
+    // ---- 3. elementwise: qg, kg (in place), kb, kg^T and 2^G to the workspace;
+    // the previous chunk's k becomes its kg (rows 64..127 of sKB).
+    if (tid < KK) {
+        const float G = gam[63];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const float gam = gr[j];
-            const float e = exp2f(gam);
-            qg[j] = fq[j] * e;
-            kgm[j] = fk[j] * e;
-            kb[j] = fast ? fk[j] * exp2f(-gam) : 0.f;
-            kg[j] = fk[j] * exp2f(sGlast[c + j] - gam);
-            qs[j] = p.scale * qg[j];
+        for (int i8 = 0; i8 < 64; i8 += 8) {
+            float kgv[8];
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                const int i = i8 + t;
+                __nv_bfloat16 *pq = reinterpret_cast<__nv_bfloat16 *>(sAG + tile_off(i, tid, KK));
+                __nv_bfloat16 *pk = reinterpret_cast<__nv_bfloat16 *>(sAG + tile_off(64 + i, tid, KK));
+                const float e = exp2f(gam[i]);
+                const float qv = __bfloat162float(*pq), kv = __bfloat162float(*pk);
+                *pq = __float2bfloat16_rn(qv * e);
+                *pk = __float2bfloat16_rn(kv * e);
+                if (fast)
+                    *reinterpret_cast<__nv_bfloat16 *>(sKB + tile_off(i, tid, KK)) =
+                        __float2bfloat16_rn(kv * exp2f(-gam[i]));
+                kgv[t] = kv * exp2f(G - gam[i]);
+            }
+            *reinterpret_cast<uint4 *>(U + Lo.kgt + tile_off(tid, i8, 64)) = pack8_at(kgv);
         }
-        *pq = pack8(qg);
-        *pk = pack8(kgm);
-        if (fast) *reinterpret_cast<uint4 *>(sKB + tile_off(i, c, KK)) = pack8(kb);
-        *reinterpret_cast<uint4 *>(U + Lo.aw + tile_off(64 + i, c, KK)) = pack8(qs);
+        reinterpret_cast<float *>(U + Lo.dec)[tid] = exp2f(G);
+    } else if (tid >= 128 && own) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-            *reinterpret_cast<__nv_bfloat16 *>(U + Lo.kgt + tile_off(c + j, i, 64)) =
-                __float2bfloat16_rn(kg[j]);
+        for (int j = 0; j < 64; ++j) {
+            __nv_bfloat16 *pk = reinterpret_cast<__nv_bfloat16 *>(sKB + tile_off(64 + j, d, KK));
+            *pk = __float2bfloat16_rn(__bfloat162float(*pk) * gam[j]);
+        }
     }
+    if (tid >= KK && tid < 128) reinterpret_cast<float *>(U + Lo.dec)[tid] = 0.f;
     if (KK < 128) {  // zero rows dk..127 of kg^T
-        for (int idx = tid; idx < (128 - KK) * 8; idx += 128) {
-            const int d = KK + idx / 8, c = (idx % 8) * 8;
-            *reinterpret_cast<uint4 *>(U + Lo.kgt + tile_off(d, c, 64)) = make_uint4(0, 0, 0, 0);
+        for (int idx = tid; idx < (128 - KK) * 8; idx += 256) {
+            const int dd = KK + idx / 8, c = (idx % 8) * 8;
+            *reinterpret_cast<uint4 *>(U + Lo.kgt + tile_off(dd, c, 64)) = make_uint4(0, 0, 0, 0);
         }
     }
-    reinterpret_cast<float *>(U + Lo.dec)[tid] = tid < KK ? exp2f(sGlast[tid]) : 0.f;
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tslot;
 
-    // ---- 4. grams on the tensor cores: D[0:128, 0:64] = [Qg; Kg] Kb^T
-    if (fast) {
-        if (tid == 0) {
-            mma_bf16_k(tmem, smem_addr(sAG), 128, KK * 16, smem_addr(sKB), 128, KK * 16,
-                       idesc_bf16(128, 64, false, false), KK / 16, 0);
-            mma_commit(&bar);
-        }
-        __syncwarp();
-        if (!mbar_wait(&bar, phase & 1, kWaitNs) && tid == 0) report(p.status, KDA_DEVICE_TIMEOUT);
-        ++phase;
-        tc_fence_after();
-        float d[16];
-        const int i = tid & 63;
-        for (int c0 = 0; c0 < 64; c0 += 16) {
-            tmem_ld16(tmem_at(tmem, warp * 32, c0), d);
-            if (tid < 64) {  // Aqk row i
-                float a[16];
+    // ---- 4. grams on the tensor cores.  D[:, 0:64] = [Qg; Kg] Kb^T (split grams),
+    // D[:, 64:128] = [Qg; Kg] kgp^T (cross-chunk gram of the previous chunk).
+    if (tid == 0) {
+        const uint32_t id64 = idesc_bf16(128, 64, false, false);
+        const uint64_t a = sdesc(smem_addr(sAG), 128, KK * 16);
+        if (fast)
+            mma_bf16_seq<KK / 16, false>(tmem, a, 16, sdesc(smem_addr(sKB), 128, KK * 16), 16, id64);
+        if (halo)
+            mma_bf16_seq<KK / 16, false>(tmem + 64, a, 16,
+                                         sdesc(smem_addr(sKB) + 64 * KK * 2, 128, KK * 16), 16, id64);
+        mma_commit(&bar);
+    }
+    // qg * scale -> workspace (rows 64..127 of the [W; qg] tile) while the MMA runs
+    for (int idx = tid; idx < 64 * KG8; idx += 256) {
+        const int i = idx / KG8, c = (idx % KG8) * 8;
+        float f[8];
+        unpack8(*reinterpret_cast<const uint4 *>(sAG + tile_off(i, c, KK)), f);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) a[j] = (c0 + j <= i) ? p.scale * d[j] : 0.f;
-                *reinterpret_cast<uint4 *>(U + Lo.aqk + tile_off(i, c0, 64)) = pack8_at(a);
-                *reinterpret_cast<uint4 *>(U + Lo.aqk + tile_off(i, c0 + 8, 64)) = pack8_at(a + 8);
-            } else {  // L row i
+        for (int j = 0; j < 8; ++j) f[j] *= p.scale;
+        *reinterpret_cast<uint4 *>(U + Lo.aw + tile_off(64 + i, c, KK)) = pack8(f);
+    }
+    __syncwarp();
+    uint32_t phase = 0;
+    if (!mbar_wait(&bar, phase & 1, kWaitNs) && tid == 0) report(p.status, KDA_DEVICE_TIMEOUT);
+    ++phase;
+    tc_fence_after();
+    {
+        const int quad = warp & 3, i = (tid & 127) & 63;
+        if (warp < 4 && fast) {  // Aqk (rows 0..63) and L (rows 64..127) from columns 0..63
+            for (int c0 = 0; c0 < 64; c0 += 16) {
+                float dd[16];
+                tmem_ld16(tmem_at(tmem, quad * 32, c0), dd);
+                if (tid < 64) {
+                    float a2[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    sL[i * kLS + c0 + j] = (c0 + j < i) ? sBeta[i] * d[j] : 0.f;
+                    for (int j = 0; j < 16; ++j) a2[j] = (c0 + j <= i) ? p.scale * dd[j] : 0.f;
+                    *reinterpret_cast<uint4 *>(U + Lo.aqk + tile_off(i, c0, 64)) = pack8_at(a2);
+                    *reinterpret_cast<uint4 *>(U + Lo.aqk + tile_off(i, c0 + 8, 64)) = pack8_at(a2 + 8);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        sL[lidx(i, c0 + j)] = (c0 + j < i) ? sBeta[i] * dd[j] : 0.f;
+                }
             }
         }
-        tc_fence_before();
-    } else {
-        const float *sLx = reinterpret_cast<const float *>(sKB);
-        for (int idx = tid; idx < 64 * 64; idx += 128) sL[(idx >> 6) * kLS + (idx & 63)] = sLx[idx];
+        if (warp >= 6 && halo) {  // P = kg_c kgp^T from rows 64..127, columns 64..127
+            for (int c0 = 0; c0 < 64; c0 += 16) {
+                float dd[16];
+                tmem_ld16(tmem_at(tmem, quad * 32, 64 + c0), dd);
+                *reinterpret_cast<uint4 *>(sPB + tile_off(i, c0, 64)) = pack8_at(dd);
+                *reinterpret_cast<uint4 *>(sPB + tile_off(i, c0 + 8, 64)) = pack8_at(dd + 8);
+            }
+        }
     }
+    tc_fence_before();
     __syncthreads();
 
-    // ---- 5. Akk = (I + L)^-1
-    for (int idx = tid; idx < 64 * 64; idx += 128) sA[(idx >> 6) * kLS + (idx & 63)] = 0.f;
+    // ---- 5. Akk = (I + L)^-1, blocked: diagonal 16 x 16 blocks by substitution,
+    // then the off-diagonal blocks level by level: A_IJ = -A_II sum_M L_IM A_MJ.
+    for (int idx = tid; idx < 64 * 64; idx += 256) sA[idx] = 0.f;
     __syncthreads();
-    if (tid < 64) {  // diagonal 16 x 16 blocks, one column per thread
+    if (tid < 64) {
         const int I = tid >> 4, c = tid & 15, o = 16 * I;
         float x[16];
 #pragma unroll
@@ -383,44 +446,41 @@ __global__ void __launch_bounds__(128) chunk_prep_tc_kernel(ChunkArgs p) {
         for (int r = 1; r < 16; ++r) {
             float s = 0.f;
 #pragma unroll
-            for (int m = 0; m < r; ++m) s = fmaf(sL[(o + r) * kLS + o + m], x[m], s);
+            for (int m = 0; m < r; ++m) s = fmaf(sL[lidx(o + r, o + m)], x[m], s);
             if (r > c) x[r] = -s;
         }
 #pragma unroll
-        for (int r = 0; r < 16; ++r) sA[(o + r) * kLS + o + c] = x[r];
+        for (int r = 0; r < 16; ++r) sA[(o + r) * 64 + o + c] = x[r];
     }
     __syncthreads();
     for (int lvl = 1; lvl < 4; ++lvl) {
         const int nblk = 4 - lvl;
-        // T_IJ = sum_{M=J}^{I-1} L_IM A_MJ   for I = J + lvl
-        for (int e = tid; e < nblk * 256; e += 128) {
+        for (int e = tid; e < nblk * 256; e += 256) {
             const int J = e >> 8, I = J + lvl, r = (e >> 4) & 15, c = e & 15;
             float s = 0.f;
             for (int M = J; M < I; ++M) {
 #pragma unroll
                 for (int m = 0; m < 16; ++m)
-                    s = fmaf(sL[(16 * I + r) * kLS + 16 * M + m], sA[(16 * M + m) * kLS + 16 * J + c], s);
+                    s = fmaf(sL[lidx(16 * I + r, 16 * M + m)], sA[(16 * M + m) * 64 + 16 * J + c], s);
             }
             sT[e] = s;
         }
         __syncthreads();
-        // A_IJ = -A_II T_IJ
-        for (int e = tid; e < nblk * 256; e += 128) {
+        for (int e = tid; e < nblk * 256; e += 256) {
             const int J = e >> 8, I = J + lvl, r = (e >> 4) & 15, c = e & 15;
             float s = 0.f;
 #pragma unroll
             for (int m = 0; m < 16; ++m)
-                s = fmaf(sA[(16 * I + r) * kLS + 16 * I + m], sT[(J << 8) + m * 16 + c], s);
-            sA[(16 * I + r) * kLS + 16 * J + c] = -s;
+                s = fmaf(sA[(16 * I + r) * 64 + 16 * I + m], sT[(J << 8) + m * 16 + c], s);
+            sA[(16 * I + r) * 64 + 16 * J + c] = -s;
         }
         __syncthreads();
     }
-    // Akk diag(beta) as a bf16 operand tile
-    for (int idx = tid; idx < 64 * 8; idx += 128) {
+    for (int idx = tid; idx < 64 * 8; idx += 256) {
         const int i = idx >> 3, c = (idx & 7) * 8;
         float f[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) f[j] = sA[i * kLS + c + j] * sBeta[c + j];
+        for (int j = 0; j < 8; ++j) f[j] = sA[i * 64 + c + j] * sBeta[c + j];
         *reinterpret_cast<uint4 *>(sAB + tile_off(i, c, 64)) = pack8(f);
     }
     fence_async_smem();
@@ -428,62 +488,110 @@ __global__ void __launch_bounds__(128) chunk_prep_tc_kernel(ChunkArgs p) {
     __syncthreads();
     tc_fence_after();
 
-    // ---- 6. w = Akk diag(beta) Kg,  u = Akk diag(beta) v  (valid rows: TMEM lanes 64..127)
+    // ---- 6. W = Akk diag(beta) Kg and M = Akk diag(beta) P (valid rows: lanes 64..127)
+    const uint64_t adesc = sdesc(smem_addr(sAB) - 8 * 1024, 128, 1024);  // rows 64..127 = Akk diag(beta)
     if (tid == 0) {
-        const uint32_t a = smem_addr(sAB) - 8 * 1024;  // rows 64..127 of the M = 128 operand
-        mma_bf16_k(tmem, a, 128, 1024, smem_addr(sAG) + 64 * KK * 2, KK * 16, 128,
-                   idesc_bf16(128, KK, false, true), 4, 0);
-        mma_bf16_k(tmem + KK, a, 128, 1024, smem_addr(sV), VV * 16, 128,
-                   idesc_bf16(128, VV, false, true), 4, 0);
+        mma_bf16_seq<4, false>(tmem, adesc, 16, sdesc(smem_addr(sAG) + 64 * KK * 2, KK * 16, 128),
+                               2 * KK * 16 / 16, idesc_bf16(128, KK, false, true));
+        if (halo)
+            mma_bf16_seq<4, false>(tmem + KK, adesc, 16, sdesc(smem_addr(sPB), 64 * 16, 128),
+                                   2 * 64 * 16 / 16, idesc_bf16(128, 64, false, true));
+        mma_commit(&bar);
+    }
+    __syncwarp();
+    if (!mbar_wait(&bar, phase & 1, kWaitNs) && tid == 0) report(p.status, KDA_DEVICE_TIMEOUT);
+    ++phase;
+    tc_fence_after();
+    {
+        const int quad = warp & 3, i = (tid & 127) - 64;
+        if (warp == 2 || warp == 3) {  // W~ = W Diag(2^G_prev) -> rows 0..63 of the [W; qg] tile
+            for (int c0 = 0; c0 < KK; c0 += 16) {
+                float dd[16];
+                tmem_ld16(tmem_at(tmem, quad * 32, c0), dd);
+                if (halo) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) dd[j] *= sDprev[c0 + j];
+                }
+                *reinterpret_cast<uint4 *>(U + Lo.aw + tile_off(i, c0, KK)) = pack8_at(dd);
+                *reinterpret_cast<uint4 *>(U + Lo.aw + tile_off(i, c0 + 8, KK)) = pack8_at(dd + 8);
+            }
+        }
+        if ((warp == 6 || warp == 7) && halo) {  // M
+            for (int c0 = 0; c0 < 64; c0 += 16) {
+                float dd[16];
+                tmem_ld16(tmem_at(tmem, quad * 32, KK + c0), dd);
+                *reinterpret_cast<uint4 *>(U + Lo.mt + tile_off(i, c0, 64)) = pack8_at(dd);
+                *reinterpret_cast<uint4 *>(U + Lo.mt + tile_off(i, c0 + 8, 64)) = pack8_at(dd + 8);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    // ---- 7. u = Akk diag(beta) v
+    if (tid == 0) {
+        mma_bf16_seq<4, false>(tmem, adesc, 16, sdesc(smem_addr(sV), VV * 16, 128),
+                               2 * VV * 16 / 16, idesc_bf16(128, VV, false, true));
         mma_commit(&bar);
     }
     __syncwarp();
     if (!mbar_wait(&bar, phase & 1, kWaitNs) && tid == 0) report(p.status, KDA_DEVICE_TIMEOUT);
     tc_fence_after();
-    if (warp >= 2) {
-        const int i = tid - 64;
-        float d[16];
-        for (int c0 = 0; c0 < KK; c0 += 16) {
-            tmem_ld16(tmem_at(tmem, warp * 32, c0), d);
-            *reinterpret_cast<uint4 *>(U + Lo.aw + tile_off(i, c0, KK)) = pack8_at(d);
-            *reinterpret_cast<uint4 *>(U + Lo.aw + tile_off(i, c0 + 8, KK)) = pack8_at(d + 8);
-        }
-        for (int c0 = 0; c0 < VV; c0 += 16) {
-            tmem_ld16(tmem_at(tmem, warp * 32, KK + c0), d);
-            unsigned char *ub = U + Lo.u + (size_t)(c0 / kBV) * 64 * kBV * 2 +
-                                ((size_t)i * kBV + (c0 % kBV)) * 2;
-            *reinterpret_cast<uint4 *>(ub) = pack8_at(d);
-            *reinterpret_cast<uint4 *>(ub + 16) = pack8_at(d + 8);
+    if (warp == 2 || warp == 3 || warp == 6 || warp == 7) {
+        const int quad = warp & 3, i = (tid & 127) - 64;
+        const int cbeg = warp < 4 ? 0 : VV / 2;
+        for (int c0 = cbeg; c0 < cbeg + VV / 2; c0 += 16) {
+            float dd[16];
+            tmem_ld16(tmem_at(tmem, quad * 32, c0), dd);
+            unsigned char *ub = U + Lo.u + ((size_t)(c0 / kSBV) * 64 + i) * kSBV * 2;
+            *reinterpret_cast<uint4 *>(ub) = pack8_at(dd);
+            *reinterpret_cast<uint4 *>(ub + 16) = pack8_at(dd + 8);
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+    if (warp == 0) tmem_dealloc(tmem, kCols);
 }
 
 // ============================================================== scan kernel
+// Rounds r = 0 .. nc of one (sequence, value head, 16 value columns); round r
+// finishes chunk c = r - 1 and starts chunk c + 1:
+//   D1 = [W~_{c+1}; qg_c] h_c + [M_{c+1}; Aqk_c] v'_c   rows 0..63 -> v'_{c+1} = u_{c+1} - D1
+//                                                      rows 64..127 -> o_c
+//   D2 = kg_c^T v'_c                                   h_{c+1} = Diag(2^G_c) h_c + D2
+// where W~_{c+1} = W_{c+1} Diag(2^G_c) and M_{c+1} = W_{c+1} kg_c^T come from the
+// prep kernel: v'_{c+1} = u_{c+1} - W_{c+1} h_{c+1} expands into the two terms, so
+// one MMA round per chunk carries the whole recurrence.  Round 0 only forms
+// v'_0 = u_0 - W_0 h_0.
 template <int KK>
 struct ScanSmem {
-    static constexpr uint32_t head = 128 * KK * 2 + 128 * 64 * 2 + 64 * 64 * 2;
-    static constexpr uint32_t stage = head + 64 * kBV * 2 + 128 * 4;
+    static constexpr uint32_t top = 0;                         // [128][KK]: W~_{c+1}; qg_c
+    static constexpr uint32_t kgt = top + 128 * KK * 2;        // [128][64]: kg_c^T
+    static constexpr uint32_t bot = kgt + 128 * 64 * 2;        // [128][64]: M_{c+1}; Aqk_c
+    static constexpr uint32_t u = bot + 128 * 64 * 2;          // [64][kSBV] bf16: u_{c+1}
+    static constexpr uint32_t dec = u + 64 * kSBV * 2;         // [128] fp32: 2^G_c
+    static constexpr uint32_t stage = dec + 512;
     static constexpr uint32_t stage_stride = (stage + 1023) / 1024 * 1024;
-    static constexpr uint32_t hs = kStages * stage_stride;   // [KK][kBV] bf16 tile
-    static constexpr uint32_t vp = hs + KK * kBV * 2;        // [64][kBV] bf16 tile
-    static constexpr uint32_t total = vp + 64 * kBV * 2;
+    static constexpr uint32_t hs = kStages * stage_stride;     // 2 x [KK][kSBV] tile
+    static constexpr uint32_t vp = hs + 2 * KK * kSBV * 2;     // 2 x [64][kSBV] tile
+    static constexpr uint32_t total = vp + 2 * 64 * kSBV * 2;
 };
 
-__device__ __forceinline__ int read_flag(const int *f) { return *reinterpret_cast<const volatile int *>(f); }
+__device__ __forceinline__ int read_flag(const int *f) {
+    return *reinterpret_cast<const volatile int *>(f);
+}
 
 template <int KK>
-__global__ void __launch_bounds__(160) chunk_scan_tc_kernel(ChunkArgs p) {
+__global__ void __launch_bounds__(192, 1) chunk_scan_tc_kernel(ChunkArgs p) {
     using S = ScanSmem<KK>;
     extern __shared__ __align__(1024) unsigned char sm[];
     __shared__ uint64_t full[kStages], empty[kStages];
-    __shared__ uint64_t bar_d1[2], bar_d2, bar_d3[2], h_ready, vp_ready;
+    __shared__ uint64_t bar_v[2], bar_h, state_ready;
     __shared__ uint32_t tslot;
     __shared__ int abort_flag;
 
-    const int nvb = p.V / kBV;
+    const int nvb = p.V / kSBV;
     const int64_t bid = blockIdx.x;
     const int vb = (int)(bid % nvb);
     const int hv = (int)((bid / nvb) % p.HV);
@@ -506,204 +614,212 @@ __global__ void __launch_bounds__(160) chunk_scan_tc_kernel(ChunkArgs p) {
         nc = (p.T + kBT - 1) / kBT;
         gc0 = (int64_t)n * nc;
     }
+    const int R = nc > 0 ? nc + 1 : 0;  // rounds
     const TcLayout Lo = tc_layout(KK, p.V);
-    const size_t sbase = ((size_t)n * p.HV + hv) * (size_t)KK * p.V + (size_t)vb * kBV;
+    const size_t sbase = ((size_t)n * p.HV + hv) * (size_t)KK * p.V + (size_t)vb * kSBV;
+    const unsigned char *units = static_cast<const unsigned char *>(p.units);
 
     if (warp == 0) {
-        tmem_alloc(&tslot, 128);
+        tmem_alloc(&tslot, 64);
         tmem_relinquish();
     }
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], 1 + 128);
         }
-        mbar_init(&bar_d1[0], 1);
-        mbar_init(&bar_d1[1], 1);
-        mbar_init(&bar_d2, 1);
-        mbar_init(&bar_d3[0], 1);
-        mbar_init(&bar_d3[1], 1);
-        mbar_init(&h_ready, 128);
-        mbar_init(&vp_ready, 64);
+        mbar_init(&bar_v[0], 1);
+        mbar_init(&bar_v[1], 1);
+        mbar_init(&bar_h, 1);
+        mbar_init(&state_ready, 192);
         mbar_fence_init();
         abort_flag = 0;
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = tslot;
-    // columns: D1 double buffer at 0 / kBV, D2 at 2 kBV
+    const uint32_t tmem = tslot;  // D1[0] at +0, D1[1] at +16, D2 at +32
     unsigned char *sH = sm + S::hs;
     unsigned char *sVp = sm + S::vp;
-    __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.o);
 
     if (warp == 4) {
-        // ------------------------------------------------ producer: bulk loads
+        // ------------------------------------------------------- producer
         if (lane == 0) {
             int issued = 0;
-            for (int c = 0; c < nc; ++c) {
-                const int s = c % kStages;
-                if (c >= kStages && !mbar_wait(&empty[s], ((c / kStages) - 1) & 1, kWaitNs)) {
+            for (int r = 0; r < R; ++r) {
+                const int s = r % kStages;
+                if (r >= kStages && !mbar_wait(&empty[s], ((r / kStages) - 1) & 1, kWaitNs)) {
                     atomicExch(&abort_flag, 1);
                     report(p.status, KDA_DEVICE_TIMEOUT);
                     break;
                 }
                 if (read_flag(&abort_flag)) break;
-                issued = c + 1;
-                const unsigned char *U =
-                    static_cast<const unsigned char *>(p.units) + ((gc0 + c) * p.HV + hv) * Lo.stride;
                 unsigned char *st = sm + s * S::stage_stride;
-                const uint32_t ubytes = 64 * kBV * 2;
-                mbar_arrive_expect_tx(&full[s], S::head + ubytes + 512);
-                for (uint32_t off = 0; off < S::head; off += 16384) {
-                    const uint32_t len = S::head - off < 16384 ? S::head - off : 16384;
-                    bulk_g2s(st + off, U + off, len, &full[s]);
+                const int c = r - 1;
+                const bool nxt = r < nc, cur = r >= 1;
+                uint32_t bytes = 0;
+                if (nxt) bytes += 64 * KK * 2 + 64 * kSBV * 2 + (cur ? 64 * 64 * 2 : 0);
+                if (cur) bytes += 64 * KK * 2 + 128 * 64 * 2 + 64 * 64 * 2 + 512;
+                mbar_arrive_expect_tx(&full[s], bytes);
+                if (nxt) {
+                    const unsigned char *U1 = units + (gc0 + c + 1) * p.HV * (int64_t)Lo.stride +
+                                              (int64_t)hv * Lo.stride;
+                    bulk_g2s(st + S::top, U1 + Lo.aw, 64 * KK * 2, &full[s]);
+                    bulk_g2s(st + S::u, U1 + Lo.u + (size_t)vb * 64 * kSBV * 2, 64 * kSBV * 2,
+                             &full[s]);
+                    if (cur) bulk_g2s(st + S::bot, U1 + Lo.mt, 64 * 64 * 2, &full[s]);
                 }
-                bulk_g2s(st + S::head, U + Lo.u + (size_t)vb * ubytes, ubytes, &full[s]);
-                bulk_g2s(st + S::head + ubytes, U + Lo.dec, 512, &full[s]);
+                if (cur) {
+                    const unsigned char *U0 = units + (gc0 + c) * p.HV * (int64_t)Lo.stride +
+                                              (int64_t)hv * Lo.stride;
+                    bulk_g2s(st + S::top + 64 * KK * 2, U0 + Lo.aw + 64 * KK * 2, 64 * KK * 2,
+                             &full[s]);
+                    bulk_g2s(st + S::kgt, U0 + Lo.kgt, 128 * 64 * 2, &full[s]);
+                    bulk_g2s(st + S::bot + 64 * 64 * 2, U0 + Lo.aqk, 64 * 64 * 2, &full[s]);
+                    bulk_g2s(st + S::dec, U0 + Lo.dec, 512, &full[s]);
+                }
+                issued = r + 1;
             }
-            // Copies still in flight must land before the CTA exits (bounded).
-            for (int c = issued - kStages > 0 ? issued - kStages : 0; c < issued; ++c)
-                mbar_wait(&full[c % kStages], (c / kStages) & 1, kWaitNs);
+            // Copies in flight must land before the CTA exits (bounded).
+            for (int r = issued - kStages > 0 ? issued - kStages : 0; r < issued; ++r)
+                mbar_wait(&full[r % kStages], (r / kStages) & 1, kWaitNs);
+        }
+    } else if (warp == 5) {
+        // ----------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            const uint32_t idn = idesc_bf16(128, kSBV, false, true);
+            const uint32_t base = smem_addr(sm);
+            uint64_t dh[2], dv[2];
+            for (int i = 0; i < 2; ++i) {
+                dh[i] = sdesc(smem_addr(sH) + i * KK * kSBV * 2, kSBV * 16, 128);
+                dv[i] = sdesc(smem_addr(sVp) + i * 64 * kSBV * 2, kSBV * 16, 128);
+            }
+            for (int r = 0; r < R; ++r) {
+                const int s = r % kStages;
+                const uint32_t st = base + s * S::stage_stride;
+                if (!mbar_spin(&full[s], (r / kStages) & 1, kWaitNs) ||
+                    !mbar_spin(&state_ready, r & 1, kWaitNs)) {
+                    atomicExch(&abort_flag, 1);
+                    report(p.status, KDA_DEVICE_TIMEOUT);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d1 = tmem + (r & 1) * kSBV;
+                mma_bf16_seq<KK / 16, false>(d1, sdesc(st + S::top, 128, KK * 16), 16, dh[r & 1],
+                                             2 * kSBV * 16 / 16, idn);
+                if (r >= 1)
+                    mma_bf16_seq<4, true>(d1, sdesc(st + S::bot, 128, 1024), 16, dv[r & 1],
+                                          2 * kSBV * 16 / 16, idn);
+                mma_commit(&bar_v[r & 1]);
+                if (r >= 1) {
+                    mma_bf16_seq<4, false>(tmem + 2 * kSBV, sdesc(st + S::kgt, 128, 1024), 16,
+                                           dv[r & 1], 2 * kSBV * 16 / 16, idn);
+                    mma_commit(&bar_h);
+                }
+                mma_commit(&empty[s]);
+            }
         }
     } else {
-        // ------------------------------------- epilogue warps 0..3 (+ MMA issue by tid 0)
-        const int r = tid;  // TMEM lane / state row d / chunk row
-        float hreg[kBV];
-        const bool has_row = r < KK;
+        // ---------------------------- epilogue: warps 0..3, thread r = lane row
+        const int rr = tid;
+        const bool has_row = rr < KK;
+        float hreg[kSBV];
 #pragma unroll
-        for (int j = 0; j < kBV; ++j) hreg[j] = 0.f;
+        for (int j = 0; j < kSBV; ++j) hreg[j] = 0.f;
         if (has_row && p.h0) {
-            const float4 *src = reinterpret_cast<const float4 *>(p.h0 + sbase + (size_t)r * p.V);
+            const float4 *src = reinterpret_cast<const float4 *>(p.h0 + sbase + (size_t)rr * p.V);
 #pragma unroll
-            for (int j = 0; j < kBV / 4; ++j) {
+            for (int j = 0; j < kSBV / 4; ++j) {
                 const float4 x = src[j];
                 hreg[4 * j] = x.x; hreg[4 * j + 1] = x.y; hreg[4 * j + 2] = x.z; hreg[4 * j + 3] = x.w;
             }
         }
-        auto write_h = [&]() {
+        auto write_h = [&](int buf) {
             if (has_row) {
-#pragma unroll
-                for (int j = 0; j < kBV; j += 8)
-                    *reinterpret_cast<uint4 *>(sH + tile_off(r, j, kBV)) = pack8_at(hreg + j);
+                unsigned char *hb = sH + buf * KK * kSBV * 2;
+                *reinterpret_cast<uint4 *>(hb + tile_off(rr, 0, kSBV)) = pack8_at(hreg);
+                *reinterpret_cast<uint4 *>(hb + tile_off(rr, 8, kSBV)) = pack8_at(hreg + 8);
             }
             fence_async_smem();
-            mbar_arrive(&h_ready);
+            mbar_arrive(&state_ready);
         };
-        write_h();
-
-        const uint32_t id_m1 = idesc_bf16(128, kBV, false, true);
-        for (int c = 0; c < nc; ++c) {
-            const int s = c % kStages;
-            const uint32_t fpar = (c / kStages) & 1;
+        if (R > 0) {
+            write_h(0);
+            if (warp < 2) mbar_arrive(&state_ready);  // no v'_{-1}
+        }
+        __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.o);
+        for (int r = 0; r < R; ++r) {
+            const int s = r % kStages;
             const unsigned char *st = sm + s * S::stage_stride;
-            const uint32_t d1 = tmem + (c & 1) * kBV, d2 = tmem + 2 * kBV;
-            bool ok = true;
-            if (tid == 0) {
-                // MMA issue for chunk c: [w; qg] h  ->  D1[c % 2]
-                ok = mbar_wait(&full[s], fpar, kWaitNs) && mbar_wait(&h_ready, c & 1, kWaitNs);
-                if (ok) {
-                    tc_fence_after();
-                    mma_bf16_k(d1, smem_addr(st), 128, KK * 16, smem_addr(sH), kBV * 16, 128,
-                               id_m1, KK / 16, 0);
-                    mma_commit(&bar_d1[c & 1]);
-                    if (c >= 1) mma_commit(&empty[(c - 1) % kStages]);
-                } else {
-                    atomicExch(&abort_flag, 1);
-                    report(p.status, KDA_DEVICE_TIMEOUT);
-                }
+            const bool nxt = r < nc;
+            if (!mbar_spin(&full[s], (r / kStages) & 1, kWaitNs)) atomicExch(&abort_flag, 1);
+            float uu[kSBV];
+            float dec = 1.f;
+            if (warp < 2 && nxt) {
+                const unsigned char *ur = st + S::u + (size_t)rr * kSBV * 2;
+                float f[8];
+                unpack8(*reinterpret_cast<const uint4 *>(ur), f);
+#pragma unroll
+                for (int t = 0; t < 8; ++t) uu[t] = f[t];
+                unpack8(*reinterpret_cast<const uint4 *>(ur + 16), f);
+#pragma unroll
+                for (int t = 0; t < 8; ++t) uu[8 + t] = f[t];
             }
-            __syncwarp();
-            // all epilogue threads need the stage (u rows and decay)
-            if (!mbar_wait(&full[s], fpar, kWaitNs)) { atomicExch(&abort_flag, 1); }
-            const float dec = has_row ? reinterpret_cast<const float *>(st + S::head + 64 * kBV * 2)[r] : 0.f;
-            if (warp < 2) {
-                // v' = u - w h for chunk row r
-                float uu[kBV];
-                const unsigned char *ur = st + S::head + (size_t)r * kBV * 2;
-#pragma unroll
-                for (int j = 0; j < kBV; j += 8) {
-                    float f[8];
-                    unpack8(*reinterpret_cast<const uint4 *>(ur + j * 2), f);
-#pragma unroll
-                    for (int t = 0; t < 8; ++t) uu[j + t] = f[t];
-                }
-                if (!mbar_wait(&bar_d1[c & 1], (c >> 1) & 1, kWaitNs)) atomicExch(&abort_flag, 1);
+            if (r >= 1 && has_row) dec = reinterpret_cast<const float *>(st + S::dec)[rr];
+            mbar_arrive(&empty[s]);  // this thread is done reading the stage
+            if (warp < 2 && nxt) {
+                // v'_{c+1} = u_{c+1} - D1[rows 0..63]
+                if (!mbar_spin(&bar_v[r & 1], (r >> 1) & 1, kWaitNs)) atomicExch(&abort_flag, 1);
                 tc_fence_after();
+                float d[16];
+                tmem_ld16(tmem_at(tmem + (r & 1) * kSBV, warp * 32, 0), d);
 #pragma unroll
-                for (int j = 0; j < kBV; j += 16) {
-                    float d[16];
-                    tmem_ld16(tmem_at(d1, warp * 32, j), d);
-#pragma unroll
-                    for (int t = 0; t < 16; ++t) uu[j + t] -= d[t];
-                }
-#pragma unroll
-                for (int j = 0; j < kBV; j += 8)
-                    *reinterpret_cast<uint4 *>(sVp + tile_off(r, j, kBV)) = pack8_at(uu + j);
+                for (int t = 0; t < kSBV; ++t) uu[t] -= d[t];
+                unsigned char *vb2 = sVp + ((r + 1) & 1) * 64 * kSBV * 2;
+                *reinterpret_cast<uint4 *>(vb2 + tile_off(rr, 0, kSBV)) = pack8_at(uu);
+                *reinterpret_cast<uint4 *>(vb2 + tile_off(rr, 8, kSBV)) = pack8_at(uu + 8);
                 fence_async_smem();
                 tc_fence_before();
-                mbar_arrive(&vp_ready);
+                mbar_arrive(&state_ready);
             }
-            if (tid == 0 && ok) {
-                // kg^T v' -> D2 ;  Aqk v' accumulated onto rows 64..127 of D1[c % 2]
-                ok = mbar_wait(&vp_ready, c & 1, kWaitNs);
-                if (ok) {
-                    tc_fence_after();
-                    mma_bf16_k(d2, smem_addr(st + 128 * KK * 2), 128, 1024, smem_addr(sVp),
-                               kBV * 16, 128, id_m1, 4, 0);
-                    mma_commit(&bar_d2);
-                    mma_bf16_k(d1, smem_addr(st + 128 * KK * 2 + 128 * 64 * 2) - 8 * 1024, 128,
-                               1024, smem_addr(sVp), kBV * 16, 128, id_m1, 4, 1);
-                    mma_commit(&bar_d3[c & 1]);
-                } else {
-                    atomicExch(&abort_flag, 1);
-                    report(p.status, KDA_DEVICE_TIMEOUT);
-                }
-            }
-            __syncwarp();
-            // h = Diag(2^G) h + kg^T v'
-            if (!mbar_wait(&bar_d2, c & 1, kWaitNs)) atomicExch(&abort_flag, 1);
-            tc_fence_after();
-#pragma unroll
-            for (int j = 0; j < kBV; j += 16) {
-                float d[16];
-                tmem_ld16(tmem_at(d2, warp * 32, j), d);
-#pragma unroll
-                for (int t = 0; t < 16; ++t) hreg[j + t] = fmaf(dec, hreg[j + t], d[t]);
-            }
-            tc_fence_before();
-            if (warp >= 2) {
-                // o rows (chunk row r - 64): qg h + Aqk v' from D1[c % 2]
-                if (!mbar_wait(&bar_d3[c & 1], (c >> 1) & 1, kWaitNs)) atomicExch(&abort_flag, 1);
+            if (r >= 1) {
+                // h_{c+1} = Diag(2^G_c) h_c + D2
+                if (!mbar_spin(&bar_h, (r - 1) & 1, kWaitNs)) atomicExch(&abort_flag, 1);
                 tc_fence_after();
-                const int i = r - 64;
-                const int row = bos + c * kBT + i;
-                const bool store = row < eos && !read_flag(&abort_flag);
-                __nv_bfloat16 *orow = o + (((size_t)b * p.T + row) * p.HV + hv) * p.V + vb * kBV;
+                float d[16];
+                tmem_ld16(tmem_at(tmem + 2 * kSBV, warp * 32, 0), d);
 #pragma unroll
-                for (int j = 0; j < kBV; j += 16) {
-                    float d[16];
-                    tmem_ld16(tmem_at(d1, warp * 32, j), d);
-                    if (store) {
-                        *reinterpret_cast<uint4 *>(orow + j) = pack8_at(d);
-                        *reinterpret_cast<uint4 *>(orow + j + 8) = pack8_at(d + 8);
-                    }
-                }
+                for (int t = 0; t < kSBV; ++t) hreg[t] = fmaf(dec, hreg[t], d[t]);
                 tc_fence_before();
             }
-            if (c + 1 < nc) write_h();
+            if (nxt) write_h((r + 1) & 1);
+            if (r >= 1 && warp >= 2) {
+                // o_c = D1[rows 64..127]
+                if (!mbar_spin(&bar_v[r & 1], (r >> 1) & 1, kWaitNs)) atomicExch(&abort_flag, 1);
+                tc_fence_after();
+                float d[16];
+                tmem_ld16(tmem_at(tmem + (r & 1) * kSBV, warp * 32, 0), d);
+                tc_fence_before();
+                const int row = bos + (r - 1) * kBT + (rr - 64);
+                if (row < eos && !read_flag(&abort_flag)) {
+                    __nv_bfloat16 *orow =
+                        o + (((size_t)b * p.T + row) * p.HV + hv) * p.V + vb * kSBV;
+                    *reinterpret_cast<uint4 *>(orow) = pack8_at(d);
+                    *reinterpret_cast<uint4 *>(orow + 8) = pack8_at(d + 8);
+                }
+            }
             if (read_flag(&abort_flag)) break;
         }
         if (p.ht && has_row && !read_flag(&abort_flag)) {
-            float4 *dst = reinterpret_cast<float4 *>(p.ht + sbase + (size_t)r * p.V);
+            float4 *dst = reinterpret_cast<float4 *>(p.ht + sbase + (size_t)rr * p.V);
 #pragma unroll
-            for (int j = 0; j < kBV / 4; ++j)
+            for (int j = 0; j < kSBV / 4; ++j)
                 dst[j] = make_float4(hreg[4 * j], hreg[4 * j + 1], hreg[4 * j + 2], hreg[4 * j + 3]);
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 128);
+    if (warp == 0) tmem_dealloc(tmem, 64);
 }
 
 template <int KK, int VV>
@@ -718,7 +834,7 @@ cudaError_t launch_prep(const ChunkArgs &a, cudaStream_t st) {
     }
     dim3 grid((unsigned)a.slots, a.HV);
     prof_begin("chunk_prep_tc", st);
-    chunk_prep_tc_kernel<KK, VV><<<grid, 128, S::total, st>>>(a);
+    chunk_prep_tc_kernel<KK, VV><<<grid, 256, S::total, st>>>(a);
     prof_end(st);
     return cudaGetLastError();
 }
@@ -733,10 +849,10 @@ cudaError_t launch_scan(const ChunkArgs &a, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    const int64_t blocks = (int64_t)a.N * a.HV * (a.V / kBV);
+    const int64_t blocks = (int64_t)a.N * a.HV * (a.V / kSBV);
     if (blocks == 0) return cudaSuccess;
     prof_begin("chunk_scan_tc", st);
-    chunk_scan_tc_kernel<KK><<<(unsigned)blocks, 160, S::total, st>>>(a);
+    chunk_scan_tc_kernel<KK><<<(unsigned)blocks, 192, S::total, st>>>(a);
     prof_end(st);
     return cudaGetLastError();
 }
@@ -764,7 +880,7 @@ cudaError_t launch_k(const ChunkArgs &a, cudaStream_t st) {
 }  // namespace
 
 bool chunk_tc_supported(int K, int V) {
-    return (K == 64 || K == 128) && V >= kBV && V <= 256 && V % kBV == 0;
+    return (K == 64 || K == 128) && V >= 32 && V <= 256 && V % 32 == 0;
 }
 
 size_t chunk_tc_unit_bytes(int K, int V) { return tc_layout(K, V).stride; }

@@ -63,6 +63,18 @@ __device__ __forceinline__ uint32_t mbar_try_wait(uint64_t *bar, uint32_t parity
         : "memory");
     return ok;
 }
+// Non-blocking probe of the phase of the given parity.
+__device__ __forceinline__ uint32_t mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok;
+}
 // Waits for the phase of the given parity to complete.  Gives up after
 // `limit_ns` of wall time and returns false, so no wait can hang the GPU.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
@@ -73,6 +85,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
         if (globaltimer_ns() - t0 > limit_ns) return false;
     }
     return true;
+}
+// Latency-critical variant: spins on the non-blocking probe and checks the
+// clock every 256 probes.  Same time limit and result as mbar_wait.
+__device__ __forceinline__ bool mbar_spin(uint64_t *bar, uint32_t parity,
+                                          uint64_t limit_ns = 1000000000ull) {
+    if (mbar_test_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_test_wait(bar, parity)) return true;
+        if ((i & 255) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
+    }
 }
 
 // ------------------------------------------------------ bulk async copies
@@ -187,6 +210,18 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
             smem_addr(bar))
         : "memory");
+}
+
+// KSTEPS MMAs from precomputed descriptors: instruction k reads the operands
+// at descriptor + k * inc (the start-address field counts 16-byte units, so
+// inc = 2 * LBO / 16).  `acc` says whether the first instruction accumulates.
+template <int KSTEPS, bool ACC>
+__device__ __forceinline__ void mma_bf16_seq(uint32_t d_tmem, uint64_t adesc, uint32_t ainc,
+                                             uint64_t bdesc, uint32_t binc, uint32_t idesc) {
+#pragma unroll
+    for (int kk = 0; kk < KSTEPS; ++kk)
+        mma_bf16(d_tmem, adesc + (uint64_t)(kk * ainc), bdesc + (uint64_t)(kk * binc), idesc,
+                 (ACC || kk > 0) ? 1u : 0u);
 }
 
 // A K-step loop of bf16 MMAs over tiles in the core-matrix layout.
