@@ -23,6 +23,7 @@ __all__ = [
     "KDA_ERR_CUDA", "KDA_ERR_TIMEOUT", "KDA_FLAG_QK_L2NORM", "KDA_FLAG_G_IS_CUMSUM",
     "KdaError", "KdaShape", "load", "library_path", "make_shape",
     "kda_gate_cumsum", "kda_chunk_fwd", "kda_recurrent_fwd", "kda_chunk_workspace_size",
+    "kda_chunk_fwd_noalloc", "KDA_NOALLOC_SCRATCH_BYTES",
     "kda_read_device_status", "kda_clear_device_status", "kda_status_string",
     "kda_last_error_message", "kda_version", "kda_profile_enable", "kda_profile_report",
     "kda_profile_reset",
@@ -70,6 +71,8 @@ _SIGNATURES = {
     "kda_chunk_fwd": (_ST, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.POINTER(KdaShape), _VP,
                             _VP, _VP, _SZ, _VP, _VP]),
     "kda_chunk_workspace_size": (_SZ, [ctypes.POINTER(KdaShape)]),
+    "kda_chunk_fwd_noalloc": (_ST, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.POINTER(KdaShape),
+                                    _VP, _VP, _VP, _VP]),
     "kda_recurrent_fwd": (_ST, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.POINTER(KdaShape),
                                 _VP, _VP, _VP, _VP]),
     "kda_read_device_status": (_ST, [_VP, ctypes.POINTER(ctypes.c_int32), _VP]),
@@ -145,6 +148,18 @@ def kda_chunk_fwd(q, k, v, g, beta, h0, cu_seqlens, shape: KdaShape, o, ht, work
     _check(load().kda_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0),
                                 _ptr(cu_seqlens), ctypes.byref(shape), _ptr(o), _ptr(ht),
                                 _ptr(workspace), nbytes, _ptr(dev_status), _stream(stream)))
+
+
+def kda_chunk_fwd_noalloc(q, k, v, g, beta, h0, cu_seqlens, shape: KdaShape, o, ht,
+                          dev_status=None, stream=None):
+    """kda_chunk_fwd without a workspace: the library's built-in scratch array
+    (KDA_NOALLOC_SCRATCH_BYTES) stands in for it; calls must not overlap."""
+    _check(load().kda_chunk_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                        _ptr(h0), _ptr(cu_seqlens), ctypes.byref(shape), _ptr(o),
+                                        _ptr(ht), _ptr(dev_status), _stream(stream)))
+
+
+KDA_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 def kda_chunk_workspace_size(shape: KdaShape) -> int:

@@ -27,6 +27,7 @@ SOURCES = [
     "kda_chunk_simt.cu",
     "kda_chunk_tc.cu",
     "kda_profile.cu",
+    "kda_noalloc.cu",
 ]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

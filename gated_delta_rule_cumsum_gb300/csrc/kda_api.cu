@@ -108,6 +108,12 @@ kda_status check_chunk_support(const char *op, const kda_shape *s) {
 
 }  // namespace
 
+namespace kda {
+// Lets other translation units of the library report a reason through
+// kda_last_error_message.
+void set_last_error(const char *msg) { g_last_error = msg; }
+}  // namespace kda
+
 extern "C" {
 
 const char *kda_version(void) { return "0.1.0"; }

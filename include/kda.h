@@ -147,6 +147,32 @@ kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const floa
 size_t kda_chunk_workspace_size(const kda_shape *shape);
 
 /*
+ * kda_chunk_fwd_noalloc -- kda_chunk_fwd for callers that cannot allocate
+ * device memory at call time (a runtime that owns a fixed, pre-planned memory
+ * budget, a plugin host that forbids allocations outside its pool, or a
+ * latency-critical loop that cannot afford cudaMalloc's implicit device
+ * synchronisation).  The pages have no counterpart to it: it is a property of
+ * this library's interface, not of the method.
+ *   Arguments, layouts, results and errors are those of kda_chunk_fwd, minus
+ *   the workspace: the call uses a scratch array of KDA_NOALLOC_SCRATCH_BYTES
+ *   built into the library, which every GPU that loads the library holds until
+ *   the process exits.  Shapes whose kda_chunk_workspace_size exceeds it are
+ *   rejected with KDA_ERR_UNSUPPORTED and a message; nothing is enqueued.
+ *   The call allocates nothing.  Its first call on a device looks up the
+ *   array's device address (cudaGetSymbolAddress) and caches it; make that
+ *   first call before any stream capture on that device.
+ *   Every call on a device shares the one array, so calls that overlap on the
+ *   GPU (different streams without ordering) race and give wrong results;
+ *   serialise them.  The array keeps the last call's contents; nothing in it
+ *   needs to start at zero.
+ */
+#define KDA_NOALLOC_SCRATCH_BYTES (32u << 20)
+kda_status kda_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const float *g,
+                                 const void *beta, const float *h0, const int32_t *cu_seqlens,
+                                 const kda_shape *shape, void *o, float *ht, int32_t *dev_status,
+                                 kda_stream_t stream);
+
+/*
  * kda_recurrent_fwd -- token-by-token forward for decode and inference prefill.
  * Defined in attention-gym PR #317, PR description: one sequential scan over
  * the tokens of each (sequence, head, value block) with the [K, BV] fp32 state
