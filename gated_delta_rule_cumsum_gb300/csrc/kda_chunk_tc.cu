@@ -37,7 +37,8 @@ namespace {
 
 using namespace tc;
 
-constexpr int kSBV = 16;              // value columns per scan CTA
+constexpr int kSBV = 32;              // value columns per scan CTA
+constexpr int kUB = 16;               // column block of u in the workspace
 constexpr int kStages = 3;            // scan pipeline depth
 constexpr float kSafeRange = 60.f;    // max |g2| (log2) for the split grams
 constexpr uint64_t kWaitNs = 1000000000ull;
@@ -49,7 +50,7 @@ struct TcLayout {
     uint32_t kgt;     // [128][64] tile: kg_c^T (rows >= dk zero)
     uint32_t mt;      // [64][64] tile: M_c = W_c kg_{c-1}^T (unused for a first chunk)
     uint32_t aqk;     // [64][64] tile: Aqk_c (scale inside)
-    uint32_t u;       // [dv / 16][64][16] bf16 row-major blocks: u_c
+    uint32_t u;       // [dv / kUB][64][kUB] bf16 row-major blocks: u_c
     uint32_t dec;     // [128] fp32: 2^G_c (0 beyond dk)
     uint32_t stride;  // unit size, 256-byte multiple
 };
@@ -91,9 +92,6 @@ __device__ __forceinline__ bool locate_chunk(const ChunkArgs &p, int64_t gc, int
 __device__ __forceinline__ void cp_async16(void *dst, const void *src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
                  : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
 
 __device__ __forceinline__ void unpack8(const uint4 &u, float (&f)[8]) {
@@ -544,7 +542,7 @@ __global__ void __launch_bounds__(256) chunk_prep_tc_kernel(ChunkArgs p) {
         for (int c0 = cbeg; c0 < cbeg + VV / 2; c0 += 16) {
             float dd[16];
             tmem_ld16(tmem_at(tmem, quad * 32, c0), dd);
-            unsigned char *ub = U + Lo.u + ((size_t)(c0 / kSBV) * 64 + i) * kSBV * 2;
+            unsigned char *ub = U + Lo.u + ((size_t)(c0 / kUB) * 64 + i) * kUB * 2;
             *reinterpret_cast<uint4 *>(ub) = pack8_at(dd);
             *reinterpret_cast<uint4 *>(ub + 16) = pack8_at(dd + 8);
         }
@@ -555,27 +553,31 @@ __global__ void __launch_bounds__(256) chunk_prep_tc_kernel(ChunkArgs p) {
 }
 
 // ============================================================== scan kernel
-// Rounds r = 0 .. nc of one (sequence, value head, 16 value columns); round r
+// Rounds r = 0 .. nc of one (sequence, value head, 32 value columns); round r
 // finishes chunk c = r - 1 and starts chunk c + 1:
-//   D1 = [W~_{c+1}; qg_c] h_c + [M_{c+1}; Aqk_c] v'_c   rows 0..63 -> v'_{c+1} = u_{c+1} - D1
-//                                                      rows 64..127 -> o_c
-//   D2 = kg_c^T v'_c                                   h_{c+1} = Diag(2^G_c) h_c + D2
+//   A: D1  = [W~_{c+1}; qg_c] h_c        (needs h_c)
+//   C: D2  = kg_c^T v'_c                 (needs v'_c)   ->  h_{c+1} = Diag(2^G_c) h_c + D2
+//   B: D1 += [M_{c+1}; Aqk_c] v'_c       (needs v'_c)   ->  v'_{c+1} = u_{c+1} - D1[0:64]
+//                                                          o_c      = D1[64:128]
 // where W~_{c+1} = W_{c+1} Diag(2^G_c) and M_{c+1} = W_{c+1} kg_c^T come from the
-// prep kernel: v'_{c+1} = u_{c+1} - W_{c+1} h_{c+1} expands into the two terms, so
-// one MMA round per chunk carries the whole recurrence.  Round 0 only forms
-// v'_0 = u_0 - W_0 h_0.
+// prep kernel: v'_{c+1} = u_{c+1} - W_{c+1} h_{c+1} expands into the A and B
+// terms.  Issue order A, C, B: the state update (after C) overlaps B, and the
+// next round's A can start as soon as h_{c+1} is written.  Round 0 only forms
+// v'_0 = u_0 - W_0 h_0.  A tcgen05.mma of these shapes occupies the tensor
+// unit for a fixed ~50 cycles whatever N <= 64 is, so 32 columns per CTA cost
+// no more MMA time than 16.
 template <int KK>
 struct ScanSmem {
     static constexpr uint32_t top = 0;                         // [128][KK]: W~_{c+1}; qg_c
     static constexpr uint32_t kgt = top + 128 * KK * 2;        // [128][64]: kg_c^T
     static constexpr uint32_t bot = kgt + 128 * 64 * 2;        // [128][64]: M_{c+1}; Aqk_c
-    static constexpr uint32_t u = bot + 128 * 64 * 2;          // [64][kSBV] bf16: u_{c+1}
+    static constexpr uint32_t u = bot + 128 * 64 * 2;          // [kSBV/kUB][64][kUB] bf16: u_{c+1}
     static constexpr uint32_t dec = u + 64 * kSBV * 2;         // [128] fp32: 2^G_c
     static constexpr uint32_t stage = dec + 512;
     static constexpr uint32_t stage_stride = (stage + 1023) / 1024 * 1024;
-    static constexpr uint32_t hs = kStages * stage_stride;     // 2 x [KK][kSBV] tile
-    static constexpr uint32_t vp = hs + 2 * KK * kSBV * 2;     // 2 x [64][kSBV] tile
-    static constexpr uint32_t total = vp + 2 * 64 * kSBV * 2;
+    static constexpr uint32_t hs = kStages * stage_stride;     // [KK][kSBV] tile
+    static constexpr uint32_t vp = hs + KK * kSBV * 2;         // [64][kSBV] tile
+    static constexpr uint32_t total = vp + 64 * kSBV * 2;
 };
 
 __device__ __forceinline__ int read_flag(const int *f) {
@@ -583,11 +585,13 @@ __device__ __forceinline__ int read_flag(const int *f) {
 }
 
 template <int KK>
-__global__ void __launch_bounds__(192, 1) chunk_scan_tc_kernel(ChunkArgs p) {
+__global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
     using S = ScanSmem<KK>;
     extern __shared__ __align__(1024) unsigned char sm[];
     __shared__ uint64_t full[kStages], empty[kStages];
-    __shared__ uint64_t bar_v[2], bar_h, state_ready;
+    // bar_v[x]: MMAs writing D1[x] done (one per buffer: the o readers arrive on
+    // h_ready before they wait here, so a single barrier could be lapped).
+    __shared__ uint64_t bar_v[2], bar_h, h_ready, v_ready;
     __shared__ uint32_t tslot;
     __shared__ int abort_flag;
 
@@ -616,33 +620,33 @@ __global__ void __launch_bounds__(192, 1) chunk_scan_tc_kernel(ChunkArgs p) {
     }
     const int R = nc > 0 ? nc + 1 : 0;  // rounds
     const TcLayout Lo = tc_layout(KK, p.V);
-    const size_t sbase = ((size_t)n * p.HV + hv) * (size_t)KK * p.V + (size_t)vb * kSBV;
     const unsigned char *units = static_cast<const unsigned char *>(p.units);
 
     if (warp == 0) {
-        tmem_alloc(&tslot, 64);
+        tmem_alloc(&tslot, 128);
         tmem_relinquish();
     }
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1 + 128);
+            mbar_init(&empty[s], 1 + 256);
         }
         mbar_init(&bar_v[0], 1);
         mbar_init(&bar_v[1], 1);
         mbar_init(&bar_h, 1);
-        mbar_init(&state_ready, 192);
+        mbar_init(&h_ready, 256);
+        mbar_init(&v_ready, 128);
         mbar_fence_init();
         abort_flag = 0;
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = tslot;  // D1[0] at +0, D1[1] at +16, D2 at +32
+    const uint32_t tmem = tslot;  // D1[0] at +0, D1[1] at +32, D2 at +64
     unsigned char *sH = sm + S::hs;
     unsigned char *sVp = sm + S::vp;
 
-    if (warp == 4) {
+    if (warp == 8) {
         // ------------------------------------------------------- producer
         if (lane == 0) {
             int issued = 0;
@@ -662,16 +666,14 @@ __global__ void __launch_bounds__(192, 1) chunk_scan_tc_kernel(ChunkArgs p) {
                 if (cur) bytes += 64 * KK * 2 + 128 * 64 * 2 + 64 * 64 * 2 + 512;
                 mbar_arrive_expect_tx(&full[s], bytes);
                 if (nxt) {
-                    const unsigned char *U1 = units + (gc0 + c + 1) * p.HV * (int64_t)Lo.stride +
-                                              (int64_t)hv * Lo.stride;
+                    const unsigned char *U1 = units + ((gc0 + c + 1) * p.HV + hv) * (int64_t)Lo.stride;
                     bulk_g2s(st + S::top, U1 + Lo.aw, 64 * KK * 2, &full[s]);
                     bulk_g2s(st + S::u, U1 + Lo.u + (size_t)vb * 64 * kSBV * 2, 64 * kSBV * 2,
                              &full[s]);
                     if (cur) bulk_g2s(st + S::bot, U1 + Lo.mt, 64 * 64 * 2, &full[s]);
                 }
                 if (cur) {
-                    const unsigned char *U0 = units + (gc0 + c) * p.HV * (int64_t)Lo.stride +
-                                              (int64_t)hv * Lo.stride;
+                    const unsigned char *U0 = units + ((gc0 + c) * p.HV + hv) * (int64_t)Lo.stride;
                     bulk_g2s(st + S::top + 64 * KK * 2, U0 + Lo.aw + 64 * KK * 2, 64 * KK * 2,
                              &full[s]);
                     bulk_g2s(st + S::kgt, U0 + Lo.kgt, 128 * 64 * 2, &full[s]);
@@ -684,79 +686,80 @@ __global__ void __launch_bounds__(192, 1) chunk_scan_tc_kernel(ChunkArgs p) {
             for (int r = issued - kStages > 0 ? issued - kStages : 0; r < issued; ++r)
                 mbar_wait(&full[r % kStages], (r / kStages) & 1, kWaitNs);
         }
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         // ----------------------------------------------------- MMA issuer
         if (lane == 0) {
             const uint32_t idn = idesc_bf16(128, kSBV, false, true);
             const uint32_t base = smem_addr(sm);
-            uint64_t dh[2], dv[2];
-            for (int i = 0; i < 2; ++i) {
-                dh[i] = sdesc(smem_addr(sH) + i * KK * kSBV * 2, kSBV * 16, 128);
-                dv[i] = sdesc(smem_addr(sVp) + i * 64 * kSBV * 2, kSBV * 16, 128);
-            }
+            const uint64_t dh = sdesc(smem_addr(sH), kSBV * 16, 128);
+            const uint64_t dv = sdesc(smem_addr(sVp), kSBV * 16, 128);
+            constexpr uint32_t binc = 2 * kSBV * 16 / 16;
             for (int r = 0; r < R; ++r) {
                 const int s = r % kStages;
                 const uint32_t st = base + s * S::stage_stride;
+                const uint32_t d1 = tmem + (r & 1) * kSBV;
                 if (!mbar_spin(&full[s], (r / kStages) & 1, kWaitNs) ||
-                    !mbar_spin(&state_ready, r & 1, kWaitNs)) {
+                    !mbar_spin(&h_ready, r & 1, kWaitNs)) {
                     atomicExch(&abort_flag, 1);
                     report(p.status, KDA_DEVICE_TIMEOUT);
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d1 = tmem + (r & 1) * kSBV;
-                mma_bf16_seq<KK / 16, false>(d1, sdesc(st + S::top, 128, KK * 16), 16, dh[r & 1],
-                                             2 * kSBV * 16 / 16, idn);
-                if (r >= 1)
-                    mma_bf16_seq<4, true>(d1, sdesc(st + S::bot, 128, 1024), 16, dv[r & 1],
-                                          2 * kSBV * 16 / 16, idn);
-                mma_commit(&bar_v[r & 1]);
+                mma_bf16_seq<KK / 16, false>(d1, sdesc(st + S::top, 128, KK * 16), 16, dh, binc, idn);
                 if (r >= 1) {
-                    mma_bf16_seq<4, false>(tmem + 2 * kSBV, sdesc(st + S::kgt, 128, 1024), 16,
-                                           dv[r & 1], 2 * kSBV * 16 / 16, idn);
+                    if (!mbar_spin(&v_ready, (r - 1) & 1, kWaitNs)) {
+                        atomicExch(&abort_flag, 1);
+                        report(p.status, KDA_DEVICE_TIMEOUT);
+                        break;
+                    }
+                    tc_fence_after();
+                    mma_bf16_seq<4, false>(tmem + 2 * kSBV, sdesc(st + S::kgt, 128, 1024), 16, dv,
+                                           binc, idn);
                     mma_commit(&bar_h);
+                    mma_bf16_seq<4, true>(d1, sdesc(st + S::bot, 128, 1024), 16, dv, binc, idn);
                 }
+                mma_commit(&bar_v[r & 1]);
                 mma_commit(&empty[s]);
             }
         }
     } else {
-        // ---------------------------- epilogue: warps 0..3, thread r = lane row
-        const int rr = tid;
-        const bool has_row = rr < KK;
-        float hreg[kSBV];
+        // ------- epilogue: warps 0..7; row = 32 (warp % 4) + lane, columns 16 (warp / 4) ..
+        const int quad = warp & 3, ch = warp >> 2;
+        const int row = quad * 32 + lane;
+        const int col0 = ch * 16;
+        const bool has_row = row < KK;
+        const size_t scol = ((size_t)n * p.HV + hv) * (size_t)KK * p.V + (size_t)vb * kSBV + col0;
+        float hreg[16];
 #pragma unroll
-        for (int j = 0; j < kSBV; ++j) hreg[j] = 0.f;
+        for (int j = 0; j < 16; ++j) hreg[j] = 0.f;
         if (has_row && p.h0) {
-            const float4 *src = reinterpret_cast<const float4 *>(p.h0 + sbase + (size_t)rr * p.V);
+            const float4 *src = reinterpret_cast<const float4 *>(p.h0 + scol + (size_t)row * p.V);
 #pragma unroll
-            for (int j = 0; j < kSBV / 4; ++j) {
+            for (int j = 0; j < 4; ++j) {
                 const float4 x = src[j];
                 hreg[4 * j] = x.x; hreg[4 * j + 1] = x.y; hreg[4 * j + 2] = x.z; hreg[4 * j + 3] = x.w;
             }
         }
-        auto write_h = [&](int buf) {
+        auto write_h = [&]() {
             if (has_row) {
-                unsigned char *hb = sH + buf * KK * kSBV * 2;
-                *reinterpret_cast<uint4 *>(hb + tile_off(rr, 0, kSBV)) = pack8_at(hreg);
-                *reinterpret_cast<uint4 *>(hb + tile_off(rr, 8, kSBV)) = pack8_at(hreg + 8);
+                *reinterpret_cast<uint4 *>(sH + tile_off(row, col0, kSBV)) = pack8_at(hreg);
+                *reinterpret_cast<uint4 *>(sH + tile_off(row, col0 + 8, kSBV)) = pack8_at(hreg + 8);
             }
             fence_async_smem();
-            mbar_arrive(&state_ready);
+            mbar_arrive(&h_ready);
         };
-        if (R > 0) {
-            write_h(0);
-            if (warp < 2) mbar_arrive(&state_ready);  // no v'_{-1}
-        }
+        if (R > 0) write_h();
+        const uint32_t lanebase = (uint32_t)(quad * 32) << 16;
         __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.o);
         for (int r = 0; r < R; ++r) {
             const int s = r % kStages;
             const unsigned char *st = sm + s * S::stage_stride;
             const bool nxt = r < nc;
             if (!mbar_spin(&full[s], (r / kStages) & 1, kWaitNs)) atomicExch(&abort_flag, 1);
-            float uu[kSBV];
+            float uu[16];
             float dec = 1.f;
-            if (warp < 2 && nxt) {
-                const unsigned char *ur = st + S::u + (size_t)rr * kSBV * 2;
+            if (quad < 2 && nxt) {
+                const unsigned char *ur = st + S::u + ((size_t)ch * 64 + row) * kUB * 2;
                 float f[8];
                 unpack8(*reinterpret_cast<const uint4 *>(ur), f);
 #pragma unroll
@@ -765,61 +768,66 @@ __global__ void __launch_bounds__(192, 1) chunk_scan_tc_kernel(ChunkArgs p) {
 #pragma unroll
                 for (int t = 0; t < 8; ++t) uu[8 + t] = f[t];
             }
-            if (r >= 1 && has_row) dec = reinterpret_cast<const float *>(st + S::dec)[rr];
-            mbar_arrive(&empty[s]);  // this thread is done reading the stage
-            if (warp < 2 && nxt) {
+            if (r >= 1 && has_row) dec = reinterpret_cast<const float *>(st + S::dec)[row];
+            mbar_arrive(&empty[s]);  // done reading the stage
+            if (r >= 1) {
+                // h_{c+1} = Diag(2^G_c) h_c + D2  (bar_h also covers A_r's reads of h_c)
+                if (!mbar_spin(&bar_h, (r - 1) & 1, kWaitNs)) atomicExch(&abort_flag, 1);
+                tc_fence_after();
+                float d[16];
+                tmem_ld16(tmem + lanebase + 2 * kSBV + col0, d);
+#pragma unroll
+                for (int t = 0; t < 16; ++t) hreg[t] = fmaf(dec, hreg[t], d[t]);
+                tc_fence_before();
+                if (nxt) write_h();
+            } else if (nxt) {
+                // Round 0 leaves h_0 in place.  Arrive only once round 0's MMA has
+                // completed: the MMA warp then has consumed the previous phase of
+                // h_ready, so this arrival cannot lap it.
+                if (!mbar_spin(&bar_v[0], 0, kWaitNs)) atomicExch(&abort_flag, 1);
+                mbar_arrive(&h_ready);
+            }
+            if (quad < 2 && nxt) {
                 // v'_{c+1} = u_{c+1} - D1[rows 0..63]
                 if (!mbar_spin(&bar_v[r & 1], (r >> 1) & 1, kWaitNs)) atomicExch(&abort_flag, 1);
                 tc_fence_after();
                 float d[16];
-                tmem_ld16(tmem_at(tmem + (r & 1) * kSBV, warp * 32, 0), d);
+                tmem_ld16(tmem + lanebase + (r & 1) * kSBV + col0, d);
+                tc_fence_before();
 #pragma unroll
-                for (int t = 0; t < kSBV; ++t) uu[t] -= d[t];
-                unsigned char *vb2 = sVp + ((r + 1) & 1) * 64 * kSBV * 2;
-                *reinterpret_cast<uint4 *>(vb2 + tile_off(rr, 0, kSBV)) = pack8_at(uu);
-                *reinterpret_cast<uint4 *>(vb2 + tile_off(rr, 8, kSBV)) = pack8_at(uu + 8);
+                for (int t = 0; t < 16; ++t) uu[t] -= d[t];
+                *reinterpret_cast<uint4 *>(sVp + tile_off(row, col0, kSBV)) = pack8_at(uu);
+                *reinterpret_cast<uint4 *>(sVp + tile_off(row, col0 + 8, kSBV)) = pack8_at(uu + 8);
                 fence_async_smem();
-                tc_fence_before();
-                mbar_arrive(&state_ready);
+                mbar_arrive(&v_ready);
             }
-            if (r >= 1) {
-                // h_{c+1} = Diag(2^G_c) h_c + D2
-                if (!mbar_spin(&bar_h, (r - 1) & 1, kWaitNs)) atomicExch(&abort_flag, 1);
-                tc_fence_after();
-                float d[16];
-                tmem_ld16(tmem_at(tmem + 2 * kSBV, warp * 32, 0), d);
-#pragma unroll
-                for (int t = 0; t < kSBV; ++t) hreg[t] = fmaf(dec, hreg[t], d[t]);
-                tc_fence_before();
-            }
-            if (nxt) write_h((r + 1) & 1);
-            if (r >= 1 && warp >= 2) {
+            if (quad >= 2 && r >= 1) {
                 // o_c = D1[rows 64..127]
                 if (!mbar_spin(&bar_v[r & 1], (r >> 1) & 1, kWaitNs)) atomicExch(&abort_flag, 1);
                 tc_fence_after();
                 float d[16];
-                tmem_ld16(tmem_at(tmem + (r & 1) * kSBV, warp * 32, 0), d);
+                tmem_ld16(tmem + lanebase + (r & 1) * kSBV + col0, d);
                 tc_fence_before();
-                const int row = bos + (r - 1) * kBT + (rr - 64);
-                if (row < eos && !read_flag(&abort_flag)) {
-                    __nv_bfloat16 *orow =
-                        o + (((size_t)b * p.T + row) * p.HV + hv) * p.V + vb * kSBV;
-                    *reinterpret_cast<uint4 *>(orow) = pack8_at(d);
-                    *reinterpret_cast<uint4 *>(orow + 8) = pack8_at(d + 8);
+                const int orow = bos + (r - 1) * kBT + (row - 64);
+                if (orow < eos && !read_flag(&abort_flag)) {
+                    __nv_bfloat16 *op =
+                        o + (((size_t)b * p.T + orow) * p.HV + hv) * p.V + vb * kSBV + col0;
+                    *reinterpret_cast<uint4 *>(op) = pack8_at(d);
+                    *reinterpret_cast<uint4 *>(op + 8) = pack8_at(d + 8);
                 }
             }
             if (read_flag(&abort_flag)) break;
         }
         if (p.ht && has_row && !read_flag(&abort_flag)) {
-            float4 *dst = reinterpret_cast<float4 *>(p.ht + sbase + (size_t)rr * p.V);
+            float4 *dst = reinterpret_cast<float4 *>(p.ht + scol + (size_t)row * p.V);
 #pragma unroll
-            for (int j = 0; j < kSBV / 4; ++j)
+            for (int j = 0; j < 4; ++j)
                 dst[j] = make_float4(hreg[4 * j], hreg[4 * j + 1], hreg[4 * j + 2], hreg[4 * j + 3]);
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 64);
+    if (warp == 0) tmem_dealloc(tmem, 128);
 }
 
 template <int KK, int VV>
@@ -852,7 +860,7 @@ cudaError_t launch_scan(const ChunkArgs &a, cudaStream_t st) {
     const int64_t blocks = (int64_t)a.N * a.HV * (a.V / kSBV);
     if (blocks == 0) return cudaSuccess;
     prof_begin("chunk_scan_tc", st);
-    chunk_scan_tc_kernel<KK><<<(unsigned)blocks, 192, S::total, st>>>(a);
+    chunk_scan_tc_kernel<KK><<<(unsigned)blocks, 320, S::total, st>>>(a);
     prof_end(st);
     return cudaGetLastError();
 }
