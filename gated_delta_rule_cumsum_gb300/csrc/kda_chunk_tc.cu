@@ -47,7 +47,8 @@ constexpr uint64_t kWaitNs = 1000000000ull;
 struct TcLayout {
     uint32_t aw;      // [128][dk] tile: rows 0..63 W~_c = W_c Diag(2^G_{c-1}) (W_0 for a
                       // sequence's first chunk), rows 64..127 scale * qg_c
-    uint32_t kgt;     // [128][64] tile: kg_c^T (rows >= dk zero)
+    uint32_t kgt;     // [64][dk] tile: kg_c (rows = tokens), read by the scan as an
+                      // MN-major operand, i.e. as kg_c^T
     uint32_t mt;      // [64][64] tile: M_c = W_c kg_{c-1}^T (unused for a first chunk)
     uint32_t aqk;     // [64][64] tile: Aqk_c (scale inside)
     uint32_t u;       // [dv / kUB][64][kUB] bf16 row-major blocks: u_c
@@ -59,7 +60,7 @@ __host__ __device__ inline TcLayout tc_layout(int K, int V) {
     TcLayout L;
     uint32_t off = 0;
     L.aw = off;  off += 128u * K * 2;
-    L.kgt = off; off += 128u * 64 * 2;
+    L.kgt = off; off += 64u * K * 2;
     L.mt = off;  off += 64u * 64 * 2;
     L.aqk = off; off += 64u * 64 * 2;
     L.u = off;   off += 64u * V * 2;
@@ -121,17 +122,21 @@ __device__ __forceinline__ uint4 pack8_at(const float *f) {
 // ============================================================== prep kernel
 template <int KK, int VV>
 struct PrepSmem {
-    static constexpr uint32_t ag = 0;                           // [128][KK]: q->qg, k->kg; Akk fp32 later
-    static constexpr uint32_t kbx = ag + 128 * KK * 2;          // [128][KK]: kb; kg of the previous chunk
-    // L (fp32 [64][64]) and the solve scratch: over the kb rows for dk = 128, after
-    // the tile for dk = 64 (so the previous chunk's kg survives the exact grams).
-    static constexpr uint32_t lbuf = (KK == 128) ? kbx : kbx + 128 * KK * 2;
-    static constexpr uint32_t kbx_bytes = (KK == 128) ? 128 * KK * 2 : 128 * KK * 2 + 64 * 64 * 4 + 4096;
-    static constexpr uint32_t ab = kbx + kbx_bytes;             // [64][64]: Akk diag(beta) (8 KB before it valid)
-    static constexpr uint32_t pb = ab + 64 * 64 * 2;            // [64][64]: P = kg_c kgp^T
-    static constexpr uint32_t v = pb + 64 * 64 * 2;             // [64][VV]
-    static constexpr uint32_t akk = (64 * KK * 2 >= 64 * 64 * 4) ? ag : v + 64 * VV * 2;  // fp32 [64][64]
-    static constexpr uint32_t used = (akk == ag) ? v + 64 * VV * 2 : akk + 64 * 64 * 4;
+    static constexpr int kGS = KK + 4;                          // padded fp32 row of g2
+    static constexpr uint32_t tile = 128 * KK * 2;
+    static constexpr uint32_t ag = 0;                           // [128][KK]: q->qg, k->kg; Akk (fp32) later
+    static constexpr uint32_t kbx = ag + tile;                  // [128][KK]: kb; kg of the previous chunk
+    static constexpr uint32_t g = kbx + tile;                   // fp32 [64][kGS] g2; later v tile + AB tile
+    static constexpr uint32_t g_need0 = 64 * kGS * 4;
+    static constexpr uint32_t g_need1 = 64 * VV * 2 + 64 * 64 * 2;
+    static constexpr uint32_t g_bytes = g_need0 > g_need1 ? g_need0 : g_need1;
+    static constexpr uint32_t extra = g + g_bytes;              // dk = 64 only: L, scratch, P, Akk
+    static constexpr bool big = KK == 128;
+    static constexpr uint32_t lbuf = big ? kbx : extra;                       // L fp32 [64][64]
+    static constexpr uint32_t tbuf = lbuf + 64 * 64 * 4;                      // solve scratch 3 KB
+    static constexpr uint32_t pbuf = tbuf + 3072;                             // P tile [64][64] bf16
+    static constexpr uint32_t abuf = big ? ag : pbuf + 64 * 64 * 2;           // Akk fp32 [64][64]
+    static constexpr uint32_t used = big ? extra : abuf + 64 * 64 * 4;
     // Floor so that at most two CTAs (256 TMEM columns each) share an SM.
     static constexpr uint32_t total = used > 80 * 1024 ? used : 80 * 1024;
 };
@@ -146,6 +151,8 @@ __global__ void __launch_bounds__(256) chunk_prep_tc_kernel(ChunkArgs p) {
     extern __shared__ __align__(1024) unsigned char sm[];
     __shared__ float sBeta[64];
     __shared__ float sDprev[128];
+    __shared__ float sEG[128];  // 2^G per channel
+    __shared__ float sGv[128];  // G per channel
     __shared__ uint64_t bar;
     __shared__ uint32_t tslot;
     __shared__ int sRangeBits;
@@ -158,15 +165,17 @@ __global__ void __launch_bounds__(256) chunk_prep_tc_kernel(ChunkArgs p) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int h = hv / (p.HV / p.H);
     constexpr uint32_t kCols = 256;
+    constexpr int kGS = S::kGS;
 
     unsigned char *sAG = sm + S::ag;
     unsigned char *sKB = sm + S::kbx;
-    unsigned char *sAB = sm + S::ab;
-    unsigned char *sPB = sm + S::pb;
-    unsigned char *sV = sm + S::v;
-    float *sL = reinterpret_cast<float *>(sm + S::lbuf);
-    float *sT = sL + 64 * 64;                                      // solve scratch (3 KB)
-    float *sA = reinterpret_cast<float *>(sm + S::akk);            // Akk, row stride 64
+    float *sG2 = reinterpret_cast<float *>(sm + S::g);
+    unsigned char *sV = sm + S::g;                          // after the elementwise phase
+    unsigned char *sAB = sm + S::g + 64 * VV * 2;           // (8 KB before it valid)
+    float *sL = reinterpret_cast<float *>(sm + S::lbuf);    // after the gram MMA
+    float *sT = reinterpret_cast<float *>(sm + S::tbuf);
+    unsigned char *sPB = sm + S::pbuf;
+    float *sA = reinterpret_cast<float *>(sm + S::abuf);
 
     const TcLayout Lo = tc_layout(KK, VV);
     unsigned char *U = static_cast<unsigned char *>(p.units) + (gc * p.HV + hv) * Lo.stride;
@@ -182,13 +191,13 @@ __global__ void __launch_bounds__(256) chunk_prep_tc_kernel(ChunkArgs p) {
     }
     __syncthreads();
 
-    // ---- 1. async loads: q, k (and the previous chunk's k) and v as operand tiles
+    // ---- 1. async loads: q, k (and the previous chunk's k) as operand tiles, g fp32
     const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(p.q);
     const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(p.k);
     const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(p.v);
     const __nv_bfloat16 *beta = static_cast<const __nv_bfloat16 *>(p.beta);
     const size_t row0 = (size_t)b * p.T + r0;
-    constexpr int KG8 = KK / 8, VG8 = VV / 8;
+    constexpr int KG8 = KK / 8, VG8 = VV / 8, KG4 = KK / 4;
     for (int idx = tid; idx < 64 * KG8; idx += 256) {
         const int i = idx / KG8, c = (idx % KG8) * 8;
         void *dq = sAG + tile_off(i, c, KK);
@@ -204,62 +213,46 @@ __global__ void __launch_bounds__(256) chunk_prep_tc_kernel(ChunkArgs p) {
         if (halo)
             cp_async16(sKB + tile_off(64 + i, c, KK), k + ((row0 - 64 + i) * p.H + h) * KK + c);
     }
-    for (int idx = tid; idx < 64 * VG8; idx += 256) {
-        const int i = idx / VG8, c = (idx % VG8) * 8;
-        void *dv = sV + tile_off(i, c, VV);
+    for (int idx = tid; idx < 64 * KG4; idx += 256) {
+        const int i = idx / KG4, c = (idx % KG4) * 4;
+        float *dg = sG2 + i * kGS + c;
         if (i < nr)
-            cp_async16(dv, v + ((row0 + i) * p.HV + hv) * VV + c);
+            cp_async16(dg, p.g + ((row0 + i) * p.HV + hv) * KK + c);
         else
-            *reinterpret_cast<uint4 *>(dv) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<float4 *>(dg) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
     if (tid < 64) sBeta[tid] = tid < nr ? to_f32(beta[(row0 + tid) * p.HV + hv]) : 0.f;
 
-    // ---- 2. gate cumsums in registers: thread d < KK owns channel d of this
-    // chunk; thread 128 + d owns channel d of the previous chunk (suffix sums).
-    float gam[64];
-    const int d = tid & 127;
-    const bool own = d < KK && (tid < 128 || halo);
-    if (own) {
-        const float *gp = p.g + ((tid < 128 ? row0 : row0 - 64) * p.HV + hv) * KK + d;
+    // The previous chunk's gates in registers: thread 128 + d turns its channel d
+    // into eprev[j] = 2^(G' - g2'_j) and 2^G' (suffix sums over the full chunk).
+    float eprev[64];
+    const int dh = tid - 128;
+    const bool halo_thread = halo && tid >= 128 && dh < KK;
+    if (halo_thread) {
+        const float *gp = p.g + ((row0 - 64) * p.HV + hv) * KK + dh;
         const size_t rs = (size_t)p.HV * KK;
-        const int lim = tid < 128 ? nr : 64;
-        // Unpredicated loads of clamped rows (one batch in flight), then masking.
 #pragma unroll
-        for (int i = 0; i < 64; ++i) gam[i] = __ldg(gp + (size_t)min(i, lim - 1) * rs);
+        for (int j = 0; j < 64; ++j) eprev[j] = __ldg(gp + j * rs);
+        float Gp;
+        if (p.g_is_cumsum) {
+            Gp = eprev[63];
 #pragma unroll
-        for (int i = 0; i < 64; ++i) gam[i] = i < lim ? gam[i] : 0.f;
-        if (tid < 128) {  // inclusive prefix sums; rows past the end keep G
-            float acc = 0.f, rng = 0.f;
+            for (int j = 0; j < 64; ++j) eprev[j] = exp2f(Gp - eprev[j]);
+        } else {
+            float acc = 0.f;
 #pragma unroll
-            for (int i = 0; i < 64; ++i) {
-                acc = p.g_is_cumsum ? (i < lim ? gam[i] : acc) : fmaf(p.g_scale, gam[i], acc);
-                gam[i] = acc;
-                rng = fmaxf(rng, fabsf(acc));
+            for (int j = 63; j >= 0; --j) {
+                const float gj = eprev[j];
+                eprev[j] = exp2f(acc);
+                acc = fmaf(p.g_scale, gj, acc);
             }
-            atomicMax(&sRangeBits, __float_as_int(rng));
-        } else {  // gam[j] <- 2^(G' - g2'_j) for the previous chunk; sDprev <- 2^G'
-            float Gp;
-            if (p.g_is_cumsum) {
-                Gp = gam[63];
-#pragma unroll
-                for (int j = 0; j < 64; ++j) gam[j] = exp2f(Gp - gam[j]);
-            } else {
-                float acc = 0.f;
-#pragma unroll
-                for (int j = 63; j >= 0; --j) {
-                    const float gj = gam[j];
-                    gam[j] = exp2f(acc);
-                    acc = fmaf(p.g_scale, gj, acc);
-                }
-                Gp = acc;
-            }
-            sDprev[d] = exp2f(Gp);
+            Gp = acc;
         }
+        sDprev[dh] = exp2f(Gp);
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
     __syncthreads();
-    const bool fast = __int_as_float(sRangeBits) <= kSafeRange;
 
     // ---- optional L2 normalisation of q, k and the previous chunk's k rows
     if (p.l2norm) {
@@ -286,21 +279,41 @@ __global__ void __launch_bounds__(256) chunk_prep_tc_kernel(ChunkArgs p) {
         __syncthreads();
     }
 
-    // ---- exact grams for chunks whose gate range is too wide to split.  g2 goes
-    // through this unit's own (not yet written) output slot as fp32 scratch.
-    if (!fast) {
-        float *gs = reinterpret_cast<float *>(U + Lo.aw);  // [64][KK] fp32
-        if (tid < KK) {
+    // ---- 2. Stage 1 cumsum in place (thread d owns channel d); the previous
+    // chunk's k becomes its kg on the halo threads meanwhile.
+    if (tid < KK) {
+        float acc = 0.f, rng = 0.f;
 #pragma unroll
-            for (int i = 0; i < 64; ++i) gs[i * KK + tid] = gam[i];
+        for (int i = 0; i < 64; ++i) {
+            const float gv = sG2[i * kGS + tid];
+            if (i < nr) acc = p.g_is_cumsum ? gv : fmaf(p.g_scale, gv, acc);
+            sG2[i * kGS + tid] = acc;  // rows past the end keep G
+            rng = fmaxf(rng, fabsf(acc));
         }
-        __threadfence_block();
-        __syncthreads();
+        const float eG = exp2f(acc);
+        sEG[tid] = eG;
+        sGv[tid] = acc;
+        reinterpret_cast<float *>(U + Lo.dec)[tid] = eG;
+        atomicMax(&sRangeBits, __float_as_int(rng));
+    } else if (tid < 128) {
+        reinterpret_cast<float *>(U + Lo.dec)[tid] = 0.f;
+    } else if (halo_thread) {
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+            __nv_bfloat16 *pk = reinterpret_cast<__nv_bfloat16 *>(sKB + tile_off(64 + j, dh, KK));
+            *pk = __float2bfloat16_rn(__bfloat162float(*pk) * eprev[j]);
+        }
+    }
+    __syncthreads();
+    const bool fast = __int_as_float(sRangeBits) <= kSafeRange;
+
+    // ---- exact grams for chunks whose gate range is too wide to split
+    if (!fast) {
         for (int i = warp; i < 64; i += 8) {
             for (int j = 0; j <= i; ++j) {
                 float aq = 0.f, ak = 0.f;
                 for (int dd = lane; dd < KK; dd += 32) {
-                    const float e = exp2f(gs[i * KK + dd] - gs[j * KK + dd]);
+                    const float e = exp2f(sG2[i * kGS + dd] - sG2[j * kGS + dd]);
                     const float qi = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
                         sAG + tile_off(i, dd, KK)));
                     const float ki = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
@@ -330,44 +343,51 @@ __global__ void __launch_bounds__(256) chunk_prep_tc_kernel(ChunkArgs p) {
         __syncthreads();
     }
 
-    // ---- 3. elementwise: qg, kg (in place), kb, kg^T and 2^G to the workspace;
-    // the previous chunk's k becomes its kg (rows 64..127 of sKB).
-    if (tid < KK) {
-        const float G = gam[63];
+    // ---- 3. elementwise, 8 channels of one row per thread; lanes 0..7 cover the
+    // 8 rows of a core matrix so every 16-byte tile access is conflict-free.
+    // qg, kg (in place), kb, scale * qg and kg to the workspace.
+    for (int idx = tid; idx < 64 * KG8; idx += 256) {
+        const int l = idx & 31, w = idx >> 5;
+        const int i = (w & 7) * 8 + (l & 7);
+        const int c = ((w >> 3) * 4 + (l >> 3)) * 8;
+        uint4 *pq = reinterpret_cast<uint4 *>(sAG + tile_off(i, c, KK));
+        uint4 *pk = reinterpret_cast<uint4 *>(sAG + tile_off(64 + i, c, KK));
+        float fq[8], fk[8], gam[8];
+        unpack8(*pq, fq);
+        unpack8(*pk, fk);
+        *reinterpret_cast<float4 *>(gam) = *reinterpret_cast<const float4 *>(sG2 + i * kGS + c);
+        *reinterpret_cast<float4 *>(gam + 4) = *reinterpret_cast<const float4 *>(sG2 + i * kGS + c + 4);
+        float qg[8], kgm[8], kb[8], kgv[8], qs[8];
 #pragma unroll
-        for (int i8 = 0; i8 < 64; i8 += 8) {
-            float kgv[8];
-#pragma unroll
-            for (int t = 0; t < 8; ++t) {
-                const int i = i8 + t;
-                __nv_bfloat16 *pq = reinterpret_cast<__nv_bfloat16 *>(sAG + tile_off(i, tid, KK));
-                __nv_bfloat16 *pk = reinterpret_cast<__nv_bfloat16 *>(sAG + tile_off(64 + i, tid, KK));
-                const float e = exp2f(gam[i]);
-                const float qv = __bfloat162float(*pq), kv = __bfloat162float(*pk);
-                *pq = __float2bfloat16_rn(qv * e);
-                *pk = __float2bfloat16_rn(kv * e);
-                if (fast)
-                    *reinterpret_cast<__nv_bfloat16 *>(sKB + tile_off(i, tid, KK)) =
-                        __float2bfloat16_rn(kv * exp2f(-gam[i]));
-                kgv[t] = kv * exp2f(G - gam[i]);
+        for (int j = 0; j < 8; ++j) {
+            const float e = exp2f(gam[j]);
+            qg[j] = fq[j] * e;
+            kgm[j] = fk[j] * e;
+            qs[j] = p.scale * qg[j];
+            if (fast) {
+                kb[j] = fk[j] * exp2f(-gam[j]);
+                kgv[j] = kb[j] * sEG[c + j];
+            } else {
+                kgv[j] = fk[j] * exp2f(sGv[c + j] - gam[j]);
             }
-            *reinterpret_cast<uint4 *>(U + Lo.kgt + tile_off(tid, i8, 64)) = pack8_at(kgv);
         }
-        reinterpret_cast<float *>(U + Lo.dec)[tid] = exp2f(G);
-    } else if (tid >= 128 && own) {
-#pragma unroll
-        for (int j = 0; j < 64; ++j) {
-            __nv_bfloat16 *pk = reinterpret_cast<__nv_bfloat16 *>(sKB + tile_off(64 + j, d, KK));
-            *pk = __float2bfloat16_rn(__bfloat162float(*pk) * gam[j]);
-        }
+        *pq = pack8(qg);
+        *pk = pack8(kgm);
+        if (fast) *reinterpret_cast<uint4 *>(sKB + tile_off(i, c, KK)) = pack8(kb);
+        *reinterpret_cast<uint4 *>(U + Lo.aw + tile_off(64 + i, c, KK)) = pack8(qs);
+        *reinterpret_cast<uint4 *>(U + Lo.kgt + tile_off(i, c, KK)) = pack8(kgv);
     }
-    if (tid >= KK && tid < 128) reinterpret_cast<float *>(U + Lo.dec)[tid] = 0.f;
-    if (KK < 128) {  // zero rows dk..127 of kg^T
-        for (int idx = tid; idx < (128 - KK) * 8; idx += 256) {
-            const int dd = KK + idx / 8, c = (idx % 8) * 8;
-            *reinterpret_cast<uint4 *>(U + Lo.kgt + tile_off(dd, c, 64)) = make_uint4(0, 0, 0, 0);
-        }
+    __syncthreads();
+    // v into the freed g2 buffer; waited for just before the u MMA
+    for (int idx = tid; idx < 64 * VG8; idx += 256) {
+        const int i = idx / VG8, c = (idx % VG8) * 8;
+        void *dv = sV + tile_off(i, c, VV);
+        if (i < nr)
+            cp_async16(dv, v + ((row0 + i) * p.HV + hv) * VV + c);
+        else
+            *reinterpret_cast<uint4 *>(dv) = make_uint4(0, 0, 0, 0);
     }
+    asm volatile("cp.async.commit_group;" ::: "memory");
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -375,7 +395,7 @@ __global__ void __launch_bounds__(256) chunk_prep_tc_kernel(ChunkArgs p) {
     const uint32_t tmem = tslot;
 
     // ---- 4. grams on the tensor cores.  D[:, 0:64] = [Qg; Kg] Kb^T (split grams),
-    // D[:, 64:128] = [Qg; Kg] kgp^T (cross-chunk gram of the previous chunk).
+    // D[:, 64:128] = [Qg; Kg] kgp^T (cross-chunk gram with the previous chunk).
     if (tid == 0) {
         const uint32_t id64 = idesc_bf16(128, 64, false, false);
         const uint64_t a = sdesc(smem_addr(sAG), 128, KK * 16);
@@ -385,15 +405,6 @@ __global__ void __launch_bounds__(256) chunk_prep_tc_kernel(ChunkArgs p) {
             mma_bf16_seq<KK / 16, false>(tmem + 64, a, 16,
                                          sdesc(smem_addr(sKB) + 64 * KK * 2, 128, KK * 16), 16, id64);
         mma_commit(&bar);
-    }
-    // qg * scale -> workspace (rows 64..127 of the [W; qg] tile) while the MMA runs
-    for (int idx = tid; idx < 64 * KG8; idx += 256) {
-        const int i = idx / KG8, c = (idx % KG8) * 8;
-        float f[8];
-        unpack8(*reinterpret_cast<const uint4 *>(sAG + tile_off(i, c, KK)), f);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) f[j] *= p.scale;
-        *reinterpret_cast<uint4 *>(U + Lo.aw + tile_off(64 + i, c, KK)) = pack8(f);
     }
     __syncwarp();
     uint32_t phase = 0;
@@ -433,8 +444,7 @@ __global__ void __launch_bounds__(256) chunk_prep_tc_kernel(ChunkArgs p) {
 
     // ---- 5. Akk = (I + L)^-1, blocked: diagonal 16 x 16 blocks by substitution,
     // then the off-diagonal blocks level by level: A_IJ = -A_II sum_M L_IM A_MJ.
-    for (int idx = tid; idx < 64 * 64; idx += 256) sA[idx] = 0.f;
-    __syncthreads();
+    // Only blocks on or below the diagonal are written; the rest is masked later.
     if (tid < 64) {
         const int I = tid >> 4, c = tid & 15, o = 16 * I;
         float x[16];
@@ -442,43 +452,54 @@ __global__ void __launch_bounds__(256) chunk_prep_tc_kernel(ChunkArgs p) {
         for (int r = 0; r < 16; ++r) x[r] = (r == c) ? 1.f : 0.f;
 #pragma unroll
         for (int r = 1; r < 16; ++r) {
-            float s = 0.f;
+            float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-            for (int m = 0; m < r; ++m) s = fmaf(sL[lidx(o + r, o + m)], x[m], s);
-            if (r > c) x[r] = -s;
+            for (int m = 0; m < r; m += 2) {
+                s0 = fmaf(sL[lidx(o + r, o + m)], x[m], s0);
+                if (m + 1 < r) s1 = fmaf(sL[lidx(o + r, o + m + 1)], x[m + 1], s1);
+            }
+            if (r > c) x[r] = -(s0 + s1);
         }
 #pragma unroll
         for (int r = 0; r < 16; ++r) sA[(o + r) * 64 + o + c] = x[r];
     }
     __syncthreads();
-    for (int lvl = 1; lvl < 4; ++lvl) {
-        const int nblk = 4 - lvl;
-        for (int e = tid; e < nblk * 256; e += 256) {
-            const int J = e >> 8, I = J + lvl, r = (e >> 4) & 15, c = e & 15;
-            float s = 0.f;
-            for (int M = J; M < I; ++M) {
+    {
+        const int r = (tid >> 4) & 15, c = tid & 15;
+#pragma unroll
+        for (int lvl = 1; lvl < 4; ++lvl) {
+#pragma unroll
+            for (int J = 0; J < 4 - lvl; ++J) {  // T_IJ = sum_{M=J}^{I-1} L_IM A_MJ
+                const int I = J + lvl;
+                float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int M = J; M < I; ++M) {
+#pragma unroll
+                    for (int m = 0; m < 16; ++m)
+                        s[m & 3] = fmaf(sL[lidx(16 * I + r, 16 * M + m)],
+                                        sA[(16 * M + m) * 64 + 16 * J + c], s[m & 3]);
+                }
+                sT[J * 256 + r * 16 + c] = (s[0] + s[1]) + (s[2] + s[3]);
+            }
+            __syncthreads();
+#pragma unroll
+            for (int J = 0; J < 4 - lvl; ++J) {  // A_IJ = -A_II T_IJ
+                const int I = J + lvl;
+                float s[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int m = 0; m < 16; ++m)
-                    s = fmaf(sL[lidx(16 * I + r, 16 * M + m)], sA[(16 * M + m) * 64 + 16 * J + c], s);
+                    s[m & 3] = fmaf(sA[(16 * I + r) * 64 + 16 * I + m], sT[J * 256 + m * 16 + c], s[m & 3]);
+                sA[(16 * I + r) * 64 + 16 * J + c] = -((s[0] + s[1]) + (s[2] + s[3]));
             }
-            sT[e] = s;
+            __syncthreads();
         }
-        __syncthreads();
-        for (int e = tid; e < nblk * 256; e += 256) {
-            const int J = e >> 8, I = J + lvl, r = (e >> 4) & 15, c = e & 15;
-            float s = 0.f;
-#pragma unroll
-            for (int m = 0; m < 16; ++m)
-                s = fmaf(sA[(16 * I + r) * 64 + 16 * I + m], sT[(J << 8) + m * 16 + c], s);
-            sA[(16 * I + r) * 64 + 16 * J + c] = -s;
-        }
-        __syncthreads();
     }
+    // Akk diag(beta) as a bf16 operand tile (Akk is lower triangular)
     for (int idx = tid; idx < 64 * 8; idx += 256) {
         const int i = idx >> 3, c = (idx & 7) * 8;
         float f[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) f[j] = sA[i * 64 + c + j] * sBeta[c + j];
+        for (int j = 0; j < 8; ++j) f[j] = (c + j <= i) ? sA[i * 64 + c + j] * sBeta[c + j] : 0.f;
         *reinterpret_cast<uint4 *>(sAB + tile_off(i, c, 64)) = pack8(f);
     }
     fence_async_smem();
@@ -523,6 +544,9 @@ __global__ void __launch_bounds__(256) chunk_prep_tc_kernel(ChunkArgs p) {
             }
         }
     }
+    // v has landed before anyone passes this barrier
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -569,8 +593,8 @@ __global__ void __launch_bounds__(256) chunk_prep_tc_kernel(ChunkArgs p) {
 template <int KK>
 struct ScanSmem {
     static constexpr uint32_t top = 0;                         // [128][KK]: W~_{c+1}; qg_c
-    static constexpr uint32_t kgt = top + 128 * KK * 2;        // [128][64]: kg_c^T
-    static constexpr uint32_t bot = kgt + 128 * 64 * 2;        // [128][64]: M_{c+1}; Aqk_c
+    static constexpr uint32_t kgt = top + 128 * KK * 2;        // [64][KK]: kg_c
+    static constexpr uint32_t bot = kgt + 64 * KK * 2;         // [128][64]: M_{c+1}; Aqk_c
     static constexpr uint32_t u = bot + 128 * 64 * 2;          // [kSBV/kUB][64][kUB] bf16: u_{c+1}
     static constexpr uint32_t dec = u + 64 * kSBV * 2;         // [128] fp32: 2^G_c
     static constexpr uint32_t stage = dec + 512;
@@ -663,7 +687,7 @@ __global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
                 const bool nxt = r < nc, cur = r >= 1;
                 uint32_t bytes = 0;
                 if (nxt) bytes += 64 * KK * 2 + 64 * kSBV * 2 + (cur ? 64 * 64 * 2 : 0);
-                if (cur) bytes += 64 * KK * 2 + 128 * 64 * 2 + 64 * 64 * 2 + 512;
+                if (cur) bytes += 64 * KK * 2 + 64 * KK * 2 + 64 * 64 * 2 + 512;
                 mbar_arrive_expect_tx(&full[s], bytes);
                 if (nxt) {
                     const unsigned char *U1 = units + ((gc0 + c + 1) * p.HV + hv) * (int64_t)Lo.stride;
@@ -676,7 +700,7 @@ __global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
                     const unsigned char *U0 = units + ((gc0 + c) * p.HV + hv) * (int64_t)Lo.stride;
                     bulk_g2s(st + S::top + 64 * KK * 2, U0 + Lo.aw + 64 * KK * 2, 64 * KK * 2,
                              &full[s]);
-                    bulk_g2s(st + S::kgt, U0 + Lo.kgt, 128 * 64 * 2, &full[s]);
+                    bulk_g2s(st + S::kgt, U0 + Lo.kgt, 64 * KK * 2, &full[s]);
                     bulk_g2s(st + S::bot + 64 * 64 * 2, U0 + Lo.aqk, 64 * 64 * 2, &full[s]);
                     bulk_g2s(st + S::dec, U0 + Lo.dec, 512, &full[s]);
                 }
@@ -690,6 +714,7 @@ __global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
         // ----------------------------------------------------- MMA issuer
         if (lane == 0) {
             const uint32_t idn = idesc_bf16(128, kSBV, false, true);
+            const uint32_t idc = idesc_bf16(128, kSBV, true, true);  // A = kg tile read MN-major
             const uint32_t base = smem_addr(sm);
             const uint64_t dh = sdesc(smem_addr(sH), kSBV * 16, 128);
             const uint64_t dv = sdesc(smem_addr(sVp), kSBV * 16, 128);
@@ -713,8 +738,8 @@ __global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
                         break;
                     }
                     tc_fence_after();
-                    mma_bf16_seq<4, false>(tmem + 2 * kSBV, sdesc(st + S::kgt, 128, 1024), 16, dv,
-                                           binc, idn);
+                    mma_bf16_seq<4, false>(tmem + 2 * kSBV, sdesc(st + S::kgt, KK * 16, 128),
+                                           2 * KK * 16 / 16, dv, binc, idc);
                     mma_commit(&bar_h);
                     mma_bf16_seq<4, true>(d1, sdesc(st + S::bot, 128, 1024), 16, dv, binc, idn);
                 }
