@@ -54,6 +54,24 @@ def _peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
 
 
+# ------------------------------------------------------------------ ranks
+def max_over_ranks(x, dist=None, device="cpu"):
+    """The largest of each rank's x (the job is as slow as its slowest rank)."""
+    if dist is None:
+        return float(x)
+    import torch
+
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world, tokens_per_rank, ms):
+    """Whole-job tokens/s: every rank processes its own replica of the workload
+    (weak scaling), all in `ms` milliseconds (the max over ranks)."""
+    return world * tokens_per_rank / (ms / 1e3)
+
+
 # ------------------------------------------------------------------ bytes
 def _nbytes(t):
     return 0 if t is None else t.numel() * t.element_size()
@@ -308,13 +326,10 @@ def run_ours(args):
     if dist:
         dist.barrier()
     clocks = sampler.stop(t_wall0, t_wall1) if sampler else None
-    ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / args.steps
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / args.steps, dist,
+                        dev)
     tokens = inp["tokens"]
-    value = world * tokens / (ms / 1e3)
+    value = job_throughput(world, tokens, ms)
 
     # Per-kernel durations, live, with CUDA events on the launching stream.
     prof_steps = min(args.steps, 50)
@@ -363,12 +378,8 @@ def run_ours(args):
         e2e_step()
     e_e.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = e_s.elapsed_time(e_e) / e2e_steps
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * tokens / (e2e_ms / 1e3)
+    e2e_ms = max_over_ranks(e_s.elapsed_time(e_e) / e2e_steps, dist, dev)
+    e2e_value = job_throughput(world, tokens, e2e_ms)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -381,8 +392,8 @@ def run_ours(args):
         dist.destroy_process_group()
     if rank != 0:
         return 0
-    compute_dtype = "bf16" if any(n.startswith(("chunk_fused", "chunk_tc")) for n in per_kernel) \
-        else "f32"
+    # bf16 operands with fp32 accumulation on the tensor-core path; fp32 on the SIMT path
+    compute_dtype = "bf16" if any(n.endswith("_tc") for n in per_kernel) else "f32"
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
