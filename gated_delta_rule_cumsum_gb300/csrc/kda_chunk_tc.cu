@@ -15,8 +15,8 @@
 //                 one exp2 per (i, j, d), exponent g2_i - g2_j <= 0 (ALGORITHM.md,
 //                 "The numerics law").
 //                 Akk = (I + L)^-1: blocked unit-lower-triangular inverse in fp32
-//                 (16 x 16 diagonal blocks by substitution, off-diagonal blocks
-//                 level by level).
+//                 (16 x 16 diagonal blocks by substitution, then two doubling
+//                 steps to 32 x 32 and 64 x 64).
 //                 w = Akk diag(beta) Kg,  u = Akk diag(beta) v    (tcgen05, N = dk / dv)
 //                 kg = k 2^(G - g2),  qg = scale q 2^g2,  decay = 2^G
 //     The results go to the workspace as ready-made MMA operand tiles.
@@ -123,30 +123,77 @@ __device__ __forceinline__ uint4 pack8_at(const float *f) {
 template <int KK, int VV>
 struct PrepSmem {
     static constexpr int kGS = KK + 4;                          // padded fp32 row of g2
-    static constexpr uint32_t tile = 128 * KK * 2;
-    static constexpr uint32_t ag = 0;                           // [128][KK]: q->qg, k->kg; Akk (fp32) later
-    static constexpr uint32_t kbx = ag + tile;                  // [128][KK]: kb; kg of the previous chunk
-    static constexpr uint32_t g = kbx + tile;                   // fp32 [64][kGS] g2; later v tile + AB tile
+    // The kb / previous-kg tile is K-major with its core matrices 144 bytes apart
+    // along K (16 bytes of padding each): the halo threads' per-channel writes
+    // then fall in distinct banks.
+    static constexpr uint32_t kLbo = 144;
+    static constexpr uint32_t kSbo = (KK / 8) * kLbo;
+    static constexpr uint32_t ag = 0;                           // [128][KK]: q->qg, k->kg
+    static constexpr uint32_t kbx = ag + 128 * KK * 2;          // [128][KK] padded: kb; kg of the previous chunk
+    static constexpr uint32_t g = kbx + 16 * kSbo;              // fp32 [64][kGS] g2; later v tile + AB tile
     static constexpr uint32_t g_need0 = 64 * kGS * 4;
     static constexpr uint32_t g_need1 = 64 * VV * 2 + 64 * 64 * 2;
     static constexpr uint32_t g_bytes = g_need0 > g_need1 ? g_need0 : g_need1;
-    static constexpr uint32_t extra = g + g_bytes;              // dk = 64 only: L, scratch, P, Akk
+    static constexpr uint32_t extra = g + g_bytes;
+    // After the gram MMA: L fp32 [64][64], T fp32 [32][32], P bf16 tile [64][64],
+    // Akk fp32 [64][64].  dk = 128 reuses the kb tile and the qg rows for them.
     static constexpr bool big = KK == 128;
-    static constexpr uint32_t lbuf = big ? kbx : extra;                       // L fp32 [64][64]
-    static constexpr uint32_t tbuf = lbuf + 64 * 64 * 4;                      // solve scratch 3 KB
-    static constexpr uint32_t pbuf = tbuf + 3072;                             // P tile [64][64] bf16
-    static constexpr uint32_t abuf = big ? ag : pbuf + 64 * 64 * 2;           // Akk fp32 [64][64]
+    static constexpr uint32_t lbuf = big ? kbx : extra;
+    static constexpr uint32_t tbuf = lbuf + 64 * 64 * 4;
+    static constexpr uint32_t pbuf = tbuf + 32 * 32 * 4;
+    static constexpr uint32_t abuf = big ? ag : pbuf + 64 * 64 * 2;
     static constexpr uint32_t used = big ? extra : abuf + 64 * 64 * 4;
+    static_assert(!big || pbuf + 64 * 64 * 2 <= g, "solve scratch overflows the kb tile");
     // Floor so that at most two CTAs (256 TMEM columns each) share an SM.
     static constexpr uint32_t total = used > 80 * 1024 ? used : 80 * 1024;
 };
 
-// L (fp32 64 x 64) with an XOR swizzle: row-per-lane writes and the solve's
-// broadcast reads both stay free of bank conflicts.
-__device__ __forceinline__ int lidx(int i, int j) { return i * 64 + (j ^ (i & 31)); }
+// Byte offset of element (r, c) in the padded kb tile.
+template <int KK>
+__device__ __forceinline__ uint32_t kbx_off(int r, int c) {
+    return (uint32_t)((r >> 3) * PrepSmem<KK, 32>::kSbo + (c >> 3) * PrepSmem<KK, 32>::kLbo +
+                      (r & 7) * 16 + (c & 7) * 2);
+}
+
+// fp32 [rows][W] with the 16-byte column group XORed by (row & 7): eight
+// consecutive rows at the same columns fall in distinct banks.
+template <int W>
+__device__ __forceinline__ int fsw(int r, int c) {
+    return r * W + ((((c >> 2) ^ r) & 7) | ((c >> 2) & ~7)) * 4 + (c & 3);
+}
+template <int W>
+__device__ __forceinline__ float4 ld4(const float *b, int r, int c) {
+    return *reinterpret_cast<const float4 *>(b + fsw<W>(r, c));
+}
+template <int W>
+__device__ __forceinline__ void st4(float *b, int r, int c, float4 v) {
+    *reinterpret_cast<float4 *>(b + fsw<W>(r, c)) = v;
+}
+__device__ __forceinline__ void fma4(float4 &s, float a, const float4 &x) {
+    s.x = fmaf(a, x.x, s.x);
+    s.y = fmaf(a, x.y, s.y);
+    s.z = fmaf(a, x.z, s.z);
+    s.w = fmaf(a, x.w, s.w);
+}
+
+// s += P[r][m] Q[m][c..c+3] over the 16 columns m of one 16 x 16 block of P
+// (rows pr, columns pc of a 64-wide buffer) and rows qr.. of Q (width QW).
+template <int QW>
+__device__ __forceinline__ void strip16(float4 &s, const float *P, int pr, int pc, const float *Q,
+                                        int qr, int qc) {
+#pragma unroll
+    for (int m4 = 0; m4 < 16; m4 += 4) {
+        const float4 a = ld4<64>(P, pr, pc + m4);
+        fma4(s, a.x, ld4<QW>(Q, qr + m4, qc));
+        fma4(s, a.y, ld4<QW>(Q, qr + m4 + 1, qc));
+        fma4(s, a.z, ld4<QW>(Q, qr + m4 + 2, qc));
+        fma4(s, a.w, ld4<QW>(Q, qr + m4 + 3, qc));
+    }
+}
+__device__ __forceinline__ float4 neg4(float4 v) { return make_float4(-v.x, -v.y, -v.z, -v.w); }
 
 template <int KK, int VV>
-__global__ void __launch_bounds__(256) chunk_prep_tc_kernel(ChunkArgs p) {
+__global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
     using S = PrepSmem<KK, VV>;
     extern __shared__ __align__(1024) unsigned char sm[];
     __shared__ float sBeta[64];
@@ -191,15 +238,19 @@ __global__ void __launch_bounds__(256) chunk_prep_tc_kernel(ChunkArgs p) {
     }
     __syncthreads();
 
-    // ---- 1. async loads: q, k (and the previous chunk's k) as operand tiles, g fp32
+    // ---- 1. async loads of q, k (and the previous chunk's k) as operand tiles;
+    // lanes 0..7 take the 8 rows of a core matrix (conflict-free 16-byte writes).
     const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(p.q);
     const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(p.k);
     const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(p.v);
     const __nv_bfloat16 *beta = static_cast<const __nv_bfloat16 *>(p.beta);
     const size_t row0 = (size_t)b * p.T + r0;
-    constexpr int KG8 = KK / 8, VG8 = VV / 8, KG4 = KK / 4;
-    for (int idx = tid; idx < 64 * KG8; idx += 256) {
-        const int i = idx / KG8, c = (idx % KG8) * 8;
+    constexpr int KG8 = KK / 8, VG8 = VV / 8;
+#pragma unroll
+    for (int it = 0; it < KK / 32; ++it) {
+        const int idx = tid + it * 256, l = idx & 31, w = idx >> 5;
+        const int i = (w & 7) * 8 + (l & 7);
+        const int c = ((w >> 3) * 4 + (l >> 3)) * 8;
         void *dq = sAG + tile_off(i, c, KK);
         void *dk = sAG + tile_off(64 + i, c, KK);
         if (i < nr) {
@@ -211,29 +262,41 @@ __global__ void __launch_bounds__(256) chunk_prep_tc_kernel(ChunkArgs p) {
             *reinterpret_cast<uint4 *>(dk) = make_uint4(0, 0, 0, 0);
         }
         if (halo)
-            cp_async16(sKB + tile_off(64 + i, c, KK), k + ((row0 - 64 + i) * p.H + h) * KK + c);
-    }
-    for (int idx = tid; idx < 64 * KG4; idx += 256) {
-        const int i = idx / KG4, c = (idx % KG4) * 4;
-        float *dg = sG2 + i * kGS + c;
-        if (i < nr)
-            cp_async16(dg, p.g + ((row0 + i) * p.HV + hv) * KK + c);
-        else
-            *reinterpret_cast<float4 *>(dg) = make_float4(0.f, 0.f, 0.f, 0.f);
+            cp_async16(sKB + kbx_off<KK>(64 + i, c), k + ((row0 - 64 + i) * p.H + h) * KK + c);
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
     if (tid < 64) sBeta[tid] = tid < nr ? to_f32(beta[(row0 + tid) * p.HV + hv]) : 0.f;
 
-    // The previous chunk's gates in registers: thread 128 + d turns its channel d
-    // into eprev[j] = 2^(G' - g2'_j) and 2^G' (suffix sums over the full chunk).
+    // ---- 2. Stage 1 in registers: thread d < dk owns channel d of this chunk and
+    // forms g2 (rows past the end keep G); thread 128 + d turns channel d of the
+    // previous chunk into eprev[j] = 2^(G' - g2'_j) and 2^G'.
+    const size_t grs = (size_t)p.HV * KK;
     float eprev[64];
     const int dh = tid - 128;
     const bool halo_thread = halo && tid >= 128 && dh < KK;
-    if (halo_thread) {
-        const float *gp = p.g + ((row0 - 64) * p.HV + hv) * KK + dh;
-        const size_t rs = (size_t)p.HV * KK;
+    if (tid < KK) {
+        const float *gp = p.g + (row0 * p.HV + hv) * KK + tid;
+        float gr[64];
 #pragma unroll
-        for (int j = 0; j < 64; ++j) eprev[j] = __ldg(gp + j * rs);
+        for (int j = 0; j < 64; ++j) gr[j] = __ldg(gp + (j < nr ? j : nr - 1) * grs);
+        float acc = 0.f, rng = 0.f;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+            if (i < nr) acc = p.g_is_cumsum ? gr[i] : fmaf(p.g_scale, gr[i], acc);
+            sG2[i * kGS + tid] = acc;
+            rng = fmaxf(rng, fabsf(acc));
+        }
+        const float eG = exp2f(acc);
+        sEG[tid] = eG;
+        sGv[tid] = acc;
+        reinterpret_cast<float *>(U + Lo.dec)[tid] = eG;
+        atomicMax(&sRangeBits, __float_as_int(rng));
+    } else if (tid < 128) {
+        reinterpret_cast<float *>(U + Lo.dec)[tid] = 0.f;
+    } else if (halo_thread) {
+        const float *gp = p.g + ((row0 - 64) * p.HV + hv) * KK + dh;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) eprev[j] = __ldg(gp + j * grs);
         float Gp;
         if (p.g_is_cumsum) {
             Gp = eprev[63];
@@ -256,55 +319,31 @@ __global__ void __launch_bounds__(256) chunk_prep_tc_kernel(ChunkArgs p) {
 
     // ---- optional L2 normalisation of q, k and the previous chunk's k rows
     if (p.l2norm) {
-        unsigned char *tileb = tid < 128 ? sAG : sKB;
-        const int row = tid < 128 ? tid : tid - 64;  // threads 128..191: rows 64..127 of sKB
+        const bool own = tid >= 128;
+        const int row = own ? tid - 64 : tid;  // threads 128..191: rows 64..127 of the kb tile
         if (tid < 128 || (halo && row < 128)) {
+            auto at = [&](int c) -> uint4 * {
+                return reinterpret_cast<uint4 *>(own ? sKB + kbx_off<KK>(row, c)
+                                                     : sAG + tile_off(row, c, KK));
+            };
             float ss = 0.f;
             for (int c = 0; c < KK; c += 8) {
                 float f[8];
-                unpack8(*reinterpret_cast<const uint4 *>(tileb + tile_off(row, c, KK)), f);
+                unpack8(*at(c), f);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) ss = fmaf(f[j], f[j], ss);
             }
             const float rsn = 1.f / sqrtf(ss + 1e-6f);
             for (int c = 0; c < KK; c += 8) {
-                uint4 *ptr = reinterpret_cast<uint4 *>(tileb + tile_off(row, c, KK));
                 float f[8];
-                unpack8(*ptr, f);
+                unpack8(*at(c), f);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) f[j] *= rsn;
-                *ptr = pack8(f);
+                *at(c) = pack8(f);
             }
         }
         __syncthreads();
     }
-
-    // ---- 2. Stage 1 cumsum in place (thread d owns channel d); the previous
-    // chunk's k becomes its kg on the halo threads meanwhile.
-    if (tid < KK) {
-        float acc = 0.f, rng = 0.f;
-#pragma unroll
-        for (int i = 0; i < 64; ++i) {
-            const float gv = sG2[i * kGS + tid];
-            if (i < nr) acc = p.g_is_cumsum ? gv : fmaf(p.g_scale, gv, acc);
-            sG2[i * kGS + tid] = acc;  // rows past the end keep G
-            rng = fmaxf(rng, fabsf(acc));
-        }
-        const float eG = exp2f(acc);
-        sEG[tid] = eG;
-        sGv[tid] = acc;
-        reinterpret_cast<float *>(U + Lo.dec)[tid] = eG;
-        atomicMax(&sRangeBits, __float_as_int(rng));
-    } else if (tid < 128) {
-        reinterpret_cast<float *>(U + Lo.dec)[tid] = 0.f;
-    } else if (halo_thread) {
-#pragma unroll
-        for (int j = 0; j < 64; ++j) {
-            __nv_bfloat16 *pk = reinterpret_cast<__nv_bfloat16 *>(sKB + tile_off(64 + j, dh, KK));
-            *pk = __float2bfloat16_rn(__bfloat162float(*pk) * eprev[j]);
-        }
-    }
-    __syncthreads();
     const bool fast = __int_as_float(sRangeBits) <= kSafeRange;
 
     // ---- exact grams for chunks whose gate range is too wide to split
@@ -331,23 +370,33 @@ __global__ void __launch_bounds__(256) chunk_prep_tc_kernel(ChunkArgs p) {
                 if (lane == 0) {
                     *reinterpret_cast<__nv_bfloat16 *>(U + Lo.aqk + tile_off(i, j, 64)) =
                         __float2bfloat16_rn(p.scale * aq);
-                    sL[lidx(i, j)] = (i > j) ? sBeta[i] * ak : 0.f;
+                    sL[fsw<64>(i, j)] = (i > j) ? sBeta[i] * ak : 0.f;
                 }
             }
             for (int j = i + 1 + lane; j < 64; j += 32) {
                 *reinterpret_cast<__nv_bfloat16 *>(U + Lo.aqk + tile_off(i, j, 64)) =
                     __float2bfloat16_rn(0.f);
-                sL[lidx(i, j)] = 0.f;
+                sL[fsw<64>(i, j)] = 0.f;
             }
         }
         __syncthreads();
     }
 
+    // The previous chunk's k becomes its kg (one channel per halo thread).
+    if (halo_thread) {
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+            __nv_bfloat16 *pk = reinterpret_cast<__nv_bfloat16 *>(sKB + kbx_off<KK>(64 + j, dh));
+            *pk = __float2bfloat16_rn(__bfloat162float(*pk) * eprev[j]);
+        }
+    }
+
     // ---- 3. elementwise, 8 channels of one row per thread; lanes 0..7 cover the
     // 8 rows of a core matrix so every 16-byte tile access is conflict-free.
     // qg, kg (in place), kb, scale * qg and kg to the workspace.
-    for (int idx = tid; idx < 64 * KG8; idx += 256) {
-        const int l = idx & 31, w = idx >> 5;
+#pragma unroll
+    for (int it = 0; it < KK / 32; ++it) {
+        const int idx = tid + it * 256, l = idx & 31, w = idx >> 5;
         const int i = (w & 7) * 8 + (l & 7);
         const int c = ((w >> 3) * 4 + (l >> 3)) * 8;
         uint4 *pq = reinterpret_cast<uint4 *>(sAG + tile_off(i, c, KK));
@@ -373,14 +422,16 @@ __global__ void __launch_bounds__(256) chunk_prep_tc_kernel(ChunkArgs p) {
         }
         *pq = pack8(qg);
         *pk = pack8(kgm);
-        if (fast) *reinterpret_cast<uint4 *>(sKB + tile_off(i, c, KK)) = pack8(kb);
+        if (fast) *reinterpret_cast<uint4 *>(sKB + kbx_off<KK>(i, c)) = pack8(kb);
         *reinterpret_cast<uint4 *>(U + Lo.aw + tile_off(64 + i, c, KK)) = pack8(qs);
         *reinterpret_cast<uint4 *>(U + Lo.kgt + tile_off(i, c, KK)) = pack8(kgv);
     }
     __syncthreads();
     // v into the freed g2 buffer; waited for just before the u MMA
     for (int idx = tid; idx < 64 * VG8; idx += 256) {
-        const int i = idx / VG8, c = (idx % VG8) * 8;
+        const int l = idx & 31, w = idx >> 5;
+        const int i = (w & 7) * 8 + (l & 7);
+        const int c = ((w >> 3) * 4 + (l >> 3)) * 8;
         void *dv = sV + tile_off(i, c, VV);
         if (i < nr)
             cp_async16(dv, v + ((row0 + i) * p.HV + hv) * VV + c);
@@ -395,15 +446,21 @@ __global__ void __launch_bounds__(256) chunk_prep_tc_kernel(ChunkArgs p) {
     const uint32_t tmem = tslot;
 
     // ---- 4. grams on the tensor cores.  D[:, 0:64] = [Qg; Kg] Kb^T (split grams),
-    // D[:, 64:128] = [Qg; Kg] kgp^T (cross-chunk gram with the previous chunk).
+    // D[:, 64:128] = [Qg; Kg] kgp^T (cross-chunk gram with the previous chunk);
+    // Kb and kgp are rows 0..63 and 64..127 of one tile, so both take one MMA
+    // series of N = 128.
     if (tid == 0) {
-        const uint32_t id64 = idesc_bf16(128, 64, false, false);
         const uint64_t a = sdesc(smem_addr(sAG), 128, KK * 16);
-        if (fast)
-            mma_bf16_seq<KK / 16, false>(tmem, a, 16, sdesc(smem_addr(sKB), 128, KK * 16), 16, id64);
-        if (halo)
+        const uint64_t bkb = sdesc(smem_addr(sKB), S::kLbo, S::kSbo);
+        constexpr uint32_t binc = 2 * S::kLbo / 16;
+        if (fast && halo)
+            mma_bf16_seq<KK / 16, false>(tmem, a, 16, bkb, binc, idesc_bf16(128, 128, false, false));
+        else if (fast)
+            mma_bf16_seq<KK / 16, false>(tmem, a, 16, bkb, binc, idesc_bf16(128, 64, false, false));
+        else if (halo)
             mma_bf16_seq<KK / 16, false>(tmem + 64, a, 16,
-                                         sdesc(smem_addr(sKB) + 64 * KK * 2, 128, KK * 16), 16, id64);
+                                         sdesc(smem_addr(sKB) + 8 * S::kSbo, S::kLbo, S::kSbo),
+                                         binc, idesc_bf16(128, 64, false, false));
         mma_commit(&bar);
     }
     __syncwarp();
@@ -414,36 +471,42 @@ __global__ void __launch_bounds__(256) chunk_prep_tc_kernel(ChunkArgs p) {
     {
         const int quad = warp & 3, i = (tid & 127) & 63;
         if (warp < 4 && fast) {  // Aqk (rows 0..63) and L (rows 64..127) from columns 0..63
-            for (int c0 = 0; c0 < 64; c0 += 16) {
-                float dd[16];
-                tmem_ld16(tmem_at(tmem, quad * 32, c0), dd);
-                if (tid < 64) {
-                    float a2[16];
+            float dd[64];
+            tmem_ld64(tmem_at(tmem, quad * 32, 0), dd);
+            if (tid < 64) {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) a2[j] = (c0 + j <= i) ? p.scale * dd[j] : 0.f;
-                    *reinterpret_cast<uint4 *>(U + Lo.aqk + tile_off(i, c0, 64)) = pack8_at(a2);
-                    *reinterpret_cast<uint4 *>(U + Lo.aqk + tile_off(i, c0 + 8, 64)) = pack8_at(a2 + 8);
-                } else {
+                for (int c0 = 0; c0 < 64; c0 += 8) {
+                    float a8[8];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        sL[lidx(i, c0 + j)] = (c0 + j < i) ? sBeta[i] * dd[j] : 0.f;
+                    for (int j = 0; j < 8; ++j) a8[j] = (c0 + j <= i) ? p.scale * dd[c0 + j] : 0.f;
+                    *reinterpret_cast<uint4 *>(U + Lo.aqk + tile_off(i, c0, 64)) = pack8(a8);
                 }
+            } else {
+                const float bi = sBeta[i];
+#pragma unroll
+                for (int c0 = 0; c0 < 64; c0 += 4)
+                    st4<64>(sL, i, c0,
+                            make_float4(c0 < i ? bi * dd[c0] : 0.f, c0 + 1 < i ? bi * dd[c0 + 1] : 0.f,
+                                        c0 + 2 < i ? bi * dd[c0 + 2] : 0.f,
+                                        c0 + 3 < i ? bi * dd[c0 + 3] : 0.f));
             }
         }
         if (warp >= 6 && halo) {  // P = kg_c kgp^T from rows 64..127, columns 64..127
-            for (int c0 = 0; c0 < 64; c0 += 16) {
-                float dd[16];
-                tmem_ld16(tmem_at(tmem, quad * 32, 64 + c0), dd);
-                *reinterpret_cast<uint4 *>(sPB + tile_off(i, c0, 64)) = pack8_at(dd);
-                *reinterpret_cast<uint4 *>(sPB + tile_off(i, c0 + 8, 64)) = pack8_at(dd + 8);
-            }
+            float dd[64];
+            tmem_ld64(tmem_at(tmem, quad * 32, 64), dd);
+#pragma unroll
+            for (int c0 = 0; c0 < 64; c0 += 8)
+                *reinterpret_cast<uint4 *>(sPB + tile_off(i, c0, 64)) = pack8_at(dd + c0);
         }
     }
     tc_fence_before();
     __syncthreads();
 
-    // ---- 5. Akk = (I + L)^-1, blocked: diagonal 16 x 16 blocks by substitution,
-    // then the off-diagonal blocks level by level: A_IJ = -A_II sum_M L_IM A_MJ.
+    // ---- 5. Akk = (I + L)^-1 in fp32.  The 16 x 16 diagonal blocks X_I by
+    // substitution, then two doubling steps: the 32 x 32 diagonal blocks
+    // (A_10 = -X_1 L_10 X_0, A_32 = -X_3 L_32 X_2), then the lower-left 32 x 32
+    // block -Y_1 L_[23][01] Y_0.  The products run as 1 x 4 strips per thread
+    // (row r = lane % 8 + 8 (t / 32), columns 4 (lane / 8) of a 16 x 16 block).
     // Only blocks on or below the diagonal are written; the rest is masked later.
     if (tid < 64) {
         const int I = tid >> 4, c = tid & 15, o = 16 * I;
@@ -454,52 +517,61 @@ __global__ void __launch_bounds__(256) chunk_prep_tc_kernel(ChunkArgs p) {
         for (int r = 1; r < 16; ++r) {
             float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-            for (int m = 0; m < r; m += 2) {
-                s0 = fmaf(sL[lidx(o + r, o + m)], x[m], s0);
-                if (m + 1 < r) s1 = fmaf(sL[lidx(o + r, o + m + 1)], x[m + 1], s1);
+            for (int m4 = 0; m4 < r; m4 += 4) {
+                const float4 l4 = ld4<64>(sL, o + r, o + m4);
+                s0 = fmaf(l4.x, x[m4], s0);
+                if (m4 + 1 < r) s1 = fmaf(l4.y, x[m4 + 1], s1);
+                if (m4 + 2 < r) s0 = fmaf(l4.z, x[m4 + 2], s0);
+                if (m4 + 3 < r) s1 = fmaf(l4.w, x[m4 + 3], s1);
             }
             if (r > c) x[r] = -(s0 + s1);
         }
 #pragma unroll
-        for (int r = 0; r < 16; ++r) sA[(o + r) * 64 + o + c] = x[r];
+        for (int r = 0; r < 16; ++r) sA[fsw<64>(o + r, o + c)] = x[r];
     }
     __syncthreads();
-    {
-        const int r = (tid >> 4) & 15, c = tid & 15;
-#pragma unroll
-        for (int lvl = 1; lvl < 4; ++lvl) {
-#pragma unroll
-            for (int J = 0; J < 4 - lvl; ++J) {  // T_IJ = sum_{M=J}^{I-1} L_IM A_MJ
-                const int I = J + lvl;
-                float s[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int M = J; M < I; ++M) {
-#pragma unroll
-                    for (int m = 0; m < 16; ++m)
-                        s[m & 3] = fmaf(sL[lidx(16 * I + r, 16 * M + m)],
-                                        sA[(16 * M + m) * 64 + 16 * J + c], s[m & 3]);
-                }
-                sT[J * 256 + r * 16 + c] = (s[0] + s[1]) + (s[2] + s[3]);
-            }
-            __syncthreads();
-#pragma unroll
-            for (int J = 0; J < 4 - lvl; ++J) {  // A_IJ = -A_II T_IJ
-                const int I = J + lvl;
-                float s[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int m = 0; m < 16; ++m)
-                    s[m & 3] = fmaf(sA[(16 * I + r) * 64 + 16 * I + m], sT[J * 256 + m * 16 + c], s[m & 3]);
-                sA[(16 * I + r) * 64 + 16 * J + c] = -((s[0] + s[1]) + (s[2] + s[3]));
-            }
-            __syncthreads();
-        }
+    const int sr = (lane & 7) + 8 * ((tid >> 5) & 1), sc = 4 * (lane >> 3), blk = tid >> 6;
+    if (tid < 128) {  // T = L_{I,I-1} X_{I-1} for I = 1, 3  -> sT block (blk, blk)
+        const int I = 2 * blk + 1;
+        float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+        strip16<64>(s, sL, 16 * I + sr, 16 * (I - 1), sA, 16 * (I - 1), 16 * (I - 1) + sc);
+        st4<32>(sT, 16 * blk + sr, 16 * blk + sc, s);
     }
+    __syncthreads();
+    if (tid < 128) {  // A_{I,I-1} = -X_I T
+        const int I = 2 * blk + 1;
+        float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+        strip16<32>(s, sA, 16 * I + sr, 16 * I, sT, 16 * blk, 16 * blk + sc);
+        st4<64>(sA, 16 * I + sr, 16 * (I - 1) + sc, neg4(s));
+    }
+    __syncthreads();
+    {  // T_IJ = sum_M L_IM Y0_MJ for I = 2, 3 and J = 0, 1  -> sT (I - 2, J)
+        const int I = 2 + (blk >> 1), J = blk & 1;
+        float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int M = J; M < 2; ++M)
+            strip16<64>(s, sL, 16 * I + sr, 16 * M, sA, 16 * M, 16 * J + sc);
+        st4<32>(sT, 16 * (I - 2) + sr, 16 * J + sc, s);
+    }
+    __syncthreads();
+    {  // A_IJ = -sum_M Y1_IM T_MJ
+        const int I = 2 + (blk >> 1), J = blk & 1;
+        float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int M = 2; M <= I; ++M)
+            strip16<32>(s, sA, 16 * I + sr, 16 * M, sT, 16 * (M - 2), 16 * J + sc);
+        st4<64>(sA, 16 * I + sr, 16 * J + sc, neg4(s));
+    }
+    __syncthreads();
     // Akk diag(beta) as a bf16 operand tile (Akk is lower triangular)
-    for (int idx = tid; idx < 64 * 8; idx += 256) {
-        const int i = idx >> 3, c = (idx & 7) * 8;
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {
+        const int idx = tid + it * 256, l = idx & 31, w = idx >> 5;
+        const int i = (w & 7) * 8 + (l & 7);
+        const int c = ((w >> 3) * 4 + (l >> 3)) * 8;
+        const float4 a0 = ld4<64>(sA, i, c), a1 = ld4<64>(sA, i, c + 4);
+        const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
         float f[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) f[j] = (c + j <= i) ? sA[i * 64 + c + j] * sBeta[c + j] : 0.f;
+        for (int j = 0; j < 8; ++j) f[j] = (c + j <= i) ? av[j] * sBeta[c + j] : 0.f;
         *reinterpret_cast<uint4 *>(sAB + tile_off(i, c, 64)) = pack8(f);
     }
     fence_async_smem();
@@ -524,24 +596,25 @@ __global__ void __launch_bounds__(256) chunk_prep_tc_kernel(ChunkArgs p) {
     {
         const int quad = warp & 3, i = (tid & 127) - 64;
         if (warp == 2 || warp == 3) {  // W~ = W Diag(2^G_prev) -> rows 0..63 of the [W; qg] tile
-            for (int c0 = 0; c0 < KK; c0 += 16) {
-                float dd[16];
-                tmem_ld16(tmem_at(tmem, quad * 32, c0), dd);
+#pragma unroll
+            for (int c0 = 0; c0 < KK; c0 += 64) {
+                float dd[64];
+                tmem_ld64(tmem_at(tmem, quad * 32, c0), dd);
                 if (halo) {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) dd[j] *= sDprev[c0 + j];
+                    for (int j = 0; j < 64; ++j) dd[j] *= sDprev[c0 + j];
                 }
-                *reinterpret_cast<uint4 *>(U + Lo.aw + tile_off(i, c0, KK)) = pack8_at(dd);
-                *reinterpret_cast<uint4 *>(U + Lo.aw + tile_off(i, c0 + 8, KK)) = pack8_at(dd + 8);
+#pragma unroll
+                for (int c8 = 0; c8 < 64; c8 += 8)
+                    *reinterpret_cast<uint4 *>(U + Lo.aw + tile_off(i, c0 + c8, KK)) = pack8_at(dd + c8);
             }
         }
         if ((warp == 6 || warp == 7) && halo) {  // M
-            for (int c0 = 0; c0 < 64; c0 += 16) {
-                float dd[16];
-                tmem_ld16(tmem_at(tmem, quad * 32, KK + c0), dd);
-                *reinterpret_cast<uint4 *>(U + Lo.mt + tile_off(i, c0, 64)) = pack8_at(dd);
-                *reinterpret_cast<uint4 *>(U + Lo.mt + tile_off(i, c0 + 8, 64)) = pack8_at(dd + 8);
-            }
+            float dd[64];
+            tmem_ld64(tmem_at(tmem, quad * 32, KK), dd);
+#pragma unroll
+            for (int c8 = 0; c8 < 64; c8 += 8)
+                *reinterpret_cast<uint4 *>(U + Lo.mt + tile_off(i, c8, 64)) = pack8_at(dd + c8);
         }
     }
     // v has landed before anyone passes this barrier
