@@ -245,7 +245,7 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
     const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(p.v);
     const __nv_bfloat16 *beta = static_cast<const __nv_bfloat16 *>(p.beta);
     const size_t row0 = (size_t)b * p.T + r0;
-    constexpr int KG8 = KK / 8, VG8 = VV / 8;
+    constexpr int VG8 = VV / 8;
 #pragma unroll
     for (int it = 0; it < KK / 32; ++it) {
         const int idx = tid + it * 256, l = idx & 31, w = idx >> 5;
@@ -681,14 +681,41 @@ __device__ __forceinline__ int read_flag(const int *f) {
     return *reinterpret_cast<const volatile int *>(f);
 }
 
+// Hardware named barriers (ids 1 and 2; 0 is __syncthreads).  bar.arrive does
+// not block; bar.sync waits for the barrier's full thread count.  Whole warps
+// execute both (the instructions are warp-aligned).  A named barrier hands over
+// in a few tens of cycles, an mbarrier arrive -> wait in a few hundred.
+__device__ __forceinline__ void named_arrive(int id, int nthreads) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+// One lane of a converged warp (the same lane every time the warp is converged).
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
+constexpr int kBarH = 1;   // h_c written: the 4 h warps arrive, the MMA warp syncs
+constexpr int kBarV = 2;   // v'_c written and D1 read: v' and o warps arrive, the MMA warp syncs
+constexpr int kThrH = 128 + 32;
+constexpr int kThrV = 128 + 32;
+
+// Warp roles: 0..3 h (state rows 32 w .. 32 w + 31, all kSBV columns, in fp32
+// registers), 4..5 v' (rows 0..63 of D1), 6..7 o (rows 64..127 of D1), 8 bulk
+// copies, 9 MMA issue.  A warp reaches TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31.
 template <int KK>
 __global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
     using S = ScanSmem<KK>;
     extern __shared__ __align__(1024) unsigned char sm[];
     __shared__ uint64_t full[kStages], empty[kStages];
-    // bar_v[x]: MMAs writing D1[x] done (one per buffer: the o readers arrive on
-    // h_ready before they wait here, so a single barrier could be lapped).
-    __shared__ uint64_t bar_v[2], bar_h, h_ready, v_ready;
+    // bar_v[x]: MMAs writing D1[x] done, one per buffer.
+    __shared__ uint64_t bar_v[2], bar_h, bar_fin;
     __shared__ uint32_t tslot;
     __shared__ int abort_flag;
 
@@ -726,13 +753,12 @@ __global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1 + 256);
+            mbar_init(&empty[s], 1 + 6);  // MMA commit + the h and v' warps
         }
         mbar_init(&bar_v[0], 1);
         mbar_init(&bar_v[1], 1);
         mbar_init(&bar_h, 1);
-        mbar_init(&h_ready, 256);
-        mbar_init(&v_ready, 128);
+        mbar_init(&bar_fin, 1);
         mbar_fence_init();
         abort_flag = 0;
     }
@@ -742,6 +768,24 @@ __global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
     const uint32_t tmem = tslot;  // D1[0] at +0, D1[1] at +32, D2 at +64
     unsigned char *sH = sm + S::hs;
     unsigned char *sVp = sm + S::vp;
+    // A wait that runs out sets the abort flag.  From then on nobody waits for
+    // copies (full / empty) and the MMA warp issues no MMAs, but it still commits
+    // every round, and every role still takes part in every named barrier: the
+    // commits keep the epilogue in step with the MMA warp, so each named-barrier
+    // instance gathers exactly one arrival per warp, and the CTA runs through its
+    // rounds and exits.
+    auto fail = [&]() {
+        atomicExch(&abort_flag, 1);
+        report(p.status, KDA_DEVICE_TIMEOUT);
+    };
+    auto wait_copy = [&](uint64_t *bar, uint32_t parity) {
+        if (read_flag(&abort_flag)) return;
+        if (!mbar_wait(bar, parity, kWaitNs)) fail();
+    };
+    auto wait_mma = [&](uint64_t *bar, uint32_t parity) {
+        if (!mbar_wait(bar, parity, kWaitNs)) fail();
+    };
+    auto stage = [&](int r) { return sm + (r % kStages) * S::stage_stride; };
 
     if (warp == 8) {
         // ------------------------------------------------------- producer
@@ -749,13 +793,9 @@ __global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
             int issued = 0;
             for (int r = 0; r < R; ++r) {
                 const int s = r % kStages;
-                if (r >= kStages && !mbar_wait(&empty[s], ((r / kStages) - 1) & 1, kWaitNs)) {
-                    atomicExch(&abort_flag, 1);
-                    report(p.status, KDA_DEVICE_TIMEOUT);
-                    break;
-                }
+                if (r >= kStages) wait_copy(&empty[s], ((r / kStages) - 1) & 1);
                 if (read_flag(&abort_flag)) break;
-                unsigned char *st = sm + s * S::stage_stride;
+                unsigned char *st = stage(r);
                 const int c = r - 1;
                 const bool nxt = r < nc, cur = r >= 1;
                 uint32_t bytes = 0;
@@ -785,142 +825,183 @@ __global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
         }
     } else if (warp == 9) {
         // ----------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            const uint32_t idn = idesc_bf16(128, kSBV, false, true);
-            const uint32_t idc = idesc_bf16(128, kSBV, true, true);  // A = kg tile read MN-major
-            const uint32_t base = smem_addr(sm);
-            const uint64_t dh = sdesc(smem_addr(sH), kSBV * 16, 128);
-            const uint64_t dv = sdesc(smem_addr(sVp), kSBV * 16, 128);
-            constexpr uint32_t binc = 2 * kSBV * 16 / 16;
-            for (int r = 0; r < R; ++r) {
-                const int s = r % kStages;
-                const uint32_t st = base + s * S::stage_stride;
-                const uint32_t d1 = tmem + (r & 1) * kSBV;
-                if (!mbar_spin(&full[s], (r / kStages) & 1, kWaitNs) ||
-                    !mbar_spin(&h_ready, r & 1, kWaitNs)) {
-                    atomicExch(&abort_flag, 1);
-                    report(p.status, KDA_DEVICE_TIMEOUT);
-                    break;
-                }
+        const uint32_t idn = idesc_bf16(128, kSBV, false, true);
+        const uint32_t idc = idesc_bf16(128, kSBV, true, true);  // A = kg tile read MN-major
+        const uint64_t dh = sdesc(smem_addr(sH), kSBV * 16, 128);
+        const uint64_t dv = sdesc(smem_addr(sVp), kSBV * 16, 128);
+        constexpr uint32_t binc = 2 * kSBV * 16 / 16;
+        for (int r = 0; r < R; ++r) {
+            const int s = r % kStages;
+            const uint32_t st = smem_addr(stage(r));
+            const uint32_t d1 = tmem + (r & 1) * kSBV;
+            wait_copy(&full[s], (r / kStages) & 1);
+            __syncwarp();
+            named_sync(kBarH, kThrH);
+            const bool go = !read_flag(&abort_flag);
+            if (elect_one()) {
                 tc_fence_after();
-                mma_bf16_seq<KK / 16, false>(d1, sdesc(st + S::top, 128, KK * 16), 16, dh, binc, idn);
-                if (r >= 1) {
-                    if (!mbar_spin(&v_ready, (r - 1) & 1, kWaitNs)) {
-                        atomicExch(&abort_flag, 1);
-                        report(p.status, KDA_DEVICE_TIMEOUT);
-                        break;
-                    }
+                if (go)
+                    mma_bf16_seq<KK / 16, false>(d1, sdesc(st + S::top, 128, KK * 16), 16, dh, binc, idn);
+            }
+            __syncwarp();
+            if (r >= 1) {
+                named_sync(kBarV, kThrV);
+                if (elect_one()) {
                     tc_fence_after();
-                    mma_bf16_seq<4, false>(tmem + 2 * kSBV, sdesc(st + S::kgt, KK * 16, 128),
-                                           2 * KK * 16 / 16, dv, binc, idc);
+                    if (go)
+                        mma_bf16_seq<4, false>(tmem + 2 * kSBV, sdesc(st + S::kgt, KK * 16, 128),
+                                               2 * KK * 16 / 16, dv, binc, idc);
                     mma_commit(&bar_h);
-                    mma_bf16_seq<4, true>(d1, sdesc(st + S::bot, 128, 1024), 16, dv, binc, idn);
+                    if (go) mma_bf16_seq<4, true>(d1, sdesc(st + S::bot, 128, 1024), 16, dv, binc, idn);
                 }
+                __syncwarp();
+            }
+            if (elect_one()) {
                 mma_commit(&bar_v[r & 1]);
                 mma_commit(&empty[s]);
             }
+            __syncwarp();
         }
-    } else {
-        // ------- epilogue: warps 0..7; row = 32 (warp % 4) + lane, columns 16 (warp / 4) ..
-        const int quad = warp & 3, ch = warp >> 2;
-        const int row = quad * 32 + lane;
-        const int col0 = ch * 16;
+        // Every MMA issued has completed before the CTA frees its tensor memory.
+        if (elect_one()) {
+            mma_commit(&bar_fin);
+            mbar_wait(&bar_fin, 0, kWaitNs);
+        }
+        __syncwarp();
+    } else if (warp < 4) {
+        // ------------------------------------------------ h warps: the state
+        const int row = warp * 32 + lane;
         const bool has_row = row < KK;
-        const size_t scol = ((size_t)n * p.HV + hv) * (size_t)KK * p.V + (size_t)vb * kSBV + col0;
-        float hreg[16];
+        const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16) + 2 * kSBV;
+        const size_t srow = (((size_t)n * p.HV + hv) * KK + row) * (size_t)p.V + (size_t)vb * kSBV;
+        float h[kSBV];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) hreg[j] = 0.f;
+        for (int j = 0; j < kSBV; ++j) h[j] = 0.f;
         if (has_row && p.h0) {
-            const float4 *src = reinterpret_cast<const float4 *>(p.h0 + scol + (size_t)row * p.V);
+            const float4 *src = reinterpret_cast<const float4 *>(p.h0 + srow);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < kSBV / 4; ++j) {
                 const float4 x = src[j];
-                hreg[4 * j] = x.x; hreg[4 * j + 1] = x.y; hreg[4 * j + 2] = x.z; hreg[4 * j + 3] = x.w;
+                h[4 * j] = x.x; h[4 * j + 1] = x.y; h[4 * j + 2] = x.z; h[4 * j + 3] = x.w;
             }
         }
         auto write_h = [&]() {
             if (has_row) {
-                *reinterpret_cast<uint4 *>(sH + tile_off(row, col0, kSBV)) = pack8_at(hreg);
-                *reinterpret_cast<uint4 *>(sH + tile_off(row, col0 + 8, kSBV)) = pack8_at(hreg + 8);
+#pragma unroll
+                for (int c = 0; c < kSBV; c += 8)
+                    *reinterpret_cast<uint4 *>(sH + tile_off(row, c, kSBV)) = pack8_at(h + c);
             }
             fence_async_smem();
-            mbar_arrive(&h_ready);
+            __syncwarp();
+            named_arrive(kBarH, kThrH);
+        };
+        // 2^G of round r's finishing chunk, read one round ahead
+        auto fetch = [&](int r) {
+            float d = 1.f;
+            wait_copy(&full[r % kStages], (r / kStages) & 1);
+            if (r >= 1 && has_row) d = reinterpret_cast<const float *>(stage(r) + S::dec)[row];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[r % kStages]);
+            return d;
         };
         if (R > 0) write_h();
-        const uint32_t lanebase = (uint32_t)(quad * 32) << 16;
-        __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.o);
+        float dec = R > 0 ? fetch(0) : 1.f;
         for (int r = 0; r < R; ++r) {
-            const int s = r % kStages;
-            const unsigned char *st = sm + s * S::stage_stride;
             const bool nxt = r < nc;
-            if (!mbar_spin(&full[s], (r / kStages) & 1, kWaitNs)) atomicExch(&abort_flag, 1);
-            float uu[16];
-            float dec = 1.f;
-            if (quad < 2 && nxt) {
-                const unsigned char *ur = st + S::u + ((size_t)ch * 64 + row) * kUB * 2;
-                float f[8];
-                unpack8(*reinterpret_cast<const uint4 *>(ur), f);
-#pragma unroll
-                for (int t = 0; t < 8; ++t) uu[t] = f[t];
-                unpack8(*reinterpret_cast<const uint4 *>(ur + 16), f);
-#pragma unroll
-                for (int t = 0; t < 8; ++t) uu[8 + t] = f[t];
-            }
-            if (r >= 1 && has_row) dec = reinterpret_cast<const float *>(st + S::dec)[row];
-            mbar_arrive(&empty[s]);  // done reading the stage
             if (r >= 1) {
                 // h_{c+1} = Diag(2^G_c) h_c + D2  (bar_h also covers A_r's reads of h_c)
-                if (!mbar_spin(&bar_h, (r - 1) & 1, kWaitNs)) atomicExch(&abort_flag, 1);
+                wait_mma(&bar_h, (r - 1) & 1);
                 tc_fence_after();
-                float d[16];
-                tmem_ld16(tmem + lanebase + 2 * kSBV + col0, d);
+                float d[kSBV];
+                tmem_ld16(taddr, *reinterpret_cast<float(*)[16]>(d));
+                tmem_ld16(taddr + 16, *reinterpret_cast<float(*)[16]>(d + 16));
 #pragma unroll
-                for (int t = 0; t < 16; ++t) hreg[t] = fmaf(dec, hreg[t], d[t]);
+                for (int t = 0; t < kSBV; ++t) h[t] = fmaf(dec, h[t], d[t]);
                 tc_fence_before();
                 if (nxt) write_h();
             } else if (nxt) {
-                // Round 0 leaves h_0 in place.  Arrive only once round 0's MMA has
-                // completed: the MMA warp then has consumed the previous phase of
-                // h_ready, so this arrival cannot lap it.
-                if (!mbar_spin(&bar_v[0], 0, kWaitNs)) atomicExch(&abort_flag, 1);
-                mbar_arrive(&h_ready);
+                // Round 0 leaves h_0 in place.  Arrive for round 1 only once round 0's
+                // MMA has completed, i.e. after the MMA warp left this barrier's
+                // round-0 instance.
+                wait_mma(&bar_v[0], 0);
+                __syncwarp();
+                named_arrive(kBarH, kThrH);
             }
-            if (quad < 2 && nxt) {
-                // v'_{c+1} = u_{c+1} - D1[rows 0..63]
-                if (!mbar_spin(&bar_v[r & 1], (r >> 1) & 1, kWaitNs)) atomicExch(&abort_flag, 1);
-                tc_fence_after();
-                float d[16];
-                tmem_ld16(tmem + lanebase + (r & 1) * kSBV + col0, d);
-                tc_fence_before();
-#pragma unroll
-                for (int t = 0; t < 16; ++t) uu[t] -= d[t];
-                *reinterpret_cast<uint4 *>(sVp + tile_off(row, col0, kSBV)) = pack8_at(uu);
-                *reinterpret_cast<uint4 *>(sVp + tile_off(row, col0 + 8, kSBV)) = pack8_at(uu + 8);
-                fence_async_smem();
-                mbar_arrive(&v_ready);
-            }
-            if (quad >= 2 && r >= 1) {
-                // o_c = D1[rows 64..127]
-                if (!mbar_spin(&bar_v[r & 1], (r >> 1) & 1, kWaitNs)) atomicExch(&abort_flag, 1);
-                tc_fence_after();
-                float d[16];
-                tmem_ld16(tmem + lanebase + (r & 1) * kSBV + col0, d);
-                tc_fence_before();
-                const int orow = bos + (r - 1) * kBT + (row - 64);
-                if (orow < eos && !read_flag(&abort_flag)) {
-                    __nv_bfloat16 *op =
-                        o + (((size_t)b * p.T + orow) * p.HV + hv) * p.V + vb * kSBV + col0;
-                    *reinterpret_cast<uint4 *>(op) = pack8_at(d);
-                    *reinterpret_cast<uint4 *>(op + 8) = pack8_at(d + 8);
-                }
-            }
-            if (read_flag(&abort_flag)) break;
+            if (r + 1 < R) dec = fetch(r + 1);
         }
         if (p.ht && has_row && !read_flag(&abort_flag)) {
-            float4 *dst = reinterpret_cast<float4 *>(p.ht + scol + (size_t)row * p.V);
+            float4 *dst = reinterpret_cast<float4 *>(p.ht + srow);
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                dst[j] = make_float4(hreg[4 * j], hreg[4 * j + 1], hreg[4 * j + 2], hreg[4 * j + 3]);
+            for (int j = 0; j < kSBV / 4; ++j)
+                dst[j] = make_float4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
+        }
+    } else if (warp < 6) {
+        // ------------------------------------- v' warps: v'_{c+1} = u_{c+1} - D1[0:64]
+        const int row = (warp - 4) * 32 + lane;
+        const uint32_t lanebase = (uint32_t)((warp - 4) * 32) << 16;
+        float u[kSBV];
+        auto fetch = [&](int r) {
+            wait_copy(&full[r % kStages], (r / kStages) & 1);
+            if (r < nc) {
+#pragma unroll
+                for (int blk = 0; blk < kSBV / kUB; ++blk) {
+                    const unsigned char *ur = stage(r) + S::u + ((size_t)blk * 64 + row) * kUB * 2;
+                    float f[8];
+                    unpack8(*reinterpret_cast<const uint4 *>(ur), f);
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) u[blk * kUB + t] = f[t];
+                    unpack8(*reinterpret_cast<const uint4 *>(ur + 16), f);
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) u[blk * kUB + 8 + t] = f[t];
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[r % kStages]);
+        };
+        if (R > 0) fetch(0);
+        for (int r = 0; r < nc; ++r) {
+            wait_mma(&bar_v[r & 1], (r >> 1) & 1);
+            tc_fence_after();
+            float d[kSBV];
+            tmem_ld16(tmem + lanebase + (r & 1) * kSBV, *reinterpret_cast<float(*)[16]>(d));
+            tmem_ld16(tmem + lanebase + (r & 1) * kSBV + 16, *reinterpret_cast<float(*)[16]>(d + 16));
+            tc_fence_before();
+#pragma unroll
+            for (int t = 0; t < kSBV; ++t) d[t] = u[t] - d[t];
+#pragma unroll
+            for (int c = 0; c < kSBV; c += 8)
+                *reinterpret_cast<uint4 *>(sVp + tile_off(row, c, kSBV)) = pack8_at(d + c);
+            fence_async_smem();
+            __syncwarp();
+            named_arrive(kBarV, kThrV);
+            if (r + 1 < R) fetch(r + 1);
+        }
+    } else {
+        // --------------------------------------------- o warps: o_c = D1[64:128]
+        const int i = (warp - 6) * 32 + lane;  // row within the chunk
+        const uint32_t lanebase = (uint32_t)(64 + (warp - 6) * 32) << 16;
+        __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.o);
+        for (int r = 0; r < R; ++r) {
+            if (r >= 1) {
+                wait_mma(&bar_v[r & 1], (r >> 1) & 1);
+                tc_fence_after();
+                float d[kSBV];
+                tmem_ld16(tmem + lanebase + (r & 1) * kSBV, *reinterpret_cast<float(*)[16]>(d));
+                tmem_ld16(tmem + lanebase + (r & 1) * kSBV + 16, *reinterpret_cast<float(*)[16]>(d + 16));
+                tc_fence_before();
+                const int orow = bos + (r - 1) * kBT + i;
+                if (orow < eos && !read_flag(&abort_flag)) {
+                    __nv_bfloat16 *op = o + (((size_t)b * p.T + orow) * p.HV + hv) * p.V + vb * kSBV;
+#pragma unroll
+                    for (int c = 0; c < kSBV; c += 8)
+                        *reinterpret_cast<uint4 *>(op + c) = pack8_at(d + c);
+                }
+            }
+            // D1[r & 1] has been read: the MMA warp may overwrite it two rounds on.
+            if (r < nc) {
+                __syncwarp();
+                named_arrive(kBarV, kThrV);
+            }
         }
     }
     tc_fence_before();

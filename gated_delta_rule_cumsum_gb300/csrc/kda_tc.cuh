@@ -63,18 +63,6 @@ __device__ __forceinline__ uint32_t mbar_try_wait(uint64_t *bar, uint32_t parity
         : "memory");
     return ok;
 }
-// Non-blocking probe of the phase of the given parity.
-__device__ __forceinline__ uint32_t mbar_test_wait(uint64_t *bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_addr(bar)), "r"(parity)
-        : "memory");
-    return ok;
-}
 // Waits for the phase of the given parity to complete.  Gives up after
 // `limit_ns` of wall time and returns false, so no wait can hang the GPU.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
@@ -86,18 +74,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
     }
     return true;
 }
-// Latency-critical variant: spins on the non-blocking probe and checks the
-// clock every 256 probes.  Same time limit and result as mbar_wait.
-__device__ __forceinline__ bool mbar_spin(uint64_t *bar, uint32_t parity,
-                                          uint64_t limit_ns = 1000000000ull) {
-    if (mbar_test_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_test_wait(bar, parity)) return true;
-        if ((i & 255) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
-    }
-}
-
 // ------------------------------------------------------ bulk async copies
 // global -> shared, completion counted in bytes on `bar`.  16-byte aligned
 // addresses, size a multiple of 16.
