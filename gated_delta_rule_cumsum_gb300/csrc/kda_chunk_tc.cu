@@ -32,6 +32,8 @@
 #include "kda_internal.cuh"
 #include "kda_tc.cuh"
 
+#include <cuda_fp16.h>
+
 namespace kda {
 namespace {
 
@@ -204,13 +206,7 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
     __shared__ uint32_t tslot;
     __shared__ int sRangeBits;
 
-    const int64_t gc = blockIdx.x;
-    const int hv = blockIdx.y;
-    int b, r0, nr, cl;
-    if (!locate_chunk(p, gc, b, r0, nr, cl)) return;
-    const bool halo = cl > 0;  // the previous chunk of the same sequence exists
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int h = hv / (p.HV / p.H);
     constexpr uint32_t kCols = 256;
     constexpr int kGS = S::kGS;
 
@@ -225,8 +221,6 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
     float *sA = reinterpret_cast<float *>(sm + S::abuf);
 
     const TcLayout Lo = tc_layout(KK, VV);
-    unsigned char *U = static_cast<unsigned char *>(p.units) + (gc * p.HV + hv) * Lo.stride;
-
     if (warp == 0) {
         tmem_alloc(&tslot, kCols);
         tmem_relinquish();
@@ -236,7 +230,34 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
         mbar_fence_init();
         sRangeBits = 0;
     }
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tslot;
+    uint32_t phase = 0;
+
+    // Persistent: the CTA takes a contiguous range of units in (value head,
+    // chunk) order, so consecutive units are usually consecutive chunks of one
+    // head.  The previous chunk's kg tile and 2^G then stay in shared memory
+    // ("carry") instead of being re-derived from its k and g.
+    const int64_t total = (int64_t)p.HV * p.slots;
+    const int64_t per = (total + gridDim.x - 1) / gridDim.x;
+    const int64_t ubeg = (int64_t)blockIdx.x * per;
+    const int64_t uend = ubeg + per < total ? ubeg + per : total;
+    int prev_hv = -1;
+    int64_t prev_gc = -1;
+    for (int64_t unit = ubeg; unit < uend; ++unit) {
+    const int hv = (int)(unit / p.slots);
+    const int64_t gc = unit % p.slots;
+    int b, r0, nr, cl;
+    if (!locate_chunk(p, gc, b, r0, nr, cl)) {
+        prev_hv = -1;
+        continue;
+    }
+    const bool halo = cl > 0;  // the previous chunk of the same sequence exists
+    const bool carry = halo && prev_hv == hv && prev_gc == gc - 1;
+    const int h = hv / (p.HV / p.H);
+    unsigned char *U = static_cast<unsigned char *>(p.units) + (gc * p.HV + hv) * Lo.stride;
 
     // ---- 1. async loads of q, k (and the previous chunk's k) as operand tiles;
     // lanes 0..7 take the 8 rows of a core matrix (conflict-free 16-byte writes).
@@ -246,6 +267,9 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
     const __nv_bfloat16 *beta = static_cast<const __nv_bfloat16 *>(p.beta);
     const size_t row0 = (size_t)b * p.T + r0;
     constexpr int VG8 = VV / 8;
+    // beta in a register now, into shared memory after the gates: its load
+    // latency overlaps everything up to there
+    const float bet = (tid < 64 && tid < nr) ? to_f32(beta[(row0 + tid) * p.HV + hv]) : 0.f;
 #pragma unroll
     for (int it = 0; it < KK / 32; ++it) {
         const int idx = tid + it * 256, l = idx & 31, w = idx >> 5;
@@ -261,19 +285,21 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
             *reinterpret_cast<uint4 *>(dq) = make_uint4(0, 0, 0, 0);
             *reinterpret_cast<uint4 *>(dk) = make_uint4(0, 0, 0, 0);
         }
-        if (halo)
+        if (halo && !carry)
             cp_async16(sKB + kbx_off<KK>(64 + i, c), k + ((row0 - 64 + i) * p.H + h) * KK + c);
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
-    if (tid < 64) sBeta[tid] = tid < nr ? to_f32(beta[(row0 + tid) * p.HV + hv]) : 0.f;
 
     // ---- 2. Stage 1 in registers: thread d < dk owns channel d of this chunk and
     // forms g2 (rows past the end keep G); thread 128 + d turns channel d of the
-    // previous chunk into eprev[j] = 2^(G' - g2'_j) and 2^G'.
+    // previous chunk into eprev[j] = 2^(G' - g2'_j) and 2^G'.  eprev is held as
+    // fp16 pairs scaled by 2^-m, m the channel's largest exponent rounded up (0
+    // for decaying gates), so it cannot overflow and costs 32 registers.
     const size_t grs = (size_t)p.HV * KK;
-    float eprev[64];
+    __half2 eprev2[32];
+    float escale = 1.f;  // 2^m
     const int dh = tid - 128;
-    const bool halo_thread = halo && tid >= 128 && dh < KK;
+    const bool halo_thread = halo && !carry && tid >= 128 && dh < KK;
     if (tid < KK) {
         const float *gp = p.g + (row0 * p.HV + hv) * KK + tid;
         float gr[64];
@@ -295,25 +321,35 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
         reinterpret_cast<float *>(U + Lo.dec)[tid] = 0.f;
     } else if (halo_thread) {
         const float *gp = p.g + ((row0 - 64) * p.HV + hv) * KK + dh;
+        float ex[64];  // exponents G' - g2'_j
 #pragma unroll
-        for (int j = 0; j < 64; ++j) eprev[j] = __ldg(gp + j * grs);
+        for (int j = 0; j < 64; ++j) ex[j] = __ldg(gp + j * grs);
         float Gp;
         if (p.g_is_cumsum) {
-            Gp = eprev[63];
+            Gp = ex[63];
 #pragma unroll
-            for (int j = 0; j < 64; ++j) eprev[j] = exp2f(Gp - eprev[j]);
+            for (int j = 0; j < 64; ++j) ex[j] = Gp - ex[j];
         } else {
             float acc = 0.f;
 #pragma unroll
             for (int j = 63; j >= 0; --j) {
-                const float gj = eprev[j];
-                eprev[j] = exp2f(acc);
+                const float gj = ex[j];
+                ex[j] = acc;
                 acc = fmaf(p.g_scale, gj, acc);
             }
             Gp = acc;
         }
+        float mx = 0.f;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) mx = fmaxf(mx, ex[j]);
+        const float m = ceilf(mx);
+        escale = exp2f(m);
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            eprev2[j] = __floats2half2_rn(exp2f(ex[2 * j] - m), exp2f(ex[2 * j + 1] - m));
         sDprev[dh] = exp2f(Gp);
     }
+    if (tid < 64) sBeta[tid] = bet;
     asm volatile("cp.async.wait_group 0;" ::: "memory");
     __syncthreads();
 
@@ -321,7 +357,7 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
     if (p.l2norm) {
         const bool own = tid >= 128;
         const int row = own ? tid - 64 : tid;  // threads 128..191: rows 64..127 of the kb tile
-        if (tid < 128 || (halo && row < 128)) {
+        if (tid < 128 || (halo && !carry && row < 128)) {
             auto at = [&](int c) -> uint4 * {
                 return reinterpret_cast<uint4 *>(own ? sKB + kbx_off<KK>(row, c)
                                                      : sAG + tile_off(row, c, KK));
@@ -387,7 +423,8 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
 #pragma unroll
         for (int j = 0; j < 64; ++j) {
             __nv_bfloat16 *pk = reinterpret_cast<__nv_bfloat16 *>(sKB + kbx_off<KK>(64 + j, dh));
-            *pk = __float2bfloat16_rn(__bfloat162float(*pk) * eprev[j]);
+            const float ej = (j & 1) ? __high2float(eprev2[j >> 1]) : __low2float(eprev2[j >> 1]);
+            *pk = __float2bfloat16_rn(__bfloat162float(*pk) * (ej * escale));
         }
     }
 
@@ -443,7 +480,6 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = tslot;
 
     // ---- 4. grams on the tensor cores.  D[:, 0:64] = [Qg; Kg] Kb^T (split grams),
     // D[:, 64:128] = [Qg; Kg] kgp^T (cross-chunk gram with the previous chunk);
@@ -464,7 +500,6 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
         mma_commit(&bar);
     }
     __syncwarp();
-    uint32_t phase = 0;
     if (!mbar_wait(&bar, phase & 1, kWaitNs) && tid == 0) report(p.status, KDA_DEVICE_TIMEOUT);
     ++phase;
     tc_fence_after();
@@ -593,28 +628,48 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
     if (!mbar_wait(&bar, phase & 1, kWaitNs) && tid == 0) report(p.status, KDA_DEVICE_TIMEOUT);
     ++phase;
     tc_fence_after();
-    {
-        const int quad = warp & 3, i = (tid & 127) - 64;
-        if (warp == 2 || warp == 3) {  // W~ = W Diag(2^G_prev) -> rows 0..63 of the [W; qg] tile
+    // The kb / previous-kg tile is free now (P was read by the M MMA): if the next
+    // unit is the next chunk of this sequence, bring this chunk's kg into the
+    // previous-kg rows for it.
+    bool next_carry = false;
+    if (unit + 1 < uend) {
+        const int64_t un = unit + 1;
+        int bn, r0n, nrn, cln;
+        next_carry = (int)(un / p.slots) == hv && locate_chunk(p, un % p.slots, bn, r0n, nrn, cln) &&
+                     cln > 0;
+    }
+    if (next_carry) {
 #pragma unroll
-            for (int c0 = 0; c0 < KK; c0 += 64) {
-                float dd[64];
-                tmem_ld64(tmem_at(tmem, quad * 32, c0), dd);
-                if (halo) {
-#pragma unroll
-                    for (int j = 0; j < 64; ++j) dd[j] *= sDprev[c0 + j];
-                }
-#pragma unroll
-                for (int c8 = 0; c8 < 64; c8 += 8)
-                    *reinterpret_cast<uint4 *>(U + Lo.aw + tile_off(i, c0 + c8, KK)) = pack8_at(dd + c8);
-            }
+        for (int it = 0; it < KK / 32; ++it) {
+            const int idx = tid + it * 256, l = idx & 31, w = idx >> 5;
+            const int i = (w & 7) * 8 + (l & 7);
+            const int c = ((w >> 3) * 4 + (l >> 3)) * 8;
+            cp_async16(sKB + kbx_off<KK>(64 + i, c), U + Lo.kgt + tile_off(i, c, KK));
         }
-        if ((warp == 6 || warp == 7) && halo) {  // M
-            float dd[64];
-            tmem_ld64(tmem_at(tmem, quad * 32, KK), dd);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    }
+    if (warp == 2 || warp == 3 || warp == 6 || warp == 7) {
+        // W~ = W Diag(2^G_prev) -> rows 0..63 of the [W; qg] tile, and M; warps
+        // 2, 3 and 6, 7 reach the same TMEM lanes and take half the columns each.
+        const int quad = warp & 3, i = (tid & 127) - 64, half = warp >> 2;
 #pragma unroll
-            for (int c8 = 0; c8 < 64; c8 += 8)
-                *reinterpret_cast<uint4 *>(U + Lo.mt + tile_off(i, c8, 64)) = pack8_at(dd + c8);
+        for (int c0 = half * (KK / 2); c0 < (half + 1) * (KK / 2); c0 += 32) {
+            float dd[32];
+            tmem_ld32(tmem_at(tmem, quad * 32, c0), dd);
+            if (halo) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) dd[j] *= sDprev[c0 + j];
+            }
+#pragma unroll
+            for (int c8 = 0; c8 < 32; c8 += 8)
+                *reinterpret_cast<uint4 *>(U + Lo.aw + tile_off(i, c0 + c8, KK)) = pack8_at(dd + c8);
+        }
+        if (halo) {
+            float dd[32];
+            tmem_ld32(tmem_at(tmem, quad * 32, KK + half * 32), dd);
+#pragma unroll
+            for (int c8 = 0; c8 < 32; c8 += 8)
+                *reinterpret_cast<uint4 *>(U + Lo.mt + tile_off(i, half * 32 + c8, 64)) = pack8_at(dd + c8);
         }
     }
     // v has landed before anyone passes this barrier
@@ -624,6 +679,8 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
     __syncthreads();
     tc_fence_after();
 
+    if (tid < KK) sDprev[tid] = sEG[tid];  // the next chunk's 2^G_prev (read after this unit)
+
     // ---- 7. u = Akk diag(beta) v
     if (tid == 0) {
         mma_bf16_seq<4, false>(tmem, adesc, 16, sdesc(smem_addr(sV), VV * 16, 128),
@@ -632,6 +689,7 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
     }
     __syncwarp();
     if (!mbar_wait(&bar, phase & 1, kWaitNs) && tid == 0) report(p.status, KDA_DEVICE_TIMEOUT);
+    ++phase;
     tc_fence_after();
     if (warp == 2 || warp == 3 || warp == 6 || warp == 7) {
         const int quad = warp & 3, i = (tid & 127) - 64;
@@ -645,7 +703,12 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
         }
     }
     tc_fence_before();
+    if (tid == 0) sRangeBits = 0;
     __syncthreads();
+    tc_fence_after();
+    prev_hv = hv;
+    prev_gc = gc;
+    }  // unit loop
     if (warp == 0) tmem_dealloc(tmem, kCols);
 }
 
@@ -1016,10 +1079,33 @@ cudaError_t launch_prep(const ChunkArgs &a, cudaStream_t st) {
     if (!attr) {
         cudaError_t e = cudaFuncSetAttribute(chunk_prep_tc_kernel<KK, VV>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::total);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(chunk_prep_tc_kernel<KK, VV>,
+                                     cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     (int)cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    dim3 grid((unsigned)a.slots, a.HV);
+    static int ctas = 0;  // resident CTAs on the device
+    if (ctas == 0) {
+        // From the kernel's registers and shared memory (TMEM: 256 columns per
+        // CTA, at most two per SM).
+        int dev = 0, sms = 0, regs_sm = 0, smem_sm = 0;
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, chunk_prep_tc_kernel<KK, VV>);
+        if (e != cudaSuccess) return e;
+        const int by_regs = regs_sm / (((fa.numRegs + 7) / 8 * 8) * 256);
+        const int by_smem = smem_sm / (int)(S::total + fa.sharedSizeBytes + 1024);
+        int per_sm = by_regs < by_smem ? by_regs : by_smem;
+        per_sm = per_sm < 1 ? 1 : (per_sm > 2 ? 2 : per_sm);
+        ctas = sms * per_sm;
+    }
+    const int64_t units = a.slots * a.HV;
+    const unsigned grid = (unsigned)(units < ctas ? units : ctas);
     prof_begin("chunk_prep_tc", st);
     chunk_prep_tc_kernel<KK, VV><<<grid, 256, S::total, st>>>(a);
     prof_end(st);
