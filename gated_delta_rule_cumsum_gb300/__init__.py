@@ -21,6 +21,7 @@ import torch
 __all__ = [
     "KDA_OK", "KDA_ERR_INVALID_ARG", "KDA_ERR_UNSUPPORTED", "KDA_ERR_BAD_CU_SEQLENS",
     "KDA_ERR_CUDA", "KDA_ERR_TIMEOUT", "KDA_FLAG_QK_L2NORM", "KDA_FLAG_G_IS_CUMSUM",
+    "KDA_FLAG_SPLIT_SCAN",
     "KdaError", "KdaShape", "load", "library_path", "make_shape",
     "kda_gate_cumsum", "kda_chunk_fwd", "kda_recurrent_fwd", "kda_chunk_workspace_size",
     "kda_chunk_fwd_noalloc", "KDA_NOALLOC_SCRATCH_BYTES",
@@ -33,7 +34,7 @@ __all__ = [
 KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED = 0, 1, 2
 KDA_ERR_BAD_CU_SEQLENS, KDA_ERR_CUDA, KDA_ERR_TIMEOUT = 3, 4, 5
 KDA_DTYPE_F32, KDA_DTYPE_BF16 = 0, 1
-KDA_FLAG_QK_L2NORM, KDA_FLAG_G_IS_CUMSUM = 1 << 0, 1 << 1
+KDA_FLAG_QK_L2NORM, KDA_FLAG_G_IS_CUMSUM, KDA_FLAG_SPLIT_SCAN = 1 << 0, 1 << 1, 1 << 2
 KDA_DEVICE_BAD_CU_SEQLENS, KDA_DEVICE_TIMEOUT = 1 << 0, 1 << 1
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -247,11 +248,11 @@ def gate_cumsum(g, cu_seqlens=None, chunk_size: int = 64, g_scale: float = 1.0, 
 
 def chunk_kda(q, k, v, g, beta, scale=None, initial_state=None, output_final_state=False,
               cu_seqlens=None, use_qk_l2norm_in_kernel=False, g_scale=1.0, g_is_cumsum=False,
-              workspace=None, dev_status=None, stream=None):
+              split_scan=False, workspace=None, dev_status=None, stream=None):
     """Chunked forward; returns (o, ht or None).  `g` is the per-token log2 gate."""
     q, k, v, g, beta, h0, cu = _prep(q, k, v, g, beta, initial_state, cu_seqlens)
     flags = (KDA_FLAG_QK_L2NORM if use_qk_l2norm_in_kernel else 0) | (
-        KDA_FLAG_G_IS_CUMSUM if g_is_cumsum else 0)
+        KDA_FLAG_G_IS_CUMSUM if g_is_cumsum else 0) | (KDA_FLAG_SPLIT_SCAN if split_scan else 0)
     shape = make_shape(q, v, cu, scale, g_scale, flags)
     o = torch.empty(v.shape, dtype=q.dtype, device=q.device)
     ht = (torch.empty(shape.num_seqs, shape.HV, shape.K, shape.V, dtype=torch.float32,

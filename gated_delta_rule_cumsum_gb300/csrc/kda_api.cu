@@ -26,7 +26,7 @@ kda_status cuda_fail(cudaError_t e, const char *where) {
     return fail(KDA_ERR_CUDA, "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
 }
 
-constexpr uint32_t kKnownFlags = KDA_FLAG_QK_L2NORM | KDA_FLAG_G_IS_CUMSUM;
+constexpr uint32_t kKnownFlags = KDA_FLAG_QK_L2NORM | KDA_FLAG_G_IS_CUMSUM | KDA_FLAG_SPLIT_SCAN;
 
 // Checks shared by the three operations.  `need_h` also checks H and HV % H.
 kda_status check_common(const char *op, const kda_shape *s, const int32_t *cu) {
@@ -79,6 +79,8 @@ kda_status check_fwd_pointers(const char *op, const kda_shape *s, const void *q,
 struct ChunkWs {
     size_t ctrl, chunk_start, units, total, unit_bytes;
     int64_t slots;
+    bool split;
+    size_t qc, e0, e1, pm, e0b;  // split launches only
 };
 
 // The tensor-core path serves bf16 inputs whose K and V it supports; fp32
@@ -96,6 +98,18 @@ ChunkWs chunk_ws_layout(const kda_shape *s, bool packed) {
     L.chunk_start = 256;
     L.units = L.chunk_start + kda::align_up(sizeof(int32_t) * ((size_t)s->num_seqs + 1), 256);
     L.total = L.units + (size_t)L.slots * s->HV * L.unit_bytes;
+    L.split = (s->flags & KDA_FLAG_SPLIT_SCAN) && use_tc(s) &&
+              kda::chunk_tc_split(s->num_seqs, s->HV, s->K, s->V, s->T);
+    L.qc = L.e0 = L.e1 = L.pm = L.e0b = 0;
+    if (L.split) {
+        const size_t nh = (size_t)s->num_seqs * s->HV;
+        L.qc = kda::align_up(L.total, 256);
+        L.e0 = kda::align_up(L.qc + (size_t)L.slots * s->HV * 64 * s->K * 2, 256);
+        L.e1 = kda::align_up(L.e0 + nh * s->K * s->V * 4, 256);
+        L.pm = kda::align_up(L.e1 + nh * s->K * s->V * 4, 256);
+        L.e0b = kda::align_up(L.pm + nh * s->K * s->K * 4, 256);
+        L.total = L.e0b + nh * s->K * s->V * 2;
+    }
     return L;
 }
 
@@ -226,6 +240,12 @@ kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const floa
     a.chunk_start = reinterpret_cast<int32_t *>(ws + L.chunk_start);
     a.units = ws + L.units;
     a.slots = L.slots;
+    a.split = L.split ? 1 : 0;
+    a.qc = L.split ? ws + L.qc : nullptr;
+    a.e0 = L.split ? reinterpret_cast<float *>(ws + L.e0) : nullptr;
+    a.e1 = L.split ? reinterpret_cast<float *>(ws + L.e1) : nullptr;
+    a.pm = L.split ? reinterpret_cast<float *>(ws + L.pm) : nullptr;
+    a.e0b = L.split ? ws + L.e0b : nullptr;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e;

@@ -39,9 +39,7 @@ namespace {
 
 using namespace tc;
 
-constexpr int kSBV = 32;              // value columns per scan CTA
 constexpr int kUB = 16;               // column block of u in the workspace
-constexpr int kStages = 3;            // scan pipeline depth
 constexpr float kSafeRange = 60.f;    // max |g2| (log2) for the split grams
 constexpr uint64_t kWaitNs = 1000000000ull;
 
@@ -71,10 +69,12 @@ __host__ __device__ inline TcLayout tc_layout(int K, int V) {
     return L;
 }
 
-// Maps a chunk slot to its rows and its index within the sequence.  Returns
-// false for slots past the last chunk or when the offsets failed validation.
+// Maps a chunk slot to its rows and its index within the sequence (and, when
+// asked, the sequence and its chunk count).  Returns false for slots past the
+// last chunk or when the offsets failed validation.
 __device__ __forceinline__ bool locate_chunk(const ChunkArgs &p, int64_t gc, int &b, int &r0,
-                                             int &nr, int &cl) {
+                                             int &nr, int &cl, int *seq = nullptr,
+                                             int *seq_chunks = nullptr) {
     if (p.cu) {
         if (!p.ctrl->valid || gc >= p.ctrl->total_chunks) return false;
         const int n = upper_bound_minus_one(p.chunk_start, p.N + 1, (int)gc);
@@ -82,14 +82,24 @@ __device__ __forceinline__ bool locate_chunk(const ChunkArgs &p, int64_t gc, int
         b = 0;
         r0 = p.cu[n] + kBT * cl;
         nr = min(kBT, p.cu[n + 1] - r0);
+        if (seq) *seq = n;
+        if (seq_chunks) *seq_chunks = p.chunk_start[n + 1] - p.chunk_start[n];
     } else {
         const int ntc = (p.T + kBT - 1) / kBT;
         b = (int)(gc / ntc);
         cl = (int)(gc % ntc);
         r0 = cl * kBT;
         nr = min(kBT, p.T - r0);
+        if (seq) *seq = b;
+        if (seq_chunks) *seq_chunks = ntc;
     }
     return nr > 0;
+}
+
+// Whether a chunk continues the scan of the chunk before it: not a sequence's
+// first chunk, nor (in a split launch) the first chunk of its second segment.
+__device__ __forceinline__ bool continues(const ChunkArgs &p, int cl, int seq_chunks) {
+    return cl > 0 && !(p.split && cl == (seq_chunks + 1) / 2);
 }
 
 __device__ __forceinline__ void cp_async16(void *dst, const void *src) {
@@ -249,12 +259,12 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
     for (int64_t unit = ubeg; unit < uend; ++unit) {
     const int hv = (int)(unit / p.slots);
     const int64_t gc = unit % p.slots;
-    int b, r0, nr, cl;
-    if (!locate_chunk(p, gc, b, r0, nr, cl)) {
+    int b, r0, nr, cl, nseq, ncs;
+    if (!locate_chunk(p, gc, b, r0, nr, cl, &nseq, &ncs)) {
         prev_hv = -1;
         continue;
     }
-    const bool halo = cl > 0;  // the previous chunk of the same sequence exists
+    const bool halo = continues(p, cl, ncs);  // the previous chunk's state feeds this one
     const bool carry = halo && prev_hv == hv && prev_gc == gc - 1;
     const int h = hv / (p.HV / p.H);
     unsigned char *U = static_cast<unsigned char *>(p.units) + (gc * p.HV + hv) * Lo.stride;
@@ -634,9 +644,9 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
     bool next_carry = false;
     if (unit + 1 < uend) {
         const int64_t un = unit + 1;
-        int bn, r0n, nrn, cln;
-        next_carry = (int)(un / p.slots) == hv && locate_chunk(p, un % p.slots, bn, r0n, nrn, cln) &&
-                     cln > 0;
+        int bn, r0n, nrn, cln, nsn, ncn;
+        next_carry = (int)(un / p.slots) == hv &&
+                     locate_chunk(p, un % p.slots, bn, r0n, nrn, cln, &nsn, &ncn) && continues(p, cln, ncn);
     }
     if (next_carry) {
 #pragma unroll
@@ -713,7 +723,7 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
 }
 
 // ============================================================== scan kernel
-// Rounds r = 0 .. nc of one (sequence, value head, 32 value columns); round r
+// Rounds r = 0 .. nc of one (sequence, value head, SBV value columns); round r
 // finishes chunk c = r - 1 and starts chunk c + 1:
 //   A: D1  = [W~_{c+1}; qg_c] h_c        (needs h_c)
 //   C: D2  = kg_c^T v'_c                 (needs v'_c)   ->  h_{c+1} = Diag(2^G_c) h_c + D2
@@ -726,18 +736,30 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
 // v'_0 = u_0 - W_0 h_0.  A tcgen05.mma of these shapes occupies the tensor
 // unit for a fixed ~50 cycles whatever N <= 64 is, so 32 columns per CTA cost
 // no more MMA time than 16.
-template <int KK>
+//
+// Split sequences (context parallel within the GPU).  The state after a segment
+// of chunks is an affine function of the state before it: h_end = P h_start + E.
+// A split launch runs a sequence's two halves at once: segment 0 from h0 as
+// above (its final state E0), segment 1 from a zero state (o partial, final state
+// E1) and, in K extra "identity" columns, from the identity matrix with u = 0:
+// their readout is Q_c, the response of o_c to the segment's initial state, and
+// their final state is P.  The fix kernel then adds Q_c E0 to segment 1's rows
+// and forms ht = P E0 + E1.  The prep treats segment 1's first chunk as a
+// sequence start (untilded W, no M), which is exactly a scan from a given state.
+template <int KK, int SBV>
 struct ScanSmem {
+    static constexpr int kStages = SBV == 32 ? 3 : 2;
     static constexpr uint32_t top = 0;                         // [128][KK]: W~_{c+1}; qg_c
     static constexpr uint32_t kgt = top + 128 * KK * 2;        // [64][KK]: kg_c
     static constexpr uint32_t bot = kgt + 64 * KK * 2;         // [128][64]: M_{c+1}; Aqk_c
-    static constexpr uint32_t u = bot + 128 * 64 * 2;          // [kSBV/kUB][64][kUB] bf16: u_{c+1}
-    static constexpr uint32_t dec = u + 64 * kSBV * 2;         // [128] fp32: 2^G_c
+    static constexpr uint32_t u = bot + 128 * 64 * 2;          // [SBV/kUB][64][kUB] bf16: u_{c+1}
+    static constexpr uint32_t dec = u + 64 * SBV * 2;          // [128] fp32: 2^G_c
     static constexpr uint32_t stage = dec + 512;
     static constexpr uint32_t stage_stride = (stage + 1023) / 1024 * 1024;
-    static constexpr uint32_t hs = kStages * stage_stride;     // [KK][kSBV] tile
-    static constexpr uint32_t vp = hs + KK * kSBV * 2;         // [64][kSBV] tile
-    static constexpr uint32_t total = vp + 64 * kSBV * 2;
+    static constexpr uint32_t hs = kStages * stage_stride;     // [KK][SBV] tile
+    static constexpr uint32_t vp = hs + KK * SBV * 2;          // [64][SBV] tile
+    static constexpr uint32_t total = vp + 64 * SBV * 2;
+    static constexpr uint32_t tmem_cols = SBV == 32 ? 128 : 256;  // D1[0], D1[1], D2 at 0, SBV, 2 SBV
 };
 
 __device__ __forceinline__ int read_flag(const int *f) {
@@ -769,12 +791,44 @@ constexpr int kBarV = 2;   // v'_c written and D1 read: v' and o warps arrive, t
 constexpr int kThrH = 128 + 32;
 constexpr int kThrV = 128 + 32;
 
-// Warp roles: 0..3 h (state rows 32 w .. 32 w + 31, all kSBV columns, in fp32
+// SBV columns of TMEM (one lane per thread) into registers.
+template <int SBV>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&d)[SBV]) {
+    if constexpr (SBV == 64) {
+        tmem_ld64(taddr, d);
+    } else {
+        tmem_ld32(taddr, d);
+    }
+}
+
+// Work item of a scan CTA.  Without a split: (n, hv, vb) over the V columns.
+// With a split, per (n, hv): V/SBV segment-0 blocks, V/SBV segment-1 blocks,
+// then KK/SBV segment-1 identity blocks.
+struct ScanItem {
+    int n, hv, vb, seg;
+    bool ident;
+};
+template <int KK, int SBV>
+__device__ __forceinline__ ScanItem scan_item(const ChunkArgs &p, int64_t bid) {
+    ScanItem it;
+    const int nreal = p.V / SBV;
+    const int bpp = p.split ? 2 * nreal + KK / SBV : nreal;
+    const int j = (int)(bid % bpp);
+    it.hv = (int)((bid / bpp) % p.HV);
+    it.n = (int)(bid / ((int64_t)bpp * p.HV));
+    it.seg = j < nreal ? 0 : 1;
+    it.ident = j >= 2 * nreal;
+    it.vb = j < nreal ? j : (j < 2 * nreal ? j - nreal : j - 2 * nreal);
+    return it;
+}
+
+// Warp roles: 0..3 h (state rows 32 w .. 32 w + 31, all SBV columns, in fp32
 // registers), 4..5 v' (rows 0..63 of D1), 6..7 o (rows 64..127 of D1), 8 bulk
 // copies, 9 MMA issue.  A warp reaches TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31.
-template <int KK>
+template <int KK, int SBV>
 __global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
-    using S = ScanSmem<KK>;
+    using S = ScanSmem<KK, SBV>;
+    constexpr int kStages = S::kStages;
     extern __shared__ __align__(1024) unsigned char sm[];
     __shared__ uint64_t full[kStages], empty[kStages];
     // bar_v[x]: MMAs writing D1[x] done, one per buffer.
@@ -782,11 +836,9 @@ __global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
     __shared__ uint32_t tslot;
     __shared__ int abort_flag;
 
-    const int nvb = p.V / kSBV;
-    const int64_t bid = blockIdx.x;
-    const int vb = (int)(bid % nvb);
-    const int hv = (int)((bid / nvb) % p.HV);
-    const int n = (int)(bid / ((int64_t)nvb * p.HV));
+    const ScanItem item = scan_item<KK, SBV>(p, blockIdx.x);
+    const int n = item.n, hv = item.hv, vb = item.vb;
+    const bool ident = item.ident;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     int b, bos, eos, nc;
@@ -805,12 +857,19 @@ __global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
         nc = (p.T + kBT - 1) / kBT;
         gc0 = (int64_t)n * nc;
     }
-    const int R = nc > 0 ? nc + 1 : 0;  // rounds
+    // this CTA's chunks [c0, c1) of the sequence
+    int c0 = 0, c1 = nc;
+    if (p.split) {
+        const int m = (nc + 1) / 2;
+        if (item.seg == 0) c1 = m; else c0 = m;
+    }
+    const int ncs = c1 - c0;
+    const int R = ncs > 0 ? ncs + 1 : 0;  // rounds
     const TcLayout Lo = tc_layout(KK, p.V);
     const unsigned char *units = static_cast<const unsigned char *>(p.units);
 
     if (warp == 0) {
-        tmem_alloc(&tslot, 128);
+        tmem_alloc(&tslot, S::tmem_cols);
         tmem_relinquish();
     }
     if (tid == 0) {
@@ -828,7 +887,7 @@ __global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = tslot;  // D1[0] at +0, D1[1] at +32, D2 at +64
+    const uint32_t tmem = tslot;  // D1[0] at +0, D1[1] at +SBV, D2 at +2 SBV
     unsigned char *sH = sm + S::hs;
     unsigned char *sVp = sm + S::vp;
     // A wait that runs out sets the abort flag.  From then on nobody waits for
@@ -859,17 +918,18 @@ __global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
                 if (r >= kStages) wait_copy(&empty[s], ((r / kStages) - 1) & 1);
                 if (read_flag(&abort_flag)) break;
                 unsigned char *st = stage(r);
-                const int c = r - 1;
-                const bool nxt = r < nc, cur = r >= 1;
+                const int c = c0 + r - 1;
+                const bool nxt = r < ncs, cur = r >= 1;
                 uint32_t bytes = 0;
-                if (nxt) bytes += 64 * KK * 2 + 64 * kSBV * 2 + (cur ? 64 * 64 * 2 : 0);
+                if (nxt) bytes += 64 * KK * 2 + (ident ? 0 : 64 * SBV * 2) + (cur ? 64 * 64 * 2 : 0);
                 if (cur) bytes += 64 * KK * 2 + 64 * KK * 2 + 64 * 64 * 2 + 512;
                 mbar_arrive_expect_tx(&full[s], bytes);
                 if (nxt) {
                     const unsigned char *U1 = units + ((gc0 + c + 1) * p.HV + hv) * (int64_t)Lo.stride;
                     bulk_g2s(st + S::top, U1 + Lo.aw, 64 * KK * 2, &full[s]);
-                    bulk_g2s(st + S::u, U1 + Lo.u + (size_t)vb * 64 * kSBV * 2, 64 * kSBV * 2,
-                             &full[s]);
+                    if (!ident)
+                        bulk_g2s(st + S::u, U1 + Lo.u + (size_t)vb * 64 * SBV * 2, 64 * SBV * 2,
+                                 &full[s]);
                     if (cur) bulk_g2s(st + S::bot, U1 + Lo.mt, 64 * 64 * 2, &full[s]);
                 }
                 if (cur) {
@@ -888,15 +948,15 @@ __global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
         }
     } else if (warp == 9) {
         // ----------------------------------------------------- MMA issuer
-        const uint32_t idn = idesc_bf16(128, kSBV, false, true);
-        const uint32_t idc = idesc_bf16(128, kSBV, true, true);  // A = kg tile read MN-major
-        const uint64_t dh = sdesc(smem_addr(sH), kSBV * 16, 128);
-        const uint64_t dv = sdesc(smem_addr(sVp), kSBV * 16, 128);
-        constexpr uint32_t binc = 2 * kSBV * 16 / 16;
+        const uint32_t idn = idesc_bf16(128, SBV, false, true);
+        const uint32_t idc = idesc_bf16(128, SBV, true, true);  // A = kg tile read MN-major
+        const uint64_t dh = sdesc(smem_addr(sH), SBV * 16, 128);
+        const uint64_t dv = sdesc(smem_addr(sVp), SBV * 16, 128);
+        constexpr uint32_t binc = 2 * SBV * 16 / 16;
         for (int r = 0; r < R; ++r) {
             const int s = r % kStages;
             const uint32_t st = smem_addr(stage(r));
-            const uint32_t d1 = tmem + (r & 1) * kSBV;
+            const uint32_t d1 = tmem + (r & 1) * SBV;
             wait_copy(&full[s], (r / kStages) & 1);
             __syncwarp();
             named_sync(kBarH, kThrH);
@@ -912,7 +972,7 @@ __global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
                 if (elect_one()) {
                     tc_fence_after();
                     if (go)
-                        mma_bf16_seq<4, false>(tmem + 2 * kSBV, sdesc(st + S::kgt, KK * 16, 128),
+                        mma_bf16_seq<4, false>(tmem + 2 * SBV, sdesc(st + S::kgt, KK * 16, 128),
                                                2 * KK * 16 / 16, dv, binc, idc);
                     mma_commit(&bar_h);
                     if (go) mma_bf16_seq<4, true>(d1, sdesc(st + S::bot, 128, 1024), 16, dv, binc, idn);
@@ -935,15 +995,18 @@ __global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
         // ------------------------------------------------ h warps: the state
         const int row = warp * 32 + lane;
         const bool has_row = row < KK;
-        const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16) + 2 * kSBV;
-        const size_t srow = (((size_t)n * p.HV + hv) * KK + row) * (size_t)p.V + (size_t)vb * kSBV;
-        float h[kSBV];
+        const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16) + 2 * SBV;
+        float h[SBV];
 #pragma unroll
-        for (int j = 0; j < kSBV; ++j) h[j] = 0.f;
-        if (has_row && p.h0) {
-            const float4 *src = reinterpret_cast<const float4 *>(p.h0 + srow);
+        for (int j = 0; j < SBV; ++j) h[j] = 0.f;
+        if (ident) {
 #pragma unroll
-            for (int j = 0; j < kSBV / 4; ++j) {
+            for (int j = 0; j < SBV; ++j) h[j] = (row == vb * SBV + j) ? 1.f : 0.f;
+        } else if (item.seg == 0 && has_row && p.h0) {
+            const float4 *src = reinterpret_cast<const float4 *>(
+                p.h0 + (((size_t)n * p.HV + hv) * KK + row) * (size_t)p.V + (size_t)vb * SBV);
+#pragma unroll
+            for (int j = 0; j < SBV / 4; ++j) {
                 const float4 x = src[j];
                 h[4 * j] = x.x; h[4 * j + 1] = x.y; h[4 * j + 2] = x.z; h[4 * j + 3] = x.w;
             }
@@ -951,8 +1014,8 @@ __global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
         auto write_h = [&]() {
             if (has_row) {
 #pragma unroll
-                for (int c = 0; c < kSBV; c += 8)
-                    *reinterpret_cast<uint4 *>(sH + tile_off(row, c, kSBV)) = pack8_at(h + c);
+                for (int c = 0; c < SBV; c += 8)
+                    *reinterpret_cast<uint4 *>(sH + tile_off(row, c, SBV)) = pack8_at(h + c);
             }
             fence_async_smem();
             __syncwarp();
@@ -970,16 +1033,15 @@ __global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
         if (R > 0) write_h();
         float dec = R > 0 ? fetch(0) : 1.f;
         for (int r = 0; r < R; ++r) {
-            const bool nxt = r < nc;
+            const bool nxt = r < ncs;
             if (r >= 1) {
                 // h_{c+1} = Diag(2^G_c) h_c + D2  (bar_h also covers A_r's reads of h_c)
                 wait_mma(&bar_h, (r - 1) & 1);
                 tc_fence_after();
-                float d[kSBV];
-                tmem_ld16(taddr, *reinterpret_cast<float(*)[16]>(d));
-                tmem_ld16(taddr + 16, *reinterpret_cast<float(*)[16]>(d + 16));
+                float d[SBV];
+                tmem_ld_cols<SBV>(taddr, d);
 #pragma unroll
-                for (int t = 0; t < kSBV; ++t) h[t] = fmaf(dec, h[t], d[t]);
+                for (int t = 0; t < SBV; ++t) h[t] = fmaf(dec, h[t], d[t]);
                 tc_fence_before();
                 if (nxt) write_h();
             } else if (nxt) {
@@ -992,22 +1054,44 @@ __global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
             }
             if (r + 1 < R) dec = fetch(r + 1);
         }
-        if (p.ht && has_row && !read_flag(&abort_flag)) {
-            float4 *dst = reinterpret_cast<float4 *>(p.ht + srow);
+        // final state: ht, or for a split sequence E0 / E1 / P
+        float *dst_base = nullptr;
+        int width = p.V;
+        if (!p.split) {
+            dst_base = p.ht;
+        } else if (ident) {
+            dst_base = p.pm;
+            width = KK;
+        } else {
+            dst_base = item.seg == 0 ? p.e0 : p.e1;
+        }
+        if (dst_base && has_row && !read_flag(&abort_flag)) {
+            float4 *dst = reinterpret_cast<float4 *>(
+                dst_base + (((size_t)n * p.HV + hv) * KK + row) * (size_t)width + (size_t)vb * SBV);
 #pragma unroll
-            for (int j = 0; j < kSBV / 4; ++j)
+            for (int j = 0; j < SBV / 4; ++j)
                 dst[j] = make_float4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
+            if (p.split && !ident && item.seg == 0) {
+                // E0 again as the fix kernel's bf16 MMA operand ([KK][V] MN-major tile)
+                unsigned char *t = static_cast<unsigned char *>(p.e0b) +
+                                   ((size_t)n * p.HV + hv) * (size_t)KK * p.V * 2;
+#pragma unroll
+                for (int c = 0; c < SBV; c += 8)
+                    *reinterpret_cast<uint4 *>(t + tile_off(row, vb * SBV + c, p.V)) = pack8_at(h + c);
+            }
         }
     } else if (warp < 6) {
         // ------------------------------------- v' warps: v'_{c+1} = u_{c+1} - D1[0:64]
         const int row = (warp - 4) * 32 + lane;
         const uint32_t lanebase = (uint32_t)((warp - 4) * 32) << 16;
-        float u[kSBV];
+        float u[SBV];
+#pragma unroll
+        for (int t = 0; t < SBV; ++t) u[t] = 0.f;
         auto fetch = [&](int r) {
             wait_copy(&full[r % kStages], (r / kStages) & 1);
-            if (r < nc) {
+            if (r < ncs && !ident) {
 #pragma unroll
-                for (int blk = 0; blk < kSBV / kUB; ++blk) {
+                for (int blk = 0; blk < SBV / kUB; ++blk) {
                     const unsigned char *ur = stage(r) + S::u + ((size_t)blk * 64 + row) * kUB * 2;
                     float f[8];
                     unpack8(*reinterpret_cast<const uint4 *>(ur), f);
@@ -1022,25 +1106,25 @@ __global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
             if (lane == 0) mbar_arrive(&empty[r % kStages]);
         };
         if (R > 0) fetch(0);
-        for (int r = 0; r < nc; ++r) {
+        for (int r = 0; r < ncs; ++r) {
             wait_mma(&bar_v[r & 1], (r >> 1) & 1);
             tc_fence_after();
-            float d[kSBV];
-            tmem_ld16(tmem + lanebase + (r & 1) * kSBV, *reinterpret_cast<float(*)[16]>(d));
-            tmem_ld16(tmem + lanebase + (r & 1) * kSBV + 16, *reinterpret_cast<float(*)[16]>(d + 16));
+            float d[SBV];
+            tmem_ld_cols<SBV>(tmem + lanebase + (r & 1) * SBV, d);
             tc_fence_before();
 #pragma unroll
-            for (int t = 0; t < kSBV; ++t) d[t] = u[t] - d[t];
+            for (int t = 0; t < SBV; ++t) d[t] = u[t] - d[t];
 #pragma unroll
-            for (int c = 0; c < kSBV; c += 8)
-                *reinterpret_cast<uint4 *>(sVp + tile_off(row, c, kSBV)) = pack8_at(d + c);
+            for (int c = 0; c < SBV; c += 8)
+                *reinterpret_cast<uint4 *>(sVp + tile_off(row, c, SBV)) = pack8_at(d + c);
             fence_async_smem();
             __syncwarp();
             named_arrive(kBarV, kThrV);
             if (r + 1 < R) fetch(r + 1);
         }
     } else {
-        // --------------------------------------------- o warps: o_c = D1[64:128]
+        // -------------------------------------------- o warps: o_c = D1[64:128]
+        // (for identity columns: Q_c, segment 1's response to its initial state)
         const int i = (warp - 6) * 32 + lane;  // row within the chunk
         const uint32_t lanebase = (uint32_t)(64 + (warp - 6) * 32) << 16;
         __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.o);
@@ -1048,20 +1132,32 @@ __global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
             if (r >= 1) {
                 wait_mma(&bar_v[r & 1], (r >> 1) & 1);
                 tc_fence_after();
-                float d[kSBV];
-                tmem_ld16(tmem + lanebase + (r & 1) * kSBV, *reinterpret_cast<float(*)[16]>(d));
-                tmem_ld16(tmem + lanebase + (r & 1) * kSBV + 16, *reinterpret_cast<float(*)[16]>(d + 16));
+                float d[SBV];
+                tmem_ld_cols<SBV>(tmem + lanebase + (r & 1) * SBV, d);
                 tc_fence_before();
-                const int orow = bos + (r - 1) * kBT + i;
-                if (orow < eos && !read_flag(&abort_flag)) {
-                    __nv_bfloat16 *op = o + (((size_t)b * p.T + orow) * p.HV + hv) * p.V + vb * kSBV;
+                const int c = c0 + r - 1;
+                if (!read_flag(&abort_flag)) {
+                    if (ident) {
+                        unsigned char *qt = static_cast<unsigned char *>(p.qc) +
+                                            ((gc0 + c) * p.HV + hv) * (int64_t)(64 * KK * 2);
 #pragma unroll
-                    for (int c = 0; c < kSBV; c += 8)
-                        *reinterpret_cast<uint4 *>(op + c) = pack8_at(d + c);
+                        for (int cc = 0; cc < SBV; cc += 8)
+                            *reinterpret_cast<uint4 *>(qt + tile_off(i, vb * SBV + cc, KK)) =
+                                pack8_at(d + cc);
+                    } else {
+                        const int orow = bos + c * kBT + i;
+                        if (orow < eos) {
+                            __nv_bfloat16 *op =
+                                o + (((size_t)b * p.T + orow) * p.HV + hv) * p.V + vb * SBV;
+#pragma unroll
+                            for (int cc = 0; cc < SBV; cc += 8)
+                                *reinterpret_cast<uint4 *>(op + cc) = pack8_at(d + cc);
+                        }
+                    }
                 }
             }
             // D1[r & 1] has been read: the MMA warp may overwrite it two rounds on.
-            if (r < nc) {
+            if (r < ncs) {
                 __syncwarp();
                 named_arrive(kBarV, kThrV);
             }
@@ -1069,7 +1165,192 @@ __global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 128);
+    if (warp == 0) tmem_dealloc(tmem, S::tmem_cols);
+}
+
+// ============================================================== fix kernel
+// For split sequences: o_c += Q_c E0 over segment 1's chunks, and
+// ht = P E0 + E1 in fp32.  Blocks [0, n_fix_o) take a pair of adjacent chunk
+// slots of one value head: both Q tiles stacked as the 128 rows of one tcgen05
+// MMA series against E0 in bf16 (N = dv), one pass per distinct sequence in the
+// pair.  The remaining blocks take (sequence, head, 32 columns) of ht.
+template <int KK, int VV>
+struct FixSmem {
+    static constexpr uint32_t e0 = 0;                      // [KK][VV] bf16, MN-major B tile
+    static constexpr uint32_t q = e0 + KK * VV * 2;        // [128][KK] bf16: Q of the two chunks
+    static constexpr uint32_t ht_need = 16 * KK * 4 + KK * 32 * 4;  // ht units: P rows + E0 block
+    static constexpr uint32_t total = q + 128 * KK * 2 > ht_need ? q + 128 * KK * 2 : ht_need;
+    static constexpr uint32_t tmem_cols = VV <= 64 ? 64 : (VV <= 128 ? 128 : 256);
+};
+
+template <int KK, int VV>
+__global__ void __launch_bounds__(256) chunk_fix_tc_kernel(ChunkArgs p) {
+    using S = FixSmem<KK, VV>;
+    extern __shared__ __align__(1024) unsigned char sm[];
+    __shared__ uint64_t bar_q, bar_m, bar_e;
+    __shared__ uint32_t tslot;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    if (p.cu && !p.ctrl->valid) return;
+
+    // Persistent over the units: first the (value head, chunk pair) units of
+    // o_c += Q_c E0, then the small units of ht = P E0 + E1; CTA b takes units
+    // b, b + gridDim.x, ...  Pairs with nothing in segment 1 cost nothing, and the
+    // ht units land mostly on CTAs with one pair to fix.
+    unsigned char *sE0 = sm + S::e0;
+    unsigned char *sQ = sm + S::q;
+    if (warp == 0) {
+        tmem_alloc(&tslot, S::tmem_cols);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        mbar_init(&bar_q, 1);
+        mbar_init(&bar_m, 1);
+        mbar_init(&bar_e, 1);
+        mbar_fence_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tslot;
+    __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.o);
+    uint32_t ph_e = 0;
+    const int quad = warp & 3, half = warp >> 2;
+    const int xr = quad >> 1, ir = (quad & 1) * 32 + (tid & 31);  // TMEM lane = row of the pair
+    const int64_t pair_units = (int64_t)p.HV * ((p.slots + 1) / 2);
+    const int64_t units = pair_units + (p.ht ? (int64_t)p.N * p.HV * (KK / 16) * (VV / 32) : 0);
+    uint32_t ph_q = 0, ph_m = 0;
+    int e0_key = -1;  // (sequence, head) whose E0 is in shared memory
+    for (int64_t unit = blockIdx.x; unit < units; unit += gridDim.x) {
+        if (unit >= pair_units) {
+            // ------------------------------------------- ht = P E0 + E1
+            // unit = (sequence, head, 16-row block, 32-column block); thread: one
+            // row, two columns, the full contraction over k.
+            const int64_t hu = unit - pair_units;
+            const int ncb = VV / 32, nrb = KK / 16;
+            const int cb = (int)(hu % ncb);
+            const int rb = (int)((hu / ncb) % nrb);
+            const int hv = (int)((hu / ((int64_t)ncb * nrb)) % p.HV);
+            const int n = (int)(hu / ((int64_t)ncb * nrb * p.HV));
+            const size_t base = ((size_t)n * p.HV + hv) * KK;
+            const int nc = p.cu ? p.chunk_start[n + 1] - p.chunk_start[n] : (p.T + kBT - 1) / kBT;
+            const int d = rb * 16 + (tid >> 4), c = cb * 32 + (tid & 15) * 2;
+            if (nc <= 1) {  // segment 1 is empty: P = I, E1 = 0, so ht = E0 exactly
+                *reinterpret_cast<float2 *>(p.ht + (base + d) * VV + c) =
+                    *reinterpret_cast<const float2 *>(p.e0 + (base + d) * VV + c);
+                continue;
+            }
+            e0_key = -1;  // the shared E0 tile is overwritten here
+            float *sP = reinterpret_cast<float *>(sm);   // [16][KK] rows of P
+            float *sE = sP + 16 * KK;                    // [KK][32] columns of E0
+            for (int idx = tid; idx < 16 * KK / 4; idx += 256) {
+                const int r = idx / (KK / 4), k4 = (idx % (KK / 4)) * 4;
+                *reinterpret_cast<float4 *>(sP + r * KK + k4) =
+                    *reinterpret_cast<const float4 *>(p.pm + (base + rb * 16 + r) * KK + k4);
+            }
+            for (int idx = tid; idx < KK * 8; idx += 256) {
+                const int r = idx >> 3, c4 = (idx & 7) * 4;
+                *reinterpret_cast<float4 *>(sE + r * 32 + c4) =
+                    *reinterpret_cast<const float4 *>(p.e0 + (base + r) * VV + cb * 32 + c4);
+            }
+            __syncthreads();
+            float2 acc = *reinterpret_cast<const float2 *>(p.e1 + (base + d) * VV + c);
+            const float *pr = sP + (tid >> 4) * KK;
+            const float *er = sE + (tid & 15) * 2;
+#pragma unroll 16
+            for (int k = 0; k < KK; ++k) {
+                const float pv = pr[k];
+                const float2 e = *reinterpret_cast<const float2 *>(er + k * 32);
+                acc.x = fmaf(pv, e.x, acc.x);
+                acc.y = fmaf(pv, e.y, acc.y);
+            }
+            *reinterpret_cast<float2 *>(p.ht + (base + d) * VV + c) = acc;
+            __syncthreads();
+            continue;
+        }
+        const int64_t pu = unit;
+        const int hv = (int)(pu % p.HV);
+        const int64_t gpair = (pu / p.HV) * 2;
+        int cb_[2], r0_[2], nr_[2], seq_[2];
+        bool need[2];
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+            int cl, ncn;
+            need[x] = gpair + x < p.slots &&
+                      locate_chunk(p, gpair + x, cb_[x], r0_[x], nr_[x], cl, &seq_[x], &ncn) &&
+                      cl >= (ncn + 1) / 2;  // in segment 1
+        }
+        if (!need[0] && !need[1]) continue;
+        if (tid == 0) {
+            uint32_t bytes = 0;
+            for (int x = 0; x < 2; ++x)
+                if (need[x]) bytes += 64 * KK * 2;
+            mbar_arrive_expect_tx(&bar_q, bytes);
+            for (int x = 0; x < 2; ++x)
+                if (need[x])
+                    bulk_g2s(sQ + x * 64 * KK * 2,
+                             static_cast<const unsigned char *>(p.qc) +
+                                 ((gpair + x) * p.HV + hv) * (int64_t)(64 * KK * 2),
+                             64 * KK * 2, &bar_q);
+        }
+        // this thread's o row segment (half of the columns), loaded now so its
+        // latency overlaps E0, the Q copy and the MMA
+        const bool has_o = need[xr] && ir < nr_[xr];
+        uint4 *orow = reinterpret_cast<uint4 *>(
+            o + (((size_t)cb_[xr] * p.T + r0_[xr] + ir) * p.HV + hv) * p.V + half * (VV / 2));
+        uint4 ov[VV / 16];
+        if (has_o) {
+#pragma unroll
+            for (int j = 0; j < VV / 16; ++j) ov[j] = orow[j];
+        }
+        // one pass per distinct sequence among the chunks that need the fix
+        const int npass = (need[0] && need[1] && seq_[0] != seq_[1]) ? 2 : 1;
+        for (int pass = 0; pass < npass; ++pass) {
+            const int seq = npass == 2 ? seq_[pass] : (need[0] ? seq_[0] : seq_[1]);
+            const int key = seq * p.HV + hv;
+            const bool load_e0 = key != e0_key;  // E0 of this sequence, a bf16 MN-major tile
+            if (load_e0 && tid == 0) {
+                mbar_arrive_expect_tx(&bar_e, KK * VV * 2);
+                bulk_g2s(sE0, static_cast<const unsigned char *>(p.e0b) + (size_t)key * KK * VV * 2,
+                         KK * VV * 2, &bar_e);
+            }
+            e0_key = key;
+            if (tid == 0) {
+                if (pass == 0 && !mbar_wait(&bar_q, ph_q & 1, kWaitNs)) report(p.status, KDA_DEVICE_TIMEOUT);
+                if (load_e0 && !mbar_wait(&bar_e, ph_e & 1, kWaitNs)) report(p.status, KDA_DEVICE_TIMEOUT);
+                tc_fence_after();
+                mma_bf16_seq<KK / 16, false>(tmem, sdesc(smem_addr(sQ), 128, KK * 16), 16,
+                                             sdesc(smem_addr(sE0), VV * 16, 128), 2 * VV * 16 / 16,
+                                             idesc_bf16(128, VV, false, true));
+                mma_commit(&bar_m);
+            }
+            __syncwarp();
+            if (load_e0) ++ph_e;
+            if (!mbar_wait(&bar_m, ph_m & 1, kWaitNs) && tid == 0) report(p.status, KDA_DEVICE_TIMEOUT);
+            ++ph_m;
+            tc_fence_after();
+            const bool mine = has_o && seq_[xr] == seq;
+#pragma unroll
+            for (int cc = 0; cc < VV / 2; cc += 32) {
+                float d[32];
+                tmem_ld32(tmem_at(tmem, quad * 32, half * (VV / 2) + cc), d);
+                if (mine) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        float f[8];
+                        unpack8(ov[cc / 8 + j], f);
+#pragma unroll
+                        for (int t = 0; t < 8; ++t) f[t] += d[8 * j + t];
+                        orow[cc / 8 + j] = pack8(f);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncthreads();
+            tc_fence_after();
+        }
+        ++ph_q;
+    }
+    if (warp == 0) tmem_dealloc(tmem, S::tmem_cols);
 }
 
 template <int KK, int VV>
@@ -1112,42 +1393,76 @@ cudaError_t launch_prep(const ChunkArgs &a, cudaStream_t st) {
     return cudaGetLastError();
 }
 
-template <int KK>
+template <int KK, int SBV>
 cudaError_t launch_scan(const ChunkArgs &a, cudaStream_t st) {
-    using S = ScanSmem<KK>;
+    using S = ScanSmem<KK, SBV>;
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(chunk_scan_tc_kernel<KK>,
+        cudaError_t e = cudaFuncSetAttribute(chunk_scan_tc_kernel<KK, SBV>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::total);
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    const int64_t blocks = (int64_t)a.N * a.HV * (a.V / kSBV);
+    const int64_t per = a.split ? 2 * (a.V / SBV) + KK / SBV : a.V / SBV;
+    const int64_t blocks = (int64_t)a.N * a.HV * per;
     if (blocks == 0) return cudaSuccess;
     prof_begin("chunk_scan_tc", st);
-    chunk_scan_tc_kernel<KK><<<(unsigned)blocks, 320, S::total, st>>>(a);
+    chunk_scan_tc_kernel<KK, SBV><<<(unsigned)blocks, 320, S::total, st>>>(a);
     prof_end(st);
     return cudaGetLastError();
 }
 
+template <int KK, int VV>
+cudaError_t launch_fix(const ChunkArgs &a, cudaStream_t st) {
+    using S = FixSmem<KK, VV>;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(chunk_fix_tc_kernel<KK, VV>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::total);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    static int slots_on_device = 0;  // two resident CTAs per SM
+    if (slots_on_device == 0) {
+        int dev = 0, sms = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        slots_on_device = 2 * sms;
+    }
+    const int64_t units = (a.ht ? (int64_t)a.N * a.HV * (KK / 16) * (VV / 32) : 0) +
+                          (int64_t)a.HV * ((a.slots + 1) / 2);
+    if (units == 0) return cudaSuccess;
+    const unsigned grid = (unsigned)(units < slots_on_device ? units : slots_on_device);
+    prof_begin("chunk_fix_tc", st);
+    chunk_fix_tc_kernel<KK, VV><<<grid, 256, S::total, st>>>(a);
+    prof_end(st);
+    return cudaGetLastError();
+}
+
+template <int KK, int VV>
+cudaError_t launch_kv(const ChunkArgs &a, cudaStream_t st) {
+    cudaError_t e = cudaSuccess;
+    if (a.slots > 0 && (e = launch_prep<KK, VV>(a, st)) != cudaSuccess) return e;
+    if (!a.split) return launch_scan<KK, 32>(a, st);
+    if ((e = launch_scan<KK, 64>(a, st)) != cudaSuccess) return e;
+    if constexpr (VV % 64 == 0) return launch_fix<KK, VV>(a, st);
+    return cudaErrorInvalidValue;
+}
+
 template <int KK>
 cudaError_t launch_k(const ChunkArgs &a, cudaStream_t st) {
-    cudaError_t e = cudaSuccess;
-    if (a.slots > 0) {
-        switch (a.V) {
-            case 32: e = launch_prep<KK, 32>(a, st); break;
-            case 64: e = launch_prep<KK, 64>(a, st); break;
-            case 96: e = launch_prep<KK, 96>(a, st); break;
-            case 128: e = launch_prep<KK, 128>(a, st); break;
-            case 160: e = launch_prep<KK, 160>(a, st); break;
-            case 192: e = launch_prep<KK, 192>(a, st); break;
-            case 224: e = launch_prep<KK, 224>(a, st); break;
-            case 256: e = launch_prep<KK, 256>(a, st); break;
-            default: return cudaErrorInvalidValue;
-        }
-        if (e != cudaSuccess) return e;
+    switch (a.V) {
+        case 32: return launch_kv<KK, 32>(a, st);
+        case 64: return launch_kv<KK, 64>(a, st);
+        case 96: return launch_kv<KK, 96>(a, st);
+        case 128: return launch_kv<KK, 128>(a, st);
+        case 160: return launch_kv<KK, 160>(a, st);
+        case 192: return launch_kv<KK, 192>(a, st);
+        case 224: return launch_kv<KK, 224>(a, st);
+        case 256: return launch_kv<KK, 256>(a, st);
+        default: return cudaErrorInvalidValue;
     }
-    return launch_scan<KK>(a, st);
 }
 
 }  // namespace
@@ -1157,6 +1472,13 @@ bool chunk_tc_supported(int K, int V) {
 }
 
 size_t chunk_tc_unit_bytes(int K, int V) { return tc_layout(K, V).stride; }
+
+bool chunk_tc_split(int N, int HV, int K, int V, int T) {
+    // Few long sequences: without a split the scan occupies under half of the
+    // SMs for its whole sequential length; with it, every scan CTA still fits
+    // one wave (at most 128 CTAs).
+    return V % 64 == 0 && (int64_t)N * HV * (V / 32) <= 64 && T >= 1024 && (K == 64 || K == 128);
+}
 
 cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st) {
     if (a.K == 64) return launch_k<64>(a, st);

@@ -109,12 +109,20 @@ struct ChunkArgs {
     int32_t *chunk_start;  // [N + 1] (packed only)
     void *units;           // per-(chunk, value head) intermediates
     int64_t slots;         // chunk slots (upper bound)
+    // split sequences (tensor-core path): see chunk_tc_split
+    int split;
+    void *qc;              // [slots][HV][64][K] bf16: segment 1's Q_c operand tiles
+    float *e0, *e1;        // [N][HV][K][V] fp32: the segments' final states from zero / h0
+    void *e0b;             // [N][HV] bf16 [K][V] operand tiles of e0
+    float *pm;             // [N][HV][K][K] fp32: segment 1's state transition
 };
 size_t chunk_simt_unit_bytes(int K, int V);
 cudaError_t launch_chunk_simt(const ChunkArgs &a, kda_dtype dt, cudaStream_t st);
 
 // Tensor-core path (bf16 inputs): K in {64, 128}, V a multiple of 32 up to 256.
 bool chunk_tc_supported(int K, int V);
+// Whether a launch splits each sequence's scan into two segments run at once.
+bool chunk_tc_split(int N, int HV, int K, int V, int T);
 size_t chunk_tc_unit_bytes(int K, int V);
 cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st);
 

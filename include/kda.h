@@ -87,6 +87,15 @@ typedef enum {
 #define KDA_FLAG_G_IS_CUMSUM (1u << 1)  /* kda_chunk_fwd only: g already holds the
                                            chunk-local cumsum (kda_gate_cumsum
                                            output with chunk_size 64)             */
+#define KDA_FLAG_SPLIT_SCAN  (1u << 2)  /* kda_chunk_fwd, bf16 tensor-core path: for
+                                           few long sequences (num_seqs * HV * V / 32
+                                           <= 64, T >= 1024, V % 64 == 0) run each
+                                           sequence's inter-chunk scan as two
+                                           segments at once and compose them after
+                                           (h_end = P h_start + E; SURVEY row f4,
+                                           context parallel within one GPU).  Needs
+                                           a larger workspace (size it with the same
+                                           flags); ignored elsewhere.              */
 
 /* Bits of the device status word. */
 #define KDA_DEVICE_BAD_CU_SEQLENS (1 << 0)

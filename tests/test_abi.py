@@ -124,6 +124,23 @@ def test_gate_cumsum_rejects_alias_and_chunk(lib):
                                None) == 2
 
 
+def test_split_scan_flag_sizes_a_larger_workspace(lib):
+    """KDA_FLAG_SPLIT_SCAN on an eligible bf16 shape (few long sequences) adds
+    the composition buffers: Q tiles per chunk slot, E0 and E1, P, and E0 as a
+    bf16 operand tile; an ineligible shape (fp32) is unchanged."""
+    import gated_delta_rule_cumsum_gb300 as kda
+
+    base = dict(B=1, T=2048, H=2, HV=2, K=128, V=128, num_seqs=1, dtype=1)
+    plain = lib.kda_chunk_workspace_size(ctypes.byref(_shape(**base)))
+    split = lib.kda_chunk_workspace_size(ctypes.byref(_shape(**base, flags=kda.KDA_FLAG_SPLIT_SCAN)))
+    slots, nh, K, V = 2048 // 64 + 1, 2, 128, 128
+    extra = slots * nh * 64 * K * 2 + nh * (2 * K * V * 4 + K * K * 4 + K * V * 2)
+    assert extra <= split - plain <= extra + 5 * 256
+    f32 = dict(base, dtype=0)
+    assert (lib.kda_chunk_workspace_size(ctypes.byref(_shape(**f32, flags=kda.KDA_FLAG_SPLIT_SCAN)))
+            == lib.kda_chunk_workspace_size(ctypes.byref(_shape(**f32))))
+
+
 def test_workspace_size_scales_with_chunks(lib):
     a = lib.kda_chunk_workspace_size(ctypes.byref(_shape(T=64)))
     b = lib.kda_chunk_workspace_size(ctypes.byref(_shape(T=640)))
