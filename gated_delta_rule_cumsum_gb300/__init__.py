@@ -21,9 +21,10 @@ import torch
 __all__ = [
     "KDA_OK", "KDA_ERR_INVALID_ARG", "KDA_ERR_UNSUPPORTED", "KDA_ERR_BAD_CU_SEQLENS",
     "KDA_ERR_CUDA", "KDA_ERR_TIMEOUT", "KDA_FLAG_QK_L2NORM", "KDA_FLAG_G_IS_CUMSUM",
-    "KDA_FLAG_SPLIT_SCAN",
+    "KDA_FLAG_SPLIT_SCAN", "KdaActivation", "make_activation",
     "KdaError", "KdaShape", "load", "library_path", "make_shape",
     "kda_gate_cumsum", "kda_chunk_fwd", "kda_recurrent_fwd", "kda_chunk_workspace_size",
+    "kda_gate_cumsum_act", "kda_chunk_fwd_act", "kda_recurrent_fwd_act",
     "kda_chunk_fwd_noalloc", "KDA_NOALLOC_SCRATCH_BYTES",
     "kda_read_device_status", "kda_clear_device_status", "kda_status_string",
     "kda_last_error_message", "kda_version", "kda_profile_enable", "kda_profile_report",
@@ -61,6 +62,21 @@ class KdaShape(ctypes.Structure):
                 ("flags", ctypes.c_uint32)]
 
 
+class KdaActivation(ctypes.Structure):
+    """Mirror of `kda_activation` in include/kda.h."""
+    _fields_ = [("A_log", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p),
+                ("beta_scale", ctypes.c_float)]
+
+
+def make_activation(A_log=None, dt_bias=None, beta_scale: float = 0.0) -> KdaActivation:
+    """A_log [HV] and dt_bias [HV, K] fp32 device tensors (or None); beta_scale 0
+    keeps beta as given, 1 or 2 applies sigmoid(beta) * beta_scale."""
+    for t, name in ((A_log, "A_log"), (dt_bias, "dt_bias")):
+        if t is not None and (t.dtype != torch.float32 or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous fp32 tensor")
+    return KdaActivation(_ptr(A_log), _ptr(dt_bias), float(beta_scale))
+
+
 def library_path() -> str:
     return _LIB_PATH
 
@@ -69,6 +85,13 @@ def library_path() -> str:
 _VP, _SZ, _I32, _ST = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32, ctypes.c_int
 _SIGNATURES = {
     "kda_gate_cumsum": (_ST, [_VP, _VP, _VP, ctypes.POINTER(KdaShape), _I32, _VP, _VP]),
+    "kda_gate_cumsum_act": (_ST, [_VP, _VP, _VP, ctypes.POINTER(KdaShape),
+                                  ctypes.POINTER(KdaActivation), _I32, _VP, _VP]),
+    "kda_chunk_fwd_act": (_ST, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.POINTER(KdaShape),
+                                ctypes.POINTER(KdaActivation), _VP, _VP, _VP, _SZ, _VP, _VP]),
+    "kda_recurrent_fwd_act": (_ST, [_VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                    ctypes.POINTER(KdaShape), ctypes.POINTER(KdaActivation),
+                                    _VP, _VP, _VP, _VP]),
     "kda_chunk_fwd": (_ST, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.POINTER(KdaShape), _VP,
                             _VP, _VP, _SZ, _VP, _VP]),
     "kda_chunk_workspace_size": (_SZ, [ctypes.POINTER(KdaShape)]),
@@ -141,6 +164,29 @@ def kda_gate_cumsum(g, g_cum, cu_seqlens, shape: KdaShape, chunk_size: int, dev_
                     stream=None):
     _check(load().kda_gate_cumsum(_ptr(g), _ptr(g_cum), _ptr(cu_seqlens), ctypes.byref(shape),
                                   int(chunk_size), _ptr(dev_status), _stream(stream)))
+
+
+def kda_gate_cumsum_act(g, g_cum, cu_seqlens, shape: KdaShape, act: KdaActivation,
+                        chunk_size: int, dev_status=None, stream=None):
+    _check(load().kda_gate_cumsum_act(_ptr(g), _ptr(g_cum), _ptr(cu_seqlens), ctypes.byref(shape),
+                                      ctypes.byref(act), int(chunk_size), _ptr(dev_status),
+                                      _stream(stream)))
+
+
+def kda_chunk_fwd_act(q, k, v, g, beta, h0, cu_seqlens, shape: KdaShape, act: KdaActivation, o,
+                      ht, workspace, dev_status=None, stream=None):
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().kda_chunk_fwd_act(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0),
+                                    _ptr(cu_seqlens), ctypes.byref(shape), ctypes.byref(act),
+                                    _ptr(o), _ptr(ht), _ptr(workspace), nbytes, _ptr(dev_status),
+                                    _stream(stream)))
+
+
+def kda_recurrent_fwd_act(q, k, v, g, beta, h0, cu_seqlens, shape: KdaShape, act: KdaActivation,
+                          o, ht, dev_status=None, stream=None):
+    _check(load().kda_recurrent_fwd_act(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0),
+                                        _ptr(cu_seqlens), ctypes.byref(shape), ctypes.byref(act),
+                                        _ptr(o), _ptr(ht), _ptr(dev_status), _stream(stream)))
 
 
 def kda_chunk_fwd(q, k, v, g, beta, h0, cu_seqlens, shape: KdaShape, o, ht, workspace,
@@ -235,21 +281,29 @@ def new_status(device=None) -> torch.Tensor:
 
 
 def gate_cumsum(g, cu_seqlens=None, chunk_size: int = 64, g_scale: float = 1.0, dev_status=None,
-                stream=None):
-    """Chunk-local cumsum of g [B,T,HV,K] fp32; rows outside every sequence are zero."""
+                stream=None, A_log=None, dt_bias=None):
+    """Chunk-local cumsum of g [B,T,HV,K] fp32; rows outside every sequence are zero.
+    With `A_log`, g is the raw gate, activated first (see chunk_kda)."""
     g, cu_seqlens = _prep(g, cu_seqlens)
     B, T, HV, K = g.shape
     shape = KdaShape(B, T, 1, HV, K, 1, B if cu_seqlens is None else cu_seqlens.numel() - 1,
                      KDA_DTYPE_F32, -1.0, float(g_scale), 0)
     out = torch.zeros_like(g)
-    kda_gate_cumsum(g, out, cu_seqlens, shape, chunk_size, dev_status, stream)
+    if A_log is not None:
+        kda_gate_cumsum_act(g, out, cu_seqlens, shape, make_activation(A_log, dt_bias),
+                            chunk_size, dev_status, stream)
+    else:
+        kda_gate_cumsum(g, out, cu_seqlens, shape, chunk_size, dev_status, stream)
     return out
 
 
 def chunk_kda(q, k, v, g, beta, scale=None, initial_state=None, output_final_state=False,
               cu_seqlens=None, use_qk_l2norm_in_kernel=False, g_scale=1.0, g_is_cumsum=False,
-              split_scan=False, workspace=None, dev_status=None, stream=None):
-    """Chunked forward; returns (o, ht or None).  `g` is the per-token log2 gate."""
+              split_scan=False, A_log=None, dt_bias=None, beta_sigmoid_scale=0.0,
+              workspace=None, dev_status=None, stream=None):
+    """Chunked forward; returns (o, ht or None).  `g` is the per-token log2 gate, or
+    with `A_log` the raw gate (activated inside: -exp(A_log) softplus(g + dt_bias),
+    times g_scale); `beta_sigmoid_scale` > 0 makes `beta` logits."""
     q, k, v, g, beta, h0, cu = _prep(q, k, v, g, beta, initial_state, cu_seqlens)
     flags = (KDA_FLAG_QK_L2NORM if use_qk_l2norm_in_kernel else 0) | (
         KDA_FLAG_G_IS_CUMSUM if g_is_cumsum else 0) | (KDA_FLAG_SPLIT_SCAN if split_scan else 0)
@@ -260,14 +314,21 @@ def chunk_kda(q, k, v, g, beta, scale=None, initial_state=None, output_final_sta
     if workspace is None:
         workspace = torch.empty(max(kda_chunk_workspace_size(shape), 256), dtype=torch.uint8,
                                 device=q.device)
-    kda_chunk_fwd(q, k, v, g, beta, h0, cu, shape, o, ht, workspace, dev_status, stream)
+    if A_log is not None or beta_sigmoid_scale:
+        act = make_activation(A_log, dt_bias, beta_sigmoid_scale)
+        kda_chunk_fwd_act(q, k, v, g, beta, h0, cu, shape, act, o, ht, workspace, dev_status,
+                          stream)
+    else:
+        kda_chunk_fwd(q, k, v, g, beta, h0, cu, shape, o, ht, workspace, dev_status, stream)
     return o, ht
 
 
 def recurrent_kda(q, k, v, gate, beta, initial_state=None, *, cu_seqlens=None,
                   output_final_state=False, scale=None, use_qk_l2norm_in_kernel=False,
-                  g_scale=1.0, dev_status=None, stream=None, final_state_out=None):
-    """Token-by-token forward; returns (o, ht or None).  `gate` is the per-token log2 gate."""
+                  g_scale=1.0, A_log=None, dt_bias=None, beta_sigmoid_scale=0.0,
+                  dev_status=None, stream=None, final_state_out=None):
+    """Token-by-token forward; returns (o, ht or None).  `gate` is the per-token log2 gate
+    (or, with `A_log`, the raw gate; see chunk_kda)."""
     q, k, v, g, beta, h0, cu = _prep(q, k, v, gate, beta, initial_state, cu_seqlens)
     flags = KDA_FLAG_QK_L2NORM if use_qk_l2norm_in_kernel else 0
     shape = make_shape(q, v, cu, scale, g_scale, flags)
@@ -276,5 +337,9 @@ def recurrent_kda(q, k, v, gate, beta, initial_state=None, *, cu_seqlens=None,
     if ht is None and output_final_state:
         ht = torch.empty(shape.num_seqs, shape.HV, shape.K, shape.V, dtype=torch.float32,
                          device=q.device)
-    kda_recurrent_fwd(q, k, v, g, beta, h0, cu, shape, o, ht, dev_status, stream)
+    if A_log is not None or beta_sigmoid_scale:
+        act = make_activation(A_log, dt_bias, beta_sigmoid_scale)
+        kda_recurrent_fwd_act(q, k, v, g, beta, h0, cu, shape, act, o, ht, dev_status, stream)
+    else:
+        kda_recurrent_fwd(q, k, v, g, beta, h0, cu, shape, o, ht, dev_status, stream)
     return o, ht

@@ -113,6 +113,24 @@ ChunkWs chunk_ws_layout(const kda_shape *s, bool packed) {
     return L;
 }
 
+// kda_activation -> the kernels' GateAct, with its argument checks.
+kda_status resolve_act(const char *op, const kda_shape *s, const kda_activation *act,
+                       kda::GateAct *out) {
+    *out = kda::GateAct();
+    if (!act) return KDA_OK;
+    if (act->dt_bias && !act->A_log)
+        return fail(KDA_ERR_INVALID_ARG, "%s: dt_bias needs A_log", op);
+    if (!(act->beta_scale >= 0.f) || !std::isfinite(act->beta_scale))
+        return fail(KDA_ERR_INVALID_ARG, "%s: beta_scale must be 0 or a positive finite scale", op);
+    if (act->A_log && (s->flags & KDA_FLAG_G_IS_CUMSUM))
+        return fail(KDA_ERR_INVALID_ARG, "%s: the gate activation needs the per-token gate, not "
+                    "KDA_FLAG_G_IS_CUMSUM", op);
+    out->A_log = act->A_log;
+    out->dt_bias = act->dt_bias;
+    out->beta_scale = act->beta_scale;
+    return KDA_OK;
+}
+
 kda_status check_chunk_support(const char *op, const kda_shape *s) {
     if (s->K != 64 && s->K != 128)
         return fail(KDA_ERR_UNSUPPORTED, "%s: K=%d (supported: 64, 128)", op, s->K);
@@ -149,9 +167,18 @@ const char *kda_last_error_message(void) { return g_last_error.c_str(); }
 kda_status kda_gate_cumsum(const float *g, float *g_cum, const int32_t *cu_seqlens,
                            const kda_shape *shape, int32_t chunk_size, int32_t *dev_status,
                            kda_stream_t stream) {
+    return kda_gate_cumsum_act(g, g_cum, cu_seqlens, shape, nullptr, chunk_size, dev_status,
+                               stream);
+}
+
+kda_status kda_gate_cumsum_act(const float *g, float *g_cum, const int32_t *cu_seqlens,
+                               const kda_shape *shape, const kda_activation *act,
+                               int32_t chunk_size, int32_t *dev_status, kda_stream_t stream) {
     const char *op = "kda_gate_cumsum";
     kda_status st = check_common(op, shape, cu_seqlens);
     if (st != KDA_OK) return st;
+    kda::GateAct ga;
+    if ((st = resolve_act(op, shape, act, &ga)) != KDA_OK) return st;
     if (chunk_size < 1 || chunk_size > 64)
         return fail(KDA_ERR_UNSUPPORTED, "%s: chunk_size=%d (supported: 1..64)", op, chunk_size);
     if ((int64_t)shape->B * shape->T > 0) {
@@ -165,7 +192,7 @@ kda_status kda_gate_cumsum(const float *g, float *g_cum, const int32_t *cu_seqle
                                          nullptr, s);
         if (e != cudaSuccess) return cuda_fail(e, op);
     }
-    e = kda::launch_gate_cumsum(g, g_cum, cu_seqlens, *shape, chunk_size, s);
+    e = kda::launch_gate_cumsum(g, g_cum, cu_seqlens, *shape, ga, chunk_size, s);
     if (e != cudaSuccess) return cuda_fail(e, op);
     g_last_error.clear();
     return KDA_OK;
@@ -175,13 +202,23 @@ kda_status kda_recurrent_fwd(const void *q, const void *k, const void *v, const 
                              const void *beta, const float *h0, const int32_t *cu_seqlens,
                              const kda_shape *shape, void *o, float *ht, int32_t *dev_status,
                              kda_stream_t stream) {
+    return kda_recurrent_fwd_act(q, k, v, g, beta, h0, cu_seqlens, shape, nullptr, o, ht,
+                                 dev_status, stream);
+}
+
+kda_status kda_recurrent_fwd_act(const void *q, const void *k, const void *v, const float *g,
+                                 const void *beta, const float *h0, const int32_t *cu_seqlens,
+                                 const kda_shape *shape, const kda_activation *act, void *o,
+                                 float *ht, int32_t *dev_status, kda_stream_t stream) {
     const char *op = "kda_recurrent_fwd";
     kda_status st = check_common(op, shape, cu_seqlens);
     if (st != KDA_OK) return st;
+    kda::GateAct ga;
     if ((st = check_fwd_pointers(op, shape, q, k, v, g, beta, o, cu_seqlens)) != KDA_OK) return st;
     if (shape->flags & KDA_FLAG_G_IS_CUMSUM)
         return fail(KDA_ERR_UNSUPPORTED, "%s: g is the per-token gate; KDA_FLAG_G_IS_CUMSUM is "
                     "for kda_chunk_fwd", op);
+    if ((st = resolve_act(op, shape, act, &ga)) != KDA_OK) return st;
     if (shape->K > 256) return fail(KDA_ERR_UNSUPPORTED, "%s: K=%d > 256", op, shape->K);
     const int64_t blocks = (int64_t)shape->num_seqs * shape->HV * ((shape->V + 127) / 128);
     if (blocks > INT_MAX) return fail(KDA_ERR_UNSUPPORTED, "%s: grid too large", op);
@@ -193,6 +230,7 @@ kda_status kda_recurrent_fwd(const void *q, const void *k, const void *v, const 
     a.scale = resolve_scale(shape);
     a.g_scale = shape->g_scale;
     a.l2norm = (shape->flags & KDA_FLAG_QK_L2NORM) ? 1 : 0;
+    a.act = ga;
     cudaError_t e = kda::launch_recurrent(a, shape->dtype, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, op);
     g_last_error.clear();
@@ -211,9 +249,20 @@ kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const floa
                          const void *beta, const float *h0, const int32_t *cu_seqlens,
                          const kda_shape *shape, void *o, float *ht, void *workspace,
                          size_t workspace_bytes, int32_t *dev_status, kda_stream_t stream) {
+    return kda_chunk_fwd_act(q, k, v, g, beta, h0, cu_seqlens, shape, nullptr, o, ht, workspace,
+                             workspace_bytes, dev_status, stream);
+}
+
+kda_status kda_chunk_fwd_act(const void *q, const void *k, const void *v, const float *g,
+                             const void *beta, const float *h0, const int32_t *cu_seqlens,
+                             const kda_shape *shape, const kda_activation *act, void *o,
+                             float *ht, void *workspace, size_t workspace_bytes,
+                             int32_t *dev_status, kda_stream_t stream) {
     const char *op = "kda_chunk_fwd";
     kda_status st = check_common(op, shape, cu_seqlens);
     if (st != KDA_OK) return st;
+    kda::GateAct ga;
+    if ((st = resolve_act(op, shape, act, &ga)) != KDA_OK) return st;
     if ((st = check_fwd_pointers(op, shape, q, k, v, g, beta, o, cu_seqlens)) != KDA_OK) return st;
     if ((st = check_chunk_support(op, shape)) != KDA_OK) return st;
     const bool packed = cu_seqlens != nullptr;
@@ -236,6 +285,7 @@ kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const floa
     a.g_scale = shape->g_scale;
     a.l2norm = (shape->flags & KDA_FLAG_QK_L2NORM) ? 1 : 0;
     a.g_is_cumsum = (shape->flags & KDA_FLAG_G_IS_CUMSUM) ? 1 : 0;
+    a.act = ga;
     a.ctrl = reinterpret_cast<kda::ChunkCtrl *>(ws + L.ctrl);
     a.chunk_start = reinterpret_cast<int32_t *>(ws + L.chunk_start);
     a.units = ws + L.units;

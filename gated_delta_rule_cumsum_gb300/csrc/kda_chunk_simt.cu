@@ -99,11 +99,19 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(ChunkArgs p) {
         sQ[idx] = ok ? to_f32(q[src]) : 0.f;
         sK[idx] = ok ? to_f32(k[src]) : 0.f;
     }
-    if (tid < kBT) sB[tid] = tid < nr ? to_f32(beta[(row0 + tid) * p.HV + hv]) : 0.f;
+    if (tid < kBT) {
+        float bv = tid < nr ? to_f32(beta[(row0 + tid) * p.HV + hv]) : 0.f;
+        if (p.act.beta_scale > 0.f && tid < nr) bv = beta_activate<T>(bv, p.act.beta_scale);
+        sB[tid] = bv;
+    }
+    const bool gate_act = p.act.A_log != nullptr;
+    const float neg_a = gate_act ? gate_neg_a(p.act, hv) : 0.f;
     for (int d = tid; d < KK; d += kThreads) {  // Stage 1: chunk-local cumsum
+        const float gbias = gate_act ? gate_bias(p.act, hv, d, KK) : 0.f;
         float acc = 0.f;
         for (int i = 0; i < nr; ++i) {
-            const float gv = p.g[((row0 + i) * p.HV + hv) * KK + d];
+            float gv = p.g[((row0 + i) * p.HV + hv) * KK + d];
+            if (gate_act) gv = neg_a * softplus_f(gv + gbias);
             acc = p.g_is_cumsum ? gv : acc + p.g_scale * gv;
             sG[i * KK + d] = acc;
         }

@@ -132,7 +132,9 @@ __device__ __forceinline__ uint4 pack8_at(const float *f) {
 }
 
 // ============================================================== prep kernel
-template <int KK, int VV>
+// Offsets of the prep's shared memory; the parts after the g2 buffer depend on
+// dv (the v tile shares that buffer), which is a runtime argument.
+template <int KK>
 struct PrepSmem {
     static constexpr int kGS = KK + 4;                          // padded fp32 row of g2
     // The kb / previous-kg tile is K-major with its core matrices 144 bytes apart
@@ -144,26 +146,34 @@ struct PrepSmem {
     static constexpr uint32_t kbx = ag + 128 * KK * 2;          // [128][KK] padded: kb; kg of the previous chunk
     static constexpr uint32_t g = kbx + 16 * kSbo;              // fp32 [64][kGS] g2; later v tile + AB tile
     static constexpr uint32_t g_need0 = 64 * kGS * 4;
-    static constexpr uint32_t g_need1 = 64 * VV * 2 + 64 * 64 * 2;
-    static constexpr uint32_t g_bytes = g_need0 > g_need1 ? g_need0 : g_need1;
-    static constexpr uint32_t extra = g + g_bytes;
+    __host__ __device__ static constexpr uint32_t g_bytes(int VV) {
+        return g_need0 > 64u * VV * 2 + 64 * 64 * 2 ? g_need0 : 64u * VV * 2 + 64 * 64 * 2;
+    }
+    __host__ __device__ static constexpr uint32_t extra(int VV) { return g + g_bytes(VV); }
     // After the gram MMA: L fp32 [64][64], T fp32 [32][32], P bf16 tile [64][64],
     // Akk fp32 [64][64].  dk = 128 reuses the kb tile and the qg rows for them.
     static constexpr bool big = KK == 128;
-    static constexpr uint32_t lbuf = big ? kbx : extra;
-    static constexpr uint32_t tbuf = lbuf + 64 * 64 * 4;
-    static constexpr uint32_t pbuf = tbuf + 32 * 32 * 4;
-    static constexpr uint32_t abuf = big ? ag : pbuf + 64 * 64 * 2;
-    static constexpr uint32_t used = big ? extra : abuf + 64 * 64 * 4;
-    static_assert(!big || pbuf + 64 * 64 * 2 <= g, "solve scratch overflows the kb tile");
+    __host__ __device__ static constexpr uint32_t lbuf(int VV) { return big ? kbx : extra(VV); }
+    __host__ __device__ static constexpr uint32_t tbuf(int VV) { return lbuf(VV) + 64 * 64 * 4; }
+    __host__ __device__ static constexpr uint32_t pbuf(int VV) { return tbuf(VV) + 32 * 32 * 4; }
+    __host__ __device__ static constexpr uint32_t abuf(int VV) {
+        return big ? ag : pbuf(VV) + 64 * 64 * 2;
+    }
+    __host__ __device__ static constexpr uint32_t used(int VV) {
+        return big ? extra(VV) : abuf(VV) + 64 * 64 * 4;
+    }
+    static_assert(!big || kbx + 64 * 64 * 4 + 32 * 32 * 4 + 64 * 64 * 2 <= g,
+                  "solve scratch overflows the kb tile");
     // Floor so that at most two CTAs (256 TMEM columns each) share an SM.
-    static constexpr uint32_t total = used > 80 * 1024 ? used : 80 * 1024;
+    __host__ __device__ static constexpr uint32_t total(int VV) {
+        return used(VV) > 80 * 1024 ? used(VV) : 80 * 1024;
+    }
 };
 
 // Byte offset of element (r, c) in the padded kb tile.
 template <int KK>
 __device__ __forceinline__ uint32_t kbx_off(int r, int c) {
-    return (uint32_t)((r >> 3) * PrepSmem<KK, 32>::kSbo + (c >> 3) * PrepSmem<KK, 32>::kLbo +
+    return (uint32_t)((r >> 3) * PrepSmem<KK>::kSbo + (c >> 3) * PrepSmem<KK>::kLbo +
                       (r & 7) * 16 + (c & 7) * 2);
 }
 
@@ -204,9 +214,11 @@ __device__ __forceinline__ void strip16(float4 &s, const float *P, int pr, int p
 }
 __device__ __forceinline__ float4 neg4(float4 v) { return make_float4(-v.x, -v.y, -v.z, -v.w); }
 
-template <int KK, int VV>
+// ACT: the gate activation (kda_activation.A_log) is compiled in.
+template <int KK, bool ACT>
 __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
-    using S = PrepSmem<KK, VV>;
+    using S = PrepSmem<KK>;
+    const int VV = p.V;
     extern __shared__ __align__(1024) unsigned char sm[];
     __shared__ float sBeta[64];
     __shared__ float sDprev[128];
@@ -225,10 +237,10 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
     float *sG2 = reinterpret_cast<float *>(sm + S::g);
     unsigned char *sV = sm + S::g;                          // after the elementwise phase
     unsigned char *sAB = sm + S::g + 64 * VV * 2;           // (8 KB before it valid)
-    float *sL = reinterpret_cast<float *>(sm + S::lbuf);    // after the gram MMA
-    float *sT = reinterpret_cast<float *>(sm + S::tbuf);
-    unsigned char *sPB = sm + S::pbuf;
-    float *sA = reinterpret_cast<float *>(sm + S::abuf);
+    float *sL = reinterpret_cast<float *>(sm + S::lbuf(VV));    // after the gram MMA
+    float *sT = reinterpret_cast<float *>(sm + S::tbuf(VV));
+    unsigned char *sPB = sm + S::pbuf(VV);
+    float *sA = reinterpret_cast<float *>(sm + S::abuf(VV));
 
     const TcLayout Lo = tc_layout(KK, VV);
     if (warp == 0) {
@@ -276,10 +288,16 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
     const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(p.v);
     const __nv_bfloat16 *beta = static_cast<const __nv_bfloat16 *>(p.beta);
     const size_t row0 = (size_t)b * p.T + r0;
-    constexpr int VG8 = VV / 8;
+    const int VG8 = VV / 8;
     // beta in a register now, into shared memory after the gates: its load
     // latency overlaps everything up to there
-    const float bet = (tid < 64 && tid < nr) ? to_f32(beta[(row0 + tid) * p.HV + hv]) : 0.f;
+    float bet = (tid < 64 && tid < nr) ? to_f32(beta[(row0 + tid) * p.HV + hv]) : 0.f;
+    if (p.act.beta_scale > 0.f && tid < 64 && tid < nr)
+        bet = beta_activate<__nv_bfloat16>(bet, p.act.beta_scale);
+    // the gate activation's per-channel constants (thread d and 128 + d: channel d)
+    constexpr bool gate_act = ACT;
+    const float neg_a = gate_act ? gate_neg_a(p.act, hv) : 0.f;
+    const float gbias = gate_act && (tid & 127) < KK ? gate_bias(p.act, hv, tid & 127, KK) : 0.f;
 #pragma unroll
     for (int it = 0; it < KK / 32; ++it) {
         const int idx = tid + it * 256, l = idx & 31, w = idx >> 5;
@@ -315,6 +333,10 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
         float gr[64];
 #pragma unroll
         for (int j = 0; j < 64; ++j) gr[j] = __ldg(gp + (j < nr ? j : nr - 1) * grs);
+        if (gate_act) {
+#pragma unroll
+            for (int j = 0; j < 64; ++j) gr[j] = neg_a * softplus_f(gr[j] + gbias);
+        }
         float acc = 0.f, rng = 0.f;
 #pragma unroll
         for (int i = 0; i < 64; ++i) {
@@ -334,6 +356,10 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
         float ex[64];  // exponents G' - g2'_j
 #pragma unroll
         for (int j = 0; j < 64; ++j) ex[j] = __ldg(gp + j * grs);
+        if (gate_act) {
+#pragma unroll
+            for (int j = 0; j < 64; ++j) ex[j] = neg_a * softplus_f(ex[j] + gbias);
+        }
         float Gp;
         if (p.g_is_cumsum) {
             Gp = ex[63];
@@ -1353,44 +1379,48 @@ __global__ void __launch_bounds__(256) chunk_fix_tc_kernel(ChunkArgs p) {
     if (warp == 0) tmem_dealloc(tmem, S::tmem_cols);
 }
 
-template <int KK, int VV>
-cudaError_t launch_prep(const ChunkArgs &a, cudaStream_t st) {
-    using S = PrepSmem<KK, VV>;
+template <int KK, bool ACT>
+cudaError_t launch_prep_t(const ChunkArgs &a, cudaStream_t st) {
+    using S = PrepSmem<KK>;
     static bool attr = false;
+    static int sms = 0, regs_sm = 0, smem_sm = 0;
+    static cudaFuncAttributes fa;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(chunk_prep_tc_kernel<KK, VV>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::total);
+        cudaError_t e = cudaFuncSetAttribute(chunk_prep_tc_kernel<KK, ACT>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)S::total(256));
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(chunk_prep_tc_kernel<KK, VV>,
+            e = cudaFuncSetAttribute(chunk_prep_tc_kernel<KK, ACT>,
                                      cudaFuncAttributePreferredSharedMemoryCarveout,
                                      (int)cudaSharedmemCarveoutMaxShared);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
-    static int ctas = 0;  // resident CTAs on the device
-    if (ctas == 0) {
-        // From the kernel's registers and shared memory (TMEM: 256 columns per
-        // CTA, at most two per SM).
-        int dev = 0, sms = 0, regs_sm = 0, smem_sm = 0;
-        cudaFuncAttributes fa;
-        cudaError_t e = cudaGetDevice(&dev);
+        int dev = 0;
+        if (e == cudaSuccess) e = cudaGetDevice(&dev);
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev);
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
-        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, chunk_prep_tc_kernel<KK, VV>);
+        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, chunk_prep_tc_kernel<KK, ACT>);
         if (e != cudaSuccess) return e;
-        const int by_regs = regs_sm / (((fa.numRegs + 7) / 8 * 8) * 256);
-        const int by_smem = smem_sm / (int)(S::total + fa.sharedSizeBytes + 1024);
-        int per_sm = by_regs < by_smem ? by_regs : by_smem;
-        per_sm = per_sm < 1 ? 1 : (per_sm > 2 ? 2 : per_sm);
-        ctas = sms * per_sm;
+        attr = true;
     }
+    // Resident CTAs, from the kernel's registers and this dv's shared memory
+    // (TMEM: 256 columns per CTA, at most two per SM).
+    const uint32_t smem = S::total(a.V);
+    const int by_regs = regs_sm / (((fa.numRegs + 7) / 8 * 8) * 256);
+    const int by_smem = smem_sm / (int)(smem + fa.sharedSizeBytes + 1024);
+    int per_sm = by_regs < by_smem ? by_regs : by_smem;
+    per_sm = per_sm < 1 ? 1 : (per_sm > 2 ? 2 : per_sm);
+    const int64_t ctas = (int64_t)sms * per_sm;
     const int64_t units = a.slots * a.HV;
     const unsigned grid = (unsigned)(units < ctas ? units : ctas);
     prof_begin("chunk_prep_tc", st);
-    chunk_prep_tc_kernel<KK, VV><<<grid, 256, S::total, st>>>(a);
+    chunk_prep_tc_kernel<KK, ACT><<<grid, 256, smem, st>>>(a);
     prof_end(st);
     return cudaGetLastError();
+}
+
+template <int KK>
+cudaError_t launch_prep(const ChunkArgs &a, cudaStream_t st) {
+    return a.act.A_log ? launch_prep_t<KK, true>(a, st) : launch_prep_t<KK, false>(a, st);
 }
 
 template <int KK, int SBV>
@@ -1443,7 +1473,7 @@ cudaError_t launch_fix(const ChunkArgs &a, cudaStream_t st) {
 template <int KK, int VV>
 cudaError_t launch_kv(const ChunkArgs &a, cudaStream_t st) {
     cudaError_t e = cudaSuccess;
-    if (a.slots > 0 && (e = launch_prep<KK, VV>(a, st)) != cudaSuccess) return e;
+    if (a.slots > 0 && (e = launch_prep<KK>(a, st)) != cudaSuccess) return e;
     if (!a.split) return launch_scan<KK, 32>(a, st);
     if ((e = launch_scan<KK, 64>(a, st)) != cudaSuccess) return e;
     if constexpr (VV % 64 == 0) return launch_fix<KK, VV>(a, st);

@@ -24,7 +24,7 @@ __global__ void __launch_bounds__(128) gate_cumsum_kernel(const float *__restric
                                                           float *__restrict__ out,
                                                           const int32_t *__restrict__ cu,
                                                           int B, int T, int HV, int K, int N,
-                                                          int chunk, float g_scale) {
+                                                          int chunk, float g_scale, GateAct act) {
     __shared__ int seg_start[kTile];
     __shared__ int row_valid[kTile];
     const int tiles = (T + kTile - 1) / kTile;
@@ -61,13 +61,21 @@ __global__ void __launch_bounds__(128) gate_cumsum_kernel(const float *__restric
     const float *gb = g + ((size_t)b * T) * rstride + (size_t)hv * K;
     float *ob = out + ((size_t)b * T) * rstride + (size_t)hv * K;
     for (int d = threadIdx.x; d < K; d += blockDim.x) {
+        // the gate of row u: g itself, or the activated -exp(A_log) softplus(g + dt_bias)
+        const bool activate = act.A_log != nullptr;
+        const float neg_a = activate ? gate_neg_a(act, hv) : 0.f;
+        const float bias = activate ? gate_bias(act, hv, d, K) : 0.f;
+        auto gate = [&](int u) {
+            const float x = gb[(size_t)u * rstride + d];
+            return activate ? neg_a * softplus_f(x + bias) : x;
+        };
         float acc = 0.f;
-        for (int u = seg_start[0]; u < t0; ++u) acc += gb[(size_t)u * rstride + d];
+        for (int u = seg_start[0]; u < t0; ++u) acc += gate(u);
         for (int i = 0; i < kTile; ++i) {
             if (!row_valid[i]) break;  // rows past the end of the valid range
             const int t = t0 + i;
             if (seg_start[i] == t) acc = 0.f;
-            acc += gb[(size_t)t * rstride + d];
+            acc += gate(t);
             ob[(size_t)t * rstride + d] = g_scale * acc;
         }
     }
@@ -138,14 +146,14 @@ cudaError_t launch_validate_offsets(const int32_t *cu, int N, int T, int32_t *de
 }
 
 cudaError_t launch_gate_cumsum(const float *g, float *out, const int32_t *cu, const kda_shape &s,
-                               int chunk, cudaStream_t st) {
+                               const GateAct &act, int chunk, cudaStream_t st) {
     const int tiles = (s.T + kTile - 1) / kTile;
     const int rows = cu ? s.HV : s.B * s.HV;
     if (tiles == 0 || rows == 0) return cudaSuccess;
     const int64_t blocks = (int64_t)tiles * rows;  // flattened onto grid x
     prof_begin("gate_cumsum", st);
     gate_cumsum_kernel<<<(unsigned)blocks, 128, 0, st>>>(g, out, cu, s.B, s.T, s.HV, s.K,
-                                                         s.num_seqs, chunk, s.g_scale);
+                                                         s.num_seqs, chunk, s.g_scale, act);
     prof_end(st);
     return cudaGetLastError();
 }

@@ -74,7 +74,28 @@ void prof_end(cudaStream_t st);
 cudaError_t launch_validate_offsets(const int32_t *cu, int N, int T, int32_t *dev_status,
                                     ChunkCtrl *ctrl, int32_t *chunk_start, cudaStream_t st);
 
+// Input activations (kda_activation): the natural-log gate
+// -exp(A_log[hv]) softplus(g + dt_bias[hv, d]) in g's place when A_log is set,
+// beta = sigmoid(x) * beta_scale rounded to the input dtype when beta_scale > 0.
+struct GateAct {
+    const float *A_log = nullptr;
+    const float *dt_bias = nullptr;
+    float beta_scale = 0.f;
+};
+__device__ __forceinline__ float softplus_f(float x) { return x > 20.f ? x : log1pf(expf(x)); }
+// -exp(A_log[hv]) for the channel loop of one value head
+__device__ __forceinline__ float gate_neg_a(const GateAct &a, int hv) { return -expf(a.A_log[hv]); }
+__device__ __forceinline__ float gate_bias(const GateAct &a, int hv, int d, int K) {
+    return a.dt_bias ? a.dt_bias[(size_t)hv * K + d] : 0.f;
+}
+template <typename T>
+__device__ __forceinline__ float beta_activate(float x, float s) {
+    const float y = s / (1.f + expf(-x));
+    return to_f32(from_f32<T>(y));
+}
+
 cudaError_t launch_gate_cumsum(const float *g, float *out, const int32_t *cu, const kda_shape &s,
+                               const GateAct &act,
                                int chunk, cudaStream_t st);
 
 struct RecurrentArgs {
@@ -89,6 +110,7 @@ struct RecurrentArgs {
     int B, T, H, HV, K, V, N;
     float scale, g_scale;
     int l2norm;
+    GateAct act;
 };
 cudaError_t launch_recurrent(const RecurrentArgs &a, kda_dtype dt, cudaStream_t st);
 
@@ -110,6 +132,7 @@ struct ChunkArgs {
     void *units;           // per-(chunk, value head) intermediates
     int64_t slots;         // chunk slots (upper bound)
     // split sequences (tensor-core path): see chunk_tc_split
+    GateAct act;
     int split;
     void *qc;              // [slots][HV][64][K] bf16: segment 1's Q_c operand tiles
     float *e0, *e1;        // [N][HV][K][V] fp32: the segments' final states from zero / h0

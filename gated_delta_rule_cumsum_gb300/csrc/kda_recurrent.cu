@@ -95,7 +95,11 @@ __global__ void __launch_bounds__(512) recurrent_kernel(RecurrentArgs p) {
     const int dl = d0 + lane;  // the row lanes 0..15 fetch
     const bool row_lane = lane < kRows && dl < p.K;
 
-    // Inputs of token t, fetched one token ahead.
+    // Inputs of token t, fetched one token ahead (the activations applied as they
+    // arrive: the gate's per-channel constants are loaded once).
+    const bool gate_act = p.act.A_log != nullptr;
+    const float neg_a = gate_act ? gate_neg_a(p.act, hv) : 0.f;
+    const float gbias = gate_act && row_lane ? gate_bias(p.act, hv, dl, p.K) : 0.f;
     float kr = 0.f, qr = 0.f, gr = 0.f, vv[kCols] = {0.f, 0.f, 0.f, 0.f}, bt = 0.f;
     auto fetch = [&](int t) {
         const size_t row = (size_t)b * p.T + t;
@@ -103,11 +107,13 @@ __global__ void __launch_bounds__(512) recurrent_kernel(RecurrentArgs p) {
             kr = to_f32(k[(row * p.H + h) * p.K + dl]);
             qr = to_f32(q[(row * p.H + h) * p.K + dl]);
             gr = p.g[(row * p.HV + hv) * p.K + dl];
+            if (gate_act) gr = neg_a * softplus_f(gr + gbias);
         }
         const size_t vrow = (row * p.HV + hv) * p.V;
 #pragma unroll
         for (int j = 0; j < kCols; ++j) vv[j] = (c0 + j < p.V) ? to_f32(v[vrow + c0 + j]) : 0.f;
         bt = to_f32(beta[row * p.HV + hv]);
+        if (p.act.beta_scale > 0.f) bt = beta_activate<T>(bt, p.act.beta_scale);
     };
     if (bos < eos) fetch(bos);
 

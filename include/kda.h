@@ -16,6 +16,8 @@
  *   kda_gate_cumsum    chunk-local gate cumsum (ALGORITHM.md, Stage 1)
  *   kda_chunk_fwd      chunked forward, BT = 64 (ALGORITHM.md, Stages 1-4)
  *   kda_recurrent_fwd  token-by-token forward for decode (PR #317)
+ * each also as an *_act variant that applies the gate and beta activations to
+ * raw inputs inside the op (kda_activation below).
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -112,6 +114,32 @@ typedef struct {
 } kda_shape;
 
 /*
+ * Input activations applied inside the op (the *_act entry points).  Defined in
+ * kernel-fun 0.2.0.dev1 wheel, kda/chain.py, gate_cumsum, and kda/ops.py,
+ * chunk_kda (use_gate_in_kernel, use_beta_sigmoid_in_kernel, allow_neg_eigval);
+ * sdist ALGORITHM.md, "Stage 1" note on the fused gate activation.
+ *   A_log       [HV] fp32 device pointer, or NULL.  When set, g holds the raw
+ *               gate pre-activation and the op uses, in g's place, the
+ *               natural-log decay
+ *                   -exp(A_log[hv]) * softplus(g[t, hv, d] + dt_bias[hv, d])
+ *               (times shape->g_scale as always: 1/ln 2 for this form).
+ *               softplus(x) = ln(1 + e^x), evaluated as x itself above 20.
+ *   dt_bias     [HV, K] fp32 device pointer, or NULL (no bias); needs A_log.
+ *   beta_scale  0: beta is the gate as given.  > 0: beta holds logits and the
+ *               op uses sigmoid(beta) * beta_scale (1, or 2 to allow negative
+ *               eigenvalues), rounded to the input dtype as the pages cast it to
+ *               q's dtype.
+ * The pages' lower_bound option has no formula there and is not provided.
+ * A NULL kda_activation, or one with A_log == NULL and beta_scale == 0, is the
+ * plain op.  The activation cannot be combined with KDA_FLAG_G_IS_CUMSUM.
+ */
+typedef struct {
+    const float *A_log;
+    const float *dt_bias;
+    float beta_scale;
+} kda_activation;
+
+/*
  * kda_gate_cumsum -- chunk-local inclusive cumsum of the gate.
  * Defined in kernel-fun 0.2.0.dev1 sdist, ALGORITHM.md, "Stage 1 -- cumsum":
  *     g_cum[t, hv, d] = g_scale * sum_{s = c(t)}^{t} g[s, hv, d]
@@ -127,6 +155,11 @@ typedef struct {
 kda_status kda_gate_cumsum(const float *g, float *g_cum, const int32_t *cu_seqlens,
                            const kda_shape *shape, int32_t chunk_size, int32_t *dev_status,
                            kda_stream_t stream);
+/* kda_gate_cumsum with the gate activation of *act applied to g first (its
+ * beta_scale is ignored). */
+kda_status kda_gate_cumsum_act(const float *g, float *g_cum, const int32_t *cu_seqlens,
+                               const kda_shape *shape, const kda_activation *act,
+                               int32_t chunk_size, int32_t *dev_status, kda_stream_t stream);
 
 /*
  * kda_chunk_fwd -- the chunked forward with chunks of BT = 64 rows.
@@ -151,6 +184,12 @@ kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const floa
                          const void *beta, const float *h0, const int32_t *cu_seqlens,
                          const kda_shape *shape, void *o, float *ht, void *workspace,
                          size_t workspace_bytes, int32_t *dev_status, kda_stream_t stream);
+/* kda_chunk_fwd on raw g / beta with the activations of *act (see above). */
+kda_status kda_chunk_fwd_act(const void *q, const void *k, const void *v, const float *g,
+                             const void *beta, const float *h0, const int32_t *cu_seqlens,
+                             const kda_shape *shape, const kda_activation *act, void *o,
+                             float *ht, void *workspace, size_t workspace_bytes,
+                             int32_t *dev_status, kda_stream_t stream);
 
 /* Bytes of workspace kda_chunk_fwd needs for *shape (0 on invalid shapes). */
 size_t kda_chunk_workspace_size(const kda_shape *shape);
@@ -196,6 +235,11 @@ kda_status kda_recurrent_fwd(const void *q, const void *k, const void *v, const 
                              const void *beta, const float *h0, const int32_t *cu_seqlens,
                              const kda_shape *shape, void *o, float *ht, int32_t *dev_status,
                              kda_stream_t stream);
+/* kda_recurrent_fwd on raw g / beta with the activations of *act (see above). */
+kda_status kda_recurrent_fwd_act(const void *q, const void *k, const void *v, const float *g,
+                                 const void *beta, const float *h0, const int32_t *cu_seqlens,
+                                 const kda_shape *shape, const kda_activation *act, void *o,
+                                 float *ht, int32_t *dev_status, kda_stream_t stream);
 
 /*
  * kda_read_device_status -- synchronise `stream`, copy the status word to

@@ -14,6 +14,9 @@ Two independent formulations live here:
   "Stage 1 -- cumsum".
 * `chunk_form.chunk_forward` -- the chunked (WY / UT-transform) formulation of
   ALGORITHM.md "Stage 1" through "Stage 3+4", in numpy fp64.
+* `activation` -- the optional input activations (gate -exp(A_log) softplus(g +
+  dt_bias), beta sigmoid) of kernel-fun 0.2.0.dev1 wheel, kda/chain.py and
+  kda/ops.py, in numpy fp64; pinned in tests/test_oracle_activation.py.
 
 Each pins the other (tests/test_oracle_pins.py), beside closed forms, invariants
 and brute force that the pages and the mathematics fix.

@@ -141,6 +141,33 @@ def test_split_scan_flag_sizes_a_larger_workspace(lib):
             == lib.kda_chunk_workspace_size(ctypes.byref(_shape(**f32))))
 
 
+@pytest.mark.parametrize("case", ["bias_without_a", "negative_beta_scale", "nan_beta_scale",
+                                  "act_with_cumsum_input"])
+def test_activation_arguments_rejected_on_host(lib, case):
+    import gated_delta_rule_cumsum_gb300 as kda
+
+    act = kda.KdaActivation(FAKE.value, FAKE.value, 0.0)
+    flags = 0
+    if case == "bias_without_a":
+        act.A_log = None
+    elif case == "negative_beta_scale":
+        act.beta_scale = -1.0
+    elif case == "nan_beta_scale":
+        act.beta_scale = float("nan")
+    else:
+        flags = kda.KDA_FLAG_G_IS_CUMSUM
+    s = _shape(flags=flags)
+    st = lib.kda_chunk_fwd_act(FAKE, FAKE, FAKE, FAKE, FAKE, None, None, ctypes.byref(s),
+                               ctypes.byref(act), FAKE, None, FAKE, 1 << 30, None, None)
+    assert st == 1, lib.kda_last_error_message()
+    if case != "act_with_cumsum_input":
+        assert lib.kda_recurrent_fwd_act(FAKE, FAKE, FAKE, FAKE, FAKE, None, None,
+                                         ctypes.byref(_shape()), ctypes.byref(act), FAKE, None,
+                                         None, None) == 1
+        assert lib.kda_gate_cumsum_act(FAKE, ctypes.c_void_p(0x2000), None, ctypes.byref(_shape()),
+                                       ctypes.byref(act), 64, None, None) == 1
+
+
 def test_workspace_size_scales_with_chunks(lib):
     a = lib.kda_chunk_workspace_size(ctypes.byref(_shape(T=64)))
     b = lib.kda_chunk_workspace_size(ctypes.byref(_shape(T=640)))
