@@ -9,11 +9,16 @@ HBM before the timed region; a 512 MiB buffer is written between timed steps
 to flush the 129 MB L2.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload train|gva|packed|decode|prefill]
 
-`--impl reference` times the fp64 CPU oracle instead, on the host cores, each
-step a bounded sample of the same workload.  Under torchrun (N > 1) every rank
-runs its own replica of the workload (weak scaling, no collective on the data
-path); rank 0 prints the line with the max-over-ranks time.
+`--workload` picks one of the other synthetic workloads instead (grouped value
+heads B4 T4096 HV32; packed varlen H=HV=32; decode 4096 x 1 token; its
+256-token prefill variant); decode and prefill steps are one in-place
+`kda_recurrent_fwd` call.  `--impl reference` times the fp64 CPU oracle
+instead, on the host cores, each step a bounded sample of the same workload.
+Under torchrun (N > 1) every rank runs its own replica of the workload (weak
+scaling, no collective on the data path); rank 0 prints the line with the
+max-over-ranks time.
 """
 from __future__ import annotations
 
@@ -33,8 +38,32 @@ sys.path.insert(0, ROOT)
 
 METRIC = "chunk_kda fwd tokens/s (T=8192,HV=16,K=V=128,bf16) and % of roofline on 1 GB300"
 UNIT = "tokens/s"
-WORKLOAD = 1
 FLUSH_BYTES = 512 << 20
+# name -> (kda_synth workload, overrides, default steps, default warm-up)
+WORKLOADS = {
+    "train": (1, {}, 2000, 20),
+    "gva": (2, {}, 500, 10),
+    "packed": (3, {}, 300, 10),
+    "decode": (4, {}, 100, 5),
+    "prefill": (4, {"T": 256}, 10, 3),
+}
+RECURRENT = ("decode", "prefill")
+FP32_LANES_PER_SM = 128      # fp32 FMA lanes per SM (4 partitions x 32)
+E2E_MAX_H2D = 8 << 30        # larger inputs are not staged through pinned host memory
+
+
+def _metric(name, w):
+    if name == "train":
+        return METRIC
+    op = "recurrent_kda" if name in RECURRENT else "chunk_kda"
+    return f"{op} fwd tokens/s ({w.name}) on 1 GB300"
+
+
+def _make_inputs(name, device):
+    import kda_synth
+
+    idx, over, _, _ = WORKLOADS[name]
+    return kda_synth.make_inputs(kda_synth.workload(idx, **over), device=device)
 
 
 def _env_int(name, default):
@@ -50,8 +79,14 @@ def _peaks():
         with open(path) as f:
             p = json.load(f)
         return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
-                "source": "measured"}
-    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+                "sm_max_mhz": float(p.get("sm_max_mhz", 2070.0)), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "sm_max_mhz": 2070.0,
+            "source": "fallback"}
+
+
+def fp32_fma_tflops(sms, sm_mhz):
+    """Plain fp32 FMA peak: SMs x 128 lanes x 2 flops per FMA x SM clock."""
+    return sms * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12
 
 
 # ------------------------------------------------------------------ ranks
@@ -96,9 +131,17 @@ def kernel_algorithmic_bytes(name, inp):
         return r - state_in
     if name.startswith("chunk_scan"):
         return wr + state_in
-    if name.startswith("chunk_fused"):
+    if name.startswith("chunk_fused") or name == "recurrent":
         return r + wr
     return 0
+
+
+def recurrent_flops(inp):
+    """fp32 flops of the token recurrence: per (token, value head) two K x V
+    reductions over the old state (2 flops per element each) and the decayed
+    rank-1 update (a multiply and an FMA per element): 7 K V."""
+    w = inp["workload"]
+    return 7 * inp["tokens"] * w.HV * w.K * w.V
 
 
 # ------------------------------------------------------------------ clocks
@@ -195,62 +238,104 @@ def _traffic(kernel):
 
 
 # ------------------------------------------------------------------ CPU oracle
-def cpu_oracle_rate(inp_cpu, budget_s=12.0, max_tokens=None):
-    """Oracle tokens/s on the first L tokens (all heads) of the workload."""
+def oracle_sample(inp, max_tokens):
+    """The first sequences (or, for one long sequence, the first tokens) of the
+    workload, up to about `max_tokens` tokens, sliced where the inputs live and
+    then copied to the host.  Returns (inputs for oracle.recurrent, tokens, text)."""
+    q, k, v, g, beta, h0, cu = (inp[n] for n in ("q", "k", "v", "g", "beta", "h0", "cu_seqlens"))
+    B, T = q.shape[0], q.shape[1]
+    if cu is not None:
+        offs = cu.cpu().tolist()
+        s = 1
+        while s < len(offs) - 1 and (offs[s + 1] <= max_tokens or offs[s] == 0):
+            s += 1
+        L = offs[s]
+        part = dict(q=q[:, :L], k=k[:, :L], v=v[:, :L], g=g[:, :L], beta=beta[:, :L],
+                    h0=None if h0 is None else h0[:s], cu_seqlens=cu[: s + 1])
+        text = f"first {s} of {len(offs) - 1} sequence slots ({L} tokens)"
+    else:
+        nb = max(1, min(B, max_tokens // T))
+        L = min(T, max(1, max_tokens)) if nb == 1 else T
+        part = dict(q=q[:nb, :L], k=k[:nb, :L], v=v[:nb, :L], g=g[:nb, :L], beta=beta[:nb, :L],
+                    h0=None if h0 is None else h0[:nb], cu_seqlens=None)
+        L = nb * L
+        text = (f"first {nb} of {B} sequences" if nb > 1 or B > 1 else "sequence") + \
+            f", {L} tokens"
+    part = {n: (None if t is None else t.cpu()) for n, t in part.items()}
+    return part, L, text
+
+
+def _oracle_run(part):
     import oracle
 
-    q, k, v, g, beta = (inp_cpu[n] for n in ("q", "k", "v", "g", "beta"))
-    T = q.shape[1]
-    L = min(T, max_tokens or T)
-    sl = lambda t: t[:, :L]
-    oracle.recurrent(sl(q)[:, :16], sl(k)[:, :16], sl(v)[:, :16], sl(g)[:, :16],
-                     sl(beta)[:, :16], want_state=False)  # warm (loads the library)
-    runs, t_total, toks = 0, 0.0, 0
-    while t_total < budget_s or runs == 0:
+    oracle.recurrent(part["q"], part["k"], part["v"], part["g"], part["beta"], h0=part["h0"],
+                     cu_seqlens=part["cu_seqlens"])
+
+
+def cpu_oracle_rate(inp, budget_s=10.0, max_runs=3):
+    """Oracle tokens/s on a bounded sample of the workload sized to ~budget_s of
+    CPU work (all value heads of the sampled sequences)."""
+    import oracle
+
+    probe, pL, _ = oracle_sample(inp, 64)
+    t0 = time.perf_counter()
+    _oracle_run(probe)  # also loads the library
+    t0 = time.perf_counter()
+    _oracle_run(probe)
+    probe_rate = pL / max(1e-6, time.perf_counter() - t0)
+    part, L, text = oracle_sample(inp, int(max(64, probe_rate * budget_s / max_runs)))
+    runs, t_total = 0, 0.0
+    while runs < max_runs and (t_total < budget_s or runs == 0):
         t0 = time.perf_counter()
-        oracle.recurrent(sl(q), sl(k), sl(v), sl(g), sl(beta), h0=inp_cpu["h0"])
+        _oracle_run(part)
         t_total += time.perf_counter() - t0
-        toks += L * q.shape[0]
         runs += 1
-        if runs >= 3:
-            break
-    return toks / t_total, runs, L, oracle.num_threads()
+    return L * runs / t_total, runs, text, oracle.num_threads()
 
 
 def run_reference(args):
     """The oracle as the reference arm: each step one bounded sample."""
     import torch  # noqa: F401
 
-    import kda_synth
-
     rank = _env_int("RANK", 0)
     if rank != 0:
         return 0
-    inp = kda_synth.make_inputs(WORKLOAD, device="cpu")
+    if args.workload in RECURRENT:
+        # The same distributions drawn for 64 sequences: the sample never needs more.
+        import kda_synth
+
+        idx, over, _, _ = WORKLOADS[args.workload]
+        inp = kda_synth.make_inputs(kda_synth.workload(idx, **over, B=64, decode_seqs=64), "cpu")
+    else:
+        inp = _make_inputs(args.workload, "cpu")
+    w = inp["workload"]
     # Size a step so that warm-up + steps end within ~2 minutes.
-    probe_rate, _, _, cores = cpu_oracle_rate(inp, budget_s=0.0, max_tokens=256)
+    probe, pL, _ = oracle_sample(inp, 256)
+    _oracle_run(probe)
+    t0 = time.perf_counter()
+    _oracle_run(probe)
+    probe_rate = pL / max(1e-6, time.perf_counter() - t0)
     per_step_s = max(0.02, 120.0 / max(1, args.steps + args.warmup))
-    L = int(max(16, min(inp["q"].shape[1], probe_rate * per_step_s)))
+    part, L, text = oracle_sample(inp, int(max(16, probe_rate * per_step_s)))
     import oracle
 
-    sl = lambda t: t[:, :L]
     for _ in range(args.warmup):
-        oracle.recurrent(sl(inp["q"]), sl(inp["k"]), sl(inp["v"]), sl(inp["g"]), sl(inp["beta"]))
+        _oracle_run(part)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.recurrent(sl(inp["q"]), sl(inp["k"]), sl(inp["v"]), sl(inp["g"]), sl(inp["beta"]))
+        _oracle_run(part)
     dt = time.perf_counter() - t0
     ms = 1e3 * dt / max(1, args.steps)
     value = L / (ms / 1e3)
-    w = inp["workload"]
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "impl": "reference", "metric": _metric(args.workload, w), "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "HV": w.HV, "K": w.K,
                    "V": w.V, "input_dtype": "bf16", "sample_tokens_per_step": L},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": f"first {L} of {w.T} tokens, all {w.HV} heads, per step"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": f"{text}, all {w.HV} heads, per step"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -262,7 +347,6 @@ def run_ours(args):
     import torch
 
     import gated_delta_rule_cumsum_gb300 as kda
-    import kda_synth
 
     world = _env_int("WORLD_SIZE", 1)
     rank = _env_int("RANK", 0)
@@ -285,19 +369,30 @@ def run_ours(args):
         dist.barrier()
     kda.load()
 
-    inp = kda_synth.make_inputs(WORKLOAD, device=dev)
+    inp = _make_inputs(args.workload, dev)
     w = inp["workload"]
+    recurrent = args.workload in RECURRENT
     q, k, v, g, beta, h0, cu = (inp[n] for n in ("q", "k", "v", "g", "beta", "h0", "cu_seqlens"))
     shape = kda.make_shape(q, v, cu)
     o = torch.empty_like(v)
-    ht = torch.empty(inp["N"], w.HV, w.K, w.V, dtype=torch.float32, device=dev)
-    ws = torch.empty(kda.kda_chunk_workspace_size(shape), dtype=torch.uint8, device=dev)
     status = kda.new_status(dev)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
+    if recurrent:
+        # Decode keeps the state resident and updates it in place (ht == h0).
+        ht, ws = h0, None
+
+        def call(q_, k_, v_, g_, beta_, h0_, o_, ht_, st):
+            kda.kda_recurrent_fwd(q_, k_, v_, g_, beta_, h0_, cu, shape, o_, ht_, status, st)
+    else:
+        ht = torch.empty(inp["N"], w.HV, w.K, w.V, dtype=torch.float32, device=dev)
+        ws = torch.empty(kda.kda_chunk_workspace_size(shape), dtype=torch.uint8, device=dev)
+
+        def call(q_, k_, v_, g_, beta_, h0_, o_, ht_, st):
+            kda.kda_chunk_fwd(q_, k_, v_, g_, beta_, h0_, cu, shape, o_, ht_, ws, status, st)
 
     def step():
-        kda.kda_chunk_fwd(q, k, v, g, beta, h0, cu, shape, o, ht, ws, status, stream)
+        call(q, k, v, g, beta, h0, o, ht, stream)
 
     for _ in range(args.warmup):
         flush.fill_(1.0)
@@ -347,90 +442,123 @@ def run_ours(args):
     dom_ms = per_kernel[dom][0] / per_kernel[dom][1]
     peaks = _peaks()
     dom_bytes = kernel_algorithmic_bytes(dom, inp)
-    achieved = dom_bytes / (dom_ms / 1e3) / 1e9
-    traffic = _traffic(dom)
+    traffic = _traffic(dom) if args.workload == "train" else None
     r_b, w_b = algorithmic_bytes(inp)
     path_gbs = (r_b + w_b) / (ms / 1e3) / 1e9
+    if args.workload == "prefill":
+        # 256 tokens per state: the recurrence's fp32 FMAs, not HBM, bound it.
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        peak = fp32_fma_tflops(sms, peaks["sm_max_mhz"])
+        flops = recurrent_flops(inp)
+        roofline = {"bound": "alu", "kernel": dom, "achieved": flops / (dom_ms / 1e3) / 1e12,
+                    "peak": peak, "unit": "TFLOP/s",
+                    "frac": flops / (dom_ms / 1e3) / 1e12 / peak, "traffic": traffic,
+                    "algorithmic_flops": flops, "kernel_ms": dom_ms,
+                    "peak_source": f"derived: {sms} SMs x {FP32_LANES_PER_SM} fp32 lanes x 2 "
+                                   f"x {peaks['sm_max_mhz']:.0f} MHz"}
+    else:
+        achieved = dom_bytes / (dom_ms / 1e3) / 1e9
+        roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved,
+                    "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                    "traffic": traffic, "algorithmic_bytes": dom_bytes,
+                    "kernel_ms": dom_ms, "peak_source": peaks["source"],
+                    "path_gbs": path_gbs, "path_frac": path_gbs / peaks["hbm_gbs"]}
 
     # End to end through the C ABI with host buffers: every step copies its inputs
-    # from pinned host memory, runs the call and reads o and the final state back.
-    # Pipelined: step i's H2D (copy stream) overlaps step i-1's call (compute
-    # stream) and step i-2's D2H (copy-back stream), with two sets of device
-    # inputs and outputs; events order each buffer's reuse.  The one-stream
-    # sequential time is reported beside it.
-    names = ("q", "k", "v", "g", "beta")
-    host = {n: inp[n].cpu().pin_memory() for n in names}
-    dev_in = [{n: torch.empty_like(inp[n]) for n in names} for _ in range(2)]
-    dev_o = [torch.empty_like(o) for _ in range(2)]
-    dev_ht = [torch.empty_like(ht) for _ in range(2)]
-    o_h = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for _ in range(2)]
-    ht_h = [torch.empty(ht.shape, dtype=ht.dtype, pin_memory=True) for _ in range(2)]
-    h2d = sum(_nbytes(t) for t in host.values())
-    d2h = _nbytes(o_h[0]) + _nbytes(ht_h[0])
-    e2e_steps = min(args.steps, 30)
-    s_up, s_down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    s_comp = torch.cuda.Stream(dev)
+    # from pinned host memory, runs the call and reads the results back (o and the
+    # final state; decode's state stays resident and is updated in place, so only
+    # o comes back).  Pipelined: step i's H2D (copy stream) overlaps step i-1's
+    # call (compute stream) and step i-2's D2H (copy-back stream), with two sets
+    # of device inputs and outputs; events order each buffer's reuse.  The
+    # one-stream sequential time is reported beside it.
+    names = ("q", "k", "v", "g", "beta") + (("h0",) if h0 is not None and not recurrent else ())
+    h2d = sum(_nbytes(inp[n]) for n in names)
+    e2e = None
+    if h2d > E2E_MAX_H2D:
+        e2e = {"value": None, "unit": UNIT,
+               "skipped": f"{h2d / 2**30:.1f} GiB of inputs per step exceed the "
+                          f"{E2E_MAX_H2D >> 30} GiB pinned staging limit"}
+    else:
+        host = {n: inp[n].cpu().pin_memory() for n in names}
+        dev_in = [{n: torch.empty_like(inp[n]) for n in names} for _ in range(2)]
+        dev_o = [torch.empty_like(o) for _ in range(2)]
+        dev_ht = [ht, ht] if recurrent else [torch.empty_like(ht) for _ in range(2)]
+        o_h = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for _ in range(2)]
+        ht_h = None if recurrent else \
+            [torch.empty(ht.shape, dtype=ht.dtype, pin_memory=True) for _ in range(2)]
+        d2h = _nbytes(o_h[0]) + (0 if recurrent else _nbytes(ht_h[0]))
+        e2e_steps = min(args.steps, 30)
+        s_up, s_down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        s_comp = torch.cuda.Stream(dev)
 
-    def run_pipeline(nsteps):
-        up_done = [torch.cuda.Event() for _ in range(nsteps)]
-        comp_done = [torch.cuda.Event() for _ in range(nsteps)]
-        down_done = [torch.cuda.Event() for _ in range(nsteps)]
-        for i in range(nsteps):
-            j = i % 2
-            with torch.cuda.stream(s_up):
-                if i >= 2:
-                    s_up.wait_event(comp_done[i - 2])  # buffer j's previous call has read it
-                for n in names:
-                    dev_in[j][n].copy_(host[n], non_blocking=True)
-                up_done[i].record(s_up)
-            s_comp.wait_event(up_done[i])
-            if i >= 2:
-                s_comp.wait_event(down_done[i - 2])  # outputs j have been read back
+        def run_call(j, st):
             d = dev_in[j]
-            kda.kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], h0, cu, shape, dev_o[j],
-                              dev_ht[j], ws, status, s_comp)
-            comp_done[i].record(s_comp)
-            with torch.cuda.stream(s_down):
-                s_down.wait_event(comp_done[i])
-                o_h[j].copy_(dev_o[j], non_blocking=True)
+            call(d["q"], d["k"], d["v"], d["g"], d["beta"], d.get("h0", h0), dev_o[j], dev_ht[j],
+                 st)
+
+        def read_back(j):
+            o_h[j].copy_(dev_o[j], non_blocking=True)
+            if ht_h is not None:
                 ht_h[j].copy_(dev_ht[j], non_blocking=True)
-                down_done[i].record(s_down)
-        return down_done[nsteps - 1]
 
-    run_pipeline(3)
-    torch.cuda.synchronize(dev)
-    t0 = time.perf_counter()
-    last = run_pipeline(e2e_steps)
-    last.synchronize()
-    e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3 / e2e_steps, dist, dev)
-    e2e_value = job_throughput(world, tokens, e2e_ms)
+        def run_pipeline(nsteps):
+            up_done = [torch.cuda.Event() for _ in range(nsteps)]
+            comp_done = [torch.cuda.Event() for _ in range(nsteps)]
+            down_done = [torch.cuda.Event() for _ in range(nsteps)]
+            for i in range(nsteps):
+                j = i % 2
+                with torch.cuda.stream(s_up):
+                    if i >= 2:
+                        s_up.wait_event(comp_done[i - 2])  # buffer j's previous call read it
+                    for n in names:
+                        dev_in[j][n].copy_(host[n], non_blocking=True)
+                    up_done[i].record(s_up)
+                s_comp.wait_event(up_done[i])
+                if i >= 2:
+                    s_comp.wait_event(down_done[i - 2])  # outputs j have been read back
+                run_call(j, s_comp)
+                comp_done[i].record(s_comp)
+                with torch.cuda.stream(s_down):
+                    s_down.wait_event(comp_done[i])
+                    read_back(j)
+                    down_done[i].record(s_down)
+            return down_done[nsteps - 1]
 
-    def seq_step():
-        d = dev_in[0]
-        for n in names:
-            d[n].copy_(host[n], non_blocking=True)
-        kda.kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], h0, cu, shape, dev_o[0],
-                          dev_ht[0], ws, status, stream)
-        o_h[0].copy_(dev_o[0], non_blocking=True)
-        ht_h[0].copy_(dev_ht[0], non_blocking=True)
+        run_pipeline(3)
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        last = run_pipeline(e2e_steps)
+        last.synchronize()
+        e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3 / e2e_steps, dist, dev)
+        e2e_value = job_throughput(world, tokens, e2e_ms)
 
-    for _ in range(3):
-        seq_step()
-    torch.cuda.synchronize(dev)
-    e_s, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e_s.record(stream)
-    for _ in range(e2e_steps):
-        seq_step()
-    e_e.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_seq_ms = max_over_ranks(e_s.elapsed_time(e_e) / e2e_steps, dist, dev)
+        def seq_step():
+            for n in names:
+                dev_in[0][n].copy_(host[n], non_blocking=True)
+            run_call(0, stream)
+            read_back(0)
+
+        for _ in range(3):
+            seq_step()
+        torch.cuda.synchronize(dev)
+        e_s, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e_s.record(stream)
+        for _ in range(e2e_steps):
+            seq_step()
+        e_e.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_seq_ms = max_over_ranks(e_s.elapsed_time(e_e) / e2e_steps, dist, dev)
+        e2e = {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+               "mode": "pipelined: step i's H2D overlaps step i-1's call and step i-2's D2H "
+                       "(two buffer sets, three streams; wall clock over the steps)",
+               "sequential_ms_per_step": e2e_seq_ms}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        inp_cpu = {n: (t.cpu() if isinstance(t, torch.Tensor) else t) for n, t in inp.items()}
-        rate, runs, L, cores = cpu_oracle_rate(inp_cpu, budget_s=10.0)
+        rate, runs, text, cores = cpu_oracle_rate(inp, budget_s=10.0)
         cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
-               "sample": f"full workload ({L} tokens x {w.HV} heads), {runs} run(s), fp64"}
+               "sample": f"{text} x {w.HV} heads, {runs} run(s), fp64"}
 
     if dist:
         dist.destroy_process_group()
@@ -439,26 +567,21 @@ def run_ours(args):
     # bf16 operands with fp32 accumulation on the tensor-core path; fp32 on the SIMT path
     compute_dtype = "bf16" if any(n.endswith("_tc") for n in per_kernel) else "f32"
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "metric": _metric(args.workload, w), "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": compute_dtype, "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "HV": w.HV, "K": w.K,
-                   "V": w.V, "input_dtype": "bf16", "gate_dtype": "f32", "h0": "none",
-                   "ht": "stored", "l2_flush": "512 MiB write between timed steps",
+                   "V": w.V, "input_dtype": "bf16", "gate_dtype": "f32",
+                   "h0": "N(0,0.1) fp32" if h0 is not None else "none",
+                   "ht": "in place (ht == h0)" if recurrent else "stored",
+                   "sequences": inp["N"], "tokens": tokens,
+                   "l2_flush": "512 MiB write between timed steps",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved,
-                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                     "traffic": traffic, "algorithmic_bytes": dom_bytes,
-                     "kernel_ms": dom_ms, "peak_source": peaks["source"],
-                     "path_gbs": path_gbs, "path_frac": path_gbs / peaks["hbm_gbs"]},
+        "roofline": roofline,
         "kernels": {n: {"ms_per_launch": t / c, "launches_per_step": c / prof_steps}
                     for n, (t, c) in per_kernel.items()},
         "cpu_baseline": cpu,
-        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                "mode": "pipelined: step i's H2D overlaps step i-1's call and step i-2's D2H "
-                        "(two buffer sets, three streams; wall clock over the steps)",
-                "sequential_ms_per_step": e2e_seq_ms},
+        "e2e": e2e,
         "gpu_launches": int(round(launches_per_step * args.steps)),
         "clocks": clocks,
     }
@@ -469,11 +592,17 @@ def run_ours(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=list(WORKLOADS), default="train")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
+    _, _, d_steps, d_warm = WORKLOADS[args.workload]
+    if args.steps is None:
+        args.steps = d_steps
+    if args.warmup is None:
+        args.warmup = d_warm
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
     if args.impl == "reference":

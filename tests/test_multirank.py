@@ -60,3 +60,57 @@ def test_reference_arm_other_ranks_exit_without_work(monkeypatch):
         steps, warmup, gpus = 5, 3, 2
 
     assert bench.run_reference(A()) == 0
+
+
+def _layout(B, T, HV=2, K=8, V=8, cu=None, h0=True, N=None):
+    import torch
+
+    q = torch.zeros(B, T, 1, K)
+    N = N if N is not None else (B if cu is None else len(cu) - 1)
+    return dict(q=q, k=q.clone(), v=torch.zeros(B, T, HV, V), g=torch.zeros(B, T, HV, K),
+                beta=torch.zeros(B, T, HV), h0=torch.zeros(N, HV, K, V) if h0 else None,
+                cu_seqlens=None if cu is None else torch.tensor(cu, dtype=torch.int32))
+
+
+def test_oracle_sample_packed_takes_whole_sequences_and_skips_leading_empty_slots():
+    inp = _layout(1, 100, cu=[0, 0, 30, 30, 70, 90])
+    part, L, _ = bench.oracle_sample(inp, 5)  # smaller than the first sequence
+    assert L == 30 and part["cu_seqlens"].tolist() == [0, 0, 30]
+    assert part["q"].shape[1] == 30 and part["h0"].shape[0] == 2
+    part, L, _ = bench.oracle_sample(inp, 75)
+    assert L == 70 and part["cu_seqlens"].tolist() == [0, 0, 30, 30, 70]
+    assert part["h0"].shape[0] == 4
+    part, L, _ = bench.oracle_sample(inp, 10 ** 6)
+    assert L == 90 and part["cu_seqlens"].tolist() == [0, 0, 30, 30, 70, 90]
+
+
+def test_oracle_sample_dense_batches_and_long_sequences():
+    inp = _layout(4096, 1)  # decode: one token per sequence
+    part, L, _ = bench.oracle_sample(inp, 64)
+    assert L == 64 and part["q"].shape[:2] == (64, 1) and part["h0"].shape[0] == 64
+    inp = _layout(1, 8192, h0=False)  # one long sequence: a token prefix
+    part, L, _ = bench.oracle_sample(inp, 1000)
+    assert L == 1000 and part["q"].shape[:2] == (1, 1000) and part["h0"] is None
+    inp = _layout(4, 256)
+    part, L, _ = bench.oracle_sample(inp, 600)
+    assert L == 512 and part["q"].shape[:2] == (2, 256)
+
+
+def test_derived_fp32_peak_and_recurrence_flops():
+    # 152 SMs x 128 lanes x 2 flops x 2070 MHz
+    assert bench.fp32_fma_tflops(152, 2070.0) == pytest.approx(80.55, abs=0.01)
+
+    class W:
+        HV, K, V = 32, 128, 128
+
+    assert bench.recurrent_flops({"tokens": 4096 * 256, "workload": W}) == \
+        7 * 4096 * 256 * 32 * 128 * 128
+
+
+def test_every_bench_workload_exists_in_the_generator():
+    import kda_synth
+
+    for name, (idx, over, steps, warm) in bench.WORKLOADS.items():
+        w = kda_synth.workload(idx, **over)
+        assert steps >= 1 and warm >= 3, name
+        assert (name in bench.RECURRENT) == bool(w.decode_seqs), name
