@@ -131,7 +131,7 @@ def kernel_algorithmic_bytes(name, inp):
         return r - state_in
     if name.startswith("chunk_scan"):
         return wr + state_in
-    if name.startswith("chunk_fused") or name == "recurrent":
+    if name.startswith("chunk_fused") or name.startswith("recurrent"):
         return r + wr
     return 0
 

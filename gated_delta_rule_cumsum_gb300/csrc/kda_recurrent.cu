@@ -212,6 +212,323 @@ __global__ void __launch_bounds__(512) recurrent_kernel(RecurrentArgs p) {
     }
 }
 
+// ---------------------------------------------------------------- long sequences
+// The same recurrence for slots of many tokens, laid out so that no token needs
+// a CTA-wide exchange.  One CTA of 8 warps per (sequence, value head, value
+// block of 128 columns); warp w owns columns [16w, 16w + 16) of the block for
+// ALL state rows (K <= 128): lane l holds rows d = 8r + (l >> 2), r = 0..15, and
+// columns 4 (l & 3) .. 4 (l & 3) + 3.  The reductions over d are a sum over the
+// thread's 16 rows plus three xor-shuffle levels across the warp's 8 row groups,
+// after which every lane holds the full S^T(2^g k) and S^T(2^g q) of its columns.
+//
+// Tokens go in groups of 16.  While a group is computed, the next group's k, q,
+// g rows (17 of them: the group plus the token after it) and v rows stream into
+// shared memory with cp.async.  A transform pass turns them into one float4 per
+// (token u, row d): {2^g_u, k_u, 2^g_{u+1} k_{u+1}, 2^g_{u+1} q_{u+1}} and the
+// token scalars {1/|k|, 1/|q|, (k.q)/(|k||q|), beta}.  The state update of token
+// u and the reductions for token u+1 then run as ONE pass over the registers:
+//     S[d][j] = 2^g_u[d] S[d][j] + k_u[d] dk_j;   a_j += S[d][j] 2^g_{u+1} k_{u+1}[d]; ...
+constexpr int kLG = 16;       // tokens per group
+constexpr int kLRows = 16;    // state rows per thread
+constexpr int kLMaxK = 8 * kLRows;
+constexpr int kLThreads = 256;
+
+template <typename T>
+struct LongSmem {
+    static constexpr int kRawRows = kLG + 1;
+    static constexpr int stage = 0;                                   // float4 [kLG][128]
+    static constexpr int pro = stage + kLG * kLMaxK * 16;             // float2 [128]
+    static constexpr int scal = pro + kLMaxK * 8;                     // float4 [kLG]
+    static constexpr int raw = scal + kLG * 16;                       // two buffers
+    static constexpr int rk = 0;                                      // T [17][128]
+    static constexpr int rq = rk + kRawRows * kLMaxK * (int)sizeof(T);
+    static constexpr int rg = rq + kRawRows * kLMaxK * (int)sizeof(T);  // float [17][128]
+    static constexpr int rv = rg + kRawRows * kLMaxK * 4;             // T [16][128]
+    static constexpr int raw_bytes = rv + kLG * 128 * (int)sizeof(T);
+    static constexpr int total = raw + 2 * raw_bytes;
+    static_assert(rq % 16 == 0 && rg % 16 == 0 && rv % 16 == 0 && raw_bytes % 16 == 0, "align");
+};
+
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    const unsigned s = (unsigned)__cvta_generic_to_shared(dst);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
+
+__device__ __forceinline__ void load4(const float *p, float (&x)[4]) {
+    const float4 f = *reinterpret_cast<const float4 *>(p);
+    x[0] = f.x; x[1] = f.y; x[2] = f.z; x[3] = f.w;
+}
+__device__ __forceinline__ void load4(const __nv_bfloat16 *p, float (&x)[4]) {
+    const uint2 u = *reinterpret_cast<const uint2 *>(p);
+    const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
+    const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
+    x[0] = lo.x; x[1] = lo.y; x[2] = hi.x; x[3] = hi.y;
+}
+__device__ __forceinline__ void store4(float *p, const float (&x)[4]) {
+    *reinterpret_cast<float4 *>(p) = make_float4(x[0], x[1], x[2], x[3]);
+}
+__device__ __forceinline__ void store4(__nv_bfloat16 *p, const float (&x)[4]) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(x[0], x[1]);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(x[2], x[3]);
+    uint2 u;
+    u.x = *reinterpret_cast<unsigned *>(&lo);
+    u.y = *reinterpret_cast<unsigned *>(&hi);
+    *reinterpret_cast<uint2 *>(p) = u;
+}
+
+// Queue the raw rows of the group starting at token t0 (nrows k/q/g rows, nv v rows).
+template <typename T>
+__device__ __forceinline__ void long_issue(const RecurrentArgs &p, unsigned char *buf, int b,
+                                           int h, int hv, int c_base, int vcols, int t0,
+                                           int nrows, int nv) {
+    using S = LongSmem<T>;
+    constexpr int kPer = 16 / (int)sizeof(T);  // elements per 16-byte chunk
+    const int kc = p.K / kPer, gc = p.K / 4, vc = vcols / kPer;
+    const int nk = nrows * kc, ng = nrows * gc, nvv = nv * vc;
+    const T *k = static_cast<const T *>(p.k);
+    const T *q = static_cast<const T *>(p.q);
+    const T *v = static_cast<const T *>(p.v);
+    for (int c = threadIdx.x; c < 2 * nk + ng + nvv; c += kLThreads) {
+        if (c < 2 * nk) {
+            const int which = c >= nk, cc = c - which * nk;
+            const int row = cc / kc, col = cc - row * kc;
+            const size_t grow = (size_t)b * p.T + t0 + row;
+            const T *src = (which ? q : k) + (grow * p.H + h) * p.K + col * kPer;
+            cp_async16(buf + (which ? S::rq : S::rk) + (row * kLMaxK + col * kPer) * sizeof(T), src);
+        } else if (c < 2 * nk + ng) {
+            const int cc = c - 2 * nk, row = cc / gc, col = cc - row * gc;
+            const size_t grow = (size_t)b * p.T + t0 + row;
+            cp_async16(buf + S::rg + (row * kLMaxK + col * 4) * 4, p.g + (grow * p.HV + hv) * p.K + col * 4);
+        } else {
+            const int cc = c - 2 * nk - ng, row = cc / vc, col = cc - row * vc;
+            const size_t grow = (size_t)b * p.T + t0 + row;
+            cp_async16(buf + S::rv + (row * 128 + col * kPer) * sizeof(T),
+                       v + (grow * p.HV + hv) * p.V + c_base + col * kPer);
+        }
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kLThreads, 2) recurrent_long_kernel(RecurrentArgs p) {
+    using SM = LongSmem<T>;
+    extern __shared__ __align__(16) unsigned char smem[];
+    float4 *stage = reinterpret_cast<float4 *>(smem + SM::stage);
+    float2 *pro = reinterpret_cast<float2 *>(smem + SM::pro);
+    float *scal = reinterpret_cast<float *>(smem + SM::scal);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rgrp = lane >> 2, cgrp = lane & 3;
+    const int nvb = (p.V + 127) / 128;
+    const int64_t bid = blockIdx.x;
+    const int vb = (int)(bid % nvb);
+    const int64_t nh = bid / nvb;
+    const int hv = (int)(nh % p.HV);
+    const int n = (int)(nh / p.HV);
+    const int h = hv / (p.HV / p.H);
+
+    int b, bos, eos;
+    if (p.cu) {
+        bos = p.cu[n];
+        eos = p.cu[n + 1];
+        b = 0;
+        const bool ok = bos >= 0 && bos <= eos && eos <= p.T && (n != 0 || bos == 0);
+        if (!ok) {
+            if (threadIdx.x == 0) report(p.status, KDA_DEVICE_BAD_CU_SEQLENS);
+            return;
+        }
+    } else {
+        b = n;
+        bos = 0;
+        eos = p.T;
+    }
+
+    const int c_base = vb * 128;
+    const int vcols = min(128, p.V - c_base);
+    const int cl = warp * 16 + cgrp * 4;  // first of this thread's columns within the block
+    const bool colok = cl < vcols;        // V % 4 == 0: the four columns are valid together
+    const size_t sbase = ((size_t)n * p.HV + hv) * (size_t)p.K * p.V + c_base + cl;
+
+    float S[kLRows][4];
+#pragma unroll
+    for (int r = 0; r < kLRows; ++r) {
+        const int d = 8 * r + rgrp;
+        if (p.h0 && colok && d < p.K) {
+            load4(p.h0 + sbase + (size_t)d * p.V, S[r]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) S[r][j] = 0.f;
+        }
+    }
+
+    const int L = eos - bos;
+    const int ngroups = (L + kLG - 1) / kLG;
+    const T *beta = static_cast<const T *>(p.beta);
+    T *o = static_cast<T *>(p.o);
+    const bool gate_act = p.act.A_log != nullptr;
+    const float neg_a = gate_act ? gate_neg_a(p.act, hv) : 0.f;
+    auto fetch_beta = [&](int t0, int cnt) {
+        float x = 0.f;
+        if ((int)threadIdx.x < cnt) {
+            const size_t row = (size_t)b * p.T + t0 + threadIdx.x;
+            x = to_f32(beta[row * p.HV + hv]);
+            if (p.act.beta_scale > 0.f) x = beta_activate<T>(x, p.act.beta_scale);
+        }
+        return x;
+    };
+
+    float a[4] = {0.f, 0.f, 0.f, 0.f}, bq[4] = {0.f, 0.f, 0.f, 0.f};
+    float bnext = 0.f;
+    if (ngroups > 0) {
+        long_issue<T>(p, smem + SM::raw, b, h, hv, c_base, vcols, bos, min(kLG + 1, L), min(kLG, L));
+        cp_async_commit();
+        bnext = fetch_beta(bos, min(kLG, L));
+    }
+    for (int gi = 0; gi < ngroups; ++gi) {
+        const int t0 = bos + gi * kLG;
+        const int ntok = min(kLG, eos - t0);
+        const int nrows = min(kLG + 1, eos - t0);
+        const unsigned char *raw = smem + SM::raw + (gi & 1) * SM::raw_bytes;
+        const T *rk = reinterpret_cast<const T *>(raw + SM::rk);
+        const T *rq = reinterpret_cast<const T *>(raw + SM::rq);
+        const float *rg = reinterpret_cast<const float *>(raw + SM::rg);
+        const T *rv = reinterpret_cast<const T *>(raw + SM::rv);
+        cp_async_wait_all();
+        __syncthreads();  // this group's rows have landed; the previous group is computed
+
+        // Transform: warp w takes tokens u = w, w + 8 (and u = 16, the next group's first).
+        for (int u = warp; u <= kLG; u += 8) {
+            const bool valid = u < nrows;
+            float ks = 0.f, qs = 0.f, kq = 0.f;
+#pragma unroll 1
+            for (int m = 0; m < 4; ++m) {
+                const int d = lane + 32 * m;
+                float kr = 0.f, qr = 0.f, dec = 0.f;
+                if (valid && d < p.K) {
+                    kr = to_f32(rk[u * kLMaxK + d]);
+                    qr = to_f32(rq[u * kLMaxK + d]);
+                    float gr = rg[u * kLMaxK + d];
+                    if (gate_act) gr = neg_a * softplus_f(gr + gate_bias(p.act, hv, d, p.K));
+                    dec = exp2f(p.g_scale * gr);
+                }
+                ks = fmaf(kr, kr, ks);
+                qs = fmaf(qr, qr, qs);
+                kq = fmaf(kr, qr, kq);
+                float *e = reinterpret_cast<float *>(stage);
+                if (u < kLG) *reinterpret_cast<float2 *>(e + (u * kLMaxK + d) * 4) = make_float2(dec, kr);
+                if (u >= 1)
+                    *reinterpret_cast<float2 *>(e + ((u - 1) * kLMaxK + d) * 4 + 2) =
+                        make_float2(kr * dec, qr * dec);
+                if (u == 0) pro[d] = make_float2(kr * dec, qr * dec);
+            }
+            if (u < kLG) {
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) {
+                    ks += __shfl_xor_sync(0xffffffffu, ks, off);
+                    qs += __shfl_xor_sync(0xffffffffu, qs, off);
+                    kq += __shfl_xor_sync(0xffffffffu, kq, off);
+                }
+                if (lane == 0) {
+                    const float rkn = p.l2norm ? 1.f / sqrtf(ks + 1e-6f) : 1.f;
+                    const float rqn = p.l2norm ? 1.f / sqrtf(qs + 1e-6f) : 1.f;
+                    scal[u * 4 + 0] = rkn;
+                    scal[u * 4 + 1] = rqn;
+                    scal[u * 4 + 2] = kq * rkn * rqn;
+                }
+            }
+        }
+        if ((int)threadIdx.x < kLG) scal[threadIdx.x * 4 + 3] = bnext;
+        if (gi + 1 < ngroups) {
+            const int t1 = t0 + kLG;
+            long_issue<T>(p, smem + SM::raw + ((gi + 1) & 1) * SM::raw_bytes, b, h, hv, c_base, vcols,
+                          t1, min(kLG + 1, eos - t1), min(kLG, eos - t1));
+            cp_async_commit();
+            bnext = fetch_beta(t1, min(kLG, eos - t1));
+        }
+        __syncthreads();  // stage ready
+
+        if (gi == 0) {
+#pragma unroll
+            for (int r = 0; r < kLRows; ++r) {
+                const float2 e = pro[8 * r + rgrp];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    a[j] = fmaf(S[r][j], e.x, a[j]);
+                    bq[j] = fmaf(S[r][j], e.y, bq[j]);
+                }
+            }
+        }
+        for (int u = 0; u < ntok; ++u) {
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    a[j] += __shfl_xor_sync(0xffffffffu, a[j], off);
+                    bq[j] += __shfl_xor_sync(0xffffffffu, bq[j], off);
+                }
+            }
+            const float4 sc = reinterpret_cast<const float4 *>(scal)[u];
+            float vv[4], dk[4], ov[4];
+            load4(rv + u * 128 + cl, vv);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float delta = sc.w * (vv[j] - sc.x * a[j]);
+                dk[j] = sc.x * delta;
+                ov[j] = p.scale * (sc.y * bq[j] + delta * sc.z);
+                a[j] = 0.f;
+                bq[j] = 0.f;
+            }
+            if (rgrp == 0 && colok)
+                store4(o + (((size_t)b * p.T + t0 + u) * p.HV + hv) * p.V + c_base + cl, ov);
+#pragma unroll
+            for (int r = 0; r < kLRows; ++r) {
+                const float4 e = stage[u * kLMaxK + 8 * r + rgrp];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    S[r][j] = fmaf(S[r][j], e.x, e.y * dk[j]);
+                    a[j] = fmaf(S[r][j], e.z, a[j]);
+                    bq[j] = fmaf(S[r][j], e.w, bq[j]);
+                }
+            }
+        }
+    }
+
+    if (p.ht && colok) {
+#pragma unroll
+        for (int r = 0; r < kLRows; ++r) {
+            const int d = 8 * r + rgrp;
+            if (d < p.K) store4(p.ht + sbase + (size_t)d * p.V, S[r]);
+        }
+    }
+}
+
+template <typename T>
+bool long_form_fits(const RecurrentArgs &a) {
+    auto al = [](const void *x) { return x == nullptr || ((uintptr_t)x % 16) == 0; };
+    const int per = 16 / (int)sizeof(T);
+    // slots average >= 8 tokens: below that the per-group staging does not pay
+    return a.K <= kLMaxK && a.K % per == 0 && a.V % per == 0 && al(a.q) && al(a.k) && al(a.v) &&
+           al(a.g) && al(a.o) && al(a.h0) && al(a.ht) && (int64_t)a.B * a.T >= 8LL * a.N;
+}
+
+template <typename T>
+cudaError_t launch_long(const RecurrentArgs &a, cudaStream_t st) {
+    static bool attr = false;
+    const int smem = LongSmem<T>::total;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(recurrent_long_kernel<T>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    const int64_t blocks = (int64_t)a.N * a.HV * ((a.V + 127) / 128);
+    prof_begin("recurrent_long", st);
+    recurrent_long_kernel<T><<<(unsigned)blocks, kLThreads, smem, st>>>(a);
+    prof_end(st);
+    return cudaGetLastError();
+}
+
 template <typename T>
 cudaError_t launch_typed(const RecurrentArgs &a, cudaStream_t st) {
     const int nwarps = (a.K + kRows - 1) / kRows;
@@ -219,6 +536,7 @@ cudaError_t launch_typed(const RecurrentArgs &a, cudaStream_t st) {
     const int nvb = (a.V + kBlockV - 1) / kBlockV;
     const int64_t blocks = (int64_t)a.N * a.HV * nvb;
     if (blocks == 0) return cudaSuccess;
+    if (long_form_fits<T>(a)) return launch_long<T>(a, st);
     const size_t smem = sizeof(float) * 2 * nwarps * kRedStride;
     const bool vec = (a.V % 4 == 0) && (!a.h0 || ((uintptr_t)a.h0 % 16 == 0)) &&
                      (!a.ht || ((uintptr_t)a.ht % 16 == 0));

@@ -207,3 +207,79 @@ def test_cuda_graph_replay_with_mutated_offsets(kda_lib):
         graph.replay()
         torch.cuda.synchronize()
         _check(inp, o, ht, 1e-4)
+
+
+def _with_kernels(kda, fn):
+    kda.kda_profile_reset()
+    kda.kda_profile_enable(True)
+    try:
+        out = fn()
+        torch.cuda.synchronize()
+        rep = kda.kda_profile_report()
+    finally:
+        kda.kda_profile_enable(False)
+    return out, rep
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("T", [8, 16, 17, 33, 83])
+def test_long_form_across_token_groups(kda_lib, dtype, T):
+    """Slots of many tokens take the grouped form (16 tokens per staged group);
+    lengths at and around the group size, and a ragged last group."""
+    inp = _small(300 + T, B=2, T=T, H=2, HV=4, K=128, V=128, dtype=dtype)
+    (o, ht), rep = _with_kernels(kda_lib, lambda: _run(kda_lib, inp))
+    assert "recurrent_long" in rep, rep
+    _check(inp, o, ht, parity.TOL[dtype])
+
+
+def test_long_form_packed_group_boundaries_and_nan_tail(kda_lib):
+    lens = [16, 17, 0, 1, 33, 47, 2, 0]
+    inp = _packed(31, lens, HV=4, H=1, K=128, V=256)
+    sentinel = 777.0
+    o = torch.full_like(inp["v"], sentinel)
+    ht = torch.full_like(inp["h0"], sentinel)
+    shape = kda_lib.make_shape(inp["q"], inp["v"], inp["cu_seqlens"])
+    st = kda_lib.new_status()
+    _, rep = _with_kernels(kda_lib, lambda: kda_lib.kda_recurrent_fwd(
+        inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["h0"], inp["cu_seqlens"],
+        shape, o, ht, st))
+    assert "recurrent_long" in rep, rep
+    assert kda_lib.kda_read_device_status(st) == (0, 0)
+    _check(inp, o, ht, 2e-2)
+    end = sum(lens)
+    assert torch.all(o[:, end:] == sentinel)
+    for n, L in enumerate(lens):
+        if L == 0:
+            assert torch.equal(ht[n].view(torch.int32), inp["h0"][n].view(torch.int32))
+
+
+def test_long_form_l2norm_and_small_k(kda_lib):
+    inp = _small(41, B=1, T=70, H=1, HV=2, K=32, V=64, dtype=torch.float32)
+    inp["q"] = inp["q"] * 2.0  # unnormalised rows: the flag must normalise them
+    inp["k"] = inp["k"] * 0.7
+    (o, ht), rep = _with_kernels(kda_lib, lambda: _run(kda_lib, inp, use_qk_l2norm_in_kernel=True))
+    assert "recurrent_long" in rep, rep
+    _check(inp, o, ht, 1e-4, l2norm=True)
+
+
+def test_single_token_slots_take_the_register_exchange_form(kda_lib):
+    inp = _small(42, B=8, T=1)
+    (o, ht), rep = _with_kernels(kda_lib, lambda: _run(kda_lib, inp))
+    assert "recurrent" in rep and "recurrent_long" not in rep, rep
+    _check(inp, o, ht, 2e-2)
+
+
+def test_long_and_short_forms_agree(kda_lib):
+    """State columns are independent, so the first 60 value columns of a 64-column
+    problem (grouped form) equal a 60-column problem, which bf16 rows of 120
+    bytes send to the register-exchange form."""
+    inp = _small(43, B=2, T=40, H=2, HV=2, K=64, V=64)
+    (o1, ht1), rep1 = _with_kernels(kda_lib, lambda: _run(kda_lib, inp))
+    assert "recurrent_long" in rep1
+    cut = dict(inp)
+    cut["v"] = inp["v"][..., :60].contiguous()
+    cut["h0"] = inp["h0"][..., :60].contiguous()
+    (o2, ht2), rep2 = _with_kernels(kda_lib, lambda: _run(kda_lib, cut))
+    assert "recurrent" in rep2 and "recurrent_long" not in rep2, rep2
+    assert parity.rel_err(ht1[..., :60], ht2) <= 1e-5
+    assert parity.rel_err(o1[..., :60], o2) <= 8e-3
