@@ -9,7 +9,7 @@ HBM before the timed region; a 512 MiB buffer is written between timed steps
 to flush the 129 MB L2.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload train|gva|packed|decode|prefill]
+                  [--workload train|gva|packed|decode|prefill|prefill_small]
 
 `--workload` picks one of the other synthetic workloads instead (grouped value
 heads B4 T4096 HV32; packed varlen H=HV=32; decode 4096 x 1 token; its
@@ -46,8 +46,10 @@ WORKLOADS = {
     "packed": (3, {}, 300, 10),
     "decode": (4, {}, 100, 5),
     "prefill": (4, {"T": 256}, 10, 3),
+    # the prefill variant on 256 of the 4096 sequences: the size an ncu capture takes
+    "prefill_small": (4, {"T": 256, "B": 256, "decode_seqs": 256}, 20, 3),
 }
-RECURRENT = ("decode", "prefill")
+RECURRENT = ("decode", "prefill", "prefill_small")
 FP32_LANES_PER_SM = 128      # fp32 FMA lanes per SM (4 partitions x 32)
 E2E_MAX_H2D = 8 << 30        # larger inputs are not staged through pinned host memory
 
@@ -217,15 +219,15 @@ def _gpu_id(torch, dev):
         return vis.split(",")[dev] if vis else str(dev)
 
 
-def _traffic(kernel):
+def _traffic(kernel, workload="train"):
     """dram bytes per launch from the committed ncu summary, if it was taken on
-    the current source of that kernel; else None."""
+    the current source of that kernel for this workload; else None."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         rec = json.load(f).get(kernel)
-    if not rec:
+    if not rec or rec.get("bench_workload", "train") != workload:
         return None
     src = os.path.join(ROOT, rec["source"])
     if not os.path.exists(src):
@@ -442,10 +444,10 @@ def run_ours(args):
     dom_ms = per_kernel[dom][0] / per_kernel[dom][1]
     peaks = _peaks()
     dom_bytes = kernel_algorithmic_bytes(dom, inp)
-    traffic = _traffic(dom) if args.workload == "train" else None
+    traffic = _traffic(dom, args.workload)
     r_b, w_b = algorithmic_bytes(inp)
     path_gbs = (r_b + w_b) / (ms / 1e3) / 1e9
-    if args.workload == "prefill":
+    if args.workload.startswith("prefill"):
         # 256 tokens per state: the recurrence's fp32 FMAs, not HBM, bound it.
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
         peak = fp32_fma_tflops(sms, peaks["sm_max_mhz"])

@@ -220,25 +220,30 @@ __global__ void __launch_bounds__(512) recurrent_kernel(RecurrentArgs p) {
 // columns 4 (l & 3) .. 4 (l & 3) + 3.  The reductions over d are a sum over the
 // thread's 16 rows plus three xor-shuffle levels across the warp's 8 row groups,
 // after which every lane holds the full S^T(2^g k) and S^T(2^g q) of its columns.
+// Rows d and d + 8 of a column sit in one float2 so that the paired fp32
+// instructions (two lanes of arithmetic per instruction, each rounded as fmaf)
+// carry the state update and both reductions.
 //
 // Tokens go in groups of 16.  While a group is computed, the next group's k, q,
 // g rows (17 of them: the group plus the token after it) and v rows stream into
-// shared memory with cp.async.  A transform pass turns them into one float4 per
-// (token u, row d): {2^g_u, k_u, 2^g_{u+1} k_{u+1}, 2^g_{u+1} q_{u+1}} and the
-// token scalars {1/|k|, 1/|q|, (k.q)/(|k||q|), beta}.  The state update of token
-// u and the reductions for token u+1 then run as ONE pass over the registers:
+// shared memory with cp.async.  A transform pass turns them, per (token u, row
+// pair), into two float4 planes: A = {2^g_u, k_u} and B = {2^g_{u+1} k_{u+1},
+// 2^g_{u+1} q_{u+1}} (each value for rows d and d + 8), plus the token scalars
+// {1/|k|, 1/|q|, (k.q)/(|k||q|), beta}.  The state update of token u and the
+// reductions for token u+1 then run as ONE pass over the registers:
 //     S[d][j] = 2^g_u[d] S[d][j] + k_u[d] dk_j;   a_j += S[d][j] 2^g_{u+1} k_{u+1}[d]; ...
 constexpr int kLG = 16;       // tokens per group
-constexpr int kLRows = 16;    // state rows per thread
-constexpr int kLMaxK = 8 * kLRows;
+constexpr int kLPairs = 8;    // row pairs per thread (16 rows)
+constexpr int kLMaxK = 128;
 constexpr int kLThreads = 256;
 
 template <typename T>
 struct LongSmem {
     static constexpr int kRawRows = kLG + 1;
-    static constexpr int stage = 0;                                   // float4 [kLG][128]
-    static constexpr int pro = stage + kLG * kLMaxK * 16;             // float2 [128]
-    static constexpr int scal = pro + kLMaxK * 8;                     // float4 [kLG]
+    static constexpr int planeA = 0;                                  // float4 [kLG][8][8]
+    static constexpr int planeB = planeA + kLG * 64 * 16;             // float4 [kLG][8][8]
+    static constexpr int pro = planeB + kLG * 64 * 16;                // float4 [8][8]
+    static constexpr int scal = pro + 64 * 16;                        // float4 [kLG]
     static constexpr int raw = scal + kLG * 16;                       // two buffers
     static constexpr int rk = 0;                                      // T [17][128]
     static constexpr int rq = rk + kRawRows * kLMaxK * (int)sizeof(T);
@@ -314,8 +319,9 @@ template <typename T>
 __global__ void __launch_bounds__(kLThreads, 2) recurrent_long_kernel(RecurrentArgs p) {
     using SM = LongSmem<T>;
     extern __shared__ __align__(16) unsigned char smem[];
-    float4 *stage = reinterpret_cast<float4 *>(smem + SM::stage);
-    float2 *pro = reinterpret_cast<float2 *>(smem + SM::pro);
+    float4 *planeA = reinterpret_cast<float4 *>(smem + SM::planeA);
+    float4 *planeB = reinterpret_cast<float4 *>(smem + SM::planeB);
+    float4 *pro = reinterpret_cast<float4 *>(smem + SM::pro);
     float *scal = reinterpret_cast<float *>(smem + SM::scal);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -350,16 +356,18 @@ __global__ void __launch_bounds__(kLThreads, 2) recurrent_long_kernel(RecurrentA
     const bool colok = cl < vcols;        // V % 4 == 0: the four columns are valid together
     const size_t sbase = ((size_t)n * p.HV + hv) * (size_t)p.K * p.V + c_base + cl;
 
-    float S[kLRows][4];
+    // S2[i][j] = {S[d][j], S[d + 8][j]} with d = 16 i + rgrp.
+    float2 S2[kLPairs][4];
 #pragma unroll
-    for (int r = 0; r < kLRows; ++r) {
-        const int d = 8 * r + rgrp;
-        if (p.h0 && colok && d < p.K) {
-            load4(p.h0 + sbase + (size_t)d * p.V, S[r]);
-        } else {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) S[r][j] = 0.f;
+    for (int i = 0; i < kLPairs; ++i) {
+        float lo[4] = {0.f, 0.f, 0.f, 0.f}, hi[4] = {0.f, 0.f, 0.f, 0.f};
+        const int d = 16 * i + rgrp;
+        if (p.h0 && colok) {
+            if (d < p.K) load4(p.h0 + sbase + (size_t)d * p.V, lo);
+            if (d + 8 < p.K) load4(p.h0 + sbase + (size_t)(d + 8) * p.V, hi);
         }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) S2[i][j] = make_float2(lo[j], hi[j]);
     }
 
     const int L = eos - bos;
@@ -378,7 +386,9 @@ __global__ void __launch_bounds__(kLThreads, 2) recurrent_long_kernel(RecurrentA
         return x;
     };
 
-    float a[4] = {0.f, 0.f, 0.f, 0.f}, bq[4] = {0.f, 0.f, 0.f, 0.f};
+    float2 a2[4], b2[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) a2[j] = b2[j] = make_float2(0.f, 0.f);
     float bnext = 0.f;
     if (ngroups > 0) {
         long_issue<T>(p, smem + SM::raw, b, h, hv, c_base, vcols, bos, min(kLG + 1, L), min(kLG, L));
@@ -397,30 +407,35 @@ __global__ void __launch_bounds__(kLThreads, 2) recurrent_long_kernel(RecurrentA
         cp_async_wait_all();
         __syncthreads();  // this group's rows have landed; the previous group is computed
 
-        // Transform: warp w takes tokens u = w, w + 8 (and u = 16, the next group's first).
+        // Transform: warp w takes tokens u = w, w + 8 (and u = 16, the next group's
+        // first); lane l takes row pairs (i, r) = (l >> 3, l & 7) and (i + 4, r),
+        // i.e. rows d = 16 i + r and d + 8.
         for (int u = warp; u <= kLG; u += 8) {
             const bool valid = u < nrows;
             float ks = 0.f, qs = 0.f, kq = 0.f;
 #pragma unroll 1
-            for (int m = 0; m < 4; ++m) {
-                const int d = lane + 32 * m;
-                float kr = 0.f, qr = 0.f, dec = 0.f;
-                if (valid && d < p.K) {
-                    kr = to_f32(rk[u * kLMaxK + d]);
-                    qr = to_f32(rq[u * kLMaxK + d]);
-                    float gr = rg[u * kLMaxK + d];
-                    if (gate_act) gr = neg_a * softplus_f(gr + gate_bias(p.act, hv, d, p.K));
-                    dec = exp2f(p.g_scale * gr);
+            for (int m = 0; m < 2; ++m) {
+                const int pi = lane + 32 * m;             // pair index = 8 i + r
+                const int d0 = 16 * (pi >> 3) + (pi & 7);
+                float kr[2] = {0.f, 0.f}, qr[2] = {0.f, 0.f}, dec[2] = {0.f, 0.f};
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int d = d0 + 8 * e;
+                    if (valid && d < p.K) {
+                        kr[e] = to_f32(rk[u * kLMaxK + d]);
+                        qr[e] = to_f32(rq[u * kLMaxK + d]);
+                        float gr = rg[u * kLMaxK + d];
+                        if (gate_act) gr = neg_a * softplus_f(gr + gate_bias(p.act, hv, d, p.K));
+                        dec[e] = exp2f(p.g_scale * gr);
+                    }
+                    ks = fmaf(kr[e], kr[e], ks);
+                    qs = fmaf(qr[e], qr[e], qs);
+                    kq = fmaf(kr[e], qr[e], kq);
                 }
-                ks = fmaf(kr, kr, ks);
-                qs = fmaf(qr, qr, qs);
-                kq = fmaf(kr, qr, kq);
-                float *e = reinterpret_cast<float *>(stage);
-                if (u < kLG) *reinterpret_cast<float2 *>(e + (u * kLMaxK + d) * 4) = make_float2(dec, kr);
-                if (u >= 1)
-                    *reinterpret_cast<float2 *>(e + ((u - 1) * kLMaxK + d) * 4 + 2) =
-                        make_float2(kr * dec, qr * dec);
-                if (u == 0) pro[d] = make_float2(kr * dec, qr * dec);
+                const float4 nb = make_float4(kr[0] * dec[0], kr[1] * dec[1], qr[0] * dec[0], qr[1] * dec[1]);
+                if (u < kLG) planeA[u * 64 + pi] = make_float4(dec[0], dec[1], kr[0], kr[1]);
+                if (u >= 1) planeB[(u - 1) * 64 + pi] = nb;
+                if (u == 0) pro[pi] = nb;
             }
             if (u < kLG) {
 #pragma unroll
@@ -446,20 +461,27 @@ __global__ void __launch_bounds__(kLThreads, 2) recurrent_long_kernel(RecurrentA
             cp_async_commit();
             bnext = fetch_beta(t1, min(kLG, eos - t1));
         }
-        __syncthreads();  // stage ready
+        __syncthreads();  // planes ready
 
         if (gi == 0) {
 #pragma unroll
-            for (int r = 0; r < kLRows; ++r) {
-                const float2 e = pro[8 * r + rgrp];
+            for (int i = 0; i < kLPairs; ++i) {
+                const float4 e = pro[8 * i + rgrp];
+                const float2 kd2 = make_float2(e.x, e.y), qd2 = make_float2(e.z, e.w);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    a[j] = fmaf(S[r][j], e.x, a[j]);
-                    bq[j] = fmaf(S[r][j], e.y, bq[j]);
+                    a2[j] = __ffma2_rn(S2[i][j], kd2, a2[j]);
+                    b2[j] = __ffma2_rn(S2[i][j], qd2, b2[j]);
                 }
             }
         }
         for (int u = 0; u < ntok; ++u) {
+            float a[4], bq[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                a[j] = a2[j].x + a2[j].y;
+                bq[j] = b2[j].x + b2[j].y;
+            }
 #pragma unroll
             for (int off = 4; off < 32; off <<= 1) {
 #pragma unroll
@@ -469,26 +491,30 @@ __global__ void __launch_bounds__(kLThreads, 2) recurrent_long_kernel(RecurrentA
                 }
             }
             const float4 sc = reinterpret_cast<const float4 *>(scal)[u];
-            float vv[4], dk[4], ov[4];
+            float vv[4], ov[4];
+            float2 dk2[4];
             load4(rv + u * 128 + cl, vv);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const float delta = sc.w * (vv[j] - sc.x * a[j]);
-                dk[j] = sc.x * delta;
+                const float dk = sc.x * delta;
+                dk2[j] = make_float2(dk, dk);
                 ov[j] = p.scale * (sc.y * bq[j] + delta * sc.z);
-                a[j] = 0.f;
-                bq[j] = 0.f;
+                a2[j] = b2[j] = make_float2(0.f, 0.f);
             }
             if (rgrp == 0 && colok)
                 store4(o + (((size_t)b * p.T + t0 + u) * p.HV + hv) * p.V + c_base + cl, ov);
 #pragma unroll
-            for (int r = 0; r < kLRows; ++r) {
-                const float4 e = stage[u * kLMaxK + 8 * r + rgrp];
+            for (int i = 0; i < kLPairs; ++i) {
+                const float4 ea = planeA[u * 64 + 8 * i + rgrp];
+                const float4 eb = planeB[u * 64 + 8 * i + rgrp];
+                const float2 dec2 = make_float2(ea.x, ea.y), k2 = make_float2(ea.z, ea.w);
+                const float2 kd2 = make_float2(eb.x, eb.y), qd2 = make_float2(eb.z, eb.w);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    S[r][j] = fmaf(S[r][j], e.x, e.y * dk[j]);
-                    a[j] = fmaf(S[r][j], e.z, a[j]);
-                    bq[j] = fmaf(S[r][j], e.w, bq[j]);
+                    S2[i][j] = __ffma2_rn(S2[i][j], dec2, __fmul2_rn(k2, dk2[j]));
+                    a2[j] = __ffma2_rn(S2[i][j], kd2, a2[j]);
+                    b2[j] = __ffma2_rn(S2[i][j], qd2, b2[j]);
                 }
             }
         }
@@ -496,9 +522,16 @@ __global__ void __launch_bounds__(kLThreads, 2) recurrent_long_kernel(RecurrentA
 
     if (p.ht && colok) {
 #pragma unroll
-        for (int r = 0; r < kLRows; ++r) {
-            const int d = 8 * r + rgrp;
-            if (d < p.K) store4(p.ht + sbase + (size_t)d * p.V, S[r]);
+        for (int i = 0; i < kLPairs; ++i) {
+            const int d = 16 * i + rgrp;
+            float lo[4], hi[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                lo[j] = S2[i][j].x;
+                hi[j] = S2[i][j].y;
+            }
+            if (d < p.K) store4(p.ht + sbase + (size_t)d * p.V, lo);
+            if (d + 8 < p.K) store4(p.ht + sbase + (size_t)(d + 8) * p.V, hi);
         }
     }
 }
