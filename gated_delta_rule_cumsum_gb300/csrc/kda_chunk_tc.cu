@@ -316,42 +316,26 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
         if (halo && !carry)
             cp_async16(sKB + kbx_off<KK>(64 + i, c), k + ((row0 - 64 + i) * p.H + h) * KK + c);
     }
+    // this chunk's g rows into the g2 buffer (the cumsum then runs in place)
+    const float *g_rows = p.g + (row0 * p.HV + hv) * KK;
+    for (int idx = tid; idx < nr * (KK / 4); idx += 256) {
+        const int i = idx / (KK / 4), c4 = idx - i * (KK / 4);
+        cp_async16(sG2 + i * kGS + 4 * c4, g_rows + (size_t)i * p.HV * KK + 4 * c4);
+    }
     asm volatile("cp.async.commit_group;" ::: "memory");
 
-    // ---- 2. Stage 1 in registers: thread d < dk owns channel d of this chunk and
-    // forms g2 (rows past the end keep G); thread 128 + d turns channel d of the
-    // previous chunk into eprev[j] = 2^(G' - g2'_j) and 2^G'.  eprev is held as
-    // fp16 pairs scaled by 2^-m, m the channel's largest exponent rounded up (0
-    // for decaying gates), so it cannot overflow and costs 32 registers.
+    // ---- 2. Stage 1.  While the copies are in flight, thread 128 + d turns channel
+    // d of the previous chunk into eprev[j] = 2^(G' - g2'_j) and 2^G' in registers.
+    // eprev is held as fp16 pairs scaled by 2^-m, m the channel's largest exponent
+    // rounded up (0 for decaying gates), so it cannot overflow and costs 32
+    // registers.  Once they have landed, thread d < dk forms g2 for channel d in
+    // place in shared memory (rows past the end keep G).
     const size_t grs = (size_t)p.HV * KK;
     __half2 eprev2[32];
     float escale = 1.f;  // 2^m
     const int dh = tid - 128;
     const bool halo_thread = halo && !carry && tid >= 128 && dh < KK;
-    if (tid < KK) {
-        const float *gp = p.g + (row0 * p.HV + hv) * KK + tid;
-        float gr[64];
-#pragma unroll
-        for (int j = 0; j < 64; ++j) gr[j] = __ldg(gp + (j < nr ? j : nr - 1) * grs);
-        if (gate_act) {
-#pragma unroll
-            for (int j = 0; j < 64; ++j) gr[j] = neg_a * softplus_f(gr[j] + gbias);
-        }
-        float acc = 0.f, rng = 0.f;
-#pragma unroll
-        for (int i = 0; i < 64; ++i) {
-            if (i < nr) acc = p.g_is_cumsum ? gr[i] : fmaf(p.g_scale, gr[i], acc);
-            sG2[i * kGS + tid] = acc;
-            rng = fmaxf(rng, fabsf(acc));
-        }
-        const float eG = exp2f(acc);
-        sEG[tid] = eG;
-        sGv[tid] = acc;
-        reinterpret_cast<float *>(U + Lo.dec)[tid] = eG;
-        atomicMax(&sRangeBits, __float_as_int(rng));
-    } else if (tid < 128) {
-        reinterpret_cast<float *>(U + Lo.dec)[tid] = 0.f;
-    } else if (halo_thread) {
+    if (halo_thread) {
         const float *gp = p.g + ((row0 - 64) * p.HV + hv) * KK + dh;
         float ex[64];  // exponents G' - g2'_j
 #pragma unroll
@@ -387,6 +371,28 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
     }
     if (tid < 64) sBeta[tid] = bet;
     asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
+    // thread d < dk: channel d's chunk-local cumsum in place (rows past the end keep G)
+    if (tid < KK) {
+        float acc = 0.f, rng = 0.f;
+#pragma unroll 8
+        for (int i = 0; i < 64; ++i) {
+            if (i < nr) {
+                float x = sG2[i * kGS + tid];
+                if (gate_act) x = neg_a * softplus_f(x + gbias);
+                acc = p.g_is_cumsum ? x : fmaf(p.g_scale, x, acc);
+            }
+            sG2[i * kGS + tid] = acc;
+            rng = fmaxf(rng, fabsf(acc));
+        }
+        const float eG = exp2f(acc);
+        sEG[tid] = eG;
+        sGv[tid] = acc;
+        reinterpret_cast<float *>(U + Lo.dec)[tid] = eG;
+        atomicMax(&sRangeBits, __float_as_int(rng));
+    } else if (tid < 128) {
+        reinterpret_cast<float *>(U + Lo.dec)[tid] = 0.f;
+    }
     __syncthreads();
 
     // ---- optional L2 normalisation of q, k and the previous chunk's k rows
