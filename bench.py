@@ -440,8 +440,11 @@ def run_ours(args):
     per_kernel = kda.kda_profile_report()
     kda.kda_profile_reset()
     launches_per_step = sum(c for _, c in per_kernel.values()) / prof_steps
+    # The dominant kernel and its device time per step: a pipelined call launches
+    # the prep and the scan twice each (two parts of every sequence), so the
+    # compulsory bytes of a step are set against the kernel's time per step.
     dom = max(per_kernel, key=lambda n: per_kernel[n][0])
-    dom_ms = per_kernel[dom][0] / per_kernel[dom][1]
+    dom_ms = per_kernel[dom][0] / prof_steps
     peaks = _peaks()
     dom_bytes = kernel_algorithmic_bytes(dom, inp)
     traffic = _traffic(dom, args.workload)

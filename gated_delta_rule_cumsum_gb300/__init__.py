@@ -21,7 +21,7 @@ import torch
 __all__ = [
     "KDA_OK", "KDA_ERR_INVALID_ARG", "KDA_ERR_UNSUPPORTED", "KDA_ERR_BAD_CU_SEQLENS",
     "KDA_ERR_CUDA", "KDA_ERR_TIMEOUT", "KDA_FLAG_QK_L2NORM", "KDA_FLAG_G_IS_CUMSUM",
-    "KDA_FLAG_SPLIT_SCAN", "KdaActivation", "make_activation",
+    "KDA_FLAG_SPLIT_SCAN", "KDA_FLAG_SERIAL", "KdaActivation", "make_activation",
     "KdaError", "KdaShape", "load", "library_path", "make_shape",
     "kda_gate_cumsum", "kda_chunk_fwd", "kda_recurrent_fwd", "kda_chunk_workspace_size",
     "kda_gate_cumsum_act", "kda_chunk_fwd_act", "kda_recurrent_fwd_act",
@@ -36,6 +36,7 @@ KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED = 0, 1, 2
 KDA_ERR_BAD_CU_SEQLENS, KDA_ERR_CUDA, KDA_ERR_TIMEOUT = 3, 4, 5
 KDA_DTYPE_F32, KDA_DTYPE_BF16 = 0, 1
 KDA_FLAG_QK_L2NORM, KDA_FLAG_G_IS_CUMSUM, KDA_FLAG_SPLIT_SCAN = 1 << 0, 1 << 1, 1 << 2
+KDA_FLAG_SERIAL = 1 << 3
 KDA_DEVICE_BAD_CU_SEQLENS, KDA_DEVICE_TIMEOUT = 1 << 0, 1 << 1
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -300,13 +301,14 @@ def gate_cumsum(g, cu_seqlens=None, chunk_size: int = 64, g_scale: float = 1.0, 
 def chunk_kda(q, k, v, g, beta, scale=None, initial_state=None, output_final_state=False,
               cu_seqlens=None, use_qk_l2norm_in_kernel=False, g_scale=1.0, g_is_cumsum=False,
               split_scan=False, A_log=None, dt_bias=None, beta_sigmoid_scale=0.0,
-              workspace=None, dev_status=None, stream=None):
+              workspace=None, dev_status=None, stream=None, serial=False):
     """Chunked forward; returns (o, ht or None).  `g` is the per-token log2 gate, or
     with `A_log` the raw gate (activated inside: -exp(A_log) softplus(g + dt_bias),
     times g_scale); `beta_sigmoid_scale` > 0 makes `beta` logits."""
     q, k, v, g, beta, h0, cu = _prep(q, k, v, g, beta, initial_state, cu_seqlens)
     flags = (KDA_FLAG_QK_L2NORM if use_qk_l2norm_in_kernel else 0) | (
-        KDA_FLAG_G_IS_CUMSUM if g_is_cumsum else 0) | (KDA_FLAG_SPLIT_SCAN if split_scan else 0)
+        KDA_FLAG_G_IS_CUMSUM if g_is_cumsum else 0) | (KDA_FLAG_SPLIT_SCAN if split_scan else 0) | (
+        KDA_FLAG_SERIAL if serial else 0)
     shape = make_shape(q, v, cu, scale, g_scale, flags)
     o = torch.empty(v.shape, dtype=q.dtype, device=q.device)
     ht = (torch.empty(shape.num_seqs, shape.HV, shape.K, shape.V, dtype=torch.float32,

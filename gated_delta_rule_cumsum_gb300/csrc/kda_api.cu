@@ -26,7 +26,8 @@ kda_status cuda_fail(cudaError_t e, const char *where) {
     return fail(KDA_ERR_CUDA, "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
 }
 
-constexpr uint32_t kKnownFlags = KDA_FLAG_QK_L2NORM | KDA_FLAG_G_IS_CUMSUM | KDA_FLAG_SPLIT_SCAN;
+constexpr uint32_t kKnownFlags =
+    KDA_FLAG_QK_L2NORM | KDA_FLAG_G_IS_CUMSUM | KDA_FLAG_SPLIT_SCAN | KDA_FLAG_SERIAL;
 
 // Checks shared by the three operations.  `need_h` also checks H and HV % H.
 kda_status check_common(const char *op, const kda_shape *s, const int32_t *cu) {
@@ -80,13 +81,28 @@ struct ChunkWs {
     size_t ctrl, chunk_start, units, total, unit_bytes;
     int64_t slots;
     bool split;
-    size_t qc, e0, e1, pm, e0b;  // split launches only
+    size_t qc, e0, e1, pm, e0b;  // split launches (e0 also pipelined ones)
+    int pipe_m;                  // > 0: a dense call is pipelined at this chunk
 };
 
 // The tensor-core path serves bf16 inputs whose K and V it supports; fp32
 // inputs (and bf16 shapes outside that set) take the fp32 SIMT path.
 bool use_tc(const kda_shape *s) {
     return s->dtype == KDA_DTYPE_BF16 && kda::chunk_tc_supported(s->K, s->V);
+}
+
+// The current device's SM count (cached per device); false when no device answers.
+bool device_sm_count(int *out) {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    if (cache[dev] == 0 &&
+        cudaDeviceGetAttribute(&cache[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cache[dev] = 0;
+        return false;
+    }
+    *out = cache[dev];
+    return true;
 }
 
 ChunkWs chunk_ws_layout(const kda_shape *s, bool packed) {
@@ -101,6 +117,17 @@ ChunkWs chunk_ws_layout(const kda_shape *s, bool packed) {
     L.split = (s->flags & KDA_FLAG_SPLIT_SCAN) && use_tc(s) &&
               kda::chunk_tc_split(s->num_seqs, s->HV, s->K, s->V, s->T);
     L.qc = L.e0 = L.e1 = L.pm = L.e0b = 0;
+    L.pipe_m = 0;
+    if (!L.split && use_tc(s) && !(s->flags & KDA_FLAG_SERIAL)) {
+        // Sized the same for dense and packed shapes (only dense calls pipeline;
+        // the workspace size cannot tell a B = 1 dense call from a packed one).
+        int sms = 0;
+        if (device_sm_count(&sms)) L.pipe_m = kda::chunk_tc_pipe_m(s->B, s->HV, s->K, s->V, s->T, sms);
+        if (L.pipe_m > 0) {
+            L.e0 = kda::align_up(L.total, 256);
+            L.total = L.e0 + (size_t)s->B * s->HV * s->K * s->V * 4;
+        }
+    }
     if (L.split) {
         const size_t nh = (size_t)s->num_seqs * s->HV;
         L.qc = kda::align_up(L.total, 256);
@@ -296,6 +323,11 @@ kda_status kda_chunk_fwd_act(const void *q, const void *k, const void *v, const 
     a.e1 = L.split ? reinterpret_cast<float *>(ws + L.e1) : nullptr;
     a.pm = L.split ? reinterpret_cast<float *>(ws + L.pm) : nullptr;
     a.e0b = L.split ? ws + L.e0b : nullptr;
+    a.pipe = (!packed && L.pipe_m > 0) ? 1 : 0;
+    a.pipe_m = a.pipe ? L.pipe_m : 0;
+    a.prep_c0 = a.prep_c1 = 0;
+    a.scan_seg = 0;
+    if (a.pipe) a.e0 = reinterpret_cast<float *>(ws + L.e0);
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e;

@@ -32,6 +32,8 @@
 #include "kda_internal.cuh"
 #include "kda_tc.cuh"
 
+#include <mutex>
+
 #include <cuda_fp16.h>
 
 namespace kda {
@@ -97,9 +99,30 @@ __device__ __forceinline__ bool locate_chunk(const ChunkArgs &p, int64_t gc, int
 }
 
 // Whether a chunk continues the scan of the chunk before it: not a sequence's
-// first chunk, nor (in a split launch) the first chunk of its second segment.
+// first chunk, nor the first chunk of the second segment of a split launch or of
+// the second part of a pipelined one (those scans start from a given state).
 __device__ __forceinline__ bool continues(const ChunkArgs &p, int cl, int seq_chunks) {
-    return cl > 0 && !(p.split && cl == (seq_chunks + 1) / 2);
+    return cl > 0 && !(p.split && cl == (seq_chunks + 1) / 2) && !(p.pipe && cl == p.pipe_m);
+}
+
+// A prep launch's units: every chunk slot of every value head, or (a pipelined
+// launch's part, dense input) chunks [prep_c0, prep_c1) of every sequence.
+// Units run value head by value head, chunks in order within a sequence.
+__host__ __device__ __forceinline__ int64_t prep_units(const ChunkArgs &p) {
+    const int64_t per_hv = p.prep_c1 > p.prep_c0 ? (int64_t)p.B * (p.prep_c1 - p.prep_c0) : p.slots;
+    return per_hv * p.HV;
+}
+__device__ __forceinline__ void prep_unit(const ChunkArgs &p, int64_t unit, int &hv, int64_t &gc) {
+    if (p.prep_c1 > p.prep_c0) {
+        const int w = p.prep_c1 - p.prep_c0;
+        const int64_t per_hv = (int64_t)p.B * w;
+        hv = (int)(unit / per_hv);
+        const int64_t r = unit - hv * per_hv;
+        gc = (r / w) * ((p.T + kBT - 1) / kBT) + p.prep_c0 + (r % w);
+    } else {
+        hv = (int)(unit / p.slots);
+        gc = unit % p.slots;
+    }
 }
 
 __device__ __forceinline__ void cp_async16(void *dst, const void *src) {
@@ -262,15 +285,16 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
     // chunk) order, so consecutive units are usually consecutive chunks of one
     // head.  The previous chunk's kg tile and 2^G then stay in shared memory
     // ("carry") instead of being re-derived from its k and g.
-    const int64_t total = (int64_t)p.HV * p.slots;
+    const int64_t total = prep_units(p);
     const int64_t per = (total + gridDim.x - 1) / gridDim.x;
     const int64_t ubeg = (int64_t)blockIdx.x * per;
     const int64_t uend = ubeg + per < total ? ubeg + per : total;
     int prev_hv = -1;
     int64_t prev_gc = -1;
     for (int64_t unit = ubeg; unit < uend; ++unit) {
-    const int hv = (int)(unit / p.slots);
-    const int64_t gc = unit % p.slots;
+    int hv;
+    int64_t gc;
+    prep_unit(p, unit, hv, gc);
     int b, r0, nr, cl, nseq, ncs;
     if (!locate_chunk(p, gc, b, r0, nr, cl, &nseq, &ncs)) {
         prev_hv = -1;
@@ -675,10 +699,11 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
     // previous-kg rows for it.
     bool next_carry = false;
     if (unit + 1 < uend) {
-        const int64_t un = unit + 1;
-        int bn, r0n, nrn, cln, nsn, ncn;
-        next_carry = (int)(un / p.slots) == hv &&
-                     locate_chunk(p, un % p.slots, bn, r0n, nrn, cln, &nsn, &ncn) && continues(p, cln, ncn);
+        int hvn, bn, r0n, nrn, cln, nsn, ncn;
+        int64_t gcn;
+        prep_unit(p, unit + 1, hvn, gcn);
+        next_carry = hvn == hv && gcn == gc + 1 &&
+                     locate_chunk(p, gcn, bn, r0n, nrn, cln, &nsn, &ncn) && continues(p, cln, ncn);
     }
     if (next_carry) {
 #pragma unroll
@@ -848,7 +873,7 @@ __device__ __forceinline__ ScanItem scan_item(const ChunkArgs &p, int64_t bid) {
     const int j = (int)(bid % bpp);
     it.hv = (int)((bid / bpp) % p.HV);
     it.n = (int)(bid / ((int64_t)bpp * p.HV));
-    it.seg = j < nreal ? 0 : 1;
+    it.seg = p.pipe ? p.scan_seg : (j < nreal ? 0 : 1);
     it.ident = j >= 2 * nreal;
     it.vb = j < nreal ? j : (j < 2 * nreal ? j - nreal : j - 2 * nreal);
     return it;
@@ -894,6 +919,8 @@ __global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
     if (p.split) {
         const int m = (nc + 1) / 2;
         if (item.seg == 0) c1 = m; else c0 = m;
+    } else if (p.pipe) {
+        if (item.seg == 0) c1 = min(p.pipe_m, nc); else c0 = min(p.pipe_m, nc);
     }
     const int ncs = c1 - c0;
     const int R = ncs > 0 ? ncs + 1 : 0;  // rounds
@@ -1034,9 +1061,11 @@ __global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
         if (ident) {
 #pragma unroll
             for (int j = 0; j < SBV; ++j) h[j] = (row == vb * SBV + j) ? 1.f : 0.f;
-        } else if (item.seg == 0 && has_row && p.h0) {
+        } else if (has_row && (item.seg == 0 ? p.h0 : (p.pipe ? p.e0 : nullptr))) {
+            // a pipelined launch's second part starts from the first part's final state
+            const float *h_init = item.seg == 0 ? p.h0 : p.e0;
             const float4 *src = reinterpret_cast<const float4 *>(
-                p.h0 + (((size_t)n * p.HV + hv) * KK + row) * (size_t)p.V + (size_t)vb * SBV);
+                h_init + (((size_t)n * p.HV + hv) * KK + row) * (size_t)p.V + (size_t)vb * SBV);
 #pragma unroll
             for (int j = 0; j < SBV / 4; ++j) {
                 const float4 x = src[j];
@@ -1089,7 +1118,9 @@ __global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
         // final state: ht, or for a split sequence E0 / E1 / P
         float *dst_base = nullptr;
         int width = p.V;
-        if (!p.split) {
+        if (p.pipe) {
+            dst_base = item.seg == 0 ? p.e0 : p.ht;
+        } else if (!p.split) {
             dst_base = p.ht;
         } else if (ident) {
             dst_base = p.pm;
@@ -1386,7 +1417,7 @@ __global__ void __launch_bounds__(256) chunk_fix_tc_kernel(ChunkArgs p) {
 }
 
 template <int KK, bool ACT>
-cudaError_t launch_prep_t(const ChunkArgs &a, cudaStream_t st) {
+cudaError_t launch_prep_t(const ChunkArgs &a, cudaStream_t st, int64_t cta_cap) {
     using S = PrepSmem<KK>;
     static bool attr = false;
     static int sms = 0, regs_sm = 0, smem_sm = 0;
@@ -1415,8 +1446,10 @@ cudaError_t launch_prep_t(const ChunkArgs &a, cudaStream_t st) {
     const int by_smem = smem_sm / (int)(smem + fa.sharedSizeBytes + 1024);
     int per_sm = by_regs < by_smem ? by_regs : by_smem;
     per_sm = per_sm < 1 ? 1 : (per_sm > 2 ? 2 : per_sm);
-    const int64_t ctas = (int64_t)sms * per_sm;
-    const int64_t units = a.slots * a.HV;
+    int64_t ctas = (int64_t)sms * per_sm;
+    if (cta_cap > 0 && cta_cap < ctas) ctas = cta_cap;
+    const int64_t units = prep_units(a);
+    if (units == 0) return cudaSuccess;
     const unsigned grid = (unsigned)(units < ctas ? units : ctas);
     prof_begin("chunk_prep_tc", st);
     chunk_prep_tc_kernel<KK, ACT><<<grid, 256, smem, st>>>(a);
@@ -1424,9 +1457,11 @@ cudaError_t launch_prep_t(const ChunkArgs &a, cudaStream_t st) {
     return cudaGetLastError();
 }
 
+// cta_cap > 0 bounds the grid (a pipelined launch's second part: the SMs the
+// concurrent scan leaves free, two CTAs each).
 template <int KK>
-cudaError_t launch_prep(const ChunkArgs &a, cudaStream_t st) {
-    return a.act.A_log ? launch_prep_t<KK, true>(a, st) : launch_prep_t<KK, false>(a, st);
+cudaError_t launch_prep(const ChunkArgs &a, cudaStream_t st, int64_t cta_cap = 0) {
+    return a.act.A_log ? launch_prep_t<KK, true>(a, st, cta_cap) : launch_prep_t<KK, false>(a, st, cta_cap);
 }
 
 template <int KK, int SBV>
@@ -1476,24 +1511,98 @@ cudaError_t launch_fix(const ChunkArgs &a, cudaStream_t st) {
     return cudaGetLastError();
 }
 
+cudaError_t sm_count(int *out) {
+    static int sms[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (sms[dev] == 0 &&
+        (e = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return e;
+    *out = sms[dev];
+    return cudaSuccess;
+}
+
+// 32 columns per CTA give the shortest rounds; once that needs more than one wave
+// of CTAs (one per SM), 64 columns halve the CTAs and the shared-memory traffic
+// per column, which wins (measured: -20% to -26% on multi-wave shapes).
+bool scan_wide(int64_t N, int HV, int V, int sms) { return V % 64 == 0 && N * HV * (V / 32) > sms; }
+
+template <int KK, int VV>
+cudaError_t launch_scan_any(const ChunkArgs &a, cudaStream_t st, int sms) {
+    if constexpr (VV % 64 == 0)
+        if (scan_wide(a.N, a.HV, a.V, sms)) return launch_scan<KK, 64>(a, st);
+    return launch_scan<KK, 32>(a, st);
+}
+
+// The library's own stream for a pipelined launch's second prep (lowest
+// priority) and the events that fork it from the caller's stream and join it
+// back, one set per device.
+struct PipeStreams {
+    cudaStream_t side = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+std::mutex g_pipe_mu;
+
+cudaError_t pipe_streams(PipeStreams **out) {
+    static PipeStreams per_dev[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    PipeStreams &ps = per_dev[dev];
+    if (!ps.side) {
+        int least = 0, greatest = 0;
+        if ((e = cudaDeviceGetStreamPriorityRange(&least, &greatest)) != cudaSuccess) return e;
+        if ((e = cudaEventCreateWithFlags(&ps.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
+        if ((e = cudaEventCreateWithFlags(&ps.join, cudaEventDisableTiming)) != cudaSuccess) return e;
+        if ((e = cudaStreamCreateWithPriority(&ps.side, cudaStreamNonBlocking, least)) != cudaSuccess)
+            return e;
+    }
+    *out = &ps;
+    return cudaSuccess;
+}
+
+// Pipelined: prep of chunks [0, m), then on the caller's stream the scan of
+// [0, m) (final state to e0) and, once the side stream's prep of [m, nc) on the
+// SMs the scan leaves free is done, the scan of [m, nc) from e0.  The first
+// scan follows the first prep in stream order, so its CTAs are placed as soon
+// as that prep ends, ahead of the second prep, which waits on an event.  No
+// kernel waits for another: the streams and events order whole launches.
+template <int KK, int VV>
+cudaError_t launch_pipelined(const ChunkArgs &a, cudaStream_t st, int sms) {
+    std::lock_guard<std::mutex> lock(g_pipe_mu);
+    PipeStreams *ps = nullptr;
+    cudaError_t e = pipe_streams(&ps);
+    if (e != cudaSuccess) return e;
+    const int nc = (a.T + kBT - 1) / kBT;
+    const int64_t scan_ctas = (int64_t)a.N * a.HV * (a.V / (scan_wide(a.N, a.HV, a.V, sms) ? 64 : 32));
+    ChunkArgs pa = a, pb = a, s0 = a, s1 = a;
+    pa.prep_c0 = 0;
+    pa.prep_c1 = a.pipe_m;
+    pb.prep_c0 = a.pipe_m;
+    pb.prep_c1 = nc;
+    s0.scan_seg = 0;
+    s1.scan_seg = 1;
+    if ((e = launch_prep<KK>(pa, st)) != cudaSuccess) return e;
+    if ((e = cudaEventRecord(ps->fork, st)) != cudaSuccess) return e;
+    if ((e = launch_scan_any<KK, VV>(s0, st, sms)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(ps->side, ps->fork, 0)) != cudaSuccess) return e;
+    if ((e = launch_prep<KK>(pb, ps->side, 2 * (sms - scan_ctas))) != cudaSuccess) return e;
+    if ((e = cudaEventRecord(ps->join, ps->side)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(st, ps->join, 0)) != cudaSuccess) return e;
+    return launch_scan_any<KK, VV>(s1, st, sms);
+}
+
 template <int KK, int VV>
 cudaError_t launch_kv(const ChunkArgs &a, cudaStream_t st) {
     cudaError_t e = cudaSuccess;
+    int sms = 0;
+    if ((e = sm_count(&sms)) != cudaSuccess) return e;
+    if (a.pipe) return launch_pipelined<KK, VV>(a, st, sms);
     if (a.slots > 0 && (e = launch_prep<KK>(a, st)) != cudaSuccess) return e;
-    if (!a.split) {
-        // 32 columns per CTA give the shortest rounds; once that needs more than one
-        // wave of CTAs (one per SM), 64 columns halve the CTAs and the shared-memory
-        // traffic per column, which wins (measured: -20% to -26% on multi-wave shapes).
-        static int sms = 0;
-        if (sms == 0) {
-            int dev = 0;
-            if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-            if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-                return e;
-        }
-        if (VV % 64 == 0 && (int64_t)a.N * a.HV * (a.V / 32) > sms) return launch_scan<KK, 64>(a, st);
-        return launch_scan<KK, 32>(a, st);
-    }
+    if (!a.split) return launch_scan_any<KK, VV>(a, st, sms);
     if ((e = launch_scan<KK, 64>(a, st)) != cudaSuccess) return e;
     if constexpr (VV % 64 == 0) return launch_fix<KK, VV>(a, st);
     return cudaErrorInvalidValue;
@@ -1521,6 +1630,34 @@ bool chunk_tc_supported(int K, int V) {
 }
 
 size_t chunk_tc_unit_bytes(int K, int V) { return tc_layout(K, V).stride; }
+
+int chunk_tc_pipe_m(int B, int HV, int K, int V, int T, int sms) {
+    // Cost model in scan rounds: at two prep CTAs per SM a prep unit takes about
+    // 23 scan rounds (17.8 us against 0.78 us at K = V = 128, measured).  Serial:
+    // every unit, then 1 + nc rounds.  Pipelined at m: the units of [0, m) on all
+    // SMs, then the longer of (1 + m rounds) and (the units of [m, nc) on the
+    // SMs the scan leaves free), then 1 + nc - m rounds.
+    constexpr int64_t kUnit = 23;
+    if (!chunk_tc_supported(K, V) || B <= 0 || HV <= 0 || T <= 0 || sms <= 0) return 0;
+    const int64_t nc = (T + kBT - 1) / kBT;
+    const int64_t scan_ctas = (int64_t)B * HV * (V / (scan_wide(B, HV, V, sms) ? 64 : 32));
+    if (2 * scan_ctas > sms || nc < 16) return 0;
+    const int64_t free_ctas = 2 * (sms - scan_ctas), all_ctas = 2 * (int64_t)sms;
+    auto waves = [](int64_t units, int64_t ctas) { return (units + ctas - 1) / ctas; };
+    const int64_t hb = (int64_t)B * HV;
+    int64_t best = waves(hb * nc, all_ctas) * kUnit + nc + 1;
+    int best_m = 0;
+    for (int64_t m = nc / 4; m + 4 <= nc; ++m) {
+        const int64_t second = waves(hb * (nc - m), free_ctas) * kUnit;
+        const int64_t cost = waves(hb * m, all_ctas) * kUnit + (m + 1 > second ? m + 1 : second) +
+                             nc - m + 1;
+        if (cost < best) {
+            best = cost;
+            best_m = (int)m;
+        }
+    }
+    return best_m;
+}
 
 bool chunk_tc_split(int N, int HV, int K, int V, int T) {
     // Few long sequences: without a split the scan occupies under half of the

@@ -138,12 +138,24 @@ struct ChunkArgs {
     float *e0, *e1;        // [N][HV][K][V] fp32: the segments' final states from zero / h0
     void *e0b;             // [N][HV] bf16 [K][V] operand tiles of e0
     float *pm;             // [N][HV][K][K] fp32: segment 1's state transition
+    // Pipelined launches (tensor-core path, dense input): chunks [0, pipe_m) of
+    // every sequence are prepped and scanned first, and the scan of that part
+    // runs while the prep of [pipe_m, nc) occupies the SMs it leaves free; the
+    // second part's scan starts from the first part's final state (in e0).
+    int pipe;              // 1: pipelined launch
+    int pipe_m;            // first chunk of the second part
+    int prep_c0, prep_c1;  // a prep launch's chunks within every sequence (c1 <= c0: all slots)
+    int scan_seg;          // a pipelined scan launch's part: 0 from h0, 1 from e0
 };
 size_t chunk_simt_unit_bytes(int K, int V);
 cudaError_t launch_chunk_simt(const ChunkArgs &a, kda_dtype dt, cudaStream_t st);
 
 // Tensor-core path (bf16 inputs): K in {64, 128}, V a multiple of 32 up to 256.
 bool chunk_tc_supported(int K, int V);
+// The first chunk of a pipelined launch's second part for a dense input of B
+// sequences of T rows on a GPU of `sms` SMs, or 0 when running the prep and the
+// scan one after the other is expected to be as fast.
+int chunk_tc_pipe_m(int B, int HV, int K, int V, int T, int sms);
 // Whether a launch splits each sequence's scan into two segments run at once.
 bool chunk_tc_split(int N, int HV, int K, int V, int T);
 size_t chunk_tc_unit_bytes(int K, int V);

@@ -9,6 +9,9 @@
 // brings its own scratch: a file-scope device array of fixed size, reserved in
 // every GPU's memory that loads this library until the process exits.
 //
+// Its launches all run on the caller's stream (KDA_FLAG_SERIAL), so no stream or
+// event is created either.
+//
 // The host cannot pass the array's name to a kernel (in host code it only
 // names a host-side stand-in), so the array's device address is looked up with
 // cudaGetSymbolAddress once per device, on that device's first call.  The
@@ -49,6 +52,11 @@ extern "C" kda_status kda_chunk_fwd_noalloc(const void *q, const void *k, const 
                                            void *o, float *ht, int32_t *dev_status,
                                            kda_stream_t stream) {
     if (!shape) return set_fail(KDA_ERR_INVALID_ARG, "kda_chunk_fwd_noalloc: shape is NULL");
+    // Every launch on the caller's stream: a pipelined call would create the
+    // library's scan stream and events on first use.
+    kda_shape serial = *shape;
+    serial.flags |= KDA_FLAG_SERIAL;
+    shape = &serial;
     const size_t need = kda_chunk_workspace_size(shape);
     if (need == 0) return set_fail(KDA_ERR_INVALID_ARG, "kda_chunk_fwd_noalloc: invalid shape");
     if (need > kScratchBytes) {

@@ -94,10 +94,22 @@ typedef enum {
                                            <= 64, T >= 1024, V % 64 == 0) run each
                                            sequence's inter-chunk scan as two
                                            segments at once and compose them after
-                                           (h_end = P h_start + E; SURVEY row f4,
-                                           context parallel within one GPU).  Needs
-                                           a larger workspace (size it with the same
-                                           flags); ignored elsewhere.              */
+                                           (h_end = P h_start + E: context parallel
+                                           within one GPU).  Needs a larger
+                                           workspace (size it with the same flags);
+                                           ignored elsewhere.                      */
+#define KDA_FLAG_SERIAL      (1u << 3)  /* kda_chunk_fwd: run every launch on the
+                                           caller's stream, one after the other.
+                                           Without it, a dense bf16 input whose
+                                           scan leaves at least half of the SMs
+                                           idle is pipelined: while the scan of
+                                           each sequence's first chunks runs on
+                                           the caller's stream, the prep of the
+                                           remaining chunks runs on a library-
+                                           owned low-priority stream (forked from
+                                           and joined back to the caller's stream
+                                           with events, so graph capture sees one
+                                           fork and one join) on the other SMs.    */
 
 /* Bits of the device status word. */
 #define KDA_DEVICE_BAD_CU_SEQLENS (1 << 0)
@@ -178,6 +190,12 @@ kda_status kda_gate_cumsum_act(const float *g, float *g_cum, const int32_t *cu_s
  *                      bytes, 256-byte aligned; its contents on entry do not
  *                      matter and on return are unspecified.  Calls that share
  *                      one workspace must be ordered on the GPU.
+ *   stream             the call's work follows earlier work on `stream` and
+ *                      later work on it sees the results.  Unless
+ *                      KDA_FLAG_SERIAL is set, a dense bf16 call may run some
+ *                      launches on a library stream forked from `stream` and
+ *                      joined back to it with events (see KDA_FLAG_SERIAL);
+ *                      such calls take a host-side lock while they enqueue.
  * Supported: K in {64, 128}; 1 <= V <= 256; K, V multiples of 16 for bf16.
  */
 kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const float *g,
@@ -191,7 +209,9 @@ kda_status kda_chunk_fwd_act(const void *q, const void *k, const void *v, const 
                              float *ht, void *workspace, size_t workspace_bytes,
                              int32_t *dev_status, kda_stream_t stream);
 
-/* Bytes of workspace kda_chunk_fwd needs for *shape (0 on invalid shapes). */
+/* Bytes of workspace kda_chunk_fwd needs for *shape (0 on invalid shapes).  For
+ * shapes that may be pipelined it depends on the current device's SM count:
+ * size the workspace with the device that will run the call current. */
 size_t kda_chunk_workspace_size(const kda_shape *shape);
 
 /*
@@ -206,7 +226,8 @@ size_t kda_chunk_workspace_size(const kda_shape *shape);
  *   built into the library, which every GPU that loads the library holds until
  *   the process exits.  Shapes whose kda_chunk_workspace_size exceeds it are
  *   rejected with KDA_ERR_UNSUPPORTED and a message; nothing is enqueued.
- *   The call allocates nothing.  Its first call on a device looks up the
+ *   The call allocates nothing and runs every launch on `stream`, one after
+ *   the other (as with KDA_FLAG_SERIAL).  Its first call on a device looks up the
  *   array's device address (cudaGetSymbolAddress) and caches it; make that
  *   first call before any stream capture on that device.
  *   Every call on a device shares the one array, so calls that overlap on the
