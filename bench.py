@@ -220,8 +220,9 @@ def _gpu_id(torch, dev):
 
 
 def _traffic(kernel, workload="train"):
-    """dram bytes per launch from the committed ncu summary, if it was taken on
-    the current source of that kernel for this workload; else None."""
+    """dram bytes per step (all the kernel's launches in one call) from the
+    committed ncu summary, if it was taken on the current source of that kernel
+    for this workload; else None."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(path):
         return None
@@ -236,7 +237,7 @@ def _traffic(kernel, workload="train"):
         digest = hashlib.sha256(f.read()).hexdigest()[:16]
     if digest != rec.get("source_sha256_16"):
         return None
-    return rec["dram_bytes_per_launch"]
+    return rec["dram_bytes_per_step"]
 
 
 # ------------------------------------------------------------------ CPU oracle
