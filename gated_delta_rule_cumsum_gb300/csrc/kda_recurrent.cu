@@ -236,6 +236,9 @@ constexpr int kLG = 16;       // tokens per group
 constexpr int kLPairs = 8;    // row pairs per thread (16 rows)
 constexpr int kLMaxK = 128;
 constexpr int kLThreads = 256;
+// A group runs in the scaled form while every row's running exponent stays
+// within 2^+-60 (k / D and S / D then stay far from fp32 overflow).
+constexpr float kLWide = 60.f;
 
 template <typename T>
 struct LongSmem {
@@ -244,7 +247,8 @@ struct LongSmem {
     static constexpr int planeB = planeA + kLG * 64 * 16;             // float4 [kLG][8][8]
     static constexpr int pro = planeB + kLG * 64 * 16;                // float4 [8][8]
     static constexpr int scal = pro + 64 * 16;                        // float4 [kLG]
-    static constexpr int raw = scal + kLG * 16;                       // two buffers
+    static constexpr int dlast = scal + kLG * 16;                     // float [128]
+    static constexpr int raw = dlast + kLMaxK * 4;                    // two buffers
     static constexpr int rk = 0;                                      // T [17][128]
     static constexpr int rq = rk + kRawRows * kLMaxK * (int)sizeof(T);
     static constexpr int rg = rq + kRawRows * kLMaxK * (int)sizeof(T);  // float [17][128]
@@ -323,6 +327,8 @@ __global__ void __launch_bounds__(kLThreads, 2) recurrent_long_kernel(RecurrentA
     float4 *planeB = reinterpret_cast<float4 *>(smem + SM::planeB);
     float4 *pro = reinterpret_cast<float4 *>(smem + SM::pro);
     float *scal = reinterpret_cast<float *>(smem + SM::scal);
+    float *sDlast = reinterpret_cast<float *>(smem + SM::dlast);
+    __shared__ int sWide;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rgrp = lane >> 2, cgrp = lane & 3;
@@ -390,6 +396,7 @@ __global__ void __launch_bounds__(kLThreads, 2) recurrent_long_kernel(RecurrentA
 #pragma unroll
     for (int j = 0; j < 4; ++j) a2[j] = b2[j] = make_float2(0.f, 0.f);
     float bnext = 0.f;
+    if (threadIdx.x == 0) sWide = 0;
     if (ngroups > 0) {
         long_issue<T>(p, smem + SM::raw, b, h, hv, c_base, vcols, bos, min(kLG + 1, L), min(kLG, L));
         cp_async_commit();
@@ -399,45 +406,29 @@ __global__ void __launch_bounds__(kLThreads, 2) recurrent_long_kernel(RecurrentA
         const int t0 = bos + gi * kLG;
         const int ntok = min(kLG, eos - t0);
         const int nrows = min(kLG + 1, eos - t0);
-        const unsigned char *raw = smem + SM::raw + (gi & 1) * SM::raw_bytes;
+        unsigned char *raw = smem + SM::raw + (gi & 1) * SM::raw_bytes;
         const T *rk = reinterpret_cast<const T *>(raw + SM::rk);
         const T *rq = reinterpret_cast<const T *>(raw + SM::rq);
-        const float *rg = reinterpret_cast<const float *>(raw + SM::rg);
+        float *rg = reinterpret_cast<float *>(raw + SM::rg);
         const T *rv = reinterpret_cast<const T *>(raw + SM::rv);
         cp_async_wait_all();
         __syncthreads();  // this group's rows have landed; the previous group is computed
 
-        // Transform: warp w takes tokens u = w, w + 8 (and u = 16, the next group's
-        // first); lane l takes row pairs (i, r) = (l >> 3, l & 7) and (i + 4, r),
-        // i.e. rows d = 16 i + r and d + 8.
-        for (int u = warp; u <= kLG; u += 8) {
-            const bool valid = u < nrows;
-            float ks = 0.f, qs = 0.f, kq = 0.f;
-#pragma unroll 1
-            for (int m = 0; m < 2; ++m) {
-                const int pi = lane + 32 * m;             // pair index = 8 i + r
-                const int d0 = 16 * (pi >> 3) + (pi & 7);
-                float kr[2] = {0.f, 0.f}, qr[2] = {0.f, 0.f}, dec[2] = {0.f, 0.f};
+        if (warp >= 4) {
+            // Token scalars: warp 4 + w takes tokens u = w, w + 4, ...; lane l rows l + 32 m.
+            for (int u = warp - 4; u < ntok; u += 4) {
+                float ks = 0.f, qs = 0.f, kq = 0.f;
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int d = d0 + 8 * e;
-                    if (valid && d < p.K) {
-                        kr[e] = to_f32(rk[u * kLMaxK + d]);
-                        qr[e] = to_f32(rq[u * kLMaxK + d]);
-                        float gr = rg[u * kLMaxK + d];
-                        if (gate_act) gr = neg_a * softplus_f(gr + gate_bias(p.act, hv, d, p.K));
-                        dec[e] = exp2f(p.g_scale * gr);
+                for (int m = 0; m < 4; ++m) {
+                    const int d = lane + 32 * m;
+                    if (d < p.K) {
+                        const float kr = to_f32(rk[u * kLMaxK + d]);
+                        const float qr = to_f32(rq[u * kLMaxK + d]);
+                        ks = fmaf(kr, kr, ks);
+                        qs = fmaf(qr, qr, qs);
+                        kq = fmaf(kr, qr, kq);
                     }
-                    ks = fmaf(kr[e], kr[e], ks);
-                    qs = fmaf(qr[e], qr[e], qs);
-                    kq = fmaf(kr[e], qr[e], kq);
                 }
-                const float4 nb = make_float4(kr[0] * dec[0], kr[1] * dec[1], qr[0] * dec[0], qr[1] * dec[1]);
-                if (u < kLG) planeA[u * 64 + pi] = make_float4(dec[0], dec[1], kr[0], kr[1]);
-                if (u >= 1) planeB[(u - 1) * 64 + pi] = nb;
-                if (u == 0) pro[pi] = nb;
-            }
-            if (u < kLG) {
 #pragma unroll
                 for (int off = 16; off > 0; off >>= 1) {
                     ks += __shfl_xor_sync(0xffffffffu, ks, off);
@@ -452,6 +443,71 @@ __global__ void __launch_bounds__(kLThreads, 2) recurrent_long_kernel(RecurrentA
                     scal[u * 4 + 2] = kq * rkn * rqn;
                 }
             }
+        } else {
+            // Thread d runs down row d: x_u = g_scale g_u (activated when asked, kept
+            // in place for the unscaled planes), G_u = x_0 + ... + x_u and D_u = 2^G_u.
+            // Plane A gets {k_u / D_u (rows d, d + 8), D_{u+1} k_{u+1} (rows d, d + 8)},
+            // plane B {D_{u+1} q_{u+1}}, the prologue D_0 {k_0, q_0}; D of the group's
+            // last token is kept for the rescale after it.
+            const int d = threadIdx.x;
+            const int pi = 8 * (d >> 4) + (d & 7), hf = (d >> 3) & 1;
+            float *c4 = reinterpret_cast<float *>(planeA);
+            float *c2 = reinterpret_cast<float *>(planeB);
+            float *pf = reinterpret_cast<float *>(pro);
+            float G = 0.f, gmax = 0.f;
+            for (int u = 0; u < nrows; ++u) {
+                float kr = 0.f, qr = 0.f;
+                if (d < p.K) {
+                    float gr = rg[u * kLMaxK + d];
+                    if (gate_act) gr = neg_a * softplus_f(gr + gate_bias(p.act, hv, d, p.K));
+                    const float x = p.g_scale * gr;
+                    rg[u * kLMaxK + d] = x;
+                    G += x;
+                    kr = to_f32(rk[u * kLMaxK + d]);
+                    qr = to_f32(rq[u * kLMaxK + d]);
+                }
+                gmax = fmaxf(gmax, fabsf(G));
+                const float Dp = exp2f(G);
+                if (u < kLG) c4[(u * 64 + pi) * 4 + hf] = kr * exp2f(-G);
+                if (u >= 1) {
+                    c4[((u - 1) * 64 + pi) * 4 + 2 + hf] = kr * Dp;
+                    c2[((u - 1) * 64 + pi) * 2 + hf] = qr * Dp;
+                }
+                if (u == 0) {
+                    pf[pi * 4 + hf] = kr * Dp;
+                    pf[pi * 4 + 2 + hf] = qr * Dp;
+                }
+                if (u == ntok - 1) sDlast[d] = Dp;
+            }
+            if (!(gmax <= kLWide)) sWide = 1;
+        }
+        __syncthreads();  // scaled planes, token scalars and the range flag ready
+        const bool wide = sWide != 0;
+        if (wide) {
+            // The unscaled planes A = {2^x_u, k_u}, B = {2^x_{u+1} k_{u+1}, 2^x_{u+1} q_{u+1}}
+            // (row pairs as above) over the scaled ones: warp w takes tokens w, w + 8, 16.
+            for (int u = warp; u <= kLG; u += 8) {
+                const bool valid = u < nrows;
+#pragma unroll 1
+                for (int m = 0; m < 2; ++m) {
+                    const int pi = lane + 32 * m;
+                    const int d0 = 16 * (pi >> 3) + (pi & 7);
+                    float kr[2] = {0.f, 0.f}, qr[2] = {0.f, 0.f}, dec[2] = {0.f, 0.f};
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int d = d0 + 8 * e;
+                        if (valid && d < p.K) {
+                            kr[e] = to_f32(rk[u * kLMaxK + d]);
+                            qr[e] = to_f32(rq[u * kLMaxK + d]);
+                            dec[e] = exp2f(rg[u * kLMaxK + d]);
+                        }
+                    }
+                    if (u < kLG) planeA[u * 64 + pi] = make_float4(dec[0], dec[1], kr[0], kr[1]);
+                    if (u >= 1)
+                        planeB[(u - 1) * 64 + pi] =
+                            make_float4(kr[0] * dec[0], kr[1] * dec[1], qr[0] * dec[0], qr[1] * dec[1]);
+                }
+            }
         }
         if ((int)threadIdx.x < kLG) scal[threadIdx.x * 4 + 3] = bnext;
         if (gi + 1 < ngroups) {
@@ -462,6 +518,7 @@ __global__ void __launch_bounds__(kLThreads, 2) recurrent_long_kernel(RecurrentA
             bnext = fetch_beta(t1, min(kLG, eos - t1));
         }
         __syncthreads();  // planes ready
+        if (threadIdx.x == 0) sWide = 0;  // every thread has read it
 
         if (gi == 0) {
 #pragma unroll
@@ -504,18 +561,43 @@ __global__ void __launch_bounds__(kLThreads, 2) recurrent_long_kernel(RecurrentA
             }
             if (rgrp == 0 && colok)
                 store4(o + (((size_t)b * p.T + t0 + u) * p.HV + hv) * p.V + c_base + cl, ov);
+            if (!wide) {
+                // S~ += (k / D) dk^T; the reductions for the next token read S~ against D k', D q'
+#pragma unroll
+                for (int i = 0; i < kLPairs; ++i) {
+                    const float4 e = planeA[u * 64 + 8 * i + rgrp];
+                    const float2 f = reinterpret_cast<const float2 *>(planeB)[u * 64 + 8 * i + rgrp];
+                    const float2 kt2 = make_float2(e.x, e.y), kd2 = make_float2(e.z, e.w);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        S2[i][j] = __ffma2_rn(kt2, dk2[j], S2[i][j]);
+                        a2[j] = __ffma2_rn(S2[i][j], kd2, a2[j]);
+                        b2[j] = __ffma2_rn(S2[i][j], f, b2[j]);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < kLPairs; ++i) {
+                    const float4 ea = planeA[u * 64 + 8 * i + rgrp];
+                    const float4 eb = planeB[u * 64 + 8 * i + rgrp];
+                    const float2 dec2 = make_float2(ea.x, ea.y), k2 = make_float2(ea.z, ea.w);
+                    const float2 kd2 = make_float2(eb.x, eb.y), qd2 = make_float2(eb.z, eb.w);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        S2[i][j] = __ffma2_rn(S2[i][j], dec2, __fmul2_rn(k2, dk2[j]));
+                        a2[j] = __ffma2_rn(S2[i][j], kd2, a2[j]);
+                        b2[j] = __ffma2_rn(S2[i][j], qd2, b2[j]);
+                    }
+                }
+            }
+        }
+        if (!wide) {
+            // back to the true state: S = D_last S~ per row
 #pragma unroll
             for (int i = 0; i < kLPairs; ++i) {
-                const float4 ea = planeA[u * 64 + 8 * i + rgrp];
-                const float4 eb = planeB[u * 64 + 8 * i + rgrp];
-                const float2 dec2 = make_float2(ea.x, ea.y), k2 = make_float2(ea.z, ea.w);
-                const float2 kd2 = make_float2(eb.x, eb.y), qd2 = make_float2(eb.z, eb.w);
+                const float2 dl = make_float2(sDlast[16 * i + rgrp], sDlast[16 * i + rgrp + 8]);
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    S2[i][j] = __ffma2_rn(S2[i][j], dec2, __fmul2_rn(k2, dk2[j]));
-                    a2[j] = __ffma2_rn(S2[i][j], kd2, a2[j]);
-                    b2[j] = __ffma2_rn(S2[i][j], qd2, b2[j]);
-                }
+                for (int j = 0; j < 4; ++j) S2[i][j] = __fmul2_rn(S2[i][j], dl);
             }
         }
     }

@@ -32,9 +32,18 @@ def test_tiny_fp32_workload(kda_lib):
 
 
 def test_training_shape_workload(kda_lib):
-    """B1 T8192 H=HV16 K=V128 bf16, h0 = 0, final state stored: every head."""
+    """B1 T8192 H=HV16 K=V128 bf16, h0 = 0, final state stored: every head, in the
+    launch configuration the benchmark times (pipelined: two preps, two scans)."""
     inp = kda_synth.make_inputs(1, device="cuda")
-    o, ht = _run(kda_lib, inp)
+    kda_lib.kda_profile_reset()
+    kda_lib.kda_profile_enable(True)
+    try:
+        o, ht = _run(kda_lib, inp)
+        torch.cuda.synchronize()
+        rep = kda_lib.kda_profile_report()
+    finally:
+        kda_lib.kda_profile_enable(False)
+    assert rep["chunk_prep_tc"][1] == 2 and rep["chunk_scan_tc"][1] == 2, rep
     _check(inp, o, ht, 2e-2)
 
 
