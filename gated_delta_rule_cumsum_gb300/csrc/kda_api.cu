@@ -159,8 +159,11 @@ kda_status resolve_act(const char *op, const kda_shape *s, const kda_activation 
 }
 
 kda_status check_chunk_support(const char *op, const kda_shape *s) {
+    if (use_tc(s)) return KDA_OK;
     if (s->K != 64 && s->K != 128)
-        return fail(KDA_ERR_UNSUPPORTED, "%s: K=%d (supported: 64, 128)", op, s->K);
+        return fail(KDA_ERR_UNSUPPORTED,
+                    "%s: K=%d (supported: 64, 128; for bf16 with V a multiple of 32 up to 256, "
+                    "any multiple of 8 up to 128)", op, s->K);
     if (s->V > 256) return fail(KDA_ERR_UNSUPPORTED, "%s: V=%d > 256", op, s->V);
     return KDA_OK;
 }

@@ -238,8 +238,11 @@ __device__ __forceinline__ void strip16(float4 &s, const float *P, int pr, int p
 __device__ __forceinline__ float4 neg4(float4 v) { return make_float4(-v.x, -v.y, -v.z, -v.w); }
 
 // ACT: the gate activation (kda_activation.A_log) is compiled in.
-template <int KK, bool ACT>
+// PADK: K < dk, the channels past K are zero (loads masked; otherwise K == dk
+// and the channel count is a compile-time constant).
+template <int KK, bool ACT, bool PADK>
 __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
+    const int Kc = PADK ? p.K : KK;  // the input's channels
     using S = PrepSmem<KK>;
     const int VV = p.V;
     extern __shared__ __align__(1024) unsigned char sm[];
@@ -275,6 +278,7 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
         mbar_fence_init();
         sRangeBits = 0;
     }
+    if (PADK && tid < 128) sDprev[tid] = 1.f;  // channels past K keep 1 (their W columns are zero)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -321,7 +325,7 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
     // the gate activation's per-channel constants (thread d and 128 + d: channel d)
     constexpr bool gate_act = ACT;
     const float neg_a = gate_act ? gate_neg_a(p.act, hv) : 0.f;
-    const float gbias = gate_act && (tid & 127) < KK ? gate_bias(p.act, hv, tid & 127, KK) : 0.f;
+    const float gbias = gate_act && (tid & 127) < Kc ? gate_bias(p.act, hv, tid & 127, Kc) : 0.f;
 #pragma unroll
     for (int it = 0; it < KK / 32; ++it) {
         const int idx = tid + it * 256, l = idx & 31, w = idx >> 5;
@@ -329,22 +333,38 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
         const int c = ((w >> 3) * 4 + (l >> 3)) * 8;
         void *dq = sAG + tile_off(i, c, KK);
         void *dk = sAG + tile_off(64 + i, c, KK);
-        if (i < nr) {
-            const size_t src = ((row0 + i) * p.H + h) * KK + c;
+        if (i < nr && c < Kc) {  // channels past K are zero: they add nothing anywhere
+            const size_t src = ((row0 + i) * p.H + h) * Kc + c;
             cp_async16(dq, q + src);
             cp_async16(dk, k + src);
         } else {
             *reinterpret_cast<uint4 *>(dq) = make_uint4(0, 0, 0, 0);
             *reinterpret_cast<uint4 *>(dk) = make_uint4(0, 0, 0, 0);
         }
-        if (halo && !carry)
-            cp_async16(sKB + kbx_off<KK>(64 + i, c), k + ((row0 - 64 + i) * p.H + h) * KK + c);
+        if (halo && !carry) {
+            if (c < Kc)
+                cp_async16(sKB + kbx_off<KK>(64 + i, c), k + ((row0 - 64 + i) * p.H + h) * Kc + c);
+            else
+                *reinterpret_cast<uint4 *>(sKB + kbx_off<KK>(64 + i, c)) = make_uint4(0, 0, 0, 0);
+        }
     }
     // this chunk's g rows into the g2 buffer (the cumsum then runs in place)
-    const float *g_rows = p.g + (row0 * p.HV + hv) * KK;
-    for (int idx = tid; idx < nr * (KK / 4); idx += 256) {
-        const int i = idx / (KK / 4), c4 = idx - i * (KK / 4);
-        cp_async16(sG2 + i * kGS + 4 * c4, g_rows + (size_t)i * p.HV * KK + 4 * c4);
+    if constexpr (!PADK) {
+        const float *g_rows = p.g + (row0 * p.HV + hv) * KK;
+        for (int idx = tid; idx < nr * (KK / 4); idx += 256) {
+            const int i = idx / (KK / 4), c4 = idx - i * (KK / 4);
+            cp_async16(sG2 + i * kGS + 4 * c4, g_rows + (size_t)i * p.HV * KK + 4 * c4);
+        }
+    } else {
+        // thread: 16-byte column chunk tid % (dk / 4), rows tid / (dk / 4) + every step
+        constexpr int kQ = KK / 4, kStep = 256 / kQ;
+        const int c4 = tid % kQ;
+        if (4 * c4 < Kc) {
+            const float *src = p.g + (row0 * p.HV + hv) * Kc + 4 * c4;
+            const size_t rstride = (size_t)p.HV * Kc;
+            for (int i = tid / kQ; i < nr; i += kStep)
+                cp_async16(sG2 + i * kGS + 4 * c4, src + i * rstride);
+        }
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
 
@@ -354,13 +374,13 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
     // rounded up (0 for decaying gates), so it cannot overflow and costs 32
     // registers.  Once they have landed, thread d < dk forms g2 for channel d in
     // place in shared memory (rows past the end keep G).
-    const size_t grs = (size_t)p.HV * KK;
+    const size_t grs = (size_t)p.HV * Kc;
     __half2 eprev2[32];
     float escale = 1.f;  // 2^m
     const int dh = tid - 128;
-    const bool halo_thread = halo && !carry && tid >= 128 && dh < KK;
+    const bool halo_thread = halo && !carry && tid >= 128 && dh < Kc;
     if (halo_thread) {
-        const float *gp = p.g + ((row0 - 64) * p.HV + hv) * KK + dh;
+        const float *gp = p.g + ((row0 - 64) * p.HV + hv) * Kc + dh;
         float ex[64];  // exponents G' - g2'_j
 #pragma unroll
         for (int j = 0; j < 64; ++j) ex[j] = __ldg(gp + j * grs);
@@ -401,7 +421,7 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
         float acc = 0.f, rng = 0.f;
 #pragma unroll 8
         for (int i = 0; i < 64; ++i) {
-            if (i < nr) {
+            if (i < nr && tid < Kc) {  // channels past K keep a zero gate
                 float x = sG2[i * kGS + tid];
                 if (gate_act) x = neg_a * softplus_f(x + gbias);
                 acc = p.g_is_cumsum ? x : fmaf(p.g_scale, x, acc);
@@ -1054,6 +1074,7 @@ __global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
         // ------------------------------------------------ h warps: the state
         const int row = warp * 32 + lane;
         const bool has_row = row < KK;
+        const bool glob_row = row < p.K;  // rows past K stay zero and are neither read nor stored
         const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16) + 2 * SBV;
         float h[SBV];
 #pragma unroll
@@ -1061,11 +1082,11 @@ __global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
         if (ident) {
 #pragma unroll
             for (int j = 0; j < SBV; ++j) h[j] = (row == vb * SBV + j) ? 1.f : 0.f;
-        } else if (has_row && (item.seg == 0 ? p.h0 : (p.pipe ? p.e0 : nullptr))) {
+        } else if (glob_row && (item.seg == 0 ? p.h0 : (p.pipe ? p.e0 : nullptr))) {
             // a pipelined launch's second part starts from the first part's final state
             const float *h_init = item.seg == 0 ? p.h0 : p.e0;
             const float4 *src = reinterpret_cast<const float4 *>(
-                h_init + (((size_t)n * p.HV + hv) * KK + row) * (size_t)p.V + (size_t)vb * SBV);
+                h_init + (((size_t)n * p.HV + hv) * p.K + row) * (size_t)p.V + (size_t)vb * SBV);
 #pragma unroll
             for (int j = 0; j < SBV / 4; ++j) {
                 const float4 x = src[j];
@@ -1128,9 +1149,9 @@ __global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
         } else {
             dst_base = item.seg == 0 ? p.e0 : p.e1;
         }
-        if (dst_base && has_row && !read_flag(&abort_flag)) {
+        if (dst_base && glob_row && !read_flag(&abort_flag)) {
             float4 *dst = reinterpret_cast<float4 *>(
-                dst_base + (((size_t)n * p.HV + hv) * KK + row) * (size_t)width + (size_t)vb * SBV);
+                dst_base + (((size_t)n * p.HV + hv) * p.K + row) * (size_t)width + (size_t)vb * SBV);
 #pragma unroll
             for (int j = 0; j < SBV / 4; ++j)
                 dst[j] = make_float4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
@@ -1416,18 +1437,18 @@ __global__ void __launch_bounds__(256) chunk_fix_tc_kernel(ChunkArgs p) {
     if (warp == 0) tmem_dealloc(tmem, S::tmem_cols);
 }
 
-template <int KK, bool ACT>
+template <int KK, bool ACT, bool PADK>
 cudaError_t launch_prep_t(const ChunkArgs &a, cudaStream_t st, int64_t cta_cap) {
     using S = PrepSmem<KK>;
     static bool attr = false;
     static int sms = 0, regs_sm = 0, smem_sm = 0;
     static cudaFuncAttributes fa;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(chunk_prep_tc_kernel<KK, ACT>,
+        cudaError_t e = cudaFuncSetAttribute(chunk_prep_tc_kernel<KK, ACT, PADK>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)S::total(256));
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(chunk_prep_tc_kernel<KK, ACT>,
+            e = cudaFuncSetAttribute(chunk_prep_tc_kernel<KK, ACT, PADK>,
                                      cudaFuncAttributePreferredSharedMemoryCarveout,
                                      (int)cudaSharedmemCarveoutMaxShared);
         int dev = 0;
@@ -1435,7 +1456,7 @@ cudaError_t launch_prep_t(const ChunkArgs &a, cudaStream_t st, int64_t cta_cap) 
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev);
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
-        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, chunk_prep_tc_kernel<KK, ACT>);
+        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, chunk_prep_tc_kernel<KK, ACT, PADK>);
         if (e != cudaSuccess) return e;
         attr = true;
     }
@@ -1452,7 +1473,7 @@ cudaError_t launch_prep_t(const ChunkArgs &a, cudaStream_t st, int64_t cta_cap) 
     if (units == 0) return cudaSuccess;
     const unsigned grid = (unsigned)(units < ctas ? units : ctas);
     prof_begin("chunk_prep_tc", st);
-    chunk_prep_tc_kernel<KK, ACT><<<grid, 256, smem, st>>>(a);
+    chunk_prep_tc_kernel<KK, ACT, PADK><<<grid, 256, smem, st>>>(a);
     prof_end(st);
     return cudaGetLastError();
 }
@@ -1461,7 +1482,11 @@ cudaError_t launch_prep_t(const ChunkArgs &a, cudaStream_t st, int64_t cta_cap) 
 // concurrent scan leaves free, two CTAs each).
 template <int KK>
 cudaError_t launch_prep(const ChunkArgs &a, cudaStream_t st, int64_t cta_cap = 0) {
-    return a.act.A_log ? launch_prep_t<KK, true>(a, st, cta_cap) : launch_prep_t<KK, false>(a, st, cta_cap);
+    if (a.K == KK)
+        return a.act.A_log ? launch_prep_t<KK, true, false>(a, st, cta_cap)
+                           : launch_prep_t<KK, false, false>(a, st, cta_cap);
+    return a.act.A_log ? launch_prep_t<KK, true, true>(a, st, cta_cap)
+                       : launch_prep_t<KK, false, true>(a, st, cta_cap);
 }
 
 template <int KK, int SBV>
@@ -1626,10 +1651,10 @@ cudaError_t launch_k(const ChunkArgs &a, cudaStream_t st) {
 }  // namespace
 
 bool chunk_tc_supported(int K, int V) {
-    return (K == 64 || K == 128) && V >= 32 && V <= 256 && V % 32 == 0;
+    return K >= 8 && K <= 128 && K % 8 == 0 && V >= 32 && V <= 256 && V % 32 == 0;
 }
 
-size_t chunk_tc_unit_bytes(int K, int V) { return tc_layout(K, V).stride; }
+size_t chunk_tc_unit_bytes(int K, int V) { return tc_layout(K <= 64 ? 64 : 128, V).stride; }
 
 int chunk_tc_pipe_m(int B, int HV, int K, int V, int T, int sms) {
     // Cost model in scan rounds: at two prep CTAs per SM a prep unit takes about
@@ -1666,8 +1691,11 @@ bool chunk_tc_split(int N, int HV, int K, int V, int T) {
     return V % 64 == 0 && (int64_t)N * HV * (V / 32) <= 64 && T >= 1024 && (K == 64 || K == 128);
 }
 
+// K up to 64 runs in the 64-channel kernels, K up to 128 in the 128-channel ones;
+// the channels past K are zero throughout (loads fill zeros, state rows past K
+// are neither read nor stored).
 cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st) {
-    if (a.K == 64) return launch_k<64>(a, st);
+    if (a.K <= 64) return launch_k<64>(a, st);
     return launch_k<128>(a, st);
 }
 

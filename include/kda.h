@@ -196,7 +196,9 @@ kda_status kda_gate_cumsum_act(const float *g, float *g_cum, const int32_t *cu_s
  *                      launches on a library stream forked from `stream` and
  *                      joined back to it with events (see KDA_FLAG_SERIAL);
  *                      such calls take a host-side lock while they enqueue.
- * Supported: K in {64, 128}; 1 <= V <= 256; K, V multiples of 16 for bf16.
+ * Supported: K in {64, 128} with 1 <= V <= 256 (K, V multiples of 16 for bf16);
+ * for bf16 also any K that is a multiple of 8 up to 128 when V is a multiple of
+ * 32 up to 256 (the tensor-core kernels run such K padded with zero channels).
  */
 kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const float *g,
                          const void *beta, const float *h0, const int32_t *cu_seqlens,

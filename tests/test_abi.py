@@ -71,7 +71,9 @@ FAKE = ctypes.c_void_p(0x1000)  # never dereferenced: the host checks fail first
     (dict(num_seqs=2), 1),        # dense: num_seqs must equal B
     (dict(dtype=7), 1),
     (dict(flags=1 << 9), 2),      # unknown flag
-    (dict(K=96), 2),              # chunk path: K in {64, 128}
+    (dict(K=96, dtype=0), 2),     # fp32 chunk path: K in {64, 128}
+    (dict(K=100), 2),             # bf16: K a multiple of 8 up to 128
+    (dict(K=96, V=48), 2),        # bf16 with K outside {64, 128}: V a multiple of 32
     (dict(V=512), 2),
 ])
 def test_chunk_fwd_rejects_on_host(lib, kw, status):

@@ -77,6 +77,35 @@ def test_packed_varlen_workload(kda_lib):
         assert torch.equal(ht[n].view(torch.int32), inp["h0"][n].view(torch.int32))
 
 
+@pytest.mark.parametrize("K,V,T,lens", [
+    (32, 64, 300, None),             # padded to the 64-channel kernels
+    (8, 32, 200, None),
+    (96, 128, 700, None),            # padded to the 128-channel kernels
+    (72, 96, 0, [450, 0, 70, 129]),  # packed, an empty slot
+    (120, 256, 0, [333, 64]),
+])
+def test_tensor_core_path_any_k_multiple_of_8(kda_lib, K, V, T, lens):
+    """bf16 K not in {64, 128}: the tensor-core kernels with zero channels past K."""
+    if lens is None:
+        inp = _small(K * 10 + V, B=2, T=T, H=2, HV=4, K=K, V=V)
+    else:
+        inp = _packed(K + V, lens, HV=2, H=1, K=K, V=V)
+    kda_lib.kda_profile_reset()
+    kda_lib.kda_profile_enable(True)
+    try:
+        o, ht = _run(kda_lib, inp)
+        torch.cuda.synchronize()
+        rep = kda_lib.kda_profile_report()
+    finally:
+        kda_lib.kda_profile_enable(False)
+    assert "chunk_prep_tc" in rep, rep
+    _check(inp, o, ht, 2e-2)
+    if lens is not None:
+        for n, L in enumerate(lens):
+            if L == 0:
+                assert torch.equal(ht[n].view(torch.int32), inp["h0"][n].view(torch.int32))
+
+
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("K,V,T", [(64, 64, 1), (64, 16, 63), (128, 96, 64), (128, 256, 65),
                                    (64, 128, 200), (128, 40, 130)])

@@ -42,6 +42,7 @@ def _assert_pipelined(rep):
     (1, 8229, 4, 128, 128, True),   # ragged last chunk, initial state
     (2, 4096, 4, 128, 128, False),  # two sequences
     (1, 8229, 4, 64, 64, True),     # K = V = 64
+    (1, 8229, 4, 96, 128, True),    # K = 96 (zero channels past K)
 ])
 def test_pipelined_matches_oracle(kda_lib, B, T, HV, K, V, h0):
     inp = _small(900 + T + K, B=B, T=T, H=HV, HV=HV, K=K, V=V, h0=h0)
