@@ -14,6 +14,10 @@ Two independent formulations live here:
   "Stage 1 -- cumsum".
 * `chunk_form.chunk_forward` -- the chunked (WY / UT-transform) formulation of
   ALGORITHM.md "Stage 1" through "Stage 3+4", in numpy fp64.
+* `backward.recurrent_grads` -- the gradients (dq, dk, dv, dg, dbeta, dh0) of the
+  token recurrence (kernel-fun 0.2.0.dev1 sdist, ALGORITHM.md, "Backward"), in
+  PyTorch fp64 by reverse mode; pinned in tests/test_oracle_backward.py against
+  finite differences of the C recurrence.
 * `activation` -- the optional input activations (gate -exp(A_log) softplus(g +
   dt_bias), beta sigmoid) of kernel-fun 0.2.0.dev1 wheel, kda/chain.py and
   kda/ops.py, in numpy fp64; pinned in tests/test_oracle_activation.py.

@@ -1,0 +1,78 @@
+"""fp64 gradients of the KDA token recurrence -- TEST INFRASTRUCTURE ONLY.
+
+The backward's contract is that of kernel-fun 0.2.0.dev1 sdist, ALGORITHM.md,
+"Backward", and of kernel-fun 0.2.0.dev1 wheel, kda/chain.py, `backward`: given
+the output gradient do and the final-state gradient dht it returns dq, dk, dv,
+dbeta, dg and dh0, where dg is taken with respect to the per-token decay (the
+gate before any cumsum) and dq / dk are summed over the value heads that share a
+q/k head.  The method reaches the result of the token recurrence, so the
+gradients are those of the plain recurrence (attention-gym PR #317, PR
+description; the same definition the C oracle in this package integrates):
+
+    S_t = Diag(2^(g_scale g_t)) S_{t-1}
+    delta_t = beta_t (v_t - S_t^T k_t)      (S_t here: after the decay)
+    S_t = S_t + k_t delta_t^T
+    o_t = scale S_t^T q_t
+
+written out once more below in PyTorch fp64 and differentiated by PyTorch's
+reverse mode (a library primitive standing for the chain rule).  The loss whose
+gradients are returned is  sum(o * do) + sum(ht * dht).  tests/test_oracle_backward.py
+pins it against central finite differences of the C oracle's forward (an
+independent implementation) and against the closed form at beta = 0.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+__all__ = ["recurrent_grads"]
+
+
+def recurrent_grads(q, k, v, g, beta, do, h0=None, dht=None, cu_seqlens=None, scale=None,
+                    g_scale=1.0):
+    """Gradients of sum(o * do) + sum(ht * dht) of the token recurrence, in fp64.
+
+    Shapes: q, k [B,T,H,K]; v, do [B,T,HV,V]; g [B,T,HV,K] (per-token log2 decay);
+    beta [B,T,HV]; h0, dht [N,HV,K,V] or None; cu_seqlens [N+1] or None (then N = B).
+    Returns a dict of float64 numpy arrays dq, dk, dv, dg, dbeta, dh0 (dh0 None when
+    h0 is None).  Rows outside every sequence get zero gradients.
+    """
+    import torch
+
+    def leaf(x):
+        return torch.tensor(np.asarray(x, dtype=np.float64), requires_grad=True)
+
+    q, k, v, g, beta = (leaf(x) for x in (q, k, v, g, beta))
+    do = torch.tensor(np.asarray(do, dtype=np.float64))
+    B, T, H, K = q.shape
+    HV, V = v.shape[2], v.shape[3]
+    G = HV // H
+    cu = None if cu_seqlens is None else [int(x) for x in np.asarray(cu_seqlens)]
+    N = B if cu is None else len(cu) - 1
+    h0t = None if h0 is None else leaf(h0)
+    dhtt = None if dht is None else torch.tensor(np.asarray(dht, dtype=np.float64))
+    if scale is None:
+        scale = 1.0 / math.sqrt(K)
+
+    loss = torch.zeros((), dtype=torch.float64)
+    for n in range(N):
+        b, bos, eos = (n, 0, T) if cu is None else (0, cu[n], cu[n + 1])
+        S = h0t[n] if h0t is not None else torch.zeros(HV, K, V, dtype=torch.float64)
+        for t in range(bos, eos):
+            qt = q[b, t].repeat_interleave(G, dim=0)           # [HV, K]
+            kt = k[b, t].repeat_interleave(G, dim=0)
+            S = torch.exp2(g_scale * g[b, t])[:, :, None] * S  # decay rows
+            a = torch.einsum("hkv,hk->hv", S, kt)
+            delta = beta[b, t][:, None] * (v[b, t] - a)
+            S = S + kt[:, :, None] * delta[:, None, :]
+            loss = loss + (scale * torch.einsum("hkv,hk->hv", S, qt) * do[b, t]).sum()
+        if dhtt is not None:
+            loss = loss + (S * dhtt[n]).sum()
+    loss.backward()
+
+    def grad(x):
+        return np.zeros(tuple(x.shape)) if x.grad is None else x.grad.numpy().copy()
+
+    return dict(dq=grad(q), dk=grad(k), dv=grad(v), dg=grad(g), dbeta=grad(beta),
+                dh0=None if h0t is None else grad(h0t))
