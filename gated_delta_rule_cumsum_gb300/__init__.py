@@ -24,6 +24,7 @@ __all__ = [
     "KDA_FLAG_SPLIT_SCAN", "KDA_FLAG_SERIAL", "KdaActivation", "make_activation",
     "KdaError", "KdaShape", "load", "library_path", "make_shape",
     "kda_gate_cumsum", "kda_chunk_fwd", "kda_recurrent_fwd", "kda_chunk_workspace_size",
+    "kda_recurrent_bwd", "kda_recurrent_bwd_workspace_size", "recurrent_kda_backward",
     "kda_gate_cumsum_act", "kda_chunk_fwd_act", "kda_recurrent_fwd_act",
     "kda_chunk_fwd_noalloc", "KDA_NOALLOC_SCRATCH_BYTES",
     "kda_read_device_status", "kda_clear_device_status", "kda_status_string",
@@ -96,6 +97,9 @@ _SIGNATURES = {
     "kda_chunk_fwd": (_ST, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.POINTER(KdaShape), _VP,
                             _VP, _VP, _SZ, _VP, _VP]),
     "kda_chunk_workspace_size": (_SZ, [ctypes.POINTER(KdaShape)]),
+    "kda_recurrent_bwd": (_ST, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.POINTER(KdaShape),
+                                _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP]),
+    "kda_recurrent_bwd_workspace_size": (_SZ, [ctypes.POINTER(KdaShape)]),
     "kda_chunk_fwd_noalloc": (_ST, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.POINTER(KdaShape),
                                     _VP, _VP, _VP, _VP]),
     "kda_recurrent_fwd": (_ST, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.POINTER(KdaShape),
@@ -214,6 +218,20 @@ def kda_chunk_workspace_size(shape: KdaShape) -> int:
     return int(load().kda_chunk_workspace_size(ctypes.byref(shape)))
 
 
+def kda_recurrent_bwd_workspace_size(shape: KdaShape) -> int:
+    return int(load().kda_recurrent_bwd_workspace_size(ctypes.byref(shape)))
+
+
+def kda_recurrent_bwd(q, k, v, g, beta, h0, cu_seqlens, shape: KdaShape, dout, dht, dq, dk, dv,
+                      dg, dbeta, dh0, workspace, dev_status=None, stream=None):
+    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().kda_recurrent_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0),
+                                    _ptr(cu_seqlens), ctypes.byref(shape), _ptr(dout), _ptr(dht),
+                                    _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg), _ptr(dbeta),
+                                    _ptr(dh0), _ptr(workspace), ws, _ptr(dev_status),
+                                    _stream(stream)))
+
+
 def kda_recurrent_fwd(q, k, v, g, beta, h0, cu_seqlens, shape: KdaShape, o, ht, dev_status=None,
                       stream=None):
     _check(load().kda_recurrent_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0),
@@ -323,6 +341,32 @@ def chunk_kda(q, k, v, g, beta, scale=None, initial_state=None, output_final_sta
     else:
         kda_chunk_fwd(q, k, v, g, beta, h0, cu, shape, o, ht, workspace, dev_status, stream)
     return o, ht
+
+
+def recurrent_kda_backward(q, k, v, gate, beta, dout, initial_state=None, dht=None, *,
+                           cu_seqlens=None, scale=None, g_scale=1.0, want_dh0=True,
+                           dev_status=None, stream=None):
+    """Gradients of the token recurrence for an output gradient `dout` and a final-state
+    gradient `dht` (or None): a dict of fp32 tensors dq, dk, dv, dg (with respect to the
+    per-token log2 gate), dbeta and dh0 (None unless `want_dh0`)."""
+    ts = [q, k, v, gate, beta, dout, initial_state, dht, cu_seqlens]
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise KdaError(KDA_ERR_INVALID_ARG, "tensors must be on a CUDA device")
+    q, k, v, g, beta, dout, h0, dht, cu = [None if t is None else t.detach().contiguous()
+                                           for t in ts]
+    shape = make_shape(q, v, cu, scale, g_scale, 0)
+    f32 = dict(dtype=torch.float32, device=q.device)
+    out = dict(dq=torch.empty(q.shape, **f32), dk=torch.empty(k.shape, **f32),
+               dv=torch.empty(v.shape, **f32), dg=torch.empty(g.shape, **f32),
+               dbeta=torch.empty(beta.shape, **f32),
+               dh0=(torch.empty(shape.num_seqs, shape.HV, shape.K, shape.V, **f32)
+                    if want_dh0 else None))
+    ws = torch.empty(max(kda_recurrent_bwd_workspace_size(shape), 16), dtype=torch.uint8,
+                     device=q.device)
+    kda_recurrent_bwd(q, k, v, g, beta, h0, cu, shape, dout, dht, out["dq"], out["dk"],
+                      out["dv"], out["dg"], out["dbeta"], out["dh0"], ws, dev_status, stream)
+    return out
 
 
 def recurrent_kda(q, k, v, gate, beta, initial_state=None, *, cu_seqlens=None,

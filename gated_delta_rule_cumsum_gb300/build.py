@@ -23,6 +23,7 @@ LIB = os.path.join(OUT, "libkda_gb300.so")
 SOURCES = [
     "kda_api.cu",
     "kda_recurrent.cu",
+    "kda_recurrent_bwd.cu",
     "kda_cumsum.cu",
     "kda_chunk_simt.cu",
     "kda_chunk_tc.cu",

@@ -267,6 +267,70 @@ kda_status kda_recurrent_fwd_act(const void *q, const void *k, const void *v, co
     return KDA_OK;
 }
 
+size_t kda_recurrent_bwd_workspace_size(const kda_shape *shape) {
+    if (!shape || shape->K <= 0 || shape->V <= 0 || shape->HV <= 0 || shape->B <= 0 ||
+        shape->T < 0 || shape->num_seqs < 0)
+        return 0;
+    return (size_t)kda::recurrent_bwd_ckpt_slots(shape->B, shape->T, shape->num_seqs) * shape->HV *
+           shape->K * shape->V * sizeof(float);
+}
+
+kda_status kda_recurrent_bwd(const void *q, const void *k, const void *v, const float *g,
+                             const void *beta, const float *h0, const int32_t *cu_seqlens,
+                             const kda_shape *shape, const void *dout, const float *dht, float *dq,
+                             float *dk, float *dv, float *dg, float *dbeta, float *dh0,
+                             void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                             kda_stream_t stream) {
+    const char *op = "kda_recurrent_bwd";
+    kda_status st = check_common(op, shape, cu_seqlens);
+    if (st != KDA_OK) return st;
+    if ((st = check_fwd_pointers(op, shape, q, k, v, g, beta, dout, cu_seqlens)) != KDA_OK) return st;
+    if (shape->flags & (KDA_FLAG_G_IS_CUMSUM | KDA_FLAG_QK_L2NORM))
+        return fail(KDA_ERR_UNSUPPORTED, "%s: KDA_FLAG_G_IS_CUMSUM and KDA_FLAG_QK_L2NORM are not "
+                    "supported by the backward", op);
+    if (shape->K > 128) return fail(KDA_ERR_UNSUPPORTED, "%s: K=%d > 128", op, shape->K);
+    const bool has_rows = (int64_t)shape->B * shape->T > 0;
+    if (has_rows && (!dq || !dk || !dv || !dg || !dbeta))
+        return fail(KDA_ERR_INVALID_ARG, "%s: dq, dk, dv, dg and dbeta must be non-NULL", op);
+    const size_t need = kda_recurrent_bwd_workspace_size(shape);
+    if (need > 0 && (!workspace || workspace_bytes < need))
+        return fail(KDA_ERR_INVALID_ARG, "%s: workspace of %zu bytes needed, %zu given", op, need,
+                    workspace_bytes);
+    if ((uintptr_t)workspace % 16 != 0)
+        return fail(KDA_ERR_INVALID_ARG, "%s: workspace must be 16-byte aligned", op);
+    const int64_t blocks = (int64_t)shape->num_seqs * shape->HV * ((shape->V + 31) / 32);
+    if (blocks > INT_MAX) return fail(KDA_ERR_UNSUPPORTED, "%s: grid too large", op);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // dq, dk, dg, dbeta accumulate over value columns (and value heads); dv and rows
+    // outside every sequence are zero unless written.
+    const size_t rows = (size_t)shape->B * shape->T;
+    cudaError_t e = cudaSuccess;
+    if (rows > 0) {
+        const size_t zero[5][2] = {{(size_t)dq, rows * shape->H * shape->K},
+                                   {(size_t)dk, rows * shape->H * shape->K},
+                                   {(size_t)dg, rows * shape->HV * shape->K},
+                                   {(size_t)dbeta, rows * shape->HV},
+                                   {(size_t)dv, rows * shape->HV * shape->V}};
+        for (const auto &z : zero)
+            if (e == cudaSuccess) e = cudaMemsetAsync(reinterpret_cast<void *>(z[0]), 0, z[1] * 4, s);
+        if (e != cudaSuccess) return cuda_fail(e, op);
+    }
+    kda::RecurrentBwdArgs a;
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.h0 = h0; a.cu = cu_seqlens;
+    a.dout = dout; a.dht = dht;
+    a.dq = dq; a.dk = dk; a.dv = dv; a.dg = dg; a.dbeta = dbeta; a.dh0 = dh0;
+    a.ckpt = static_cast<float *>(workspace);
+    a.status = dev_status;
+    a.B = shape->B; a.T = shape->T; a.H = shape->H; a.HV = shape->HV; a.K = shape->K;
+    a.V = shape->V; a.N = shape->num_seqs;
+    a.scale = resolve_scale(shape);
+    a.g_scale = shape->g_scale;
+    e = kda::launch_recurrent_bwd(a, shape->dtype, s);
+    if (e != cudaSuccess) return cuda_fail(e, op);
+    g_last_error.clear();
+    return KDA_OK;
+}
+
 size_t kda_chunk_workspace_size(const kda_shape *shape) {
     if (!shape || shape->K <= 0 || shape->V <= 0 || shape->HV <= 0 || shape->B <= 0 ||
         shape->T < 0 || shape->num_seqs < 0)

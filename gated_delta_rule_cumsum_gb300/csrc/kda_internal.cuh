@@ -114,6 +114,24 @@ struct RecurrentArgs {
 };
 cudaError_t launch_recurrent(const RecurrentArgs &a, kda_dtype dt, cudaStream_t st);
 
+// Gradients of the token recurrence (kda_recurrent_bwd).
+struct RecurrentBwdArgs {
+    const void *q, *k, *v;
+    const float *g;
+    const void *beta;
+    const float *h0;
+    const int32_t *cu;
+    const void *dout;          // [B,T,HV,V], q's dtype
+    const float *dht;          // [N,HV,K,V] or NULL
+    float *dq, *dk, *dv, *dg, *dbeta, *dh0;  // fp32; dq, dk, dg, dbeta accumulate (zeroed first)
+    float *ckpt;               // [slots][HV][K][V]: S at the start of every 16-token group
+    int32_t *status;
+    int B, T, H, HV, K, V, N;
+    float scale, g_scale;
+};
+int64_t recurrent_bwd_ckpt_slots(int B, int T, int N);
+cudaError_t launch_recurrent_bwd(const RecurrentBwdArgs &a, kda_dtype dt, cudaStream_t st);
+
 struct ChunkArgs {
     const void *q, *k, *v;
     const float *g;

@@ -12,20 +12,23 @@
  * ALGORITHM.md, preamble; attention-gym PR #317 "Add fused recurrent_kda for
  * decode and inference prefill", PR description).
  *
- * Three operations:
+ * Operations:
  *   kda_gate_cumsum    chunk-local gate cumsum (ALGORITHM.md, Stage 1)
  *   kda_chunk_fwd      chunked forward, BT = 64 (ALGORITHM.md, Stages 1-4)
  *   kda_recurrent_fwd  token-by-token forward for decode (PR #317)
  * each also as an *_act variant that applies the gate and beta activations to
- * raw inputs inside the op (kda_activation below).
+ * raw inputs inside the op (kda_activation below), and
+ *   kda_recurrent_bwd  the gradients of the recurrence (ALGORITHM.md, Backward)
  *
  * Conventions shared by every entry point
  * ---------------------------------------
  * Memory.  Every tensor pointer is a DEVICE pointer owned by the caller, on
  * the current CUDA device.  The library allocates no memory and keeps no
- * global state beyond a per-process cache of device attributes.  All work is
- * enqueued on `stream` (NULL = the legacy default stream); calls return
- * without synchronising, except kda_read_device_status.
+ * global state beyond a per-process cache of device attributes and, once a
+ * pipelined kda_chunk_fwd call has run on a device, one stream and two events
+ * there (KDA_FLAG_SERIAL).  All work is enqueued on `stream` (NULL = the legacy
+ * default stream); calls return without synchronising, except
+ * kda_read_device_status.
  *
  * Layouts (all C-contiguous, row-major):
  *   q, k        [B, T, H, K]     dtype `shape->dtype`
@@ -263,6 +266,34 @@ kda_status kda_recurrent_fwd_act(const void *q, const void *k, const void *v, co
                                  const void *beta, const float *h0, const int32_t *cu_seqlens,
                                  const kda_shape *shape, const kda_activation *act, void *o,
                                  float *ht, int32_t *dev_status, kda_stream_t stream);
+
+/*
+ * kda_recurrent_bwd -- gradients of the token recurrence: given do = dL/do and
+ * dht = dL/dht, dq, dk, dv, dbeta, dg (with respect to the per-token gate g, the
+ * same g kda_recurrent_fwd takes) and dh0.  The contract is kernel-fun
+ * 0.2.0.dev1 sdist, ALGORITHM.md, "Backward" (kernel-fun wheel, kda/chain.py,
+ * backward: dq, dk, dv, dbeta, dg, dh0; GVA gradients of q and k summed over the
+ * value heads that share them); the result is computed for the recurrence the
+ * chunked form reaches exactly, in fp32 whatever the input dtype.
+ *   q, k, v, g, beta, h0, cu_seqlens, shape   as for kda_recurrent_fwd.
+ *   dout               [B, T, HV, V], dtype of q.
+ *   dht                [N, HV, K, V] fp32, or NULL (zero).
+ *   dq, dk             [B, T, H, K] fp32 outputs; dv [B, T, HV, V]; dg [B, T, HV, K];
+ *                      dbeta [B, T, HV]; dh0 [N, HV, K, V] or NULL (not stored).
+ *                      Rows outside every sequence are zero.  dq, dk, dg and dbeta
+ *                      are summed with atomic adds: their rounding order varies.
+ *   workspace          kda_recurrent_bwd_workspace_size() bytes, 16-byte aligned:
+ *                      the state at the start of every 16-token group.
+ * Supported: K <= 128, any V; not with KDA_FLAG_QK_L2NORM or KDA_FLAG_G_IS_CUMSUM.
+ */
+kda_status kda_recurrent_bwd(const void *q, const void *k, const void *v, const float *g,
+                             const void *beta, const float *h0, const int32_t *cu_seqlens,
+                             const kda_shape *shape, const void *dout, const float *dht,
+                             float *dq, float *dk, float *dv, float *dg, float *dbeta, float *dh0,
+                             void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                             kda_stream_t stream);
+/* Bytes of workspace kda_recurrent_bwd needs for *shape (0 on invalid shapes). */
+size_t kda_recurrent_bwd_workspace_size(const kda_shape *shape);
 
 /*
  * kda_read_device_status -- synchronise `stream`, copy the status word to

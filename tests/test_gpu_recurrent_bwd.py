@@ -1,0 +1,104 @@
+"""kda_recurrent_bwd against the fp64 oracle's gradients, through the C ABI (GPU)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import backward as ob
+from tests import parity
+from tests.test_gpu_recurrent import _packed, _small
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-3  # max |error| / max |gradient|, per gradient (fp32 arithmetic, fp64 oracle)
+
+
+def _np(t):
+    return None if t is None else t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def _ref(inp, dout, dht, g_scale=1.0, h0_zero=False):
+    h0 = inp["h0"]
+    if h0 is None and h0_zero:
+        N, HV, K, V = inp["N"], inp["v"].shape[2], inp["q"].shape[3], inp["v"].shape[3]
+        h0 = torch.zeros(N, HV, K, V)
+    cu = inp["cu_seqlens"]
+    return ob.recurrent_grads(_np(inp["q"]), _np(inp["k"]), _np(inp["v"]), _np(inp["g"]),
+                              _np(inp["beta"]), _np(dout), _np(h0), _np(dht),
+                              cu_seqlens=None if cu is None else cu.cpu().numpy(),
+                              g_scale=g_scale)
+
+
+def _run(kda, inp, dout, dht, **kw):
+    return kda.recurrent_kda_backward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], dout,
+                                      inp["h0"], dht, cu_seqlens=inp["cu_seqlens"], **kw)
+
+
+def _grads_in(inp, seed):
+    gen = torch.Generator().manual_seed(seed)
+    dout = torch.randn(inp["v"].shape, generator=gen).to(inp["q"].dtype).cuda()
+    N, HV, K, V = inp["N"], inp["v"].shape[2], inp["q"].shape[3], inp["v"].shape[3]
+    dht = torch.randn(N, HV, K, V, generator=gen).cuda()
+    return dout, dht
+
+
+def _compare(got, ref, rows=None):
+    for name in ("dq", "dk", "dv", "dg", "dbeta", "dh0"):
+        if ref.get(name) is None or got.get(name) is None:
+            continue
+        g, r = _np(got[name]), ref[name]
+        if rows is not None and name != "dh0":
+            g, r = g[:, :rows], r[:, :rows]
+        err = parity.rel_err(g, r)
+        assert err <= TOL, (name, err)
+
+
+@pytest.mark.parametrize("dtype,K,V,T", [
+    (torch.float32, 64, 48, 50),     # a partly used column block, ragged groups
+    (torch.bfloat16, 128, 128, 40),
+    (torch.float32, 32, 64, 17),     # one group plus one token
+])
+def test_dense(kda_lib, dtype, K, V, T):
+    inp = _small(500 + K + T, B=2, T=T, H=2, HV=4, K=K, V=V, dtype=dtype)
+    dout, dht = _grads_in(inp, K + V)
+    got = _run(kda_lib, inp, dout, dht)
+    torch.cuda.synchronize()
+    _compare(got, _ref(inp, dout, dht))
+
+
+def test_packed_with_empty_slots_and_nan_tail(kda_lib):
+    lens = [5, 0, 17, 33, 1, 0]
+    inp = _packed(61, lens, HV=4, H=2, K=64, V=48)
+    dout, dht = _grads_in(inp, 62)
+    st = kda_lib.new_status()
+    got = _run(kda_lib, inp, dout, dht, dev_status=st)
+    assert kda_lib.kda_read_device_status(st) == (0, 0)
+    end = sum(lens)
+    _compare(got, _ref(inp, dout, dht), rows=end)
+    for name in ("dq", "dk", "dv", "dg", "dbeta"):  # rows past the last offset stay zero
+        assert torch.all(got[name][:, end:] == 0), name
+    for n, L in enumerate(lens):
+        if L == 0:  # an empty slot passes the state gradient through bitwise
+            assert torch.equal(got["dh0"][n].view(torch.int32), dht[n].view(torch.int32))
+
+
+def test_natural_log_gate_scale(kda_lib):
+    inp = _small(71, B=1, T=45, H=1, HV=2, K=64, V=64, dtype=torch.float32)
+    dout, dht = _grads_in(inp, 72)
+    got = _run(kda_lib, inp, dout, dht, g_scale=1.0 / math.log(2.0))
+    _compare(got, _ref(inp, dout, dht, g_scale=1.0 / math.log(2.0)))
+
+
+def test_without_initial_state_and_final_state_gradient(kda_lib):
+    inp = _small(81, B=2, T=30, H=2, HV=2, K=64, V=32, h0=False, dtype=torch.float32)
+    dout, _ = _grads_in(inp, 82)
+    got = _run(kda_lib, inp, dout, None)
+    _compare(got, _ref(inp, dout, None, h0_zero=True))
+
+
+def test_grouped_value_heads_sum_into_q_and_k(kda_lib):
+    inp = _small(91, B=1, T=33, H=1, HV=4, K=64, V=64, dtype=torch.float32)
+    dout, dht = _grads_in(inp, 92)
+    got = _run(kda_lib, inp, dout, dht)
+    _compare(got, _ref(inp, dout, dht))
