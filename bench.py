@@ -9,7 +9,7 @@ HBM before the timed region; a 512 MiB buffer is written between timed steps
 to flush the 129 MB L2.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload train|gva|packed|decode|prefill|prefill_small]
+                  [--workload train|gva|packed|decode|prefill|prefill_small|train_bwd]
 
 `--workload` picks one of the other synthetic workloads instead (grouped value
 heads B4 T4096 HV32; packed varlen H=HV=32; decode 4096 x 1 token; its
@@ -48,7 +48,10 @@ WORKLOADS = {
     "prefill": (4, {"T": 256}, 10, 3),
     # the prefill variant on 256 of the 4096 sequences: the size an ncu capture takes
     "prefill_small": (4, {"T": 256, "B": 256, "decode_seqs": 256}, 20, 3),
+    # gradients of the training shape's recurrence (kda_recurrent_bwd)
+    "train_bwd": (1, {}, 10, 3),
 }
+BWD_FLOPS_PER_ELEMENT = 26   # one forward pass (7) + the reverse sweep (19) per state element
 RECURRENT = ("decode", "prefill", "prefill_small")
 FP32_LANES_PER_SM = 128      # fp32 FMA lanes per SM (4 partitions x 32)
 E2E_MAX_H2D = 8 << 30        # larger inputs are not staged through pinned host memory
@@ -57,6 +60,8 @@ E2E_MAX_H2D = 8 << 30        # larger inputs are not staged through pinned host 
 def _metric(name, w):
     if name == "train":
         return METRIC
+    if name == "train_bwd":
+        return f"recurrent_kda bwd tokens/s ({w.name}) on 1 GB300"
     op = "recurrent_kda" if name in RECURRENT else "chunk_kda"
     return f"{op} fwd tokens/s ({w.name}) on 1 GB300"
 
@@ -381,7 +386,22 @@ def run_ours(args):
     status = kda.new_status(dev)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    if recurrent:
+    backward = args.workload == "train_bwd"
+    if backward:
+        # dL/do and dL/dht drawn once; the gradients land in preallocated fp32 buffers.
+        gen = torch.Generator(device=dev).manual_seed(11)
+        dout = torch.randn(v.shape, generator=gen, device=dev).to(q.dtype)
+        ht = torch.randn(inp["N"], w.HV, w.K, w.V, generator=gen, device=dev)  # dht
+        ws = torch.empty(kda.kda_recurrent_bwd_workspace_size(shape), dtype=torch.uint8,
+                         device=dev)
+        grads = [torch.empty(t.shape, dtype=torch.float32, device=dev) for t in (q, k, v, g, beta)]
+        dh0 = torch.empty(inp["N"], w.HV, w.K, w.V, dtype=torch.float32, device=dev)
+
+        def call(q_, k_, v_, g_, beta_, h0_, o_, ht_, st):
+            kda.kda_recurrent_bwd(q_, k_, v_, g_, beta_, h0_, cu, shape, o_, ht_, *grads, dh0, ws,
+                                  status, st)
+        o = dout
+    elif recurrent:
         # Decode keeps the state resident and updates it in place (ht == h0).
         ht, ws = h0, None
 
@@ -451,7 +471,18 @@ def run_ours(args):
     traffic = _traffic(dom, args.workload)
     r_b, w_b = algorithmic_bytes(inp)
     path_gbs = (r_b + w_b) / (ms / 1e3) / 1e9
-    if args.workload.startswith("prefill"):
+    if backward:
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        peak = fp32_fma_tflops(sms, peaks["sm_max_mhz"])
+        flops = BWD_FLOPS_PER_ELEMENT * inp["tokens"] * w.HV * w.K * w.V
+        step_ms = sum(t for t, _ in per_kernel.values()) / prof_steps
+        roofline = {"bound": "alu", "kernel": "recurrent_ckpt+recurrent_bwd",
+                    "achieved": flops / (step_ms / 1e3) / 1e12, "peak": peak, "unit": "TFLOP/s",
+                    "frac": flops / (step_ms / 1e3) / 1e12 / peak, "traffic": None,
+                    "algorithmic_flops": flops, "kernel_ms": step_ms,
+                    "peak_source": f"derived: {sms} SMs x {FP32_LANES_PER_SM} fp32 lanes x 2 "
+                                   f"x {peaks['sm_max_mhz']:.0f} MHz"}
+    elif args.workload.startswith("prefill"):
         # 256 tokens per state: the recurrence's fp32 FMAs, not HBM, bound it.
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
         peak = fp32_fma_tflops(sms, peaks["sm_max_mhz"])
@@ -480,7 +511,10 @@ def run_ours(args):
     names = ("q", "k", "v", "g", "beta") + (("h0",) if h0 is not None and not recurrent else ())
     h2d = sum(_nbytes(inp[n]) for n in names)
     e2e = None
-    if h2d > E2E_MAX_H2D:
+    if backward:
+        e2e = {"value": None, "unit": UNIT,
+               "skipped": "backward: in training the gradients stay on the device"}
+    elif h2d > E2E_MAX_H2D:
         e2e = {"value": None, "unit": UNIT,
                "skipped": f"{h2d / 2**30:.1f} GiB of inputs per step exceed the "
                           f"{E2E_MAX_H2D >> 30} GiB pinned staging limit"}
@@ -561,7 +595,7 @@ def run_ours(args):
                "sequential_ms_per_step": e2e_seq_ms}
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not backward:
         rate, runs, text, cores = cpu_oracle_rate(inp, budget_s=10.0)
         cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": f"{text} x {w.HV} heads, {runs} run(s), fp64"}
@@ -580,6 +614,7 @@ def run_ours(args):
                    "V": w.V, "input_dtype": "bf16", "gate_dtype": "f32",
                    "h0": "N(0,0.1) fp32" if h0 is not None else "none",
                    "ht": "in place (ht == h0)" if recurrent else "stored",
+                   "pass": "backward" if backward else "forward",
                    "sequences": inp["N"], "tokens": tokens,
                    "l2_flush": "512 MiB write between timed steps",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
