@@ -16,13 +16,15 @@
 //     dS' = dS + k da^T             de = rowsum(dS' o S_{t-1}),  dg = de e ln2 g_scale
 //     dS  = Diag(e) dS'             (the gradient of S_{t-1})
 //
-// Layout: one CTA of 8 warps per (sequence, value head, 32 value columns); warp w
-// owns columns 4w .. 4w + 3 of the block for all K <= 128 state rows, lane l the
-// rows l + 32 r.  Value columns evolve independently in the recurrence, so the
-// warps never exchange state: only dq, dk, de and dbeta sum over columns (shared
-// memory atomics within the CTA, then one fp32 global atomic add per (token,
-// row) per CTA).  The states S_{t-1} are recomputed: a first pass stores S at
-// the start of every 16-token group; the backward then takes each group's two
+// Layout: one CTA of 16 warps per (sequence, value head, 16 value columns); warp
+// w owns column w of the block for all K <= 128 state rows, lane l the rows
+// l + 32 r.  Value columns evolve independently in the recurrence, so the warps
+// never exchange state: only dq, dk, de and dbeta sum over columns (shared memory
+// atomics within the CTA, then one fp32 global atomic add per (token, row) per
+// CTA).  Tokens go in groups of 16: the CTA stages a group's k, 2^g, q, v, do and
+// beta in shared memory, the next group's values travelling in registers while
+// the current one is computed.  The states S_{t-1} are recomputed: a first pass
+// stores S at the start of every group; the backward then takes each group's two
 // 8-token halves in reverse, recomputing from the group's checkpoint and keeping
 // the half's eight states in shared memory.
 #include "kda_internal.cuh"
@@ -30,35 +32,13 @@
 namespace kda {
 namespace {
 
-constexpr int kBG = 16;      // tokens per checkpoint
-constexpr int kBR = 8;       // tokens per backward half-group
-constexpr int kBWarps = 8;
-constexpr int kBCols = 4;    // value columns per warp
-constexpr int kBBlock = kBWarps * kBCols;
-constexpr int kBRows = 4;    // state rows per lane (K <= 128)
+constexpr int kBG = 16;       // tokens per group and per checkpoint
+constexpr int kBR = 8;        // tokens per backward half-group
+constexpr int kBWarps = 16;   // one value column per warp
+constexpr int kBThreads = kBWarps * 32;
+constexpr int kBRows = 4;     // state rows per lane (K <= 128)
+constexpr int kBK = 128;
 constexpr float kLn2 = 0.69314718055994531f;
-
-struct Lane {
-    int d[kBRows];      // state rows
-    bool rok[kBRows];
-    int col[kBCols];    // value columns
-    bool cok[kBCols];
-};
-
-__device__ __forceinline__ Lane lane_map(const RecurrentBwdArgs &p, int vb, int warp, int lane) {
-    Lane L;
-#pragma unroll
-    for (int r = 0; r < kBRows; ++r) {
-        L.d[r] = lane + 32 * r;
-        L.rok[r] = L.d[r] < p.K;
-    }
-#pragma unroll
-    for (int c = 0; c < kBCols; ++c) {
-        L.col[c] = vb * kBBlock + warp * kBCols + c;
-        L.cok[c] = L.col[c] < p.V;
-    }
-    return L;
-}
 
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
@@ -90,83 +70,117 @@ __device__ __forceinline__ int64_t ckpt_slot(const RecurrentBwdArgs &p, int n, i
     return (int64_t)(bos / kBG) + n + grp;
 }
 
-// One token's inputs as this lane needs them.
-struct Tok {
-    float e[kBRows], k[kBRows], q[kBRows];
-    float v[kBCols], dout[kBCols];
-    float beta;
+// A group's token inputs in shared memory: rows [kBG][128] of k, 2^g and (for
+// the backward) q; columns [kBG][kBWarps] of v and do; beta [kBG].
+struct Stage {
+    float *k, *e, *q, *v, *dout, *beta;
+};
+constexpr int kStageFloats = 3 * kBG * kBK + 2 * kBG * kBWarps + kBG;
+
+__device__ __forceinline__ Stage stage_at(float *base) {
+    Stage s;
+    s.k = base;
+    s.e = s.k + kBG * kBK;
+    s.q = s.e + kBG * kBK;
+    s.v = s.q + kBG * kBK;
+    s.dout = s.v + kBG * kBWarps;
+    s.beta = s.dout + kBG * kBWarps;
+    return s;
+}
+
+// The group's values this thread carries: (token, row) pairs tid + 512 i of the
+// 16 x 128 rows, (token, column) pair tid of the 16 x 16 columns, beta tid < 16.
+struct Carry {
+    float k[4], g[4], q[4];
+    float v, dout, beta;
 };
 
-template <typename T>
-__device__ __forceinline__ Tok load_tok(const RecurrentBwdArgs &p, const Lane &L, int b, int t,
-                                        int h, int hv, bool need_q) {
-    Tok x;
-    const size_t row = (size_t)b * p.T + t;
+template <typename T, bool Q>
+__device__ __forceinline__ void carry_load(const RecurrentBwdArgs &p, Carry &c, int b, int t0, int t1,
+                                           int h, int hv, int col0) {
     const T *k = static_cast<const T *>(p.k);
     const T *q = static_cast<const T *>(p.q);
     const T *v = static_cast<const T *>(p.v);
     const T *dout = static_cast<const T *>(p.dout);
 #pragma unroll
-    for (int r = 0; r < kBRows; ++r) {
-        x.e[r] = 0.f;
-        x.k[r] = 0.f;
-        x.q[r] = 0.f;
-        if (L.rok[r]) {
-            x.k[r] = to_f32(k[(row * p.H + h) * p.K + L.d[r]]);
-            if (need_q) x.q[r] = to_f32(q[(row * p.H + h) * p.K + L.d[r]]);
-            x.e[r] = exp2f(p.g_scale * p.g[(row * p.HV + hv) * p.K + L.d[r]]);
+    for (int i = 0; i < 4; ++i) {
+        const int idx = threadIdx.x + kBThreads * i, u = idx >> 7, d = idx & 127;
+        c.k[i] = c.g[i] = c.q[i] = 0.f;
+        if (t0 + u < t1 && d < p.K) {
+            const size_t row = (size_t)b * p.T + t0 + u;
+            c.k[i] = to_f32(k[(row * p.H + h) * p.K + d]);
+            c.g[i] = p.g[(row * p.HV + hv) * p.K + d];
+            if (Q) c.q[i] = to_f32(q[(row * p.H + h) * p.K + d]);
         }
     }
-#pragma unroll
-    for (int c = 0; c < kBCols; ++c) {
-        x.v[c] = L.cok[c] ? to_f32(v[(row * p.HV + hv) * p.V + L.col[c]]) : 0.f;
-        x.dout[c] = (need_q && L.cok[c]) ? to_f32(dout[(row * p.HV + hv) * p.V + L.col[c]]) : 0.f;
+    const int u = threadIdx.x / kBWarps, cc = threadIdx.x % kBWarps;  // 512 threads: 32 x 16
+    c.v = c.dout = 0.f;
+    if (u < kBG && t0 + u < t1 && col0 + cc < p.V) {
+        const size_t vr = (((size_t)b * p.T + t0 + u) * p.HV + hv) * p.V + col0 + cc;
+        c.v = to_f32(v[vr]);
+        if (Q) c.dout = to_f32(dout[vr]);
     }
-    x.beta = to_f32(static_cast<const T *>(p.beta)[row * p.HV + hv]);
-    return x;
+    c.beta = 0.f;
+    if ((int)threadIdx.x < kBG && t0 + (int)threadIdx.x < t1)
+        c.beta = to_f32(static_cast<const T *>(p.beta)[((size_t)b * p.T + t0 + threadIdx.x) * p.HV + hv]);
 }
 
-// S <- Diag(e) S + k (beta (v - (Diag(e) S)^T k))^T for this warp's columns.
-__device__ __forceinline__ void step(float (&S)[kBRows][kBCols], const Tok &x) {
-    float a[kBCols];
+template <bool Q>
+__device__ __forceinline__ void carry_store(const RecurrentBwdArgs &p, const Carry &c, const Stage &s) {
 #pragma unroll
-    for (int c = 0; c < kBCols; ++c) {
-        float part = 0.f;
-#pragma unroll
-        for (int r = 0; r < kBRows; ++r) part = fmaf(x.e[r] * S[r][c], x.k[r], part);
-        a[c] = warp_sum(part);
+    for (int i = 0; i < 4; ++i) {
+        const int idx = threadIdx.x + kBThreads * i;
+        s.k[idx] = c.k[i];
+        s.e[idx] = exp2f(p.g_scale * c.g[i]);  // entries past K or the group: g = 0, unused
+        if (Q) s.q[idx] = c.q[i];
     }
+    const int u = threadIdx.x / kBWarps, cc = threadIdx.x % kBWarps;
+    if (u < kBG) {
+        s.v[u * kBWarps + cc] = c.v;
+        if (Q) s.dout[u * kBWarps + cc] = c.dout;
+    }
+    if ((int)threadIdx.x < kBG) s.beta[threadIdx.x] = c.beta;
+}
+
+// S <- Diag(e) S + k (beta (v - (Diag(e) S)^T k))^T for this warp's column (token u of the stage).
+__device__ __forceinline__ void step(float (&S)[kBRows], const Stage &s, int u, int lane, int w) {
+    float e[kBRows], k[kBRows], part = 0.f;
 #pragma unroll
-    for (int c = 0; c < kBCols; ++c) {
-        const float delta = x.beta * (x.v[c] - a[c]);
+    for (int r = 0; r < kBRows; ++r) {
+        e[r] = s.e[u * kBK + lane + 32 * r];
+        k[r] = s.k[u * kBK + lane + 32 * r];
+        part = fmaf(e[r] * S[r], k[r], part);
+    }
+    const float a = warp_sum(part);
+    const float delta = s.beta[u] * (s.v[u * kBWarps + w] - a);
 #pragma unroll
-        for (int r = 0; r < kBRows; ++r) S[r][c] = fmaf(x.e[r], S[r][c], x.k[r] * delta);
+    for (int r = 0; r < kBRows; ++r) S[r] = fmaf(e[r], S[r], k[r] * delta);
+}
+
+__device__ __forceinline__ void load_col(const float *src, const RecurrentBwdArgs &p, int lane,
+                                         int col, float (&S)[kBRows]) {
+#pragma unroll
+    for (int r = 0; r < kBRows; ++r) {
+        const int d = lane + 32 * r;
+        S[r] = (src && d < p.K && col < p.V) ? src[(size_t)d * p.V + col] : 0.f;
     }
 }
 
-__device__ __forceinline__ void load_state(const float *src, const RecurrentBwdArgs &p, const Lane &L,
-                                           float (&S)[kBRows][kBCols]) {
+__device__ __forceinline__ void store_col(float *dst, const RecurrentBwdArgs &p, int lane, int col,
+                                          const float (&S)[kBRows]) {
 #pragma unroll
-    for (int r = 0; r < kBRows; ++r)
-#pragma unroll
-        for (int c = 0; c < kBCols; ++c)
-            S[r][c] = (src && L.rok[r] && L.cok[c]) ? src[(size_t)L.d[r] * p.V + L.col[c]] : 0.f;
-}
-
-__device__ __forceinline__ void store_state(float *dst, const RecurrentBwdArgs &p, const Lane &L,
-                                            const float (&S)[kBRows][kBCols]) {
-#pragma unroll
-    for (int r = 0; r < kBRows; ++r)
-#pragma unroll
-        for (int c = 0; c < kBCols; ++c)
-            if (L.rok[r] && L.cok[c]) dst[(size_t)L.d[r] * p.V + L.col[c]] = S[r][c];
+    for (int r = 0; r < kBRows; ++r) {
+        const int d = lane + 32 * r;
+        if (d < p.K && col < p.V) dst[(size_t)d * p.V + col] = S[r];
+    }
 }
 
 // Pass 1: the recurrence, storing S at the start of every 16-token group.
 template <typename T>
-__global__ void __launch_bounds__(kBWarps * 32) recurrent_ckpt_kernel(RecurrentBwdArgs p) {
+__global__ void __launch_bounds__(kBThreads) recurrent_ckpt_kernel(RecurrentBwdArgs p) {
+    __shared__ float sm[kStageFloats];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nvb = (p.V + kBBlock - 1) / kBBlock;
+    const int nvb = (p.V + kBWarps - 1) / kBWarps;
     const int64_t bid = blockIdx.x;
     const int vb = (int)(bid % nvb);
     const int hv = (int)((bid / nvb) % p.HV);
@@ -174,32 +188,38 @@ __global__ void __launch_bounds__(kBWarps * 32) recurrent_ckpt_kernel(RecurrentB
     const int h = hv / (p.HV / p.H);
     int b, bos, eos;
     if (!seq_range(p, n, b, bos, eos)) return;
-    const Lane L = lane_map(p, vb, warp, lane);
+    const int col0 = vb * kBWarps, col = col0 + warp;
     const size_t hvo = (size_t)hv * p.K * p.V;
-    float S[kBRows][kBCols];
-    load_state(p.h0 ? p.h0 + (size_t)n * p.HV * p.K * p.V + hvo : nullptr, p, L, S);
-    for (int t = bos; t < eos; ++t) {
-        const int u = t - bos;
-        if (u % kBG == 0)
-            store_state(p.ckpt + ckpt_slot(p, n, bos, u / kBG) * p.HV * p.K * p.V + hvo, p, L, S);
-        const Tok x = load_tok<T>(p, L, b, t, h, hv, false);
-        step(S, x);
+    const Stage s = stage_at(sm);
+    float S[kBRows];
+    load_col(p.h0 ? p.h0 + (size_t)n * p.HV * p.K * p.V + hvo : nullptr, p, lane, col, S);
+    const int ng = (eos - bos + kBG - 1) / kBG;
+    Carry c;
+    if (ng > 0) carry_load<T, false>(p, c, b, bos, eos, h, hv, col0);
+    for (int grp = 0; grp < ng; ++grp) {
+        const int t0 = bos + grp * kBG, t1 = min(t0 + kBG, eos);
+        __syncthreads();  // the previous group is done with the stage
+        carry_store<false>(p, c, s);
+        if (grp + 1 < ng) carry_load<T, false>(p, c, b, t1, min(t1 + kBG, eos), h, hv, col0);
+        __syncthreads();
+        store_col(p.ckpt + ckpt_slot(p, n, bos, grp) * p.HV * p.K * p.V + hvo, p, lane, col, S);
+        for (int u = 0; u < t1 - t0; ++u) step(S, s, u, lane, warp);
     }
 }
 
 // Pass 2: the reverse sweep.
 template <typename T>
-__global__ void __launch_bounds__(kBWarps * 32, 1) recurrent_bwd_kernel(RecurrentBwdArgs p) {
+__global__ void __launch_bounds__(kBThreads) recurrent_bwd_kernel(RecurrentBwdArgs p) {
     extern __shared__ __align__(16) float sm[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // per warp: the half-group's states S_{t-1}, [kBR][kBRows][32 lanes] float4 (4 columns)
-    float4 *st = reinterpret_cast<float4 *>(sm) + (size_t)warp * kBR * kBRows * 32;
-    float *acc_q = sm + kBWarps * kBR * kBRows * 32 * 4;  // [kBR][128]
-    float *acc_k = acc_q + kBR * 128;
-    float *acc_e = acc_k + kBR * 128;
-    float *acc_b = acc_e + kBR * 128;                    // [kBR]
+    const Stage s = stage_at(sm);
+    float *st = sm + kStageFloats + (size_t)warp * kBR * kBRows * 32;  // [kBR][kBRows][32]
+    float *acc_q = sm + kStageFloats + kBWarps * kBR * kBRows * 32;    // [kBR][128]
+    float *acc_k = acc_q + kBR * kBK;
+    float *acc_e = acc_k + kBR * kBK;
+    float *acc_b = acc_e + kBR * kBK;                                   // [kBR]
 
-    const int nvb = (p.V + kBBlock - 1) / kBBlock;
+    const int nvb = (p.V + kBWarps - 1) / kBWarps;
     const int64_t bid = blockIdx.x;
     const int vb = (int)(bid % nvb);
     const int hv = (int)((bid / nvb) % p.HV);
@@ -207,132 +227,111 @@ __global__ void __launch_bounds__(kBWarps * 32, 1) recurrent_bwd_kernel(Recurren
     const int h = hv / (p.HV / p.H);
     int b, bos, eos;
     if (!seq_range(p, n, b, bos, eos)) return;  // uniform over the CTA
-    const Lane L = lane_map(p, vb, warp, lane);
+    const int col0 = vb * kBWarps, col = col0 + warp;
+    const bool cok = col < p.V;
     const size_t hvo = (size_t)hv * p.K * p.V;
     const size_t nso = (size_t)n * p.HV * p.K * p.V;
 
-    for (int i = threadIdx.x; i < 3 * kBR * 128 + kBR; i += blockDim.x) acc_q[i] = 0.f;
-    float dS[kBRows][kBCols];
-    load_state(p.dht ? p.dht + nso + hvo : nullptr, p, L, dS);
-    __syncthreads();
+    for (int i = threadIdx.x; i < 3 * kBR * kBK + kBR; i += blockDim.x) acc_q[i] = 0.f;
+    float dS[kBRows];
+    load_col(p.dht ? p.dht + nso + hvo : nullptr, p, lane, col, dS);
 
-    const int len = eos - bos;
-    for (int grp = (len + kBG - 1) / kBG - 1; grp >= 0; --grp) {
-        const int g0 = bos + grp * kBG;
-        const int g1 = min(g0 + kBG, eos);
+    const int ng = (eos - bos + kBG - 1) / kBG;
+    Carry c;
+    if (ng > 0) {
+        const int g0 = bos + (ng - 1) * kBG;
+        carry_load<T, true>(p, c, b, g0, eos, h, hv, col0);
+    }
+    for (int grp = ng - 1; grp >= 0; --grp) {
+        const int g0 = bos + grp * kBG, g1 = min(g0 + kBG, eos);
+        __syncthreads();  // the previous group is done with the stage
+        carry_store<true>(p, c, s);
+        if (grp > 0) carry_load<T, true>(p, c, b, g0 - kBG, g0, h, hv, col0);
+        __syncthreads();
         const float *ck = p.ckpt + ckpt_slot(p, n, bos, grp) * p.HV * p.K * p.V + hvo;
         for (int half = (g1 - g0 - 1) / kBR; half >= 0; --half) {
-            const int s0 = g0 + half * kBR;
-            const int s1 = min(s0 + kBR, g1);
-            // recompute S_{t-1} for t in [s0, s1) from the group's checkpoint
-            float S[kBRows][kBCols];
-            load_state(ck, p, L, S);
-            for (int t = g0; t < s1; ++t) {
-                if (t >= s0) {
+            const int u0 = half * kBR, u1 = min(u0 + kBR, g1 - g0);
+            // recompute S_{t-1} for the half's tokens from the group's checkpoint
+            float S[kBRows];
+            load_col(ck, p, lane, col, S);
+            for (int u = 0; u < u1; ++u) {
+                if (u >= u0) {
 #pragma unroll
-                    for (int r = 0; r < kBRows; ++r)
-                        st[((t - s0) * kBRows + r) * 32 + lane] =
-                            make_float4(S[r][0], S[r][1], S[r][2], S[r][3]);
+                    for (int r = 0; r < kBRows; ++r) st[((u - u0) * kBRows + r) * 32 + lane] = S[r];
                 }
-                const Tok x = load_tok<T>(p, L, b, t, h, hv, false);
-                step(S, x);
+                step(S, s, u, lane, warp);
             }
-            for (int t = s1 - 1; t >= s0; --t) {
-                const int u = t - s0;
-                const Tok x = load_tok<T>(p, L, b, t, h, hv, true);
-                float Sp[kBRows][kBCols];
+            for (int u = u1 - 1; u >= u0; --u) {
+                const int j = u - u0;
+                float e[kBRows], k[kBRows], q[kBRows], Sp[kBRows], part = 0.f;
 #pragma unroll
                 for (int r = 0; r < kBRows; ++r) {
-                    const float4 f = st[(u * kBRows + r) * 32 + lane];
-                    Sp[r][0] = f.x; Sp[r][1] = f.y; Sp[r][2] = f.z; Sp[r][3] = f.w;
+                    e[r] = s.e[u * kBK + lane + 32 * r];
+                    k[r] = s.k[u * kBK + lane + 32 * r];
+                    q[r] = s.q[u * kBK + lane + 32 * r];
+                    Sp[r] = st[(j * kBRows + r) * 32 + lane];
+                    part = fmaf(e[r] * Sp[r], k[r], part);
                 }
-                float a[kBCols], delta[kBCols];
-#pragma unroll
-                for (int c = 0; c < kBCols; ++c) {
-                    float part = 0.f;
-#pragma unroll
-                    for (int r = 0; r < kBRows; ++r) part = fmaf(x.e[r] * Sp[r][c], x.k[r], part);
-                    a[c] = warp_sum(part);
-                    delta[c] = x.beta * (x.v[c] - a[c]);
-                }
-                // o's gradient into dS, and dq = scale S_t do
-                float dqp[kBRows];
+                const float beta = s.beta[u];
+                const float vv = s.v[u * kBWarps + warp], dd = s.dout[u * kBWarps + warp];
+                const float a = warp_sum(part);
+                const float delta = beta * (vv - a);
+                float dpart = 0.f;
 #pragma unroll
                 for (int r = 0; r < kBRows; ++r) {
-                    float s = 0.f;
-#pragma unroll
-                    for (int c = 0; c < kBCols; ++c) {
-                        const float St = fmaf(x.e[r], Sp[r][c], x.k[r] * delta[c]);
-                        s = fmaf(St, x.dout[c], s);
-                        dS[r][c] = fmaf(p.scale * x.q[r], x.dout[c], dS[r][c]);
-                    }
-                    dqp[r] = p.scale * s;
+                    const float St = fmaf(e[r], Sp[r], k[r] * delta);
+                    if (lane + 32 * r < p.K) atomicAdd(&acc_q[j * kBK + lane + 32 * r], p.scale * St * dd);
+                    dS[r] = fmaf(p.scale * q[r], dd, dS[r]);
+                    dpart = fmaf(dS[r], k[r], dpart);
                 }
-                float ddel[kBCols], da[kBCols];
-                float dbp = 0.f;
-#pragma unroll
-                for (int c = 0; c < kBCols; ++c) {
-                    float part = 0.f;
-#pragma unroll
-                    for (int r = 0; r < kBRows; ++r) part = fmaf(dS[r][c], x.k[r], part);
-                    ddel[c] = warp_sum(part);
-                    da[c] = -x.beta * ddel[c];
-                    dbp = fmaf(ddel[c], x.v[c] - a[c], dbp);
-                }
-                if (lane == 0) {
-                    const size_t vrow = ((size_t)b * p.T + t) * p.HV + hv;
-#pragma unroll
-                    for (int c = 0; c < kBCols; ++c)
-                        if (L.cok[c]) p.dv[vrow * p.V + L.col[c]] = x.beta * ddel[c];
-                    atomicAdd(&acc_b[u], dbp);
+                const float ddel = warp_sum(dpart);
+                const float da = -beta * ddel;
+                if (lane == 0 && cok) {
+                    p.dv[(((size_t)b * p.T + g0 + u) * p.HV + hv) * p.V + col] = beta * ddel;
+                    atomicAdd(&acc_b[j], ddel * (vv - a));
                 }
 #pragma unroll
                 for (int r = 0; r < kBRows; ++r) {
-                    float kp = 0.f, ep = 0.f;
-#pragma unroll
-                    for (int c = 0; c < kBCols; ++c) {
-                        kp = fmaf(dS[r][c], delta[c], kp);
-                        kp = fmaf(x.e[r] * Sp[r][c], da[c], kp);
-                        const float dSp = fmaf(x.k[r], da[c], dS[r][c]);
-                        ep = fmaf(dSp, Sp[r][c], ep);
-                        dS[r][c] = x.e[r] * dSp;
+                    const float kp = fmaf(dS[r], delta, e[r] * Sp[r] * da);
+                    const float dSp = fmaf(k[r], da, dS[r]);
+                    if (lane + 32 * r < p.K) {
+                        atomicAdd(&acc_k[j * kBK + lane + 32 * r], kp);
+                        atomicAdd(&acc_e[j * kBK + lane + 32 * r], dSp * Sp[r]);
                     }
-                    if (L.rok[r]) {
-                        atomicAdd(&acc_q[u * 128 + L.d[r]], dqp[r]);
-                        atomicAdd(&acc_k[u * 128 + L.d[r]], kp);
-                        atomicAdd(&acc_e[u * 128 + L.d[r]], ep);
-                    }
+                    dS[r] = e[r] * dSp;
                 }
             }
             __syncthreads();  // the half-group's sums are complete
-            for (int i = threadIdx.x; i < (s1 - s0) * 128; i += blockDim.x) {
-                const int u = i >> 7, d = i & 127;
+            const int hl = u1 - u0;
+            for (int i = threadIdx.x; i < hl * kBK; i += blockDim.x) {
+                const int j = i >> 7, d = i & 127;
                 if (d < p.K) {
-                    const size_t row = (size_t)b * p.T + s0 + u;
+                    const int u = u0 + j;
+                    const size_t row = (size_t)b * p.T + g0 + u;
                     atomicAdd(&p.dq[(row * p.H + h) * p.K + d], acc_q[i]);
                     atomicAdd(&p.dk[(row * p.H + h) * p.K + d], acc_k[i]);
-                    const size_t gi = (row * p.HV + hv) * p.K + d;
-                    const float e = exp2f(p.g_scale * p.g[gi]);
-                    atomicAdd(&p.dg[gi], acc_e[i] * e * kLn2 * p.g_scale);
+                    atomicAdd(&p.dg[(row * p.HV + hv) * p.K + d],
+                              acc_e[i] * s.e[u * kBK + d] * kLn2 * p.g_scale);
                 }
                 acc_q[i] = acc_k[i] = acc_e[i] = 0.f;
             }
-            if ((int)threadIdx.x < s1 - s0) {
-                atomicAdd(&p.dbeta[((size_t)b * p.T + s0 + threadIdx.x) * p.HV + hv],
+            if ((int)threadIdx.x < hl) {
+                atomicAdd(&p.dbeta[((size_t)b * p.T + g0 + u0 + threadIdx.x) * p.HV + hv],
                           acc_b[threadIdx.x]);
                 acc_b[threadIdx.x] = 0.f;
             }
             __syncthreads();
         }
     }
-    if (p.dh0) store_state(p.dh0 + nso + hvo, p, L, dS);
+    if (p.dh0) store_col(p.dh0 + nso + hvo, p, lane, col, dS);
 }
 
 template <typename T>
 cudaError_t launch_bwd_typed(const RecurrentBwdArgs &a, cudaStream_t st) {
-    const int64_t blocks = (int64_t)a.N * a.HV * ((a.V + kBBlock - 1) / kBBlock);
+    const int64_t blocks = (int64_t)a.N * a.HV * ((a.V + kBWarps - 1) / kBWarps);
     if (blocks == 0) return cudaSuccess;
-    const int smem = (kBWarps * kBR * kBRows * 32 * 4 + 3 * kBR * 128 + kBR) * (int)sizeof(float);
+    const int smem = (kStageFloats + kBWarps * kBR * kBRows * 32 + 3 * kBR * kBK + kBR) *
+                     (int)sizeof(float);
     static bool attr = false;
     if (!attr) {
         cudaError_t e = cudaFuncSetAttribute(recurrent_bwd_kernel<T>,
@@ -341,12 +340,12 @@ cudaError_t launch_bwd_typed(const RecurrentBwdArgs &a, cudaStream_t st) {
         attr = true;
     }
     prof_begin("recurrent_ckpt", st);
-    recurrent_ckpt_kernel<T><<<(unsigned)blocks, kBWarps * 32, 0, st>>>(a);
+    recurrent_ckpt_kernel<T><<<(unsigned)blocks, kBThreads, 0, st>>>(a);
     prof_end(st);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     prof_begin("recurrent_bwd", st);
-    recurrent_bwd_kernel<T><<<(unsigned)blocks, kBWarps * 32, smem, st>>>(a);
+    recurrent_bwd_kernel<T><<<(unsigned)blocks, kBThreads, smem, st>>>(a);
     prof_end(st);
     return cudaGetLastError();
 }
