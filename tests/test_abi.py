@@ -189,3 +189,34 @@ def test_product_never_imports_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "kda_oracle" not in text, f
+
+
+def _bwd(lib, s, grads=True, ws=(FAKE, 1 << 34)):
+    g = FAKE if grads else None
+    return lib.kda_recurrent_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, None, None, ctypes.byref(s), FAKE,
+                                 None, g, g, g, g, g, None, ws[0], ws[1], None, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(K=160), 2),                  # the backward keeps K <= 128
+    (dict(flags=1), 2),                # KDA_FLAG_QK_L2NORM
+    (dict(flags=2), 2),                # KDA_FLAG_G_IS_CUMSUM
+    (dict(HV=3), 1),
+])
+def test_recurrent_bwd_rejects_on_host(lib, kw, status):
+    st = _bwd(lib, _shape(**kw))
+    assert st == status, lib.kda_last_error_message()
+    assert lib.kda_last_error_message()
+
+
+def test_recurrent_bwd_needs_gradients_and_workspace(lib):
+    s = _shape()
+    assert _bwd(lib, s, grads=False) == 1
+    assert b"dq" in lib.kda_last_error_message()
+    need = lib.kda_recurrent_bwd_workspace_size(ctypes.byref(s))
+    # B=1, T=128, H=2, HV=4, K=V=64: 8 (dense) or 8 + 1 + 1 (packed) checkpoint slots of HV*K*V fp32
+    assert need == 10 * 4 * 64 * 64 * 4
+    assert _bwd(lib, s, ws=(ctypes.c_void_p(0x100000), need - 1)) == 1
+    assert b"workspace" in lib.kda_last_error_message()
+    assert _bwd(lib, s, ws=(ctypes.c_void_p(0x100004), need)) == 1
+    assert b"aligned" in lib.kda_last_error_message()

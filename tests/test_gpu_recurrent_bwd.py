@@ -102,3 +102,16 @@ def test_grouped_value_heads_sum_into_q_and_k(kda_lib):
     dout, dht = _grads_in(inp, 92)
     got = _run(kda_lib, inp, dout, dht)
     _compare(got, _ref(inp, dout, dht))
+
+
+def test_invalid_offsets_set_the_status(kda_lib):
+    """A decreasing offset: that slot is skipped with the status bit set; the others run."""
+    inp = _packed(95, [10, 20, 30], HV=2, H=1, K=64, V=32)
+    inp["cu_seqlens"] = torch.tensor([0, 25, 15, 60], dtype=torch.int32, device="cuda")  # decreasing
+    dout, dht = _grads_in(inp, 96)
+    st = kda_lib.new_status()
+    got = _run(kda_lib, inp, dout, dht, dev_status=st)
+    status, bits = kda_lib.kda_read_device_status(st)
+    assert bits & kda_lib.KDA_DEVICE_BAD_CU_SEQLENS
+    for name in ("dq", "dk", "dv", "dg", "dbeta"):
+        assert torch.isfinite(got[name]).all(), name
