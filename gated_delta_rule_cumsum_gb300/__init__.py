@@ -24,7 +24,7 @@ __all__ = [
     "KDA_FLAG_SPLIT_SCAN", "KDA_FLAG_SERIAL", "KdaActivation", "make_activation",
     "KdaError", "KdaShape", "load", "library_path", "make_shape",
     "kda_gate_cumsum", "kda_chunk_fwd", "kda_recurrent_fwd", "kda_chunk_workspace_size",
-    "kda_recurrent_bwd", "kda_recurrent_bwd_workspace_size", "recurrent_kda_backward",
+    "kda_recurrent_bwd", "kda_recurrent_bwd_workspace_size", "recurrent_kda_backward", "kda_autograd",
     "kda_gate_cumsum_act", "kda_chunk_fwd_act", "kda_recurrent_fwd_act",
     "kda_chunk_fwd_noalloc", "KDA_NOALLOC_SCRATCH_BYTES",
     "kda_read_device_status", "kda_clear_device_status", "kda_status_string",
@@ -367,6 +367,46 @@ def recurrent_kda_backward(q, k, v, gate, beta, dout, initial_state=None, dht=No
     kda_recurrent_bwd(q, k, v, g, beta, h0, cu, shape, dout, dht, out["dq"], out["dk"],
                       out["dv"], out["dg"], out["dbeta"], out["dh0"], ws, dev_status, stream)
     return out
+
+
+class _KdaFunction(torch.autograd.Function):
+    """Forward by the chunked (or token) kernels, backward by kda_recurrent_bwd: the
+    chunked form computes the recurrence, so its gradients are the recurrence's."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, g, beta, h0, cu, scale, g_scale, chunked):
+        with torch.no_grad():
+            kw = dict(cu_seqlens=cu, output_final_state=True, scale=scale, g_scale=g_scale)
+            if chunked:
+                o, ht = chunk_kda(q.detach(), k.detach(), v.detach(), g.detach(), beta.detach(),
+                                  initial_state=None if h0 is None else h0.detach(), **kw)
+            else:
+                o, ht = recurrent_kda(q.detach(), k.detach(), v.detach(), g.detach(),
+                                      beta.detach(),
+                                      None if h0 is None else h0.detach(), **kw)
+        ctx.save_for_backward(q, k, v, g, beta, h0, cu)
+        ctx.scale, ctx.g_scale = scale, g_scale
+        return o, ht
+
+    @staticmethod
+    def backward(ctx, do, dht):
+        q, k, v, g, beta, h0, cu = ctx.saved_tensors
+        do = torch.zeros_like(v) if do is None else do.to(q.dtype)
+        gr = recurrent_kda_backward(q, k, v, g, beta, do, h0, dht, cu_seqlens=cu,
+                                    scale=ctx.scale, g_scale=ctx.g_scale, want_dh0=h0 is not None)
+        dh0 = gr["dh0"] if h0 is not None else None
+        return (gr["dq"].to(q.dtype), gr["dk"].to(k.dtype), gr["dv"].to(v.dtype),
+                gr["dg"].to(g.dtype), gr["dbeta"].to(beta.dtype), dh0, None, None, None, None)
+
+
+def kda_autograd(q, k, v, g, beta, initial_state=None, *, cu_seqlens=None, scale=None,
+                 g_scale=1.0, chunked=True):
+    """(o, ht) with gradients: forward by chunk_kda (or recurrent_kda when `chunked` is
+    False), backward by kda_recurrent_bwd; `g` is the per-token log2 gate."""
+    for t in (q, k, v, g, beta, initial_state, cu_seqlens):
+        if t is not None and not t.is_cuda:
+            raise KdaError(KDA_ERR_INVALID_ARG, "tensors must be on a CUDA device")
+    return _KdaFunction.apply(q, k, v, g, beta, initial_state, cu_seqlens, scale, g_scale, chunked)
 
 
 def recurrent_kda(q, k, v, gate, beta, initial_state=None, *, cu_seqlens=None,

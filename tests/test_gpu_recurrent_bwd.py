@@ -115,3 +115,23 @@ def test_invalid_offsets_set_the_status(kda_lib):
     assert bits & kda_lib.KDA_DEVICE_BAD_CU_SEQLENS
     for name in ("dq", "dk", "dv", "dg", "dbeta"):
         assert torch.isfinite(got[name]).all(), name
+
+
+@pytest.mark.parametrize("chunked", [True, False])
+def test_autograd_through_the_forward_kernels(kda_lib, chunked):
+    """loss.backward() through kda_autograd: the forward kernels, then kda_recurrent_bwd;
+    the gradients match the oracle's for the same dL/do and dL/dht."""
+    inp = _small(97, B=1, T=70, H=2, HV=2, K=64, V=64)  # bf16: the tensor-core forward
+    dout, dht = _grads_in(inp, 98)
+    leaves = {n: inp[n].clone().requires_grad_(True) for n in ("q", "k", "v", "g", "beta", "h0")}
+    o, ht = kda_lib.kda_autograd(leaves["q"], leaves["k"], leaves["v"], leaves["g"],
+                                 leaves["beta"], leaves["h0"], chunked=chunked)
+    loss = (o.float() * dout.float()).sum() + (ht * dht).sum()
+    loss.backward()
+    ref = _ref(inp, dout, dht)
+    for name, key in (("q", "dq"), ("k", "dk"), ("v", "dv"), ("g", "dg"), ("beta", "dbeta"),
+                      ("h0", "dh0")):
+        got = leaves[name].grad
+        # bf16 parameters receive gradients rounded to bf16
+        tol = 1e-2 if got.dtype == torch.bfloat16 else TOL
+        assert parity.rel_err(got, ref[key]) <= tol, (name, parity.rel_err(got, ref[key]))
