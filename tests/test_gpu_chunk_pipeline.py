@@ -115,3 +115,26 @@ def test_pipelined_call_replays_in_a_cuda_graph(kda_lib):
         torch.cuda.synchronize()
         assert torch.equal(o, o_eager) and torch.equal(ht, ht_eager)
     assert kda_lib.kda_read_device_status(st) == (0, 0)
+
+
+def test_pipelined_without_final_state_and_with_l2norm(kda_lib):
+    """No final state stored (the first part's state still travels in the workspace)
+    and the q/k L2 norm applied inside, in both parts."""
+    inp = _small(45, B=1, T=8229, H=4, HV=4, K=128, V=128)
+    inp["q"] = (inp["q"].float() * 3.0).to(inp["q"].dtype)  # unnormalised rows
+    inp["k"] = (inp["k"].float() * 0.5).to(inp["k"].dtype)
+    kda_lib.kda_profile_reset()
+    kda_lib.kda_profile_enable(True)
+    try:
+        o, ht = kda_lib.chunk_kda(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                                  initial_state=inp["h0"], output_final_state=False,
+                                  use_qk_l2norm_in_kernel=True)
+        torch.cuda.synchronize()
+        rep = kda_lib.kda_profile_report()
+    finally:
+        kda_lib.kda_profile_enable(False)
+    assert ht is None
+    _assert_pipelined(rep)
+    ref = parity.oracle_forward(inp, l2norm=True)
+    e_o, _ = parity.compare_sampled(inp, o, None, ref, TOL)
+    assert e_o <= TOL, e_o
