@@ -30,8 +30,11 @@ __all__ = ["recurrent_grads"]
 
 
 def recurrent_grads(q, k, v, g, beta, do, h0=None, dht=None, cu_seqlens=None, scale=None,
-                    g_scale=1.0):
+                    g_scale=1.0, l2norm=False):
     """Gradients of sum(o * do) + sum(ht * dht) of the token recurrence, in fp64.
+    With `l2norm` the recurrence uses q / sqrt(sum q^2 + 1e-6) and the same of k per
+    (token, head) (kernel-fun 0.2.0.dev1 wheel, kda/autograd.py, l2norm option), and
+    the gradients are those of the raw q and k.
 
     Shapes: q, k [B,T,H,K]; v, do [B,T,HV,V]; g [B,T,HV,K] (per-token log2 decay);
     beta [B,T,HV]; h0, dht [N,HV,K,V] or None; cu_seqlens [N+1] or None (then N = B).
@@ -60,8 +63,12 @@ def recurrent_grads(q, k, v, g, beta, do, h0=None, dht=None, cu_seqlens=None, sc
         b, bos, eos = (n, 0, T) if cu is None else (0, cu[n], cu[n + 1])
         S = h0t[n] if h0t is not None else torch.zeros(HV, K, V, dtype=torch.float64)
         for t in range(bos, eos):
-            qt = q[b, t].repeat_interleave(G, dim=0)           # [HV, K]
-            kt = k[b, t].repeat_interleave(G, dim=0)
+            qr, kr = q[b, t], k[b, t]                           # [H, K]
+            if l2norm:
+                qr = qr / torch.sqrt((qr * qr).sum(-1, keepdim=True) + 1e-6)
+                kr = kr / torch.sqrt((kr * kr).sum(-1, keepdim=True) + 1e-6)
+            qt = qr.repeat_interleave(G, dim=0)                 # [HV, K]
+            kt = kr.repeat_interleave(G, dim=0)
             S = torch.exp2(g_scale * g[b, t])[:, :, None] * S  # decay rows
             a = torch.einsum("hkv,hk->hv", S, kt)
             delta = beta[b, t][:, None] * (v[b, t] - a)

@@ -26,22 +26,22 @@ def _problem(seed, B=1, T=5, H=1, HV=2, K=3, V=2, packed=True):
     return dict(q=q, k=k, v=v, g=g, beta=beta, h0=h0, do=do, dht=dht, cu=cu)
 
 
-def _loss(p, g_scale=1.0):
+def _loss(p, g_scale=1.0, l2norm=False):
     """sum(o * do) + sum(ht * dht) through the C oracle's forward."""
     o, ht = oracle.recurrent(p["q"], p["k"], p["v"], p["g"], p["beta"], h0=p["h0"],
-                             cu_seqlens=p["cu"], g_scale=g_scale, o_fill=0.0)
+                             cu_seqlens=p["cu"], g_scale=g_scale, l2norm=l2norm, o_fill=0.0)
     return float((o * p["do"]).sum() + (ht * p["dht"]).sum())
 
 
-def _fd(p, name, g_scale=1.0, eps=1e-6):
+def _fd(p, name, g_scale=1.0, eps=1e-6, l2norm=False):
     x = p[name]
     out = np.zeros_like(x)
     for idx in np.ndindex(*x.shape):
         keep = x[idx]
         x[idx] = keep + eps
-        up = _loss(p, g_scale)
+        up = _loss(p, g_scale, l2norm)
         x[idx] = keep - eps
-        dn = _loss(p, g_scale)
+        dn = _loss(p, g_scale, l2norm)
         x[idx] = keep
         out[idx] = (up - dn) / (2 * eps)
     return out
@@ -106,3 +106,18 @@ def test_a_planted_sign_error_fails_the_finite_differences():
     loss.backward()
     err = np.abs(kk.grad.numpy() - want).max() / np.abs(want).max()
     assert err > 1e-2
+
+
+def test_l2norm_gradients_match_finite_differences():
+    p = _problem(8)
+    p["q"] *= 2.5  # unnormalised rows
+    got = ob.recurrent_grads(p["q"], p["k"], p["v"], p["g"], p["beta"], p["do"], p["h0"],
+                             p["dht"], cu_seqlens=p["cu"], l2norm=True)
+    for name, key in (("q", "dq"), ("k", "dk"), ("g", "dg"), ("beta", "dbeta")):
+        want = _fd(p, name, l2norm=True)
+        err = np.abs(got[key] - want).max() / max(1e-12, np.abs(want).max())
+        assert err < 1e-6, (name, err)
+    # a row's gradient is orthogonal to the row itself up to the epsilon: rescaling q
+    # leaves the output unchanged
+    dots = (got["dq"] * p["q"]).sum(-1)
+    assert np.abs(dots).max() < 1e-5 * np.abs(got["dq"]).max() * np.abs(p["q"]).max()
