@@ -345,7 +345,7 @@ def chunk_kda(q, k, v, g, beta, scale=None, initial_state=None, output_final_sta
 
 def recurrent_kda_backward(q, k, v, gate, beta, dout, initial_state=None, dht=None, *,
                            cu_seqlens=None, scale=None, g_scale=1.0, want_dh0=True,
-                           dev_status=None, stream=None):
+                           use_qk_l2norm_in_kernel=False, dev_status=None, stream=None):
     """Gradients of the token recurrence for an output gradient `dout` and a final-state
     gradient `dht` (or None): a dict of fp32 tensors dq, dk, dv, dg (with respect to the
     per-token log2 gate), dbeta and dh0 (None unless `want_dh0`)."""
@@ -355,7 +355,8 @@ def recurrent_kda_backward(q, k, v, gate, beta, dout, initial_state=None, dht=No
             raise KdaError(KDA_ERR_INVALID_ARG, "tensors must be on a CUDA device")
     q, k, v, g, beta, dout, h0, dht, cu = [None if t is None else t.detach().contiguous()
                                            for t in ts]
-    shape = make_shape(q, v, cu, scale, g_scale, 0)
+    shape = make_shape(q, v, cu, scale, g_scale,
+                       KDA_FLAG_QK_L2NORM if use_qk_l2norm_in_kernel else 0)
     f32 = dict(dtype=torch.float32, device=q.device)
     out = dict(dq=torch.empty(q.shape, **f32), dk=torch.empty(k.shape, **f32),
                dv=torch.empty(v.shape, **f32), dg=torch.empty(g.shape, **f32),
@@ -374,9 +375,10 @@ class _KdaFunction(torch.autograd.Function):
     chunked form computes the recurrence, so its gradients are the recurrence's."""
 
     @staticmethod
-    def forward(ctx, q, k, v, g, beta, h0, cu, scale, g_scale, chunked):
+    def forward(ctx, q, k, v, g, beta, h0, cu, scale, g_scale, chunked, l2norm):
         with torch.no_grad():
-            kw = dict(cu_seqlens=cu, output_final_state=True, scale=scale, g_scale=g_scale)
+            kw = dict(cu_seqlens=cu, output_final_state=True, scale=scale, g_scale=g_scale,
+                      use_qk_l2norm_in_kernel=l2norm)
             if chunked:
                 o, ht = chunk_kda(q.detach(), k.detach(), v.detach(), g.detach(), beta.detach(),
                                   initial_state=None if h0 is None else h0.detach(), **kw)
@@ -385,7 +387,7 @@ class _KdaFunction(torch.autograd.Function):
                                       beta.detach(),
                                       None if h0 is None else h0.detach(), **kw)
         ctx.save_for_backward(q, k, v, g, beta, h0, cu)
-        ctx.scale, ctx.g_scale = scale, g_scale
+        ctx.scale, ctx.g_scale, ctx.l2norm = scale, g_scale, l2norm
         return o, ht
 
     @staticmethod
@@ -393,20 +395,23 @@ class _KdaFunction(torch.autograd.Function):
         q, k, v, g, beta, h0, cu = ctx.saved_tensors
         do = torch.zeros_like(v) if do is None else do.to(q.dtype)
         gr = recurrent_kda_backward(q, k, v, g, beta, do, h0, dht, cu_seqlens=cu,
-                                    scale=ctx.scale, g_scale=ctx.g_scale, want_dh0=h0 is not None)
+                                    scale=ctx.scale, g_scale=ctx.g_scale, want_dh0=h0 is not None,
+                                    use_qk_l2norm_in_kernel=ctx.l2norm)
         dh0 = gr["dh0"] if h0 is not None else None
         return (gr["dq"].to(q.dtype), gr["dk"].to(k.dtype), gr["dv"].to(v.dtype),
-                gr["dg"].to(g.dtype), gr["dbeta"].to(beta.dtype), dh0, None, None, None, None)
+                gr["dg"].to(g.dtype), gr["dbeta"].to(beta.dtype), dh0, None, None, None, None,
+                None)
 
 
 def kda_autograd(q, k, v, g, beta, initial_state=None, *, cu_seqlens=None, scale=None,
-                 g_scale=1.0, chunked=True):
+                 g_scale=1.0, chunked=True, use_qk_l2norm_in_kernel=False):
     """(o, ht) with gradients: forward by chunk_kda (or recurrent_kda when `chunked` is
     False), backward by kda_recurrent_bwd; `g` is the per-token log2 gate."""
     for t in (q, k, v, g, beta, initial_state, cu_seqlens):
         if t is not None and not t.is_cuda:
             raise KdaError(KDA_ERR_INVALID_ARG, "tensors must be on a CUDA device")
-    return _KdaFunction.apply(q, k, v, g, beta, initial_state, cu_seqlens, scale, g_scale, chunked)
+    return _KdaFunction.apply(q, k, v, g, beta, initial_state, cu_seqlens, scale, g_scale, chunked,
+                              bool(use_qk_l2norm_in_kernel))
 
 
 def recurrent_kda(q, k, v, gate, beta, initial_state=None, *, cu_seqlens=None,

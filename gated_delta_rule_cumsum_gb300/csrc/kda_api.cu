@@ -285,9 +285,9 @@ kda_status kda_recurrent_bwd(const void *q, const void *k, const void *v, const 
     kda_status st = check_common(op, shape, cu_seqlens);
     if (st != KDA_OK) return st;
     if ((st = check_fwd_pointers(op, shape, q, k, v, g, beta, dout, cu_seqlens)) != KDA_OK) return st;
-    if (shape->flags & (KDA_FLAG_G_IS_CUMSUM | KDA_FLAG_QK_L2NORM))
-        return fail(KDA_ERR_UNSUPPORTED, "%s: KDA_FLAG_G_IS_CUMSUM and KDA_FLAG_QK_L2NORM are not "
-                    "supported by the backward", op);
+    if (shape->flags & KDA_FLAG_G_IS_CUMSUM)
+        return fail(KDA_ERR_UNSUPPORTED, "%s: g is the per-token gate; KDA_FLAG_G_IS_CUMSUM is "
+                    "for kda_chunk_fwd", op);
     if (shape->K > 128) return fail(KDA_ERR_UNSUPPORTED, "%s: K=%d > 128", op, shape->K);
     const bool has_rows = (int64_t)shape->B * shape->T > 0;
     if (has_rows && (!dq || !dk || !dv || !dg || !dbeta))
@@ -325,6 +325,7 @@ kda_status kda_recurrent_bwd(const void *q, const void *k, const void *v, const 
     a.V = shape->V; a.N = shape->num_seqs;
     a.scale = resolve_scale(shape);
     a.g_scale = shape->g_scale;
+    a.l2norm = (shape->flags & KDA_FLAG_QK_L2NORM) ? 1 : 0;
     e = kda::launch_recurrent_bwd(a, shape->dtype, s);
     if (e != cudaSuccess) return cuda_fail(e, op);
     g_last_error.clear();

@@ -128,6 +128,7 @@ struct RecurrentBwdArgs {
     int32_t *status;
     int B, T, H, HV, K, V, N;
     float scale, g_scale;
+    int l2norm;                // q, k normalised per (token, head) inside the op
 };
 int64_t recurrent_bwd_ckpt_slots(int B, int T, int N);
 cudaError_t launch_recurrent_bwd(const RecurrentBwdArgs &a, kda_dtype dt, cudaStream_t st);

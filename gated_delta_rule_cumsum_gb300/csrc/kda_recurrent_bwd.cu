@@ -26,7 +26,9 @@
 // the current one is computed.  The states S_{t-1} are recomputed: a first pass
 // stores S at the start of every group; the backward then takes each group's two
 // 8-token halves in reverse, recomputing from the group's checkpoint and keeping
-// the half's eight states in shared memory.
+// the half's eight states in shared memory.  With the q/k L2-norm flag the staged
+// rows are normalised per token and a last kernel applies the norm's chain rule
+// to the summed dq and dk.
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -142,6 +144,24 @@ __device__ __forceinline__ void carry_store(const RecurrentBwdArgs &p, const Car
     if ((int)threadIdx.x < kBG) s.beta[threadIdx.x] = c.beta;
 }
 
+// With the L2-norm flag: the staged k (and q) rows of each token scaled by
+// 1 / sqrt(sum x^2 + 1e-6); warp w takes token w (16 warps, 16 tokens).
+template <bool Q>
+__device__ __forceinline__ void normalise_stage(const Stage &s, int warp, int lane) {
+    if (warp >= kBG) return;
+    float *rows[2] = {s.k, s.q};
+#pragma unroll
+    for (int x = 0; x < (Q ? 2 : 1); ++x) {
+        float *r = rows[x] + warp * kBK;
+        float ss = 0.f;
+#pragma unroll
+        for (int i = 0; i < kBRows; ++i) ss = fmaf(r[lane + 32 * i], r[lane + 32 * i], ss);
+        const float rn = 1.f / sqrtf(warp_sum(ss) + 1e-6f);
+#pragma unroll
+        for (int i = 0; i < kBRows; ++i) r[lane + 32 * i] *= rn;
+    }
+}
+
 // S <- Diag(e) S + k (beta (v - (Diag(e) S)^T k))^T for this warp's column (token u of the stage).
 __device__ __forceinline__ void step(float (&S)[kBRows], const Stage &s, int u, int lane, int w) {
     float e[kBRows], k[kBRows], part = 0.f;
@@ -202,6 +222,10 @@ __global__ void __launch_bounds__(kBThreads) recurrent_ckpt_kernel(RecurrentBwdA
         carry_store<false>(p, c, s);
         if (grp + 1 < ng) carry_load<T, false>(p, c, b, t1, min(t1 + kBG, eos), h, hv, col0);
         __syncthreads();
+        if (p.l2norm) {
+            normalise_stage<false>(s, warp, lane);
+            __syncthreads();
+        }
         store_col(p.ckpt + ckpt_slot(p, n, bos, grp) * p.HV * p.K * p.V + hvo, p, lane, col, S);
         for (int u = 0; u < t1 - t0; ++u) step(S, s, u, lane, warp);
     }
@@ -248,6 +272,10 @@ __global__ void __launch_bounds__(kBThreads) recurrent_bwd_kernel(RecurrentBwdAr
         carry_store<true>(p, c, s);
         if (grp > 0) carry_load<T, true>(p, c, b, g0 - kBG, g0, h, hv, col0);
         __syncthreads();
+        if (p.l2norm) {
+            normalise_stage<true>(s, warp, lane);
+            __syncthreads();
+        }
         const float *ck = p.ckpt + ckpt_slot(p, n, bos, grp) * p.HV * p.K * p.V + hvo;
         for (int half = (g1 - g0 - 1) / kBR; half >= 0; --half) {
             const int u0 = half * kBR, u1 = min(u0 + kBR, g1 - g0);
@@ -326,6 +354,41 @@ __global__ void __launch_bounds__(kBThreads) recurrent_bwd_kernel(RecurrentBwdAr
     if (p.dh0) store_col(p.dh0 + nso + hvo, p, lane, col, dS);
 }
 
+// The L2 norm's chain rule, after every contribution to dq and dk has been
+// summed: for a raw row x with r = 1 / sqrt(sum x^2 + 1e-6) and x^ = r x, the
+// gradient of x is r (dx^ - x^ (x^ . dx^)).  One warp per (row, head) of q or k;
+// rows at or past the last offset (packed) hold zeros and are left alone.
+template <typename T>
+__global__ void __launch_bounds__(256) l2norm_bwd_kernel(RecurrentBwdArgs p, int64_t rows) {
+    const int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (w >= 2 * rows) return;
+    const bool is_k = w >= rows;
+    const int64_t rh = is_k ? w - rows : w;  // (token row) * H + head
+    const int64_t tok = rh / p.H;
+    if (p.cu && (tok % p.T) >= p.cu[p.N]) return;
+    const T *x = static_cast<const T *>(is_k ? p.k : p.q) + rh * p.K;
+    float *dx = (is_k ? p.dk : p.dq) + rh * p.K;
+    float xv[kBRows], dv[kBRows], ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < kBRows; ++i) {
+        const int d = lane + 32 * i;
+        xv[i] = d < p.K ? to_f32(x[d]) : 0.f;
+        dv[i] = d < p.K ? dx[d] : 0.f;
+        ss = fmaf(xv[i], xv[i], ss);
+    }
+    const float r = 1.f / sqrtf(warp_sum(ss) + 1e-6f);
+    float dot = 0.f;
+#pragma unroll
+    for (int i = 0; i < kBRows; ++i) dot = fmaf(xv[i] * r, dv[i], dot);
+    dot = warp_sum(dot);
+#pragma unroll
+    for (int i = 0; i < kBRows; ++i) {
+        const int d = lane + 32 * i;
+        if (d < p.K) dx[d] = r * (dv[i] - xv[i] * r * dot);
+    }
+}
+
 template <typename T>
 cudaError_t launch_bwd_typed(const RecurrentBwdArgs &a, cudaStream_t st) {
     const int64_t blocks = (int64_t)a.N * a.HV * ((a.V + kBWarps - 1) / kBWarps);
@@ -346,6 +409,13 @@ cudaError_t launch_bwd_typed(const RecurrentBwdArgs &a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     prof_begin("recurrent_bwd", st);
     recurrent_bwd_kernel<T><<<(unsigned)blocks, kBThreads, smem, st>>>(a);
+    prof_end(st);
+    if ((e = cudaGetLastError()) != cudaSuccess || !a.l2norm) return e;
+    const int64_t rows = (int64_t)a.B * a.T * a.H;
+    if (rows == 0) return cudaSuccess;
+    const int64_t nb = (2 * rows * 32 + 255) / 256;
+    prof_begin("l2norm_bwd", st);
+    l2norm_bwd_kernel<T><<<(unsigned)nb, 256, 0, st>>>(a, rows);
     prof_end(st);
     return cudaGetLastError();
 }

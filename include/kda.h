@@ -284,7 +284,9 @@ kda_status kda_recurrent_fwd_act(const void *q, const void *k, const void *v, co
  *                      are summed with atomic adds: their rounding order varies.
  *   workspace          kda_recurrent_bwd_workspace_size() bytes, 16-byte aligned:
  *                      the state at the start of every 16-token group.
- * Supported: K <= 128, any V; not with KDA_FLAG_QK_L2NORM or KDA_FLAG_G_IS_CUMSUM.
+ *   flags              KDA_FLAG_QK_L2NORM: q, k are normalised inside the op (as in
+ *                      the forward) and dq, dk are the gradients of the raw rows.
+ * Supported: K <= 128, any V; not with KDA_FLAG_G_IS_CUMSUM.
  */
 kda_status kda_recurrent_bwd(const void *q, const void *k, const void *v, const float *g,
                              const void *beta, const float *h0, const int32_t *cu_seqlens,

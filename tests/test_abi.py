@@ -199,7 +199,6 @@ def _bwd(lib, s, grads=True, ws=(FAKE, 1 << 34)):
 
 @pytest.mark.parametrize("kw,status", [
     (dict(K=160), 2),                  # the backward keeps K <= 128
-    (dict(flags=1), 2),                # KDA_FLAG_QK_L2NORM
     (dict(flags=2), 2),                # KDA_FLAG_G_IS_CUMSUM
     (dict(HV=3), 1),
 ])

@@ -18,7 +18,7 @@ def _np(t):
     return None if t is None else t.detach().float().cpu().numpy().astype(np.float64)
 
 
-def _ref(inp, dout, dht, g_scale=1.0, h0_zero=False):
+def _ref(inp, dout, dht, g_scale=1.0, h0_zero=False, l2norm=False):
     h0 = inp["h0"]
     if h0 is None and h0_zero:
         N, HV, K, V = inp["N"], inp["v"].shape[2], inp["q"].shape[3], inp["v"].shape[3]
@@ -27,7 +27,7 @@ def _ref(inp, dout, dht, g_scale=1.0, h0_zero=False):
     return ob.recurrent_grads(_np(inp["q"]), _np(inp["k"]), _np(inp["v"]), _np(inp["g"]),
                               _np(inp["beta"]), _np(dout), _np(h0), _np(dht),
                               cu_seqlens=None if cu is None else cu.cpu().numpy(),
-                              g_scale=g_scale)
+                              g_scale=g_scale, l2norm=l2norm)
 
 
 def _run(kda, inp, dout, dht, **kw):
@@ -133,5 +133,33 @@ def test_autograd_through_the_forward_kernels(kda_lib, chunked):
                       ("h0", "dh0")):
         got = leaves[name].grad
         # bf16 parameters receive gradients rounded to bf16
+        tol = 1e-2 if got.dtype == torch.bfloat16 else TOL
+        assert parity.rel_err(got, ref[key]) <= tol, (name, parity.rel_err(got, ref[key]))
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_l2norm_flag(kda_lib, dtype):
+    """q, k normalised inside the op: gradients of the raw rows (packed, unnormalised)."""
+    inp = _packed(101, [20, 0, 37], HV=4, H=2, K=64, V=48, dtype=dtype)
+    inp["q"] = (inp["q"].float() * 3.0).to(dtype)
+    inp["k"] = (inp["k"].float() * 0.4).to(dtype)
+    dout, dht = _grads_in(inp, 102)
+    got = _run(kda_lib, inp, dout, dht, use_qk_l2norm_in_kernel=True)
+    end = 57
+    _compare(got, _ref(inp, dout, dht, l2norm=True), rows=end)
+    assert torch.all(got["dq"][:, end:] == 0) and torch.all(got["dk"][:, end:] == 0)
+
+
+def test_autograd_with_l2norm(kda_lib):
+    inp = _small(103, B=1, T=50, H=2, HV=2, K=64, V=64)
+    inp["q"] = (inp["q"].float() * 2.0).to(inp["q"].dtype)
+    dout, dht = _grads_in(inp, 104)
+    leaves = {n: inp[n].clone().requires_grad_(True) for n in ("q", "k", "v", "g", "beta", "h0")}
+    o, ht = kda_lib.kda_autograd(leaves["q"], leaves["k"], leaves["v"], leaves["g"],
+                                 leaves["beta"], leaves["h0"], use_qk_l2norm_in_kernel=True)
+    ((o.float() * dout.float()).sum() + (ht * dht).sum()).backward()
+    ref = _ref(inp, dout, dht, l2norm=True)
+    for name, key in (("q", "dq"), ("k", "dk"), ("v", "dv"), ("g", "dg"), ("beta", "dbeta")):
+        got = leaves[name].grad
         tol = 1e-2 if got.dtype == torch.bfloat16 else TOL
         assert parity.rel_err(got, ref[key]) <= tol, (name, parity.rel_err(got, ref[key]))
