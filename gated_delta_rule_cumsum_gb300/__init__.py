@@ -25,7 +25,7 @@ __all__ = [
     "KdaError", "KdaShape", "load", "library_path", "make_shape",
     "kda_gate_cumsum", "kda_chunk_fwd", "kda_recurrent_fwd", "kda_chunk_workspace_size",
     "kda_recurrent_bwd", "kda_recurrent_bwd_workspace_size", "recurrent_kda_backward", "kda_autograd",
-    "kda_gate_cumsum_act", "kda_chunk_fwd_act", "kda_recurrent_fwd_act",
+    "kda_gate_cumsum_act", "kda_chunk_fwd_act", "kda_recurrent_fwd_act", "kda_recurrent_bwd_act",
     "kda_chunk_fwd_noalloc", "KDA_NOALLOC_SCRATCH_BYTES",
     "kda_read_device_status", "kda_clear_device_status", "kda_status_string",
     "kda_last_error_message", "kda_version", "kda_profile_enable", "kda_profile_report",
@@ -99,6 +99,9 @@ _SIGNATURES = {
     "kda_chunk_workspace_size": (_SZ, [ctypes.POINTER(KdaShape)]),
     "kda_recurrent_bwd": (_ST, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.POINTER(KdaShape),
                                 _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP]),
+    "kda_recurrent_bwd_act": (_ST, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.POINTER(KdaShape),
+                                    ctypes.POINTER(KdaActivation), _VP, _VP, _VP, _VP, _VP, _VP,
+                                    _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP]),
     "kda_recurrent_bwd_workspace_size": (_SZ, [ctypes.POINTER(KdaShape)]),
     "kda_chunk_fwd_noalloc": (_ST, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.POINTER(KdaShape),
                                     _VP, _VP, _VP, _VP]),
@@ -232,6 +235,18 @@ def kda_recurrent_bwd(q, k, v, g, beta, h0, cu_seqlens, shape: KdaShape, dout, d
                                     _stream(stream)))
 
 
+def kda_recurrent_bwd_act(q, k, v, g, beta, h0, cu_seqlens, shape: KdaShape, act: KdaActivation,
+                          dout, dht, dq, dk, dv, dg, dbeta, dh0, dA_log, ddt_bias, workspace,
+                          dev_status=None, stream=None):
+    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().kda_recurrent_bwd_act(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0),
+                                        _ptr(cu_seqlens), ctypes.byref(shape), ctypes.byref(act),
+                                        _ptr(dout), _ptr(dht), _ptr(dq), _ptr(dk), _ptr(dv),
+                                        _ptr(dg), _ptr(dbeta), _ptr(dh0), _ptr(dA_log),
+                                        _ptr(ddt_bias), _ptr(workspace), ws, _ptr(dev_status),
+                                        _stream(stream)))
+
+
 def kda_recurrent_fwd(q, k, v, g, beta, h0, cu_seqlens, shape: KdaShape, o, ht, dev_status=None,
                       stream=None):
     _check(load().kda_recurrent_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0),
@@ -345,16 +360,19 @@ def chunk_kda(q, k, v, g, beta, scale=None, initial_state=None, output_final_sta
 
 def recurrent_kda_backward(q, k, v, gate, beta, dout, initial_state=None, dht=None, *,
                            cu_seqlens=None, scale=None, g_scale=1.0, want_dh0=True,
-                           use_qk_l2norm_in_kernel=False, dev_status=None, stream=None):
+                           use_qk_l2norm_in_kernel=False, A_log=None, dt_bias=None,
+                           beta_sigmoid_scale=0.0, dev_status=None, stream=None):
     """Gradients of the token recurrence for an output gradient `dout` and a final-state
     gradient `dht` (or None): a dict of fp32 tensors dq, dk, dv, dg (with respect to the
-    per-token log2 gate), dbeta and dh0 (None unless `want_dh0`)."""
-    ts = [q, k, v, gate, beta, dout, initial_state, dht, cu_seqlens]
+    per-token log2 gate), dbeta and dh0 (None unless `want_dh0`).  With `A_log` (and
+    `dt_bias`, `beta_sigmoid_scale`) the inputs are raw as in chunk_kda: dg and dbeta are
+    the raw inputs' gradients and the dict adds dA_log and ddt_bias."""
+    ts = [q, k, v, gate, beta, dout, initial_state, dht, cu_seqlens, A_log, dt_bias]
     for t in ts:
         if t is not None and not t.is_cuda:
             raise KdaError(KDA_ERR_INVALID_ARG, "tensors must be on a CUDA device")
-    q, k, v, g, beta, dout, h0, dht, cu = [None if t is None else t.detach().contiguous()
-                                           for t in ts]
+    q, k, v, g, beta, dout, h0, dht, cu, A_log, dt_bias = [
+        None if t is None else t.detach().contiguous() for t in ts]
     shape = make_shape(q, v, cu, scale, g_scale,
                        KDA_FLAG_QK_L2NORM if use_qk_l2norm_in_kernel else 0)
     f32 = dict(dtype=torch.float32, device=q.device)
@@ -365,8 +383,16 @@ def recurrent_kda_backward(q, k, v, gate, beta, dout, initial_state=None, dht=No
                     if want_dh0 else None))
     ws = torch.empty(max(kda_recurrent_bwd_workspace_size(shape), 16), dtype=torch.uint8,
                      device=q.device)
-    kda_recurrent_bwd(q, k, v, g, beta, h0, cu, shape, dout, dht, out["dq"], out["dk"],
-                      out["dv"], out["dg"], out["dbeta"], out["dh0"], ws, dev_status, stream)
+    if A_log is not None or beta_sigmoid_scale:
+        out["dA_log"] = None if A_log is None else torch.empty(A_log.shape, **f32)
+        out["ddt_bias"] = None if dt_bias is None else torch.empty(dt_bias.shape, **f32)
+        kda_recurrent_bwd_act(q, k, v, g, beta, h0, cu, shape,
+                              make_activation(A_log, dt_bias, beta_sigmoid_scale), dout, dht,
+                              out["dq"], out["dk"], out["dv"], out["dg"], out["dbeta"], out["dh0"],
+                              out["dA_log"], out["ddt_bias"], ws, dev_status, stream)
+    else:
+        kda_recurrent_bwd(q, k, v, g, beta, h0, cu, shape, dout, dht, out["dq"], out["dk"],
+                          out["dv"], out["dg"], out["dbeta"], out["dh0"], ws, dev_status, stream)
     return out
 
 
@@ -375,10 +401,14 @@ class _KdaFunction(torch.autograd.Function):
     chunked form computes the recurrence, so its gradients are the recurrence's."""
 
     @staticmethod
-    def forward(ctx, q, k, v, g, beta, h0, cu, scale, g_scale, chunked, l2norm):
+    def forward(ctx, q, k, v, g, beta, h0, cu, scale, g_scale, chunked, l2norm, A_log, dt_bias,
+                beta_sigmoid_scale):
         with torch.no_grad():
             kw = dict(cu_seqlens=cu, output_final_state=True, scale=scale, g_scale=g_scale,
-                      use_qk_l2norm_in_kernel=l2norm)
+                      use_qk_l2norm_in_kernel=l2norm,
+                      A_log=None if A_log is None else A_log.detach(),
+                      dt_bias=None if dt_bias is None else dt_bias.detach(),
+                      beta_sigmoid_scale=beta_sigmoid_scale)
             if chunked:
                 o, ht = chunk_kda(q.detach(), k.detach(), v.detach(), g.detach(), beta.detach(),
                                   initial_state=None if h0 is None else h0.detach(), **kw)
@@ -386,32 +416,39 @@ class _KdaFunction(torch.autograd.Function):
                 o, ht = recurrent_kda(q.detach(), k.detach(), v.detach(), g.detach(),
                                       beta.detach(),
                                       None if h0 is None else h0.detach(), **kw)
-        ctx.save_for_backward(q, k, v, g, beta, h0, cu)
+        ctx.save_for_backward(q, k, v, g, beta, h0, cu, A_log, dt_bias)
         ctx.scale, ctx.g_scale, ctx.l2norm = scale, g_scale, l2norm
+        ctx.beta_sigmoid_scale = beta_sigmoid_scale
         return o, ht
 
     @staticmethod
     def backward(ctx, do, dht):
-        q, k, v, g, beta, h0, cu = ctx.saved_tensors
+        q, k, v, g, beta, h0, cu, A_log, dt_bias = ctx.saved_tensors
         do = torch.zeros_like(v) if do is None else do.to(q.dtype)
         gr = recurrent_kda_backward(q, k, v, g, beta, do, h0, dht, cu_seqlens=cu,
                                     scale=ctx.scale, g_scale=ctx.g_scale, want_dh0=h0 is not None,
-                                    use_qk_l2norm_in_kernel=ctx.l2norm)
+                                    use_qk_l2norm_in_kernel=ctx.l2norm, A_log=A_log,
+                                    dt_bias=dt_bias, beta_sigmoid_scale=ctx.beta_sigmoid_scale)
         dh0 = gr["dh0"] if h0 is not None else None
+        dA = None if A_log is None else gr["dA_log"].to(A_log.dtype)
+        ddt = None if dt_bias is None else gr["ddt_bias"].to(dt_bias.dtype)
         return (gr["dq"].to(q.dtype), gr["dk"].to(k.dtype), gr["dv"].to(v.dtype),
                 gr["dg"].to(g.dtype), gr["dbeta"].to(beta.dtype), dh0, None, None, None, None,
-                None)
+                None, dA, ddt, None)
 
 
 def kda_autograd(q, k, v, g, beta, initial_state=None, *, cu_seqlens=None, scale=None,
-                 g_scale=1.0, chunked=True, use_qk_l2norm_in_kernel=False):
+                 g_scale=1.0, chunked=True, use_qk_l2norm_in_kernel=False, A_log=None,
+                 dt_bias=None, beta_sigmoid_scale=0.0):
     """(o, ht) with gradients: forward by chunk_kda (or recurrent_kda when `chunked` is
-    False), backward by kda_recurrent_bwd; `g` is the per-token log2 gate."""
-    for t in (q, k, v, g, beta, initial_state, cu_seqlens):
+    False), backward by kda_recurrent_bwd; `g` is the per-token log2 gate, or with
+    `A_log` the raw gate (A_log and dt_bias then receive gradients too)."""
+    for t in (q, k, v, g, beta, initial_state, cu_seqlens, A_log, dt_bias):
         if t is not None and not t.is_cuda:
             raise KdaError(KDA_ERR_INVALID_ARG, "tensors must be on a CUDA device")
     return _KdaFunction.apply(q, k, v, g, beta, initial_state, cu_seqlens, scale, g_scale, chunked,
-                              bool(use_qk_l2norm_in_kernel))
+                              bool(use_qk_l2norm_in_kernel), A_log, dt_bias,
+                              float(beta_sigmoid_scale))
 
 
 def recurrent_kda(q, k, v, gate, beta, initial_state=None, *, cu_seqlens=None,

@@ -281,9 +281,26 @@ kda_status kda_recurrent_bwd(const void *q, const void *k, const void *v, const 
                              float *dk, float *dv, float *dg, float *dbeta, float *dh0,
                              void *workspace, size_t workspace_bytes, int32_t *dev_status,
                              kda_stream_t stream) {
+    return kda_recurrent_bwd_act(q, k, v, g, beta, h0, cu_seqlens, shape, nullptr, dout, dht, dq,
+                                 dk, dv, dg, dbeta, dh0, nullptr, nullptr, workspace,
+                                 workspace_bytes, dev_status, stream);
+}
+
+kda_status kda_recurrent_bwd_act(const void *q, const void *k, const void *v, const float *g,
+                                 const void *beta, const float *h0, const int32_t *cu_seqlens,
+                                 const kda_shape *shape, const kda_activation *act,
+                                 const void *dout, const float *dht, float *dq, float *dk,
+                                 float *dv, float *dg, float *dbeta, float *dh0, float *dA_log,
+                                 float *ddt_bias, void *workspace, size_t workspace_bytes,
+                                 int32_t *dev_status, kda_stream_t stream) {
     const char *op = "kda_recurrent_bwd";
     kda_status st = check_common(op, shape, cu_seqlens);
     if (st != KDA_OK) return st;
+    kda::GateAct ga;
+    if ((st = resolve_act(op, shape, act, &ga)) != KDA_OK) return st;
+    if ((ga.A_log && !dA_log) || (ga.dt_bias && !ddt_bias))
+        return fail(KDA_ERR_INVALID_ARG, "%s: dA_log (and ddt_bias with dt_bias) must be non-NULL "
+                    "with the gate activation", op);
     if ((st = check_fwd_pointers(op, shape, q, k, v, g, beta, dout, cu_seqlens)) != KDA_OK) return st;
     if (shape->flags & KDA_FLAG_G_IS_CUMSUM)
         return fail(KDA_ERR_UNSUPPORTED, "%s: g is the per-token gate; KDA_FLAG_G_IS_CUMSUM is "
@@ -315,6 +332,10 @@ kda_status kda_recurrent_bwd(const void *q, const void *k, const void *v, const 
             if (e == cudaSuccess) e = cudaMemsetAsync(reinterpret_cast<void *>(z[0]), 0, z[1] * 4, s);
         if (e != cudaSuccess) return cuda_fail(e, op);
     }
+    if (ga.A_log && e == cudaSuccess) e = cudaMemsetAsync(dA_log, 0, (size_t)shape->HV * 4, s);
+    if (ga.dt_bias && e == cudaSuccess)
+        e = cudaMemsetAsync(ddt_bias, 0, (size_t)shape->HV * shape->K * 4, s);
+    if (e != cudaSuccess) return cuda_fail(e, op);
     kda::RecurrentBwdArgs a;
     a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.h0 = h0; a.cu = cu_seqlens;
     a.dout = dout; a.dht = dht;
@@ -326,6 +347,9 @@ kda_status kda_recurrent_bwd(const void *q, const void *k, const void *v, const 
     a.scale = resolve_scale(shape);
     a.g_scale = shape->g_scale;
     a.l2norm = (shape->flags & KDA_FLAG_QK_L2NORM) ? 1 : 0;
+    a.act = ga;
+    a.dA_log = dA_log;
+    a.ddt_bias = ddt_bias;
     e = kda::launch_recurrent_bwd(a, shape->dtype, s);
     if (e != cudaSuccess) return cuda_fail(e, op);
     g_last_error.clear();

@@ -129,6 +129,8 @@ struct RecurrentBwdArgs {
     int B, T, H, HV, K, V, N;
     float scale, g_scale;
     int l2norm;                // q, k normalised per (token, head) inside the op
+    GateAct act;               // raw g / beta activated inside the op
+    float *dA_log, *ddt_bias;  // [HV], [HV][K]: summed (zeroed first) when act sets them
 };
 int64_t recurrent_bwd_ckpt_slots(int B, int T, int N);
 cudaError_t launch_recurrent_bwd(const RecurrentBwdArgs &a, kda_dtype dt, cudaStream_t st);

@@ -28,8 +28,13 @@
 // 8-token halves in reverse, recomputing from the group's checkpoint and keeping
 // the half's eight states in shared memory.  With the q/k L2-norm flag the staged
 // rows are normalised per token and a last kernel applies the norm's chain rule
-// to the summed dq and dk.
+// to the summed dq and dk.  With the input activations (raw gate and beta) the
+// staging activates them exactly as the forward does, and a last kernel turns the
+// summed gradients of the gate and beta the recurrence used into those of the raw
+// inputs, A_log and dt_bias.
 #include "kda_internal.cuh"
+
+#include <algorithm>
 
 namespace kda {
 namespace {
@@ -127,13 +132,17 @@ __device__ __forceinline__ void carry_load(const RecurrentBwdArgs &p, Carry &c, 
         c.beta = to_f32(static_cast<const T *>(p.beta)[((size_t)b * p.T + t0 + threadIdx.x) * p.HV + hv]);
 }
 
-template <bool Q>
-__device__ __forceinline__ void carry_store(const RecurrentBwdArgs &p, const Carry &c, const Stage &s) {
+template <typename T, bool Q>
+__device__ __forceinline__ void carry_store(const RecurrentBwdArgs &p, const Carry &c, const Stage &s,
+                                            int hv) {
+    const float na = p.act.A_log ? gate_neg_a(p.act, hv) : 0.f;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const int idx = threadIdx.x + kBThreads * i;
+        const int idx = threadIdx.x + kBThreads * i, d = idx & 127;
+        float g = c.g[i];  // entries past K or the group: g = 0, unused
+        if (p.act.A_log && d < p.K) g = na * softplus_f(g + gate_bias(p.act, hv, d, p.K));
         s.k[idx] = c.k[i];
-        s.e[idx] = exp2f(p.g_scale * c.g[i]);  // entries past K or the group: g = 0, unused
+        s.e[idx] = exp2f(p.g_scale * g);
         if (Q) s.q[idx] = c.q[i];
     }
     const int u = threadIdx.x / kBWarps, cc = threadIdx.x % kBWarps;
@@ -141,7 +150,9 @@ __device__ __forceinline__ void carry_store(const RecurrentBwdArgs &p, const Car
         s.v[u * kBWarps + cc] = c.v;
         if (Q) s.dout[u * kBWarps + cc] = c.dout;
     }
-    if ((int)threadIdx.x < kBG) s.beta[threadIdx.x] = c.beta;
+    if ((int)threadIdx.x < kBG)
+        s.beta[threadIdx.x] = p.act.beta_scale > 0.f ? beta_activate<T>(c.beta, p.act.beta_scale)
+                                                     : c.beta;
 }
 
 // With the L2-norm flag: the staged k (and q) rows of each token scaled by
@@ -219,7 +230,7 @@ __global__ void __launch_bounds__(kBThreads) recurrent_ckpt_kernel(RecurrentBwdA
     for (int grp = 0; grp < ng; ++grp) {
         const int t0 = bos + grp * kBG, t1 = min(t0 + kBG, eos);
         __syncthreads();  // the previous group is done with the stage
-        carry_store<false>(p, c, s);
+        carry_store<T, false>(p, c, s, hv);
         if (grp + 1 < ng) carry_load<T, false>(p, c, b, t1, min(t1 + kBG, eos), h, hv, col0);
         __syncthreads();
         if (p.l2norm) {
@@ -269,7 +280,7 @@ __global__ void __launch_bounds__(kBThreads) recurrent_bwd_kernel(RecurrentBwdAr
     for (int grp = ng - 1; grp >= 0; --grp) {
         const int g0 = bos + grp * kBG, g1 = min(g0 + kBG, eos);
         __syncthreads();  // the previous group is done with the stage
-        carry_store<true>(p, c, s);
+        carry_store<T, true>(p, c, s, hv);
         if (grp > 0) carry_load<T, true>(p, c, b, g0 - kBG, g0, h, hv, col0);
         __syncthreads();
         if (p.l2norm) {
@@ -389,6 +400,52 @@ __global__ void __launch_bounds__(256) l2norm_bwd_kernel(RecurrentBwdArgs p, int
     }
 }
 
+// The input activations' chain rule, after the sweep has summed dg and dbeta with
+// respect to the gate and beta the recurrence used.  With x = g + dt_bias and
+// g' = -exp(A_log) softplus(x): dg'/dx = -exp(A_log) sigmoid(x) (also dt_bias's
+// gradient) and dg'/dA_log = g'.  With beta' = s sigmoid(y): dbeta'/dy =
+// s sigmoid(y) (1 - sigmoid(y)); the rounding of beta' to the input dtype passes
+// the gradient through.  Thread column c of the HV * K gate columns takes rows
+// blockIdx.y, + gridDim.y, ...; the sums over rows go to dt_bias's gradient by
+// one atomic per (block, column) and to A_log's through shared memory.  Rows at
+// or past the last offset (packed) are left alone.
+template <typename T>
+__global__ void __launch_bounds__(256) act_bwd_kernel(RecurrentBwdArgs p, int64_t rows) {
+    __shared__ float sA[256];  // A_log sums of the value heads this block's columns touch
+    const int cols = p.HV * p.K;
+    const int c0 = blockIdx.x * 256, c = c0 + threadIdx.x, hv0 = c0 / p.K;
+    const int64_t end = p.cu ? min((int64_t)max(p.cu[p.N], 0), rows) : rows;
+    sA[threadIdx.x] = 0.f;
+    __syncthreads();
+    if (p.act.A_log && c < cols) {
+        const int hv = c / p.K, d = c - hv * p.K;
+        const float na = gate_neg_a(p.act, hv), bias = gate_bias(p.act, hv, d, p.K);
+        float sb = 0.f, sa = 0.f;
+        for (int64_t r = blockIdx.y; r < end; r += gridDim.y) {
+            const size_t i = (size_t)r * cols + c;
+            const float x = p.g[i] + bias, dga = p.dg[i];
+            const float dx = dga * na / (1.f + expf(-x));
+            p.dg[i] = dx;
+            sb += dx;
+            sa = fmaf(dga, na * softplus_f(x), sa);
+        }
+        if (p.ddt_bias) atomicAdd(&p.ddt_bias[c], sb);
+        atomicAdd(&sA[hv - hv0], sa);
+    }
+    if (blockIdx.x == 0 && p.act.beta_scale > 0.f) {
+        const T *beta = static_cast<const T *>(p.beta);
+        for (int hv = threadIdx.x; hv < p.HV; hv += blockDim.x)
+            for (int64_t r = blockIdx.y; r < end; r += gridDim.y) {
+                const size_t i = (size_t)r * p.HV + hv;
+                const float sg = 1.f / (1.f + expf(-to_f32(beta[i])));
+                p.dbeta[i] *= p.act.beta_scale * sg * (1.f - sg);
+            }
+    }
+    __syncthreads();
+    const int hv = hv0 + threadIdx.x;
+    if (p.act.A_log && hv <= (min(cols, c0 + 256) - 1) / p.K) atomicAdd(&p.dA_log[hv], sA[threadIdx.x]);
+}
+
 template <typename T>
 cudaError_t launch_bwd_typed(const RecurrentBwdArgs &a, cudaStream_t st) {
     const int64_t blocks = (int64_t)a.N * a.HV * ((a.V + kBWarps - 1) / kBWarps);
@@ -410,14 +467,31 @@ cudaError_t launch_bwd_typed(const RecurrentBwdArgs &a, cudaStream_t st) {
     prof_begin("recurrent_bwd", st);
     recurrent_bwd_kernel<T><<<(unsigned)blocks, kBThreads, smem, st>>>(a);
     prof_end(st);
-    if ((e = cudaGetLastError()) != cudaSuccess || !a.l2norm) return e;
-    const int64_t rows = (int64_t)a.B * a.T * a.H;
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const int64_t rows = (int64_t)a.B * a.T;
     if (rows == 0) return cudaSuccess;
-    const int64_t nb = (2 * rows * 32 + 255) / 256;
-    prof_begin("l2norm_bwd", st);
-    l2norm_bwd_kernel<T><<<(unsigned)nb, 256, 0, st>>>(a, rows);
-    prof_end(st);
-    return cudaGetLastError();
+    if (a.l2norm) {
+        const int64_t nb = (2 * rows * a.H * 32 + 255) / 256;
+        prof_begin("l2norm_bwd", st);
+        l2norm_bwd_kernel<T><<<(unsigned)nb, 256, 0, st>>>(a, rows * a.H);
+        prof_end(st);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    if (a.act.A_log || a.act.beta_scale > 0.f) {
+        // about four blocks per SM, each block's threads over a share of the rows
+        const unsigned gx = (unsigned)((a.HV * a.K + 255) / 256);
+        int dev = 0, sms = 0;
+        if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return e;
+        const int64_t want = (4 * (int64_t)sms + gx - 1) / gx;
+        const unsigned gy = (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, std::min<int64_t>(rows, 65535)));
+        prof_begin("act_bwd", st);
+        act_bwd_kernel<T><<<dim3(gx, gy), 256, 0, st>>>(a, rows);
+        prof_end(st);
+        e = cudaGetLastError();
+    }
+    return e;
 }
 
 }  // namespace

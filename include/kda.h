@@ -18,7 +18,8 @@
  *   kda_recurrent_fwd  token-by-token forward for decode (PR #317)
  * each also as an *_act variant that applies the gate and beta activations to
  * raw inputs inside the op (kda_activation below), and
- *   kda_recurrent_bwd  the gradients of the recurrence (ALGORITHM.md, Backward)
+ *   kda_recurrent_bwd  the gradients of the recurrence (ALGORITHM.md, Backward),
+ *                      also as kda_recurrent_bwd_act (gradients of the raw inputs)
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -294,6 +295,29 @@ kda_status kda_recurrent_bwd(const void *q, const void *k, const void *v, const 
                              float *dq, float *dk, float *dv, float *dg, float *dbeta, float *dh0,
                              void *workspace, size_t workspace_bytes, int32_t *dev_status,
                              kda_stream_t stream);
+/*
+ * kda_recurrent_bwd on raw g / beta with the activations of *act (see
+ * kda_activation): the forward is kda_recurrent_fwd_act's (or kda_chunk_fwd_act's)
+ * and the gradients are those of its inputs.  The chain rule through the
+ * activations (kernel-fun 0.2.0.dev1 wheel, kda/chain.py, gate_backward):
+ *   dg       with respect to the raw gate g;
+ *   dbeta    with respect to the raw beta logits when beta_scale > 0 (the
+ *            rounding of the activated beta to the input dtype passes the
+ *            gradient through);
+ *   dA_log   [HV] fp32, required when act->A_log is set: sum over tokens and
+ *            channels of dL/dg' * g', g' the activated gate (zeroed, then summed);
+ *   ddt_bias [HV, K] fp32, required when act->dt_bias is set: the sum over tokens
+ *            of dg (zeroed, then summed).
+ * Both may be NULL when the corresponding input is not set; their rounding
+ * order varies (atomic adds).
+ */
+kda_status kda_recurrent_bwd_act(const void *q, const void *k, const void *v, const float *g,
+                                 const void *beta, const float *h0, const int32_t *cu_seqlens,
+                                 const kda_shape *shape, const kda_activation *act,
+                                 const void *dout, const float *dht, float *dq, float *dk,
+                                 float *dv, float *dg, float *dbeta, float *dh0, float *dA_log,
+                                 float *ddt_bias, void *workspace, size_t workspace_bytes,
+                                 int32_t *dev_status, kda_stream_t stream);
 /* Bytes of workspace kda_recurrent_bwd needs for *shape (0 on invalid shapes). */
 size_t kda_recurrent_bwd_workspace_size(const kda_shape *shape);
 

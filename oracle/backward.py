@@ -30,11 +30,18 @@ __all__ = ["recurrent_grads"]
 
 
 def recurrent_grads(q, k, v, g, beta, do, h0=None, dht=None, cu_seqlens=None, scale=None,
-                    g_scale=1.0, l2norm=False):
+                    g_scale=1.0, l2norm=False, A_log=None, dt_bias=None, beta_scale=0.0,
+                    beta_bf16=False):
     """Gradients of sum(o * do) + sum(ht * dht) of the token recurrence, in fp64.
     With `l2norm` the recurrence uses q / sqrt(sum q^2 + 1e-6) and the same of k per
     (token, head) (kernel-fun 0.2.0.dev1 wheel, kda/autograd.py, l2norm option), and
     the gradients are those of the raw q and k.
+    With `A_log` the gate is raw: the recurrence uses -exp(A_log[hv]) softplus(g +
+    dt_bias[hv, d]) (natural log, times g_scale), and with `beta_scale` > 0 beta is
+    raw too: sigmoid(beta) * beta_scale (kernel-fun 0.2.0.dev1 wheel, kda/chain.py,
+    gate_cumsum and gate_backward; kda/ops.py, chunk_kda), rounded to bf16 in value
+    when `beta_bf16` (the rounding passes gradients straight through).  The
+    gradients are then those of the raw g and beta, plus dA_log [HV] and dt_bias's.
 
     Shapes: q, k [B,T,H,K]; v, do [B,T,HV,V]; g [B,T,HV,K] (per-token log2 decay);
     beta [B,T,HV]; h0, dht [N,HV,K,V] or None; cu_seqlens [N+1] or None (then N = B).
@@ -47,6 +54,8 @@ def recurrent_grads(q, k, v, g, beta, do, h0=None, dht=None, cu_seqlens=None, sc
         return torch.tensor(np.asarray(x, dtype=np.float64), requires_grad=True)
 
     q, k, v, g, beta = (leaf(x) for x in (q, k, v, g, beta))
+    A_log_t = None if A_log is None else leaf(A_log)
+    dt_t = None if dt_bias is None else leaf(dt_bias)
     do = torch.tensor(np.asarray(do, dtype=np.float64))
     B, T, H, K = q.shape
     HV, V = v.shape[2], v.shape[3]
@@ -69,9 +78,17 @@ def recurrent_grads(q, k, v, g, beta, do, h0=None, dht=None, cu_seqlens=None, sc
                 kr = kr / torch.sqrt((kr * kr).sum(-1, keepdim=True) + 1e-6)
             qt = qr.repeat_interleave(G, dim=0)                 # [HV, K]
             kt = kr.repeat_interleave(G, dim=0)
-            S = torch.exp2(g_scale * g[b, t])[:, :, None] * S  # decay rows
+            gt, bt = g[b, t], beta[b, t]
+            if A_log_t is not None:
+                x = gt if dt_t is None else gt + dt_t
+                gt = -torch.exp(A_log_t)[:, None] * torch.nn.functional.softplus(x)
+            if beta_scale > 0:
+                bt = torch.sigmoid(bt) * beta_scale
+                if beta_bf16:
+                    bt = bt + (bt.to(torch.bfloat16).to(torch.float64) - bt).detach()
+            S = torch.exp2(g_scale * gt)[:, :, None] * S  # decay rows
             a = torch.einsum("hkv,hk->hv", S, kt)
-            delta = beta[b, t][:, None] * (v[b, t] - a)
+            delta = bt[:, None] * (v[b, t] - a)
             S = S + kt[:, :, None] * delta[:, None, :]
             loss = loss + (scale * torch.einsum("hkv,hk->hv", S, qt) * do[b, t]).sum()
         if dhtt is not None:
@@ -82,4 +99,6 @@ def recurrent_grads(q, k, v, g, beta, do, h0=None, dht=None, cu_seqlens=None, sc
         return np.zeros(tuple(x.shape)) if x.grad is None else x.grad.numpy().copy()
 
     return dict(dq=grad(q), dk=grad(k), dv=grad(v), dg=grad(g), dbeta=grad(beta),
-                dh0=None if h0t is None else grad(h0t))
+                dh0=None if h0t is None else grad(h0t),
+                dA_log=None if A_log_t is None else grad(A_log_t),
+                ddt_bias=None if dt_t is None else grad(dt_t))

@@ -219,3 +219,26 @@ def test_recurrent_bwd_needs_gradients_and_workspace(lib):
     assert b"workspace" in lib.kda_last_error_message()
     assert _bwd(lib, s, ws=(ctypes.c_void_p(0x100004), need)) == 1
     assert b"aligned" in lib.kda_last_error_message()
+
+
+@pytest.mark.parametrize("case", ["bias_without_a", "negative_beta_scale", "no_dA_log",
+                                  "no_ddt_bias"])
+def test_recurrent_bwd_act_rejects_on_host(lib, case):
+    import gated_delta_rule_cumsum_gb300 as kda
+
+    act = kda.KdaActivation(FAKE.value, FAKE.value, 0.0)
+    dA, ddt = FAKE, FAKE
+    if case == "bias_without_a":
+        act.A_log = None
+    elif case == "negative_beta_scale":
+        act.beta_scale = -2.0
+    elif case == "no_dA_log":
+        dA = None
+    else:
+        ddt = None
+    g = FAKE
+    st = lib.kda_recurrent_bwd_act(FAKE, FAKE, FAKE, FAKE, FAKE, None, None,
+                                   ctypes.byref(_shape()), ctypes.byref(act), FAKE, None, g, g, g,
+                                   g, g, None, dA, ddt, FAKE, 1 << 34, None, None)
+    assert st == 1, lib.kda_last_error_message()
+    assert lib.kda_last_error_message()

@@ -163,3 +163,89 @@ def test_autograd_with_l2norm(kda_lib):
         got = leaves[name].grad
         tol = 1e-2 if got.dtype == torch.bfloat16 else TOL
         assert parity.rel_err(got, ref[key]) <= tol, (name, parity.rel_err(got, ref[key]))
+
+
+def _raw_act(inp, seed, tail=None):
+    """Raw gate and beta logits for `inp` (NaN from row `tail` on), A_log, dt_bias."""
+    gen = torch.Generator().manual_seed(seed)
+    B, T, HV, K = inp["g"].shape
+    g_raw = torch.randn(B, T, HV, K, generator=gen) - 1.5
+    b_raw = torch.randn(B, T, HV, generator=gen)
+    if tail is not None:
+        g_raw[:, tail:] = float("nan")
+        b_raw[:, tail:] = float("nan")
+    A_log = torch.log(1.0 + 3.0 * torch.rand(HV, generator=gen))
+    dt_bias = 0.5 * torch.randn(HV, K, generator=gen)
+    return (g_raw.cuda(), b_raw.to(inp["beta"].dtype).cuda(), A_log.cuda(), dt_bias.cuda())
+
+
+def _ref_act(inp, dout, dht, g_raw, b_raw, A_log, dt_bias, beta_scale):
+    cu = inp["cu_seqlens"]
+    return ob.recurrent_grads(_np(inp["q"]), _np(inp["k"]), _np(inp["v"]), _np(g_raw),
+                              _np(b_raw), _np(dout), _np(inp["h0"]), _np(dht),
+                              cu_seqlens=None if cu is None else cu.cpu().numpy(),
+                              g_scale=RCP_LN2, A_log=_np(A_log), dt_bias=_np(dt_bias),
+                              beta_scale=beta_scale,
+                              beta_bf16=inp["beta"].dtype == torch.bfloat16)
+
+
+RCP_LN2 = 1.0 / math.log(2.0)
+
+
+@pytest.mark.parametrize("dtype,beta_scale", [(torch.float32, 2.0), (torch.bfloat16, 1.0)])
+def test_input_activations(kda_lib, dtype, beta_scale):
+    """Raw gate through -exp(A_log) softplus(g + dt_bias) and beta logits through the
+    sigmoid: gradients of the raw inputs, A_log and dt_bias (packed, NaN tail)."""
+    lens = [23, 0, 41, 9]
+    inp = _packed(111, lens, HV=4, H=2, K=64, V=48, dtype=dtype)
+    end = sum(lens)
+    g_raw, b_raw, A_log, dt_bias = _raw_act(inp, 112, tail=end)
+    dout, dht = _grads_in(inp, 113)
+    st = kda_lib.new_status()
+    got = kda_lib.recurrent_kda_backward(inp["q"], inp["k"], inp["v"], g_raw, b_raw, dout,
+                                         inp["h0"], dht, cu_seqlens=inp["cu_seqlens"],
+                                         g_scale=RCP_LN2, A_log=A_log, dt_bias=dt_bias,
+                                         beta_sigmoid_scale=beta_scale, dev_status=st)
+    assert kda_lib.kda_read_device_status(st) == (0, 0)
+    ref = _ref_act(inp, dout, dht, g_raw, b_raw, A_log, dt_bias, beta_scale)
+    _compare(got, ref, rows=end)
+    for name in ("dA_log", "ddt_bias"):
+        err = parity.rel_err(_np(got[name]), ref[name])
+        assert err <= TOL, (name, err)
+    for name in ("dg", "dbeta"):
+        assert torch.all(got[name][:, end:] == 0), name
+
+
+def test_gate_activation_without_bias_or_beta_sigmoid(kda_lib):
+    inp = _small(121, B=2, T=37, H=1, HV=2, K=32, V=32, dtype=torch.float32)
+    g_raw, _, A_log, _ = _raw_act(inp, 122)
+    dout, dht = _grads_in(inp, 123)
+    got = kda_lib.recurrent_kda_backward(inp["q"], inp["k"], inp["v"], g_raw, inp["beta"], dout,
+                                         inp["h0"], dht, g_scale=RCP_LN2, A_log=A_log)
+    assert got["ddt_bias"] is None
+    ref = _ref_act(inp, dout, dht, g_raw, inp["beta"], A_log, None, 0.0)
+    _compare(got, ref)
+    assert parity.rel_err(_np(got["dA_log"]), ref["dA_log"]) <= TOL
+
+
+@pytest.mark.parametrize("chunked", [True, False])
+def test_autograd_with_input_activations(kda_lib, chunked):
+    """A_log and dt_bias as parameters: loss.backward() fills their gradients."""
+    inp = _small(131, B=1, T=90, H=2, HV=2, K=64, V=64)  # bf16: the tensor-core forward
+    g_raw, b_raw, A_log, dt_bias = _raw_act(inp, 132)
+    dout, dht = _grads_in(inp, 133)
+    leaves = {n: inp[n].clone().requires_grad_(True) for n in ("q", "k", "v", "h0")}
+    leaves.update(g=g_raw.clone().requires_grad_(True), beta=b_raw.clone().requires_grad_(True),
+                  A_log=A_log.clone().requires_grad_(True),
+                  dt_bias=dt_bias.clone().requires_grad_(True))
+    o, ht = kda_lib.kda_autograd(leaves["q"], leaves["k"], leaves["v"], leaves["g"],
+                                 leaves["beta"], leaves["h0"], g_scale=RCP_LN2, chunked=chunked,
+                                 A_log=leaves["A_log"], dt_bias=leaves["dt_bias"],
+                                 beta_sigmoid_scale=2.0)
+    ((o.float() * dout.float()).sum() + (ht * dht).sum()).backward()
+    ref = _ref_act(inp, dout, dht, g_raw, b_raw, A_log, dt_bias, 2.0)
+    for name, key in (("q", "dq"), ("k", "dk"), ("v", "dv"), ("g", "dg"), ("beta", "dbeta"),
+                      ("h0", "dh0"), ("A_log", "dA_log"), ("dt_bias", "ddt_bias")):
+        got = leaves[name].grad
+        tol = 1e-2 if got.dtype == torch.bfloat16 else TOL
+        assert parity.rel_err(got, ref[key]) <= tol, (name, parity.rel_err(got, ref[key]))
