@@ -249,3 +249,36 @@ def test_autograd_with_input_activations(kda_lib, chunked):
         got = leaves[name].grad
         tol = 1e-2 if got.dtype == torch.bfloat16 else TOL
         assert parity.rel_err(got, ref[key]) <= tol, (name, parity.rel_err(got, ref[key]))
+
+
+def test_training_shape_directional_derivative(kda_lib):
+    """At the size and in the call the benchmark times (B=1, T=8192, H=HV=16, K=V=128,
+    bf16 inputs, dL/do and dL/dht drawn once): the gradients' inner product with a
+    random direction d equals the central difference of L = sum(o do) + sum(ht dht)
+    along d, L evaluated by the fp32 token forward on the same values.  A property
+    that holds at any size, where the fp64 oracle cannot run."""
+    import kda_synth
+
+    inp = kda_synth.make_inputs(kda_synth.workload(1), device="cuda")
+    names = ("q", "k", "v", "g", "beta")
+    gen = torch.Generator(device="cuda").manual_seed(11)
+    dout = torch.randn(inp["v"].shape, generator=gen, device="cuda").to(inp["q"].dtype)
+    dht = torch.randn(1, 16, 128, 128, generator=gen, device="cuda")
+    st = kda_lib.new_status()
+    got = kda_lib.recurrent_kda_backward(*(inp[n] for n in names), dout, None, dht,
+                                         want_dh0=False, dev_status=st)
+    assert kda_lib.kda_read_device_status(st) == (0, 0)
+    x = {n: inp[n].float() for n in names}
+    gd = torch.Generator(device="cuda").manual_seed(12)
+    d = {n: torch.randn(x[n].shape, generator=gd, device="cuda") for n in names}
+    key = dict(q="dq", k="dk", v="dv", g="dg", beta="dbeta")
+    want = sum(float((got[key[n]].double() * d[n].double()).sum()) for n in names)
+
+    def loss(eps):
+        o, ht = kda_lib.recurrent_kda(*(x[n] + eps * d[n] for n in names), None,
+                                      output_final_state=True)
+        return float((o.double() * dout.double()).sum() + (ht.double() * dht.double()).sum())
+
+    eps = 2e-3
+    fd = (loss(eps) - loss(-eps)) / (2 * eps)
+    assert abs(fd - want) <= 1e-2 * abs(want), (fd, want)
