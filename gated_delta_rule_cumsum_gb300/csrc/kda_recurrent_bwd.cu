@@ -19,14 +19,20 @@
 // Layout: one CTA of 16 warps per (sequence, value head, 16 value columns); warp
 // w owns column w of the block for all K <= 128 state rows, lane l the rows
 // l + 32 r.  Value columns evolve independently in the recurrence, so the warps
-// never exchange state: only dq, dk, de and dbeta sum over columns (shared memory
-// atomics within the CTA, then one fp32 global atomic add per (token, row) per
-// CTA).  Tokens go in groups of 16: the CTA stages a group's k, 2^g, q, v, do and
-// beta in shared memory, the next group's values travelling in registers while
-// the current one is computed.  The states S_{t-1} are recomputed: a first pass
-// stores S at the start of every group; the backward then takes each group's two
-// 8-token halves in reverse, recomputing from the group's checkpoint and keeping
-// the half's eight states in shared memory.  With the q/k L2-norm flag the staged
+// never exchange state: only dq, dk, de and dbeta sum over columns.  Tokens go in
+// groups of 16: the CTA stages a group's k, 2^g, q, v, do and beta in shared
+// memory, the next group's values travelling in registers while the current one
+// is computed.  The states S_{t-1} are recomputed: a first pass stores S at the
+// start of every group; the backward then takes each group's two 8-token halves
+// in reverse, recomputing from the group's checkpoint and keeping the half's
+// eight states in shared memory.  The reverse loop keeps only what is per column
+// (dS, delta, da, dv); the sums over columns follow from the stored S_{t-1} and
+// dS after the half:
+//     dq = scale (e . sum_c S'_c do_c + k sum_c delta_c do_c)     (S_t = e S' + k delta^T)
+//     dk = sum_c dS_c delta_c + e . sum_c S'_c da_c
+//     de = sum_c dS_c . S'_c + k . sum_c da_c S'_c
+// one thread per (token, row), then one fp32 global atomic add per (token, row)
+// per CTA.  With the q/k L2-norm flag the staged
 // rows are normalised per token and a last kernel applies the norm's chain rule
 // to the summed dq and dk.  With the input activations (raw gate and beta) the
 // staging activates them exactly as the forward does, and a last kernel turns the
@@ -45,6 +51,7 @@ constexpr int kBWarps = 16;   // one value column per warp
 constexpr int kBThreads = kBWarps * 32;
 constexpr int kBRows = 4;     // state rows per lane (K <= 128)
 constexpr int kBK = 128;
+constexpr int kBPlane = kBWarps * kBR * kBK;  // one value per (warp, token, row)
 constexpr float kLn2 = 0.69314718055994531f;
 
 __device__ __forceinline__ float warp_sum(float x) {
@@ -248,11 +255,15 @@ __global__ void __launch_bounds__(kBThreads) recurrent_bwd_kernel(RecurrentBwdAr
     extern __shared__ __align__(16) float sm[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const Stage s = stage_at(sm);
-    float *st = sm + kStageFloats + (size_t)warp * kBR * kBRows * 32;  // [kBR][kBRows][32]
-    float *acc_q = sm + kStageFloats + kBWarps * kBR * kBRows * 32;    // [kBR][128]
-    float *acc_k = acc_q + kBR * kBK;
-    float *acc_e = acc_k + kBR * kBK;
-    float *acc_b = acc_e + kBR * kBK;                                   // [kBR]
+    // [warp][kBR][kBRows][32] planes: S_{t-1} and dL/dS_t of each warp's column;
+    // element (token j, row d) of warp w at (w kBR + j) 128 + d
+    float *sSp = sm + kStageFloats;
+    float *sdS = sSp + kBPlane;
+    float *sDel = sdS + kBPlane;            // [kBR][kBWarps]: delta
+    float *sDa = sDel + kBR * kBWarps;      // da
+    float *sDb = sDa + kBR * kBWarps;       // ddelta (v - a): the column's dbeta term
+    float *st = sSp + (size_t)warp * kBR * kBK;
+    float *sd = sdS + (size_t)warp * kBR * kBK;
 
     const int nvb = (p.V + kBWarps - 1) / kBWarps;
     const int64_t bid = blockIdx.x;
@@ -267,7 +278,6 @@ __global__ void __launch_bounds__(kBThreads) recurrent_bwd_kernel(RecurrentBwdAr
     const size_t hvo = (size_t)hv * p.K * p.V;
     const size_t nso = (size_t)n * p.HV * p.K * p.V;
 
-    for (int i = threadIdx.x; i < 3 * kBR * kBK + kBR; i += blockDim.x) acc_q[i] = 0.f;
     float dS[kBRows];
     load_col(p.dht ? p.dht + nso + hvo : nullptr, p, lane, col, dS);
 
@@ -318,46 +328,52 @@ __global__ void __launch_bounds__(kBThreads) recurrent_bwd_kernel(RecurrentBwdAr
                 float dpart = 0.f;
 #pragma unroll
                 for (int r = 0; r < kBRows; ++r) {
-                    const float St = fmaf(e[r], Sp[r], k[r] * delta);
-                    if (lane + 32 * r < p.K) atomicAdd(&acc_q[j * kBK + lane + 32 * r], p.scale * St * dd);
-                    dS[r] = fmaf(p.scale * q[r], dd, dS[r]);
+                    dS[r] = fmaf(p.scale * q[r], dd, dS[r]);  // dL/dS_t
                     dpart = fmaf(dS[r], k[r], dpart);
+                    sd[(j * kBRows + r) * 32 + lane] = dS[r];
                 }
                 const float ddel = warp_sum(dpart);
                 const float da = -beta * ddel;
-                if (lane == 0 && cok) {
-                    p.dv[(((size_t)b * p.T + g0 + u) * p.HV + hv) * p.V + col] = beta * ddel;
-                    atomicAdd(&acc_b[j], ddel * (vv - a));
+                if (lane == 0) {  // a column past V has all of these zero
+                    if (cok) p.dv[(((size_t)b * p.T + g0 + u) * p.HV + hv) * p.V + col] = beta * ddel;
+                    sDel[j * kBWarps + warp] = delta;
+                    sDa[j * kBWarps + warp] = da;
+                    sDb[j * kBWarps + warp] = ddel * (vv - a);
                 }
 #pragma unroll
-                for (int r = 0; r < kBRows; ++r) {
-                    const float kp = fmaf(dS[r], delta, e[r] * Sp[r] * da);
-                    const float dSp = fmaf(k[r], da, dS[r]);
-                    if (lane + 32 * r < p.K) {
-                        atomicAdd(&acc_k[j * kBK + lane + 32 * r], kp);
-                        atomicAdd(&acc_e[j * kBK + lane + 32 * r], dSp * Sp[r]);
-                    }
-                    dS[r] = e[r] * dSp;
-                }
+                for (int r = 0; r < kBRows; ++r) dS[r] = e[r] * fmaf(k[r], da, dS[r]);
             }
-            __syncthreads();  // the half-group's sums are complete
-            const int hl = u1 - u0;
-            for (int i = threadIdx.x; i < hl * kBK; i += blockDim.x) {
-                const int j = i >> 7, d = i & 127;
+            __syncthreads();  // the half-group's planes are complete
+            // sums over the block's columns: thread (token j, row d)
+            const int hl = u1 - u0, d = threadIdx.x & (kBK - 1);
+            for (int j = threadIdx.x / kBK; j < hl; j += kBThreads / kBK) {
+                const int u = u0 + j;
+                float sa = 0.f, sb = 0.f, sc = 0.f, sdd = 0.f, ed = 0.f;
+#pragma unroll
+                for (int w = 0; w < kBWarps; ++w) {
+                    const float sp = sSp[(w * kBR + j) * kBK + d], ds = sdS[(w * kBR + j) * kBK + d];
+                    const float dow = s.dout[u * kBWarps + w];
+                    const float del = sDel[j * kBWarps + w], daw = sDa[j * kBWarps + w];
+                    sa = fmaf(sp, dow, sa);
+                    sb = fmaf(sp, daw, sb);
+                    sc = fmaf(ds, del, sc);
+                    sdd = fmaf(ds, sp, sdd);
+                    ed = fmaf(del, dow, ed);
+                }
+                const size_t row = (size_t)b * p.T + g0 + u;
                 if (d < p.K) {
-                    const int u = u0 + j;
-                    const size_t row = (size_t)b * p.T + g0 + u;
-                    atomicAdd(&p.dq[(row * p.H + h) * p.K + d], acc_q[i]);
-                    atomicAdd(&p.dk[(row * p.H + h) * p.K + d], acc_k[i]);
+                    const float e = s.e[u * kBK + d], kk = s.k[u * kBK + d];
+                    atomicAdd(&p.dq[(row * p.H + h) * p.K + d], p.scale * fmaf(e, sa, kk * ed));
+                    atomicAdd(&p.dk[(row * p.H + h) * p.K + d], fmaf(e, sb, sc));
                     atomicAdd(&p.dg[(row * p.HV + hv) * p.K + d],
-                              acc_e[i] * s.e[u * kBK + d] * kLn2 * p.g_scale);
+                              fmaf(kk, sb, sdd) * e * kLn2 * p.g_scale);
                 }
-                acc_q[i] = acc_k[i] = acc_e[i] = 0.f;
-            }
-            if ((int)threadIdx.x < hl) {
-                atomicAdd(&p.dbeta[((size_t)b * p.T + g0 + u0 + threadIdx.x) * p.HV + hv],
-                          acc_b[threadIdx.x]);
-                acc_b[threadIdx.x] = 0.f;
+                if (d == 0) {
+                    float db = 0.f;
+#pragma unroll
+                    for (int w = 0; w < kBWarps; ++w) db += sDb[j * kBWarps + w];
+                    atomicAdd(&p.dbeta[row * p.HV + hv], db);
+                }
             }
             __syncthreads();
         }
@@ -450,8 +466,7 @@ template <typename T>
 cudaError_t launch_bwd_typed(const RecurrentBwdArgs &a, cudaStream_t st) {
     const int64_t blocks = (int64_t)a.N * a.HV * ((a.V + kBWarps - 1) / kBWarps);
     if (blocks == 0) return cudaSuccess;
-    const int smem = (kStageFloats + kBWarps * kBR * kBRows * 32 + 3 * kBR * kBK + kBR) *
-                     (int)sizeof(float);
+    const int smem = (kStageFloats + 2 * kBPlane + 3 * kBR * kBWarps) * (int)sizeof(float);
     static bool attr = false;
     if (!attr) {
         cudaError_t e = cudaFuncSetAttribute(recurrent_bwd_kernel<T>,
