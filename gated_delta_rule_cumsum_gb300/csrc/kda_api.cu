@@ -271,8 +271,8 @@ size_t kda_recurrent_bwd_workspace_size(const kda_shape *shape) {
     if (!shape || shape->K <= 0 || shape->V <= 0 || shape->HV <= 0 || shape->B <= 0 ||
         shape->T < 0 || shape->num_seqs < 0)
         return 0;
-    return (size_t)kda::recurrent_bwd_ckpt_slots(shape->B, shape->T, shape->num_seqs) * shape->HV *
-           shape->K * shape->V * sizeof(float);
+    return kda::recurrent_bwd_ckpt_bytes(shape->B, shape->T, shape->num_seqs, shape->HV, shape->K,
+                                         shape->V);
 }
 
 kda_status kda_recurrent_bwd(const void *q, const void *k, const void *v, const float *g,

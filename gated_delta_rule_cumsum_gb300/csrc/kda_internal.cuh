@@ -124,7 +124,7 @@ struct RecurrentBwdArgs {
     const void *dout;          // [B,T,HV,V], q's dtype
     const float *dht;          // [N,HV,K,V] or NULL
     float *dq, *dk, *dv, *dg, *dbeta, *dh0;  // fp32; dq, dk, dg, dbeta accumulate (zeroed first)
-    float *ckpt;               // [slots][HV][K][V]: S at the start of every 16-token group
+    float *ckpt;               // S at the start of every 8 tokens (per-column blocks)
     int32_t *status;
     int B, T, H, HV, K, V, N;
     float scale, g_scale;
@@ -132,7 +132,8 @@ struct RecurrentBwdArgs {
     GateAct act;               // raw g / beta activated inside the op
     float *dA_log, *ddt_bias;  // [HV], [HV][K]: summed (zeroed first) when act sets them
 };
-int64_t recurrent_bwd_ckpt_slots(int B, int T, int N);
+// Workspace of kda_recurrent_bwd: the checkpoints of every 8 tokens.
+size_t recurrent_bwd_ckpt_bytes(int B, int T, int N, int HV, int K, int V);
 cudaError_t launch_recurrent_bwd(const RecurrentBwdArgs &a, kda_dtype dt, cudaStream_t st);
 
 struct ChunkArgs {

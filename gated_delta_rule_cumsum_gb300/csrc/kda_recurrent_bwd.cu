@@ -23,9 +23,9 @@
 // groups of 16: the CTA stages a group's k, 2^g, q, v, do and beta in shared
 // memory, the next group's values travelling in registers while the current one
 // is computed.  The states S_{t-1} are recomputed: a first pass stores S at the
-// start of every group; the backward then takes each group's two 8-token halves
-// in reverse, recomputing from the group's checkpoint and keeping the half's
-// eight states in shared memory.  The reverse loop keeps only what is per column
+// start of every 8-token half of a group; the backward then takes the halves in
+// reverse, recomputing each from its own checkpoint and keeping its eight states
+// in shared memory.  The reverse loop keeps only what is per column
 // (dS, delta, da, dv); the sums over columns follow from the stored S_{t-1} and
 // dS after the half:
 //     dq = scale (e . sum_c S'_c do_c + k sum_c delta_c do_c)     (S_t = e S' + k delta^T)
@@ -45,8 +45,8 @@
 namespace kda {
 namespace {
 
-constexpr int kBG = 16;       // tokens per group and per checkpoint
-constexpr int kBR = 8;        // tokens per backward half-group
+constexpr int kBG = 16;       // tokens per staged group
+constexpr int kBR = 8;        // tokens per backward half-group and per checkpoint
 constexpr int kBWarps = 16;   // one value column per warp
 constexpr int kBThreads = kBWarps * 32;
 constexpr int kBRows = 4;     // state rows per lane (K <= 128)
@@ -77,11 +77,29 @@ __device__ __forceinline__ bool seq_range(const RecurrentBwdArgs &p, int n, int 
     return true;
 }
 
-// Checkpoint slot of group `grp` of sequence n (dense: n * groups per row + grp;
-// packed: bos / 16 + n + grp, which never overlaps the next sequence's slots).
-__device__ __forceinline__ int64_t ckpt_slot(const RecurrentBwdArgs &p, int n, int bos, int grp) {
-    if (!p.cu) return (int64_t)n * ((p.T + kBG - 1) / kBG) + grp;
-    return (int64_t)(bos / kBG) + n + grp;
+// Checkpoint slot of half-group `hg` (tokens 8 hg ..) of sequence n (dense:
+// n * halves per row + hg; packed: bos / 8 + n + hg, which never overlaps the
+// next sequence's slots).
+__device__ __forceinline__ int64_t ckpt_slot(const RecurrentBwdArgs &p, int n, int bos, int hg) {
+    if (!p.cu) return (int64_t)n * ((p.T + kBR - 1) / kBR) + hg;
+    return (int64_t)(bos / kBR) + n + hg;
+}
+
+// A checkpoint slot holds, per value head, the CTA blocks' 16 columns one after
+// another, each column as the ceil(K / 32) x 32 rows its warp holds (lane l of
+// row block r at r * 32 + l): every warp's stores and loads are whole lines.
+__device__ __forceinline__ float *ckpt_col(const RecurrentBwdArgs &p, int64_t slot, int hv, int col) {
+    const int nvb = (p.V + kBWarps - 1) / kBWarps, nr = (p.K + 31) / 32;
+    return p.ckpt + (((size_t)slot * p.HV + hv) * nvb * kBWarps + col) * (size_t)nr * 32;
+}
+__device__ __forceinline__ void ckpt_store(float *dst, int K, int lane, const float (&S)[kBRows]) {
+#pragma unroll
+    for (int r = 0; r < kBRows; ++r)
+        if (32 * r < K) dst[r * 32 + lane] = S[r];
+}
+__device__ __forceinline__ void ckpt_load(const float *src, int K, int lane, float (&S)[kBRows]) {
+#pragma unroll
+    for (int r = 0; r < kBRows; ++r) S[r] = 32 * r < K ? src[r * 32 + lane] : 0.f;
 }
 
 // A group's token inputs in shared memory: rows [kBG][128] of k, 2^g and (for
@@ -213,7 +231,7 @@ __device__ __forceinline__ void store_col(float *dst, const RecurrentBwdArgs &p,
     }
 }
 
-// Pass 1: the recurrence, storing S at the start of every 16-token group.
+// Pass 1: the recurrence, storing S at the start of every 8-token half-group.
 template <typename T>
 __global__ void __launch_bounds__(kBThreads) recurrent_ckpt_kernel(RecurrentBwdArgs p) {
     __shared__ float sm[kStageFloats];
@@ -244,8 +262,11 @@ __global__ void __launch_bounds__(kBThreads) recurrent_ckpt_kernel(RecurrentBwdA
             normalise_stage<false>(s, warp, lane);
             __syncthreads();
         }
-        store_col(p.ckpt + ckpt_slot(p, n, bos, grp) * p.HV * p.K * p.V + hvo, p, lane, col, S);
-        for (int u = 0; u < t1 - t0; ++u) step(S, s, u, lane, warp);
+        for (int u = 0; u < t1 - t0; ++u) {
+            if (u % kBR == 0)
+                ckpt_store(ckpt_col(p, ckpt_slot(p, n, bos, 2 * grp + u / kBR), hv, col), p.K, lane, S);
+            step(S, s, u, lane, warp);
+        }
     }
 }
 
@@ -283,9 +304,12 @@ __global__ void __launch_bounds__(kBThreads) recurrent_bwd_kernel(RecurrentBwdAr
 
     const int ng = (eos - bos + kBG - 1) / kBG;
     Carry c;
+    // the checkpoint of the next half to run, loaded one half ahead
+    float Sn[kBRows];
     if (ng > 0) {
         const int g0 = bos + (ng - 1) * kBG;
         carry_load<T, true>(p, c, b, g0, eos, h, hv, col0);
+        ckpt_load(ckpt_col(p, ckpt_slot(p, n, bos, (eos - bos - 1) / kBR), hv, col), p.K, lane, Sn);
     }
     for (int grp = ng - 1; grp >= 0; --grp) {
         const int g0 = bos + grp * kBG, g1 = min(g0 + kBG, eos);
@@ -297,17 +321,17 @@ __global__ void __launch_bounds__(kBThreads) recurrent_bwd_kernel(RecurrentBwdAr
             normalise_stage<true>(s, warp, lane);
             __syncthreads();
         }
-        const float *ck = p.ckpt + ckpt_slot(p, n, bos, grp) * p.HV * p.K * p.V + hvo;
         for (int half = (g1 - g0 - 1) / kBR; half >= 0; --half) {
             const int u0 = half * kBR, u1 = min(u0 + kBR, g1 - g0);
-            // recompute S_{t-1} for the half's tokens from the group's checkpoint
+            // recompute S_{t-1} for the half's tokens from its checkpoint
             float S[kBRows];
-            load_col(ck, p, lane, col, S);
-            for (int u = 0; u < u1; ++u) {
-                if (u >= u0) {
 #pragma unroll
-                    for (int r = 0; r < kBRows; ++r) st[((u - u0) * kBRows + r) * 32 + lane] = S[r];
-                }
+            for (int r = 0; r < kBRows; ++r) S[r] = Sn[r];
+            const int hg = 2 * grp + half;
+            if (hg > 0) ckpt_load(ckpt_col(p, ckpt_slot(p, n, bos, hg - 1), hv, col), p.K, lane, Sn);
+            for (int u = u0; u < u1; ++u) {
+#pragma unroll
+                for (int r = 0; r < kBRows; ++r) st[((u - u0) * kBRows + r) * 32 + lane] = S[r];
                 step(S, s, u, lane, warp);
             }
             for (int u = u1 - 1; u >= u0; --u) {
@@ -511,10 +535,12 @@ cudaError_t launch_bwd_typed(const RecurrentBwdArgs &a, cudaStream_t st) {
 
 }  // namespace
 
-int64_t recurrent_bwd_ckpt_slots(int B, int T, int N) {
-    const int64_t dense = (int64_t)B * ((T + kBG - 1) / kBG);
-    const int64_t packed = (int64_t)T / kBG + N + 1;
-    return dense > packed ? dense : packed;
+size_t recurrent_bwd_ckpt_bytes(int B, int T, int N, int HV, int K, int V) {
+    const int64_t dense = (int64_t)B * ((T + kBR - 1) / kBR);
+    const int64_t packed = (int64_t)T / kBR + N + 1;
+    const int64_t slots = dense > packed ? dense : packed;
+    const int64_t cols = (int64_t)((V + kBWarps - 1) / kBWarps) * kBWarps;
+    return (size_t)(slots * HV * cols * ((K + 31) / 32) * 32 * (int64_t)sizeof(float));
 }
 
 cudaError_t launch_recurrent_bwd(const RecurrentBwdArgs &a, kda_dtype dt, cudaStream_t st) {

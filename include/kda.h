@@ -284,7 +284,7 @@ kda_status kda_recurrent_fwd_act(const void *q, const void *k, const void *v, co
  *                      Rows outside every sequence are zero.  dq, dk, dg and dbeta
  *                      are summed with atomic adds: their rounding order varies.
  *   workspace          kda_recurrent_bwd_workspace_size() bytes, 16-byte aligned:
- *                      the state at the start of every 16-token group.
+ *                      the state at the start of every 8 tokens.
  *   flags              KDA_FLAG_QK_L2NORM: q, k are normalised inside the op (as in
  *                      the forward) and dq, dk are the gradients of the raw rows.
  * Supported: K <= 128, any V; not with KDA_FLAG_G_IS_CUMSUM.
