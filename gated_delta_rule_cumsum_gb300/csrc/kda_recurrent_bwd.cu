@@ -198,8 +198,10 @@ __device__ __forceinline__ void normalise_stage(const Stage &s, int warp, int la
     }
 }
 
-// S <- Diag(e) S + k (beta (v - (Diag(e) S)^T k))^T for this warp's column (token u of the stage).
-__device__ __forceinline__ void step(float (&S)[kBRows], const Stage &s, int u, int lane, int w) {
+// S <- Diag(e) S + k (beta (v - (Diag(e) S)^T k))^T for this warp's column (token u of the stage);
+// a = (Diag(e) S)^T k and delta are returned.
+__device__ __forceinline__ void step(float (&S)[kBRows], const Stage &s, int u, int lane, int w,
+                                     float &a, float &delta) {
     float e[kBRows], k[kBRows], part = 0.f;
 #pragma unroll
     for (int r = 0; r < kBRows; ++r) {
@@ -207,8 +209,8 @@ __device__ __forceinline__ void step(float (&S)[kBRows], const Stage &s, int u, 
         k[r] = s.k[u * kBK + lane + 32 * r];
         part = fmaf(e[r] * S[r], k[r], part);
     }
-    const float a = warp_sum(part);
-    const float delta = s.beta[u] * (s.v[u * kBWarps + w] - a);
+    a = warp_sum(part);
+    delta = s.beta[u] * (s.v[u * kBWarps + w] - a);
 #pragma unroll
     for (int r = 0; r < kBRows; ++r) S[r] = fmaf(e[r], S[r], k[r] * delta);
 }
@@ -265,7 +267,8 @@ __global__ void __launch_bounds__(kBThreads) recurrent_ckpt_kernel(RecurrentBwdA
         for (int u = 0; u < t1 - t0; ++u) {
             if (u % kBR == 0)
                 ckpt_store(ckpt_col(p, ckpt_slot(p, n, bos, 2 * grp + u / kBR), hv, col), p.K, lane, S);
-            step(S, s, u, lane, warp);
+            float a, delta;
+            step(S, s, u, lane, warp, a, delta);
         }
     }
 }
@@ -283,6 +286,7 @@ __global__ void __launch_bounds__(kBThreads) recurrent_bwd_kernel(RecurrentBwdAr
     float *sDel = sdS + kBPlane;            // [kBR][kBWarps]: delta
     float *sDa = sDel + kBR * kBWarps;      // da
     float *sDb = sDa + kBR * kBWarps;       // ddelta (v - a): the column's dbeta term
+    float *sAv = sDb + kBR * kBWarps;       // a = S'^T k, from the recompute
     float *st = sSp + (size_t)warp * kBR * kBK;
     float *sd = sdS + (size_t)warp * kBR * kBK;
 
@@ -332,23 +336,26 @@ __global__ void __launch_bounds__(kBThreads) recurrent_bwd_kernel(RecurrentBwdAr
             for (int u = u0; u < u1; ++u) {
 #pragma unroll
                 for (int r = 0; r < kBRows; ++r) st[((u - u0) * kBRows + r) * 32 + lane] = S[r];
-                step(S, s, u, lane, warp);
+                float a, delta;
+                step(S, s, u, lane, warp, a, delta);
+                if (lane == 0) {  // a column past V has both zero
+                    sAv[(u - u0) * kBWarps + warp] = a;
+                    sDel[(u - u0) * kBWarps + warp] = delta;
+                }
             }
+            __syncwarp();
             for (int u = u1 - 1; u >= u0; --u) {
                 const int j = u - u0;
-                float e[kBRows], k[kBRows], q[kBRows], Sp[kBRows], part = 0.f;
+                float e[kBRows], k[kBRows], q[kBRows];
 #pragma unroll
                 for (int r = 0; r < kBRows; ++r) {
                     e[r] = s.e[u * kBK + lane + 32 * r];
                     k[r] = s.k[u * kBK + lane + 32 * r];
                     q[r] = s.q[u * kBK + lane + 32 * r];
-                    Sp[r] = st[(j * kBRows + r) * 32 + lane];
-                    part = fmaf(e[r] * Sp[r], k[r], part);
                 }
                 const float beta = s.beta[u];
                 const float vv = s.v[u * kBWarps + warp], dd = s.dout[u * kBWarps + warp];
-                const float a = warp_sum(part);
-                const float delta = beta * (vv - a);
+                const float a = sAv[j * kBWarps + warp];
                 float dpart = 0.f;
 #pragma unroll
                 for (int r = 0; r < kBRows; ++r) {
@@ -360,7 +367,6 @@ __global__ void __launch_bounds__(kBThreads) recurrent_bwd_kernel(RecurrentBwdAr
                 const float da = -beta * ddel;
                 if (lane == 0) {  // a column past V has all of these zero
                     if (cok) p.dv[(((size_t)b * p.T + g0 + u) * p.HV + hv) * p.V + col] = beta * ddel;
-                    sDel[j * kBWarps + warp] = delta;
                     sDa[j * kBWarps + warp] = da;
                     sDb[j * kBWarps + warp] = ddel * (vv - a);
                 }
@@ -490,7 +496,7 @@ template <typename T>
 cudaError_t launch_bwd_typed(const RecurrentBwdArgs &a, cudaStream_t st) {
     const int64_t blocks = (int64_t)a.N * a.HV * ((a.V + kBWarps - 1) / kBWarps);
     if (blocks == 0) return cudaSuccess;
-    const int smem = (kStageFloats + 2 * kBPlane + 3 * kBR * kBWarps) * (int)sizeof(float);
+    const int smem = (kStageFloats + 2 * kBPlane + 4 * kBR * kBWarps) * (int)sizeof(float);
     static bool attr = false;
     if (!attr) {
         cudaError_t e = cudaFuncSetAttribute(recurrent_bwd_kernel<T>,
