@@ -93,14 +93,13 @@ bool use_tc(const kda_shape *s) {
 
 // The current device's SM count (cached per device); false when no device answers.
 bool device_sm_count(int *out) {
-    static int cache[64] = {0};
+    static kda::DeviceOnce once;
+    static int cache[64];
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
-    if (cache[dev] == 0 &&
-        cudaDeviceGetAttribute(&cache[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-        cache[dev] = 0;
+    if (once.run(&dev, [](int d) {
+            return cudaDeviceGetAttribute(&cache[d], cudaDevAttrMultiProcessorCount, d);
+        }) != cudaSuccess)
         return false;
-    }
     *out = cache[dev];
     return true;
 }

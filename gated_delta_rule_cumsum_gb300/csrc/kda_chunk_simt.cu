@@ -317,16 +317,17 @@ cudaError_t launch_kk(const ChunkArgs &a, cudaStream_t st) {
     const size_t scan_smem = sizeof(float) * (KK * kScanBV + 3 * kBT * KK + kBT * kBT +
                                               2 * kBT * kScanBV + KK);
     cudaError_t e;
-    static bool attrs_set = false;  // once per process (per current device)
-    if (!attrs_set) {
-        e = cudaFuncSetAttribute(chunk_prep_kernel<T, KK>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)prep_smem);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(chunk_scan_kernel<T, KK>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)scan_smem);
-        if (e != cudaSuccess) return e;
-        attrs_set = true;
-    }
+    static DeviceOnce once;
+    int dev = 0;
+    e = once.run(&dev, [&](int) {
+        cudaError_t r = cudaFuncSetAttribute(chunk_prep_kernel<T, KK>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)prep_smem);
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(chunk_scan_kernel<T, KK>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)scan_smem);
+        return r;
+    });
+    if (e != cudaSuccess) return e;
     if (a.slots > 0) {
         dim3 grid((unsigned)a.slots, a.HV);
         prof_begin("chunk_prep_simt", st);

@@ -6,9 +6,34 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "kda.h"
 
 namespace kda {
+
+// One-time setup per device (kernel attributes such as the dynamic shared-memory
+// limit, device properties): run(dev, set) calls set(*dev) for the current device
+// the first time any thread asks for it, and only records success.  Devices
+// 0..63; others fail with cudaErrorInvalidDevice.
+struct DeviceOnce {
+    std::atomic<uint64_t> done{0};
+    std::mutex mu;
+    template <typename F>
+    cudaError_t run(int *dev, F &&set) {
+        cudaError_t e = cudaGetDevice(dev);
+        if (e != cudaSuccess) return e;
+        if (*dev < 0 || *dev >= 64) return cudaErrorInvalidDevice;
+        const uint64_t bit = 1ull << *dev;
+        if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+        std::lock_guard<std::mutex> lock(mu);
+        if (done.load(std::memory_order_relaxed) & bit) return cudaSuccess;
+        e = set(*dev);
+        if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_release);
+        return e;
+    }
+};
 
 // Chunk length of the chunked form (kernel-fun 0.2.0.dev1 sdist, ALGORITHM.md,
 // preamble: BT = 64).

@@ -122,62 +122,70 @@ __device__ __forceinline__ Stage stage_at(float *base) {
 
 // The group's values this thread carries: (token, row) pairs tid + 512 i of the
 // 16 x 128 rows, (token, column) pair tid of the 16 x 16 columns, beta tid < 16.
+// They stay in the input dtype until carry_store: a conversion right after the
+// load would wait for it there, and the loads would no longer overlap the
+// current group's work.
+template <typename T>
 struct Carry {
-    float k[4], g[4], q[4];
-    float v, dout, beta;
+    T k[4], q[4];
+    float g[4];
+    T v, dout, beta;
 };
 
 template <typename T, bool Q>
-__device__ __forceinline__ void carry_load(const RecurrentBwdArgs &p, Carry &c, int b, int t0, int t1,
-                                           int h, int hv, int col0) {
+__device__ __forceinline__ void carry_load(const RecurrentBwdArgs &p, Carry<T> &c, int b, int t0,
+                                           int t1, int h, int hv, int col0) {
     const T *k = static_cast<const T *>(p.k);
     const T *q = static_cast<const T *>(p.q);
     const T *v = static_cast<const T *>(p.v);
     const T *dout = static_cast<const T *>(p.dout);
+    const T zero = from_f32<T>(0.f);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int idx = threadIdx.x + kBThreads * i, u = idx >> 7, d = idx & 127;
-        c.k[i] = c.g[i] = c.q[i] = 0.f;
+        c.k[i] = c.q[i] = zero;
+        c.g[i] = 0.f;
         if (t0 + u < t1 && d < p.K) {
             const size_t row = (size_t)b * p.T + t0 + u;
-            c.k[i] = to_f32(k[(row * p.H + h) * p.K + d]);
+            c.k[i] = k[(row * p.H + h) * p.K + d];
             c.g[i] = p.g[(row * p.HV + hv) * p.K + d];
-            if (Q) c.q[i] = to_f32(q[(row * p.H + h) * p.K + d]);
+            if (Q) c.q[i] = q[(row * p.H + h) * p.K + d];
         }
     }
     const int u = threadIdx.x / kBWarps, cc = threadIdx.x % kBWarps;  // 512 threads: 32 x 16
-    c.v = c.dout = 0.f;
+    c.v = c.dout = zero;
     if (u < kBG && t0 + u < t1 && col0 + cc < p.V) {
         const size_t vr = (((size_t)b * p.T + t0 + u) * p.HV + hv) * p.V + col0 + cc;
-        c.v = to_f32(v[vr]);
-        if (Q) c.dout = to_f32(dout[vr]);
+        c.v = v[vr];
+        if (Q) c.dout = dout[vr];
     }
-    c.beta = 0.f;
+    c.beta = zero;
     if ((int)threadIdx.x < kBG && t0 + (int)threadIdx.x < t1)
-        c.beta = to_f32(static_cast<const T *>(p.beta)[((size_t)b * p.T + t0 + threadIdx.x) * p.HV + hv]);
+        c.beta = static_cast<const T *>(p.beta)[((size_t)b * p.T + t0 + threadIdx.x) * p.HV + hv];
 }
 
 template <typename T, bool Q>
-__device__ __forceinline__ void carry_store(const RecurrentBwdArgs &p, const Carry &c, const Stage &s,
-                                            int hv) {
+__device__ __forceinline__ void carry_store(const RecurrentBwdArgs &p, const Carry<T> &c,
+                                            const Stage &s, int hv) {
     const float na = p.act.A_log ? gate_neg_a(p.act, hv) : 0.f;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int idx = threadIdx.x + kBThreads * i, d = idx & 127;
         float g = c.g[i];  // entries past K or the group: g = 0, unused
         if (p.act.A_log && d < p.K) g = na * softplus_f(g + gate_bias(p.act, hv, d, p.K));
-        s.k[idx] = c.k[i];
+        s.k[idx] = to_f32(c.k[i]);
         s.e[idx] = exp2f(p.g_scale * g);
-        if (Q) s.q[idx] = c.q[i];
+        if (Q) s.q[idx] = to_f32(c.q[i]);
     }
     const int u = threadIdx.x / kBWarps, cc = threadIdx.x % kBWarps;
     if (u < kBG) {
-        s.v[u * kBWarps + cc] = c.v;
-        if (Q) s.dout[u * kBWarps + cc] = c.dout;
+        s.v[u * kBWarps + cc] = to_f32(c.v);
+        if (Q) s.dout[u * kBWarps + cc] = to_f32(c.dout);
     }
-    if ((int)threadIdx.x < kBG)
-        s.beta[threadIdx.x] = p.act.beta_scale > 0.f ? beta_activate<T>(c.beta, p.act.beta_scale)
-                                                     : c.beta;
+    if ((int)threadIdx.x < kBG) {
+        const float x = to_f32(c.beta);
+        s.beta[threadIdx.x] = p.act.beta_scale > 0.f ? beta_activate<T>(x, p.act.beta_scale) : x;
+    }
 }
 
 // With the L2-norm flag: the staged k (and q) rows of each token scaled by
@@ -252,7 +260,7 @@ __global__ void __launch_bounds__(kBThreads) recurrent_ckpt_kernel(RecurrentBwdA
     float S[kBRows];
     load_col(p.h0 ? p.h0 + (size_t)n * p.HV * p.K * p.V + hvo : nullptr, p, lane, col, S);
     const int ng = (eos - bos + kBG - 1) / kBG;
-    Carry c;
+    Carry<T> c;
     if (ng > 0) carry_load<T, false>(p, c, b, bos, eos, h, hv, col0);
     for (int grp = 0; grp < ng; ++grp) {
         const int t0 = bos + grp * kBG, t1 = min(t0 + kBG, eos);
@@ -307,7 +315,7 @@ __global__ void __launch_bounds__(kBThreads) recurrent_bwd_kernel(RecurrentBwdAr
     load_col(p.dht ? p.dht + nso + hvo : nullptr, p, lane, col, dS);
 
     const int ng = (eos - bos + kBG - 1) / kBG;
-    Carry c;
+    Carry<T> c;
     // the checkpoint of the next half to run, loaded one half ahead
     float Sn[kBRows];
     if (ng > 0) {
@@ -497,12 +505,14 @@ cudaError_t launch_bwd_typed(const RecurrentBwdArgs &a, cudaStream_t st) {
     const int64_t blocks = (int64_t)a.N * a.HV * ((a.V + kBWarps - 1) / kBWarps);
     if (blocks == 0) return cudaSuccess;
     const int smem = (kStageFloats + 2 * kBPlane + 4 * kBR * kBWarps) * (int)sizeof(float);
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(recurrent_bwd_kernel<T>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    static DeviceOnce once;
+    int dev = 0;
+    {
+        const cudaError_t e = once.run(&dev, [smem](int) {
+            return cudaFuncSetAttribute(recurrent_bwd_kernel<T>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        });
         if (e != cudaSuccess) return e;
-        attr = true;
     }
     prof_begin("recurrent_ckpt", st);
     recurrent_ckpt_kernel<T><<<(unsigned)blocks, kBThreads, 0, st>>>(a);
