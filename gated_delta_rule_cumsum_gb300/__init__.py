@@ -1,18 +1,23 @@
-"""GB300 (sm_103a) KDA forward: Python binding over the C ABI of libkda_gb300.so.
+"""GB300 (sm_103a) KDA: Python binding over the C ABI of libkda_gb300.so.
 
-Argument marshalling only.  Every step of the forward runs in the library's CUDA
-kernels; torch provides device memory and streams.  There is no CPU fallback:
-`load()` raises when the library has not been built.
+Argument marshalling only.  Every step of the forward and the backward runs in the
+library's CUDA kernels; torch provides device memory and streams.  There is no CPU
+fallback: `load()` raises when the library has not been built.
 
 Binding functions carry the C names (`kda_chunk_fwd`, `kda_recurrent_fwd`,
-`kda_gate_cumsum`, ...) and take preallocated tensors exactly like the C calls.
-`chunk_kda`, `recurrent_kda` and `gate_cumsum` allocate the outputs and call
-them, mirroring kernel-fun 0.2.0.dev1 wheel, kda/ops.py `chunk_kda` and
-attention-gym PR #317 `recurrent_kda` (forward only).
+`kda_gate_cumsum`, `kda_recurrent_bwd`, ...) and take preallocated tensors exactly
+like the C calls.  `chunk_kda`, `recurrent_kda`, `gate_cumsum` and
+`recurrent_kda_backward` allocate the outputs and call them, mirroring kernel-fun
+0.2.0.dev1 wheel, kda/ops.py `chunk_kda` and attention-gym PR #317 `recurrent_kda`;
+`kda_autograd` puts them behind torch.autograd.  These run on their tensors'
+device (the library launches on the current device and its current stream) and
+reject tensors that are not all on one CUDA device.
 """
 from __future__ import annotations
 
 import ctypes
+import functools
+import itertools
 import os
 from typing import Optional
 
@@ -74,6 +79,8 @@ def make_activation(A_log=None, dt_bias=None, beta_scale: float = 0.0) -> KdaAct
     """A_log [HV] and dt_bias [HV, K] fp32 device tensors (or None); beta_scale 0
     keeps beta as given, 1 or 2 applies sigmoid(beta) * beta_scale."""
     for t, name in ((A_log, "A_log"), (dt_bias, "dt_bias")):
+        if t is not None and not t.is_cuda:
+            raise KdaError(KDA_ERR_INVALID_ARG, f"{name} must be on a CUDA device")
         if t is not None and (t.dtype != torch.float32 or not t.is_contiguous()):
             raise ValueError(f"{name} must be a contiguous fp32 tensor")
     return KdaActivation(_ptr(A_log), _ptr(dt_bias), float(beta_scale))
@@ -298,14 +305,42 @@ def kda_profile_report(max_entries: int = 32) -> dict:
 
 
 # ------------------------------------------------------- allocating wrappers
+def _one_device(*ts):
+    """Every given tensor on the same CUDA device, else KdaError (pointers of
+    another device, or of the host, must never reach the kernels)."""
+    dev = None
+    for t in ts:
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise KdaError(KDA_ERR_INVALID_ARG, "tensors must be on a CUDA device")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise KdaError(KDA_ERR_INVALID_ARG,
+                           f"tensors must be on one CUDA device ({dev} and {t.device})")
+    return dev
+
+
+def _on_tensor_device(fn):
+    """Run fn with its first CUDA tensor's device as the current device: the library
+    launches on the current device and takes that device's current stream."""
+    @functools.wraps(fn)
+    def wrapper(*args, **kwargs):
+        for x in itertools.chain(args, kwargs.values()):
+            if isinstance(x, torch.Tensor) and x.is_cuda:
+                with torch.cuda.device(x.device):
+                    return fn(*args, **kwargs)
+        return fn(*args, **kwargs)
+    return wrapper
+
+
 def _prep(*ts):
     for t in ts:
-        if t is not None:
-            if t.requires_grad:
-                raise KdaError(KDA_ERR_UNSUPPORTED,
-                               "forward only: inputs requiring grad are rejected")
-            if not t.is_cuda:
-                raise KdaError(KDA_ERR_INVALID_ARG, "tensors must be on a CUDA device")
+        if t is not None and t.requires_grad:
+            raise KdaError(KDA_ERR_UNSUPPORTED,
+                           "inputs requiring grad are rejected here: use kda_autograd")
+    _one_device(*ts)
     return [None if t is None else t.contiguous() for t in ts]
 
 
@@ -314,11 +349,13 @@ def new_status(device=None) -> torch.Tensor:
     return torch.zeros(1, dtype=torch.int32, device=device or "cuda")
 
 
+@_on_tensor_device
 def gate_cumsum(g, cu_seqlens=None, chunk_size: int = 64, g_scale: float = 1.0, dev_status=None,
                 stream=None, A_log=None, dt_bias=None):
     """Chunk-local cumsum of g [B,T,HV,K] fp32; rows outside every sequence are zero.
     With `A_log`, g is the raw gate, activated first (see chunk_kda)."""
     g, cu_seqlens = _prep(g, cu_seqlens)
+    _one_device(g, dev_status, A_log, dt_bias)
     B, T, HV, K = g.shape
     shape = KdaShape(B, T, 1, HV, K, 1, B if cu_seqlens is None else cu_seqlens.numel() - 1,
                      KDA_DTYPE_F32, -1.0, float(g_scale), 0)
@@ -331,6 +368,7 @@ def gate_cumsum(g, cu_seqlens=None, chunk_size: int = 64, g_scale: float = 1.0, 
     return out
 
 
+@_on_tensor_device
 def chunk_kda(q, k, v, g, beta, scale=None, initial_state=None, output_final_state=False,
               cu_seqlens=None, use_qk_l2norm_in_kernel=False, g_scale=1.0, g_is_cumsum=False,
               split_scan=False, A_log=None, dt_bias=None, beta_sigmoid_scale=0.0,
@@ -339,6 +377,7 @@ def chunk_kda(q, k, v, g, beta, scale=None, initial_state=None, output_final_sta
     with `A_log` the raw gate (activated inside: -exp(A_log) softplus(g + dt_bias),
     times g_scale); `beta_sigmoid_scale` > 0 makes `beta` logits."""
     q, k, v, g, beta, h0, cu = _prep(q, k, v, g, beta, initial_state, cu_seqlens)
+    _one_device(q, workspace, dev_status, A_log, dt_bias)
     flags = (KDA_FLAG_QK_L2NORM if use_qk_l2norm_in_kernel else 0) | (
         KDA_FLAG_G_IS_CUMSUM if g_is_cumsum else 0) | (KDA_FLAG_SPLIT_SCAN if split_scan else 0) | (
         KDA_FLAG_SERIAL if serial else 0)
@@ -358,6 +397,7 @@ def chunk_kda(q, k, v, g, beta, scale=None, initial_state=None, output_final_sta
     return o, ht
 
 
+@_on_tensor_device
 def recurrent_kda_backward(q, k, v, gate, beta, dout, initial_state=None, dht=None, *,
                            cu_seqlens=None, scale=None, g_scale=1.0, want_dh0=True,
                            use_qk_l2norm_in_kernel=False, A_log=None, dt_bias=None,
@@ -367,10 +407,9 @@ def recurrent_kda_backward(q, k, v, gate, beta, dout, initial_state=None, dht=No
     per-token log2 gate), dbeta and dh0 (None unless `want_dh0`).  With `A_log` (and
     `dt_bias`, `beta_sigmoid_scale`) the inputs are raw as in chunk_kda: dg and dbeta are
     the raw inputs' gradients and the dict adds dA_log and ddt_bias."""
-    ts = [q, k, v, gate, beta, dout, initial_state, dht, cu_seqlens, A_log, dt_bias]
-    for t in ts:
-        if t is not None and not t.is_cuda:
-            raise KdaError(KDA_ERR_INVALID_ARG, "tensors must be on a CUDA device")
+    ts = [q, k, v, gate, beta, dout, initial_state, dht, cu_seqlens, A_log, dt_bias, dev_status]
+    _one_device(*ts)
+    ts = ts[:-1]
     q, k, v, g, beta, dout, h0, dht, cu, A_log, dt_bias = [
         None if t is None else t.detach().contiguous() for t in ts]
     shape = make_shape(q, v, cu, scale, g_scale,
@@ -437,20 +476,20 @@ class _KdaFunction(torch.autograd.Function):
                 None, dA, ddt, None)
 
 
+@_on_tensor_device
 def kda_autograd(q, k, v, g, beta, initial_state=None, *, cu_seqlens=None, scale=None,
                  g_scale=1.0, chunked=True, use_qk_l2norm_in_kernel=False, A_log=None,
                  dt_bias=None, beta_sigmoid_scale=0.0):
     """(o, ht) with gradients: forward by chunk_kda (or recurrent_kda when `chunked` is
     False), backward by kda_recurrent_bwd; `g` is the per-token log2 gate, or with
     `A_log` the raw gate (A_log and dt_bias then receive gradients too)."""
-    for t in (q, k, v, g, beta, initial_state, cu_seqlens, A_log, dt_bias):
-        if t is not None and not t.is_cuda:
-            raise KdaError(KDA_ERR_INVALID_ARG, "tensors must be on a CUDA device")
+    _one_device(q, k, v, g, beta, initial_state, cu_seqlens, A_log, dt_bias)
     return _KdaFunction.apply(q, k, v, g, beta, initial_state, cu_seqlens, scale, g_scale, chunked,
                               bool(use_qk_l2norm_in_kernel), A_log, dt_bias,
                               float(beta_sigmoid_scale))
 
 
+@_on_tensor_device
 def recurrent_kda(q, k, v, gate, beta, initial_state=None, *, cu_seqlens=None,
                   output_final_state=False, scale=None, use_qk_l2norm_in_kernel=False,
                   g_scale=1.0, A_log=None, dt_bias=None, beta_sigmoid_scale=0.0,
@@ -458,6 +497,7 @@ def recurrent_kda(q, k, v, gate, beta, initial_state=None, *, cu_seqlens=None,
     """Token-by-token forward; returns (o, ht or None).  `gate` is the per-token log2 gate
     (or, with `A_log`, the raw gate; see chunk_kda)."""
     q, k, v, g, beta, h0, cu = _prep(q, k, v, gate, beta, initial_state, cu_seqlens)
+    _one_device(q, dev_status, final_state_out, A_log, dt_bias)
     flags = KDA_FLAG_QK_L2NORM if use_qk_l2norm_in_kernel else 0
     shape = make_shape(q, v, cu, scale, g_scale, flags)
     o = torch.empty(v.shape, dtype=q.dtype, device=q.device)
