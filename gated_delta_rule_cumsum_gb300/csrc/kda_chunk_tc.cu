@@ -1440,42 +1440,34 @@ __global__ void __launch_bounds__(256) chunk_fix_tc_kernel(ChunkArgs p) {
 template <int KK, bool ACT, bool PADK>
 cudaError_t launch_prep_t(const ChunkArgs &a, cudaStream_t st, int64_t cta_cap) {
     using S = PrepSmem<KK>;
-    struct Info {
-        int sms, regs_sm, smem_sm, regs, static_smem;
-    };
-    static DeviceOnce once;
-    static Info info[64];
-    int dev = 0;
-    cudaError_t e = once.run(&dev, [](int d) {
-        cudaError_t r = cudaFuncSetAttribute(chunk_prep_tc_kernel<KK, ACT, PADK>,
+    static bool attr = false;
+    static int sms = 0, regs_sm = 0, smem_sm = 0;
+    static cudaFuncAttributes fa;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(chunk_prep_tc_kernel<KK, ACT, PADK>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)S::total(256));
-        if (r == cudaSuccess)
-            r = cudaFuncSetAttribute(chunk_prep_tc_kernel<KK, ACT, PADK>,
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(chunk_prep_tc_kernel<KK, ACT, PADK>,
                                      cudaFuncAttributePreferredSharedMemoryCarveout,
                                      (int)cudaSharedmemCarveoutMaxShared);
-        Info &in = info[d];
-        cudaFuncAttributes fa;
-        if (r == cudaSuccess) r = cudaDeviceGetAttribute(&in.sms, cudaDevAttrMultiProcessorCount, d);
-        if (r == cudaSuccess) r = cudaDeviceGetAttribute(&in.regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, d);
-        if (r == cudaSuccess) r = cudaDeviceGetAttribute(&in.smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, d);
-        if (r == cudaSuccess) r = cudaFuncGetAttributes(&fa, chunk_prep_tc_kernel<KK, ACT, PADK>);
-        if (r == cudaSuccess) {
-            in.regs = fa.numRegs;
-            in.static_smem = (int)fa.sharedSizeBytes;
-        }
-        return r;
-    });
-    if (e != cudaSuccess) return e;
-    const Info &in = info[dev];
+        int dev = 0;
+        if (e == cudaSuccess) e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, chunk_prep_tc_kernel<KK, ACT, PADK>);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
     // Resident CTAs, from the kernel's registers and this dv's shared memory
     // (TMEM: 256 columns per CTA, at most two per SM).
     const uint32_t smem = S::total(a.V);
-    const int by_regs = in.regs_sm / (((in.regs + 7) / 8 * 8) * 256);
-    const int by_smem = in.smem_sm / (int)(smem + in.static_smem + 1024);
+    const int by_regs = regs_sm / (((fa.numRegs + 7) / 8 * 8) * 256);
+    const int by_smem = smem_sm / (int)(smem + fa.sharedSizeBytes + 1024);
     int per_sm = by_regs < by_smem ? by_regs : by_smem;
     per_sm = per_sm < 1 ? 1 : (per_sm > 2 ? 2 : per_sm);
-    int64_t ctas = (int64_t)in.sms * per_sm;
+    int64_t ctas = (int64_t)sms * per_sm;
     if (cta_cap > 0 && cta_cap < ctas) ctas = cta_cap;
     const int64_t units = prep_units(a);
     if (units == 0) return cudaSuccess;
@@ -1500,13 +1492,13 @@ cudaError_t launch_prep(const ChunkArgs &a, cudaStream_t st, int64_t cta_cap = 0
 template <int KK, int SBV>
 cudaError_t launch_scan(const ChunkArgs &a, cudaStream_t st) {
     using S = ScanSmem<KK, SBV>;
-    static DeviceOnce once;
-    int dev = 0;
-    const cudaError_t e = once.run(&dev, [](int) {
-        return cudaFuncSetAttribute(chunk_scan_tc_kernel<KK, SBV>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::total);
-    });
-    if (e != cudaSuccess) return e;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(chunk_scan_tc_kernel<KK, SBV>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::total);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
     const int64_t per = a.split ? 2 * (a.V / SBV) + KK / SBV : a.V / SBV;
     const int64_t blocks = (int64_t)a.N * a.HV * per;
     if (blocks == 0) return cudaSuccess;
@@ -1519,19 +1511,21 @@ cudaError_t launch_scan(const ChunkArgs &a, cudaStream_t st) {
 template <int KK, int VV>
 cudaError_t launch_fix(const ChunkArgs &a, cudaStream_t st) {
     using S = FixSmem<KK, VV>;
-    static DeviceOnce once;
-    static int slots[64];  // two resident CTAs per SM
-    int dev = 0;
-    const cudaError_t e = once.run(&dev, [](int d) {
-        cudaError_t r = cudaFuncSetAttribute(chunk_fix_tc_kernel<KK, VV>,
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(chunk_fix_tc_kernel<KK, VV>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::total);
-        int sms = 0;
-        if (r == cudaSuccess) r = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, d);
-        slots[d] = 2 * sms;
-        return r;
-    });
-    if (e != cudaSuccess) return e;
-    const int slots_on_device = slots[dev];
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    static int slots_on_device = 0;  // two resident CTAs per SM
+    if (slots_on_device == 0) {
+        int dev = 0, sms = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        slots_on_device = 2 * sms;
+    }
     const int64_t units = (a.ht ? (int64_t)a.N * a.HV * (KK / 16) * (VV / 32) : 0) +
                           (int64_t)a.HV * ((a.slots + 1) / 2);
     if (units == 0) return cudaSuccess;
@@ -1543,13 +1537,14 @@ cudaError_t launch_fix(const ChunkArgs &a, cudaStream_t st) {
 }
 
 cudaError_t sm_count(int *out) {
-    static DeviceOnce once;
-    static int sms[64];
+    static int sms[64] = {0};
     int dev = 0;
-    const cudaError_t e = once.run(&dev, [](int d) {
-        return cudaDeviceGetAttribute(&sms[d], cudaDevAttrMultiProcessorCount, d);
-    });
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (sms[dev] == 0 &&
+        (e = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return e;
     *out = sms[dev];
     return cudaSuccess;
 }
