@@ -629,14 +629,14 @@ bool long_form_fits(const RecurrentArgs &a) {
 
 template <typename T>
 cudaError_t launch_long(const RecurrentArgs &a, cudaStream_t st) {
-    static DeviceOnce once;
+    static bool attr = false;
     const int smem = LongSmem<T>::total;
-    int dev = 0;
-    const cudaError_t e = once.run(&dev, [](int) {
-        return cudaFuncSetAttribute(recurrent_long_kernel<T>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, LongSmem<T>::total);
-    });
-    if (e != cudaSuccess) return e;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(recurrent_long_kernel<T>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
     const int64_t blocks = (int64_t)a.N * a.HV * ((a.V + 127) / 128);
     prof_begin("recurrent_long", st);
     recurrent_long_kernel<T><<<(unsigned)blocks, kLThreads, smem, st>>>(a);
