@@ -21,7 +21,8 @@ Two independent formulations live here:
 * `chunk_backward.chunk_grads` -- the same gradients by the chunk form, stage by
   stage in the order of ALGORITHM.md, "Backward" (recompute, re-scan, dAv, dhu,
   wy_dqkg, intra, dg cumsum), in numpy fp64, with the per-chunk intermediates on
-  request; pinned in tests/test_oracle_chunk_backward.py against `backward`.
+  request and the L2-norm and activation options; pinned in
+  tests/test_oracle_chunk_backward.py against `backward`.
 * `activation` -- the optional input activations (gate -exp(A_log) softplus(g +
   dt_bias), beta sigmoid) of kernel-fun 0.2.0.dev1 wheel, kda/chain.py and
   kda/ops.py, in numpy fp64; pinned in tests/test_oracle_activation.py.

@@ -21,8 +21,15 @@ through the chunk form's own formulas (ALGORITHM.md, "Forward", Stages 1-4):
 
 The pages print some of these formulas and not others; each step here is derived
 from the forward formulas above (2^x contributes ln 2 to its exponent's gradient).
-It is the plain op: no q/k L2 norm and no input activations (oracle/backward.py has
-both).  tests/test_oracle_chunk_backward.py pins every gradient against
+The op's options wrap this core exactly as they wrap the forward: with `l2norm` the
+core sees q / sqrt(sum q^2 + 1e-6) (and the same of k) per (token, head), and the
+raw rows' gradients are r (dx^ - x^ (x^ . dx^)), r the row's inverse norm; with
+`A_log` the core's gate is -exp(A_log) softplus(g + dt_bias) (natural log; kernel-fun
+wheel, kda/chain.py, gate_backward) and the raw gate's gradient is the core's times
+-exp(A_log) sigmoid(g + dt_bias), plus dA_log = sum dg' g' and dt_bias's sum over
+tokens; with `beta_scale` > 0 the core's beta is sigmoid(beta) beta_scale (rounded to
+bf16 in value when `beta_bf16`, the gradient passing straight through).
+tests/test_oracle_chunk_backward.py pins every gradient against
 oracle/backward.py, the reverse-mode derivative of the token recurrence -- an
 independent derivation of the same numbers -- at chunk sizes from 1 to past T, with
 packing, empty slots, partial chunks and grouped value heads.
@@ -110,9 +117,63 @@ def _chunk_backward(f, qc, kc, vc, bc, do_c, dh_next, scale):
     return dict(dq=dq, dk=dk, dv=dv, dbeta=dbeta, dg2=dg2, dAqk=dAqk, dAkk=dAkk), dh
 
 
+def _l2norm_rows(x):
+    """x / sqrt(sum x^2 + 1e-6) over the last axis, and the inverse norms."""
+    r = 1.0 / np.sqrt(np.sum(x * x, axis=-1, keepdims=True) + 1e-6)
+    return x * r, r
+
+
+def _l2norm_bwd(xh, r, dxh):
+    """Gradient of the raw rows from that of the normalised rows xh = r x."""
+    return r * (dxh - xh * np.sum(xh * dxh, axis=-1, keepdims=True))
+
+
 def chunk_grads(q, k, v, g, beta, do, h0=None, dht=None, cu_seqlens=None, scale=None,
+                g_scale=1.0, chunk_size=64, stages=False, l2norm=False, A_log=None,
+                dt_bias=None, beta_scale=0.0, beta_bf16=False):
+    """The chunk-form gradients with the op's options (see the module docstring):
+    the plain core (`_core_grads`) between the options' forward transforms and their
+    chain rules.  Adds dA_log [HV] and ddt_bias [HV, K] (None when not given)."""
+    f64 = lambda x: None if x is None else np.asarray(x, dtype=np.float64)
+    q, k, g, beta = f64(q), f64(k), f64(g), f64(beta)
+    if l2norm:
+        qh, rq = _l2norm_rows(q)
+        kh, rk = _l2norm_rows(k)
+    else:
+        qh, kh = q, k
+    ga, bact = g, beta
+    if A_log is not None:
+        a = np.exp(f64(A_log))[None, None, :, None]
+        x = g if dt_bias is None else g + f64(dt_bias)[None, None]
+        ga = -a * np.logaddexp(0.0, x)
+        sig = 0.5 * (1.0 + np.tanh(0.5 * x))
+    if beta_scale > 0:
+        sb = 0.5 * (1.0 + np.tanh(0.5 * beta))
+        bact = beta_scale * sb
+        if beta_bf16:
+            import torch
+
+            bact = torch.from_numpy(bact).to(torch.bfloat16).to(torch.float64).numpy()
+    out = _core_grads(qh, kh, v, ga, bact, do, h0, dht, cu_seqlens, scale, g_scale, chunk_size,
+                      stages)
+    if l2norm:
+        out["dq"] = _l2norm_bwd(qh, rq, out["dq"])
+        out["dk"] = _l2norm_bwd(kh, rk, out["dk"])
+    out["dA_log"] = out["ddt_bias"] = None
+    if A_log is not None:
+        dga = out["dg"]
+        out["dg"] = dga * (-a) * sig
+        out["dA_log"] = np.sum(dga * ga, axis=(0, 1, 3))
+        if dt_bias is not None:
+            out["ddt_bias"] = np.sum(out["dg"], axis=(0, 1))
+    if beta_scale > 0:
+        out["dbeta"] = out["dbeta"] * beta_scale * sb * (1.0 - sb)
+    return out
+
+
+def _core_grads(q, k, v, g, beta, do, h0=None, dht=None, cu_seqlens=None, scale=None,
                 g_scale=1.0, chunk_size=64, stages=False):
-    """Gradients of sum(o * do) + sum(ht * dht) by the chunk form, in fp64.
+    """Gradients of sum(o * do) + sum(ht * dht) by the chunk form, in fp64 (plain op).
 
     Shapes as oracle.backward.recurrent_grads: q, k [B,T,H,K]; v, do [B,T,HV,V];
     g [B,T,HV,K] per-token log gate (times g_scale: log2 units after it); beta

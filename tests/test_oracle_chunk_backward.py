@@ -96,3 +96,32 @@ def test_planted_mistakes_are_caught(monkeypatch, mutant):
         monkeypatch.setattr(cb, "LN2", 1.0)
     got, ref = _both(_problem(5), 4)
     assert _err(got, ref)["dg"] > 1e-3
+
+
+def test_l2norm_option():
+    p = _problem(6)
+    p["q"] *= 2.5
+    args = (p["q"], p["k"], p["v"], p["g"], p["beta"], p["do"], p["h0"], p["dht"])
+    ref = ob.recurrent_grads(*args, cu_seqlens=p["cu"], l2norm=True)
+    got = cb.chunk_grads(*args, cu_seqlens=p["cu"], chunk_size=4, l2norm=True)
+    assert max(_err(got, ref).values()) < 1e-12, _err(got, ref)
+
+
+@pytest.mark.parametrize("bias,beta_scale", [(True, 2.0), (False, 0.0)])
+def test_activation_options(bias, beta_scale):
+    p = _problem(7)
+    r = np.random.default_rng(8)
+    g_raw = r.standard_normal(p["g"].shape) - 1.0
+    b_raw = r.standard_normal(p["beta"].shape) if beta_scale else p["beta"]
+    A_log = r.uniform(-0.5, 0.8, 2)
+    dt_bias = 0.5 * r.standard_normal((2, 3)) if bias else None
+    args = (p["q"], p["k"], p["v"], g_raw, b_raw, p["do"], p["h0"], p["dht"])
+    kw = dict(cu_seqlens=p["cu"], g_scale=1.0 / math.log(2.0), A_log=A_log, dt_bias=dt_bias,
+              beta_scale=beta_scale)
+    ref = ob.recurrent_grads(*args, **kw)
+    got = cb.chunk_grads(*args, chunk_size=4, **kw)
+    names = NAMES + ("dA_log",) + (("ddt_bias",) if bias else ())
+    err = {n: float(np.abs(got[n] - ref[n]).max() / np.abs(ref[n]).max()) for n in names}
+    assert max(err.values()) < 1e-12, err
+    if not bias:
+        assert got["ddt_bias"] is None
