@@ -114,3 +114,27 @@ def test_every_bench_workload_exists_in_the_generator():
         w = kda_synth.workload(idx, **over)
         assert steps >= 1 and warm >= 3, name
         assert (name in bench.RECURRENT) == bool(w.decode_seqs), name
+
+
+def test_reference_arm_prints_the_contract_line():
+    """`bench.py --impl reference` end to end on the host (the oracle timed on a bounded
+    sample): one JSON line with the arm's keys, its e2e moving nothing."""
+    import json
+    import subprocess
+    import sys
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "3"], capture_output=True, text=True,
+                       timeout=600, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [x for x in r.stdout.splitlines() if x.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["value"] > 0 and d["steps"] == 1 and d["warmup"] == 3
+    assert d["n_gpus"] == 1 and d["higher_is_better"] is True and d["unit"] == "tokens/s"
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+    assert d["config"]["workload"].startswith("train_bf16_B1_T8192")
