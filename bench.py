@@ -14,7 +14,9 @@ to flush the 129 MB L2.
 `--workload` picks one of the other synthetic workloads instead (grouped value
 heads B4 T4096 HV32; packed varlen H=HV=32; decode 4096 x 1 token; its
 256-token prefill variant); decode and prefill steps are one in-place
-`kda_recurrent_fwd` call.  `--impl reference` times the fp64 CPU oracle
+`kda_recurrent_fwd` call, and a train_bwd step is one `kda_recurrent_bwd` call
+(the gradients of the training shape's recurrence for dL/do and dL/dht drawn
+once).  `--impl reference` times the fp64 CPU oracle
 instead, on the host cores, each step a bounded sample of the same workload.
 Under torchrun (N > 1) every rank runs its own replica of the workload (weak
 scaling, no collective on the data path); rank 0 prints the line with the
