@@ -1,5 +1,6 @@
 /*
- * kda.h -- C ABI of the GB300 (sm_103a) library for the KDA forward pass.
+ * kda.h -- C ABI of the GB300 (sm_103a) library for KDA: the forward passes and
+ * the recurrence's backward.
  *
  * KDA (Kimi Delta Attention) is a gated delta rule with a per-channel diagonal
  * decay.  Per (sequence n, value head hv), with q/k taken from head
