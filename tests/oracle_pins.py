@@ -266,6 +266,96 @@ def check_extreme_decay(rec):
         _close(o[0, t, 0], want, rtol=2e-4, what=f"extreme decay t={t}")
 
 
+
+# ---------------------------------------------------------------- a0: L2-norm option
+# kernel-fun 0.2.0.dev1 wheel, kda/autograd.py, ChunkKDAFunction.forward
+# (use_qk_l2norm) and attention-gym PR #345 commit message "fuse q l2norm": every
+# (token, head) row of q and of k is divided by its L2 norm over the K channels;
+# the epsilon's value is not printed there (reading: 1e-6 inside the square root).
+
+def _row_scaled_inputs(seed, B, T, H, HV, K, V, lo=1.0, hi=40.0):
+    """Rows that are NOT unit norm: q, k ~ N(0,1), each (token, head) row then
+    multiplied by its own scale in [lo, hi] (norms well above the epsilon)."""
+    q, k, v, g, beta = _rand_inputs(seed, B, T, H, HV, K, V, unit_k=False)
+    r = _rng(seed + 1000)
+    for x in (q, k):
+        n = np.linalg.norm(x, axis=-1, keepdims=True)
+        x *= np.maximum(n, 0.5) / n                      # no row shorter than 0.5
+        x *= r.uniform(lo, hi, x.shape[:-1] + (1,))
+    return q, k, v, g, beta
+
+
+def check_l2norm_is_scale_invariant_unit_rows(rec):
+    """With the option, rows of any length give the result of the plain
+    recurrence on the exactly normalised rows q / |q|, k / |k| (to the
+    epsilon's relative effect, below 1e-6 here).  Per-row scales differ across
+    tokens and heads, so a norm over the wrong extent, a norm applied to q only
+    or to k only, or a missing square root changes the result."""
+    B, T, H, HV, K, V = 1, 10, 2, 4, 5, 3
+    q, k, v, g, beta = _row_scaled_inputs(111, B, T, H, HV, K, V)
+    h0 = 0.3 * _rng(112).standard_normal((B, HV, K, V))
+    unit = lambda x: x / np.linalg.norm(x, axis=-1, keepdims=True)
+    o1, s1 = rec(q, k, v, g, beta, h0=h0, l2norm=True)
+    o2, s2 = rec(unit(q), unit(k), v, g, beta, h0=h0, l2norm=False)
+    _close(o1, o2, rtol=1e-5, what="l2norm o vs unit rows")
+    _close(s1, s2, rtol=1e-5, what="l2norm ht vs unit rows")
+    # the option must matter on such rows: the raw recurrence differs a lot
+    o3, _ = rec(q, k, v, g, beta, h0=h0, l2norm=False)
+    assert float(np.max(np.abs(o3 - o1))) > 1e-2, "the L2-norm flag had no effect"
+
+
+def check_l2norm_zero_and_short_rows(rec):
+    """A zero q row reads out exactly zero (the epsilon keeps 0 / 0 away); a zero
+    k row writes nothing, so the state only decays at that token.  A row of
+    length r = 1e-4 (r^2 far below the epsilon) is scaled by 1 / sqrt(r^2 +
+    1e-6) to length r / sqrt(r^2 + 1e-6) ~ 0.0995, not to 1: the reading of the
+    epsilon, pinned on the one input where it decides the result."""
+    B, T, H, HV, K, V = 1, 6, 1, 1, 4, 3
+    q, k, v, g, beta = _row_scaled_inputs(121, B, T, H, HV, K, V)
+    h0 = _rng(122).standard_normal((B, HV, K, V))
+    q[0, 2, 0] = 0.0
+    k[0, 4, 0] = 0.0
+    o, _ = rec(q, k, v, g, beta, h0=h0, l2norm=True)
+    assert np.all(np.isfinite(o)), "zero rows must not produce NaN"
+    assert np.all(o[0, 2, 0] == 0.0), "a zero query row must read out zero"
+    unit = lambda x: x / np.linalg.norm(x, axis=-1, keepdims=True)
+    # token 4 (k = 0): o_4 = scale * (Diag(2^g_4) S_3)^T q_4 / |q_4|
+    _, S3 = rec(q[:, :4], k[:, :4], v[:, :4], g[:, :4], beta[:, :4], h0=h0, l2norm=True)
+    S4 = np.exp2(g[0, 4, 0])[:, None] * S3[0, 0]
+    _close(o[0, 4, 0], S4.T @ unit(q)[0, 4, 0] / math.sqrt(K), rtol=1e-6,
+           what="zero key row writes nothing")  # 1e-6: the epsilon's effect on q_4
+    # short rows: q_t = r u with |u| = 1
+    r = 1e-4
+    qs, ks = q.copy(), k.copy()
+    qs[0, 1, 0] = r * unit(q)[0, 1, 0]
+    ks[0, 3, 0] = r * unit(k)[0, 3, 0]
+    o_s, s_s = rec(qs, ks, v, g, beta, h0=h0, l2norm=True)
+    f = r / math.sqrt(r * r + 1e-6)
+    unit0 = lambda x: x / np.maximum(np.linalg.norm(x, axis=-1, keepdims=True), 1e-300)
+    qe, ke = unit0(qs), unit0(ks)  # the zero rows stay zero
+    qe[0, 1, 0] *= f
+    ke[0, 3, 0] *= f
+    o_e, s_e = rec(qe, ke, v, g, beta, h0=h0, l2norm=False)
+    _close(o_s, o_e, rtol=1e-6, what="short rows o")  # 1e-6: epsilon's effect on the long rows
+    _close(s_s, s_e, rtol=1e-6, what="short rows ht")
+
+
+def check_l2norm_rows_are_independent(rec):
+    """The norm of a (token, head) row involves that row only: rescaling every
+    row of q/k head 1 leaves the value heads of q/k head 0 bit for bit unchanged
+    (grouped value heads, HV = 2H) and those of head 1 unchanged to rounding."""
+    B, T, H, HV, K, V = 1, 8, 2, 4, 4, 3
+    q, k, v, g, beta = _row_scaled_inputs(131, B, T, H, HV, K, V)
+    o1, s1 = rec(q, k, v, g, beta, l2norm=True)
+    q2, k2 = q.copy(), k.copy()
+    q2[:, :, 1] *= 37.0
+    k2[:, :, 1] *= 0.03
+    o2, s2 = rec(q2, k2, v, g, beta, l2norm=True)
+    assert np.array_equal(o1[:, :, :2], o2[:, :, :2]), "head 0 outputs changed"
+    assert np.array_equal(s1[:, :2], s2[:, :2]), "head 0 states changed"
+    _close(o1[:, :, 2:], o2[:, :, 2:], rtol=1e-5, what="head 1 rescaled rows")
+
+
 ALL_CHECKS = [
     check_chunked_equals_recurrent,
     check_beta_zero_is_pure_decay,
@@ -278,6 +368,9 @@ ALL_CHECKS = [
     check_gva_equals_repeated_heads,
     check_packed_equals_dense_slices,
     check_extreme_decay,
+    check_l2norm_is_scale_invariant_unit_rows,
+    check_l2norm_zero_and_short_rows,
+    check_l2norm_rows_are_independent,
 ]
 
 

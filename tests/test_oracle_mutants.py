@@ -32,6 +32,18 @@ MUTANTS = [
     ("l2norm_no_sqrt", "qn = 1.0 / sqrt(sq + KDA_ORACLE_L2NORM_EPS);",
      "qn = 1.0 / (sq + KDA_ORACLE_L2NORM_EPS);"),
     ("decay_after_write", None, None),  # built below: the decay moved after the rank-1 write
+    # the L2-norm option (kernel-fun wheel, kda/autograd.py, use_qk_l2norm)
+    ("l2norm_q_only", "kn = 1.0 / sqrt(sk + KDA_ORACLE_L2NORM_EPS);", "kn = 1.0;"),
+    ("l2norm_k_takes_q_norm", "kn = 1.0 / sqrt(sk + KDA_ORACLE_L2NORM_EPS);", "kn = qn;"),
+    ("l2norm_eps_outside_sqrt", "qn = 1.0 / sqrt(sq + KDA_ORACLE_L2NORM_EPS);\n"
+     "                    kn = 1.0 / sqrt(sk + KDA_ORACLE_L2NORM_EPS);",
+     "qn = 1.0 / (sqrt(sq) + KDA_ORACLE_L2NORM_EPS);\n"
+     "                    kn = 1.0 / (sqrt(sk) + KDA_ORACLE_L2NORM_EPS);"),
+    ("l2norm_over_first_head", "sq += qsrc[d] * qsrc[d];\n                        sk += ksrc[d] * ksrc[d];",
+     "sq += q[(row * H) * (size_t)K + d] * q[(row * H) * (size_t)K + d];\n"
+     "                        sk += k[(row * H) * (size_t)K + d] * k[(row * H) * (size_t)K + d];"),
+    ("l2norm_half_the_channels", "                    for (int d = 0; d < K; ++d) {\n                        sq +=",
+     "                    for (int d = 0; d < K / 2; ++d) {\n                        sq +="),
 ]
 
 
