@@ -247,6 +247,39 @@ def _traffic(kernel, workload="train"):
     return rec["dram_bytes_per_step"]
 
 
+def workload_config(name, world=1):
+    """The `config` of a bench line, from the workload's definition alone, so
+    both arms (ours and the reference) report the same keys and values."""
+    import kda_synth
+
+    idx, over, _, _ = WORKLOADS[name]
+    w = kda_synth.workload(idx, **over)
+    recurrent = name in RECURRENT
+    if w.packed:
+        # the packed layout is drawn from the seed: count its sequences and tokens
+        offs = kda_synth.make_inputs(kda_synth.workload(w, B=1, T=1, H=1, HV=1, K=1, V=1,
+                                                        fill_limit=w.fill_limit,
+                                                        len_max=w.len_max),
+                                     "cpu")
+        seqs, tokens = offs["N"], offs["tokens"]
+    else:
+        seqs, tokens = w.B, w.B * w.T
+    return {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "HV": w.HV, "K": w.K, "V": w.V,
+            "input_dtype": "bf16" if w.dtype == _bf16() else "f32", "gate_dtype": "f32",
+            "h0": "N(0,0.1) fp32" if w.has_h0 else "none",
+            "ht": "in place (ht == h0)" if recurrent else "stored",
+            "pass": "backward" if name == "train_bwd" else "forward",
+            "sequences": seqs, "tokens": tokens,
+            "l2_flush": "512 MiB write between timed steps",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+
+def _bf16():
+    import torch
+
+    return torch.bfloat16
+
+
 # ------------------------------------------------------------------ CPU oracle
 def oracle_sample(inp, max_tokens):
     """The first sequences (or, for one long sequence, the first tokens) of the
@@ -342,10 +375,10 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "HV": w.HV, "K": w.K,
-                   "V": w.V, "input_dtype": "bf16", "sample_tokens_per_step": L},
+        "config": workload_config(args.workload, args.gpus),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
-                         "kind": "oracle", "sample": f"{text}, all {w.HV} heads, per step"},
+                         "kind": "oracle", "sample_tokens_per_step": L,
+                         "sample": f"{text}, all {w.HV} heads, per step"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -612,14 +645,7 @@ def run_ours(args):
         "metric": _metric(args.workload, w), "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": compute_dtype, "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "HV": w.HV, "K": w.K,
-                   "V": w.V, "input_dtype": "bf16", "gate_dtype": "f32",
-                   "h0": "N(0,0.1) fp32" if h0 is not None else "none",
-                   "ht": "in place (ht == h0)" if recurrent else "stored",
-                   "pass": "backward" if backward else "forward",
-                   "sequences": inp["N"], "tokens": tokens,
-                   "l2_flush": "512 MiB write between timed steps",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "config": workload_config(args.workload, world),
         "roofline": roofline,
         "kernels": {n: {"ms_per_launch": t / c, "launches_per_step": c / prof_steps}
                     for n, (t, c) in per_kernel.items()},

@@ -26,9 +26,10 @@ import torch
 __all__ = [
     "KDA_OK", "KDA_ERR_INVALID_ARG", "KDA_ERR_UNSUPPORTED", "KDA_ERR_BAD_CU_SEQLENS",
     "KDA_ERR_CUDA", "KDA_ERR_TIMEOUT", "KDA_FLAG_QK_L2NORM", "KDA_FLAG_G_IS_CUMSUM",
-    "KDA_FLAG_SPLIT_SCAN", "KDA_FLAG_SERIAL", "KdaActivation", "make_activation",
+    "KDA_FLAG_SPLIT_SCAN", "KDA_FLAG_SERIAL", "KDA_FLAG_TEST_WAIT_TIMEOUT", "KdaActivation", "make_activation",
     "KdaError", "KdaShape", "load", "library_path", "make_shape",
     "kda_gate_cumsum", "kda_chunk_fwd", "kda_recurrent_fwd", "kda_chunk_workspace_size",
+    "kda_workspace_size",
     "kda_recurrent_bwd", "kda_recurrent_bwd_workspace_size", "recurrent_kda_backward", "kda_autograd",
     "kda_gate_cumsum_act", "kda_chunk_fwd_act", "kda_recurrent_fwd_act", "kda_recurrent_bwd_act",
     "kda_chunk_fwd_noalloc", "KDA_NOALLOC_SCRATCH_BYTES",
@@ -43,6 +44,7 @@ KDA_ERR_BAD_CU_SEQLENS, KDA_ERR_CUDA, KDA_ERR_TIMEOUT = 3, 4, 5
 KDA_DTYPE_F32, KDA_DTYPE_BF16 = 0, 1
 KDA_FLAG_QK_L2NORM, KDA_FLAG_G_IS_CUMSUM, KDA_FLAG_SPLIT_SCAN = 1 << 0, 1 << 1, 1 << 2
 KDA_FLAG_SERIAL = 1 << 3
+KDA_FLAG_TEST_WAIT_TIMEOUT = 1 << 31
 KDA_DEVICE_BAD_CU_SEQLENS, KDA_DEVICE_TIMEOUT = 1 << 0, 1 << 1
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -104,6 +106,7 @@ _SIGNATURES = {
     "kda_chunk_fwd": (_ST, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.POINTER(KdaShape), _VP,
                             _VP, _VP, _SZ, _VP, _VP]),
     "kda_chunk_workspace_size": (_SZ, [ctypes.POINTER(KdaShape)]),
+    "kda_workspace_size": (_SZ, [ctypes.POINTER(KdaShape)]),
     "kda_recurrent_bwd": (_ST, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.POINTER(KdaShape),
                                 _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP]),
     "kda_recurrent_bwd_act": (_ST, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.POINTER(KdaShape),
@@ -226,6 +229,11 @@ KDA_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 def kda_chunk_workspace_size(shape: KdaShape) -> int:
     return int(load().kda_chunk_workspace_size(ctypes.byref(shape)))
+
+
+def kda_workspace_size(shape: KdaShape) -> int:
+    """kda_chunk_workspace_size under the boundary's original name."""
+    return int(load().kda_workspace_size(ctypes.byref(shape)))
 
 
 def kda_recurrent_bwd_workspace_size(shape: KdaShape) -> int:

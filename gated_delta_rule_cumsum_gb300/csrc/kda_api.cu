@@ -26,8 +26,9 @@ kda_status cuda_fail(cudaError_t e, const char *where) {
     return fail(KDA_ERR_CUDA, "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
 }
 
-constexpr uint32_t kKnownFlags =
-    KDA_FLAG_QK_L2NORM | KDA_FLAG_G_IS_CUMSUM | KDA_FLAG_SPLIT_SCAN | KDA_FLAG_SERIAL;
+constexpr uint32_t kKnownFlags = KDA_FLAG_QK_L2NORM | KDA_FLAG_G_IS_CUMSUM |
+                                  KDA_FLAG_SPLIT_SCAN | KDA_FLAG_SERIAL |
+                                  KDA_FLAG_TEST_WAIT_TIMEOUT;
 
 // Checks shared by the three operations.  `need_h` also checks H and HV % H.
 kda_status check_common(const char *op, const kda_shape *s, const int32_t *cu) {
@@ -363,6 +364,8 @@ size_t kda_chunk_workspace_size(const kda_shape *shape) {
     return chunk_ws_layout(shape, packed).total;
 }
 
+size_t kda_workspace_size(const kda_shape *shape) { return kda_chunk_workspace_size(shape); }
+
 kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const float *g,
                          const void *beta, const float *h0, const int32_t *cu_seqlens,
                          const kda_shape *shape, void *o, float *ht, void *workspace,
@@ -403,6 +406,7 @@ kda_status kda_chunk_fwd_act(const void *q, const void *k, const void *v, const 
     a.g_scale = shape->g_scale;
     a.l2norm = (shape->flags & KDA_FLAG_QK_L2NORM) ? 1 : 0;
     a.g_is_cumsum = (shape->flags & KDA_FLAG_G_IS_CUMSUM) ? 1 : 0;
+    a.test_timeout = (shape->flags & KDA_FLAG_TEST_WAIT_TIMEOUT) ? 1 : 0;
     a.act = ga;
     a.ctrl = reinterpret_cast<kda::ChunkCtrl *>(ws + L.ctrl);
     a.chunk_start = reinterpret_cast<int32_t *>(ws + L.chunk_start);

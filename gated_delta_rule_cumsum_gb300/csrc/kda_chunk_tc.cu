@@ -909,7 +909,7 @@ __global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
     extern __shared__ __align__(1024) unsigned char sm[];
     __shared__ uint64_t full[kStages], empty[kStages];
     // bar_v[x]: MMAs writing D1[x] done, one per buffer.
-    __shared__ uint64_t bar_v[2], bar_h, bar_fin;
+    __shared__ uint64_t bar_v[2], bar_h, bar_fin, bar_never;
     __shared__ uint32_t tslot;
     __shared__ int abort_flag;
 
@@ -960,6 +960,7 @@ __global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
         mbar_init(&bar_v[1], 1);
         mbar_init(&bar_h, 1);
         mbar_init(&bar_fin, 1);
+        mbar_init(&bar_never, 1);  // the test hook's barrier: nothing ever arrives on it
         mbar_fence_init();
         abort_flag = 0;
     }
@@ -1032,6 +1033,11 @@ __global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
         const uint64_t dh = sdesc(smem_addr(sH), SBV * 16, 128);
         const uint64_t dv = sdesc(smem_addr(sVp), SBV * 16, 128);
         constexpr uint32_t binc = 2 * SBV * 16 / 16;
+        if (p.test_timeout) {
+            // KDA_FLAG_TEST_WAIT_TIMEOUT: a consumer wait that runs out, on purpose
+            if (elect_one() && !mbar_wait(&bar_never, 0, 2000)) fail();
+            __syncwarp();
+        }
         for (int r = 0; r < R; ++r) {
             const int s = r % kStages;
             const uint32_t st = smem_addr(stage(r));
@@ -1440,31 +1446,43 @@ __global__ void __launch_bounds__(256) chunk_fix_tc_kernel(ChunkArgs p) {
 template <int KK, bool ACT, bool PADK>
 cudaError_t launch_prep_t(const ChunkArgs &a, cudaStream_t st, int64_t cta_cap) {
     using S = PrepSmem<KK>;
-    static bool attr = false;
-    static int sms = 0, regs_sm = 0, smem_sm = 0;
-    static cudaFuncAttributes fa;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(chunk_prep_tc_kernel<KK, ACT, PADK>,
+    // Kernel attributes and the device's limits, set and read once per device.
+    struct Info {
+        int sms, regs_sm, smem_sm, num_regs, static_smem;
+    };
+    static DeviceOnce once;
+    static Info info[64];
+    int dev = 0;
+    cudaError_t e = once.run(&dev, [](int d) {
+        cudaError_t r = cudaFuncSetAttribute(chunk_prep_tc_kernel<KK, ACT, PADK>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)S::total(256));
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(chunk_prep_tc_kernel<KK, ACT, PADK>,
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(chunk_prep_tc_kernel<KK, ACT, PADK>,
                                      cudaFuncAttributePreferredSharedMemoryCarveout,
                                      (int)cudaSharedmemCarveoutMaxShared);
-        int dev = 0;
-        if (e == cudaSuccess) e = cudaGetDevice(&dev);
-        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev);
-        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
-        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, chunk_prep_tc_kernel<KK, ACT, PADK>);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+        Info x{};
+        cudaFuncAttributes fa{};
+        if (r == cudaSuccess) r = cudaDeviceGetAttribute(&x.sms, cudaDevAttrMultiProcessorCount, d);
+        if (r == cudaSuccess)
+            r = cudaDeviceGetAttribute(&x.regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, d);
+        if (r == cudaSuccess)
+            r = cudaDeviceGetAttribute(&x.smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, d);
+        if (r == cudaSuccess) r = cudaFuncGetAttributes(&fa, chunk_prep_tc_kernel<KK, ACT, PADK>);
+        if (r == cudaSuccess && fa.numRegs <= 0) r = cudaErrorInvalidDeviceFunction;
+        x.num_regs = fa.numRegs;
+        x.static_smem = (int)fa.sharedSizeBytes;
+        if (r == cudaSuccess) info[d] = x;
+        return r;
+    });
+    if (e != cudaSuccess) return e;
+    const Info &I = info[dev];
     // Resident CTAs, from the kernel's registers and this dv's shared memory
     // (TMEM: 256 columns per CTA, at most two per SM).
     const uint32_t smem = S::total(a.V);
-    const int by_regs = regs_sm / (((fa.numRegs + 7) / 8 * 8) * 256);
-    const int by_smem = smem_sm / (int)(smem + fa.sharedSizeBytes + 1024);
+    const int sms = I.sms;
+    const int by_regs = I.regs_sm / (((I.num_regs + 7) / 8 * 8) * 256);
+    const int by_smem = I.smem_sm / (int)(smem + I.static_smem + 1024);
     int per_sm = by_regs < by_smem ? by_regs : by_smem;
     per_sm = per_sm < 1 ? 1 : (per_sm > 2 ? 2 : per_sm);
     int64_t ctas = (int64_t)sms * per_sm;
@@ -1492,13 +1510,13 @@ cudaError_t launch_prep(const ChunkArgs &a, cudaStream_t st, int64_t cta_cap = 0
 template <int KK, int SBV>
 cudaError_t launch_scan(const ChunkArgs &a, cudaStream_t st) {
     using S = ScanSmem<KK, SBV>;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(chunk_scan_tc_kernel<KK, SBV>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::total);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    static DeviceOnce once;
+    int dev = 0;
+    cudaError_t e = once.run(&dev, [](int) {
+        return cudaFuncSetAttribute(chunk_scan_tc_kernel<KK, SBV>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::total);
+    });
+    if (e != cudaSuccess) return e;
     const int64_t per = a.split ? 2 * (a.V / SBV) + KK / SBV : a.V / SBV;
     const int64_t blocks = (int64_t)a.N * a.HV * per;
     if (blocks == 0) return cudaSuccess;
@@ -1511,21 +1529,20 @@ cudaError_t launch_scan(const ChunkArgs &a, cudaStream_t st) {
 template <int KK, int VV>
 cudaError_t launch_fix(const ChunkArgs &a, cudaStream_t st) {
     using S = FixSmem<KK, VV>;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(chunk_fix_tc_kernel<KK, VV>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::total);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
-    static int slots_on_device = 0;  // two resident CTAs per SM
-    if (slots_on_device == 0) {
-        int dev = 0, sms = 0;
-        cudaError_t e = cudaGetDevice(&dev);
-        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
-        slots_on_device = 2 * sms;
-    }
+    static DeviceOnce once;
+    static int slots[64];  // two resident CTAs per SM
+    int dev = 0;
+    cudaError_t e = once.run(&dev, [](int d) {
+        cudaError_t r = cudaFuncSetAttribute(chunk_fix_tc_kernel<KK, VV>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)S::total);
+        int sms = 0;
+        if (r == cudaSuccess) r = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, d);
+        if (r == cudaSuccess) slots[d] = 2 * sms;
+        return r;
+    });
+    if (e != cudaSuccess) return e;
+    const int slots_on_device = slots[dev];
     const int64_t units = (a.ht ? (int64_t)a.N * a.HV * (KK / 16) * (VV / 32) : 0) +
                           (int64_t)a.HV * ((a.slots + 1) / 2);
     if (units == 0) return cudaSuccess;
@@ -1537,14 +1554,13 @@ cudaError_t launch_fix(const ChunkArgs &a, cudaStream_t st) {
 }
 
 cudaError_t sm_count(int *out) {
-    static int sms[64] = {0};
+    static DeviceOnce once;
+    static int sms[64];
     int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    cudaError_t e = once.run(&dev, [](int d) {
+        return cudaDeviceGetAttribute(&sms[d], cudaDevAttrMultiProcessorCount, d);
+    });
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (sms[dev] == 0 &&
-        (e = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-        return e;
     *out = sms[dev];
     return cudaSuccess;
 }

@@ -173,6 +173,8 @@ struct ChunkArgs {
     int B, T, H, HV, K, V, N;
     float scale, g_scale;
     int l2norm, g_is_cumsum;
+    int test_timeout;      // KDA_FLAG_TEST_WAIT_TIMEOUT: the scan's MMA issuer waits on a
+                           // barrier nothing signals (2 us limit) before its first round
     // workspace, carved by the host
     ChunkCtrl *ctrl;
     int32_t *chunk_start;  // [N + 1] (packed only)

@@ -17,6 +17,13 @@
 // cudaGetSymbolAddress once per device, on that device's first call.  The
 // computation itself is kda_chunk_fwd, unchanged, given that address as its
 // workspace.
+//
+// With lazy module loading (the CUDA default since 12.2) this translation
+// unit's device code, and with it the array, is loaded onto a device only when
+// it is first used there: that first lookup is when the 32 MiB are reserved,
+// and it can fail for lack of device memory or wait on the device.  So the
+// first call on each device belongs in the caller's set-up, before any stream
+// capture and before the caller's memory budget is fixed.
 #include <cstdio>
 #include <mutex>
 
@@ -78,10 +85,17 @@ extern "C" kda_status kda_chunk_fwd_noalloc(const void *q, const void *k, const 
             void *ptr = nullptr;
             e = cudaGetSymbolAddress(&ptr, g_scratch);
             if (e != cudaSuccess || ptr == nullptr) {
-                char buf[256];
-                snprintf(buf, sizeof(buf),
-                         "kda_chunk_fwd_noalloc: cudaGetSymbolAddress failed: %s",
-                         cudaGetErrorString(e));
+                char buf[320];
+                if (e == cudaErrorMemoryAllocation)
+                    snprintf(buf, sizeof(buf),
+                             "kda_chunk_fwd_noalloc: the device has no room for the library's "
+                             "%zu-byte scratch array (reserved when this device's first call "
+                             "loads it; make that call during set-up)",
+                             kScratchBytes);
+                else
+                    snprintf(buf, sizeof(buf),
+                             "kda_chunk_fwd_noalloc: cudaGetSymbolAddress failed: %s",
+                             cudaGetErrorString(e));
                 return set_fail(KDA_ERR_CUDA, buf);
             }
             g_addr[dev] = ptr;

@@ -629,14 +629,14 @@ bool long_form_fits(const RecurrentArgs &a) {
 
 template <typename T>
 cudaError_t launch_long(const RecurrentArgs &a, cudaStream_t st) {
-    static bool attr = false;
+    static DeviceOnce once;
     const int smem = LongSmem<T>::total;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(recurrent_long_kernel<T>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    int dev = 0;
+    cudaError_t e = once.run(&dev, [&](int) {
+        return cudaFuncSetAttribute(recurrent_long_kernel<T>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    });
+    if (e != cudaSuccess) return e;
     const int64_t blocks = (int64_t)a.N * a.HV * ((a.V + 127) / 128);
     prof_begin("recurrent_long", st);
     recurrent_long_kernel<T><<<(unsigned)blocks, kLThreads, smem, st>>>(a);

@@ -116,6 +116,21 @@ typedef enum {
                                            with events, so graph capture sees one
                                            fork and one join) on the other SMs.    */
 
+#define KDA_FLAG_TEST_WAIT_TIMEOUT (1u << 31)
+                                        /* Test hook, kda_chunk_fwd on the bf16
+                                           tensor-core path: the scan kernel's MMA
+                                           issuer first waits on a barrier that
+                                           nothing signals, with a 2 us limit.  The
+                                           wait gives up, KDA_DEVICE_TIMEOUT is set,
+                                           and the kernel takes the path of any
+                                           wait that runs out: no further MMA is
+                                           issued, the copies already in flight are
+                                           drained (bounded), every warp finishes
+                                           its rounds and the kernel returns.  The
+                                           outputs of such a call are unspecified;
+                                           the context stays usable.  Ignored by
+                                           the other kernels.                      */
+
 /* Bits of the device status word. */
 #define KDA_DEVICE_BAD_CU_SEQLENS (1 << 0)
 #define KDA_DEVICE_TIMEOUT        (1 << 1)
@@ -220,6 +235,8 @@ kda_status kda_chunk_fwd_act(const void *q, const void *k, const void *v, const 
  * shapes that may be pipelined it depends on the current device's SM count:
  * size the workspace with the device that will run the call current. */
 size_t kda_chunk_workspace_size(const kda_shape *shape);
+/* The same number under the name the boundary was first specified with. */
+size_t kda_workspace_size(const kda_shape *shape);
 
 /*
  * kda_chunk_fwd_noalloc -- kda_chunk_fwd for callers that cannot allocate
@@ -235,8 +252,11 @@ size_t kda_chunk_workspace_size(const kda_shape *shape);
  *   rejected with KDA_ERR_UNSUPPORTED and a message; nothing is enqueued.
  *   The call allocates nothing and runs every launch on `stream`, one after
  *   the other (as with KDA_FLAG_SERIAL).  Its first call on a device looks up the
- *   array's device address (cudaGetSymbolAddress) and caches it; make that
- *   first call before any stream capture on that device.
+ *   array's device address (cudaGetSymbolAddress) and caches it.  With lazy
+ *   module loading (the CUDA default) that lookup is what loads the array onto
+ *   the device and reserves its 32 MiB, so it can fail for lack of device
+ *   memory (KDA_ERR_CUDA with a message saying so) or wait on the device: make
+ *   the first call on each device during set-up, before any stream capture.
  *   Every call on a device shares the one array, so calls that overlap on the
  *   GPU (different streams without ordering) race and give wrong results;
  *   serialise them.  The array keeps the last call's contents; nothing in it

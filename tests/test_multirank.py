@@ -138,3 +138,9 @@ def test_reference_arm_prints_the_contract_line():
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
     assert d["config"]["workload"].startswith("train_bf16_B1_T8192")
+    # the same config keys and values as the GPU arm's line (both come from the
+    # workload's definition), so the two lines compare as one workload
+    sys.path.insert(0, root)
+    import bench
+
+    assert d["config"] == bench.workload_config("train")
