@@ -45,7 +45,7 @@ KDA_DTYPE_F32, KDA_DTYPE_BF16 = 0, 1
 KDA_FLAG_QK_L2NORM, KDA_FLAG_G_IS_CUMSUM, KDA_FLAG_SPLIT_SCAN = 1 << 0, 1 << 1, 1 << 2
 KDA_FLAG_SERIAL = 1 << 3
 KDA_FLAG_TEST_WAIT_TIMEOUT = 1 << 31
-KDA_DEVICE_BAD_CU_SEQLENS, KDA_DEVICE_TIMEOUT = 1 << 0, 1 << 1
+KDA_DEVICE_BAD_CU_SEQLENS, KDA_DEVICE_TIMEOUT, KDA_DEVICE_INTERNAL = 1 << 0, 1 << 1, 1 << 2
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "_build", "libkda_gb300.so")

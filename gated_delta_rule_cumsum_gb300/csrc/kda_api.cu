@@ -458,6 +458,8 @@ kda_status kda_read_device_status(const int32_t *dev_status, int32_t *host_bits,
         return fail(KDA_ERR_BAD_CU_SEQLENS, "device reported invalid cu_seqlens");
     if (bits & KDA_DEVICE_TIMEOUT)
         return fail(KDA_ERR_TIMEOUT, "a bounded device-side wait timed out");
+    if (bits & KDA_DEVICE_INTERNAL)
+        return fail(KDA_ERR_CUDA, "a kernel found an internal launch invariant broken");
     return KDA_OK;
 }
 

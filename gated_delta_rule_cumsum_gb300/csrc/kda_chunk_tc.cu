@@ -34,6 +34,7 @@
 
 #include <mutex>
 
+#include <cuda.h>
 #include <cuda_fp16.h>
 
 namespace kda {
@@ -155,50 +156,102 @@ __device__ __forceinline__ uint4 pack8_at(const float *f) {
 }
 
 // ============================================================== prep kernel
-// Offsets of the prep's shared memory; the parts after the g2 buffer depend on
-// dv (the v tile shares that buffer), which is a runtime argument.
+// Shared memory of the prep kernel.  The kernel declares no static shared
+// memory, so the dynamic region starts 1024-byte aligned (checked at run time)
+// and every offset below is a constant.
+//
+// Inputs arrive by TMA tensor copies with 128-byte swizzling, directly in the
+// layout the tensor cores read (sdesc_sw128): the [q; k] tile ("ag") and the
+// [kb; kg of the previous chunk] tile ("kbx") each hold 128 rows in KK / 64
+// column blocks of 16 KB (rows 0..63 in the first 8 KB, rows 64..127 in the
+// second), and g lands in g2 as KK / 32 boxes of [64 rows][32 fp32].  The
+// elementwise pass then works in place.
+// With dk = 128 the solve's fp32 matrices are stored split by rows: L (rows 0..31
+// and 32..63) in the two kb pieces of kbx (which the split grams of a chunk with
+// a wide gate range never read), T and P in the two previous-kg pieces once the
+// gram MMA has read them, Akk in the two q pieces of ag.
+// Buffer plan when dk = 128 and dv <= 128 ("pref"): after the elementwise pass
+// v goes into the second half of g2 and the next unit's g channels 0..63 into the
+// first half; Akk diag(beta) goes over the second q piece.  The k rows of ag are
+// free after the W MMA (the next unit's k goes there), the q rows and v after the
+// u MMA (the next unit's q and its g channels 64..127).  Otherwise v and
+// Akk diag(beta) sit in g2 and every copy of the next unit starts after the u
+// MMA.
 template <int KK>
 struct PrepSmem {
-    static constexpr int kGS = KK + 4;                          // padded fp32 row of g2
-    // The kb / previous-kg tile is K-major with its core matrices 144 bytes apart
-    // along K (16 bytes of padding each): the halo threads' per-channel writes
-    // then fall in distinct banks.
-    static constexpr uint32_t kLbo = 144;
-    static constexpr uint32_t kSbo = (KK / 8) * kLbo;
-    static constexpr uint32_t ag = 0;                           // [128][KK]: q->qg, k->kg
-    static constexpr uint32_t kbx = ag + 128 * KK * 2;          // [128][KK] padded: kb; kg of the previous chunk
-    static constexpr uint32_t g = kbx + 16 * kSbo;              // fp32 [64][kGS] g2; later v tile + AB tile
-    static constexpr uint32_t g_need0 = 64 * kGS * 4;
+    static constexpr uint32_t kBlk = 16384;                     // column block of ag / kbx
+    static constexpr uint32_t beta = 0;                         // fp32 [64]
+    static constexpr uint32_t dprev = beta + 64 * 4;            // fp32 [128]: 2^G of the previous chunk
+    static constexpr uint32_t eg = dprev + 128 * 4;             // fp32 [128]: 2^G
+    static constexpr uint32_t gv = eg + 128 * 4;                // fp32 [128]: G
+    static constexpr uint32_t bars = gv + 128 * 4;              // 3 mbarriers
+    static constexpr uint32_t misc = bars + 3 * 8;              // tslot, range bits
+    static constexpr uint32_t cur = 1856;                       // two unit cursors (UnitCur, 40 B)
+    static constexpr uint32_t ag = 2048;                        // [q; k] tile
+    static constexpr uint32_t kbx = ag + (KK / 64) * kBlk;      // [kb; previous kg] tile
+    static constexpr uint32_t g = kbx + (KK / 64) * kBlk;       // fp32 [64][KK] g2 (swizzled); later v + AB
+    static constexpr uint32_t g_need0 = 64 * KK * 4;
+    static_assert(misc + 8 <= cur && cur + 96 <= ag && g % 1024 == 0, "prep layout");
     __host__ __device__ static constexpr uint32_t g_bytes(int VV) {
         return g_need0 > 64u * VV * 2 + 64 * 64 * 2 ? g_need0 : 64u * VV * 2 + 64 * 64 * 2;
     }
     __host__ __device__ static constexpr uint32_t extra(int VV) { return g + g_bytes(VV); }
-    // After the gram MMA: L fp32 [64][64], T fp32 [32][32], P bf16 tile [64][64],
-    // Akk fp32 [64][64].  dk = 128 reuses the kb tile and the qg rows for them.
+    // L fp32 [64][64], T fp32 [32][32], P bf16 tile [64][64], Akk fp32 [64][64].
+    // dk = 128 reuses kbx and the q pieces of ag for them (L and Akk split by rows,
+    // the second half kBlk further on); dk = 64 keeps them after g2.
     static constexpr bool big = KK == 128;
     __host__ __device__ static constexpr uint32_t lbuf(int VV) { return big ? kbx : extra(VV); }
-    __host__ __device__ static constexpr uint32_t tbuf(int VV) { return lbuf(VV) + 64 * 64 * 4; }
-    __host__ __device__ static constexpr uint32_t pbuf(int VV) { return tbuf(VV) + 32 * 32 * 4; }
+    __host__ __device__ static constexpr uint32_t tbuf(int VV) {
+        return big ? kbx + 8192 : lbuf(VV) + 64 * 64 * 4;
+    }
+    __host__ __device__ static constexpr uint32_t pbuf(int VV) {
+        return big ? kbx + kBlk + 8192 : tbuf(VV) + 32 * 32 * 4;
+    }
     __host__ __device__ static constexpr uint32_t abuf(int VV) {
         return big ? ag : pbuf(VV) + 64 * 64 * 2;
     }
     __host__ __device__ static constexpr uint32_t used(int VV) {
         return big ? extra(VV) : abuf(VV) + 64 * 64 * 4;
     }
-    static_assert(!big || kbx + 64 * 64 * 4 + 32 * 32 * 4 + 64 * 64 * 2 <= g,
-                  "solve scratch overflows the kb tile");
     // Floor so that at most two CTAs (256 TMEM columns each) share an SM.
     __host__ __device__ static constexpr uint32_t total(int VV) {
         return used(VV) > 80 * 1024 ? used(VV) : 80 * 1024;
     }
 };
 
-// Byte offset of element (r, c) in the padded kb tile.
-template <int KK>
-__device__ __forceinline__ uint32_t kbx_off(int r, int c) {
-    return (uint32_t)((r >> 3) * PrepSmem<KK>::kSbo + (c >> 3) * PrepSmem<KK>::kLbo +
-                      (r & 7) * 16 + (c & 7) * 2);
+// Where a prep unit is: written by thread 0 for the next unit while the current
+// one runs (two slots, alternating), read by every thread.
+struct UnitCur {
+    long long unit, gc;
+    int hv, b, r0, nr, cl, ncs;
+};
+static_assert(sizeof(UnitCur) <= 48, "two cursors fit their area");
+
+// The TMA descriptors of one prep launch: q and k as [B*T rows][H][K] bf16 with
+// 64 x 64 boxes, g as [B*T rows][HV][K] fp32 with 64 x 32 boxes, 128-byte swizzle.
+struct PrepMaps {
+    CUtensorMap q, k, g;
+};
+
+// One 3-D tensor-map tile load into shared memory, completion counted in bytes
+// on `bar` (coordinates innermost first: channel, head, row).
+__device__ __forceinline__ void tma_load3(void *dst, const CUtensorMap *map, int c0, int c1,
+                                          int c2, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar))
+        : "memory");
 }
+
+// fp32 index of g2 element (r, c): box c / 32 of [64][32] fp32, 128-byte rows,
+// 16-byte chunk (c % 32) / 4 stored at chunk position ((c % 32) / 4) ^ (r % 8).
+__device__ __forceinline__ int gsw(int r, int c) {
+    return (c >> 5) * 2048 + r * 32 + ((((c >> 2) & 7) ^ (r & 7)) << 2) + (c & 3);
+}
+// Byte offset of element (r, c) / of the 16-byte chunk holding channels
+// c .. c + 7 (c a multiple of 8) in the ag and kbx tiles.
+__device__ __forceinline__ uint32_t qk_off(int r, int c) { return sw128_off(r, c, 16384); }
 
 // fp32 [rows][W] with the 16-byte column group XORed by (row & 7): eight
 // consecutive rows at the same columns fall in distinct banks.
@@ -221,48 +274,88 @@ __device__ __forceinline__ void fma4(float4 &s, float a, const float4 &x) {
     s.w = fmaf(a, x.w, s.w);
 }
 
-// s += P[r][m] Q[m][c..c+3] over the 16 columns m of one 16 x 16 block of P
-// (rows pr, columns pc of a 64-wide buffer) and rows qr.. of Q (width QW).
-template <int QW>
-__device__ __forceinline__ void strip16(float4 &s, const float *P, int pr, int pc, const float *Q,
-                                        int qr, int qc) {
-#pragma unroll
-    for (int m4 = 0; m4 < 16; m4 += 4) {
-        const float4 a = ld4<64>(P, pr, pc + m4);
-        fma4(s, a.x, ld4<QW>(Q, qr + m4, qc));
-        fma4(s, a.y, ld4<QW>(Q, qr + m4 + 1, qc));
-        fma4(s, a.z, ld4<QW>(Q, qr + m4 + 2, qc));
-        fma4(s, a.w, ld4<QW>(Q, qr + m4 + 3, qc));
-    }
-}
 __device__ __forceinline__ float4 neg4(float4 v) { return make_float4(-v.x, -v.y, -v.z, -v.w); }
 
+// L and Akk (fp32 [64][64], fsw<64> layout) with dk = 128 are split by rows: rows
+// 0..31 at +0, rows 32..63 at +16 KB (two 8 KB pieces of kbx or ag).  Float index
+// of (r, c).
+template <bool SPLIT>
+__device__ __forceinline__ int akk_idx(int r, int c) {
+    return fsw<64>(r, c) + (SPLIT ? (r >> 5) * 2048 : 0);
+}
+template <bool SPLIT>
+__device__ __forceinline__ float4 lda4(const float *A, int r, int c) {
+    return *reinterpret_cast<const float4 *>(A + akk_idx<SPLIT>(r, c));
+}
+template <bool SPLIT>
+__device__ __forceinline__ void sta4(float *A, int r, int c, float4 v) {
+    *reinterpret_cast<float4 *>(A + akk_idx<SPLIT>(r, c)) = v;
+}
+// s += P[r][m] Q[m][c..c+3] over 16 columns m, P = L (64 wide) or Akk, Q = Akk or
+// T (32 wide): the strip products of the blocked solve.
+template <bool SPLIT>
+__device__ __forceinline__ void strip_la(float4 &s, const float *L, int pr, int pc, const float *A,
+                                         int qr, int qc) {
+#pragma unroll
+    for (int m4 = 0; m4 < 16; m4 += 4) {
+        const float4 a = lda4<SPLIT>(L, pr, pc + m4);
+        fma4(s, a.x, lda4<SPLIT>(A, qr + m4, qc));
+        fma4(s, a.y, lda4<SPLIT>(A, qr + m4 + 1, qc));
+        fma4(s, a.z, lda4<SPLIT>(A, qr + m4 + 2, qc));
+        fma4(s, a.w, lda4<SPLIT>(A, qr + m4 + 3, qc));
+    }
+}
+template <bool SPLIT>
+__device__ __forceinline__ void strip_at(float4 &s, const float *A, int pr, int pc, const float *T,
+                                         int qr, int qc) {
+#pragma unroll
+    for (int m4 = 0; m4 < 16; m4 += 4) {
+        const float4 a = lda4<SPLIT>(A, pr, pc + m4);
+        fma4(s, a.x, ld4<32>(T, qr + m4, qc));
+        fma4(s, a.y, ld4<32>(T, qr + m4 + 1, qc));
+        fma4(s, a.z, ld4<32>(T, qr + m4 + 2, qc));
+        fma4(s, a.w, ld4<32>(T, qr + m4 + 3, qc));
+    }
+}
+
 // ACT: the gate activation (kda_activation.A_log) is compiled in.
-// PADK: K < dk, the channels past K are zero (loads masked; otherwise K == dk
+// PADK: K < dk, the channels past K are zero (TMA fills them; otherwise K == dk
 // and the channel count is a compile-time constant).
 template <int KK, bool ACT, bool PADK>
-__global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
+__global__ void __launch_bounds__(256, 2)
+    chunk_prep_tc_kernel(ChunkArgs p, const __grid_constant__ PrepMaps maps) {
     const int Kc = PADK ? p.K : KK;  // the input's channels
     using S = PrepSmem<KK>;
+    constexpr bool kSplitA = S::big;
     const int VV = p.V;
     extern __shared__ __align__(1024) unsigned char sm[];
-    __shared__ float sBeta[64];
-    __shared__ float sDprev[128];
-    __shared__ float sEG[128];  // 2^G per channel
-    __shared__ float sGv[128];  // G per channel
-    __shared__ uint64_t bar;
-    __shared__ uint32_t tslot;
-    __shared__ int sRangeBits;
+    float *sBeta = reinterpret_cast<float *>(sm + S::beta);
+    float *sDprev = reinterpret_cast<float *>(sm + S::dprev);
+    float *sEG = reinterpret_cast<float *>(sm + S::eg);   // 2^G per channel
+    float *sGv = reinterpret_cast<float *>(sm + S::gv);   // G per channel
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + S::bars);
+    uint64_t &bar = bars[0], &bar_g = bars[1], &bar_qk = bars[2];
+    uint32_t &tslot = *reinterpret_cast<uint32_t *>(sm + S::misc);
+    int &sRangeBits = *reinterpret_cast<int *>(sm + S::misc + 4);
+    UnitCur *curs = reinterpret_cast<UnitCur *>(sm + S::cur);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     constexpr uint32_t kCols = 256;
-    constexpr int kGS = S::kGS;
+    // The swizzled TMA destinations need a 1024-byte aligned base, which a kernel
+    // without static shared memory has; checked once, never assumed silently.
+    if (smem_addr(sm) & 1023u) {
+        if (tid == 0) report(p.status, KDA_DEVICE_INTERNAL);
+        return;
+    }
+    const bool pref = KK == 128 && VV <= 128;  // see PrepSmem
 
     unsigned char *sAG = sm + S::ag;
     unsigned char *sKB = sm + S::kbx;
     float *sG2 = reinterpret_cast<float *>(sm + S::g);
-    unsigned char *sV = sm + S::g;                          // after the elementwise phase
-    unsigned char *sAB = sm + S::g + 64 * VV * 2;           // (8 KB before it valid)
+    // v: with the pref plan in the second half of g2
+    unsigned char *sV = pref ? sm + S::g + 64 * 64 * 4 : sm + S::g;
+    constexpr uint32_t v_half = 0;  // extra gap before v's rows 32..63 (none)
+    unsigned char *sAB = pref ? sAG + S::kBlk : sm + S::g + 64 * VV * 2;
     float *sL = reinterpret_cast<float *>(sm + S::lbuf(VV));    // after the gram MMA
     float *sT = reinterpret_cast<float *>(sm + S::tbuf(VV));
     unsigned char *sPB = sm + S::pbuf(VV);
@@ -273,18 +366,6 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
         tmem_alloc(&tslot, kCols);
         tmem_relinquish();
     }
-    if (tid == 0) {
-        mbar_init(&bar, 1);
-        mbar_fence_init();
-        sRangeBits = 0;
-    }
-    if (PADK && tid < 128) sDprev[tid] = 1.f;  // channels past K keep 1 (their W columns are zero)
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = tslot;
-    uint32_t phase = 0;
-
     // Persistent: the CTA takes a contiguous range of units in (value head,
     // chunk) order, so consecutive units are usually consecutive chunks of one
     // head.  The previous chunk's kg tile and 2^G then stay in shared memory
@@ -293,25 +374,110 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
     const int64_t per = (total + gridDim.x - 1) / gridDim.x;
     const int64_t ubeg = (int64_t)blockIdx.x * per;
     const int64_t uend = ubeg + per < total ? ubeg + per : total;
+    // Thread 0 only: the first unit at or after u that has rows, into *c.
+    auto find = [&](int64_t u, UnitCur *c) {
+        for (; u < uend; ++u) {
+            int hv_, b_, r0_, nr_, cl_, ns_, nc_;
+            int64_t gc_;
+            prep_unit(p, u, hv_, gc_);
+            if (locate_chunk(p, gc_, b_, r0_, nr_, cl_, &ns_, &nc_)) {
+                c->unit = u; c->gc = gc_; c->hv = hv_; c->b = b_; c->r0 = r0_; c->nr = nr_;
+                c->cl = cl_; c->ncs = nc_;
+                return;
+            }
+        }
+        c->unit = uend;
+    };
+    // Thread 0 only: the unit after *c.  Dense inputs step without divisions:
+    // chunk cl of sequence b runs over [c0, c1) (a pipelined part) or all chunks.
+    auto advance = [&](const UnitCur *c, UnitCur *n) {
+        if (c->unit + 1 >= uend) {
+            n->unit = uend;
+            return;
+        }
+        if (__builtin_expect(p.cu != nullptr, 0)) {
+            find(c->unit + 1, n);
+            return;
+        }
+        const int ntc = (p.T + kBT - 1) / kBT;
+        const int c0 = p.prep_c1 > p.prep_c0 ? p.prep_c0 : 0;
+        const int c1 = p.prep_c1 > p.prep_c0 ? p.prep_c1 : ntc;
+        int hv_ = c->hv, b_ = c->b, cl_ = c->cl + 1;
+        if (cl_ >= c1) {
+            cl_ = c0;
+            if (++b_ >= p.B) {
+                b_ = 0;
+                ++hv_;
+            }
+        }
+        n->unit = c->unit + 1;
+        n->gc = (int64_t)b_ * ntc + cl_;
+        n->hv = hv_; n->b = b_; n->cl = cl_; n->ncs = ntc;
+        n->r0 = cl_ * kBT;
+        n->nr = min(kBT, p.T - n->r0);
+    };
+    // TMA copies of a unit's g rows (into g2) and q / k rows (into ag); issued by
+    // thread 0 after a fence that orders the buffers' earlier generic-proxy
+    // accesses before the copies' writes.
+    // g goes in two halves of KK / 64 boxes each (two arrivals on bar_g per unit).
+    auto issue = [&](const UnitCur *c, bool do_g_lo, bool do_g_hi, bool do_q, bool do_k) {
+        const int row = c->b * p.T + c->r0;
+        const int h_ = c->hv / (p.HV / p.H);
+        fence_async_smem();
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            if (half ? !do_g_hi : !do_g_lo) continue;
+            mbar_arrive_expect_tx(&bar_g, 64 * KK * 2);
+#pragma unroll
+            for (int x = half * (KK / 64); x < (half + 1) * (KK / 64); ++x)
+                tma_load3(sm + S::g + x * 8192, &maps.g, x * 32, c->hv, row, &bar_g);
+        }
+        if (do_q) {
+            mbar_arrive_expect_tx(&bar_qk, 64 * KK * 2);
+#pragma unroll
+            for (int x = 0; x < KK / 64; ++x)
+                tma_load3(sAG + x * S::kBlk, &maps.q, x * 64, h_, row, &bar_qk);
+        }
+        if (do_k) {
+            mbar_arrive_expect_tx(&bar_qk, 64 * KK * 2);
+#pragma unroll
+            for (int x = 0; x < KK / 64; ++x)
+                tma_load3(sAG + x * S::kBlk + 8192, &maps.k, x * 64, h_, row, &bar_qk);
+        }
+    };
+    if (tid == 0) {
+        mbar_init(&bar, 1);
+        mbar_init(&bar_g, 2);   // the two halves of g arrive separately
+        mbar_init(&bar_qk, 2);  // the q copies and the k copies arrive separately
+        mbar_fence_init();
+        sRangeBits = 0;
+        find(ubeg, &curs[0]);
+        if (curs[0].unit < uend) issue(&curs[0], true, true, true, true);
+    }
+    if (PADK && tid < 128) sDprev[tid] = 1.f;  // channels past K keep 1 (their W columns are zero)
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tslot;
+    uint32_t phase = 0, ph_in = 0;  // MMA barrier phases; input copies (g and q/k) per unit
+    int slot = 0;
     int prev_hv = -1;
     int64_t prev_gc = -1;
-    for (int64_t unit = ubeg; unit < uend; ++unit) {
-    int hv;
-    int64_t gc;
-    prep_unit(p, unit, hv, gc);
-    int b, r0, nr, cl, nseq, ncs;
-    if (!locate_chunk(p, gc, b, r0, nr, cl, &nseq, &ncs)) {
-        prev_hv = -1;
-        continue;
-    }
-    const bool halo = continues(p, cl, ncs);  // the previous chunk's state feeds this one
+    while (true) {
+    const UnitCur *cur = &curs[slot];
+    const UnitCur *nxt = &curs[slot ^ 1];  // written below by thread 0, read after a barrier
+    const int64_t unit = cur->unit;
+    if (unit >= uend) break;
+    const int hv = cur->hv, b = cur->b, r0 = cur->r0, nr = cur->nr, cl = cur->cl;
+    const int64_t gc = cur->gc;
+    if (tid == 0) advance(cur, &curs[slot ^ 1]);
+    const bool halo = continues(p, cl, cur->ncs);  // the previous chunk's state feeds this one
     const bool carry = halo && prev_hv == hv && prev_gc == gc - 1;
     const int h = hv / (p.HV / p.H);
     unsigned char *U = static_cast<unsigned char *>(p.units) + (gc * p.HV + hv) * Lo.stride;
 
-    // ---- 1. async loads of q, k (and the previous chunk's k) as operand tiles;
-    // lanes 0..7 take the 8 rows of a core matrix (conflict-free 16-byte writes).
-    const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(p.q);
+    // ---- 1. the previous chunk's k rows when they are not carried over (the
+    // run's first unit), 16-byte chunks into the swizzled kbx rows 64..127
     const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(p.k);
     const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(p.v);
     const __nv_bfloat16 *beta = static_cast<const __nv_bfloat16 *>(p.beta);
@@ -326,107 +492,95 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
     constexpr bool gate_act = ACT;
     const float neg_a = gate_act ? gate_neg_a(p.act, hv) : 0.f;
     const float gbias = gate_act && (tid & 127) < Kc ? gate_bias(p.act, hv, tid & 127, Kc) : 0.f;
+    if (__builtin_expect(halo && !carry, 0)) {
 #pragma unroll
-    for (int it = 0; it < KK / 32; ++it) {
-        const int idx = tid + it * 256, l = idx & 31, w = idx >> 5;
-        const int i = (w & 7) * 8 + (l & 7);
-        const int c = ((w >> 3) * 4 + (l >> 3)) * 8;
-        void *dq = sAG + tile_off(i, c, KK);
-        void *dk = sAG + tile_off(64 + i, c, KK);
-        if (i < nr && c < Kc) {  // channels past K are zero: they add nothing anywhere
-            const size_t src = ((row0 + i) * p.H + h) * Kc + c;
-            cp_async16(dq, q + src);
-            cp_async16(dk, k + src);
-        } else {
-            *reinterpret_cast<uint4 *>(dq) = make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4 *>(dk) = make_uint4(0, 0, 0, 0);
-        }
-        if (halo && !carry) {
+        for (int it = 0; it < KK / 32; ++it) {
+            const int idx = tid + it * 256, i = idx & 63, c = (idx >> 6) * 8;
             if (c < Kc)
-                cp_async16(sKB + kbx_off<KK>(64 + i, c), k + ((row0 - 64 + i) * p.H + h) * Kc + c);
+                cp_async16(sKB + qk_off(64 + i, c), k + ((row0 - 64 + i) * p.H + h) * Kc + c);
             else
-                *reinterpret_cast<uint4 *>(sKB + kbx_off<KK>(64 + i, c)) = make_uint4(0, 0, 0, 0);
-        }
-    }
-    // this chunk's g rows into the g2 buffer (the cumsum then runs in place)
-    if constexpr (!PADK) {
-        const float *g_rows = p.g + (row0 * p.HV + hv) * KK;
-        for (int idx = tid; idx < nr * (KK / 4); idx += 256) {
-            const int i = idx / (KK / 4), c4 = idx - i * (KK / 4);
-            cp_async16(sG2 + i * kGS + 4 * c4, g_rows + (size_t)i * p.HV * KK + 4 * c4);
-        }
-    } else {
-        // thread: 16-byte column chunk tid % (dk / 4), rows tid / (dk / 4) + every step
-        constexpr int kQ = KK / 4, kStep = 256 / kQ;
-        const int c4 = tid % kQ;
-        if (4 * c4 < Kc) {
-            const float *src = p.g + (row0 * p.HV + hv) * Kc + 4 * c4;
-            const size_t rstride = (size_t)p.HV * Kc;
-            for (int i = tid / kQ; i < nr; i += kStep)
-                cp_async16(sG2 + i * kGS + 4 * c4, src + i * rstride);
+                *reinterpret_cast<uint4 *>(sKB + qk_off(64 + i, c)) = make_uint4(0, 0, 0, 0);
         }
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
 
-    // ---- 2. Stage 1.  While the copies are in flight, thread 128 + d turns channel
-    // d of the previous chunk into eprev[j] = 2^(G' - g2'_j) and 2^G' in registers.
-    // eprev is held as fp16 pairs scaled by 2^-m, m the channel's largest exponent
-    // rounded up (0 for decaying gates), so it cannot overflow and costs 32
-    // registers.  Once they have landed, thread d < dk forms g2 for channel d in
-    // place in shared memory (rows past the end keep G).
+    // ---- 2. Stage 1.  While the copies are in flight, the previous chunk's gate
+    // rows are prefetched into L2; once its k rows have landed, thread 128 + d
+    // turns channel d of them into kg' = k' 2^(G' - g2'_j) (a reverse running sum)
+    // and records 2^G'.  Thread d < dk then forms g2 for channel d in place in
+    // shared memory (rows past the end keep G).
     const size_t grs = (size_t)p.HV * Kc;
-    __half2 eprev2[32];
-    float escale = 1.f;  // 2^m
     const int dh = tid - 128;
     const bool halo_thread = halo && !carry && tid >= 128 && dh < Kc;
-    if (halo_thread) {
-        const float *gp = p.g + ((row0 - 64) * p.HV + hv) * Kc + dh;
-        float ex[64];  // exponents G' - g2'_j
-#pragma unroll
-        for (int j = 0; j < 64; ++j) ex[j] = __ldg(gp + j * grs);
-        if (gate_act) {
-#pragma unroll
-            for (int j = 0; j < 64; ++j) ex[j] = neg_a * softplus_f(ex[j] + gbias);
-        }
-        float Gp;
-        if (p.g_is_cumsum) {
-            Gp = ex[63];
-#pragma unroll
-            for (int j = 0; j < 64; ++j) ex[j] = Gp - ex[j];
-        } else {
-            float acc = 0.f;
-#pragma unroll
-            for (int j = 63; j >= 0; --j) {
-                const float gj = ex[j];
-                ex[j] = acc;
-                acc = fmaf(p.g_scale, gj, acc);
-            }
-            Gp = acc;
-        }
-        float mx = 0.f;
-#pragma unroll
-        for (int j = 0; j < 64; ++j) mx = fmaxf(mx, ex[j]);
-        const float m = ceilf(mx);
-        escale = exp2f(m);
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-            eprev2[j] = __floats2half2_rn(exp2f(ex[2 * j] - m), exp2f(ex[2 * j + 1] - m));
-        sDprev[dh] = exp2f(Gp);
+    if (__builtin_expect(halo && !carry, 0) && tid >= 128 && (dh & ~31) < Kc) {
+        // the 64 gate rows of this warp's 32 channels into L2 now (two rows per
+        // lane, no registers held), read after the barrier below
+        const float *gp = p.g + ((row0 - 64) * p.HV + hv) * Kc + (dh & ~31);
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(gp + lane * grs));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(gp + (lane + 32) * grs));
     }
     if (tid < 64) sBeta[tid] = bet;
+    // One thread polls each completion; the others wait at the barrier after it.
+    if (tid == 0 && !mbar_wait(&bar_g, ph_in & 1, kWaitNs)) report(p.status, KDA_DEVICE_TIMEOUT);
     asm volatile("cp.async.wait_group 0;" ::: "memory");
     __syncthreads();
+    // the previous chunk's k rows, L2-normalised first when asked (threads 128..191,
+    // one row each)
+    if (__builtin_expect(p.l2norm && halo && !carry, 0)) {
+        if (tid >= 128 && tid < 192) {
+            const int row = tid - 64;  // rows 64..127 of kbx
+            float ss = 0.f;
+            for (int c = 0; c < KK; c += 8) {
+                float f[8];
+                unpack8(*reinterpret_cast<const uint4 *>(sKB + qk_off(row, c)), f);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) ss = fmaf(f[j], f[j], ss);
+            }
+            const float rsn = 1.f / sqrtf(ss + 1e-6f);
+            for (int c = 0; c < KK; c += 8) {
+                uint4 *at = reinterpret_cast<uint4 *>(sKB + qk_off(row, c));
+                float f[8];
+                unpack8(*at, f);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) f[j] *= rsn;
+                *at = pack8(f);
+            }
+        }
+        __syncthreads();
+    }
+    if (__builtin_expect(halo_thread, 0)) {
+        // ... then it becomes its kg (one channel per halo thread), while threads
+        // 0..127 run the cumsum below: row j is scaled by 2^(sum of the gates
+        // after it), G' - g2'_j for per-token gates, G' - g'_j for a cumsum input.
+        float gprev[64];
+        const float *gp = p.g + ((row0 - 64) * p.HV + hv) * Kc + dh;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) gprev[j] = __ldg(gp + j * grs);
+        float acc = 0.f;
+        const float Gc = gate_act ? 0.f : gprev[63];  // G' when g already holds the cumsum
+#pragma unroll
+        for (int j = 63; j >= 0; --j) {
+            __nv_bfloat16 *pk = reinterpret_cast<__nv_bfloat16 *>(sKB + qk_off(64 + j, dh));
+            const float ex = p.g_is_cumsum ? Gc - gprev[j] : acc;
+            *pk = __float2bfloat16_rn(__bfloat162float(*pk) * exp2f(ex));
+            float gj = gprev[j];
+            if (gate_act) gj = neg_a * softplus_f(gj + gbias);
+            acc = fmaf(p.g_scale, gj, acc);
+        }
+        sDprev[dh] = exp2f(p.g_is_cumsum ? Gc : acc);
+    }
     // thread d < dk: channel d's chunk-local cumsum in place (rows past the end keep G)
     if (tid < KK) {
         float acc = 0.f, rng = 0.f;
 #pragma unroll 8
         for (int i = 0; i < 64; ++i) {
+            const int gi = gsw(i, tid);
             if (i < nr && tid < Kc) {  // channels past K keep a zero gate
-                float x = sG2[i * kGS + tid];
+                float x = sG2[gi];
                 if (gate_act) x = neg_a * softplus_f(x + gbias);
                 acc = p.g_is_cumsum ? x : fmaf(p.g_scale, x, acc);
             }
-            sG2[i * kGS + tid] = acc;
+            sG2[gi] = acc;
             rng = fmaxf(rng, fabsf(acc));
         }
         const float eG = exp2f(acc);
@@ -437,31 +591,38 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
     } else if (tid < 128) {
         reinterpret_cast<float *>(U + Lo.dec)[tid] = 0.f;
     }
+    if (tid == 0 && !mbar_wait(&bar_qk, ph_in & 1, kWaitNs)) report(p.status, KDA_DEVICE_TIMEOUT);
+    ++ph_in;
     __syncthreads();
+    // rows past the chunk's end hold another sequence's rows (or NaN): zero them
+    // before anything reads them
+    if (__builtin_expect(nr < 64, 0)) {
+        for (int idx = tid; idx < (64 - nr) * (KK / 8); idx += 256) {
+            const int i = nr + idx / (KK / 8), c = (idx % (KK / 8)) * 8;
+            *reinterpret_cast<uint4 *>(sAG + qk_off(i, c)) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4 *>(sAG + qk_off(64 + i, c)) = make_uint4(0, 0, 0, 0);
+        }
+        __syncthreads();
+    }
 
-    // ---- optional L2 normalisation of q, k and the previous chunk's k rows
-    if (p.l2norm) {
-        const bool own = tid >= 128;
-        const int row = own ? tid - 64 : tid;  // threads 128..191: rows 64..127 of the kb tile
-        if (tid < 128 || (halo && !carry && row < 128)) {
-            auto at = [&](int c) -> uint4 * {
-                return reinterpret_cast<uint4 *>(own ? sKB + kbx_off<KK>(row, c)
-                                                     : sAG + tile_off(row, c, KK));
-            };
+    // ---- optional L2 normalisation of the q and k rows (thread t: row t)
+    if (__builtin_expect(p.l2norm != 0, 0)) {
+        if (tid < 128) {
             float ss = 0.f;
             for (int c = 0; c < KK; c += 8) {
                 float f[8];
-                unpack8(*at(c), f);
+                unpack8(*reinterpret_cast<const uint4 *>(sAG + qk_off(tid, c)), f);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) ss = fmaf(f[j], f[j], ss);
             }
             const float rsn = 1.f / sqrtf(ss + 1e-6f);
             for (int c = 0; c < KK; c += 8) {
+                uint4 *at = reinterpret_cast<uint4 *>(sAG + qk_off(tid, c));
                 float f[8];
-                unpack8(*at(c), f);
+                unpack8(*at, f);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) f[j] *= rsn;
-                *at(c) = pack8(f);
+                *at = pack8(f);
             }
         }
         __syncthreads();
@@ -469,18 +630,18 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
     const bool fast = __int_as_float(sRangeBits) <= kSafeRange;
 
     // ---- exact grams for chunks whose gate range is too wide to split
-    if (!fast) {
+    if (__builtin_expect(!fast, 0)) {
         for (int i = warp; i < 64; i += 8) {
             for (int j = 0; j <= i; ++j) {
                 float aq = 0.f, ak = 0.f;
                 for (int dd = lane; dd < KK; dd += 32) {
-                    const float e = exp2f(sG2[i * kGS + dd] - sG2[j * kGS + dd]);
-                    const float qi = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
-                        sAG + tile_off(i, dd, KK)));
-                    const float ki = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
-                        sAG + tile_off(64 + i, dd, KK)));
+                    const float e = exp2f(sG2[gsw(i, dd)] - sG2[gsw(j, dd)]);
+                    const float qi = __bfloat162float(
+                        *reinterpret_cast<const __nv_bfloat16 *>(sAG + qk_off(i, dd)));
+                    const float ki = __bfloat162float(
+                        *reinterpret_cast<const __nv_bfloat16 *>(sAG + qk_off(64 + i, dd)));
                     const float kj = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
-                        sAG + tile_off(64 + j, dd, KK))) * e;
+                        sAG + qk_off(64 + j, dd))) * e;
                     aq = fmaf(qi, kj, aq);
                     ak = fmaf(ki, kj, ak);
                 }
@@ -492,43 +653,33 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
                 if (lane == 0) {
                     *reinterpret_cast<__nv_bfloat16 *>(U + Lo.aqk + tile_off(i, j, 64)) =
                         __float2bfloat16_rn(p.scale * aq);
-                    sL[fsw<64>(i, j)] = (i > j) ? sBeta[i] * ak : 0.f;
+                    sL[akk_idx<kSplitA>(i, j)] = (i > j) ? sBeta[i] * ak : 0.f;
                 }
             }
             for (int j = i + 1 + lane; j < 64; j += 32) {
                 *reinterpret_cast<__nv_bfloat16 *>(U + Lo.aqk + tile_off(i, j, 64)) =
                     __float2bfloat16_rn(0.f);
-                sL[fsw<64>(i, j)] = 0.f;
+                sL[akk_idx<kSplitA>(i, j)] = 0.f;
             }
         }
         __syncthreads();
     }
 
-    // The previous chunk's k becomes its kg (one channel per halo thread).
-    if (halo_thread) {
-#pragma unroll
-        for (int j = 0; j < 64; ++j) {
-            __nv_bfloat16 *pk = reinterpret_cast<__nv_bfloat16 *>(sKB + kbx_off<KK>(64 + j, dh));
-            const float ej = (j & 1) ? __high2float(eprev2[j >> 1]) : __low2float(eprev2[j >> 1]);
-            *pk = __float2bfloat16_rn(__bfloat162float(*pk) * (ej * escale));
-        }
-    }
-
-    // ---- 3. elementwise, 8 channels of one row per thread; lanes 0..7 cover the
-    // 8 rows of a core matrix so every 16-byte tile access is conflict-free.
-    // qg, kg (in place), kb, scale * qg and kg to the workspace.
+    // ---- 3. elementwise, in place: 8 channels of one row per thread; lanes 0..7
+    // take 8 consecutive rows of one column chunk, which the swizzle spreads over
+    // all banks.  qg, kg, kb, scale * qg and kg to the workspace.
 #pragma unroll
     for (int it = 0; it < KK / 32; ++it) {
         const int idx = tid + it * 256, l = idx & 31, w = idx >> 5;
         const int i = (w & 7) * 8 + (l & 7);
         const int c = ((w >> 3) * 4 + (l >> 3)) * 8;
-        uint4 *pq = reinterpret_cast<uint4 *>(sAG + tile_off(i, c, KK));
-        uint4 *pk = reinterpret_cast<uint4 *>(sAG + tile_off(64 + i, c, KK));
+        uint4 *pq = reinterpret_cast<uint4 *>(sAG + qk_off(i, c));
+        uint4 *pk = reinterpret_cast<uint4 *>(sAG + qk_off(64 + i, c));
         float fq[8], fk[8], gam[8];
         unpack8(*pq, fq);
         unpack8(*pk, fk);
-        *reinterpret_cast<float4 *>(gam) = *reinterpret_cast<const float4 *>(sG2 + i * kGS + c);
-        *reinterpret_cast<float4 *>(gam + 4) = *reinterpret_cast<const float4 *>(sG2 + i * kGS + c + 4);
+        *reinterpret_cast<float4 *>(gam) = *reinterpret_cast<const float4 *>(sG2 + gsw(i, c));
+        *reinterpret_cast<float4 *>(gam + 4) = *reinterpret_cast<const float4 *>(sG2 + gsw(i, c + 4));
         float qg[8], kgm[8], kb[8], kgv[8], qs[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
@@ -545,23 +696,29 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
         }
         *pq = pack8(qg);
         *pk = pack8(kgm);
-        if (fast) *reinterpret_cast<uint4 *>(sKB + kbx_off<KK>(i, c)) = pack8(kb);
+        if (fast) *reinterpret_cast<uint4 *>(sKB + qk_off(i, c)) = pack8(kb);
         *reinterpret_cast<uint4 *>(U + Lo.aw + tile_off(64 + i, c, KK)) = pack8(qs);
         *reinterpret_cast<uint4 *>(U + Lo.kgt + tile_off(i, c, KK)) = pack8(kgv);
     }
     __syncthreads();
-    // v into the freed g2 buffer; waited for just before the u MMA
-    for (int idx = tid; idx < 64 * VG8; idx += 256) {
-        const int l = idx & 31, w = idx >> 5;
-        const int i = (w & 7) * 8 + (l & 7);
-        const int c = ((w >> 3) * 4 + (l >> 3)) * 8;
-        void *dv = sV + tile_off(i, c, VV);
-        if (i < nr)
-            cp_async16(dv, v + ((row0 + i) * p.HV + hv) * VV + c);
-        else
-            *reinterpret_cast<uint4 *>(dv) = make_uint4(0, 0, 0, 0);
+    {
+        // v into the freed g2 buffer (its second half with the pref plan);
+        // waited for just before the u MMA
+        for (int idx = tid; idx < 64 * VG8; idx += 256) {
+            const int l = idx & 31, w = idx >> 5;
+            const int i = (w & 7) * 8 + (l & 7);
+            const int c = ((w >> 3) * 4 + (l >> 3)) * 8;
+            void *dv = sV + tile_off(i, c, VV) + (i >= 32 ? v_half : 0);
+            if (i < nr)
+                cp_async16(dv, v + ((row0 + i) * p.HV + hv) * VV + c);
+            else
+                *reinterpret_cast<uint4 *>(dv) = make_uint4(0, 0, 0, 0);
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        // with the pref plan the first half of g2 is free for good: the next
+        // unit's g channels 0..63
+        if (pref && tid == 0 && nxt->unit < uend) issue(nxt, true, false, false, false);
     }
-    asm volatile("cp.async.commit_group;" ::: "memory");
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -569,24 +726,24 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
 
     // ---- 4. grams on the tensor cores.  D[:, 0:64] = [Qg; Kg] Kb^T (split grams),
     // D[:, 64:128] = [Qg; Kg] kgp^T (cross-chunk gram with the previous chunk);
-    // Kb and kgp are rows 0..63 and 64..127 of one tile, so both take one MMA
-    // series of N = 128.
+    // Kb and kgp are rows 0..63 and 64..127 of kbx, so both take one MMA series
+    // of N = 128.  Both operands K-major, 128-byte swizzled: a K step of 16
+    // channels moves 32 bytes inside a column block, every fourth step a block.
     if (tid == 0) {
-        const uint64_t a = sdesc(smem_addr(sAG), 128, KK * 16);
-        const uint64_t bkb = sdesc(smem_addr(sKB), S::kLbo, S::kSbo);
-        constexpr uint32_t binc = 2 * S::kLbo / 16;
-        if (fast && halo)
-            mma_bf16_seq<KK / 16, false>(tmem, a, 16, bkb, binc, idesc_bf16(128, 128, false, false));
-        else if (fast)
-            mma_bf16_seq<KK / 16, false>(tmem, a, 16, bkb, binc, idesc_bf16(128, 64, false, false));
-        else if (halo)
-            mma_bf16_seq<KK / 16, false>(tmem + 64, a, 16,
-                                         sdesc(smem_addr(sKB) + 8 * S::kSbo, S::kLbo, S::kSbo),
-                                         binc, idesc_bf16(128, 64, false, false));
+        const uint32_t a0 = smem_addr(sAG), b0 = smem_addr(sKB) + ((fast || !halo) ? 0 : 8192);
+        const uint32_t idn = idesc_bf16(128, (fast && halo) ? 128 : 64, false, false);
+        if (fast || halo) {
+#pragma unroll
+            for (int kk = 0; kk < KK / 16; ++kk) {
+                const uint32_t ko = (kk >> 2) * S::kBlk + (kk & 3) * 32;
+                mma_bf16(tmem + (fast ? 0 : 64), sdesc_sw128(a0 + ko, 16, 1024),
+                         sdesc_sw128(b0 + ko, 16, 1024), idn, kk > 0);
+            }
+        }
         mma_commit(&bar);
     }
-    __syncwarp();
-    if (!mbar_wait(&bar, phase & 1, kWaitNs) && tid == 0) report(p.status, KDA_DEVICE_TIMEOUT);
+    if (tid == 0 && !mbar_wait(&bar, phase & 1, kWaitNs)) report(p.status, KDA_DEVICE_TIMEOUT);
+    __syncthreads();
     ++phase;
     tc_fence_after();
     {
@@ -606,7 +763,7 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
                 const float bi = sBeta[i];
 #pragma unroll
                 for (int c0 = 0; c0 < 64; c0 += 4)
-                    st4<64>(sL, i, c0,
+                    sta4<kSplitA>(sL, i, c0,
                             make_float4(c0 < i ? bi * dd[c0] : 0.f, c0 + 1 < i ? bi * dd[c0 + 1] : 0.f,
                                         c0 + 2 < i ? bi * dd[c0 + 2] : 0.f,
                                         c0 + 3 < i ? bi * dd[c0 + 3] : 0.f));
@@ -639,7 +796,7 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
             float s0 = 0.f, s1 = 0.f;
 #pragma unroll
             for (int m4 = 0; m4 < r; m4 += 4) {
-                const float4 l4 = ld4<64>(sL, o + r, o + m4);
+                const float4 l4 = lda4<kSplitA>(sL, o + r, o + m4);
                 s0 = fmaf(l4.x, x[m4], s0);
                 if (m4 + 1 < r) s1 = fmaf(l4.y, x[m4 + 1], s1);
                 if (m4 + 2 < r) s0 = fmaf(l4.z, x[m4 + 2], s0);
@@ -648,29 +805,29 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
             if (r > c) x[r] = -(s0 + s1);
         }
 #pragma unroll
-        for (int r = 0; r < 16; ++r) sA[fsw<64>(o + r, o + c)] = x[r];
+        for (int r = 0; r < 16; ++r) sA[akk_idx<kSplitA>(o + r, o + c)] = x[r];
     }
     __syncthreads();
     const int sr = (lane & 7) + 8 * ((tid >> 5) & 1), sc = 4 * (lane >> 3), blk = tid >> 6;
     if (tid < 128) {  // T = L_{I,I-1} X_{I-1} for I = 1, 3  -> sT block (blk, blk)
         const int I = 2 * blk + 1;
         float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-        strip16<64>(s, sL, 16 * I + sr, 16 * (I - 1), sA, 16 * (I - 1), 16 * (I - 1) + sc);
+        strip_la<kSplitA>(s, sL, 16 * I + sr, 16 * (I - 1), sA, 16 * (I - 1), 16 * (I - 1) + sc);
         st4<32>(sT, 16 * blk + sr, 16 * blk + sc, s);
     }
     __syncthreads();
     if (tid < 128) {  // A_{I,I-1} = -X_I T
         const int I = 2 * blk + 1;
         float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-        strip16<32>(s, sA, 16 * I + sr, 16 * I, sT, 16 * blk, 16 * blk + sc);
-        st4<64>(sA, 16 * I + sr, 16 * (I - 1) + sc, neg4(s));
+        strip_at<kSplitA>(s, sA, 16 * I + sr, 16 * I, sT, 16 * blk, 16 * blk + sc);
+        sta4<kSplitA>(sA, 16 * I + sr, 16 * (I - 1) + sc, neg4(s));
     }
     __syncthreads();
     {  // T_IJ = sum_M L_IM Y0_MJ for I = 2, 3 and J = 0, 1  -> sT (I - 2, J)
         const int I = 2 + (blk >> 1), J = blk & 1;
         float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int M = J; M < 2; ++M)
-            strip16<64>(s, sL, 16 * I + sr, 16 * M, sA, 16 * M, 16 * J + sc);
+            strip_la<kSplitA>(s, sL, 16 * I + sr, 16 * M, sA, 16 * M, 16 * J + sc);
         st4<32>(sT, 16 * (I - 2) + sr, 16 * J + sc, s);
     }
     __syncthreads();
@@ -678,63 +835,62 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
         const int I = 2 + (blk >> 1), J = blk & 1;
         float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int M = 2; M <= I; ++M)
-            strip16<32>(s, sA, 16 * I + sr, 16 * M, sT, 16 * (M - 2), 16 * J + sc);
-        st4<64>(sA, 16 * I + sr, 16 * J + sc, neg4(s));
+            strip_at<kSplitA>(s, sA, 16 * I + sr, 16 * M, sT, 16 * (M - 2), 16 * J + sc);
+        sta4<kSplitA>(sA, 16 * I + sr, 16 * J + sc, neg4(s));
     }
     __syncthreads();
-    // Akk diag(beta) as a bf16 operand tile (Akk is lower triangular)
+    // Akk diag(beta) as a bf16 operand tile (Akk is lower triangular).  With the
+    // pref plan it overwrites Akk's second half: every read before any write.
+    {
+        uint4 ab[2];
 #pragma unroll
-    for (int it = 0; it < 2; ++it) {
-        const int idx = tid + it * 256, l = idx & 31, w = idx >> 5;
-        const int i = (w & 7) * 8 + (l & 7);
-        const int c = ((w >> 3) * 4 + (l >> 3)) * 8;
-        const float4 a0 = ld4<64>(sA, i, c), a1 = ld4<64>(sA, i, c + 4);
-        const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-        float f[8];
+        for (int it = 0; it < 2; ++it) {
+            const int idx = tid + it * 256, l = idx & 31, w = idx >> 5;
+            const int i = (w & 7) * 8 + (l & 7);
+            const int c = ((w >> 3) * 4 + (l >> 3)) * 8;
+            const float4 a0 = lda4<kSplitA>(sA, i, c), a1 = lda4<kSplitA>(sA, i, c + 4);
+            const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            float f[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) f[j] = (c + j <= i) ? av[j] * sBeta[c + j] : 0.f;
-        *reinterpret_cast<uint4 *>(sAB + tile_off(i, c, 64)) = pack8(f);
+            for (int j = 0; j < 8; ++j) f[j] = (c + j <= i) ? av[j] * sBeta[c + j] : 0.f;
+            ab[it] = pack8(f);
+        }
+        if (pref) __syncthreads();
+#pragma unroll
+        for (int it = 0; it < 2; ++it) {
+            const int idx = tid + it * 256, l = idx & 31, w = idx >> 5;
+            const int i = (w & 7) * 8 + (l & 7);
+            const int c = ((w >> 3) * 4 + (l >> 3)) * 8;
+            *reinterpret_cast<uint4 *>(sAB + tile_off(i, c, 64)) = ab[it];
+        }
     }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
 
-    // ---- 6. W = Akk diag(beta) Kg and M = Akk diag(beta) P (valid rows: lanes 64..127)
+    // ---- 6. W = Akk diag(beta) Kg and M = Akk diag(beta) P (valid rows: lanes 64..127).
+    // Kg is an MN-major 128-byte swizzled operand here: a K step (16 rows) moves
+    // two 8-row groups (2 KB); its 64-column blocks lie 16 KB apart.
     const uint64_t adesc = sdesc(smem_addr(sAB) - 8 * 1024, 128, 1024);  // rows 64..127 = Akk diag(beta)
     if (tid == 0) {
-        mma_bf16_seq<4, false>(tmem, adesc, 16, sdesc(smem_addr(sAG) + 64 * KK * 2, KK * 16, 128),
-                               2 * KK * 16 / 16, idesc_bf16(128, KK, false, true));
+        const uint32_t kg0 = smem_addr(sAG) + 8192;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            mma_bf16(tmem, adesc + (uint64_t)(kk * 16), sdesc_sw128(kg0 + kk * 2048, S::kBlk, 1024),
+                     idesc_bf16(128, KK, false, true), kk > 0);
         if (halo)
             mma_bf16_seq<4, false>(tmem + KK, adesc, 16, sdesc(smem_addr(sPB), 64 * 16, 128),
                                    2 * 64 * 16 / 16, idesc_bf16(128, 64, false, true));
         mma_commit(&bar);
     }
-    __syncwarp();
-    if (!mbar_wait(&bar, phase & 1, kWaitNs) && tid == 0) report(p.status, KDA_DEVICE_TIMEOUT);
+    if (tid == 0 && !mbar_wait(&bar, phase & 1, kWaitNs)) report(p.status, KDA_DEVICE_TIMEOUT);
+    __syncthreads();
     ++phase;
     tc_fence_after();
-    // The kb / previous-kg tile is free now (P was read by the M MMA): if the next
-    // unit is the next chunk of this sequence, bring this chunk's kg into the
-    // previous-kg rows for it.
-    bool next_carry = false;
-    if (unit + 1 < uend) {
-        int hvn, bn, r0n, nrn, cln, nsn, ncn;
-        int64_t gcn;
-        prep_unit(p, unit + 1, hvn, gcn);
-        next_carry = hvn == hv && gcn == gc + 1 &&
-                     locate_chunk(p, gcn, bn, r0n, nrn, cln, &nsn, &ncn) && continues(p, cln, ncn);
-    }
-    if (next_carry) {
-#pragma unroll
-        for (int it = 0; it < KK / 32; ++it) {
-            const int idx = tid + it * 256, l = idx & 31, w = idx >> 5;
-            const int i = (w & 7) * 8 + (l & 7);
-            const int c = ((w >> 3) * 4 + (l >> 3)) * 8;
-            cp_async16(sKB + kbx_off<KK>(64 + i, c), U + Lo.kgt + tile_off(i, c, KK));
-        }
-        asm volatile("cp.async.commit_group;" ::: "memory");
-    }
+    // The k rows of ag were the W MMA's last use of them: with the pref plan, the
+    // next unit's k rows go there now.
+    if (pref && tid == 0 && nxt->unit < uend) issue(nxt, false, false, false, true);
     if (warp == 2 || warp == 3 || warp == 6 || warp == 7) {
         // W~ = W Diag(2^G_prev) -> rows 0..63 of the [W; qg] tile, and M; warps
         // 2, 3 and 6, 7 reach the same TMEM lanes and take half the columns each.
@@ -770,14 +926,32 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
 
     // ---- 7. u = Akk diag(beta) v
     if (tid == 0) {
-        mma_bf16_seq<4, false>(tmem, adesc, 16, sdesc(smem_addr(sV), VV * 16, 128),
-                               2 * VV * 16 / 16, idesc_bf16(128, VV, false, true));
+        // K step kk: v rows 16 kk .. 16 kk + 15 (the second half v_half further on)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            mma_bf16(tmem, adesc + (uint64_t)(kk * 16),
+                     sdesc(smem_addr(sV) + kk * 2 * VV * 16 + (kk >= 2 ? v_half : 0), VV * 16, 128),
+                     idesc_bf16(128, VV, false, true), kk > 0);
         mma_commit(&bar);
     }
-    __syncwarp();
-    if (!mbar_wait(&bar, phase & 1, kWaitNs) && tid == 0) report(p.status, KDA_DEVICE_TIMEOUT);
+    if (tid == 0 && !mbar_wait(&bar, phase & 1, kWaitNs)) report(p.status, KDA_DEVICE_TIMEOUT);
+    __syncthreads();
     ++phase;
     tc_fence_after();
+    // Every operand of this unit has been read: the next unit's remaining copies,
+    // and, if it is the next chunk of this sequence, this chunk's kg as its
+    // previous-kg rows (waited for at the start of that unit).
+    if (nxt->unit < uend) {
+        if (tid == 0) issue(nxt, !pref, true, true, !pref);
+        if (nxt->hv == hv && nxt->gc == gc + 1 && continues(p, nxt->cl, nxt->ncs)) {
+#pragma unroll
+            for (int it = 0; it < KK / 32; ++it) {
+                const int idx = tid + it * 256, i = idx & 63, c = (idx >> 6) * 8;
+                cp_async16(sKB + qk_off(64 + i, c), U + Lo.kgt + tile_off(i, c, KK));
+            }
+            asm volatile("cp.async.commit_group;" ::: "memory");
+        }
+    }
     if (warp == 2 || warp == 3 || warp == 6 || warp == 7) {
         const int quad = warp & 3, i = (tid & 127) - 64;
         const int cbeg = warp < 4 ? 0 : VV / 2;
@@ -795,7 +969,17 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(ChunkArgs p) {
     tc_fence_after();
     prev_hv = hv;
     prev_gc = gc;
+    slot ^= 1;
     }  // unit loop
+    // Every copy was waited for, but a wait that gave up may have left its copy
+    // in flight: wait for the last ones once more (bounded; immediate when they
+    // landed) before the shared memory they write is released.
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    if (tid == 0 && ph_in > 0) {
+        mbar_wait(&bar_g, (ph_in - 1) & 1, kWaitNs);
+        mbar_wait(&bar_qk, (ph_in - 1) & 1, kWaitNs);
+    }
+    __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, kCols);
 }
 
@@ -1443,6 +1627,51 @@ __global__ void __launch_bounds__(256) chunk_fix_tc_kernel(ChunkArgs p) {
     if (warp == 0) tmem_dealloc(tmem, S::tmem_cols);
 }
 
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against the driver library); null when the driver does not provide it.
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled() {
+    static const EncodeTiledFn fn = [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return static_cast<EncodeTiledFn>(nullptr);
+        return reinterpret_cast<EncodeTiledFn>(f);
+    }();
+    return fn;
+}
+
+// A [rows][mid][inner] row-major tensor as a 3-D map with boxes of
+// [64 rows][1][box_inner], 128-byte swizzle, zero fill out of bounds.
+cudaError_t encode3(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int elem,
+                    uint64_t inner, uint64_t mid, uint64_t rows, uint32_t box_inner) {
+    const EncodeTiledFn fn = encode_tiled();
+    if (!fn) return cudaErrorNotSupported;
+    const cuuint64_t dims[3] = {inner, mid, rows};
+    const cuuint64_t strides[2] = {inner * elem, mid * inner * elem};
+    const cuuint32_t box[3] = {box_inner, 1, 64};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = fn(m, dt, 3, const_cast<void *>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t prep_maps(const ChunkArgs &a, PrepMaps *m) {
+    const uint64_t rows = (uint64_t)a.B * a.T;
+    cudaError_t e = encode3(&m->q, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.K, a.H, rows, 64);
+    if (e == cudaSuccess)
+        e = encode3(&m->k, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.K, a.H, rows, 64);
+    if (e == cudaSuccess)
+        e = encode3(&m->g, a.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.K, a.HV, rows, 32);
+    return e;
+}
+
 template <int KK, bool ACT, bool PADK>
 cudaError_t launch_prep_t(const ChunkArgs &a, cudaStream_t st, int64_t cta_cap) {
     using S = PrepSmem<KK>;
@@ -1490,8 +1719,10 @@ cudaError_t launch_prep_t(const ChunkArgs &a, cudaStream_t st, int64_t cta_cap) 
     const int64_t units = prep_units(a);
     if (units == 0) return cudaSuccess;
     const unsigned grid = (unsigned)(units < ctas ? units : ctas);
+    PrepMaps maps;
+    if ((e = prep_maps(a, &maps)) != cudaSuccess) return e;
     prof_begin("chunk_prep_tc", st);
-    chunk_prep_tc_kernel<KK, ACT, PADK><<<grid, 256, smem, st>>>(a);
+    chunk_prep_tc_kernel<KK, ACT, PADK><<<grid, 256, smem, st>>>(a, maps);
     prof_end(st);
     return cudaGetLastError();
 }

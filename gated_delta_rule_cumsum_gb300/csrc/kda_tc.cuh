@@ -206,6 +206,28 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
            ((uint64_t)((sbo & 0x3FFFFu) >> 4) << 32) | (1ull << 46);
 }
 
+// Shared-memory descriptor of a 128-byte swizzled operand (descriptor version 1,
+// layout type 2).  The tile is made of 1024-byte atoms of 8 rows x 128 bytes,
+// each 16-byte chunk j of row r stored at chunk position j ^ (r % 8) -- the
+// pattern a TMA copy with 128-byte swizzle writes -- with atoms 1024-byte
+// aligned.
+//   K-major:  rows = M or N, 64 bf16 of K per atom row; sbo = the stride between
+//             8-row groups (1024 for packed rows); lbo unused.  Consecutive
+//             K = 16 steps inside an atom advance the start address by 32 bytes.
+//   MN-major: rows = K, 64 bf16 of M or N per atom row; lbo = the stride between
+//             atoms along M / N, sbo = the stride between 8-row groups of K.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo & 0x3FFFFu) >> 4) << 16) |
+           ((uint64_t)((sbo & 0x3FFFFu) >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Byte offset of element (r, c) in a 128-byte swizzled tile whose 64-column
+// blocks lie `block` bytes apart (rows 128 bytes apart inside a block).
+__host__ __device__ constexpr uint32_t sw128_off(int r, int c, uint32_t block) {
+    return (uint32_t)((c >> 6) * block + r * 128 + ((((c >> 3) & 7) ^ (r & 7)) << 4) +
+                      (c & 7) * 2);
+}
+
 // Instruction descriptor of kind::f16 with bf16 A and B and an fp32 accumulator.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
     return (1u << 4)                       // D format: f32

@@ -134,6 +134,10 @@ typedef enum {
 /* Bits of the device status word. */
 #define KDA_DEVICE_BAD_CU_SEQLENS (1 << 0)
 #define KDA_DEVICE_TIMEOUT        (1 << 1)
+#define KDA_DEVICE_INTERNAL       (1 << 2)  /* a launch found an internal invariant broken
+                                               (e.g. the alignment of its shared memory)
+                                               and skipped its work; reported as
+                                               KDA_ERR_CUDA                            */
 
 typedef struct {
     int32_t B, T, H, HV, K, V;  /* see Layouts; HV % H == 0                         */

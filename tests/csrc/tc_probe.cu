@@ -8,17 +8,26 @@
 
 using namespace kda::tc;
 
-// D[128][N] = A[128][Kd] * B[Kd][N]; mode bit 0: B MN-major, bit 1: A MN-major.
+// D[128][N] = A[128][Kd] * B[Kd][N]; mode bit 0: B MN-major, bit 1: A MN-major,
+// bit 2: the K-major operands in the 128-byte swizzled layout (64-column blocks
+// of rows x 128 bytes), bit 3: an MN-major B in the 128-byte swizzled layout
+// (64-column blocks of Kd x 128 bytes).
 __global__ void __launch_bounds__(128) tc_probe_kernel(const __nv_bfloat16 *A,
                                                        const __nv_bfloat16 *B, float *D, int N,
                                                        int Kd, int mode, int *err) {
+    // no static shared memory: the dynamic region starts 1024-byte aligned, as the
+    // swizzled layouts need (checked below)
     extern __shared__ __align__(1024) unsigned char sm[];
     unsigned char *sA = sm;
     unsigned char *sB = sm + 128 * Kd * 2;
-    __shared__ uint64_t bar;
-    __shared__ uint32_t slot;
+    uint64_t &bar = *reinterpret_cast<uint64_t *>(sm + 190 * 1024);
+    uint32_t &slot = *reinterpret_cast<uint32_t *>(sm + 190 * 1024 + 8);
+    if (smem_addr(sm) & 1023u) {
+        if (threadIdx.x == 0) atomicExch(err, 2);
+        return;
+    }
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const bool a_mn = mode & 2, b_mn = mode & 1;
+    const bool a_mn = mode & 2, b_mn = mode & 1, swk = mode & 4, swmn = mode & 8;
     if (warp == 0) {
         tmem_alloc(&slot, 256);
         tmem_relinquish();
@@ -29,12 +38,14 @@ __global__ void __launch_bounds__(128) tc_probe_kernel(const __nv_bfloat16 *A,
     }
     for (int idx = tid; idx < 128 * Kd; idx += 128) {
         const int m = idx / Kd, k = idx % Kd;
-        const uint32_t off = a_mn ? tile_off(k, m, 128) : tile_off(m, k, Kd);
+        const uint32_t off = a_mn ? tile_off(k, m, 128)
+                                  : (swk ? sw128_off(m, k, 128 * 128) : tile_off(m, k, Kd));
         *reinterpret_cast<__nv_bfloat16 *>(sA + off) = A[idx];
     }
     for (int idx = tid; idx < Kd * N; idx += 128) {
         const int k = idx / N, n = idx % N;
-        const uint32_t off = b_mn ? tile_off(k, n, N) : tile_off(n, k, Kd);
+        const uint32_t off = b_mn ? (swmn ? sw128_off(k, n, Kd * 128) : tile_off(k, n, N))
+                                  : (swk ? sw128_off(n, k, N * 128) : tile_off(n, k, Kd));
         *reinterpret_cast<__nv_bfloat16 *>(sB + off) = B[idx];
     }
     fence_async_smem();
@@ -43,10 +54,33 @@ __global__ void __launch_bounds__(128) tc_probe_kernel(const __nv_bfloat16 *A,
     tc_fence_after();
     const uint32_t tmem = slot;
     if (tid == 0) {
-        const uint32_t a_lbo = a_mn ? 128 * 16 : 128, a_sbo = a_mn ? 128 : Kd * 16;
-        const uint32_t b_lbo = b_mn ? N * 16 : 128, b_sbo = b_mn ? 128 : Kd * 16;
-        mma_bf16_k(tmem, smem_addr(sA), a_lbo, a_sbo, smem_addr(sB), b_lbo, b_sbo,
-                   idesc_bf16(128, N, a_mn, b_mn), Kd / 16, 0);
+        const uint32_t idesc = idesc_bf16(128, N, a_mn, b_mn);
+        if (swk || swmn) {
+            // K step kk: K-major swizzled operands move 32 bytes inside an atom row
+            // and a whole 64-column block every 4 steps; an MN-major swizzled B
+            // moves 16 rows (two 8-row groups)
+            for (int kk = 0; kk < Kd / 16; ++kk) {
+                const uint32_t ksw = (kk & 3) * 32;
+                const uint64_t a =
+                    (swk && !a_mn) ? sdesc_sw128(smem_addr(sA) + (kk >> 2) * 128 * 128 + ksw, 16, 1024)
+                                   : sdesc(smem_addr(sA) + kk * 2 * (a_mn ? 128 * 16 : 128),
+                                           a_mn ? 128 * 16 : 128, a_mn ? 128 : Kd * 16);
+                uint64_t b;
+                if (b_mn && swmn)
+                    b = sdesc_sw128(smem_addr(sB) + kk * 2048, Kd * 128, 1024);
+                else if (!b_mn && swk)
+                    b = sdesc_sw128(smem_addr(sB) + (kk >> 2) * N * 128 + ksw, 16, 1024);
+                else
+                    b = sdesc(smem_addr(sB) + kk * 2 * (b_mn ? N * 16 : 128), b_mn ? N * 16 : 128,
+                              b_mn ? 128 : Kd * 16);
+                mma_bf16(tmem, a, b, idesc, kk > 0);
+            }
+        } else {
+            const uint32_t a_lbo = a_mn ? 128 * 16 : 128, a_sbo = a_mn ? 128 : Kd * 16;
+            const uint32_t b_lbo = b_mn ? N * 16 : 128, b_sbo = b_mn ? 128 : Kd * 16;
+            mma_bf16_k(tmem, smem_addr(sA), a_lbo, a_sbo, smem_addr(sB), b_lbo, b_sbo, idesc,
+                       Kd / 16, 0);
+        }
         mma_commit(&bar);
     }
     if (!mbar_wait(&bar, 0) && tid == 0) atomicExch(err, 1);
@@ -69,6 +103,7 @@ extern "C" int tc_probe(const void *A, const void *B, float *D, int N, int Kd, i
     // Room for the tiles read with either descriptor interpretation.
     const int smem = 200 * 1024;
     cudaFuncSetAttribute(tc_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if ((mode & 8) && N % 64) return -1;  // swizzled MN-major B: whole 64-column blocks
     tc_probe_kernel<<<1, 128, smem, st>>>(static_cast<const __nv_bfloat16 *>(A),
                                           static_cast<const __nv_bfloat16 *>(B), D, N, Kd, mode,
                                           err);

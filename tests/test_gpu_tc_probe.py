@@ -44,3 +44,12 @@ def test_single_tile_gemm(probe, mode, N, Kd):
     assert rc == 0 and int(err) == 0
     want = A.float() @ B.float()
     assert torch.allclose(D, want, rtol=1e-4, atol=1e-3), (D - want).abs().max()
+
+
+# The 128-byte swizzled layouts a TMA copy writes: K-major A and B (the prep's
+# gram operands), and a no-swizzle A with an MN-major swizzled B (its W product).
+@pytest.mark.parametrize("mode", [4, 8 | 1, 8 | 4 | 1], ids=["Aksw_Bksw", "Ak_Bmnsw", "Aksw_Bmnsw"])
+@pytest.mark.parametrize("N,Kd", [(64, 64), (128, 128), (64, 128), (128, 64)])
+def test_single_tile_gemm_swizzled(probe, mode, N, Kd):
+    test_single_tile_gemm(probe, mode, N, Kd)
+
