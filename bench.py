@@ -9,7 +9,7 @@ HBM before the timed region; a 512 MiB buffer is written between timed steps
 to flush the 129 MB L2.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload train|gva|packed|decode|prefill|prefill_small|train_bwd]
+                  [--workload train|gva|packed|decode|decode_small|prefill|prefill_small|train_bwd]
 
 `--workload` picks one of the other synthetic workloads instead (grouped value
 heads B4 T4096 HV32; packed varlen H=HV=32; decode 4096 x 1 token; its
@@ -50,11 +50,13 @@ WORKLOADS = {
     "prefill": (4, {"T": 256}, 10, 3),
     # the prefill variant on 256 of the 4096 sequences: the size an ncu capture takes
     "prefill_small": (4, {"T": 256, "B": 256, "decode_seqs": 256}, 20, 3),
+    # decode on 512 of the 4096 sequences (1 GiB of state): the size an ncu capture takes
+    "decode_small": (4, {"B": 512, "decode_seqs": 512}, 100, 5),
     # gradients of the training shape's recurrence (kda_recurrent_bwd)
     "train_bwd": (1, {}, 10, 3),
 }
 BWD_FLOPS_PER_ELEMENT = 26   # one forward pass (7) + the reverse sweep (19) per state element
-RECURRENT = ("decode", "prefill", "prefill_small")
+RECURRENT = ("decode", "decode_small", "prefill", "prefill_small")
 FP32_LANES_PER_SM = 128      # fp32 FMA lanes per SM (4 partitions x 32)
 E2E_MAX_H2D = 8 << 30        # larger inputs are not staged through pinned host memory
 
@@ -234,7 +236,8 @@ def _traffic(kernel, workload="train"):
     if not os.path.exists(path):
         return None
     with open(path) as f:
-        rec = json.load(f).get(kernel)
+        table = json.load(f)
+    rec = table.get(f"{kernel}@{workload}") or table.get(kernel)
     if not rec or rec.get("bench_workload", "train") != workload:
         return None
     src = os.path.join(ROOT, rec["source"])
@@ -506,28 +509,31 @@ def run_ours(args):
     traffic = _traffic(dom, args.workload)
     r_b, w_b = algorithmic_bytes(inp)
     path_gbs = (r_b + w_b) / (ms / 1e3) / 1e9
+    if backward or args.workload.startswith("prefill"):
+        # the fp32-bound kernels' denominator, measured here by an FMA-loop kernel
+        peak = kda.kda_measure_fp32_fma_peak(stream)
+        peak_source = ("measured in this run: FMA-loop microbenchmark "
+                       "(kda_measure_fp32_fma_peak, 16 chains x 8x256 threads per SM)")
     if backward:
-        sms = torch.cuda.get_device_properties(dev).multi_processor_count
-        peak = fp32_fma_tflops(sms, peaks["sm_max_mhz"])
         flops = BWD_FLOPS_PER_ELEMENT * inp["tokens"] * w.HV * w.K * w.V
         step_ms = sum(t for t, _ in per_kernel.values()) / prof_steps
         roofline = {"bound": "alu", "kernel": "recurrent_ckpt+recurrent_bwd",
                     "achieved": flops / (step_ms / 1e3) / 1e12, "peak": peak, "unit": "TFLOP/s",
                     "frac": flops / (step_ms / 1e3) / 1e12 / peak, "traffic": None,
                     "algorithmic_flops": flops, "kernel_ms": step_ms,
-                    "peak_source": f"derived: {sms} SMs x {FP32_LANES_PER_SM} fp32 lanes x 2 "
-                                   f"x {peaks['sm_max_mhz']:.0f} MHz"}
+                    "peak_source": peak_source,
+                    "nominal_peak": fp32_fma_tflops(torch.cuda.get_device_properties(dev)
+                                                    .multi_processor_count, peaks["sm_max_mhz"])}
     elif args.workload.startswith("prefill"):
         # 256 tokens per state: the recurrence's fp32 FMAs, not HBM, bound it.
-        sms = torch.cuda.get_device_properties(dev).multi_processor_count
-        peak = fp32_fma_tflops(sms, peaks["sm_max_mhz"])
         flops = recurrent_flops(inp)
         roofline = {"bound": "alu", "kernel": dom, "achieved": flops / (dom_ms / 1e3) / 1e12,
                     "peak": peak, "unit": "TFLOP/s",
                     "frac": flops / (dom_ms / 1e3) / 1e12 / peak, "traffic": traffic,
                     "algorithmic_flops": flops, "kernel_ms": dom_ms,
-                    "peak_source": f"derived: {sms} SMs x {FP32_LANES_PER_SM} fp32 lanes x 2 "
-                                   f"x {peaks['sm_max_mhz']:.0f} MHz"}
+                    "peak_source": peak_source,
+                    "nominal_peak": fp32_fma_tflops(torch.cuda.get_device_properties(dev)
+                                                    .multi_processor_count, peaks["sm_max_mhz"])}
     else:
         achieved = dom_bytes / (dom_ms / 1e3) / 1e9
         roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved,

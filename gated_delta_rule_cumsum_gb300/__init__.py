@@ -35,7 +35,7 @@ __all__ = [
     "kda_chunk_fwd_noalloc", "KDA_NOALLOC_SCRATCH_BYTES",
     "kda_read_device_status", "kda_clear_device_status", "kda_status_string",
     "kda_last_error_message", "kda_version", "kda_profile_enable", "kda_profile_report",
-    "kda_profile_reset",
+    "kda_profile_reset", "kda_measure_fp32_fma_peak",
     "chunk_kda", "recurrent_kda", "gate_cumsum",
 ]
 
@@ -126,6 +126,7 @@ _SIGNATURES = {
     "kda_profile_report": (ctypes.c_int, [ctypes.c_char_p, _SZ, ctypes.POINTER(ctypes.c_double),
                                           ctypes.POINTER(ctypes.c_int64), ctypes.c_int]),
     "kda_profile_reset": (None, []),
+    "kda_measure_fp32_fma_peak": (_ST, [ctypes.POINTER(ctypes.c_double), _VP]),
 }
 
 
@@ -298,6 +299,13 @@ def kda_profile_enable(enable: bool = True):
 
 def kda_profile_reset():
     load().kda_profile_reset()
+
+
+def kda_measure_fp32_fma_peak(stream=None) -> float:
+    """The device's fp32 FMA peak in TFLOP/s, measured by an FMA-loop kernel."""
+    out = ctypes.c_double(0.0)
+    _check(load().kda_measure_fp32_fma_peak(ctypes.byref(out), _stream(stream)))
+    return float(out.value)
 
 
 def kda_profile_report(max_entries: int = 32) -> dict:

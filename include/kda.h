@@ -372,6 +372,15 @@ int kda_profile_report(char *names, size_t names_len, double *total_ms, int64_t 
                        int max_entries);
 void kda_profile_reset(void);
 
+/*
+ * Peak fp32 FMA throughput of the current device, measured: a kernel of 16
+ * independent FMA chains per thread on 8 x 256 threads per SM, timed with CUDA
+ * events on `stream` (best of three after a warm-up launch), in TFLOP/s (two
+ * flops per FMA).  The roofline denominator for the fp32-bound kernels (the
+ * recurrent prefill and backward).  Synchronises the stream.
+ */
+kda_status kda_measure_fp32_fma_peak(double *tflops, kda_stream_t stream);
+
 /* Static text for a status code. */
 const char *kda_status_string(kda_status status);
 
