@@ -530,6 +530,7 @@ __global__ void __launch_bounds__(256, 2)
         if (tid >= 128 && tid < 192) {
             const int row = tid - 64;  // rows 64..127 of kbx
             float ss = 0.f;
+#pragma unroll 1
             for (int c = 0; c < KK; c += 8) {
                 float f[8];
                 unpack8(*reinterpret_cast<const uint4 *>(sKB + qk_off(row, c)), f);
@@ -537,6 +538,7 @@ __global__ void __launch_bounds__(256, 2)
                 for (int j = 0; j < 8; ++j) ss = fmaf(f[j], f[j], ss);
             }
             const float rsn = 1.f / sqrtf(ss + 1e-6f);
+#pragma unroll 1
             for (int c = 0; c < KK; c += 8) {
                 uint4 *at = reinterpret_cast<uint4 *>(sKB + qk_off(row, c));
                 float f[8];
@@ -552,20 +554,29 @@ __global__ void __launch_bounds__(256, 2)
         // ... then it becomes its kg (one channel per halo thread), while threads
         // 0..127 run the cumsum below: row j is scaled by 2^(sum of the gates
         // after it), G' - g2'_j for per-token gates, G' - g'_j for a cumsum input.
-        float gprev[64];
+        // eight rows at a time from the last, the next eight loaded meanwhile
         const float *gp = p.g + ((row0 - 64) * p.HV + hv) * Kc + dh;
+        const float Gc = gate_act ? 0.f : __ldg(gp + 63 * grs);  // G' when g holds the cumsum
+        float cur[8], nxt[8];
 #pragma unroll
-        for (int j = 0; j < 64; ++j) gprev[j] = __ldg(gp + j * grs);
+        for (int j = 0; j < 8; ++j) cur[j] = __ldg(gp + (56 + j) * grs);
         float acc = 0.f;
-        const float Gc = gate_act ? 0.f : gprev[63];  // G' when g already holds the cumsum
+#pragma unroll 1
+        for (int j0 = 56; j0 >= 0; j0 -= 8) {
+            const int jn = j0 > 0 ? j0 - 8 : 0;
 #pragma unroll
-        for (int j = 63; j >= 0; --j) {
-            __nv_bfloat16 *pk = reinterpret_cast<__nv_bfloat16 *>(sKB + qk_off(64 + j, dh));
-            const float ex = p.g_is_cumsum ? Gc - gprev[j] : acc;
-            *pk = __float2bfloat16_rn(__bfloat162float(*pk) * exp2f(ex));
-            float gj = gprev[j];
-            if (gate_act) gj = neg_a * softplus_f(gj + gbias);
-            acc = fmaf(p.g_scale, gj, acc);
+            for (int j = 0; j < 8; ++j) nxt[j] = __ldg(gp + (jn + j) * grs);
+#pragma unroll
+            for (int j = 7; j >= 0; --j) {
+                __nv_bfloat16 *pk = reinterpret_cast<__nv_bfloat16 *>(sKB + qk_off(64 + j0 + j, dh));
+                const float ex = p.g_is_cumsum ? Gc - cur[j] : acc;
+                *pk = __float2bfloat16_rn(__bfloat162float(*pk) * exp2f(ex));
+                float gj = cur[j];
+                if (gate_act) gj = neg_a * softplus_f(gj + gbias);
+                acc = fmaf(p.g_scale, gj, acc);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) cur[j] = nxt[j];
         }
         sDprev[dh] = exp2f(p.g_is_cumsum ? Gc : acc);
     }
@@ -609,6 +620,7 @@ __global__ void __launch_bounds__(256, 2)
     if (__builtin_expect(p.l2norm != 0, 0)) {
         if (tid < 128) {
             float ss = 0.f;
+#pragma unroll 1
             for (int c = 0; c < KK; c += 8) {
                 float f[8];
                 unpack8(*reinterpret_cast<const uint4 *>(sAG + qk_off(tid, c)), f);
@@ -616,6 +628,7 @@ __global__ void __launch_bounds__(256, 2)
                 for (int j = 0; j < 8; ++j) ss = fmaf(f[j], f[j], ss);
             }
             const float rsn = 1.f / sqrtf(ss + 1e-6f);
+#pragma unroll 1
             for (int c = 0; c < KK; c += 8) {
                 uint4 *at = reinterpret_cast<uint4 *>(sAG + qk_off(tid, c));
                 float f[8];
