@@ -184,8 +184,8 @@ struct PrepSmem {
     static constexpr uint32_t dprev = beta + 64 * 4;            // fp32 [128]: 2^G of the previous chunk
     static constexpr uint32_t eg = dprev + 128 * 4;             // fp32 [128]: 2^G
     static constexpr uint32_t gv = eg + 128 * 4;                // fp32 [128]: G
-    static constexpr uint32_t bars = gv + 128 * 4;              // 3 mbarriers
-    static constexpr uint32_t misc = bars + 3 * 8;              // tslot, range bits
+    static constexpr uint32_t bars = gv + 128 * 4;              // 4 mbarriers
+    static constexpr uint32_t misc = bars + 4 * 8;              // tslot, range bits
     static constexpr uint32_t cur = 1856;                       // two unit cursors (UnitCur, 40 B)
     static constexpr uint32_t ag = 2048;                        // [q; k] tile
     static constexpr uint32_t kbx = ag + (KK / 64) * kBlk;      // [kb; previous kg] tile
@@ -228,9 +228,11 @@ struct UnitCur {
 static_assert(sizeof(UnitCur) <= 48, "two cursors fit their area");
 
 // The TMA descriptors of one prep launch: q and k as [B*T rows][H][K] bf16 with
-// 64 x 64 boxes, g as [B*T rows][HV][K] fp32 with 64 x 32 boxes, 128-byte swizzle.
+// 64 x 64 boxes, g as [B*T rows][HV][K] fp32 with 64 x 32 boxes, v as
+// [B*T rows][HV][V] bf16 with 64 x 64 boxes (encoded when dv is 64 or 128, unused
+// otherwise), 128-byte swizzle.
 struct PrepMaps {
-    CUtensorMap q, k, g;
+    CUtensorMap q, k, g, v;
 };
 
 // One 3-D tensor-map tile load into shared memory, completion counted in bytes
@@ -334,7 +336,7 @@ __global__ void __launch_bounds__(256, 2)
     float *sEG = reinterpret_cast<float *>(sm + S::eg);   // 2^G per channel
     float *sGv = reinterpret_cast<float *>(sm + S::gv);   // G per channel
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + S::bars);
-    uint64_t &bar = bars[0], &bar_g = bars[1], &bar_qk = bars[2];
+    uint64_t &bar = bars[0], &bar_g = bars[1], &bar_qk = bars[2], &bar_v = bars[3];
     uint32_t &tslot = *reinterpret_cast<uint32_t *>(sm + S::misc);
     int &sRangeBits = *reinterpret_cast<int *>(sm + S::misc + 4);
     UnitCur *curs = reinterpret_cast<UnitCur *>(sm + S::cur);
@@ -348,6 +350,9 @@ __global__ void __launch_bounds__(256, 2)
         return;
     }
     const bool pref = KK == 128 && VV <= 128;  // see PrepSmem
+    // v by TMA (64 x 64 boxes, 128-byte swizzle) when dv is 64 or 128 with the pref
+    // plan; 16-byte cp.async copies into the plain core-matrix layout otherwise
+    const bool vtma = pref && (VV & 63) == 0;
 
     unsigned char *sAG = sm + S::ag;
     unsigned char *sKB = sm + S::kbx;
@@ -449,6 +454,7 @@ __global__ void __launch_bounds__(256, 2)
         mbar_init(&bar, 1);
         mbar_init(&bar_g, 2);   // the two halves of g arrive separately
         mbar_init(&bar_qk, 2);  // the q copies and the k copies arrive separately
+        mbar_init(&bar_v, 1);
         mbar_fence_init();
         sRangeBits = 0;
         find(ubeg, &curs[0]);
@@ -460,6 +466,7 @@ __global__ void __launch_bounds__(256, 2)
     tc_fence_after();
     const uint32_t tmem = tslot;
     uint32_t phase = 0, ph_in = 0;  // MMA barrier phases; input copies (g and q/k) per unit
+    uint32_t ph_v = 0;              // v copies by TMA (one per unit)
     int slot = 0;
     int prev_hv = -1;
     int64_t prev_gc = -1;
@@ -570,7 +577,7 @@ __global__ void __launch_bounds__(256, 2)
             for (int j = 7; j >= 0; --j) {
                 __nv_bfloat16 *pk = reinterpret_cast<__nv_bfloat16 *>(sKB + qk_off(64 + j0 + j, dh));
                 const float ex = p.g_is_cumsum ? Gc - cur[j] : acc;
-                *pk = __float2bfloat16_rn(__bfloat162float(*pk) * exp2f(ex));
+                *pk = __float2bfloat16_rn(__bfloat162float(*pk) * ex2_ftz(ex));
                 float gj = cur[j];
                 if (gate_act) gj = neg_a * softplus_f(gj + gbias);
                 acc = fmaf(p.g_scale, gj, acc);
@@ -578,23 +585,73 @@ __global__ void __launch_bounds__(256, 2)
 #pragma unroll
             for (int j = 0; j < 8; ++j) cur[j] = nxt[j];
         }
-        sDprev[dh] = exp2f(p.g_is_cumsum ? Gc : acc);
+        sDprev[dh] = ex2_ftz(p.g_is_cumsum ? Gc : acc);
     }
-    // thread d < dk: channel d's chunk-local cumsum in place (rows past the end keep G)
+    // thread d < dk: channel d's chunk-local cumsum in place (rows past the end keep
+    // G).  Per-token gates: all 64 rows in registers, four independent 16-row
+    // running sums, then each quarter offset by the totals before it.  Otherwise
+    // (activation or a cumsum input) 16 rows at a time, each block's loads issued
+    // before the previous block's stores: a store to the tile between two of its
+    // loads would order them and put the shared-memory latency on every row.
     if (tid < KK) {
         float acc = 0.f, rng = 0.f;
-#pragma unroll 8
-        for (int i = 0; i < 64; ++i) {
-            const int gi = gsw(i, tid);
-            if (i < nr && tid < Kc) {  // channels past K keep a zero gate
-                float x = sG2[gi];
-                if (gate_act) x = neg_a * softplus_f(x + gbias);
-                acc = p.g_is_cumsum ? x : fmaf(p.g_scale, x, acc);
+        const bool live = tid < Kc;  // channels past K keep a zero gate
+        if (!gate_act && !p.g_is_cumsum) {
+            float x[64];
+#pragma unroll
+            for (int i = 0; i < 64; ++i) x[i] = sG2[gsw(i, tid)];
+            float tot[4];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                float a = 0.f;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int i = 16 * q4 + j;
+                    a = fmaf(p.g_scale, (i < nr && live) ? x[i] : 0.f, a);
+                    x[i] = a;
+                }
+                tot[q4] = a;
             }
-            sG2[gi] = acc;
-            rng = fmaxf(rng, fabsf(acc));
+            float off = 0.f;
+#pragma unroll
+            for (int q4 = 1; q4 < 4; ++q4) {
+                off += tot[q4 - 1];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) x[16 * q4 + j] += off;
+            }
+#pragma unroll
+            for (int i = 0; i < 64; ++i) {
+                rng = fmaxf(rng, fabsf(x[i]));
+                sG2[gsw(i, tid)] = x[i];
+            }
+            acc = x[63];
+        } else {
+            float x[16], y[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) x[j] = sG2[gsw(j, tid)];
+#pragma unroll 1
+            for (int i0 = 0; i0 < 64; i0 += 16) {
+                if (i0 + 16 < 64) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) y[j] = sG2[gsw(i0 + 16 + j, tid)];
+                }
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    if (i0 + j < nr && live) {
+                        float gj = x[j];
+                        if (gate_act) gj = neg_a * softplus_f(gj + gbias);
+                        acc = p.g_is_cumsum ? gj : fmaf(p.g_scale, gj, acc);
+                    }
+                    x[j] = acc;
+                    rng = fmaxf(rng, fabsf(acc));
+                }
+#pragma unroll
+                for (int j = 0; j < 16; ++j) sG2[gsw(i0 + j, tid)] = x[j];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) x[j] = y[j];
+            }
         }
-        const float eG = exp2f(acc);
+        const float eG = ex2_ftz(acc);
         sEG[tid] = eG;
         sGv[tid] = acc;
         reinterpret_cast<float *>(U + Lo.dec)[tid] = eG;
@@ -696,15 +753,15 @@ __global__ void __launch_bounds__(256, 2)
         float qg[8], kgm[8], kb[8], kgv[8], qs[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            const float e = exp2f(gam[j]);
+            const float e = ex2_ftz(gam[j]);
             qg[j] = fq[j] * e;
             kgm[j] = fk[j] * e;
             qs[j] = p.scale * qg[j];
             if (fast) {
-                kb[j] = fk[j] * exp2f(-gam[j]);
+                kb[j] = fk[j] * ex2_ftz(-gam[j]);
                 kgv[j] = kb[j] * sEG[c + j];
             } else {
-                kgv[j] = fk[j] * exp2f(sGv[c + j] - gam[j]);
+                kgv[j] = fk[j] * ex2_ftz(sGv[c + j] - gam[j]);
             }
         }
         *pq = pack8(qg);
@@ -713,10 +770,26 @@ __global__ void __launch_bounds__(256, 2)
         *reinterpret_cast<uint4 *>(U + Lo.aw + tile_off(64 + i, c, KK)) = pack8(qs);
         *reinterpret_cast<uint4 *>(U + Lo.kgt + tile_off(i, c, KK)) = pack8(kgv);
     }
-    __syncthreads();
-    {
-        // v into the freed g2 buffer (its second half with the pref plan);
-        // waited for just before the u MMA
+    if (vtma) {
+        // One barrier: the elementwise pass has read g2 and written the gram
+        // operands before thread 0 issues v into g2's second half, the next unit's
+        // g channels 0..63 into its first half, and the gram MMA.  v is waited for
+        // just before the u MMA.
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (tid == 0) {
+            fence_async_smem();
+            mbar_arrive_expect_tx(&bar_v, 64 * VV * 2);
+            for (int x = 0; x < VV / 64; ++x)
+                tma_load3(sV + x * 8192, &maps.v, x * 64, hv, b * p.T + r0, &bar_v);
+            if (nxt->unit < uend) issue(nxt, true, false, false, false);
+        }
+    } else {
+        __syncthreads();
+        // v into the freed g2 buffer (its second half with the pref plan); waited
+        // for just before the u MMA
         for (int idx = tid; idx < 64 * VG8; idx += 256) {
             const int l = idx & 31, w = idx >> 5;
             const int i = (w & 7) * 8 + (l & 7);
@@ -731,11 +804,11 @@ __global__ void __launch_bounds__(256, 2)
         // with the pref plan the first half of g2 is free for good: the next
         // unit's g channels 0..63
         if (pref && tid == 0 && nxt->unit < uend) issue(nxt, true, false, false, false);
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
     }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
 
     // ---- 4. grams on the tensor cores.  D[:, 0:64] = [Qg; Kg] Kb^T (split grams),
     // D[:, 64:128] = [Qg; Kg] kgp^T (cross-chunk gram with the previous chunk);
@@ -908,18 +981,19 @@ __global__ void __launch_bounds__(256, 2)
         // W~ = W Diag(2^G_prev) -> rows 0..63 of the [W; qg] tile, and M; warps
         // 2, 3 and 6, 7 reach the same TMEM lanes and take half the columns each.
         const int quad = warp & 3, i = (tid & 127) - 64, half = warp >> 2;
+        constexpr int kHalf = KK / 2;  // the warp's columns, in one load
+        float dd[kHalf];
+        if constexpr (kHalf == 64)
+            tmem_ld64(tmem_at(tmem, quad * 32, half * kHalf), dd);
+        else
+            tmem_ld32(tmem_at(tmem, quad * 32, half * kHalf), dd);
+        if (halo) {
 #pragma unroll
-        for (int c0 = half * (KK / 2); c0 < (half + 1) * (KK / 2); c0 += 32) {
-            float dd[32];
-            tmem_ld32(tmem_at(tmem, quad * 32, c0), dd);
-            if (halo) {
-#pragma unroll
-                for (int j = 0; j < 32; ++j) dd[j] *= sDprev[c0 + j];
-            }
-#pragma unroll
-            for (int c8 = 0; c8 < 32; c8 += 8)
-                *reinterpret_cast<uint4 *>(U + Lo.aw + tile_off(i, c0 + c8, KK)) = pack8_at(dd + c8);
+            for (int j = 0; j < kHalf; ++j) dd[j] *= sDprev[half * kHalf + j];
         }
+#pragma unroll
+        for (int c8 = 0; c8 < kHalf; c8 += 8)
+            *reinterpret_cast<uint4 *>(U + Lo.aw + tile_off(i, half * kHalf + c8, KK)) = pack8_at(dd + c8);
         if (halo) {
             float dd[32];
             tmem_ld32(tmem_at(tmem, quad * 32, KK + half * 32), dd);
@@ -928,7 +1002,15 @@ __global__ void __launch_bounds__(256, 2)
                 *reinterpret_cast<uint4 *>(U + Lo.mt + tile_off(i, half * 32 + c8, 64)) = pack8_at(dd + c8);
         }
     }
-    // v has landed before anyone passes this barrier
+    // v has landed before anyone passes this barrier.  With v by TMA, rows past
+    // the chunk's end (another sequence's rows, or NaN) are zeroed once it has.
+    if (vtma && __builtin_expect(nr < 64, 0)) {
+        if (!mbar_wait(&bar_v, ph_v & 1, kWaitNs) && tid == 0) report(p.status, KDA_DEVICE_TIMEOUT);
+        for (int idx = tid; idx < (64 - nr) * (VV / 8); idx += 256) {
+            const int i = nr + idx / (VV / 8), c = (idx % (VV / 8)) * 8;
+            *reinterpret_cast<uint4 *>(sV + sw128_off(i, c, 8192)) = make_uint4(0, 0, 0, 0);
+        }
+    }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
     fence_async_smem();
     tc_fence_before();
@@ -939,14 +1021,26 @@ __global__ void __launch_bounds__(256, 2)
 
     // ---- 7. u = Akk diag(beta) v
     if (tid == 0) {
-        // K step kk: v rows 16 kk .. 16 kk + 15 (the second half v_half further on)
+        if (vtma) {
+            // v MN-major, 128-byte swizzled: a K step (16 rows) moves 2 KB, its
+            // 64-column boxes lie 8 KB apart
+            if (!mbar_wait(&bar_v, ph_v & 1, kWaitNs)) report(p.status, KDA_DEVICE_TIMEOUT);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-            mma_bf16(tmem, adesc + (uint64_t)(kk * 16),
-                     sdesc(smem_addr(sV) + kk * 2 * VV * 16 + (kk >= 2 ? v_half : 0), VV * 16, 128),
-                     idesc_bf16(128, VV, false, true), kk > 0);
+            for (int kk = 0; kk < 4; ++kk)
+                mma_bf16(tmem, adesc + (uint64_t)(kk * 16),
+                         sdesc_sw128(smem_addr(sV) + kk * 2048, 8192, 1024),
+                         idesc_bf16(128, VV, false, true), kk > 0);
+        } else {
+            // K step kk: v rows 16 kk .. 16 kk + 15 (the second half v_half further on)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                mma_bf16(tmem, adesc + (uint64_t)(kk * 16),
+                         sdesc(smem_addr(sV) + kk * 2 * VV * 16 + (kk >= 2 ? v_half : 0), VV * 16, 128),
+                         idesc_bf16(128, VV, false, true), kk > 0);
+        }
         mma_commit(&bar);
     }
+    if (vtma) ++ph_v;
     if (tid == 0 && !mbar_wait(&bar, phase & 1, kWaitNs)) report(p.status, KDA_DEVICE_TIMEOUT);
     __syncthreads();
     ++phase;
@@ -968,12 +1062,23 @@ __global__ void __launch_bounds__(256, 2)
     if (warp == 2 || warp == 3 || warp == 6 || warp == 7) {
         const int quad = warp & 3, i = (tid & 127) - 64;
         const int cbeg = warp < 4 ? 0 : VV / 2;
-        for (int c0 = cbeg; c0 < cbeg + VV / 2; c0 += 16) {
-            float dd[16];
-            tmem_ld16(tmem_at(tmem, quad * 32, c0), dd);
-            unsigned char *ub = U + Lo.u + ((size_t)(c0 / kUB) * 64 + i) * kUB * 2;
-            *reinterpret_cast<uint4 *>(ub) = pack8_at(dd);
-            *reinterpret_cast<uint4 *>(ub + 16) = pack8_at(dd + 8);
+        if (VV == 128) {  // the warp's 64 columns in one load
+            float dd[64];
+            tmem_ld64(tmem_at(tmem, quad * 32, cbeg), dd);
+#pragma unroll
+            for (int c = 0; c < 64; c += 16) {
+                unsigned char *ub = U + Lo.u + ((size_t)((cbeg + c) / kUB) * 64 + i) * kUB * 2;
+                *reinterpret_cast<uint4 *>(ub) = pack8_at(dd + c);
+                *reinterpret_cast<uint4 *>(ub + 16) = pack8_at(dd + c + 8);
+            }
+        } else {
+            for (int c0 = cbeg; c0 < cbeg + VV / 2; c0 += 16) {
+                float dd[16];
+                tmem_ld16(tmem_at(tmem, quad * 32, c0), dd);
+                unsigned char *ub = U + Lo.u + ((size_t)(c0 / kUB) * 64 + i) * kUB * 2;
+                *reinterpret_cast<uint4 *>(ub) = pack8_at(dd);
+                *reinterpret_cast<uint4 *>(ub + 16) = pack8_at(dd + 8);
+            }
         }
     }
     tc_fence_before();
@@ -991,6 +1096,7 @@ __global__ void __launch_bounds__(256, 2)
     if (tid == 0 && ph_in > 0) {
         mbar_wait(&bar_g, (ph_in - 1) & 1, kWaitNs);
         mbar_wait(&bar_qk, (ph_in - 1) & 1, kWaitNs);
+        if (ph_v > 0) mbar_wait(&bar_v, (ph_v - 1) & 1, kWaitNs);
     }
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, kCols);
@@ -1682,6 +1788,8 @@ cudaError_t prep_maps(const ChunkArgs &a, PrepMaps *m) {
         e = encode3(&m->k, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.K, a.H, rows, 64);
     if (e == cudaSuccess)
         e = encode3(&m->g, a.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.K, a.HV, rows, 32);
+    if (e == cudaSuccess && a.V % 64 == 0 && a.V <= 128)
+        e = encode3(&m->v, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.V, a.HV, rows, 64);
     return e;
 }
 
@@ -1732,7 +1840,7 @@ cudaError_t launch_prep_t(const ChunkArgs &a, cudaStream_t st, int64_t cta_cap) 
     const int64_t units = prep_units(a);
     if (units == 0) return cudaSuccess;
     const unsigned grid = (unsigned)(units < ctas ? units : ctas);
-    PrepMaps maps;
+    PrepMaps maps{};
     if ((e = prep_maps(a, &maps)) != cudaSuccess) return e;
     prof_begin("chunk_prep_tc", st);
     chunk_prep_tc_kernel<KK, ACT, PADK><<<grid, 256, smem, st>>>(a, maps);

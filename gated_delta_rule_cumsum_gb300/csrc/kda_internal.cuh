@@ -108,6 +108,13 @@ struct GateAct {
     float beta_scale = 0.f;
 };
 __device__ __forceinline__ float softplus_f(float x) { return x > 20.f ? x : log1pf(expf(x)); }
+// 2^x by the PTX instruction ex2.approx.ftz.f32: one special-function-unit op,
+// relative error near 2^-22, results below 2^-126 flushed to zero.
+__device__ __forceinline__ float ex2_ftz(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 // -exp(A_log[hv]) for the channel loop of one value head
 __device__ __forceinline__ float gate_neg_a(const GateAct &a, int hv) { return -expf(a.A_log[hv]); }
 __device__ __forceinline__ float gate_bias(const GateAct &a, int hv, int d, int K) {

@@ -108,7 +108,7 @@ def test_tensor_core_path_any_k_multiple_of_8(kda_lib, K, V, T, lens):
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("K,V,T", [(64, 64, 1), (64, 16, 63), (128, 96, 64), (128, 256, 65),
-                                   (64, 128, 200), (128, 40, 130)])
+                                   (64, 128, 200), (128, 40, 130), (128, 64, 100)])
 def test_shapes(kda_lib, dtype, K, V, T):
     inp = _small(K + V + T, B=2, T=T, K=K, V=V, dtype=dtype)
     o, ht = _run(kda_lib, inp)
