@@ -6,7 +6,7 @@
 //
 //   prep kernel, one CTA per (chunk, value head), all in parallel:
 //     Stage 1     g2, G (fp32, per channel)
-//     Stage 2     Aqk = scale * tril(Qg Kb^T),  L = diag(beta) * strictly_tril(Kg Kb^T)
+//     Stage 2     Aqk = tril(Qg Kb^T),  L = diag(beta) * strictly_tril(Kg Kb^T)
 //                 with Qg = q 2^g2, Kg = k 2^g2, Kb = k 2^-g2: the per-channel gate
 //                 2^(g2_i - g2_j) split through the chunk start, one tcgen05 MMA
 //                 (M = 128: [Qg; Kg] stacked, N = 64, K = dk).  This split keeps
@@ -18,11 +18,11 @@
 //                 (16 x 16 diagonal blocks by substitution, then two doubling
 //                 steps to 32 x 32 and 64 x 64).
 //                 w = Akk diag(beta) Kg,  u = Akk diag(beta) v    (tcgen05, N = dk / dv)
-//                 kg = k 2^(G - g2),  qg = scale q 2^g2,  decay = 2^G
+//                 kg = k 2^(G - g2),  qg = q 2^g2,  decay = 2^G
 //     The results go to the workspace as ready-made MMA operand tiles.
 //
 //   scan kernel, one CTA per (sequence, value head, 32 value columns):
-//     Stage 3+4   v' = u - w h;   o = qg h + Aqk v';   h = Diag(2^G) h + kg^T v'
+//     Stage 3+4   v' = u - w h;   o = scale (qg h + Aqk v');   h = Diag(2^G) h + kg^T v'
 //                 [w; qg] h    : one MMA, M = 128, N = 32, K = dk
 //                 kg^T v'      : one MMA, M = 128 (= dk, zero-padded for dk = 64)
 //                 Aqk v'       : accumulated onto the qg h rows of the first MMA
@@ -49,11 +49,12 @@ constexpr uint64_t kWaitNs = 1000000000ull;
 // Byte layout of one workspace unit (chunk c, value head).
 struct TcLayout {
     uint32_t aw;      // [128][dk] tile: rows 0..63 W~_c = W_c Diag(2^G_{c-1}) (W_0 for a
-                      // sequence's first chunk), rows 64..127 scale * qg_c
+                      // sequence's first chunk), rows 64..127 qg_c (the scan
+                      // applies the attention scale to o)
     uint32_t kgt;     // [64][dk] tile: kg_c (rows = tokens), read by the scan as an
                       // MN-major operand, i.e. as kg_c^T
     uint32_t mt;      // [64][64] tile: M_c = W_c kg_{c-1}^T (unused for a first chunk)
-    uint32_t aqk;     // [64][64] tile: Aqk_c (scale inside)
+    uint32_t aqk;     // [64][64] tile: Aqk_c (unscaled, like qg_c)
     uint32_t u;       // [dv / kUB][64][kUB] bf16 row-major blocks: u_c
     uint32_t dec;     // [128] fp32: 2^G_c (0 beyond dk)
     uint32_t stride;  // unit size, 256-byte multiple
@@ -722,7 +723,7 @@ __global__ void __launch_bounds__(256, 2)
                 }
                 if (lane == 0) {
                     *reinterpret_cast<__nv_bfloat16 *>(U + Lo.aqk + tile_off(i, j, 64)) =
-                        __float2bfloat16_rn(p.scale * aq);
+                        __float2bfloat16_rn(aq);
                     sL[akk_idx<kSplitA>(i, j)] = (i > j) ? sBeta[i] * ak : 0.f;
                 }
             }
@@ -737,7 +738,7 @@ __global__ void __launch_bounds__(256, 2)
 
     // ---- 3. elementwise, in place: 8 channels of one row per thread; lanes 0..7
     // take 8 consecutive rows of one column chunk, which the swizzle spreads over
-    // all banks.  qg, kg, kb, scale * qg and kg to the workspace.
+    // all banks.  qg, kg, kb in place; qg and kg to the workspace.
 #pragma unroll
     for (int it = 0; it < KK / 32; ++it) {
         const int idx = tid + it * 256, l = idx & 31, w = idx >> 5;
@@ -750,13 +751,12 @@ __global__ void __launch_bounds__(256, 2)
         unpack8(*pk, fk);
         *reinterpret_cast<float4 *>(gam) = *reinterpret_cast<const float4 *>(sG2 + gsw(i, c));
         *reinterpret_cast<float4 *>(gam + 4) = *reinterpret_cast<const float4 *>(sG2 + gsw(i, c + 4));
-        float qg[8], kgm[8], kb[8], kgv[8], qs[8];
+        float qg[8], kgm[8], kb[8], kgv[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const float e = ex2_ftz(gam[j]);
             qg[j] = fq[j] * e;
             kgm[j] = fk[j] * e;
-            qs[j] = p.scale * qg[j];
             if (fast) {
                 kb[j] = fk[j] * ex2_ftz(-gam[j]);
                 kgv[j] = kb[j] * sEG[c + j];
@@ -764,10 +764,11 @@ __global__ void __launch_bounds__(256, 2)
                 kgv[j] = fk[j] * ex2_ftz(sGv[c + j] - gam[j]);
             }
         }
-        *pq = pack8(qg);
+        const uint4 qpk = pack8(qg);
+        *pq = qpk;
         *pk = pack8(kgm);
         if (fast) *reinterpret_cast<uint4 *>(sKB + qk_off(i, c)) = pack8(kb);
-        *reinterpret_cast<uint4 *>(U + Lo.aw + tile_off(64 + i, c, KK)) = pack8(qs);
+        *reinterpret_cast<uint4 *>(U + Lo.aw + tile_off(64 + i, c, KK)) = qpk;
         *reinterpret_cast<uint4 *>(U + Lo.kgt + tile_off(i, c, KK)) = pack8(kgv);
     }
     if (vtma) {
@@ -842,7 +843,7 @@ __global__ void __launch_bounds__(256, 2)
                 for (int c0 = 0; c0 < 64; c0 += 8) {
                     float a8[8];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) a8[j] = (c0 + j <= i) ? p.scale * dd[c0 + j] : 0.f;
+                    for (int j = 0; j < 8; ++j) a8[j] = (c0 + j <= i) ? dd[c0 + j] : 0.f;
                     *reinterpret_cast<uint4 *>(U + Lo.aqk + tile_off(i, c0, 64)) = pack8(a8);
                 }
             } else {
@@ -1108,7 +1109,7 @@ __global__ void __launch_bounds__(256, 2)
 //   A: D1  = [W~_{c+1}; qg_c] h_c        (needs h_c)
 //   C: D2  = kg_c^T v'_c                 (needs v'_c)   ->  h_{c+1} = Diag(2^G_c) h_c + D2
 //   B: D1 += [M_{c+1}; Aqk_c] v'_c       (needs v'_c)   ->  v'_{c+1} = u_{c+1} - D1[0:64]
-//                                                          o_c      = D1[64:128]
+//                                                          o_c      = scale D1[64:128]
 // where W~_{c+1} = W_{c+1} Diag(2^G_c) and M_{c+1} = W_{c+1} kg_c^T come from the
 // prep kernel: v'_{c+1} = u_{c+1} - W_{c+1} h_{c+1} expands into the A and B
 // terms.  Issue order A, C, B: the state update (after C) overlaps B, and the
@@ -1516,7 +1517,7 @@ __global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
             if (r + 1 < R) fetch(r + 1);
         }
     } else {
-        // -------------------------------------------- o warps: o_c = D1[64:128]
+        // ------------------------------------- o warps: o_c = scale D1[64:128]
         // (for identity columns: Q_c, segment 1's response to its initial state)
         const int i = (warp - 6) * 32 + lane;  // row within the chunk
         const uint32_t lanebase = (uint32_t)(64 + (warp - 6) * 32) << 16;
@@ -1528,6 +1529,8 @@ __global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
                 float d[SBV];
                 tmem_ld_cols<SBV>(tmem + lanebase + (r & 1) * SBV, d);
                 tc_fence_before();
+#pragma unroll
+                for (int t = 0; t < SBV; ++t) d[t] *= p.scale;
                 const int c = c0 + r - 1;
                 if (!read_flag(&abort_flag)) {
                     if (ident) {
