@@ -361,7 +361,9 @@ __global__ void __launch_bounds__(256, 2)
     // v: with the pref plan in the second half of g2
     unsigned char *sV = pref ? sm + S::g + 64 * 64 * 4 : sm + S::g;
     constexpr uint32_t v_half = 0;  // extra gap before v's rows 32..63 (none)
-    unsigned char *sAB = pref ? sAG + S::kBlk : sm + S::g + 64 * VV * 2;
+    // Akk diag(beta), twice (rows 0..63 and 64..127 of the M = 128 A operand), in
+    // L's place once the solve is done with L and T
+    unsigned char *sAB = sm + S::lbuf(VV);
     float *sL = reinterpret_cast<float *>(sm + S::lbuf(VV));    // after the gram MMA
     float *sT = reinterpret_cast<float *>(sm + S::tbuf(VV));
     unsigned char *sPB = sm + S::pbuf(VV);
@@ -926,40 +928,32 @@ __global__ void __launch_bounds__(256, 2)
         sta4<kSplitA>(sA, 16 * I + sr, 16 * J + sc, neg4(s));
     }
     __syncthreads();
-    // Akk diag(beta) as a bf16 operand tile (Akk is lower triangular).  With the
-    // pref plan it overwrites Akk's second half: every read before any write.
-    {
-        uint4 ab[2];
+    // Akk diag(beta) as a bf16 operand tile (Akk is lower triangular), stored twice so
+    // that the MMAs below give every result row in both TMEM lane halves.
 #pragma unroll
-        for (int it = 0; it < 2; ++it) {
-            const int idx = tid + it * 256, l = idx & 31, w = idx >> 5;
-            const int i = (w & 7) * 8 + (l & 7);
-            const int c = ((w >> 3) * 4 + (l >> 3)) * 8;
-            const float4 a0 = lda4<kSplitA>(sA, i, c), a1 = lda4<kSplitA>(sA, i, c + 4);
-            const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            float f[8];
+    for (int it = 0; it < 2; ++it) {
+        const int idx = tid + it * 256, l = idx & 31, w = idx >> 5;
+        const int i = (w & 7) * 8 + (l & 7);
+        const int c = ((w >> 3) * 4 + (l >> 3)) * 8;
+        const float4 a0 = lda4<kSplitA>(sA, i, c), a1 = lda4<kSplitA>(sA, i, c + 4);
+        const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        float f[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) f[j] = (c + j <= i) ? av[j] * sBeta[c + j] : 0.f;
-            ab[it] = pack8(f);
-        }
-        if (pref) __syncthreads();
-#pragma unroll
-        for (int it = 0; it < 2; ++it) {
-            const int idx = tid + it * 256, l = idx & 31, w = idx >> 5;
-            const int i = (w & 7) * 8 + (l & 7);
-            const int c = ((w >> 3) * 4 + (l >> 3)) * 8;
-            *reinterpret_cast<uint4 *>(sAB + tile_off(i, c, 64)) = ab[it];
-        }
+        for (int j = 0; j < 8; ++j) f[j] = (c + j <= i) ? av[j] * sBeta[c + j] : 0.f;
+        const uint4 ab = pack8(f);
+        *reinterpret_cast<uint4 *>(sAB + tile_off(i, c, 64)) = ab;
+        *reinterpret_cast<uint4 *>(sAB + tile_off(64 + i, c, 64)) = ab;
     }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
 
-    // ---- 6. W = Akk diag(beta) Kg and M = Akk diag(beta) P (valid rows: lanes 64..127).
+    // ---- 6. W = Akk diag(beta) Kg and M = Akk diag(beta) P (TMEM lanes 64..127 repeat
+    // lanes 0..63).
     // Kg is an MN-major 128-byte swizzled operand here: a K step (16 rows) moves
     // two 8-row groups (2 KB); its 64-column blocks lie 16 KB apart.
-    const uint64_t adesc = sdesc(smem_addr(sAB) - 8 * 1024, 128, 1024);  // rows 64..127 = Akk diag(beta)
+    const uint64_t adesc = sdesc(smem_addr(sAB), 128, 1024);  // [Akk diag(beta); the same]
     if (tid == 0) {
         const uint32_t kg0 = smem_addr(sAG) + 8192;
 #pragma unroll
@@ -978,29 +972,30 @@ __global__ void __launch_bounds__(256, 2)
     // The k rows of ag were the W MMA's last use of them: with the pref plan, the
     // next unit's k rows go there now.
     if (pref && tid == 0 && nxt->unit < uend) issue(nxt, false, false, false, true);
-    if (warp == 2 || warp == 3 || warp == 6 || warp == 7) {
-        // W~ = W Diag(2^G_prev) -> rows 0..63 of the [W; qg] tile, and M; warps
-        // 2, 3 and 6, 7 reach the same TMEM lanes and take half the columns each.
-        const int quad = warp & 3, i = (tid & 127) - 64, half = warp >> 2;
-        constexpr int kHalf = KK / 2;  // the warp's columns, in one load
-        float dd[kHalf];
-        if constexpr (kHalf == 64)
-            tmem_ld64(tmem_at(tmem, quad * 32, half * kHalf), dd);
+    {
+        // W~ = W Diag(2^G_prev) -> rows 0..63 of the [W; qg] tile, and M.  Row i sits in
+        // TMEM lanes i and 64 + i; the four warps that reach those lanes (w % 4 = i / 32
+        // or 2 + i / 32) take a quarter of its columns each.
+        const int quad = warp & 3, i = (tid & 127) & 63, part = (warp >> 2) + 2 * (quad >> 1);
+        constexpr int kQ = KK / 4;
+        float dd[kQ];
+        if constexpr (kQ == 32)
+            tmem_ld32(tmem_at(tmem, quad * 32, part * kQ), dd);
         else
-            tmem_ld32(tmem_at(tmem, quad * 32, half * kHalf), dd);
+            tmem_ld16(tmem_at(tmem, quad * 32, part * kQ), dd);
         if (halo) {
 #pragma unroll
-            for (int j = 0; j < kHalf; ++j) dd[j] *= sDprev[half * kHalf + j];
+            for (int j = 0; j < kQ; ++j) dd[j] *= sDprev[part * kQ + j];
         }
 #pragma unroll
-        for (int c8 = 0; c8 < kHalf; c8 += 8)
-            *reinterpret_cast<uint4 *>(U + Lo.aw + tile_off(i, half * kHalf + c8, KK)) = pack8_at(dd + c8);
+        for (int c8 = 0; c8 < kQ; c8 += 8)
+            *reinterpret_cast<uint4 *>(U + Lo.aw + tile_off(i, part * kQ + c8, KK)) = pack8_at(dd + c8);
         if (halo) {
-            float dd[32];
-            tmem_ld32(tmem_at(tmem, quad * 32, KK + half * 32), dd);
+            float dm[16];
+            tmem_ld16(tmem_at(tmem, quad * 32, KK + part * 16), dm);
 #pragma unroll
-            for (int c8 = 0; c8 < 32; c8 += 8)
-                *reinterpret_cast<uint4 *>(U + Lo.mt + tile_off(i, half * 32 + c8, 64)) = pack8_at(dd + c8);
+            for (int c8 = 0; c8 < 16; c8 += 8)
+                *reinterpret_cast<uint4 *>(U + Lo.mt + tile_off(i, part * 16 + c8, 64)) = pack8_at(dm + c8);
         }
     }
     // v has landed before anyone passes this barrier.  With v by TMA, rows past
@@ -1060,25 +1055,28 @@ __global__ void __launch_bounds__(256, 2)
             asm volatile("cp.async.commit_group;" ::: "memory");
         }
     }
-    if (warp == 2 || warp == 3 || warp == 6 || warp == 7) {
-        const int quad = warp & 3, i = (tid & 127) - 64;
-        const int cbeg = warp < 4 ? 0 : VV / 2;
-        if (VV == 128) {  // the warp's 64 columns in one load
-            float dd[64];
-            tmem_ld64(tmem_at(tmem, quad * 32, cbeg), dd);
+    {
+        // u: the same row split as W, a quarter of the dv columns per warp
+        const int quad = warp & 3, i = (tid & 127) & 63, part = (warp >> 2) + 2 * (quad >> 1);
+        const int per = VV / 4, cbeg = part * per;  // per: a multiple of 8
+        if (per % 32 == 0) {
+            for (int c0 = cbeg; c0 < cbeg + per; c0 += 32) {
+                float dd[32];
+                tmem_ld32(tmem_at(tmem, quad * 32, c0), dd);
 #pragma unroll
-            for (int c = 0; c < 64; c += 16) {
-                unsigned char *ub = U + Lo.u + ((size_t)((cbeg + c) / kUB) * 64 + i) * kUB * 2;
-                *reinterpret_cast<uint4 *>(ub) = pack8_at(dd + c);
-                *reinterpret_cast<uint4 *>(ub + 16) = pack8_at(dd + c + 8);
+                for (int c = 0; c < 32; c += 16) {
+                    unsigned char *ub = U + Lo.u + ((size_t)((c0 + c) / kUB) * 64 + i) * kUB * 2;
+                    *reinterpret_cast<uint4 *>(ub) = pack8_at(dd + c);
+                    *reinterpret_cast<uint4 *>(ub + 16) = pack8_at(dd + c + 8);
+                }
             }
         } else {
-            for (int c0 = cbeg; c0 < cbeg + VV / 2; c0 += 16) {
-                float dd[16];
-                tmem_ld16(tmem_at(tmem, quad * 32, c0), dd);
-                unsigned char *ub = U + Lo.u + ((size_t)(c0 / kUB) * 64 + i) * kUB * 2;
+            for (int c0 = cbeg; c0 < cbeg + per; c0 += 8) {
+                float dd[8];
+                tmem_ld8(tmem_at(tmem, quad * 32, c0), dd);
+                unsigned char *ub =
+                    U + Lo.u + ((size_t)(c0 / kUB) * 64 + i) * kUB * 2 + (c0 % kUB) * 2;
                 *reinterpret_cast<uint4 *>(ub) = pack8_at(dd);
-                *reinterpret_cast<uint4 *>(ub + 16) = pack8_at(dd + 8);
             }
         }
     }

@@ -135,6 +135,20 @@ __device__ __forceinline__ uint32_t tmem_at(uint32_t base, uint32_t lane, uint32
     return base + (lane << 16) + col;
 }
 
+// 32 lanes x 8 consecutive 32-bit columns, then wait (lanes as for tmem_ld16).
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
+    uint32_t r[8];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 // 32 lanes x 16 consecutive 32-bit columns, then wait: thread t of the warp
 // receives lane (warp % 4) * 32 + t.  `taddr` must carry that lane base.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
