@@ -1138,7 +1138,8 @@ struct ScanSmem {
     static constexpr uint32_t hs = kStages * stage_stride;     // [KK][SBV] tile
     static constexpr uint32_t vp = hs + KK * SBV * 2;          // [64][SBV] tile
     static constexpr uint32_t total = vp + 64 * SBV * 2;
-    static constexpr uint32_t tmem_cols = SBV == 32 ? 128 : 256;  // D1[0], D1[1], D2 at 0, SBV, 2 SBV
+    // D1[0], D1[1], D2 at 0, SBV, 2 SBV
+    static constexpr uint32_t tmem_cols = SBV == 32 ? 128 : (SBV == 64 ? 256 : 512);
 };
 
 __device__ __forceinline__ int read_flag(const int *f) {
@@ -1170,15 +1171,6 @@ constexpr int kBarV = 2;   // v'_c written and D1 read: v' and o warps arrive, t
 constexpr int kThrH = 128 + 32;
 constexpr int kThrV = 128 + 32;
 
-// SBV columns of TMEM (one lane per thread) into registers.
-template <int SBV>
-__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&d)[SBV]) {
-    if constexpr (SBV == 64) {
-        tmem_ld64(taddr, d);
-    } else {
-        tmem_ld32(taddr, d);
-    }
-}
 
 // Work item of a scan CTA.  Without a split: (n, hv, vb) over the V columns.
 // With a split, per (n, hv): V/SBV segment-0 blocks, V/SBV segment-1 blocks,
@@ -1428,10 +1420,18 @@ __global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
                 // h_{c+1} = Diag(2^G_c) h_c + D2  (bar_h also covers A_r's reads of h_c)
                 wait_mma(&bar_h, (r - 1) & 1);
                 tc_fence_after();
-                float d[SBV];
-                tmem_ld_cols<SBV>(taddr, d);
+                // D2 a slice at a time (128-column CTAs cannot hold all of D2 beside h)
+                constexpr int kSl = SBV == 128 ? 16 : 32;
 #pragma unroll
-                for (int t = 0; t < SBV; ++t) h[t] = fmaf(dec, h[t], d[t]);
+                for (int cb = 0; cb < SBV; cb += kSl) {
+                    float d[kSl];
+                    if constexpr (kSl == 16)
+                        tmem_ld16(taddr + cb, d);
+                    else
+                        tmem_ld32(taddr + cb, d);
+#pragma unroll
+                    for (int t = 0; t < kSl; ++t) h[cb + t] = fmaf(dec, h[cb + t], d[t]);
+                }
                 tc_fence_before();
                 if (nxt) write_h();
             } else if (nxt) {
@@ -1476,22 +1476,21 @@ __global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
         // ------------------------------------- v' warps: v'_{c+1} = u_{c+1} - D1[0:64]
         const int row = (warp - 4) * 32 + lane;
         const uint32_t lanebase = (uint32_t)((warp - 4) * 32) << 16;
-        float u[SBV];
+        // u_{c+1} of this row, kept as packed bf16 pairs (the registers of 128-column
+        // CTAs), unpacked as v' is formed
+        uint32_t u2[SBV / 2];
 #pragma unroll
-        for (int t = 0; t < SBV; ++t) u[t] = 0.f;
+        for (int t = 0; t < SBV / 2; ++t) u2[t] = 0u;
         auto fetch = [&](int r) {
             wait_copy(&full[r % kStages], (r / kStages) & 1);
             if (r < ncs && !ident) {
 #pragma unroll
                 for (int blk = 0; blk < SBV / kUB; ++blk) {
-                    const unsigned char *ur = stage(r) + S::u + ((size_t)blk * 64 + row) * kUB * 2;
-                    float f[8];
-                    unpack8(*reinterpret_cast<const uint4 *>(ur), f);
-#pragma unroll
-                    for (int t = 0; t < 8; ++t) u[blk * kUB + t] = f[t];
-                    unpack8(*reinterpret_cast<const uint4 *>(ur + 16), f);
-#pragma unroll
-                    for (int t = 0; t < 8; ++t) u[blk * kUB + 8 + t] = f[t];
+                    const uint4 *ur = reinterpret_cast<const uint4 *>(
+                        stage(r) + S::u + ((size_t)blk * 64 + row) * kUB * 2);
+                    const uint4 a = ur[0], c = ur[1];
+                    u2[blk * 8 + 0] = a.x; u2[blk * 8 + 1] = a.y; u2[blk * 8 + 2] = a.z; u2[blk * 8 + 3] = a.w;
+                    u2[blk * 8 + 4] = c.x; u2[blk * 8 + 5] = c.y; u2[blk * 8 + 6] = c.z; u2[blk * 8 + 7] = c.w;
                 }
             }
             __syncwarp();
@@ -1501,14 +1500,21 @@ __global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
         for (int r = 0; r < ncs; ++r) {
             wait_mma(&bar_v[r & 1], (r >> 1) & 1);
             tc_fence_after();
-            float d[SBV];
-            tmem_ld_cols<SBV>(tmem + lanebase + (r & 1) * SBV, d);
+#pragma unroll
+            for (int cb = 0; cb < SBV; cb += 32) {
+                float d[32];
+                tmem_ld32(tmem + lanebase + (r & 1) * SBV + cb, d);
+#pragma unroll
+                for (int t = 0; t < 32; t += 2) {
+                    const uint32_t w = u2[(cb + t) / 2];
+                    d[t] = __uint_as_float(w << 16) - d[t];
+                    d[t + 1] = __uint_as_float(w & 0xffff0000u) - d[t + 1];
+                }
+#pragma unroll
+                for (int c = 0; c < 32; c += 8)
+                    *reinterpret_cast<uint4 *>(sVp + tile_off(row, cb + c, SBV)) = pack8_at(d + c);
+            }
             tc_fence_before();
-#pragma unroll
-            for (int t = 0; t < SBV; ++t) d[t] = u[t] - d[t];
-#pragma unroll
-            for (int c = 0; c < SBV; c += 8)
-                *reinterpret_cast<uint4 *>(sVp + tile_off(row, c, SBV)) = pack8_at(d + c);
             fence_async_smem();
             __syncwarp();
             named_arrive(kBarV, kThrV);
@@ -1524,31 +1530,32 @@ __global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
             if (r >= 1) {
                 wait_mma(&bar_v[r & 1], (r >> 1) & 1);
                 tc_fence_after();
-                float d[SBV];
-                tmem_ld_cols<SBV>(tmem + lanebase + (r & 1) * SBV, d);
-                tc_fence_before();
-#pragma unroll
-                for (int t = 0; t < SBV; ++t) d[t] *= p.scale;
                 const int c = c0 + r - 1;
-                if (!read_flag(&abort_flag)) {
-                    if (ident) {
-                        unsigned char *qt = static_cast<unsigned char *>(p.qc) +
-                                            ((gc0 + c) * p.HV + hv) * (int64_t)(64 * KK * 2);
+                const bool store = !read_flag(&abort_flag);
+                const int orow = bos + c * kBT + i;
+                unsigned char *qt = ident ? static_cast<unsigned char *>(p.qc) +
+                                                ((gc0 + c) * p.HV + hv) * (int64_t)(64 * KK * 2)
+                                          : nullptr;
+                __nv_bfloat16 *op = o + (((size_t)b * p.T + orow) * p.HV + hv) * p.V + vb * SBV;
+                // 32 columns at a time
 #pragma unroll
-                        for (int cc = 0; cc < SBV; cc += 8)
-                            *reinterpret_cast<uint4 *>(qt + tile_off(i, vb * SBV + cc, KK)) =
+                for (int cb = 0; cb < SBV; cb += 32) {
+                    float d[32];
+                    tmem_ld32(tmem + lanebase + (r & 1) * SBV + cb, d);
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) d[t] *= p.scale;
+                    if (store && ident) {
+#pragma unroll
+                        for (int cc = 0; cc < 32; cc += 8)
+                            *reinterpret_cast<uint4 *>(qt + tile_off(i, vb * SBV + cb + cc, KK)) =
                                 pack8_at(d + cc);
-                    } else {
-                        const int orow = bos + c * kBT + i;
-                        if (orow < eos) {
-                            __nv_bfloat16 *op =
-                                o + (((size_t)b * p.T + orow) * p.HV + hv) * p.V + vb * SBV;
+                    } else if (store && orow < eos) {
 #pragma unroll
-                            for (int cc = 0; cc < SBV; cc += 8)
-                                *reinterpret_cast<uint4 *>(op + cc) = pack8_at(d + cc);
-                        }
+                        for (int cc = 0; cc < 32; cc += 8)
+                            *reinterpret_cast<uint4 *>(op + cb + cc) = pack8_at(d + cc);
                     }
                 }
+                tc_fence_before();
             }
             // D1[r & 1] has been read: the MMA warp may overwrite it two rounds on.
             if (r < ncs) {
@@ -1922,9 +1929,14 @@ cudaError_t sm_count(int *out) {
 // of CTAs (one per SM), 64 columns halve the CTAs and the shared-memory traffic
 // per column, which wins (measured: -20% to -26% on multi-wave shapes).
 bool scan_wide(int64_t N, int HV, int V, int sms) { return V % 64 == 0 && N * HV * (V / 32) > sms; }
+// 128 columns per CTA once 64-column CTAs would not fit one wave of SMs: a round
+// then shares its operand tiles over twice the columns.
+bool scan_wider(int64_t N, int HV, int V, int sms) { return V % 128 == 0 && N * HV * (V / 64) > sms; }
 
 template <int KK, int VV>
 cudaError_t launch_scan_any(const ChunkArgs &a, cudaStream_t st, int sms) {
+    if constexpr (VV % 128 == 0)
+        if (scan_wider(a.N, a.HV, a.V, sms)) return launch_scan<KK, 128>(a, st);
     if constexpr (VV % 64 == 0)
         if (scan_wide(a.N, a.HV, a.V, sms)) return launch_scan<KK, 64>(a, st);
     return launch_scan<KK, 32>(a, st);
