@@ -106,6 +106,15 @@ def test_tensor_core_path_any_k_multiple_of_8(kda_lib, K, V, T, lens):
                 assert torch.equal(ht[n].view(torch.int32), inp["h0"][n].view(torch.int32))
 
 
+def test_wide_scan_two_ctas_per_head(kda_lib):
+    """128 value columns per scan CTA with two CTAs per (sequence, head): B=2, HV=48,
+    V=256 is 384 CTAs of 64 columns, more than one wave of SMs, and chunks with a
+    ragged tail (T=200)."""
+    inp = _small(77, B=2, T=200, H=16, HV=48, K=128, V=256)
+    o, ht = _run(kda_lib, inp)
+    _check(inp, o, ht, 2e-2, heads=[0, 7, 15])
+
+
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("K,V,T", [(64, 64, 1), (64, 16, 63), (128, 96, 64), (128, 256, 65),
                                    (64, 128, 200), (128, 40, 130), (128, 64, 100)])
