@@ -110,6 +110,12 @@ __device__ __forceinline__ bool continues(const ChunkArgs &p, int cl, int seq_ch
 // A prep launch's units: every chunk slot of every value head, or (a pipelined
 // launch's part, dense input) chunks [prep_c0, prep_c1) of every sequence.
 // Units run value head by value head, chunks in order within a sequence.
+// Index of the workspace unit of chunk slot gc and value head hv.  Head-major: a
+// head's consecutive chunks are adjacent, so the scan, which walks one head's
+// chunks, stays within a few memory pages instead of stepping HV units per round.
+__host__ __device__ __forceinline__ int64_t unit_index(const ChunkArgs &p, int64_t gc, int hv) {
+    return (int64_t)hv * p.slots + gc;
+}
 __host__ __device__ __forceinline__ int64_t prep_units(const ChunkArgs &p) {
     const int64_t per_hv = p.prep_c1 > p.prep_c0 ? (int64_t)p.B * (p.prep_c1 - p.prep_c0) : p.slots;
     return per_hv * p.HV;
@@ -484,7 +490,7 @@ __global__ void __launch_bounds__(256, 2)
     const bool halo = continues(p, cl, cur->ncs);  // the previous chunk's state feeds this one
     const bool carry = halo && prev_hv == hv && prev_gc == gc - 1;
     const int h = hv / (p.HV / p.H);
-    unsigned char *U = static_cast<unsigned char *>(p.units) + (gc * p.HV + hv) * Lo.stride;
+    unsigned char *U = static_cast<unsigned char *>(p.units) + unit_index(p, gc, hv) * Lo.stride;
 
     // ---- 1. the previous chunk's k rows when they are not carried over (the
     // run's first unit), 16-byte chunks into the swizzled kbx rows 64..127
@@ -1299,7 +1305,7 @@ __global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
                 if (cur) bytes += 64 * KK * 2 + 64 * KK * 2 + 64 * 64 * 2 + 512;
                 mbar_arrive_expect_tx(&full[s], bytes);
                 if (nxt) {
-                    const unsigned char *U1 = units + ((gc0 + c + 1) * p.HV + hv) * (int64_t)Lo.stride;
+                    const unsigned char *U1 = units + unit_index(p, gc0 + c + 1, hv) * (int64_t)Lo.stride;
                     bulk_g2s(st + S::top, U1 + Lo.aw, 64 * KK * 2, &full[s]);
                     if (!ident)
                         bulk_g2s(st + S::u, U1 + Lo.u + (size_t)vb * 64 * SBV * 2, 64 * SBV * 2,
@@ -1307,7 +1313,7 @@ __global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
                     if (cur) bulk_g2s(st + S::bot, U1 + Lo.mt, 64 * 64 * 2, &full[s]);
                 }
                 if (cur) {
-                    const unsigned char *U0 = units + ((gc0 + c) * p.HV + hv) * (int64_t)Lo.stride;
+                    const unsigned char *U0 = units + unit_index(p, gc0 + c, hv) * (int64_t)Lo.stride;
                     bulk_g2s(st + S::top + 64 * KK * 2, U0 + Lo.aw + 64 * KK * 2, 64 * KK * 2,
                              &full[s]);
                     bulk_g2s(st + S::kgt, U0 + Lo.kgt, 64 * KK * 2, &full[s]);
