@@ -31,6 +31,7 @@ __all__ = [
     "kda_gate_cumsum", "kda_chunk_fwd", "kda_recurrent_fwd", "kda_chunk_workspace_size",
     "kda_workspace_size",
     "kda_recurrent_bwd", "kda_recurrent_bwd_workspace_size", "recurrent_kda_backward", "kda_autograd",
+    "kda_chunk_bwd", "kda_chunk_bwd_workspace_size", "chunk_kda_backward",
     "kda_gate_cumsum_act", "kda_chunk_fwd_act", "kda_recurrent_fwd_act", "kda_recurrent_bwd_act",
     "kda_chunk_fwd_noalloc", "KDA_NOALLOC_SCRATCH_BYTES",
     "kda_read_device_status", "kda_clear_device_status", "kda_status_string",
@@ -46,6 +47,7 @@ KDA_FLAG_QK_L2NORM, KDA_FLAG_G_IS_CUMSUM, KDA_FLAG_SPLIT_SCAN = 1 << 0, 1 << 1, 
 KDA_FLAG_SERIAL = 1 << 3
 KDA_FLAG_TEST_WAIT_TIMEOUT = 1 << 31
 KDA_DEVICE_BAD_CU_SEQLENS, KDA_DEVICE_TIMEOUT, KDA_DEVICE_INTERNAL = 1 << 0, 1 << 1, 1 << 2
+KDA_DEVICE_GATE_RANGE = 1 << 3
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "_build", "libkda_gb300.so")
@@ -113,6 +115,9 @@ _SIGNATURES = {
                                     ctypes.POINTER(KdaActivation), _VP, _VP, _VP, _VP, _VP, _VP,
                                     _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP]),
     "kda_recurrent_bwd_workspace_size": (_SZ, [ctypes.POINTER(KdaShape)]),
+    "kda_chunk_bwd": (_ST, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.POINTER(KdaShape),
+                            _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP]),
+    "kda_chunk_bwd_workspace_size": (_SZ, [ctypes.POINTER(KdaShape)]),
     "kda_chunk_fwd_noalloc": (_ST, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.POINTER(KdaShape),
                                     _VP, _VP, _VP, _VP]),
     "kda_recurrent_fwd": (_ST, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.POINTER(KdaShape),
@@ -249,6 +254,19 @@ def kda_recurrent_bwd(q, k, v, g, beta, h0, cu_seqlens, shape: KdaShape, dout, d
                                     _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg), _ptr(dbeta),
                                     _ptr(dh0), _ptr(workspace), ws, _ptr(dev_status),
                                     _stream(stream)))
+
+
+def kda_chunk_bwd_workspace_size(shape: KdaShape) -> int:
+    return int(load().kda_chunk_bwd_workspace_size(ctypes.byref(shape)))
+
+
+def kda_chunk_bwd(q, k, v, g, beta, h0, cu_seqlens, shape: KdaShape, dout, dht, dq, dk, dv, dg,
+                  dbeta, dh0, workspace, dev_status=None, stream=None):
+    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().kda_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0),
+                                _ptr(cu_seqlens), ctypes.byref(shape), _ptr(dout), _ptr(dht),
+                                _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg), _ptr(dbeta), _ptr(dh0),
+                                _ptr(workspace), ws, _ptr(dev_status), _stream(stream)))
 
 
 def kda_recurrent_bwd_act(q, k, v, g, beta, h0, cu_seqlens, shape: KdaShape, act: KdaActivation,
@@ -448,6 +466,32 @@ def recurrent_kda_backward(q, k, v, gate, beta, dout, initial_state=None, dht=No
     else:
         kda_recurrent_bwd(q, k, v, g, beta, h0, cu, shape, dout, dht, out["dq"], out["dk"],
                           out["dv"], out["dg"], out["dbeta"], out["dh0"], ws, dev_status, stream)
+    return out
+
+
+def chunk_kda_backward(q, k, v, gate, beta, dout, initial_state=None, dht=None, *,
+                       cu_seqlens=None, scale=None, g_scale=1.0, want_dh0=True, dev_status=None,
+                       stream=None, workspace=None):
+    """The gradients recurrent_kda_backward returns (dq, dk, dv, dg, dbeta, dh0 as fp32),
+    computed by kda_chunk_bwd in the chunked form on the tensor cores (bf16 inputs,
+    K = V = 128).  `workspace`, if given, is a uint8 device tensor of at least
+    kda_chunk_bwd_workspace_size bytes."""
+    ts = [q, k, v, gate, beta, dout, initial_state, dht, cu_seqlens, dev_status, workspace]
+    _one_device(*ts)
+    q, k, v, g, beta, dout, h0, dht, cu = [
+        None if t is None else t.detach().contiguous() for t in ts[:9]]
+    shape = make_shape(q, v, cu, scale, g_scale, 0)
+    f32 = dict(dtype=torch.float32, device=q.device)
+    out = dict(dq=torch.empty(q.shape, **f32), dk=torch.empty(k.shape, **f32),
+               dv=torch.empty(v.shape, **f32), dg=torch.empty(g.shape, **f32),
+               dbeta=torch.empty(beta.shape, **f32),
+               dh0=(torch.empty(shape.num_seqs, shape.HV, shape.K, shape.V, **f32)
+                    if want_dh0 else None))
+    if workspace is None:
+        workspace = torch.empty(max(kda_chunk_bwd_workspace_size(shape), 256), dtype=torch.uint8,
+                                device=q.device)
+    kda_chunk_bwd(q, k, v, g, beta, h0, cu, shape, dout, dht, out["dq"], out["dk"], out["dv"],
+                  out["dg"], out["dbeta"], out["dh0"], workspace, dev_status, stream)
     return out
 
 

@@ -27,6 +27,7 @@ SOURCES = [
     "kda_cumsum.cu",
     "kda_chunk_simt.cu",
     "kda_chunk_tc.cu",
+    "kda_chunk_bwd.cu",
     "kda_profile.cu",
     "kda_noalloc.cu",
 ]

@@ -105,16 +105,18 @@ bool device_sm_count(int *out) {
     return true;
 }
 
-ChunkWs chunk_ws_layout(const kda_shape *s, bool packed) {
+// `bwd`: the units of kda_chunk_bwd's re-run of the forward (tensor-core path,
+// with the backward's extra tiles; never split).
+ChunkWs chunk_ws_layout(const kda_shape *s, bool packed, bool bwd = false) {
     ChunkWs L;
     L.slots = kda::chunk_slots(*s, packed);
-    L.unit_bytes = use_tc(s) ? kda::chunk_tc_unit_bytes(s->K, s->V)
+    L.unit_bytes = use_tc(s) ? kda::chunk_tc_unit_bytes(s->K, s->V, bwd)
                              : kda::chunk_simt_unit_bytes(s->K, s->V);
     L.ctrl = 0;
     L.chunk_start = 256;
     L.units = L.chunk_start + kda::align_up(sizeof(int32_t) * ((size_t)s->num_seqs + 1), 256);
     L.total = L.units + (size_t)L.slots * s->HV * L.unit_bytes;
-    L.split = (s->flags & KDA_FLAG_SPLIT_SCAN) && use_tc(s) &&
+    L.split = !bwd && (s->flags & KDA_FLAG_SPLIT_SCAN) && use_tc(s) &&
               kda::chunk_tc_split(s->num_seqs, s->HV, s->K, s->V, s->T);
     L.qc = L.e0 = L.e1 = L.pm = L.e0b = 0;
     L.pipe_m = 0;
@@ -138,6 +140,26 @@ ChunkWs chunk_ws_layout(const kda_shape *s, bool packed) {
         L.total = L.e0b + nh * s->K * s->V * 2;
     }
     return L;
+}
+
+// kda_chunk_bwd's workspace: the forward's (with the backward's unit tiles),
+// then per unit the checkpoints h_c ([K][V] bf16) and v'_c ([64][V]), and the
+// reverse scan's dL/dh_{c+1} ([K][V]) and dL/dv'_c ([64][V]).
+struct ChunkBwdWs {
+    ChunkWs f;
+    size_t ck_h, ck_vp, dhn, dvp, total;
+};
+ChunkBwdWs chunk_bwd_ws_layout(const kda_shape *s, bool packed) {
+    ChunkBwdWs W;
+    W.f = chunk_ws_layout(s, packed, true);
+    const size_t units = (size_t)W.f.slots * s->HV;
+    const size_t hb = (size_t)s->K * s->V * 2, vb = (size_t)64 * s->V * 2;
+    W.ck_h = kda::align_up(W.f.total, 256);
+    W.ck_vp = W.ck_h + units * hb;
+    W.dhn = W.ck_vp + units * vb;
+    W.dvp = W.dhn + units * hb;
+    W.total = W.dvp + units * vb;
+    return W;
 }
 
 // kda_activation -> the kernels' GateAct, with its argument checks.
@@ -445,6 +467,99 @@ kda_status kda_chunk_fwd_act(const void *q, const void *k, const void *v, const 
     return KDA_OK;
 }
 
+size_t kda_chunk_bwd_workspace_size(const kda_shape *shape) {
+    if (!shape || shape->K <= 0 || shape->V <= 0 || shape->HV <= 0 || shape->B <= 0 ||
+        shape->T < 0 || shape->num_seqs < 0)
+        return 0;
+    // sized for packed input when the shape may be packed: it covers a dense call too
+    const bool packed = shape->num_seqs != shape->B || shape->B == 1;
+    return chunk_bwd_ws_layout(shape, packed).total;
+}
+
+kda_status kda_chunk_bwd(const void *q, const void *k, const void *v, const float *g,
+                         const void *beta, const float *h0, const int32_t *cu_seqlens,
+                         const kda_shape *shape, const void *dout, const float *dht, float *dq,
+                         float *dk, float *dv, float *dg, float *dbeta, float *dh0,
+                         void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                         kda_stream_t stream) {
+    const char *op = "kda_chunk_bwd";
+    kda_status st = check_common(op, shape, cu_seqlens);
+    if (st != KDA_OK) return st;
+    if (shape->dtype != KDA_DTYPE_BF16 || !kda::chunk_bwd_tc_supported(shape->K, shape->V))
+        return fail(KDA_ERR_UNSUPPORTED, "%s: bf16 inputs with K = V = 128 only (got dtype %d, "
+                    "K=%d, V=%d); kda_recurrent_bwd takes the rest", op, (int)shape->dtype,
+                    shape->K, shape->V);
+    if (shape->flags & ~(uint32_t)KDA_FLAG_SERIAL)
+        return fail(KDA_ERR_UNSUPPORTED, "%s: flags 0x%x (only KDA_FLAG_SERIAL is taken; the "
+                    "q/k L2 norm and a cumsummed gate go through kda_recurrent_bwd)", op,
+                    shape->flags);
+    const bool has_rows = (int64_t)shape->B * shape->T > 0;
+    if (has_rows && (!q || !k || !v || !g || !beta || !dout || !dq || !dk || !dv || !dg || !dbeta))
+        return fail(KDA_ERR_INVALID_ARG, "%s: inputs, dout and dq, dk, dv, dg, dbeta must be "
+                    "non-NULL", op);
+    const bool packed = cu_seqlens != nullptr;
+    const ChunkBwdWs W = chunk_bwd_ws_layout(shape, packed);
+    if (W.f.slots > INT_MAX) return fail(KDA_ERR_UNSUPPORTED, "%s: too many chunks", op);
+    const size_t need = kda_chunk_bwd_workspace_size(shape);
+    if (!workspace || workspace_bytes < need)
+        return fail(KDA_ERR_INVALID_ARG, "%s: workspace of %zu bytes needed, %zu given", op, need,
+                    workspace_bytes);
+    if ((uintptr_t)workspace % 256 != 0)
+        return fail(KDA_ERR_INVALID_ARG, "%s: workspace must be 256-byte aligned", op);
+    const void *ptrs[] = {q, k, v, g, h0, dout, dht, dq, dk, dv, dg, dh0};
+    for (const void *ptr : ptrs)
+        if ((uintptr_t)ptr % 16 != 0)
+            return fail(KDA_ERR_INVALID_ARG, "%s: tensors must be 16-byte aligned", op);
+
+    char *ws = static_cast<char *>(workspace);
+    kda::ChunkArgs a;
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.h0 = h0; a.cu = cu_seqlens;
+    a.o = nullptr; a.ht = nullptr; a.status = dev_status;
+    a.B = shape->B; a.T = shape->T; a.H = shape->H; a.HV = shape->HV; a.K = shape->K;
+    a.V = shape->V; a.N = shape->num_seqs;
+    a.scale = resolve_scale(shape);
+    a.g_scale = shape->g_scale;
+    a.l2norm = 0;
+    a.g_is_cumsum = 0;
+    a.test_timeout = 0;
+    a.act = kda::GateAct();
+    a.ctrl = reinterpret_cast<kda::ChunkCtrl *>(ws + W.f.ctrl);
+    a.chunk_start = reinterpret_cast<int32_t *>(ws + W.f.chunk_start);
+    a.units = ws + W.f.units;
+    a.slots = W.f.slots;
+    a.split = 0;
+    a.qc = nullptr; a.e1 = nullptr; a.pm = nullptr; a.e0b = nullptr;
+    a.pipe = (!packed && W.f.pipe_m > 0) ? 1 : 0;
+    a.pipe_m = a.pipe ? W.f.pipe_m : 0;
+    a.e0 = a.pipe ? reinterpret_cast<float *>(ws + W.f.e0) : nullptr;
+    a.prep_c0 = a.prep_c1 = 0;
+    a.scan_seg = 0;
+    a.bwd = 1;
+    a.ck_h = ws + W.ck_h;
+    a.ck_vp = ws + W.ck_vp;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaSuccess;
+    if (packed) {
+        e = kda::launch_validate_offsets(cu_seqlens, a.N, a.T, dev_status, a.ctrl, a.chunk_start, s);
+        if (e != cudaSuccess) return cuda_fail(e, op);
+    }
+    // dq, dk accumulate; with packed sequences rows outside every sequence stay zero
+    const size_t rows = (size_t)shape->B * shape->T;
+    const size_t zero[][2] = {{(size_t)dq, rows * shape->H * shape->K * 4},
+                              {(size_t)dk, rows * shape->H * shape->K * 4},
+                              {(size_t)dv, packed ? rows * shape->HV * shape->V * 4 : 0},
+                              {(size_t)dg, packed ? rows * shape->HV * shape->K * 4 : 0},
+                              {(size_t)dbeta, packed ? rows * shape->HV * 4 : 0}};
+    for (const auto &z : zero)
+        if (z[1] && (e = cudaMemsetAsync(reinterpret_cast<void *>(z[0]), 0, z[1], s)) != cudaSuccess)
+            return cuda_fail(e, op);
+    e = kda::launch_chunk_bwd_tc(a, dout, dht, dq, dk, dv, dg, dbeta, dh0, ws + W.dhn, ws + W.dvp, s);
+    if (e != cudaSuccess) return cuda_fail(e, op);
+    g_last_error.clear();
+    return KDA_OK;
+}
+
 kda_status kda_read_device_status(const int32_t *dev_status, int32_t *host_bits,
                                   kda_stream_t stream) {
     if (!dev_status) return fail(KDA_ERR_INVALID_ARG, "kda_read_device_status: NULL status word");
@@ -458,6 +573,9 @@ kda_status kda_read_device_status(const int32_t *dev_status, int32_t *host_bits,
         return fail(KDA_ERR_BAD_CU_SEQLENS, "device reported invalid cu_seqlens");
     if (bits & KDA_DEVICE_TIMEOUT)
         return fail(KDA_ERR_TIMEOUT, "a bounded device-side wait timed out");
+    if (bits & KDA_DEVICE_GATE_RANGE)
+        return fail(KDA_ERR_UNSUPPORTED, "kda_chunk_bwd: a chunk's gate range exceeds what the "
+                    "chunked backward takes (its gradients were not computed)");
     if (bits & KDA_DEVICE_INTERNAL)
         return fail(KDA_ERR_CUDA, "a kernel found an internal launch invariant broken");
     return KDA_OK;

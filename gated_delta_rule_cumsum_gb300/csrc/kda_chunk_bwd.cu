@@ -1,0 +1,1003 @@
+// kda_chunk_bwd.cu -- chunked KDA backward for bf16 inputs on the sm_103a tensor
+// cores (tcgen05.mma with accumulators in tensor memory, bulk async copies).
+//
+// kernel-fun 0.2.0.dev1 sdist, ALGORITHM.md, "Backward" (the seven launches:
+// recompute, re-scan, dAv, dhu, wy_dqkg, intra, dg cumsum), per value head and
+// chunk of BT = 64 rows, g2 the chunk-local cumsum of g_scale g (log2), G its
+// last row, qg = q 2^g2, kg = k 2^(G - g2), kp = k 2^g2, kn = k 2^-g2, Aqk the
+// unscaled q-k gram (o = scale (qg h + Aqk v')), Akk = (I + L)^-1 with
+// L = diag(beta) strictly_tril(kp kn^T) =: diag(beta) P, w = Akk diag(beta) kp:
+//
+//   1, 2  the forward's prep and scan run again and also store, per unit, w and
+//         Akk (prep) and the state h_c at the start of the chunk and v'_c (scan);
+//   4     dhu, one CTA per (sequence, value head, 32 value columns), chunks in
+//         reverse (chunk_dhu_tc_kernel):
+//           dv'_c = scale Aqk^T do_c + kg_c dh_{c+1}
+//           dh_c  = 2^G dh_{c+1} + scale qg_c^T do_c - w_c^T dv'_c
+//         storing dh_{c+1} and dv'_c per unit;
+//   3, 5, 6, 7  one CTA per (chunk, value head), all in parallel
+//         (chunk_bwd_unit_tc_kernel): with dA = scale tril(do v'^T)
+//           dq  = scale (do h^T) 2^g2 + (dA kn) 2^g2
+//           dk  = (v' dh^T) 2^(G - g2) + diag(beta) (Akk^T dw) 2^g2
+//                 + (dP kn) 2^g2 + (dP^T kp + dA^T qp) 2^-g2,   dw = -dv' h^T
+//           dv  = diag(beta) Akk^T dv'
+//           dP  = diag(beta) dL,  dL = -strictly_tril(Akk^T dAkk Akk^T),
+//           dAkk = (dv' v^T + dw kp^T) diag(beta)
+//           dbeta = rowsum(Akk^T dv' . v) + rowsum(Akk^T dw . kp) + rowsum(dL . P)
+//           dg2 = ln2 [ scale (do h^T) . qg - (v' dh^T) . kg + diag(beta)(Akk^T dw) . kp
+//                      + (dP kn) . kp + (dA kn) . qp - (dP^T kp + dA^T qp) . kn ]
+//                 plus, on the last row, ln2 2^G rowsum(h . dh_{c+1}) + ln2 colsum((v' dh^T) . kg)
+//           dg  = g_scale x the reverse cumsum of dg2 over the chunk's rows.
+//         The gated grams are split through the chunk start (kp, kn), as in the
+//         forward's prep; chunks whose gate range max |g2| exceeds kBwdRange are not
+//         computed and raise KDA_DEVICE_GATE_RANGE.
+#include "kda_internal.cuh"
+#include "kda_tc.cuh"
+#include "kda_chunk_layout.cuh"
+
+namespace kda {
+namespace {
+
+using namespace tc;
+
+constexpr float kLn2 = 0.69314718055994531f;
+// Largest chunk gate range (log2) the split grams of the backward take: kn reaches
+// 2^range, and its products with dP stay well inside fp32.
+constexpr float kBwdRange = 100.f;
+
+__device__ __forceinline__ int read_flag(const int *f) {
+    return *reinterpret_cast<const volatile int *>(f);
+}
+__device__ __forceinline__ void named_arrive(int id, int nthreads) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
+
+// ============================================================== dhu kernel
+// Rounds i = 0 .. nc - 1 of one (sequence, value head, SBV value columns) take the
+// chunks c = nc - 1 - i in reverse.  dh_{c+1} (fp32, thread d of the dh warps owns
+// row d) enters as a bf16 operand tile; per round
+//   D1a = Aqk_c^T do_c,  D2a = qg_c^T do_c     (off the chain, issued first)
+//   D1b = kg_c dh_{c+1}                         ->  dv'_c = scale D1a + D1b
+//   D2b = w_c^T dv'_c                           ->  dh_c = 2^G_c dh_{c+1} + scale D2a - D2b
+// Aqk, qg and w are read as MN-major operands of the tiles the forward stored.
+template <int KK, int SBV>
+struct DhuSmem {
+    static constexpr int kStages = 3;
+    static constexpr uint32_t kg = 0;                        // [64][KK] kg_c
+    static constexpr uint32_t wq = kg + 64 * KK * 2;         // [128][KK]: w_c; qg_c
+    static constexpr uint32_t aqk = wq + 128 * KK * 2;       // [64][64] Aqk_c
+    static constexpr uint32_t dec = aqk + 64 * 64 * 2;       // [128] fp32 2^G_c
+    static constexpr uint32_t stage = dec + 512;
+    static constexpr uint32_t stage_stride = (stage + 1023) / 1024 * 1024;
+    static constexpr uint32_t dh = kStages * stage_stride;   // [KK][SBV] bf16 tile
+    static constexpr uint32_t dout = dh + KK * SBV * 2;      // two [64][SBV] tiles
+    static constexpr uint32_t dvp = dout + 2 * 64 * SBV * 2; // [64][SBV] tile
+    static constexpr uint32_t total = dvp + 64 * SBV * 2;
+    // TMEM columns: D1a at 0 / SBV, D1b at 2 SBV, D2a at 3 SBV / 4 SBV, D2b at 5 SBV.
+    static constexpr uint32_t tmem_cols = 6 * SBV <= 256 ? 256 : 512;
+};
+constexpr int kDhuBarH = 1;  // dh_{c+1} written: the 4 dh warps arrive, the MMA warp syncs
+constexpr int kDhuBarV = 2;  // dv'_c written: the 4 dv' warps arrive, the MMA warp syncs
+
+struct BwdArgs {
+    ChunkArgs c;           // the forward's arguments, bwd set, its checkpoints
+    const void *dout;      // [B,T,HV,V] bf16
+    const float *dht;      // [N,HV,K,V] or null
+    float *dq, *dk;        // [B,T,H,K], accumulated (zeroed first)
+    float *dv, *dg;        // [B,T,HV,V], [B,T,HV,K]
+    float *dbeta;          // [B,T,HV]
+    float *dh0;            // [N,HV,K,V] or null
+    void *dhn, *dvp;       // per unit: [K][V] tile dL/dh_{c+1}, [64][V] tile dL/dv'_c
+};
+
+// Warp roles: 0..3 dh (rows 32 w .. 32 w + 31), 4..7 dv' (M = 64 rows 16 (w % 4) ..
+// + 15 in TMEM lanes 32 (w % 4) .. + 15) and the do tiles, 8 bulk copies, 9 MMA issue.
+template <int KK, int SBV>
+__global__ void __launch_bounds__(320, 1) chunk_dhu_tc_kernel(BwdArgs a) {
+    using S = DhuSmem<KK, SBV>;
+    constexpr int kStages = S::kStages;
+    const ChunkArgs &p = a.c;
+    extern __shared__ __align__(1024) unsigned char sm[];
+    __shared__ uint64_t full[kStages], empty[kStages], do_full[2], bar_d1, bar_d2, bar_fin;
+    __shared__ uint32_t tslot;
+    __shared__ int abort_flag;
+
+    const int nvb = p.V / SBV;
+    const int vb = (int)(blockIdx.x % nvb);
+    const int hv = (int)((blockIdx.x / nvb) % p.HV);
+    const int n = (int)(blockIdx.x / ((int64_t)nvb * p.HV));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    int b, bos, eos, nc;
+    int64_t gc0;
+    if (p.cu) {
+        if (!p.ctrl->valid) return;
+        b = 0;
+        bos = p.cu[n];
+        eos = p.cu[n + 1];
+        nc = (eos - bos + kBT - 1) / kBT;
+        gc0 = p.chunk_start[n];
+    } else {
+        b = n;
+        bos = 0;
+        eos = p.T;
+        nc = (p.T + kBT - 1) / kBT;
+        gc0 = (int64_t)n * nc;
+    }
+    const TcLayout Lo = tc_layout(KK, p.V, true);
+    const unsigned char *units = static_cast<const unsigned char *>(p.units);
+
+    if (warp == 0) {
+        tmem_alloc(&tslot, S::tmem_cols);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1 + 4);  // MMA commit + the dh warps (they read 2^G)
+        }
+        mbar_init(&do_full[0], 4);
+        mbar_init(&do_full[1], 4);
+        mbar_init(&bar_d1, 1);
+        mbar_init(&bar_d2, 1);
+        mbar_init(&bar_fin, 1);
+        mbar_fence_init();
+        abort_flag = 0;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tslot;
+    unsigned char *sDh = sm + S::dh;
+    unsigned char *sDo = sm + S::dout;
+    unsigned char *sDvp = sm + S::dvp;
+    auto fail = [&]() {
+        atomicExch(&abort_flag, 1);
+        report(p.status, KDA_DEVICE_TIMEOUT);
+    };
+    auto wait_copy = [&](uint64_t *bar, uint32_t parity) {
+        if (read_flag(&abort_flag)) return;
+        if (!mbar_wait(bar, parity, kWaitNs)) fail();
+    };
+    auto wait_mma = [&](uint64_t *bar, uint32_t parity) {
+        if (!mbar_wait(bar, parity, kWaitNs)) fail();
+    };
+    auto stage = [&](int i) { return sm + (i % kStages) * S::stage_stride; };
+    auto uidx = [&](int c) { return unit_index(p, gc0 + c, hv); };
+
+    if (warp == 8) {
+        // ------------------------------------------------------- producer
+        if (lane == 0) {
+            int issued = 0;
+            for (int i = 0; i < nc; ++i) {
+                const int s = i % kStages;
+                if (i >= kStages) wait_copy(&empty[s], ((i / kStages) - 1) & 1);
+                if (read_flag(&abort_flag)) break;
+                unsigned char *st = stage(i);
+                const unsigned char *U = units + uidx(nc - 1 - i) * (int64_t)Lo.stride;
+                mbar_arrive_expect_tx(&full[s], 3 * 64 * KK * 2 + 64 * 64 * 2 + 512);
+                bulk_g2s(st + S::kg, U + Lo.kgt, 64 * KK * 2, &full[s]);
+                bulk_g2s(st + S::wq, U + Lo.wb, 64 * KK * 2, &full[s]);
+                bulk_g2s(st + S::wq + 64 * KK * 2, U + Lo.aw + 64 * KK * 2, 64 * KK * 2, &full[s]);
+                bulk_g2s(st + S::aqk, U + Lo.aqk, 64 * 64 * 2, &full[s]);
+                bulk_g2s(st + S::dec, U + Lo.dec, 512, &full[s]);
+                issued = i + 1;
+            }
+            for (int i = issued - kStages > 0 ? issued - kStages : 0; i < issued; ++i)
+                mbar_wait(&full[i % kStages], (i / kStages) & 1, kWaitNs);
+        }
+    } else if (warp == 9) {
+        // ----------------------------------------------------- MMA issuer
+        const uint32_t id_d1a = idesc_bf16(64, SBV, true, true);    // Aqk^T (MN-major), do
+        const uint32_t id_d1b = idesc_bf16(64, SBV, false, true);   // kg (K-major), dh
+        const uint32_t id_d2 = idesc_bf16(128, SBV, true, true);    // qg^T / w^T, do / dv'
+        constexpr uint32_t binc = 2 * SBV * 16 / 16;
+        const uint64_t ddh = sdesc(smem_addr(sDh), SBV * 16, 128);
+        const uint64_t ddv = sdesc(smem_addr(sDvp), SBV * 16, 128);
+        for (int i = 0; i < nc; ++i) {
+            const int s = i % kStages;
+            const uint32_t st = smem_addr(stage(i));
+            const uint64_t ddo = sdesc(smem_addr(sDo) + (i & 1) * 64 * SBV * 2, SBV * 16, 128);
+            wait_copy(&full[s], (i / kStages) & 1);
+            wait_copy(&do_full[i & 1], (i >> 1) & 1);
+            __syncwarp();
+            bool go = !read_flag(&abort_flag);
+            if (elect_one()) {
+                tc_fence_after();
+                if (go) {
+                    mma_bf16_seq<4, false>(tmem + (i & 1) * SBV, sdesc(st + S::aqk, 64 * 16, 128),
+                                           2 * 64 * 16 / 16, ddo, binc, id_d1a);
+                    mma_bf16_seq<4, false>(tmem + (3 + (i & 1)) * SBV,
+                                           sdesc(st + S::wq + 64 * KK * 2, KK * 16, 128),
+                                           2 * KK * 16 / 16, ddo, binc, id_d2);
+                }
+            }
+            __syncwarp();
+            named_sync(kDhuBarH, 128 + 32);
+            go = !read_flag(&abort_flag);
+            if (elect_one()) {
+                tc_fence_after();
+                if (go)
+                    mma_bf16_seq<KK / 16, false>(tmem + 2 * SBV, sdesc(st + S::kg, 128, KK * 16), 16,
+                                                 ddh, binc, id_d1b);
+                mma_commit(&bar_d1);
+            }
+            __syncwarp();
+            named_sync(kDhuBarV, 128 + 32);
+            go = !read_flag(&abort_flag);
+            if (elect_one()) {
+                tc_fence_after();
+                if (go)
+                    mma_bf16_seq<4, false>(tmem + 5 * SBV, sdesc(st + S::wq, KK * 16, 128),
+                                           2 * KK * 16 / 16, ddv, binc, id_d2);
+                mma_commit(&bar_d2);
+                mma_commit(&empty[s]);
+            }
+            __syncwarp();
+        }
+        if (elect_one()) {
+            mma_commit(&bar_fin);
+            mbar_wait(&bar_fin, 0, kWaitNs);
+        }
+        __syncwarp();
+    } else if (warp < 4) {
+        // ------------------------------------------ dh warps: the state gradient
+        const int row = warp * 32 + lane;
+        const bool glob_row = row < p.K;
+        const uint32_t lanebase = (uint32_t)(warp * 32) << 16;
+        float dh[SBV];
+#pragma unroll
+        for (int j = 0; j < SBV; ++j) dh[j] = 0.f;
+        if (a.dht && glob_row) {
+            const float4 *src = reinterpret_cast<const float4 *>(
+                a.dht + (((size_t)n * p.HV + hv) * p.K + row) * (size_t)p.V + (size_t)vb * SBV);
+#pragma unroll
+            for (int j = 0; j < SBV / 4; ++j) {
+                const float4 x = src[j];
+                dh[4 * j] = x.x; dh[4 * j + 1] = x.y; dh[4 * j + 2] = x.z; dh[4 * j + 3] = x.w;
+            }
+        }
+        for (int i = 0; i < nc; ++i) {
+            const int c = nc - 1 - i;
+            // dh_{c+1}: the D1b operand and chunk c's dL/dh_{c+1} tile
+            unsigned char *t = static_cast<unsigned char *>(a.dhn) +
+                               uidx(c) * (int64_t)(KK * p.V * 2);
+#pragma unroll
+            for (int cc = 0; cc < SBV; cc += 8) {
+                const uint4 v8 = pack8_at(dh + cc);
+                *reinterpret_cast<uint4 *>(sDh + tile_off(row, cc, SBV)) = v8;
+                *reinterpret_cast<uint4 *>(t + tile_off(row, vb * SBV + cc, p.V)) = v8;
+            }
+            fence_async_smem();
+            __syncwarp();
+            named_arrive(kDhuBarH, 128 + 32);
+            float dec = 0.f;
+            wait_copy(&full[i % kStages], (i / kStages) & 1);
+            if (!read_flag(&abort_flag)) dec = reinterpret_cast<const float *>(stage(i) + S::dec)[row];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[i % kStages]);
+            wait_mma(&bar_d2, i & 1);
+            tc_fence_after();
+            float d2a[SBV], d2b[SBV];
+            if constexpr (SBV == 32) {
+                tmem_ld32(tmem + lanebase + (3 + (i & 1)) * SBV, d2a);
+                tmem_ld32(tmem + lanebase + 5 * SBV, d2b);
+            } else {
+                tmem_ld16(tmem + lanebase + (3 + (i & 1)) * SBV, d2a);
+                tmem_ld16(tmem + lanebase + 5 * SBV, d2b);
+            }
+#pragma unroll
+            for (int j = 0; j < SBV; ++j) dh[j] = fmaf(dec, dh[j], fmaf(p.scale, d2a[j], -d2b[j]));
+            tc_fence_before();
+        }
+        if (a.dh0 && glob_row && !read_flag(&abort_flag)) {
+            float4 *dst = reinterpret_cast<float4 *>(
+                a.dh0 + (((size_t)n * p.HV + hv) * p.K + row) * (size_t)p.V + (size_t)vb * SBV);
+#pragma unroll
+            for (int j = 0; j < SBV / 4; ++j)
+                dst[j] = make_float4(dh[4 * j], dh[4 * j + 1], dh[4 * j + 2], dh[4 * j + 3]);
+        }
+    } else {
+        // ------------------------------------- dv' warps: dv'_c = scale D1a + D1b
+        const int q = warp & 3, t128 = tid - 128;
+        const int r = 16 * q + (lane & 15);
+        const uint32_t lanebase = (uint32_t)(32 * q) << 16;
+        const __nv_bfloat16 *dout = static_cast<const __nv_bfloat16 *>(a.dout);
+        // do rows of chunk c into tile buf: 64 rows x SBV / 8 pieces of 16 bytes
+        auto load_do = [&](int c, int buf) {
+            const int row0 = bos + c * kBT;
+            const int nr = min(kBT, eos - row0);
+            unsigned char *dst = sDo + buf * 64 * SBV * 2;
+            for (int pc = t128; pc < 64 * (SBV / 8); pc += 128) {
+                const int rr = pc / (SBV / 8), ch = (pc % (SBV / 8)) * 8;
+                uint4 x = make_uint4(0, 0, 0, 0);
+                if (rr < nr)
+                    x = *reinterpret_cast<const uint4 *>(
+                        dout + (((size_t)b * p.T + row0 + rr) * p.HV + hv) * p.V + vb * SBV + ch);
+                *reinterpret_cast<uint4 *>(dst + tile_off(rr, ch, SBV)) = x;
+            }
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&do_full[buf]);
+        };
+        if (nc > 0) load_do(nc - 1, 0);
+        for (int i = 0; i < nc; ++i) {
+            const int c = nc - 1 - i;
+            wait_mma(&bar_d1, i & 1);
+            tc_fence_after();
+            float d1a[SBV], d1b[SBV];
+            if constexpr (SBV == 32) {
+                tmem_ld32(tmem + lanebase + (i & 1) * SBV, d1a);
+                tmem_ld32(tmem + lanebase + 2 * SBV, d1b);
+            } else {
+                tmem_ld16(tmem + lanebase + (i & 1) * SBV, d1a);
+                tmem_ld16(tmem + lanebase + 2 * SBV, d1b);
+            }
+            tc_fence_before();
+            if (lane < 16) {
+                unsigned char *t = static_cast<unsigned char *>(a.dvp) +
+                                   uidx(c) * (int64_t)(64 * p.V * 2);
+#pragma unroll
+                for (int j = 0; j < SBV; ++j) d1a[j] = fmaf(p.scale, d1a[j], d1b[j]);
+#pragma unroll
+                for (int cc = 0; cc < SBV; cc += 8) {
+                    const uint4 v8 = pack8_at(d1a + cc);
+                    *reinterpret_cast<uint4 *>(sDvp + tile_off(r, cc, SBV)) = v8;
+                    *reinterpret_cast<uint4 *>(t + tile_off(r, vb * SBV + cc, p.V)) = v8;
+                }
+            }
+            fence_async_smem();
+            __syncwarp();
+            named_arrive(kDhuBarV, 128 + 32);
+            // the other do tile was last read by round i - 1's MMAs, complete once
+            // bar_d1 of round i fired
+            if (i + 1 < nc) load_do(c - 1, (i + 1) & 1);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, S::tmem_cols);
+}
+
+// ============================================================ unit kernel
+// Shared memory of one (chunk, value head) unit.  Operand tiles in the no-swizzle
+// core-matrix layout (tile_off); g2 fp32 with 16-byte column groups XORed by row.
+template <int KK, int VV>
+struct UnitSmem {
+    static constexpr uint32_t g2 = 0;                         // fp32 [64][KK]
+    static constexpr uint32_t kp = g2 + 64 * KK * 4;          // [64][KK] k 2^g2
+    static constexpr uint32_t kn = kp + 64 * KK * 2;          // [64][KK] k 2^-g2
+    static constexpr uint32_t qp = kn + 64 * KK * 2;          // [64][KK] q 2^g2
+    static constexpr uint32_t vt = qp + 64 * KK * 2;          // [64][VV] v
+    static constexpr uint32_t akk = vt + 64 * VV * 2;         // [64][64] Akk
+    static constexpr uint32_t dout = akk + 64 * 64 * 2;       // [64][VV] do; later [dP; dA] [128][64]
+    static constexpr uint32_t dvp = dout + 64 * VV * 2;       // [64][VV] dv' (right below do)
+    static constexpr uint32_t vp = dvp + 64 * VV * 2;         // [64][VV] v'
+    static constexpr uint32_t h = vp + 64 * VV * 2;           // [KK][VV] h_c
+    static constexpr uint32_t dhn = h + KK * VV * 2;          // [KK][VV] dh_{c+1}
+    static constexpr uint32_t misc = dhn + KK * VV * 2;
+    // once h and dh_{c+1} have been read
+    static constexpr uint32_t dg2 = h;                        // fp32 [64][KK]
+    static constexpr uint32_t dakk = dg2 + 64 * KK * 4;       // [64][64]
+    static constexpr uint32_t xt = dakk + 64 * 64 * 2;        // [64][64] Akk^T dAkk
+    static constexpr uint32_t dw = xt + 64 * 64 * 2;          // [64][KK]
+    static constexpr uint32_t dap = dout;                     // [128][64]: dP; dA
+    static constexpr uint32_t beta = misc;                    // fp32 [64]
+    static constexpr uint32_t gl = beta + 64 * 4;             // fp32 [KK]: G
+    static constexpr uint32_t dG = gl + KK * 4;               // fp32 [KK]
+    static constexpr uint32_t dbeta = dG + KK * 4;            // fp32 [64]
+    static constexpr uint32_t total = dbeta + 64 * 4;
+    static_assert(dw + 64 * KK * 2 <= misc, "phase-two tiles fit over h and dh");
+    static_assert(128 * 64 * 2 <= 64 * VV * 2, "[dP; dA] fits over do");
+};
+
+template <int W>
+__device__ __forceinline__ int fsw(int r, int c) {
+    return r * W + ((((c >> 2) ^ r) & 7) | ((c >> 2) & ~7)) * 4 + (c & 3);
+}
+__device__ __forceinline__ float ex2f(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ void unpack8(const unsigned char *p, float (&f)[8]) {
+    unpack8(*reinterpret_cast<const uint4 *>(p), f);
+}
+// fp32 accumulation into a gradient in global memory (several CTAs may add to
+// the same q / k row when value heads share it).
+__device__ __forceinline__ void add8(float *dst, const float (&x)[8]) {
+    atomicAdd(reinterpret_cast<float4 *>(dst), make_float4(x[0], x[1], x[2], x[3]));
+    atomicAdd(reinterpret_cast<float4 *>(dst + 4), make_float4(x[4], x[5], x[6], x[7]));
+}
+
+// One CTA per (chunk, value head).  Epilogue threads read accumulators with
+// 32-lane TMEM loads: for an M = 128 result, warp w reaches rows 32 (w % 4) .. + 31,
+// warps w and w + 4 take one half of the columns each; for an M = 64 result row r
+// sits in lane 32 (r / 16) + r % 16, so lanes 0..15 of every warp hold a row.
+template <int KK, int VV>
+__global__ void __launch_bounds__(256, 1) chunk_bwd_unit_tc_kernel(BwdArgs a) {
+    using S = UnitSmem<KK, VV>;
+    const ChunkArgs &p = a.c;
+    extern __shared__ __align__(1024) unsigned char sm[];
+    __shared__ uint64_t bar_ld, bar_mma;
+    __shared__ uint32_t tslot;
+    __shared__ int range_bad;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, quad = warp & 3, half = warp >> 2;
+    const int64_t unit = blockIdx.x;
+    const int hv = (int)(unit / p.slots);
+    const int64_t gc = unit % p.slots;
+    int b, row0, nr, cl;
+    if (!locate_chunk(p, gc, b, row0, nr, cl)) return;
+    const int hq = hv / (p.HV / p.H);
+    const TcLayout Lo = tc_layout(KK, VV, true);
+    const int64_t ui = unit_index(p, gc, hv);
+
+    float *sG = reinterpret_cast<float *>(sm + S::g2);
+    float *sBeta = reinterpret_cast<float *>(sm + S::beta);
+    float *sGl = reinterpret_cast<float *>(sm + S::gl);
+    float *sDG = reinterpret_cast<float *>(sm + S::dG);
+    float *sDbeta = reinterpret_cast<float *>(sm + S::dbeta);
+    float *sDg2 = reinterpret_cast<float *>(sm + S::dg2);
+
+    if (warp == 0) {
+        tmem_alloc(&tslot, 512);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        mbar_init(&bar_ld, 1);
+        mbar_init(&bar_mma, 1);
+        mbar_fence_init();
+        range_bad = 0;
+        // the forward's and the dhu's tiles of this unit
+        mbar_arrive_expect_tx(&bar_ld, 2 * KK * VV * 2 + 2 * 64 * VV * 2 + 64 * 64 * 2);
+        bulk_g2s(sm + S::h, static_cast<const unsigned char *>(p.ck_h) + ui * (int64_t)(KK * VV * 2),
+                 KK * VV * 2, &bar_ld);
+        bulk_g2s(sm + S::dhn, static_cast<const unsigned char *>(a.dhn) + ui * (int64_t)(KK * VV * 2),
+                 KK * VV * 2, &bar_ld);
+        bulk_g2s(sm + S::vp, static_cast<const unsigned char *>(p.ck_vp) + ui * (int64_t)(64 * VV * 2),
+                 64 * VV * 2, &bar_ld);
+        bulk_g2s(sm + S::dvp, static_cast<const unsigned char *>(a.dvp) + ui * (int64_t)(64 * VV * 2),
+                 64 * VV * 2, &bar_ld);
+        bulk_g2s(sm + S::akk, static_cast<const unsigned char *>(p.units) + ui * (int64_t)Lo.stride + Lo.akk,
+                 64 * 64 * 2, &bar_ld);
+    }
+    // g rows (fp32), beta, v and do rows
+    const size_t rowbase = (size_t)b * p.T + row0;
+    for (int pc = tid; pc < 64 * (KK / 4); pc += 256) {
+        const int r = pc / (KK / 4), c = (pc % (KK / 4)) * 4;
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (r < nr && c < p.K)
+            x = *reinterpret_cast<const float4 *>(p.g + ((rowbase + r) * p.HV + hv) * p.K + c);
+        *reinterpret_cast<float4 *>(sG + fsw<KK>(r, c)) = x;
+    }
+    if (tid < 64) {
+        float bt = 0.f;
+        if (tid < nr)
+            bt = to_f32(static_cast<const __nv_bfloat16 *>(p.beta)[(rowbase + tid) * p.HV + hv]);
+        sBeta[tid] = bt;
+        sDbeta[tid] = 0.f;
+    }
+    {
+        const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(p.v);
+        const __nv_bfloat16 *dout = static_cast<const __nv_bfloat16 *>(a.dout);
+        for (int pc = tid; pc < 64 * (VV / 8); pc += 256) {
+            const int r = pc / (VV / 8), c = (pc % (VV / 8)) * 8;
+            uint4 x = make_uint4(0, 0, 0, 0), y = make_uint4(0, 0, 0, 0);
+            if (r < nr) {
+                const size_t off = ((rowbase + r) * p.HV + hv) * p.V + c;
+                x = *reinterpret_cast<const uint4 *>(v + off);
+                y = *reinterpret_cast<const uint4 *>(dout + off);
+            }
+            *reinterpret_cast<uint4 *>(sm + S::vt + tile_off(r, c, VV)) = x;
+            *reinterpret_cast<uint4 *>(sm + S::dout + tile_off(r, c, VV)) = y;
+        }
+    }
+    __syncthreads();
+    // chunk-local cumsum of g_scale g, one channel per thread; rows past the chunk
+    // keep the last row's value
+    if (tid < KK) {
+        float acc = 0.f;
+        bool bad = false;
+        for (int r = 0; r < 64; ++r) {
+            const int i = fsw<KK>(r, tid);
+            if (r < nr) acc = fmaf(p.g_scale, sG[i], acc);
+            sG[i] = acc;
+            bad |= !(fabsf(acc) <= kBwdRange);  // also NaN
+        }
+        sGl[tid] = acc;
+        sDG[tid] = 0.f;
+        if (bad) range_bad = 1;
+    }
+    __syncthreads();
+    if (range_bad) {
+        if (tid == 0) report(p.status, KDA_DEVICE_GATE_RANGE);
+        if (tid == 0) mbar_wait(&bar_ld, 0, kWaitNs);  // the copies land before the CTA exits
+        __syncthreads();
+        if (warp == 0) tmem_dealloc(tslot, 512);
+        return;
+    }
+    // q, k rows -> kp, kn, qp tiles
+    {
+        const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(p.q);
+        const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(p.k);
+        for (int pc = tid; pc < 64 * (KK / 8); pc += 256) {
+            const int r = pc / (KK / 8), c = (pc % (KK / 8)) * 8;
+            float fq[8], fk[8];
+            if (r < nr && c < p.K) {
+                const size_t off = ((rowbase + r) * p.H + hq) * p.K + c;
+                unpack8(*reinterpret_cast<const uint4 *>(q + off), fq);
+                unpack8(*reinterpret_cast<const uint4 *>(k + off), fk);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) fq[j] = fk[j] = 0.f;
+            }
+            const float4 g0 = *reinterpret_cast<const float4 *>(sG + fsw<KK>(r, c));
+            const float4 g1 = *reinterpret_cast<const float4 *>(sG + fsw<KK>(r, c + 4));
+            const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+            float kp[8], kn[8], qp[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float e = ex2f(gg[j]), ei = ex2f(-gg[j]);
+                kp[j] = fk[j] * e;
+                kn[j] = fk[j] * ei;
+                qp[j] = fq[j] * e;
+            }
+            *reinterpret_cast<uint4 *>(sm + S::kp + tile_off(r, c, KK)) = pack8(kp);
+            *reinterpret_cast<uint4 *>(sm + S::kn + tile_off(r, c, KK)) = pack8(kn);
+            *reinterpret_cast<uint4 *>(sm + S::qp + tile_off(r, c, KK)) = pack8(qp);
+        }
+    }
+    fence_async_smem();
+    __syncthreads();
+    if (tid == 0 && !mbar_wait(&bar_ld, 0, kWaitNs)) report(p.status, KDA_DEVICE_TIMEOUT);
+    __syncthreads();
+    tc_fence_after();
+
+    const uint32_t tmem = tslot;
+    const uint32_t s0 = smem_addr(sm);
+    uint32_t phase = 0;
+    auto mma_wait = [&]() {
+        if (!mbar_wait(&bar_mma, phase & 1, kWaitNs) && tid == 0) report(p.status, KDA_DEVICE_TIMEOUT);
+        ++phase;
+        tc_fence_after();
+    };
+    // K-major tile [rows][C]: per K = 16 step +256 bytes; MN-major: +2 C * 16 bytes.
+    auto kmaj = [&](uint32_t off, int C) { return sdesc(s0 + off, 128, C * 16); };
+    auto mnmaj = [&](uint32_t off, int C) { return sdesc(s0 + off, C * 16, 128); };
+
+    // ---- P = kp kn^T, do v'^T, [do; dv'] h^T, v' dh^T
+    if (tid == 0) {
+        mma_bf16_seq<KK / 16, false>(tmem + 0, kmaj(S::kp, KK), 16, kmaj(S::kn, KK), 16,
+                                     idesc_bf16(64, 64, false, false));
+        mma_bf16_seq<VV / 16, false>(tmem + 64, kmaj(S::dout, VV), 16, kmaj(S::vp, VV), 16,
+                                     idesc_bf16(64, 64, false, false));
+        mma_bf16_seq<VV / 16, false>(tmem + 128, kmaj(S::dout, VV), 16, kmaj(S::h, VV), 16,
+                                     idesc_bf16(128, KK, false, false));
+        mma_bf16_seq<VV / 16, false>(tmem + 256, kmaj(S::vp, VV), 16, kmaj(S::dhn, VV), 16,
+                                     idesc_bf16(64, KK, false, false));
+        mma_commit(&bar_mma);
+    }
+    // meanwhile: ln2 2^G rowsum(h . dh_{c+1}) per channel, two threads a row
+    {
+        const int d = tid >> 1, j0 = (tid & 1) * (VV / 2);
+        float acc = 0.f;
+        for (int j = j0; j < j0 + VV / 2; j += 8) {
+            float x[8], y[8];
+            unpack8(sm + S::h + tile_off(d, j, VV), x);
+            unpack8(sm + S::dhn + tile_off(d, j, VV), y);
+#pragma unroll
+            for (int t = 0; t < 8; ++t) acc = fmaf(x[t], y[t], acc);
+        }
+        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+        if ((tid & 1) == 0 && d < KK) sDG[d] = kLn2 * ex2f(sGl[d]) * acc;
+    }
+    mma_wait();
+    __syncthreads();
+
+    const float scale = p.scale;
+    float *dq_row = nullptr, *dk_row = nullptr;
+    auto grow = [&](float *base, int r) { return base + ((rowbase + r) * p.H + hq) * p.K; };
+    auto g2v = [&](int r, int c, float (&o)[8]) {
+        const float4 x = *reinterpret_cast<const float4 *>(sG + fsw<KK>(r, c));
+        const float4 y = *reinterpret_cast<const float4 *>(sG + fsw<KK>(r, c + 4));
+        o[0] = x.x; o[1] = x.y; o[2] = x.z; o[3] = x.w; o[4] = y.x; o[5] = y.y; o[6] = y.z; o[7] = y.w;
+    };
+    auto dg2_add = [&](int r, int c, const float (&x)[8], bool init) {
+        float4 *d0 = reinterpret_cast<float4 *>(sDg2 + fsw<KK>(r, c));
+        float4 *d1 = reinterpret_cast<float4 *>(sDg2 + fsw<KK>(r, c + 4));
+        if (init) {
+            *d0 = make_float4(x[0], x[1], x[2], x[3]);
+            *d1 = make_float4(x[4], x[5], x[6], x[7]);
+        } else {
+            float4 u = *d0, v = *d1;
+            u.x += x[0]; u.y += x[1]; u.z += x[2]; u.w += x[3];
+            v.x += x[4]; v.y += x[5]; v.z += x[6]; v.w += x[7];
+            *d0 = u;
+            *d1 = v;
+        }
+    };
+
+    // ---- E1a: dqg = scale do h^T (rows 0..63 of the M = 128 result) -> dq, dg2;
+    //      dw = -(dv' h^T) (rows 64..127) -> bf16 tile; dA = scale tril(do v'^T)
+    if (quad < 2) {
+        const int r = 32 * quad + lane;
+        for (int cb = 0; cb < KK / 2; cb += 32) {
+            const int c0 = half * (KK / 2) + cb;
+            float d[32];
+            tmem_ld32(tmem_at(tmem, 32 * quad, 128 + c0), d);
+#pragma unroll
+            for (int c8 = 0; c8 < 32; c8 += 8) {
+                float gg[8], qp[8], dq8[8], dg8[8];
+                g2v(r, c0 + c8, gg);
+                unpack8(sm + S::qp + tile_off(r, c0 + c8, KK), qp);
+#pragma unroll
+                for (int t = 0; t < 8; ++t) {
+                    const float x = scale * d[c8 + t];
+                    dq8[t] = x * ex2f(gg[t]);
+                    dg8[t] = kLn2 * x * qp[t];
+                }
+                if (r < nr && c0 + c8 < p.K) add8(grow(a.dq, r) + c0 + c8, dq8);
+                dg2_add(r, c0 + c8, dg8, true);
+            }
+        }
+    } else {
+        const int r = 32 * (quad - 2) + lane;
+        for (int cb = 0; cb < KK / 2; cb += 32) {
+            const int c0 = half * (KK / 2) + cb;
+            float d[32];
+            tmem_ld32(tmem_at(tmem, 32 * quad, 128 + c0), d);
+#pragma unroll
+            for (int t = 0; t < 32; ++t) d[t] = -d[t];
+#pragma unroll
+            for (int c8 = 0; c8 < 32; c8 += 8)
+                *reinterpret_cast<uint4 *>(sm + S::dw + tile_off(r, c0 + c8, KK)) = pack8_at(d + c8);
+        }
+    }
+    {
+        const int r = 16 * quad + (lane & 15);
+        float d[32];
+        tmem_ld32(tmem_at(tmem, 32 * quad, 64 + half * 32), d);
+        if (lane < 16) {
+#pragma unroll
+            for (int t = 0; t < 32; ++t) d[t] = (half * 32 + t <= r) ? scale * d[t] : 0.f;
+#pragma unroll
+            for (int c8 = 0; c8 < 32; c8 += 8)
+                *reinterpret_cast<uint4 *>(sm + S::dap + tile_off(64 + r, half * 32 + c8, 64)) =
+                    pack8_at(d + c8);
+        }
+    }
+    __syncthreads();
+    // ---- E1b: dkg = v' dh^T (M = 64) -> dk, dg2, and the G terms
+    {
+        const int r = 16 * quad + (lane & 15);
+        const bool live = lane < 16;
+        for (int cb = 0; cb < KK / 2; cb += 32) {
+            const int c0 = half * (KK / 2) + cb;
+            float d[32];
+            tmem_ld32(tmem_at(tmem, 32 * quad, 256 + c0), d);
+#pragma unroll
+            for (int c8 = 0; c8 < 32; c8 += 8) {
+                float gg[8], kn[8], dk8[8], dg8[8], colp[8];
+                g2v(r, c0 + c8, gg);
+                unpack8(sm + S::kn + tile_off(r, c0 + c8, KK), kn);
+#pragma unroll
+                for (int t = 0; t < 8; ++t) {
+                    const float gl = sGl[c0 + c8 + t];
+                    const float x = live ? d[c8 + t] : 0.f;
+                    dk8[t] = x * ex2f(gl - gg[t]);
+                    const float kgx = x * kn[t] * ex2f(gl);   // dkg . kg
+                    dg8[t] = -kLn2 * kgx;
+                    colp[t] = kLn2 * kgx;
+                }
+                if (live) {
+                    if (r < nr && c0 + c8 < p.K) add8(grow(a.dk, r) + c0 + c8, dk8);
+                    dg2_add(r, c0 + c8, dg8, false);
+                }
+#pragma unroll
+                for (int t = 0; t < 8; ++t) {
+                    float s = colp[t];
+                    s += __shfl_xor_sync(0xffffffffu, s, 1);
+                    s += __shfl_xor_sync(0xffffffffu, s, 2);
+                    s += __shfl_xor_sync(0xffffffffu, s, 4);
+                    s += __shfl_xor_sync(0xffffffffu, s, 8);
+                    if (lane == 0) atomicAdd(&sDG[c0 + c8 + t], s);
+                }
+            }
+        }
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    // ---- dAkk = dv' v^T + dw kp^T (columns scaled by beta below); Akk^T [dv' | dw]
+    if (tid == 0) {
+        mma_bf16_seq<VV / 16, false>(tmem + 384, kmaj(S::dvp, VV), 16, kmaj(S::vt, VV), 16,
+                                     idesc_bf16(64, 64, false, false));
+        mma_bf16_seq<KK / 16, true>(tmem + 384, kmaj(S::dw, KK), 16, kmaj(S::kp, KK), 16,
+                                    idesc_bf16(64, 64, false, false));
+        mma_bf16_seq<4, false>(tmem + 128, mnmaj(S::akk, 64), 2 * 64, mnmaj(S::dvp, VV), 2 * VV,
+                               idesc_bf16(64, VV, true, true));
+        mma_bf16_seq<4, false>(tmem + 256, mnmaj(S::akk, 64), 2 * 64, mnmaj(S::dw, KK), 2 * KK,
+                               idesc_bf16(64, KK, true, true));
+        mma_commit(&bar_mma);
+    }
+    mma_wait();
+    // ---- E2: dv = diag(beta) Akk^T dv'; dkgate = diag(beta) Akk^T dw; dbeta; dAkk tile
+    {
+        const int r = 16 * quad + (lane & 15);
+        const bool live = lane < 16;
+        const float br = sBeta[r];
+        float db = 0.f;
+        for (int cb = 0; cb < VV / 2; cb += 32) {
+            const int c0 = half * (VV / 2) + cb;
+            float d[32];
+            tmem_ld32(tmem_at(tmem, 32 * quad, 128 + c0), d);
+            if (live) {
+                float *dvr = a.dv + ((rowbase + r) * p.HV + hv) * p.V + c0;
+#pragma unroll
+                for (int c8 = 0; c8 < 32; c8 += 8) {
+                    float vv[8];
+                    unpack8(sm + S::vt + tile_off(r, c0 + c8, VV), vv);
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) db = fmaf(d[c8 + t], vv[t], db);
+                }
+                if (r < nr) {
+#pragma unroll
+                    for (int t = 0; t < 32; t += 4)
+                        *reinterpret_cast<float4 *>(dvr + t) =
+                            make_float4(br * d[t], br * d[t + 1], br * d[t + 2], br * d[t + 3]);
+                }
+            }
+        }
+        for (int cb = 0; cb < KK / 2; cb += 32) {
+            const int c0 = half * (KK / 2) + cb;
+            float d[32];
+            tmem_ld32(tmem_at(tmem, 32 * quad, 256 + c0), d);
+            if (live) {
+#pragma unroll
+                for (int c8 = 0; c8 < 32; c8 += 8) {
+                    float gg[8], kp[8], dk8[8], dg8[8];
+                    g2v(r, c0 + c8, gg);
+                    unpack8(sm + S::kp + tile_off(r, c0 + c8, KK), kp);
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) {
+                        db = fmaf(d[c8 + t], kp[t], db);
+                        const float x = br * d[c8 + t];
+                        dk8[t] = x * ex2f(gg[t]);
+                        dg8[t] = kLn2 * x * kp[t];
+                    }
+                    if (r < nr && c0 + c8 < p.K) add8(grow(a.dk, r) + c0 + c8, dk8);
+                    dg2_add(r, c0 + c8, dg8, false);
+                }
+            }
+        }
+        {
+            float d[32];
+            tmem_ld32(tmem_at(tmem, 32 * quad, 384 + half * 32), d);
+            if (live) {
+#pragma unroll
+                for (int t = 0; t < 32; ++t) d[t] *= sBeta[half * 32 + t];
+#pragma unroll
+                for (int c8 = 0; c8 < 32; c8 += 8)
+                    *reinterpret_cast<uint4 *>(sm + S::dakk + tile_off(r, half * 32 + c8, 64)) =
+                        pack8_at(d + c8);
+                atomicAdd(&sDbeta[r], db);
+            }
+        }
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    // ---- X = Akk^T dAkk
+    if (tid == 0) {
+        mma_bf16_seq<4, false>(tmem + 448, mnmaj(S::akk, 64), 2 * 64, mnmaj(S::dakk, 64), 2 * 64,
+                               idesc_bf16(64, 64, true, true));
+        mma_commit(&bar_mma);
+    }
+    mma_wait();
+    {
+        const int r = 16 * quad + (lane & 15);
+        float d[32];
+        tmem_ld32(tmem_at(tmem, 32 * quad, 448 + half * 32), d);
+        if (lane < 16) {
+#pragma unroll
+            for (int c8 = 0; c8 < 32; c8 += 8)
+                *reinterpret_cast<uint4 *>(sm + S::xt + tile_off(r, half * 32 + c8, 64)) = pack8_at(d + c8);
+        }
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    // ---- Y = X Akk^T
+    if (tid == 0) {
+        mma_bf16_seq<4, false>(tmem + 64, kmaj(S::xt, 64), 16, kmaj(S::akk, 64), 16,
+                               idesc_bf16(64, 64, false, false));
+        mma_commit(&bar_mma);
+    }
+    mma_wait();
+    // ---- E4: dL = -strictly_tril(Y); dbeta += rowsum(dL . P); dP = diag(beta) dL
+    {
+        const int r = 16 * quad + (lane & 15);
+        float y[32], pp[32];
+        tmem_ld32(tmem_at(tmem, 32 * quad, 64 + half * 32), y);
+        tmem_ld32(tmem_at(tmem, 32 * quad, 0 + half * 32), pp);
+        if (lane < 16) {
+            const float br = sBeta[r];
+            float db = 0.f;
+#pragma unroll
+            for (int t = 0; t < 32; ++t) {
+                const float dl = (half * 32 + t < r) ? -y[t] : 0.f;
+                db = fmaf(dl, pp[t], db);
+                y[t] = br * dl;
+            }
+#pragma unroll
+            for (int c8 = 0; c8 < 32; c8 += 8)
+                *reinterpret_cast<uint4 *>(sm + S::dap + tile_off(r, half * 32 + c8, 64)) = pack8_at(y + c8);
+            atomicAdd(&sDbeta[r], db);
+        }
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    // ---- [dP; dA] kn and dP^T kp + dA^T qp
+    if (tid == 0) {
+        mma_bf16_seq<4, false>(tmem + 128, kmaj(S::dap, 64), 16, mnmaj(S::kn, KK), 2 * KK,
+                               idesc_bf16(128, KK, false, true));
+        mma_bf16_seq<4, false>(tmem + 256, mnmaj(S::dap, 64), 2 * 64, mnmaj(S::kp, KK), 2 * KK,
+                               idesc_bf16(64, KK, true, true));
+        mma_bf16_seq<4, true>(tmem + 256, mnmaj(S::dap + 64 * 64 * 2, 64), 2 * 64, mnmaj(S::qp, KK),
+                              2 * KK, idesc_bf16(64, KK, true, true));
+        mma_commit(&bar_mma);
+    }
+    mma_wait();
+    // ---- E5: (dP kn) 2^g2 -> dk, (dA kn) 2^g2 -> dq, (dP^T kp + dA^T qp) 2^-g2 -> dk,
+    // and their dg2 terms, in three passes so that no two threads share a dg2 element.
+    // Pass 0: rows 0..63 of the M = 128 result (dP kn) -> dk, dg2; rows 64..127
+    // (dA kn) -> dq.  Pass 1: rows 64..127 -> dg2.
+    for (int pass = 0; pass < 2; ++pass) {
+        const bool top = quad < 2;
+        const int r = 32 * (quad & 1) + lane;
+        if (pass == 0 || !top) {
+            for (int cb = 0; cb < KK / 2; cb += 32) {
+                const int c0 = half * (KK / 2) + cb;
+                float d[32];
+                tmem_ld32(tmem_at(tmem, 32 * quad, 128 + c0), d);
+#pragma unroll
+                for (int c8 = 0; c8 < 32; c8 += 8) {
+                    float gg[8], fac[8], g8[8], dg8[8];
+                    g2v(r, c0 + c8, gg);
+                    unpack8(sm + (top ? S::kp : S::qp) + tile_off(r, c0 + c8, KK), fac);
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) {
+                        g8[t] = d[c8 + t] * ex2f(gg[t]);
+                        dg8[t] = kLn2 * d[c8 + t] * fac[t];
+                    }
+                    if (pass == 0 && r < nr && c0 + c8 < p.K)
+                        add8(grow(top ? a.dk : a.dq, r) + c0 + c8, g8);
+                    if (pass == 0 ? top : !top) dg2_add(r, c0 + c8, dg8, false);
+                }
+            }
+        }
+        __syncthreads();
+    }
+    {
+        const int r = 16 * quad + (lane & 15);
+        const bool live = lane < 16;
+        for (int cb = 0; cb < KK / 2; cb += 32) {
+            const int c0 = half * (KK / 2) + cb;
+            float d[32];
+            tmem_ld32(tmem_at(tmem, 32 * quad, 256 + c0), d);
+            if (live) {
+#pragma unroll
+                for (int c8 = 0; c8 < 32; c8 += 8) {
+                    float gg[8], kn[8], dk8[8], dg8[8];
+                    g2v(r, c0 + c8, gg);
+                    unpack8(sm + S::kn + tile_off(r, c0 + c8, KK), kn);
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) {
+                        dk8[t] = d[c8 + t] * ex2f(-gg[t]);
+                        dg8[t] = -kLn2 * d[c8 + t] * kn[t];
+                    }
+                    if (r < nr && c0 + c8 < p.K) add8(grow(a.dk, r) + c0 + c8, dk8);
+                    dg2_add(r, c0 + c8, dg8, false);
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    // ---- dg: g_scale x reverse cumsum of dg2 (G's gradient on the last row); dbeta
+    if (tid < KK) {
+        float acc = sDG[tid];
+        for (int r = nr - 1; r >= 0; --r) {
+            acc += sDg2[fsw<KK>(r, tid)];
+            if (tid < p.K) a.dg[((rowbase + r) * p.HV + hv) * p.K + tid] = p.g_scale * acc;
+        }
+    } else if (tid - 128 < nr && tid - 128 < 64) {
+        const int r = tid - 128;
+        a.dbeta[(rowbase + r) * p.HV + hv] = sDbeta[r];
+    }
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+template <int KK, int SBV>
+cudaError_t launch_dhu(const BwdArgs &a, cudaStream_t st) {
+    using S = DhuSmem<KK, SBV>;
+    static DeviceOnce once;
+    int dev = 0;
+    cudaError_t e = once.run(&dev, [](int) {
+        return cudaFuncSetAttribute(chunk_dhu_tc_kernel<KK, SBV>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::total);
+    });
+    if (e != cudaSuccess) return e;
+    const int64_t blocks = (int64_t)a.c.N * a.c.HV * (a.c.V / SBV);
+    if (blocks == 0) return cudaSuccess;
+    prof_begin("chunk_dhu_tc", st);
+    chunk_dhu_tc_kernel<KK, SBV><<<(unsigned)blocks, 320, S::total, st>>>(a);
+    prof_end(st);
+    return cudaGetLastError();
+}
+
+template <int KK, int VV>
+cudaError_t launch_unit(const BwdArgs &a, cudaStream_t st) {
+    using S = UnitSmem<KK, VV>;
+    static DeviceOnce once;
+    int dev = 0;
+    cudaError_t e = once.run(&dev, [](int) {
+        return cudaFuncSetAttribute(chunk_bwd_unit_tc_kernel<KK, VV>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::total);
+    });
+    if (e != cudaSuccess) return e;
+    const int64_t units = a.c.slots * a.c.HV;
+    if (units == 0) return cudaSuccess;
+    prof_begin("chunk_bwd_unit_tc", st);
+    chunk_bwd_unit_tc_kernel<KK, VV><<<(unsigned)units, 256, S::total, st>>>(a);
+    prof_end(st);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool chunk_bwd_tc_supported(int K, int V) { return K == 128 && V == 128; }
+
+cudaError_t launch_chunk_bwd_tc(const ChunkArgs &c, const void *dout, const float *dht, float *dq,
+                                float *dk, float *dv, float *dg, float *dbeta, float *dh0,
+                                void *dhn, void *dvp, cudaStream_t st) {
+    if (!chunk_bwd_tc_supported(c.K, c.V)) return cudaErrorInvalidValue;
+    BwdArgs a;
+    a.c = c;
+    a.dout = dout;
+    a.dht = dht;
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv;
+    a.dg = dg;
+    a.dbeta = dbeta;
+    a.dh0 = dh0;
+    a.dhn = dhn;
+    a.dvp = dvp;
+    cudaError_t e = launch_chunk_tc(c, st);  // recompute and re-scan, with checkpoints
+    if (e != cudaSuccess) return e;
+    if ((e = launch_dhu<128, 32>(a, st)) != cudaSuccess) return e;
+    return launch_unit<128, 128>(a, st);
+}
+
+}  // namespace kda

@@ -31,6 +31,7 @@
 //     stream in by bulk async copies while the current chunk computes.
 #include "kda_internal.cuh"
 #include "kda_tc.cuh"
+#include "kda_chunk_layout.cuh"
 
 #include <mutex>
 
@@ -42,64 +43,6 @@ namespace {
 
 using namespace tc;
 
-constexpr int kUB = 16;               // column block of u in the workspace
-constexpr float kSafeRange = 60.f;    // max |g2| (log2) for the split grams
-constexpr uint64_t kWaitNs = 1000000000ull;
-
-// Byte layout of one workspace unit (chunk c, value head).
-struct TcLayout {
-    uint32_t aw;      // [128][dk] tile: rows 0..63 W~_c = W_c Diag(2^G_{c-1}) (W_0 for a
-                      // sequence's first chunk), rows 64..127 qg_c (the scan
-                      // applies the attention scale to o)
-    uint32_t kgt;     // [64][dk] tile: kg_c (rows = tokens), read by the scan as an
-                      // MN-major operand, i.e. as kg_c^T
-    uint32_t mt;      // [64][64] tile: M_c = W_c kg_{c-1}^T (unused for a first chunk)
-    uint32_t aqk;     // [64][64] tile: Aqk_c (unscaled, like qg_c)
-    uint32_t u;       // [dv / kUB][64][kUB] bf16 row-major blocks: u_c
-    uint32_t dec;     // [128] fp32: 2^G_c (0 beyond dk)
-    uint32_t stride;  // unit size, 256-byte multiple
-};
-
-__host__ __device__ inline TcLayout tc_layout(int K, int V) {
-    TcLayout L;
-    uint32_t off = 0;
-    L.aw = off;  off += 128u * K * 2;
-    L.kgt = off; off += 64u * K * 2;
-    L.mt = off;  off += 64u * 64 * 2;
-    L.aqk = off; off += 64u * 64 * 2;
-    L.u = off;   off += 64u * V * 2;
-    L.dec = off; off += 128u * 4;
-    L.stride = (uint32_t)align_up(off, 256);
-    return L;
-}
-
-// Maps a chunk slot to its rows and its index within the sequence (and, when
-// asked, the sequence and its chunk count).  Returns false for slots past the
-// last chunk or when the offsets failed validation.
-__device__ __forceinline__ bool locate_chunk(const ChunkArgs &p, int64_t gc, int &b, int &r0,
-                                             int &nr, int &cl, int *seq = nullptr,
-                                             int *seq_chunks = nullptr) {
-    if (p.cu) {
-        if (!p.ctrl->valid || gc >= p.ctrl->total_chunks) return false;
-        const int n = upper_bound_minus_one(p.chunk_start, p.N + 1, (int)gc);
-        cl = (int)gc - p.chunk_start[n];
-        b = 0;
-        r0 = p.cu[n] + kBT * cl;
-        nr = min(kBT, p.cu[n + 1] - r0);
-        if (seq) *seq = n;
-        if (seq_chunks) *seq_chunks = p.chunk_start[n + 1] - p.chunk_start[n];
-    } else {
-        const int ntc = (p.T + kBT - 1) / kBT;
-        b = (int)(gc / ntc);
-        cl = (int)(gc % ntc);
-        r0 = cl * kBT;
-        nr = min(kBT, p.T - r0);
-        if (seq) *seq = b;
-        if (seq_chunks) *seq_chunks = ntc;
-    }
-    return nr > 0;
-}
-
 // Whether a chunk continues the scan of the chunk before it: not a sequence's
 // first chunk, nor the first chunk of the second segment of a split launch or of
 // the second part of a pipelined one (those scans start from a given state).
@@ -110,12 +53,6 @@ __device__ __forceinline__ bool continues(const ChunkArgs &p, int cl, int seq_ch
 // A prep launch's units: every chunk slot of every value head, or (a pipelined
 // launch's part, dense input) chunks [prep_c0, prep_c1) of every sequence.
 // Units run value head by value head, chunks in order within a sequence.
-// Index of the workspace unit of chunk slot gc and value head hv.  Head-major: a
-// head's consecutive chunks are adjacent, so the scan, which walks one head's
-// chunks, stays within a few memory pages instead of stepping HV units per round.
-__host__ __device__ __forceinline__ int64_t unit_index(const ChunkArgs &p, int64_t gc, int hv) {
-    return (int64_t)hv * p.slots + gc;
-}
 __host__ __device__ __forceinline__ int64_t prep_units(const ChunkArgs &p) {
     const int64_t per_hv = p.prep_c1 > p.prep_c0 ? (int64_t)p.B * (p.prep_c1 - p.prep_c0) : p.slots;
     return per_hv * p.HV;
@@ -138,29 +75,6 @@ __device__ __forceinline__ void cp_async16(void *dst, const void *src) {
                  : "memory");
 }
 
-__device__ __forceinline__ void unpack8(const uint4 &u, float (&f)[8]) {
-    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float2 t = __bfloat1622float2(h[i]);
-        f[2 * i] = t.x;
-        f[2 * i + 1] = t.y;
-    }
-}
-__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
-    uint4 u;
-    __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&u);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
-    return u;
-}
-__device__ __forceinline__ uint4 pack8_at(const float *f) {
-    uint4 u;
-    __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&u);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
-    return u;
-}
 
 // ============================================================== prep kernel
 // Shared memory of the prep kernel.  The kernel declares no static shared
@@ -375,7 +289,7 @@ __global__ void __launch_bounds__(256, 2)
     unsigned char *sPB = sm + S::pbuf(VV);
     float *sA = reinterpret_cast<float *>(sm + S::abuf(VV));
 
-    const TcLayout Lo = tc_layout(KK, VV);
+    const TcLayout Lo = tc_layout(KK, VV, p.bwd);
     if (warp == 0) {
         tmem_alloc(&tslot, kCols);
         tmem_relinquish();
@@ -949,6 +863,11 @@ __global__ void __launch_bounds__(256, 2)
         const uint4 ab = pack8(f);
         *reinterpret_cast<uint4 *>(sAB + tile_off(i, c, 64)) = ab;
         *reinterpret_cast<uint4 *>(sAB + tile_off(64 + i, c, 64)) = ab;
+        if (__builtin_expect(p.bwd, 0)) {  // Akk itself for the backward
+#pragma unroll
+            for (int j = 0; j < 8; ++j) f[j] = (c + j <= i) ? av[j] : 0.f;
+            *reinterpret_cast<uint4 *>(U + Lo.akk + tile_off(i, c, 64)) = pack8(f);
+        }
     }
     fence_async_smem();
     tc_fence_before();
@@ -989,6 +908,11 @@ __global__ void __launch_bounds__(256, 2)
             tmem_ld32(tmem_at(tmem, quad * 32, part * kQ), dd);
         else
             tmem_ld16(tmem_at(tmem, quad * 32, part * kQ), dd);
+        if (__builtin_expect(p.bwd, 0)) {  // W itself for the backward
+#pragma unroll
+            for (int c8 = 0; c8 < kQ; c8 += 8)
+                *reinterpret_cast<uint4 *>(U + Lo.wb + tile_off(i, part * kQ + c8, KK)) = pack8_at(dd + c8);
+        }
         if (halo) {
 #pragma unroll
             for (int j = 0; j < kQ; ++j) dd[j] *= sDprev[part * kQ + j];
@@ -1244,7 +1168,7 @@ __global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
     }
     const int ncs = c1 - c0;
     const int R = ncs > 0 ? ncs + 1 : 0;  // rounds
-    const TcLayout Lo = tc_layout(KK, p.V);
+    const TcLayout Lo = tc_layout(KK, p.V, p.bwd);
     const unsigned char *units = static_cast<const unsigned char *>(p.units);
 
     if (warp == 0) {
@@ -1399,11 +1323,20 @@ __global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
                 h[4 * j] = x.x; h[4 * j + 1] = x.y; h[4 * j + 2] = x.z; h[4 * j + 3] = x.w;
             }
         }
-        auto write_h = [&]() {
+        // h at the start of chunk cc: the next MMA's operand (and, for the backward,
+        // the chunk's checkpoint tile)
+        auto write_h = [&](int cc) {
             if (has_row) {
+                unsigned char *t = p.ck_h ? static_cast<unsigned char *>(p.ck_h) +
+                                                unit_index(p, gc0 + cc, hv) * (int64_t)(KK * p.V * 2) +
+                                                tile_off(row, vb * SBV, p.V)
+                                          : nullptr;
 #pragma unroll
-                for (int c = 0; c < SBV; c += 8)
-                    *reinterpret_cast<uint4 *>(sH + tile_off(row, c, SBV)) = pack8_at(h + c);
+                for (int c = 0; c < SBV; c += 8) {
+                    const uint4 v8 = pack8_at(h + c);
+                    *reinterpret_cast<uint4 *>(sH + tile_off(row, c, SBV)) = v8;
+                    if (t) *reinterpret_cast<uint4 *>(t + c * 16) = v8;  // next 8 columns: +128 B
+                }
             }
             fence_async_smem();
             __syncwarp();
@@ -1418,7 +1351,7 @@ __global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
             if (lane == 0) mbar_arrive(&empty[r % kStages]);
             return d;
         };
-        if (R > 0) write_h();
+        if (R > 0) write_h(c0);
         float dec = R > 0 ? fetch(0) : 1.f;
         for (int r = 0; r < R; ++r) {
             const bool nxt = r < ncs;
@@ -1439,7 +1372,7 @@ __global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
                     for (int t = 0; t < kSl; ++t) h[cb + t] = fmaf(dec, h[cb + t], d[t]);
                 }
                 tc_fence_before();
-                if (nxt) write_h();
+                if (nxt) write_h(c0 + r);
             } else if (nxt) {
                 // Round 0 leaves h_0 in place.  Arrive for round 1 only once round 0's
                 // MMA has completed, i.e. after the MMA warp left this barrier's
@@ -1519,6 +1452,14 @@ __global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
 #pragma unroll
                 for (int c = 0; c < 32; c += 8)
                     *reinterpret_cast<uint4 *>(sVp + tile_off(row, cb + c, SBV)) = pack8_at(d + c);
+                if (p.ck_vp) {  // v' of chunk c0 + r for the backward
+                    unsigned char *t = static_cast<unsigned char *>(p.ck_vp) +
+                                       unit_index(p, gc0 + c0 + r, hv) * (int64_t)(64 * p.V * 2);
+#pragma unroll
+                    for (int c = 0; c < 32; c += 8)
+                        *reinterpret_cast<uint4 *>(t + tile_off(row, vb * SBV + cb + c, p.V)) =
+                            pack8_at(d + c);
+                }
             }
             tc_fence_before();
             fence_async_smem();
@@ -1537,7 +1478,7 @@ __global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
                 wait_mma(&bar_v[r & 1], (r >> 1) & 1);
                 tc_fence_after();
                 const int c = c0 + r - 1;
-                const bool store = !read_flag(&abort_flag);
+                const bool store = !read_flag(&abort_flag) && (ident || o != nullptr);
                 const int orow = bos + c * kBT + i;
                 unsigned char *qt = ident ? static_cast<unsigned char *>(p.qc) +
                                                 ((gc0 + c) * p.HV + hv) * (int64_t)(64 * KK * 2)
@@ -2041,7 +1982,9 @@ bool chunk_tc_supported(int K, int V) {
     return K >= 8 && K <= 128 && K % 8 == 0 && V >= 32 && V <= 256 && V % 32 == 0;
 }
 
-size_t chunk_tc_unit_bytes(int K, int V) { return tc_layout(K <= 64 ? 64 : 128, V).stride; }
+size_t chunk_tc_unit_bytes(int K, int V, bool bwd) {
+    return tc_layout(K <= 64 ? 64 : 128, V, bwd).stride;
+}
 
 int chunk_tc_pipe_m(int B, int HV, int K, int V, int T, int sms) {
     // Cost model in scan rounds: at two prep CTAs per SM a prep unit takes about

@@ -202,6 +202,12 @@ struct ChunkArgs {
     int pipe_m;            // first chunk of the second part
     int prep_c0, prep_c1;  // a prep launch's chunks within every sequence (c1 <= c0: all slots)
     int scan_seg;          // a pipelined scan launch's part: 0 from h0, 1 from e0
+    // The chunked backward's re-run of the forward: the prep also stores W_c and
+    // Akk_c in each unit (tc_layout with bwd), the scan stores the state at the
+    // start of every chunk (ck_h, a [dk][V] bf16 operand tile per unit) and v'_c
+    // (ck_vp, a [64][V] tile per unit); o may then be null (not stored).
+    int bwd = 0;
+    void *ck_h = nullptr, *ck_vp = nullptr;
 };
 size_t chunk_simt_unit_bytes(int K, int V);
 cudaError_t launch_chunk_simt(const ChunkArgs &a, kda_dtype dt, cudaStream_t st);
@@ -214,7 +220,15 @@ bool chunk_tc_supported(int K, int V);
 int chunk_tc_pipe_m(int B, int HV, int K, int V, int T, int sms);
 // Whether a launch splits each sequence's scan into two segments run at once.
 bool chunk_tc_split(int N, int HV, int K, int V, int T);
-size_t chunk_tc_unit_bytes(int K, int V);
+size_t chunk_tc_unit_bytes(int K, int V, bool bwd = false);
 cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st);
+
+// Chunked backward (kda_chunk_bwd), bf16 with K = V = 128: the forward re-run with
+// `c.bwd` and its checkpoints, the reverse state scan (dhn, dvp: per-unit tiles in
+// the workspace), then the per-chunk gradients.  dq and dk must be zeroed first.
+bool chunk_bwd_tc_supported(int K, int V);
+cudaError_t launch_chunk_bwd_tc(const ChunkArgs &c, const void *dout, const float *dht, float *dq,
+                                float *dk, float *dv, float *dg, float *dbeta, float *dh0,
+                                void *dhn, void *dvp, cudaStream_t st);
 
 }  // namespace kda

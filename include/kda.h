@@ -21,6 +21,8 @@
  * raw inputs inside the op (kda_activation below), and
  *   kda_recurrent_bwd  the gradients of the recurrence (ALGORITHM.md, Backward),
  *                      also as kda_recurrent_bwd_act (gradients of the raw inputs)
+ *   kda_chunk_bwd      the same gradients in the chunked form on the tensor cores
+ *                      (ALGORITHM.md, Backward, the seven launches)
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -138,6 +140,12 @@ typedef enum {
                                                (e.g. the alignment of its shared memory)
                                                and skipped its work; reported as
                                                KDA_ERR_CUDA                            */
+#define KDA_DEVICE_GATE_RANGE     (1 << 3)  /* kda_chunk_bwd: a chunk's gate range
+                                               max |g2| (log2, chunk-local cumsum of
+                                               g_scale g) exceeds 100, or is not
+                                               finite; that chunk's gradients were not
+                                               computed.  Reported as
+                                               KDA_ERR_UNSUPPORTED                     */
 
 typedef struct {
     int32_t B, T, H, HV, K, V;  /* see Layouts; HV % H == 0                         */
@@ -345,6 +353,37 @@ kda_status kda_recurrent_bwd_act(const void *q, const void *k, const void *v, co
                                  int32_t *dev_status, kda_stream_t stream);
 /* Bytes of workspace kda_recurrent_bwd needs for *shape (0 on invalid shapes). */
 size_t kda_recurrent_bwd_workspace_size(const kda_shape *shape);
+
+/*
+ * kda_chunk_bwd -- the same gradients as kda_recurrent_bwd, computed in the chunked
+ * form of kernel-fun 0.2.0.dev1 sdist, ALGORITHM.md, "Backward" (the seven launches:
+ * recompute, re-scan, dAv, dhu, wy_dqkg, intra, dg cumsum; kernel-fun wheel,
+ * kda/chain.py, backward) on the tensor cores: the forward's prep and scan run again
+ * and store, per (chunk, value head), w, Akk, the state at the chunk's start and v';
+ * a reverse scan forms dL/dv' and dL/dh per chunk; one kernel per (chunk, value
+ * head) then forms dq, dk, dv, dbeta and dg.  Operands are bf16 (the inputs, the
+ * checkpoints and the intermediate gradients), accumulation fp32.
+ *   q, k, v, g, beta, h0, cu_seqlens, shape   as for kda_chunk_fwd.
+ *   dout, dht, dq, dk, dv, dg, dbeta, dh0     as for kda_recurrent_bwd.  dq and dk
+ *                      are summed with atomic adds (their rounding order varies);
+ *                      with cu_seqlens, rows outside every sequence are zero.
+ *   workspace          kda_chunk_bwd_workspace_size() bytes, 256-byte aligned.
+ *   flags              KDA_FLAG_SERIAL only (the q/k L2 norm, a cumsummed gate and
+ *                      the input activations take kda_recurrent_bwd /
+ *                      kda_recurrent_bwd_act).
+ * Supported: bf16, K = V = 128.  A chunk whose gate range is too wide raises
+ * KDA_DEVICE_GATE_RANGE in *dev_status.  Tensors 16-byte aligned.
+ */
+kda_status kda_chunk_bwd(const void *q, const void *k, const void *v, const float *g,
+                         const void *beta, const float *h0, const int32_t *cu_seqlens,
+                         const kda_shape *shape, const void *dout, const float *dht, float *dq,
+                         float *dk, float *dv, float *dg, float *dbeta, float *dh0,
+                         void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                         kda_stream_t stream);
+/* Bytes of workspace kda_chunk_bwd needs for *shape (0 on invalid shapes).  As for
+ * kda_chunk_workspace_size, a shape that may be packed (B == 1) is sized for packed
+ * input, which covers a dense call of the same shape too. */
+size_t kda_chunk_bwd_workspace_size(const kda_shape *shape);
 
 /*
  * kda_read_device_status -- synchronise `stream`, copy the status word to
