@@ -9,14 +9,16 @@ HBM before the timed region; a 512 MiB buffer is written between timed steps
 to flush the 129 MB L2.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload train|gva|packed|decode|decode_small|prefill|prefill_small|train_bwd]
+                  [--workload train|gva|packed|decode|decode_small|prefill|prefill_small|
+                              train_bwd|train_bwd_recurrent]
 
 `--workload` picks one of the other synthetic workloads instead (grouped value
 heads B4 T4096 HV32; packed varlen H=HV=32; decode 4096 x 1 token; its
 256-token prefill variant); decode and prefill steps are one in-place
-`kda_recurrent_fwd` call, and a train_bwd step is one `kda_recurrent_bwd` call
-(the gradients of the training shape's recurrence for dL/do and dL/dht drawn
-once).  `--impl reference` times the fp64 CPU oracle
+`kda_recurrent_fwd` call, a train_bwd step is one `kda_chunk_bwd` call (the
+gradients of the training shape for dL/do and dL/dht drawn once, in the chunked
+form on the tensor cores) and a train_bwd_recurrent step one `kda_recurrent_bwd`
+call (the same gradients by the token recurrence).  `--impl reference` times the fp64 CPU oracle
 instead, on the host cores, each step a bounded sample of the same workload.
 Under torchrun (N > 1) every rank runs its own replica of the workload (weak
 scaling, no collective on the data path); rank 0 prints the line with the
@@ -52,9 +54,12 @@ WORKLOADS = {
     "prefill_small": (4, {"T": 256, "B": 256, "decode_seqs": 256}, 20, 3),
     # decode on 512 of the 4096 sequences (1 GiB of state): the size an ncu capture takes
     "decode_small": (4, {"B": 512, "decode_seqs": 512}, 100, 5),
-    # gradients of the training shape's recurrence (kda_recurrent_bwd)
-    "train_bwd": (1, {}, 10, 3),
+    # gradients of the training shape: chunked on the tensor cores (kda_chunk_bwd) and
+    # by the token recurrence (kda_recurrent_bwd)
+    "train_bwd": (1, {}, 50, 5),
+    "train_bwd_recurrent": (1, {}, 10, 3),
 }
+BACKWARD = ("train_bwd", "train_bwd_recurrent")
 BWD_FLOPS_PER_ELEMENT = 26   # one forward pass (7) + the reverse sweep (19) per state element
 RECURRENT = ("decode", "decode_small", "prefill", "prefill_small")
 FP32_LANES_PER_SM = 128      # fp32 FMA lanes per SM (4 partitions x 32)
@@ -65,6 +70,8 @@ def _metric(name, w):
     if name == "train":
         return METRIC
     if name == "train_bwd":
+        return f"chunk_kda bwd tokens/s ({w.name}) on 1 GB300"
+    if name == "train_bwd_recurrent":
         return f"recurrent_kda bwd tokens/s ({w.name}) on 1 GB300"
     op = "recurrent_kda" if name in RECURRENT else "chunk_kda"
     return f"{op} fwd tokens/s ({w.name}) on 1 GB300"
@@ -145,6 +152,56 @@ def kernel_algorithmic_bytes(name, inp):
     if name.startswith("chunk_fused") or name.startswith("recurrent"):
         return r + wr
     return 0
+
+
+def chunk_bwd_bytes(inp):
+    """Compulsory HBM traffic of one chunked backward: q, k, v, g, beta, dL/do and
+    dL/dht read once; dq, dk, dv, dg, dbeta (fp32) and dh0 written once."""
+    w = inp["workload"]
+    reads = sum(_nbytes(inp[n]) for n in ("q", "k", "v", "g", "beta", "h0", "cu_seqlens"))
+    reads += _nbytes(inp["v"]) + inp["N"] * w.HV * w.K * w.V * 4          # do, dht
+    rows = inp["q"].shape[0] * inp["q"].shape[1]
+    writes = 4 * rows * (2 * w.H * w.K + w.HV * (w.V + w.K + 1))           # dq dk dv dg dbeta
+    writes += inp["N"] * w.HV * w.K * w.V * 4                              # dh0
+    return reads, writes
+
+
+def chunk_bwd_flops(inp):
+    """Useful tensor-core flops of one chunked backward per (64-row chunk, value
+    head), K = V = 128, counted from the products the seven stages form:
+    recompute + re-scan (the forward's 1.41e5 per token-head x 64), the reverse
+    state scan (Aqk^T do, kg dh, qg^T do, w^T dv': 7.3e6) and the per-chunk
+    gradients (P, do v'^T, [do; dv'] h^T, v' dh^T, dAkk, Akk^T [dv' | dw],
+    Akk^T dAkk, X Akk^T, [dP; dA] kn, dP^T kp + dA^T qp: 1.78e7)."""
+    w = inp["workload"]
+    units = inp["tokens"] / 64 * w.HV
+    return units * (64 * 1.41e5 + 7.3e6 + 1.78e7)
+
+
+def chunk_bwd_roofline(inp, per_kernel, prof_steps, ms, peaks, name):
+    """The whole call against the tighter of HBM (its compulsory bytes) and the bf16
+    tensor peak (its useful flops); the per-chunk gradient kernel, which reads and
+    writes almost all of those bytes, reported beside it."""
+    r, wr = chunk_bwd_bytes(inp)
+    flops = chunk_bwd_flops(inp)
+    t_hbm = (r + wr) / (peaks["hbm_gbs"] * 1e9)
+    t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+    sec = ms / 1e3
+    unit_ms = sum(t for n, (t, _) in per_kernel.items() if n.startswith("chunk_bwd_unit")) / prof_steps
+    out = {"kernel": "kda_chunk_bwd (all launches)", "kernel_ms": ms,
+           "hbm": {"achieved": (r + wr) / sec / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                   "frac": (r + wr) / sec / 1e9 / peaks["hbm_gbs"], "algorithmic_bytes": r + wr},
+           "tensor": {"achieved": flops / sec / 1e12, "peak": peaks["bf16_tflops"],
+                      "unit": "TFLOP/s", "frac": flops / sec / 1e12 / peaks["bf16_tflops"],
+                      "algorithmic_flops": flops},
+           "unit_kernel": {"ms": unit_ms,
+                           "gbs": (r + wr - _nbytes(inp["h0"])) / (unit_ms / 1e3) / 1e9
+                           if unit_ms > 0 else None},
+           "peak_source": peaks["source"], "traffic": _traffic("chunk_bwd_unit_tc", name)}
+    top = out["hbm"] if t_hbm >= t_tc else out["tensor"]
+    out.update({"bound": "hbm" if t_hbm >= t_tc else "tensor", "achieved": top["achieved"],
+                "peak": top["peak"], "unit": top["unit"], "frac": top["frac"]})
+    return out
 
 
 def recurrent_flops(inp):
@@ -271,7 +328,7 @@ def workload_config(name, world=1):
             "input_dtype": "bf16" if w.dtype == _bf16() else "f32", "gate_dtype": "f32",
             "h0": "N(0,0.1) fp32" if w.has_h0 else "none",
             "ht": "in place (ht == h0)" if recurrent else "stored",
-            "pass": "backward" if name == "train_bwd" else "forward",
+            "pass": "backward" if name in BACKWARD else "forward",
             "sequences": seqs, "tokens": tokens,
             "l2_flush": "512 MiB write between timed steps",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
@@ -424,20 +481,22 @@ def run_ours(args):
     status = kda.new_status(dev)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    backward = args.workload == "train_bwd"
+    backward = args.workload in BACKWARD
+    chunk_bwd = args.workload == "train_bwd"
     if backward:
         # dL/do and dL/dht drawn once; the gradients land in preallocated fp32 buffers.
         gen = torch.Generator(device=dev).manual_seed(11)
         dout = torch.randn(v.shape, generator=gen, device=dev).to(q.dtype)
         ht = torch.randn(inp["N"], w.HV, w.K, w.V, generator=gen, device=dev)  # dht
-        ws = torch.empty(kda.kda_recurrent_bwd_workspace_size(shape), dtype=torch.uint8,
-                         device=dev)
+        ws_bytes = (kda.kda_chunk_bwd_workspace_size(shape) if chunk_bwd
+                    else kda.kda_recurrent_bwd_workspace_size(shape))
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
         grads = [torch.empty(t.shape, dtype=torch.float32, device=dev) for t in (q, k, v, g, beta)]
         dh0 = torch.empty(inp["N"], w.HV, w.K, w.V, dtype=torch.float32, device=dev)
+        bwd_call = kda.kda_chunk_bwd if chunk_bwd else kda.kda_recurrent_bwd
 
         def call(q_, k_, v_, g_, beta_, h0_, o_, ht_, st):
-            kda.kda_recurrent_bwd(q_, k_, v_, g_, beta_, h0_, cu, shape, o_, ht_, *grads, dh0, ws,
-                                  status, st)
+            bwd_call(q_, k_, v_, g_, beta_, h0_, cu, shape, o_, ht_, *grads, dh0, ws, status, st)
         o = dout
     elif recurrent:
         # Decode keeps the state resident and updates it in place (ht == h0).
@@ -509,12 +568,14 @@ def run_ours(args):
     traffic = _traffic(dom, args.workload)
     r_b, w_b = algorithmic_bytes(inp)
     path_gbs = (r_b + w_b) / (ms / 1e3) / 1e9
-    if backward or args.workload.startswith("prefill"):
+    if (backward and not chunk_bwd) or args.workload.startswith("prefill"):
         # the fp32-bound kernels' denominator, measured here by an FMA-loop kernel
         peak = kda.kda_measure_fp32_fma_peak(stream)
         peak_source = ("measured in this run: FMA-loop microbenchmark "
                        "(kda_measure_fp32_fma_peak, 16 chains x 8x256 threads per SM)")
-    if backward:
+    if chunk_bwd:
+        roofline = chunk_bwd_roofline(inp, per_kernel, prof_steps, ms, peaks, args.workload)
+    elif backward:
         flops = BWD_FLOPS_PER_ELEMENT * inp["tokens"] * w.HV * w.K * w.V
         step_ms = sum(t for t, _ in per_kernel.values()) / prof_steps
         roofline = {"bound": "alu", "kernel": "recurrent_ckpt+recurrent_bwd",

@@ -82,8 +82,9 @@ struct DhuSmem {
     static constexpr uint32_t stage = dec + 512;
     static constexpr uint32_t stage_stride = (stage + 1023) / 1024 * 1024;
     static constexpr uint32_t dh = kStages * stage_stride;   // [KK][SBV] bf16 tile
-    static constexpr uint32_t dout = dh + KK * SBV * 2;      // two [64][SBV] tiles
-    static constexpr uint32_t dvp = dout + 2 * 64 * SBV * 2; // [64][SBV] tile
+    static constexpr int kDoBufs = 3;                        // do of chunks c, c - 1, c - 2
+    static constexpr uint32_t dout = dh + KK * SBV * 2;      // kDoBufs [64][SBV] tiles
+    static constexpr uint32_t dvp = dout + kDoBufs * 64 * SBV * 2;  // [64][SBV] tile
     static constexpr uint32_t total = dvp + 64 * SBV * 2;
     // TMEM columns: D1a at 0 / SBV, D1b at 2 SBV, D2a at 3 SBV / 4 SBV, D2b at 5 SBV.
     static constexpr uint32_t tmem_cols = 6 * SBV <= 256 ? 256 : 512;
@@ -110,7 +111,7 @@ __global__ void __launch_bounds__(320, 1) chunk_dhu_tc_kernel(BwdArgs a) {
     constexpr int kStages = S::kStages;
     const ChunkArgs &p = a.c;
     extern __shared__ __align__(1024) unsigned char sm[];
-    __shared__ uint64_t full[kStages], empty[kStages], do_full[2], bar_d1, bar_d2, bar_fin;
+    __shared__ uint64_t full[kStages], empty[kStages], do_full[S::kDoBufs], bar_d1, bar_d2, bar_fin;
     __shared__ uint32_t tslot;
     __shared__ int abort_flag;
 
@@ -148,8 +149,7 @@ __global__ void __launch_bounds__(320, 1) chunk_dhu_tc_kernel(BwdArgs a) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1 + 4);  // MMA commit + the dh warps (they read 2^G)
         }
-        mbar_init(&do_full[0], 4);
-        mbar_init(&do_full[1], 4);
+        for (int x = 0; x < S::kDoBufs; ++x) mbar_init(&do_full[x], 4);
         mbar_init(&bar_d1, 1);
         mbar_init(&bar_d2, 1);
         mbar_init(&bar_fin, 1);
@@ -209,9 +209,9 @@ __global__ void __launch_bounds__(320, 1) chunk_dhu_tc_kernel(BwdArgs a) {
         for (int i = 0; i < nc; ++i) {
             const int s = i % kStages;
             const uint32_t st = smem_addr(stage(i));
-            const uint64_t ddo = sdesc(smem_addr(sDo) + (i & 1) * 64 * SBV * 2, SBV * 16, 128);
+            const uint64_t ddo = sdesc(smem_addr(sDo) + (i % S::kDoBufs) * 64 * SBV * 2, SBV * 16, 128);
             wait_copy(&full[s], (i / kStages) & 1);
-            wait_copy(&do_full[i & 1], (i >> 1) & 1);
+            wait_copy(&do_full[i % S::kDoBufs], (i / S::kDoBufs) & 1);
             __syncwarp();
             bool go = !read_flag(&abort_flag);
             if (elect_one()) {
@@ -315,24 +315,37 @@ __global__ void __launch_bounds__(320, 1) chunk_dhu_tc_kernel(BwdArgs a) {
         const int r = 16 * q + (lane & 15);
         const uint32_t lanebase = (uint32_t)(32 * q) << 16;
         const __nv_bfloat16 *dout = static_cast<const __nv_bfloat16 *>(a.dout);
-        // do rows of chunk c into tile buf: 64 rows x SBV / 8 pieces of 16 bytes
-        auto load_do = [&](int c, int buf) {
-            const int row0 = bos + c * kBT;
-            const int nr = min(kBT, eos - row0);
-            unsigned char *dst = sDo + buf * 64 * SBV * 2;
-            for (int pc = t128; pc < 64 * (SBV / 8); pc += 128) {
-                const int rr = pc / (SBV / 8), ch = (pc % (SBV / 8)) * 8;
-                uint4 x = make_uint4(0, 0, 0, 0);
-                if (rr < nr)
-                    x = *reinterpret_cast<const uint4 *>(
-                        dout + (((size_t)b * p.T + row0 + rr) * p.HV + hv) * p.V + vb * SBV + ch);
-                *reinterpret_cast<uint4 *>(dst + tile_off(rr, ch, SBV)) = x;
+        // do rows of chunk c into tile buf by 16-byte cp.async (zero fill past the
+        // sequence), one commit group per chunk; issued two rounds ahead so that the
+        // loads' latency stays off the chain
+        auto issue_do = [&](int c, int buf) {
+            if (c >= 0) {
+                const int row0 = bos + c * kBT;
+                const int nr = min(kBT, eos - row0);
+                unsigned char *dst = sDo + buf * 64 * SBV * 2;
+                for (int pc = t128; pc < 64 * (SBV / 8); pc += 128) {
+                    const int rr = pc / (SBV / 8), ch = (pc % (SBV / 8)) * 8;
+                    const __nv_bfloat16 *src =
+                        dout + (((size_t)b * p.T + row0 + (rr < nr ? rr : 0)) * p.HV + hv) * p.V +
+                        vb * SBV + ch;
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                                     smem_addr(dst + tile_off(rr, ch, SBV))),
+                                 "l"(src), "r"(rr < nr ? 16 : 0)
+                                 : "memory");
+                }
             }
+            asm volatile("cp.async.commit_group;" ::: "memory");
+        };
+        // the oldest group in flight (chunk c's) has landed: hand its tile to the MMAs
+        auto publish_do = [&](int buf) {
+            asm volatile("cp.async.wait_group 1;" ::: "memory");
             fence_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&do_full[buf]);
         };
-        if (nc > 0) load_do(nc - 1, 0);
+        issue_do(nc - 1, 0);
+        issue_do(nc - 2, 1);
+        if (nc > 0) publish_do(0);
         for (int i = 0; i < nc; ++i) {
             const int c = nc - 1 - i;
             wait_mma(&bar_d1, i & 1);
@@ -361,11 +374,13 @@ __global__ void __launch_bounds__(320, 1) chunk_dhu_tc_kernel(BwdArgs a) {
             fence_async_smem();
             __syncwarp();
             named_arrive(kDhuBarV, 128 + 32);
-            // the other do tile was last read by round i - 1's MMAs, complete once
+            // tile (i + 2) % 3 was last read by round i - 1's MMAs, complete once
             // bar_d1 of round i fired
-            if (i + 1 < nc) load_do(c - 1, (i + 1) & 1);
+            issue_do(c - 2, (i + 2) % S::kDoBufs);
+            if (i + 1 < nc) publish_do((i + 1) % S::kDoBufs);
         }
     }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, S::tmem_cols);
@@ -422,20 +437,24 @@ __device__ __forceinline__ void add8(float *dst, const float (&x)[8]) {
     atomicAdd(reinterpret_cast<float4 *>(dst + 4), make_float4(x[4], x[5], x[6], x[7]));
 }
 
-// One CTA per (chunk, value head).  Epilogue threads read accumulators with
-// 32-lane TMEM loads: for an M = 128 result, warp w reaches rows 32 (w % 4) .. + 31,
-// warps w and w + 4 take one half of the columns each; for an M = 64 result row r
-// sits in lane 32 (r / 16) + r % 16, so lanes 0..15 of every warp hold a row.
+// One CTA of 16 warps per (chunk, value head).  Epilogue threads read accumulators
+// with 32-lane TMEM loads: warp w reaches lanes 32 (w % 4) .. + 31 and the four
+// warps of a lane quadrant take a quarter of the columns each.  For an M = 128
+// result that is rows 32 (w % 4) .. + 31; for an M = 64 result row r sits in lane
+// 32 (r / 16) + r % 16, so lanes 0..15 of every warp hold a row.
+constexpr int kUnitThreads = 512;
+
 template <int KK, int VV>
-__global__ void __launch_bounds__(256, 1) chunk_bwd_unit_tc_kernel(BwdArgs a) {
+__global__ void __launch_bounds__(kUnitThreads, 1) chunk_bwd_unit_tc_kernel(BwdArgs a) {
     using S = UnitSmem<KK, VV>;
+    constexpr int NT = kUnitThreads;
     const ChunkArgs &p = a.c;
     extern __shared__ __align__(1024) unsigned char sm[];
     __shared__ uint64_t bar_ld, bar_mma;
     __shared__ uint32_t tslot;
     __shared__ int range_bad;
 
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, quad = warp & 3, half = warp >> 2;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, quad = warp & 3, part = warp >> 2;
     const int64_t unit = blockIdx.x;
     const int hv = (int)(unit / p.slots);
     const int64_t gc = unit % p.slots;
@@ -474,35 +493,65 @@ __global__ void __launch_bounds__(256, 1) chunk_bwd_unit_tc_kernel(BwdArgs a) {
         bulk_g2s(sm + S::akk, static_cast<const unsigned char *>(p.units) + ui * (int64_t)Lo.stride + Lo.akk,
                  64 * 64 * 2, &bar_ld);
     }
-    // g rows (fp32), beta, v and do rows
     const size_t rowbase = (size_t)b * p.T + row0;
-    for (int pc = tid; pc < 64 * (KK / 4); pc += 256) {
-        const int r = pc / (KK / 4), c = (pc % (KK / 4)) * 4;
-        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (r < nr && c < p.K)
-            x = *reinterpret_cast<const float4 *>(p.g + ((rowbase + r) * p.HV + hv) * p.K + c);
-        *reinterpret_cast<float4 *>(sG + fsw<KK>(r, c)) = x;
-    }
-    if (tid < 64) {
-        float bt = 0.f;
-        if (tid < nr)
-            bt = to_f32(static_cast<const __nv_bfloat16 *>(p.beta)[(rowbase + tid) * p.HV + hv]);
-        sBeta[tid] = bt;
-        sDbeta[tid] = 0.f;
+    // Input rows: every load of a thread is issued before its first store, so that
+    // their latencies overlap; q and k stay in registers across the cumsum.
+    constexpr int kQkIt = 64 * (KK / 8) / NT;
+    uint4 qraw[kQkIt], kraw[kQkIt];
+    {
+        const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(p.q);
+        const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(p.k);
+#pragma unroll
+        for (int it = 0; it < kQkIt; ++it) {
+            const int pc = tid + it * NT, r = pc / (KK / 8), c = (pc % (KK / 8)) * 8;
+            qraw[it] = kraw[it] = make_uint4(0, 0, 0, 0);
+            if (r < nr && c < p.K) {
+                const size_t off = ((rowbase + r) * p.H + hq) * p.K + c;
+                qraw[it] = *reinterpret_cast<const uint4 *>(q + off);
+                kraw[it] = *reinterpret_cast<const uint4 *>(k + off);
+            }
+        }
     }
     {
+        constexpr int kGIt = 64 * (KK / 4) / NT, kVIt = 64 * (VV / 8) / NT;
         const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(p.v);
         const __nv_bfloat16 *dout = static_cast<const __nv_bfloat16 *>(a.dout);
-        for (int pc = tid; pc < 64 * (VV / 8); pc += 256) {
-            const int r = pc / (VV / 8), c = (pc % (VV / 8)) * 8;
-            uint4 x = make_uint4(0, 0, 0, 0), y = make_uint4(0, 0, 0, 0);
+        float4 x[kGIt];
+        uint4 y[kVIt], z[kVIt];
+#pragma unroll
+        for (int it = 0; it < kGIt; ++it) {
+            const int pc = tid + it * NT, r = pc / (KK / 4), c = (pc % (KK / 4)) * 4;
+            x[it] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (r < nr && c < p.K)
+                x[it] = *reinterpret_cast<const float4 *>(p.g + ((rowbase + r) * p.HV + hv) * p.K + c);
+        }
+#pragma unroll
+        for (int it = 0; it < kVIt; ++it) {
+            const int pc = tid + it * NT, r = pc / (VV / 8), c = (pc % (VV / 8)) * 8;
+            y[it] = z[it] = make_uint4(0, 0, 0, 0);
             if (r < nr) {
                 const size_t off = ((rowbase + r) * p.HV + hv) * p.V + c;
-                x = *reinterpret_cast<const uint4 *>(v + off);
-                y = *reinterpret_cast<const uint4 *>(dout + off);
+                y[it] = *reinterpret_cast<const uint4 *>(v + off);
+                z[it] = *reinterpret_cast<const uint4 *>(dout + off);
             }
-            *reinterpret_cast<uint4 *>(sm + S::vt + tile_off(r, c, VV)) = x;
-            *reinterpret_cast<uint4 *>(sm + S::dout + tile_off(r, c, VV)) = y;
+        }
+        if (tid < 64) {
+            float bt = 0.f;
+            if (tid < nr)
+                bt = to_f32(static_cast<const __nv_bfloat16 *>(p.beta)[(rowbase + tid) * p.HV + hv]);
+            sBeta[tid] = bt;
+            sDbeta[tid] = 0.f;
+        }
+#pragma unroll
+        for (int it = 0; it < kGIt; ++it) {
+            const int pc = tid + it * NT, r = pc / (KK / 4), c = (pc % (KK / 4)) * 4;
+            *reinterpret_cast<float4 *>(sG + fsw<KK>(r, c)) = x[it];
+        }
+#pragma unroll
+        for (int it = 0; it < kVIt; ++it) {
+            const int pc = tid + it * NT, r = pc / (VV / 8), c = (pc % (VV / 8)) * 8;
+            *reinterpret_cast<uint4 *>(sm + S::vt + tile_off(r, c, VV)) = y[it];
+            *reinterpret_cast<uint4 *>(sm + S::dout + tile_off(r, c, VV)) = z[it];
         }
     }
     __syncthreads();
@@ -530,35 +579,26 @@ __global__ void __launch_bounds__(256, 1) chunk_bwd_unit_tc_kernel(BwdArgs a) {
         return;
     }
     // q, k rows -> kp, kn, qp tiles
-    {
-        const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(p.q);
-        const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(p.k);
-        for (int pc = tid; pc < 64 * (KK / 8); pc += 256) {
-            const int r = pc / (KK / 8), c = (pc % (KK / 8)) * 8;
-            float fq[8], fk[8];
-            if (r < nr && c < p.K) {
-                const size_t off = ((rowbase + r) * p.H + hq) * p.K + c;
-                unpack8(*reinterpret_cast<const uint4 *>(q + off), fq);
-                unpack8(*reinterpret_cast<const uint4 *>(k + off), fk);
-            } else {
 #pragma unroll
-                for (int j = 0; j < 8; ++j) fq[j] = fk[j] = 0.f;
-            }
-            const float4 g0 = *reinterpret_cast<const float4 *>(sG + fsw<KK>(r, c));
-            const float4 g1 = *reinterpret_cast<const float4 *>(sG + fsw<KK>(r, c + 4));
-            const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-            float kp[8], kn[8], qp[8];
+    for (int it = 0; it < kQkIt; ++it) {
+        const int pc = tid + it * NT, r = pc / (KK / 8), c = (pc % (KK / 8)) * 8;
+        float fq[8], fk[8];
+        unpack8(qraw[it], fq);
+        unpack8(kraw[it], fk);
+        const float4 g0 = *reinterpret_cast<const float4 *>(sG + fsw<KK>(r, c));
+        const float4 g1 = *reinterpret_cast<const float4 *>(sG + fsw<KK>(r, c + 4));
+        const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+        float kp[8], kn[8], qp[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float e = ex2f(gg[j]), ei = ex2f(-gg[j]);
-                kp[j] = fk[j] * e;
-                kn[j] = fk[j] * ei;
-                qp[j] = fq[j] * e;
-            }
-            *reinterpret_cast<uint4 *>(sm + S::kp + tile_off(r, c, KK)) = pack8(kp);
-            *reinterpret_cast<uint4 *>(sm + S::kn + tile_off(r, c, KK)) = pack8(kn);
-            *reinterpret_cast<uint4 *>(sm + S::qp + tile_off(r, c, KK)) = pack8(qp);
+        for (int j = 0; j < 8; ++j) {
+            const float e = ex2f(gg[j]), ei = ex2f(-gg[j]);
+            kp[j] = fk[j] * e;
+            kn[j] = fk[j] * ei;
+            qp[j] = fq[j] * e;
         }
+        *reinterpret_cast<uint4 *>(sm + S::kp + tile_off(r, c, KK)) = pack8(kp);
+        *reinterpret_cast<uint4 *>(sm + S::kn + tile_off(r, c, KK)) = pack8(kn);
+        *reinterpret_cast<uint4 *>(sm + S::qp + tile_off(r, c, KK)) = pack8(qp);
     }
     fence_async_smem();
     __syncthreads();
@@ -577,6 +617,7 @@ __global__ void __launch_bounds__(256, 1) chunk_bwd_unit_tc_kernel(BwdArgs a) {
     // K-major tile [rows][C]: per K = 16 step +256 bytes; MN-major: +2 C * 16 bytes.
     auto kmaj = [&](uint32_t off, int C) { return sdesc(s0 + off, 128, C * 16); };
     auto mnmaj = [&](uint32_t off, int C) { return sdesc(s0 + off, C * 16, 128); };
+    auto tl = [&](uint32_t col) { return tmem_at(tmem, 32 * quad, col); };
 
     // ---- P = kp kn^T, do v'^T, [do; dv'] h^T, v' dh^T
     if (tid == 0) {
@@ -590,11 +631,12 @@ __global__ void __launch_bounds__(256, 1) chunk_bwd_unit_tc_kernel(BwdArgs a) {
                                      idesc_bf16(64, KK, false, false));
         mma_commit(&bar_mma);
     }
-    // meanwhile: ln2 2^G rowsum(h . dh_{c+1}) per channel, two threads a row
+    // meanwhile: ln2 2^G rowsum(h . dh_{c+1}) per channel, four threads a row
     {
-        const int d = tid >> 1, j0 = (tid & 1) * (VV / 2);
+        const int d = tid >> 2, j0 = (tid & 3) * (VV / 4);
         float acc = 0.f;
-        for (int j = j0; j < j0 + VV / 2; j += 8) {
+#pragma unroll
+        for (int j = j0; j < j0 + VV / 4; j += 8) {
             float x[8], y[8];
             unpack8(sm + S::h + tile_off(d, j, VV), x);
             unpack8(sm + S::dhn + tile_off(d, j, VV), y);
@@ -602,13 +644,13 @@ __global__ void __launch_bounds__(256, 1) chunk_bwd_unit_tc_kernel(BwdArgs a) {
             for (int t = 0; t < 8; ++t) acc = fmaf(x[t], y[t], acc);
         }
         acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-        if ((tid & 1) == 0 && d < KK) sDG[d] = kLn2 * ex2f(sGl[d]) * acc;
+        acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+        if ((tid & 3) == 0 && d < KK) sDG[d] = kLn2 * ex2f(sGl[d]) * acc;
     }
     mma_wait();
     __syncthreads();
 
     const float scale = p.scale;
-    float *dq_row = nullptr, *dk_row = nullptr;
     auto grow = [&](float *base, int r) { return base + ((rowbase + r) * p.H + hq) * p.K; };
     auto g2v = [&](int r, int c, float (&o)[8]) {
         const float4 x = *reinterpret_cast<const float4 *>(sG + fsw<KK>(r, c));
@@ -629,92 +671,86 @@ __global__ void __launch_bounds__(256, 1) chunk_bwd_unit_tc_kernel(BwdArgs a) {
             *d1 = v;
         }
     };
+    // Rows of this thread in an M = 64 result, and in the top / bottom half of an
+    // M = 128 result; the first of its columns in a result N wide.
+    const int r64 = 16 * quad + (lane & 15), r128 = 32 * (quad & 1) + lane;
+    const bool live64 = lane < 16, top = quad < 2;
+    auto col0 = [&](int N) { return part * (N / 4); };
 
-    // ---- E1a: dqg = scale do h^T (rows 0..63 of the M = 128 result) -> dq, dg2;
+    // ---- dqg = scale do h^T (rows 0..63 of the M = 128 result) -> dq, dg2;
     //      dw = -(dv' h^T) (rows 64..127) -> bf16 tile; dA = scale tril(do v'^T)
-    if (quad < 2) {
-        const int r = 32 * quad + lane;
-        for (int cb = 0; cb < KK / 2; cb += 32) {
-            const int c0 = half * (KK / 2) + cb;
-            float d[32];
-            tmem_ld32(tmem_at(tmem, 32 * quad, 128 + c0), d);
+    {
+        const int c0 = col0(KK);
+        float d[KK / 4];
+        tmem_ld32(tl(128 + c0), d);
+        if (top) {
 #pragma unroll
-            for (int c8 = 0; c8 < 32; c8 += 8) {
+            for (int c8 = 0; c8 < KK / 4; c8 += 8) {
                 float gg[8], qp[8], dq8[8], dg8[8];
-                g2v(r, c0 + c8, gg);
-                unpack8(sm + S::qp + tile_off(r, c0 + c8, KK), qp);
+                g2v(r128, c0 + c8, gg);
+                unpack8(sm + S::qp + tile_off(r128, c0 + c8, KK), qp);
 #pragma unroll
                 for (int t = 0; t < 8; ++t) {
                     const float x = scale * d[c8 + t];
                     dq8[t] = x * ex2f(gg[t]);
                     dg8[t] = kLn2 * x * qp[t];
                 }
-                if (r < nr && c0 + c8 < p.K) add8(grow(a.dq, r) + c0 + c8, dq8);
-                dg2_add(r, c0 + c8, dg8, true);
+                if (r128 < nr && c0 + c8 < p.K) add8(grow(a.dq, r128) + c0 + c8, dq8);
+                dg2_add(r128, c0 + c8, dg8, true);
             }
-        }
-    } else {
-        const int r = 32 * (quad - 2) + lane;
-        for (int cb = 0; cb < KK / 2; cb += 32) {
-            const int c0 = half * (KK / 2) + cb;
-            float d[32];
-            tmem_ld32(tmem_at(tmem, 32 * quad, 128 + c0), d);
+        } else {
 #pragma unroll
-            for (int t = 0; t < 32; ++t) d[t] = -d[t];
+            for (int t = 0; t < KK / 4; ++t) d[t] = -d[t];
 #pragma unroll
-            for (int c8 = 0; c8 < 32; c8 += 8)
-                *reinterpret_cast<uint4 *>(sm + S::dw + tile_off(r, c0 + c8, KK)) = pack8_at(d + c8);
+            for (int c8 = 0; c8 < KK / 4; c8 += 8)
+                *reinterpret_cast<uint4 *>(sm + S::dw + tile_off(r128, c0 + c8, KK)) = pack8_at(d + c8);
         }
     }
     {
-        const int r = 16 * quad + (lane & 15);
-        float d[32];
-        tmem_ld32(tmem_at(tmem, 32 * quad, 64 + half * 32), d);
-        if (lane < 16) {
+        const int c0 = col0(64);
+        float d[16];
+        tmem_ld16(tl(64 + c0), d);
+        if (live64) {
 #pragma unroll
-            for (int t = 0; t < 32; ++t) d[t] = (half * 32 + t <= r) ? scale * d[t] : 0.f;
+            for (int t = 0; t < 16; ++t) d[t] = (c0 + t <= r64) ? scale * d[t] : 0.f;
 #pragma unroll
-            for (int c8 = 0; c8 < 32; c8 += 8)
-                *reinterpret_cast<uint4 *>(sm + S::dap + tile_off(64 + r, half * 32 + c8, 64)) =
+            for (int c8 = 0; c8 < 16; c8 += 8)
+                *reinterpret_cast<uint4 *>(sm + S::dap + tile_off(64 + r64, c0 + c8, 64)) =
                     pack8_at(d + c8);
         }
     }
     __syncthreads();
-    // ---- E1b: dkg = v' dh^T (M = 64) -> dk, dg2, and the G terms
+    // ---- dkg = v' dh^T (M = 64) -> dk, dg2, and the G terms
     {
-        const int r = 16 * quad + (lane & 15);
-        const bool live = lane < 16;
-        for (int cb = 0; cb < KK / 2; cb += 32) {
-            const int c0 = half * (KK / 2) + cb;
-            float d[32];
-            tmem_ld32(tmem_at(tmem, 32 * quad, 256 + c0), d);
+        const int c0 = col0(KK);
+        float d[KK / 4];
+        tmem_ld32(tl(256 + c0), d);
 #pragma unroll
-            for (int c8 = 0; c8 < 32; c8 += 8) {
-                float gg[8], kn[8], dk8[8], dg8[8], colp[8];
-                g2v(r, c0 + c8, gg);
-                unpack8(sm + S::kn + tile_off(r, c0 + c8, KK), kn);
+        for (int c8 = 0; c8 < KK / 4; c8 += 8) {
+            float gg[8], kn[8], dk8[8], dg8[8], colp[8];
+            g2v(r64, c0 + c8, gg);
+            unpack8(sm + S::kn + tile_off(r64, c0 + c8, KK), kn);
 #pragma unroll
-                for (int t = 0; t < 8; ++t) {
-                    const float gl = sGl[c0 + c8 + t];
-                    const float x = live ? d[c8 + t] : 0.f;
-                    dk8[t] = x * ex2f(gl - gg[t]);
-                    const float kgx = x * kn[t] * ex2f(gl);   // dkg . kg
-                    dg8[t] = -kLn2 * kgx;
-                    colp[t] = kLn2 * kgx;
-                }
-                if (live) {
-                    if (r < nr && c0 + c8 < p.K) add8(grow(a.dk, r) + c0 + c8, dk8);
-                    dg2_add(r, c0 + c8, dg8, false);
-                }
+            for (int t = 0; t < 8; ++t) {
+                const float gl = sGl[c0 + c8 + t];
+                const float x = live64 ? d[c8 + t] : 0.f;
+                dk8[t] = x * ex2f(gl - gg[t]);
+                const float kgx = x * kn[t] * ex2f(gl);   // dkg . kg
+                dg8[t] = -kLn2 * kgx;
+                colp[t] = kLn2 * kgx;
+            }
+            if (live64) {
+                if (r64 < nr && c0 + c8 < p.K) add8(grow(a.dk, r64) + c0 + c8, dk8);
+                dg2_add(r64, c0 + c8, dg8, false);
+            }
 #pragma unroll
-                for (int t = 0; t < 8; ++t) {
-                    float s = colp[t];
-                    s += __shfl_xor_sync(0xffffffffu, s, 1);
-                    s += __shfl_xor_sync(0xffffffffu, s, 2);
-                    s += __shfl_xor_sync(0xffffffffu, s, 4);
-                    s += __shfl_xor_sync(0xffffffffu, s, 8);
-                    if (lane == 0) atomicAdd(&sDG[c0 + c8 + t], s);
-                }
+            for (int t = 0; t < 8; ++t) {
+                float s = colp[t];
+                s += __shfl_xor_sync(0xffffffffu, s, 1);
+                s += __shfl_xor_sync(0xffffffffu, s, 2);
+                s += __shfl_xor_sync(0xffffffffu, s, 4);
+                s += __shfl_xor_sync(0xffffffffu, s, 8);
+                if (lane == 0) atomicAdd(&sDG[c0 + c8 + t], s);
             }
         }
     }
@@ -736,43 +772,41 @@ __global__ void __launch_bounds__(256, 1) chunk_bwd_unit_tc_kernel(BwdArgs a) {
         mma_commit(&bar_mma);
     }
     mma_wait();
-    // ---- E2: dv = diag(beta) Akk^T dv'; dkgate = diag(beta) Akk^T dw; dbeta; dAkk tile
+    // ---- dv = diag(beta) Akk^T dv'; dkgate = diag(beta) Akk^T dw; dbeta; dAkk tile
     {
-        const int r = 16 * quad + (lane & 15);
-        const bool live = lane < 16;
-        const float br = sBeta[r];
+        const float br = sBeta[r64];
         float db = 0.f;
-        for (int cb = 0; cb < VV / 2; cb += 32) {
-            const int c0 = half * (VV / 2) + cb;
-            float d[32];
-            tmem_ld32(tmem_at(tmem, 32 * quad, 128 + c0), d);
-            if (live) {
-                float *dvr = a.dv + ((rowbase + r) * p.HV + hv) * p.V + c0;
+        {
+            const int c0 = col0(VV);
+            float d[VV / 4];
+            tmem_ld32(tl(128 + c0), d);
+            if (live64) {
+                float *dvr = a.dv + ((rowbase + r64) * p.HV + hv) * p.V + c0;
 #pragma unroll
-                for (int c8 = 0; c8 < 32; c8 += 8) {
+                for (int c8 = 0; c8 < VV / 4; c8 += 8) {
                     float vv[8];
-                    unpack8(sm + S::vt + tile_off(r, c0 + c8, VV), vv);
+                    unpack8(sm + S::vt + tile_off(r64, c0 + c8, VV), vv);
 #pragma unroll
                     for (int t = 0; t < 8; ++t) db = fmaf(d[c8 + t], vv[t], db);
                 }
-                if (r < nr) {
+                if (r64 < nr) {
 #pragma unroll
-                    for (int t = 0; t < 32; t += 4)
+                    for (int t = 0; t < VV / 4; t += 4)
                         *reinterpret_cast<float4 *>(dvr + t) =
                             make_float4(br * d[t], br * d[t + 1], br * d[t + 2], br * d[t + 3]);
                 }
             }
         }
-        for (int cb = 0; cb < KK / 2; cb += 32) {
-            const int c0 = half * (KK / 2) + cb;
-            float d[32];
-            tmem_ld32(tmem_at(tmem, 32 * quad, 256 + c0), d);
-            if (live) {
+        {
+            const int c0 = col0(KK);
+            float d[KK / 4];
+            tmem_ld32(tl(256 + c0), d);
+            if (live64) {
 #pragma unroll
-                for (int c8 = 0; c8 < 32; c8 += 8) {
+                for (int c8 = 0; c8 < KK / 4; c8 += 8) {
                     float gg[8], kp[8], dk8[8], dg8[8];
-                    g2v(r, c0 + c8, gg);
-                    unpack8(sm + S::kp + tile_off(r, c0 + c8, KK), kp);
+                    g2v(r64, c0 + c8, gg);
+                    unpack8(sm + S::kp + tile_off(r64, c0 + c8, KK), kp);
 #pragma unroll
                     for (int t = 0; t < 8; ++t) {
                         db = fmaf(d[c8 + t], kp[t], db);
@@ -780,22 +814,23 @@ __global__ void __launch_bounds__(256, 1) chunk_bwd_unit_tc_kernel(BwdArgs a) {
                         dk8[t] = x * ex2f(gg[t]);
                         dg8[t] = kLn2 * x * kp[t];
                     }
-                    if (r < nr && c0 + c8 < p.K) add8(grow(a.dk, r) + c0 + c8, dk8);
-                    dg2_add(r, c0 + c8, dg8, false);
+                    if (r64 < nr && c0 + c8 < p.K) add8(grow(a.dk, r64) + c0 + c8, dk8);
+                    dg2_add(r64, c0 + c8, dg8, false);
                 }
             }
         }
         {
-            float d[32];
-            tmem_ld32(tmem_at(tmem, 32 * quad, 384 + half * 32), d);
-            if (live) {
+            const int c0 = col0(64);
+            float d[16];
+            tmem_ld16(tl(384 + c0), d);
+            if (live64) {
 #pragma unroll
-                for (int t = 0; t < 32; ++t) d[t] *= sBeta[half * 32 + t];
+                for (int t = 0; t < 16; ++t) d[t] *= sBeta[c0 + t];
 #pragma unroll
-                for (int c8 = 0; c8 < 32; c8 += 8)
-                    *reinterpret_cast<uint4 *>(sm + S::dakk + tile_off(r, half * 32 + c8, 64)) =
+                for (int c8 = 0; c8 < 16; c8 += 8)
+                    *reinterpret_cast<uint4 *>(sm + S::dakk + tile_off(r64, c0 + c8, 64)) =
                         pack8_at(d + c8);
-                atomicAdd(&sDbeta[r], db);
+                atomicAdd(&sDbeta[r64], db);
             }
         }
     }
@@ -811,13 +846,13 @@ __global__ void __launch_bounds__(256, 1) chunk_bwd_unit_tc_kernel(BwdArgs a) {
     }
     mma_wait();
     {
-        const int r = 16 * quad + (lane & 15);
-        float d[32];
-        tmem_ld32(tmem_at(tmem, 32 * quad, 448 + half * 32), d);
-        if (lane < 16) {
+        const int c0 = col0(64);
+        float d[16];
+        tmem_ld16(tl(448 + c0), d);
+        if (live64) {
 #pragma unroll
-            for (int c8 = 0; c8 < 32; c8 += 8)
-                *reinterpret_cast<uint4 *>(sm + S::xt + tile_off(r, half * 32 + c8, 64)) = pack8_at(d + c8);
+            for (int c8 = 0; c8 < 16; c8 += 8)
+                *reinterpret_cast<uint4 *>(sm + S::xt + tile_off(r64, c0 + c8, 64)) = pack8_at(d + c8);
         }
     }
     fence_async_smem();
@@ -831,25 +866,25 @@ __global__ void __launch_bounds__(256, 1) chunk_bwd_unit_tc_kernel(BwdArgs a) {
         mma_commit(&bar_mma);
     }
     mma_wait();
-    // ---- E4: dL = -strictly_tril(Y); dbeta += rowsum(dL . P); dP = diag(beta) dL
+    // ---- dL = -strictly_tril(Y); dbeta += rowsum(dL . P); dP = diag(beta) dL
     {
-        const int r = 16 * quad + (lane & 15);
-        float y[32], pp[32];
-        tmem_ld32(tmem_at(tmem, 32 * quad, 64 + half * 32), y);
-        tmem_ld32(tmem_at(tmem, 32 * quad, 0 + half * 32), pp);
-        if (lane < 16) {
-            const float br = sBeta[r];
+        const int c0 = col0(64);
+        float y[16], pp[16];
+        tmem_ld16(tl(64 + c0), y);
+        tmem_ld16(tl(0 + c0), pp);
+        if (live64) {
+            const float br = sBeta[r64];
             float db = 0.f;
 #pragma unroll
-            for (int t = 0; t < 32; ++t) {
-                const float dl = (half * 32 + t < r) ? -y[t] : 0.f;
+            for (int t = 0; t < 16; ++t) {
+                const float dl = (c0 + t < r64) ? -y[t] : 0.f;
                 db = fmaf(dl, pp[t], db);
                 y[t] = br * dl;
             }
 #pragma unroll
-            for (int c8 = 0; c8 < 32; c8 += 8)
-                *reinterpret_cast<uint4 *>(sm + S::dap + tile_off(r, half * 32 + c8, 64)) = pack8_at(y + c8);
-            atomicAdd(&sDbeta[r], db);
+            for (int c8 = 0; c8 < 16; c8 += 8)
+                *reinterpret_cast<uint4 *>(sm + S::dap + tile_off(r64, c0 + c8, 64)) = pack8_at(y + c8);
+            atomicAdd(&sDbeta[r64], db);
         }
     }
     fence_async_smem();
@@ -867,57 +902,52 @@ __global__ void __launch_bounds__(256, 1) chunk_bwd_unit_tc_kernel(BwdArgs a) {
         mma_commit(&bar_mma);
     }
     mma_wait();
-    // ---- E5: (dP kn) 2^g2 -> dk, (dA kn) 2^g2 -> dq, (dP^T kp + dA^T qp) 2^-g2 -> dk,
-    // and their dg2 terms, in three passes so that no two threads share a dg2 element.
+    // ---- (dP kn) 2^g2 -> dk, (dA kn) 2^g2 -> dq, (dP^T kp + dA^T qp) 2^-g2 -> dk, and
+    // their dg2 terms, in three passes so that no two threads share a dg2 element.
     // Pass 0: rows 0..63 of the M = 128 result (dP kn) -> dk, dg2; rows 64..127
     // (dA kn) -> dq.  Pass 1: rows 64..127 -> dg2.
-    for (int pass = 0; pass < 2; ++pass) {
-        const bool top = quad < 2;
-        const int r = 32 * (quad & 1) + lane;
-        if (pass == 0 || !top) {
-            for (int cb = 0; cb < KK / 2; cb += 32) {
-                const int c0 = half * (KK / 2) + cb;
-                float d[32];
-                tmem_ld32(tmem_at(tmem, 32 * quad, 128 + c0), d);
+    {
+        const int c0 = col0(KK);
+        float d[KK / 4];
+        tmem_ld32(tl(128 + c0), d);
 #pragma unroll
-                for (int c8 = 0; c8 < 32; c8 += 8) {
+        for (int pass = 0; pass < 2; ++pass) {
+            if (pass == 0 || !top) {
+#pragma unroll
+                for (int c8 = 0; c8 < KK / 4; c8 += 8) {
                     float gg[8], fac[8], g8[8], dg8[8];
-                    g2v(r, c0 + c8, gg);
-                    unpack8(sm + (top ? S::kp : S::qp) + tile_off(r, c0 + c8, KK), fac);
+                    g2v(r128, c0 + c8, gg);
+                    unpack8(sm + (top ? S::kp : S::qp) + tile_off(r128, c0 + c8, KK), fac);
 #pragma unroll
                     for (int t = 0; t < 8; ++t) {
                         g8[t] = d[c8 + t] * ex2f(gg[t]);
                         dg8[t] = kLn2 * d[c8 + t] * fac[t];
                     }
-                    if (pass == 0 && r < nr && c0 + c8 < p.K)
-                        add8(grow(top ? a.dk : a.dq, r) + c0 + c8, g8);
-                    if (pass == 0 ? top : !top) dg2_add(r, c0 + c8, dg8, false);
+                    if (pass == 0 && r128 < nr && c0 + c8 < p.K)
+                        add8(grow(top ? a.dk : a.dq, r128) + c0 + c8, g8);
+                    if (pass == 0 ? top : !top) dg2_add(r128, c0 + c8, dg8, false);
                 }
             }
+            __syncthreads();
         }
-        __syncthreads();
     }
     {
-        const int r = 16 * quad + (lane & 15);
-        const bool live = lane < 16;
-        for (int cb = 0; cb < KK / 2; cb += 32) {
-            const int c0 = half * (KK / 2) + cb;
-            float d[32];
-            tmem_ld32(tmem_at(tmem, 32 * quad, 256 + c0), d);
-            if (live) {
+        const int c0 = col0(KK);
+        float d[KK / 4];
+        tmem_ld32(tl(256 + c0), d);
+        if (live64) {
 #pragma unroll
-                for (int c8 = 0; c8 < 32; c8 += 8) {
-                    float gg[8], kn[8], dk8[8], dg8[8];
-                    g2v(r, c0 + c8, gg);
-                    unpack8(sm + S::kn + tile_off(r, c0 + c8, KK), kn);
+            for (int c8 = 0; c8 < KK / 4; c8 += 8) {
+                float gg[8], kn[8], dk8[8], dg8[8];
+                g2v(r64, c0 + c8, gg);
+                unpack8(sm + S::kn + tile_off(r64, c0 + c8, KK), kn);
 #pragma unroll
-                    for (int t = 0; t < 8; ++t) {
-                        dk8[t] = d[c8 + t] * ex2f(-gg[t]);
-                        dg8[t] = -kLn2 * d[c8 + t] * kn[t];
-                    }
-                    if (r < nr && c0 + c8 < p.K) add8(grow(a.dk, r) + c0 + c8, dk8);
-                    dg2_add(r, c0 + c8, dg8, false);
+                for (int t = 0; t < 8; ++t) {
+                    dk8[t] = d[c8 + t] * ex2f(-gg[t]);
+                    dg8[t] = -kLn2 * d[c8 + t] * kn[t];
                 }
+                if (r64 < nr && c0 + c8 < p.K) add8(grow(a.dk, r64) + c0 + c8, dk8);
+                dg2_add(r64, c0 + c8, dg8, false);
             }
         }
     }
@@ -930,7 +960,7 @@ __global__ void __launch_bounds__(256, 1) chunk_bwd_unit_tc_kernel(BwdArgs a) {
             acc += sDg2[fsw<KK>(r, tid)];
             if (tid < p.K) a.dg[((rowbase + r) * p.HV + hv) * p.K + tid] = p.g_scale * acc;
         }
-    } else if (tid - 128 < nr && tid - 128 < 64) {
+    } else if (tid >= 128 && tid - 128 < nr && tid - 128 < 64) {
         const int r = tid - 128;
         a.dbeta[(rowbase + r) * p.HV + hv] = sDbeta[r];
     }
@@ -969,7 +999,7 @@ cudaError_t launch_unit(const BwdArgs &a, cudaStream_t st) {
     const int64_t units = a.c.slots * a.c.HV;
     if (units == 0) return cudaSuccess;
     prof_begin("chunk_bwd_unit_tc", st);
-    chunk_bwd_unit_tc_kernel<KK, VV><<<(unsigned)units, 256, S::total, st>>>(a);
+    chunk_bwd_unit_tc_kernel<KK, VV><<<(unsigned)units, kUnitThreads, S::total, st>>>(a);
     prof_end(st);
     return cudaGetLastError();
 }
