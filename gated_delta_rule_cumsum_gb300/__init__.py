@@ -496,8 +496,9 @@ def chunk_kda_backward(q, k, v, gate, beta, dout, initial_state=None, dht=None, 
 
 
 class _KdaFunction(torch.autograd.Function):
-    """Forward by the chunked (or token) kernels, backward by kda_recurrent_bwd: the
-    chunked form computes the recurrence, so its gradients are the recurrence's."""
+    """Forward by the chunked (or token) kernels, backward by kda_chunk_bwd or
+    kda_recurrent_bwd: the chunked form computes the recurrence, so its gradients
+    are the recurrence's."""
 
     @staticmethod
     def forward(ctx, q, k, v, g, beta, h0, cu, scale, g_scale, chunked, l2norm, A_log, dt_bias,
@@ -527,10 +528,24 @@ class _KdaFunction(torch.autograd.Function):
         # upstream gradient is rounded to bf16 here (a relative change of at most
         # 2^-9 per element) before the fp32 backward uses it.
         do = torch.zeros_like(v) if do is None else do.to(q.dtype)
-        gr = recurrent_kda_backward(q, k, v, g, beta, do, h0, dht, cu_seqlens=cu,
-                                    scale=ctx.scale, g_scale=ctx.g_scale, want_dh0=h0 is not None,
-                                    use_qk_l2norm_in_kernel=ctx.l2norm, A_log=A_log,
-                                    dt_bias=dt_bias, beta_sigmoid_scale=ctx.beta_sigmoid_scale)
+        gr = None
+        if (q.dtype == torch.bfloat16 and q.shape[3] == 128 and v.shape[3] == 128
+                and not ctx.l2norm and A_log is None and not ctx.beta_sigmoid_scale):
+            # the chunked backward on the tensor cores; a chunk whose gate range it
+            # does not take is reported on the status word, and then the token
+            # recurrence's backward runs instead (this reads the word: one sync)
+            st = new_status(q.device)
+            gr = chunk_kda_backward(q, k, v, g, beta, do, h0, dht, cu_seqlens=cu,
+                                    scale=ctx.scale, g_scale=ctx.g_scale,
+                                    want_dh0=h0 is not None, dev_status=st)
+            if kda_read_device_status(st)[1] & KDA_DEVICE_GATE_RANGE:
+                gr = None
+        if gr is None:
+            gr = recurrent_kda_backward(q, k, v, g, beta, do, h0, dht, cu_seqlens=cu,
+                                        scale=ctx.scale, g_scale=ctx.g_scale,
+                                        want_dh0=h0 is not None,
+                                        use_qk_l2norm_in_kernel=ctx.l2norm, A_log=A_log,
+                                        dt_bias=dt_bias, beta_sigmoid_scale=ctx.beta_sigmoid_scale)
         dh0 = gr["dh0"] if h0 is not None else None
         dA = None if A_log is None else gr["dA_log"].to(A_log.dtype)
         ddt = None if dt_bias is None else gr["ddt_bias"].to(dt_bias.dtype)
@@ -544,8 +559,9 @@ def kda_autograd(q, k, v, g, beta, initial_state=None, *, cu_seqlens=None, scale
                  g_scale=1.0, chunked=True, use_qk_l2norm_in_kernel=False, A_log=None,
                  dt_bias=None, beta_sigmoid_scale=0.0):
     """(o, ht) with gradients: forward by chunk_kda (or recurrent_kda when `chunked` is
-    False), backward by kda_recurrent_bwd; `g` is the per-token log2 gate, or with
-    `A_log` the raw gate (A_log and dt_bias then receive gradients too)."""
+    False), backward by kda_chunk_bwd where it applies (bf16, K = V = 128, no in-op
+    L2 norm or activations), else kda_recurrent_bwd; `g` is the per-token log2 gate,
+    or with `A_log` the raw gate (A_log and dt_bias then receive gradients too)."""
     _one_device(q, k, v, g, beta, initial_state, cu_seqlens, A_log, dt_bias)
     return _KdaFunction.apply(q, k, v, g, beta, initial_state, cu_seqlens, scale, g_scale, chunked,
                               bool(use_qk_l2norm_in_kernel), A_log, dt_bias,

@@ -123,3 +123,23 @@ def test_training_shape_sampled_heads(kda_lib):
     got = _run(kda_lib, inp, dout, dht)
     heads = [0, 15]
     _check(got, _oracle(inp, dout, dht, heads=heads), heads=heads)
+
+
+@pytest.mark.parametrize("wide_gate", [False, True])
+def test_autograd_takes_the_chunked_backward(kda_lib, wide_gate):
+    """loss.backward() through kda_autograd with bf16, K = V = 128: kda_chunk_bwd, or,
+    for a chunk whose gate range it refuses, the token recurrence's backward."""
+    inp = _small(1401, B=1, T=150, H=1, HV=1, K=128, V=128, g_hi=0.3)
+    if wide_gate:
+        inp["g"][:, 64:128] = -3.0
+    dout, dht = _grads_in(inp, 1402)
+    leaves = {n: inp[n].clone().requires_grad_(True) for n in ("q", "k", "v", "g", "beta", "h0")}
+    o, ht = kda_lib.kda_autograd(leaves["q"], leaves["k"], leaves["v"], leaves["g"],
+                                 leaves["beta"], leaves["h0"])
+    ((o.float() * dout.float()).sum() + (ht * dht).sum()).backward()
+    ref = _oracle(inp, dout, dht)
+    for name, key in (("q", "dq"), ("k", "dk"), ("v", "dv"), ("g", "dg"), ("beta", "dbeta"),
+                      ("h0", "dh0")):
+        got = leaves[name].grad
+        err = parity.rel_err(got, ref[key])
+        assert err <= TOL, (name, err)
