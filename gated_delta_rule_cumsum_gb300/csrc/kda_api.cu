@@ -144,10 +144,11 @@ ChunkWs chunk_ws_layout(const kda_shape *s, bool packed, bool bwd = false) {
 
 // kda_chunk_bwd's workspace: the forward's (with the backward's unit tiles),
 // then per unit the checkpoints h_c ([K][V] bf16) and v'_c ([64][V]), and the
-// reverse scan's dL/dh_{c+1} ([K][V]) and dL/dv'_c ([64][V]).
+// reverse scan's dL/dh_{c+1} ([K][V]) and dL/dv'_c ([64][V]); the final states
+// ([N][HV][K][V] fp32) and per unit [V/32][K] fp32 sums of h_{c+1} dh_{c+1}.
 struct ChunkBwdWs {
     ChunkWs f;
-    size_t ck_h, ck_vp, dhn, dvp, total;
+    size_t ck_h, ck_vp, dhn, dvp, hend, dgs, total;
 };
 ChunkBwdWs chunk_bwd_ws_layout(const kda_shape *s, bool packed) {
     ChunkBwdWs W;
@@ -158,7 +159,9 @@ ChunkBwdWs chunk_bwd_ws_layout(const kda_shape *s, bool packed) {
     W.ck_vp = W.ck_h + units * hb;
     W.dhn = W.ck_vp + units * vb;
     W.dvp = W.dhn + units * hb;
-    W.total = W.dvp + units * vb;
+    W.hend = kda::align_up(W.dvp + units * vb, 256);
+    W.dgs = kda::align_up(W.hend + (size_t)s->num_seqs * s->HV * s->K * s->V * 4, 256);
+    W.total = W.dgs + units * (size_t)(s->V / 32) * s->K * 4;
     return W;
 }
 
@@ -554,7 +557,9 @@ kda_status kda_chunk_bwd(const void *q, const void *k, const void *v, const floa
     for (const auto &z : zero)
         if (z[1] && (e = cudaMemsetAsync(reinterpret_cast<void *>(z[0]), 0, z[1], s)) != cudaSuccess)
             return cuda_fail(e, op);
-    e = kda::launch_chunk_bwd_tc(a, dout, dht, dq, dk, dv, dg, dbeta, dh0, ws + W.dhn, ws + W.dvp, s);
+    e = kda::launch_chunk_bwd_tc(a, dout, dht, dq, dk, dv, dg, dbeta, dh0, ws + W.dhn, ws + W.dvp,
+                                 reinterpret_cast<float *>(ws + W.hend),
+                                 reinterpret_cast<float *>(ws + W.dgs), s);
     if (e != cudaSuccess) return cuda_fail(e, op);
     g_last_error.clear();
     return KDA_OK;

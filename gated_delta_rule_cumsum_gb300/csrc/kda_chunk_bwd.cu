@@ -45,6 +45,10 @@ constexpr float kLn2 = 0.69314718055994531f;
 // 2^range, and its products with dP stay well inside fp32.
 constexpr float kBwdRange = 100.f;
 
+// L2 prefetch of a contiguous range (16-byte aligned, a multiple of 16 bytes).
+__device__ __forceinline__ void bulk_prefetch(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ int read_flag(const int *f) {
     return *reinterpret_cast<const volatile int *>(f);
 }
@@ -101,6 +105,8 @@ struct BwdArgs {
     float *dbeta;          // [B,T,HV]
     float *dh0;            // [N,HV,K,V] or null
     void *dhn, *dvp;       // per unit: [K][V] tile dL/dh_{c+1}, [64][V] tile dL/dv'_c
+    const float *hend;     // [N,HV,K,V]: the final states, stored by the forward re-run
+    float *dgs;            // per unit [V/32][K]: sum over 32 value columns of h_{c+1} dh_{c+1}
 };
 
 // Warp roles: 0..3 dh (rows 32 w .. 32 w + 31), 4..7 dv' (M = 64 rows 16 (w % 4) ..
@@ -269,6 +275,12 @@ __global__ void __launch_bounds__(320, 1) chunk_dhu_tc_kernel(BwdArgs a) {
                 dh[4 * j] = x.x; dh[4 * j + 1] = x.y; dh[4 * j + 2] = x.z; dh[4 * j + 3] = x.w;
             }
         }
+        // The decay's gradient needs sum_j h_{c+1} dh_{c+1} per row: the state at the
+        // end of chunk c against its gradient (the two terms the chain rule gives,
+        // 2^G h_c . dh_{c+1} and colsum(dkg . kg), add up to it since kg^T v'_c =
+        // h_{c+1} - 2^G h_c).  h_{c+1} is chunk c + 1's checkpoint, loaded a round
+        // ahead; for the last chunk it is the final state.
+        uint4 hnext[SBV / 8];
         for (int i = 0; i < nc; ++i) {
             const int c = nc - 1 - i;
             // dh_{c+1}: the D1b operand and chunk c's dL/dh_{c+1} tile
@@ -283,6 +295,39 @@ __global__ void __launch_bounds__(320, 1) chunk_dhu_tc_kernel(BwdArgs a) {
             fence_async_smem();
             __syncwarp();
             named_arrive(kDhuBarH, 128 + 32);
+            // off the chain: dh_{c+1} stays in registers until the update below
+            {
+                float dot = 0.f;
+                if (i == 0) {
+                    if (glob_row) {
+                        const float4 *src = reinterpret_cast<const float4 *>(
+                            a.hend + (((size_t)n * p.HV + hv) * p.K + row) * (size_t)p.V + (size_t)vb * SBV);
+#pragma unroll
+                        for (int j = 0; j < SBV / 4; ++j) {
+                            const float4 x = src[j];
+                            dot = fmaf(x.x, dh[4 * j], fmaf(x.y, dh[4 * j + 1],
+                                  fmaf(x.z, dh[4 * j + 2], fmaf(x.w, dh[4 * j + 3], dot))));
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < SBV / 8; ++j) {
+                        float f[8];
+                        unpack8(hnext[j], f);
+#pragma unroll
+                        for (int t = 0; t < 8; ++t) dot = fmaf(f[t], dh[8 * j + t], dot);
+                    }
+                }
+                a.dgs[(uidx(c) * (p.V / SBV) + vb) * KK + row] = dot;
+                if (c > 0) {  // chunk c's checkpoint is h_{c} = the next round's h_{c'+1}
+                    const unsigned char *hc = static_cast<const unsigned char *>(p.ck_h) +
+                                              uidx(c) * (int64_t)(KK * p.V * 2) +
+                                              tile_off(row, vb * SBV, p.V);
+#pragma unroll
+                    for (int j = 0; j < SBV / 8; ++j)
+                        hnext[j] = *reinterpret_cast<const uint4 *>(hc + j * 128);
+                }
+            }
             float dec = 0.f;
             wait_copy(&full[i % kStages], (i / kStages) & 1);
             if (!read_flag(&abort_flag)) dec = reinterpret_cast<const float *>(stage(i) + S::dec)[row];
@@ -413,7 +458,9 @@ struct UnitSmem {
     static constexpr uint32_t gl = beta + 64 * 4;             // fp32 [KK]: G
     static constexpr uint32_t dG = gl + KK * 4;               // fp32 [KK]
     static constexpr uint32_t dbeta = dG + KK * 4;            // fp32 [64]
-    static constexpr uint32_t total = dbeta + 64 * 4;
+    static constexpr uint32_t egl = dbeta + 64 * 4;           // fp32 [KK]: 2^G
+    static constexpr uint32_t seg = egl + KK * 4;             // fp32 [4][KK]: cumsum segment totals
+    static constexpr uint32_t total = seg + 4 * KK * 4;
     static_assert(dw + 64 * KK * 2 <= misc, "phase-two tiles fit over h and dh");
     static_assert(128 * 64 * 2 <= 64 * VV * 2, "[dP; dA] fits over do");
 };
@@ -455,15 +502,7 @@ __global__ void __launch_bounds__(kUnitThreads, 1) chunk_bwd_unit_tc_kernel(BwdA
     __shared__ int range_bad;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, quad = warp & 3, part = warp >> 2;
-    const int64_t unit = blockIdx.x;
-    const int hv = (int)(unit / p.slots);
-    const int64_t gc = unit % p.slots;
-    int b, row0, nr, cl;
-    if (!locate_chunk(p, gc, b, row0, nr, cl)) return;
-    const int hq = hv / (p.HV / p.H);
     const TcLayout Lo = tc_layout(KK, VV, true);
-    const int64_t ui = unit_index(p, gc, hv);
-
     float *sG = reinterpret_cast<float *>(sm + S::g2);
     float *sBeta = reinterpret_cast<float *>(sm + S::beta);
     float *sGl = reinterpret_cast<float *>(sm + S::gl);
@@ -479,7 +518,67 @@ __global__ void __launch_bounds__(kUnitThreads, 1) chunk_bwd_unit_tc_kernel(BwdA
         mbar_init(&bar_ld, 1);
         mbar_init(&bar_mma, 1);
         mbar_fence_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tslot;
+    const uint32_t s0 = smem_addr(sm);
+    uint32_t phase = 0, ld_phase = 0;
+    const int64_t units = p.slots * p.HV;
+    // A unit's inputs into L2: one thread bulk-prefetches the five tiles (one TMA
+    // operation each); the 64 rows of q, k, g, v and do, 12 lines of 128 bytes a row
+    // at K = V = 128, take a line prefetch per thread (a bulk prefetch per row was
+    // measured to hold its warp for ~16K cycles).
+    auto prefetch_unit = [&](int64_t u) {
+        if (u >= units) return;
+        const int uhv = (int)(u / p.slots);
+        const int64_t ugc = u % p.slots;
+        int ub, ur0, unr, ucl;
+        if (!locate_chunk(p, ugc, ub, ur0, unr, ucl)) return;
+        const int64_t uui = unit_index(p, ugc, uhv);
+        const int uhq = uhv / (p.HV / p.H);
+        const size_t urb = (size_t)ub * p.T + ur0;
+        if (tid == 32) {
+            bulk_prefetch(static_cast<const unsigned char *>(p.ck_h) + uui * (int64_t)(KK * VV * 2), KK * VV * 2);
+            bulk_prefetch(static_cast<const unsigned char *>(a.dhn) + uui * (int64_t)(KK * VV * 2), KK * VV * 2);
+            bulk_prefetch(static_cast<const unsigned char *>(p.ck_vp) + uui * (int64_t)(64 * VV * 2), 64 * VV * 2);
+            bulk_prefetch(static_cast<const unsigned char *>(a.dvp) + uui * (int64_t)(64 * VV * 2), 64 * VV * 2);
+            bulk_prefetch(static_cast<const unsigned char *>(p.units) + uui * (int64_t)Lo.stride + Lo.akk,
+                          64 * 64 * 2);
+        }
+        constexpr int kLines = KK * 2 / 128 * 2 + KK * 4 / 128 + VV * 2 / 128 * 2;  // per row
+        for (int li = tid; li < unr * kLines; li += NT) {
+            const int r = li / kLines, j = li % kLines;
+            const char *ptr;
+            if (j < 2 * (KK * 2 / 128)) {
+                const int t = j / (KK * 2 / 128), o = j % (KK * 2 / 128);
+                ptr = reinterpret_cast<const char *>(static_cast<const __nv_bfloat16 *>(t ? p.k : p.q) +
+                                                     ((urb + r) * p.H + uhq) * p.K) + 128 * o;
+            } else if (j < 2 * (KK * 2 / 128) + KK * 4 / 128) {
+                const int o = j - 2 * (KK * 2 / 128);
+                ptr = reinterpret_cast<const char *>(p.g + ((urb + r) * p.HV + uhv) * p.K) + 128 * o;
+            } else {
+                const int jj = j - 2 * (KK * 2 / 128) - KK * 4 / 128;
+                const int t = jj / (VV * 2 / 128), o = jj % (VV * 2 / 128);
+                ptr = reinterpret_cast<const char *>(static_cast<const __nv_bfloat16 *>(t ? a.dout : p.v) +
+                                                     ((urb + r) * p.HV + uhv) * p.V) + 128 * o;
+            }
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+        }
+    };
+
+    for (int64_t unit = blockIdx.x; unit < units; unit += gridDim.x) {
+    const int hv = (int)(unit / p.slots);
+    const int64_t gc = unit % p.slots;
+    int b, row0, nr, cl;
+    if (!locate_chunk(p, gc, b, row0, nr, cl)) continue;
+    const int hq = hv / (p.HV / p.H);
+    const int64_t ui = unit_index(p, gc, hv);
+    if (tid == 0) {
         range_bad = 0;
+        // the previous unit's reads of these buffers precede the copies' writes
+        fence_async_smem();
         // the forward's and the dhu's tiles of this unit
         mbar_arrive_expect_tx(&bar_ld, 2 * KK * VV * 2 + 2 * 64 * VV * 2 + 64 * 64 * 2);
         bulk_g2s(sm + S::h, static_cast<const unsigned char *>(p.ck_h) + ui * (int64_t)(KK * VV * 2),
@@ -555,28 +654,51 @@ __global__ void __launch_bounds__(kUnitThreads, 1) chunk_bwd_unit_tc_kernel(BwdA
         }
     }
     __syncthreads();
-    // chunk-local cumsum of g_scale g, one channel per thread; rows past the chunk
-    // keep the last row's value
-    if (tid < KK) {
+    // chunk-local cumsum of g_scale g (rows past the chunk hold zeros, so they keep
+    // the last row's value): per channel four threads take 16 rows each, then add
+    // the totals of the segments before theirs.  The decay's gradient: ln2 times the
+    // reverse scan's per-column-block sums of h_{c+1} dh_{c+1}.
+    float *sSeg = reinterpret_cast<float *>(sm + S::seg);
+    const int cd = tid & (KK - 1), cs = tid / KK;  // channel, 16-row segment
+    float gsum[16];
+    if (cs < 4) {
         float acc = 0.f;
-        bool bad = false;
-        for (int r = 0; r < 64; ++r) {
-            const int i = fsw<KK>(r, tid);
-            if (r < nr) acc = fmaf(p.g_scale, sG[i], acc);
-            sG[i] = acc;
-            bad |= !(fabsf(acc) <= kBwdRange);  // also NaN
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            acc = fmaf(p.g_scale, sG[fsw<KK>(16 * cs + r, cd)], acc);
+            gsum[r] = acc;
         }
-        sGl[tid] = acc;
-        sDG[tid] = 0.f;
+        sSeg[cs * KK + cd] = acc;
+    }
+    if (tid < KK) {
+        float x = 0.f;
+        for (int vb = 0; vb < VV / 32; ++vb) x += a.dgs[(ui * (VV / 32) + vb) * KK + tid];
+        sDG[tid] = kLn2 * x;
+    }
+    __syncthreads();
+    if (cs < 4) {
+        float off = 0.f;
+        for (int t = 0; t < cs; ++t) off += sSeg[t * KK + cd];
+        bool bad = false;
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            const float g2 = gsum[r] + off;
+            sG[fsw<KK>(16 * cs + r, cd)] = g2;
+            bad |= !(fabsf(g2) <= kBwdRange);  // also NaN
+        }
+        if (cs == 3) {
+            sGl[cd] = gsum[15] + off;
+            reinterpret_cast<float *>(sm + S::egl)[cd] = ex2f(gsum[15] + off);
+        }
         if (bad) range_bad = 1;
     }
     __syncthreads();
     if (range_bad) {
         if (tid == 0) report(p.status, KDA_DEVICE_GATE_RANGE);
-        if (tid == 0) mbar_wait(&bar_ld, 0, kWaitNs);  // the copies land before the CTA exits
+        if (tid == 0) mbar_wait(&bar_ld, ld_phase & 1, kWaitNs);  // the copies land first
+        ++ld_phase;
         __syncthreads();
-        if (warp == 0) tmem_dealloc(tslot, 512);
-        return;
+        continue;
     }
     // q, k rows -> kp, kn, qp tiles
 #pragma unroll
@@ -602,13 +724,12 @@ __global__ void __launch_bounds__(kUnitThreads, 1) chunk_bwd_unit_tc_kernel(BwdA
     }
     fence_async_smem();
     __syncthreads();
-    if (tid == 0 && !mbar_wait(&bar_ld, 0, kWaitNs)) report(p.status, KDA_DEVICE_TIMEOUT);
+    if (tid == 0 && !mbar_wait(&bar_ld, ld_phase & 1, kWaitNs)) report(p.status, KDA_DEVICE_TIMEOUT);
+    ++ld_phase;
     __syncthreads();
     tc_fence_after();
+    prefetch_unit(unit + gridDim.x);  // this CTA's next unit, into L2 while this one computes
 
-    const uint32_t tmem = tslot;
-    const uint32_t s0 = smem_addr(sm);
-    uint32_t phase = 0;
     auto mma_wait = [&]() {
         if (!mbar_wait(&bar_mma, phase & 1, kWaitNs) && tid == 0) report(p.status, KDA_DEVICE_TIMEOUT);
         ++phase;
@@ -630,22 +751,6 @@ __global__ void __launch_bounds__(kUnitThreads, 1) chunk_bwd_unit_tc_kernel(BwdA
         mma_bf16_seq<VV / 16, false>(tmem + 256, kmaj(S::vp, VV), 16, kmaj(S::dhn, VV), 16,
                                      idesc_bf16(64, KK, false, false));
         mma_commit(&bar_mma);
-    }
-    // meanwhile: ln2 2^G rowsum(h . dh_{c+1}) per channel, four threads a row
-    {
-        const int d = tid >> 2, j0 = (tid & 3) * (VV / 4);
-        float acc = 0.f;
-#pragma unroll
-        for (int j = j0; j < j0 + VV / 4; j += 8) {
-            float x[8], y[8];
-            unpack8(sm + S::h + tile_off(d, j, VV), x);
-            unpack8(sm + S::dhn + tile_off(d, j, VV), y);
-#pragma unroll
-            for (int t = 0; t < 8; ++t) acc = fmaf(x[t], y[t], acc);
-        }
-        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-        acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-        if ((tid & 3) == 0 && d < KK) sDG[d] = kLn2 * ex2f(sGl[d]) * acc;
     }
     mma_wait();
     __syncthreads();
@@ -720,37 +825,25 @@ __global__ void __launch_bounds__(kUnitThreads, 1) chunk_bwd_unit_tc_kernel(BwdA
         }
     }
     __syncthreads();
-    // ---- dkg = v' dh^T (M = 64) -> dk, dg2, and the G terms
+    // ---- dkg = v' dh^T (M = 64) -> dk, dg2 (kg = kn 2^G)
     {
         const int c0 = col0(KK);
+        const float *sEgl = reinterpret_cast<const float *>(sm + S::egl);
         float d[KK / 4];
         tmem_ld32(tl(256 + c0), d);
+        if (live64) {
 #pragma unroll
-        for (int c8 = 0; c8 < KK / 4; c8 += 8) {
-            float gg[8], kn[8], dk8[8], dg8[8], colp[8];
-            g2v(r64, c0 + c8, gg);
-            unpack8(sm + S::kn + tile_off(r64, c0 + c8, KK), kn);
+            for (int c8 = 0; c8 < KK / 4; c8 += 8) {
+                float gg[8], kn[8], dk8[8], dg8[8];
+                g2v(r64, c0 + c8, gg);
+                unpack8(sm + S::kn + tile_off(r64, c0 + c8, KK), kn);
 #pragma unroll
-            for (int t = 0; t < 8; ++t) {
-                const float gl = sGl[c0 + c8 + t];
-                const float x = live64 ? d[c8 + t] : 0.f;
-                dk8[t] = x * ex2f(gl - gg[t]);
-                const float kgx = x * kn[t] * ex2f(gl);   // dkg . kg
-                dg8[t] = -kLn2 * kgx;
-                colp[t] = kLn2 * kgx;
-            }
-            if (live64) {
+                for (int t = 0; t < 8; ++t) {
+                    dk8[t] = d[c8 + t] * ex2f(sGl[c0 + c8 + t] - gg[t]);
+                    dg8[t] = -kLn2 * d[c8 + t] * kn[t] * sEgl[c0 + c8 + t];
+                }
                 if (r64 < nr && c0 + c8 < p.K) add8(grow(a.dk, r64) + c0 + c8, dk8);
                 dg2_add(r64, c0 + c8, dg8, false);
-            }
-#pragma unroll
-            for (int t = 0; t < 8; ++t) {
-                float s = colp[t];
-                s += __shfl_xor_sync(0xffffffffu, s, 1);
-                s += __shfl_xor_sync(0xffffffffu, s, 2);
-                s += __shfl_xor_sync(0xffffffffu, s, 4);
-                s += __shfl_xor_sync(0xffffffffu, s, 8);
-                if (lane == 0) atomicAdd(&sDG[c0 + c8 + t], s);
             }
         }
     }
@@ -953,18 +1046,36 @@ __global__ void __launch_bounds__(kUnitThreads, 1) chunk_bwd_unit_tc_kernel(BwdA
     }
     tc_fence_before();
     __syncthreads();
-    // ---- dg: g_scale x reverse cumsum of dg2 (G's gradient on the last row); dbeta
-    if (tid < KK) {
-        float acc = sDG[tid];
-        for (int r = nr - 1; r >= 0; --r) {
-            acc += sDg2[fsw<KK>(r, tid)];
-            if (tid < p.K) a.dg[((rowbase + r) * p.HV + hv) * p.K + tid] = p.g_scale * acc;
+    // ---- dg: g_scale x reverse cumsum of dg2 (G's gradient on the last row), per
+    // channel in four 16-row segments; dbeta
+    if (cs < 4) {
+        float acc = 0.f;
+#pragma unroll
+        for (int r = 15; r >= 0; --r) {
+            const int rr = 16 * cs + r;
+            float x = rr < nr ? sDg2[fsw<KK>(rr, cd)] : 0.f;
+            if (rr == nr - 1) x += sDG[cd];
+            acc += x;
+            gsum[r] = acc;
         }
-    } else if (tid >= 128 && tid - 128 < nr && tid - 128 < 64) {
-        const int r = tid - 128;
-        a.dbeta[(rowbase + r) * p.HV + hv] = sDbeta[r];
+        sSeg[cs * KK + cd] = acc;
     }
     __syncthreads();
+    if (cs < 4) {
+        float off = 0.f;
+        for (int t = cs + 1; t < 4; ++t) off += sSeg[t * KK + cd];
+        if (cd < p.K) {
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                const int rr = 16 * cs + r;
+                if (rr < nr) a.dg[((rowbase + rr) * p.HV + hv) * p.K + cd] = p.g_scale * (gsum[r] + off);
+            }
+        }
+    }
+    if (tid < nr && tid < 64) a.dbeta[(rowbase + tid) * p.HV + hv] = sDbeta[tid];
+    tc_fence_before();
+    __syncthreads();
+    }
     if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
@@ -990,16 +1101,22 @@ template <int KK, int VV>
 cudaError_t launch_unit(const BwdArgs &a, cudaStream_t st) {
     using S = UnitSmem<KK, VV>;
     static DeviceOnce once;
+    static int sms[64];
     int dev = 0;
-    cudaError_t e = once.run(&dev, [](int) {
-        return cudaFuncSetAttribute(chunk_bwd_unit_tc_kernel<KK, VV>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::total);
+    cudaError_t e = once.run(&dev, [](int d) {
+        cudaError_t r = cudaFuncSetAttribute(chunk_bwd_unit_tc_kernel<KK, VV>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)S::total);
+        if (r == cudaSuccess) r = cudaDeviceGetAttribute(&sms[d], cudaDevAttrMultiProcessorCount, d);
+        return r;
     });
     if (e != cudaSuccess) return e;
     const int64_t units = a.c.slots * a.c.HV;
     if (units == 0) return cudaSuccess;
+    // persistent: one CTA per SM (its shared memory allows no second), units strided
+    const unsigned grid = (unsigned)(units < sms[dev] ? units : sms[dev]);
     prof_begin("chunk_bwd_unit_tc", st);
-    chunk_bwd_unit_tc_kernel<KK, VV><<<(unsigned)units, kUnitThreads, S::total, st>>>(a);
+    chunk_bwd_unit_tc_kernel<KK, VV><<<grid, kUnitThreads, S::total, st>>>(a);
     prof_end(st);
     return cudaGetLastError();
 }
@@ -1010,10 +1127,13 @@ bool chunk_bwd_tc_supported(int K, int V) { return K == 128 && V == 128; }
 
 cudaError_t launch_chunk_bwd_tc(const ChunkArgs &c, const void *dout, const float *dht, float *dq,
                                 float *dk, float *dv, float *dg, float *dbeta, float *dh0,
-                                void *dhn, void *dvp, cudaStream_t st) {
+                                void *dhn, void *dvp, float *hend, float *dgs, cudaStream_t st) {
     if (!chunk_bwd_tc_supported(c.K, c.V)) return cudaErrorInvalidValue;
     BwdArgs a;
     a.c = c;
+    a.c.ht = hend;  // the re-run forward stores the final states there
+    a.hend = hend;
+    a.dgs = dgs;
     a.dout = dout;
     a.dht = dht;
     a.dq = dq;
@@ -1024,7 +1144,7 @@ cudaError_t launch_chunk_bwd_tc(const ChunkArgs &c, const void *dout, const floa
     a.dh0 = dh0;
     a.dhn = dhn;
     a.dvp = dvp;
-    cudaError_t e = launch_chunk_tc(c, st);  // recompute and re-scan, with checkpoints
+    cudaError_t e = launch_chunk_tc(a.c, st);  // recompute and re-scan, with checkpoints
     if (e != cudaSuccess) return e;
     if ((e = launch_dhu<128, 32>(a, st)) != cudaSuccess) return e;
     return launch_unit<128, 128>(a, st);

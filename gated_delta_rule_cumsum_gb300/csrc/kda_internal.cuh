@@ -224,11 +224,12 @@ size_t chunk_tc_unit_bytes(int K, int V, bool bwd = false);
 cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st);
 
 // Chunked backward (kda_chunk_bwd), bf16 with K = V = 128: the forward re-run with
-// `c.bwd` and its checkpoints, the reverse state scan (dhn, dvp: per-unit tiles in
-// the workspace), then the per-chunk gradients.  dq and dk must be zeroed first.
+// `c.bwd` and its checkpoints (final states to hend, [N][HV][K][V] fp32), the reverse
+// state scan (dhn, dvp: per-unit tiles; dgs: per unit [V/32][K] fp32 sums of
+// h_{c+1} dh_{c+1}), then the per-chunk gradients.  dq and dk must be zeroed first.
 bool chunk_bwd_tc_supported(int K, int V);
 cudaError_t launch_chunk_bwd_tc(const ChunkArgs &c, const void *dout, const float *dht, float *dq,
                                 float *dk, float *dv, float *dg, float *dbeta, float *dh0,
-                                void *dhn, void *dvp, cudaStream_t st);
+                                void *dhn, void *dvp, float *hend, float *dgs, cudaStream_t st);
 
 }  // namespace kda
