@@ -778,9 +778,12 @@ __global__ void __launch_bounds__(kUnitThreads, 1) chunk_bwd_unit_tc_kernel(BwdA
     };
     // Rows of this thread in an M = 64 result, and in the top / bottom half of an
     // M = 128 result; the first of its columns in a result N wide.
-    const int r64 = 16 * quad + (lane & 15), r128 = 32 * (quad & 1) + lane;
-    const bool live64 = lane < 16, top = quad < 2;
+    // An M = 64 result is read with the 16x32bx2 shape: the two half-warps hold the
+    // same 16 rows, each half one of two adjacent column blocks.
+    const int r64 = 16 * quad + (lane & 15), r128 = 32 * (quad & 1) + lane, hs = lane >> 4;
+    const bool top = quad < 2;
     auto col0 = [&](int N) { return part * (N / 4); };
+    auto c64 = [&](int N) { return part * (N / 4) + hs * (N / 8); };
 
     // ---- dqg = scale do h^T (rows 0..63 of the M = 128 result) -> dq, dg2;
     //      dw = -(dv' h^T) (rows 64..127) -> bf16 tile; dA = scale tril(do v'^T)
@@ -812,28 +815,23 @@ __global__ void __launch_bounds__(kUnitThreads, 1) chunk_bwd_unit_tc_kernel(BwdA
         }
     }
     {
-        const int c0 = col0(64);
-        float d[16];
-        tmem_ld16(tl(64 + c0), d);
-        if (live64) {
+        const int c0 = c64(64);
+        float d[8];
+        tmem_ld16x2_8<8>(tl(64 + col0(64)), d);
 #pragma unroll
-            for (int t = 0; t < 16; ++t) d[t] = (c0 + t <= r64) ? scale * d[t] : 0.f;
-#pragma unroll
-            for (int c8 = 0; c8 < 16; c8 += 8)
-                *reinterpret_cast<uint4 *>(sm + S::dap + tile_off(64 + r64, c0 + c8, 64)) =
-                    pack8_at(d + c8);
-        }
+        for (int t = 0; t < 8; ++t) d[t] = (c0 + t <= r64) ? scale * d[t] : 0.f;
+        *reinterpret_cast<uint4 *>(sm + S::dap + tile_off(64 + r64, c0, 64)) = pack8_at(d);
     }
     __syncthreads();
     // ---- dkg = v' dh^T (M = 64) -> dk, dg2 (kg = kn 2^G)
     {
-        const int c0 = col0(KK);
+        const int c0 = c64(KK);
         const float *sEgl = reinterpret_cast<const float *>(sm + S::egl);
-        float d[KK / 4];
-        tmem_ld32(tl(256 + c0), d);
-        if (live64) {
+        float d[KK / 8];
+        tmem_ld16x2_16<KK / 8>(tl(256 + col0(KK)), d);
+        {
 #pragma unroll
-            for (int c8 = 0; c8 < KK / 4; c8 += 8) {
+            for (int c8 = 0; c8 < KK / 8; c8 += 8) {
                 float gg[8], kn[8], dk8[8], dg8[8];
                 g2v(r64, c0 + c8, gg);
                 unpack8(sm + S::kn + tile_off(r64, c0 + c8, KK), kn);
@@ -870,13 +868,13 @@ __global__ void __launch_bounds__(kUnitThreads, 1) chunk_bwd_unit_tc_kernel(BwdA
         const float br = sBeta[r64];
         float db = 0.f;
         {
-            const int c0 = col0(VV);
-            float d[VV / 4];
-            tmem_ld32(tl(128 + c0), d);
-            if (live64) {
+            const int c0 = c64(VV);
+            float d[VV / 8];
+            tmem_ld16x2_16<VV / 8>(tl(128 + col0(VV)), d);
+            {
                 float *dvr = a.dv + ((rowbase + r64) * p.HV + hv) * p.V + c0;
 #pragma unroll
-                for (int c8 = 0; c8 < VV / 4; c8 += 8) {
+                for (int c8 = 0; c8 < VV / 8; c8 += 8) {
                     float vv[8];
                     unpack8(sm + S::vt + tile_off(r64, c0 + c8, VV), vv);
 #pragma unroll
@@ -884,19 +882,19 @@ __global__ void __launch_bounds__(kUnitThreads, 1) chunk_bwd_unit_tc_kernel(BwdA
                 }
                 if (r64 < nr) {
 #pragma unroll
-                    for (int t = 0; t < VV / 4; t += 4)
+                    for (int t = 0; t < VV / 8; t += 4)
                         *reinterpret_cast<float4 *>(dvr + t) =
                             make_float4(br * d[t], br * d[t + 1], br * d[t + 2], br * d[t + 3]);
                 }
             }
         }
         {
-            const int c0 = col0(KK);
-            float d[KK / 4];
-            tmem_ld32(tl(256 + c0), d);
-            if (live64) {
+            const int c0 = c64(KK);
+            float d[KK / 8];
+            tmem_ld16x2_16<KK / 8>(tl(256 + col0(KK)), d);
+            {
 #pragma unroll
-                for (int c8 = 0; c8 < KK / 4; c8 += 8) {
+                for (int c8 = 0; c8 < KK / 8; c8 += 8) {
                     float gg[8], kp[8], dk8[8], dg8[8];
                     g2v(r64, c0 + c8, gg);
                     unpack8(sm + S::kp + tile_off(r64, c0 + c8, KK), kp);
@@ -913,18 +911,13 @@ __global__ void __launch_bounds__(kUnitThreads, 1) chunk_bwd_unit_tc_kernel(BwdA
             }
         }
         {
-            const int c0 = col0(64);
-            float d[16];
-            tmem_ld16(tl(384 + c0), d);
-            if (live64) {
+            const int c0 = c64(64);
+            float d[8];
+            tmem_ld16x2_8<8>(tl(384 + col0(64)), d);
 #pragma unroll
-                for (int t = 0; t < 16; ++t) d[t] *= sBeta[c0 + t];
-#pragma unroll
-                for (int c8 = 0; c8 < 16; c8 += 8)
-                    *reinterpret_cast<uint4 *>(sm + S::dakk + tile_off(r64, c0 + c8, 64)) =
-                        pack8_at(d + c8);
-                atomicAdd(&sDbeta[r64], db);
-            }
+            for (int t = 0; t < 8; ++t) d[t] *= sBeta[c0 + t];
+            *reinterpret_cast<uint4 *>(sm + S::dakk + tile_off(r64, c0, 64)) = pack8_at(d);
+            atomicAdd(&sDbeta[r64], db);
         }
     }
     fence_async_smem();
@@ -939,14 +932,10 @@ __global__ void __launch_bounds__(kUnitThreads, 1) chunk_bwd_unit_tc_kernel(BwdA
     }
     mma_wait();
     {
-        const int c0 = col0(64);
-        float d[16];
-        tmem_ld16(tl(448 + c0), d);
-        if (live64) {
-#pragma unroll
-            for (int c8 = 0; c8 < 16; c8 += 8)
-                *reinterpret_cast<uint4 *>(sm + S::xt + tile_off(r64, c0 + c8, 64)) = pack8_at(d + c8);
-        }
+        const int c0 = c64(64);
+        float d[8];
+        tmem_ld16x2_8<8>(tl(448 + col0(64)), d);
+        *reinterpret_cast<uint4 *>(sm + S::xt + tile_off(r64, c0, 64)) = pack8_at(d);
     }
     fence_async_smem();
     tc_fence_before();
@@ -961,22 +950,20 @@ __global__ void __launch_bounds__(kUnitThreads, 1) chunk_bwd_unit_tc_kernel(BwdA
     mma_wait();
     // ---- dL = -strictly_tril(Y); dbeta += rowsum(dL . P); dP = diag(beta) dL
     {
-        const int c0 = col0(64);
-        float y[16], pp[16];
-        tmem_ld16(tl(64 + c0), y);
-        tmem_ld16(tl(0 + c0), pp);
-        if (live64) {
+        const int c0 = c64(64);
+        float y[8], pp[8];
+        tmem_ld16x2_8<8>(tl(64 + col0(64)), y);
+        tmem_ld16x2_8<8>(tl(0 + col0(64)), pp);
+        {
             const float br = sBeta[r64];
             float db = 0.f;
 #pragma unroll
-            for (int t = 0; t < 16; ++t) {
+            for (int t = 0; t < 8; ++t) {
                 const float dl = (c0 + t < r64) ? -y[t] : 0.f;
                 db = fmaf(dl, pp[t], db);
                 y[t] = br * dl;
             }
-#pragma unroll
-            for (int c8 = 0; c8 < 16; c8 += 8)
-                *reinterpret_cast<uint4 *>(sm + S::dap + tile_off(r64, c0 + c8, 64)) = pack8_at(y + c8);
+            *reinterpret_cast<uint4 *>(sm + S::dap + tile_off(r64, c0, 64)) = pack8_at(y);
             atomicAdd(&sDbeta[r64], db);
         }
     }
@@ -1025,12 +1012,12 @@ __global__ void __launch_bounds__(kUnitThreads, 1) chunk_bwd_unit_tc_kernel(BwdA
         }
     }
     {
-        const int c0 = col0(KK);
-        float d[KK / 4];
-        tmem_ld32(tl(256 + c0), d);
-        if (live64) {
+        const int c0 = c64(KK);
+        float d[KK / 8];
+        tmem_ld16x2_16<KK / 8>(tl(256 + col0(KK)), d);
+        {
 #pragma unroll
-            for (int c8 = 0; c8 < KK / 4; c8 += 8) {
+            for (int c8 = 0; c8 < KK / 8; c8 += 8) {
                 float gg[8], kn[8], dk8[8], dg8[8];
                 g2v(r64, c0 + c8, gg);
                 unpack8(sm + S::kn + tile_off(r64, c0 + c8, KK), kn);

@@ -109,3 +109,53 @@ extern "C" int tc_probe(const void *A, const void *B, float *D, int N, int Kd, i
                                           err);
     return (int)cudaGetLastError();
 }
+
+// TMEM read-back shapes: every warp stores lane * 1000 + column into its 32 lanes x
+// 64 columns (32x32b stores), then reads them back with the 16-lane shape that
+// hands the second half of the warp the same 16 lanes at a column offset
+// (16x32bx2, offset 32): out[warp][thread][0..15].
+__global__ void __launch_bounds__(128) tmem_ld16x2_kernel(float *out) {
+    __shared__ uint32_t slot;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (warp == 0) {
+        tmem_alloc(&slot, 64);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = slot;
+    const uint32_t row = tmem + ((uint32_t)(32 * warp) << 16);
+    for (int c0 = 0; c0 < 64; c0 += 8) {
+        uint32_t v[8];
+        for (int j = 0; j < 8; ++j) v[j] = __float_as_uint((float)((32 * warp + lane) * 1000 + c0 + j));
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(
+                         row + c0),
+                     "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
+                     "r"(v[7])
+                     : "memory");
+    }
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16], 32;\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(row)
+        : "memory");
+    for (int j = 0; j < 16; ++j) out[(warp * 32 + lane) * 16 + j] = __uint_as_float(r[j]);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 64);
+}
+
+extern "C" int tmem_ld16x2_probe(float *out, cudaStream_t st) {
+    tmem_ld16x2_kernel<<<1, 128, 0, st>>>(out);
+    return (int)cudaGetLastError();
+}

@@ -53,3 +53,18 @@ def test_single_tile_gemm(probe, mode, N, Kd):
 def test_single_tile_gemm_swizzled(probe, mode, N, Kd):
     test_single_tile_gemm(probe, mode, N, Kd)
 
+
+
+def test_tmem_16x32bx2_readback(probe):
+    """The 16-lane TMEM load with a column offset: thread t < 16 of warp w gets lane
+    32 w + t, columns 0..15; thread t >= 16 the same lane 32 w + t - 16, columns
+    32..47 -- the layout the backward's M = 64 epilogues read their rows with."""
+    probe.tmem_ld16x2_probe.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+    out = torch.full((4, 32, 16), float("nan"), device="cuda")
+    assert probe.tmem_ld16x2_probe(out.data_ptr(), torch.cuda.current_stream().cuda_stream) == 0
+    torch.cuda.synchronize()
+    w = torch.arange(4, device="cuda").view(4, 1, 1)
+    t = torch.arange(32, device="cuda").view(1, 32, 1)
+    j = torch.arange(16, device="cuda").view(1, 1, 16)
+    want = (32 * w + (t % 16)) * 1000 + j + 32 * (t // 16)
+    assert torch.equal(out, want.float())
