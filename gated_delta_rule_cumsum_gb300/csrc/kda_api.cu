@@ -547,10 +547,12 @@ kda_status kda_chunk_bwd(const void *q, const void *k, const void *v, const floa
         e = kda::launch_validate_offsets(cu_seqlens, a.N, a.T, dev_status, a.ctrl, a.chunk_start, s);
         if (e != cudaSuccess) return cuda_fail(e, op);
     }
-    // dq, dk accumulate; with packed sequences rows outside every sequence stay zero
+    // dq, dk accumulate over the value heads that share a q/k head (else each chunk
+    // stores its rows once); with packed sequences rows outside every sequence stay zero
     const size_t rows = (size_t)shape->B * shape->T;
-    const size_t zero[][2] = {{(size_t)dq, rows * shape->H * shape->K * 4},
-                              {(size_t)dk, rows * shape->H * shape->K * 4},
+    const bool qk_zero = packed || shape->HV != shape->H;
+    const size_t zero[][2] = {{(size_t)dq, qk_zero ? rows * shape->H * shape->K * 4 : 0},
+                              {(size_t)dk, qk_zero ? rows * shape->H * shape->K * 4 : 0},
                               {(size_t)dv, packed ? rows * shape->HV * shape->V * 4 : 0},
                               {(size_t)dg, packed ? rows * shape->HV * shape->K * 4 : 0},
                               {(size_t)dbeta, packed ? rows * shape->HV * 4 : 0}};

@@ -100,7 +100,7 @@ struct BwdArgs {
     ChunkArgs c;           // the forward's arguments, bwd set, its checkpoints
     const void *dout;      // [B,T,HV,V] bf16
     const float *dht;      // [N,HV,K,V] or null
-    float *dq, *dk;        // [B,T,H,K], accumulated (zeroed first)
+    float *dq, *dk;        // [B,T,H,K]: stored, or with HV > H added (zeroed first)
     float *dv, *dg;        // [B,T,HV,V], [B,T,HV,K]
     float *dbeta;          // [B,T,HV]
     float *dh0;            // [N,HV,K,V] or null
@@ -448,11 +448,11 @@ struct UnitSmem {
     static constexpr uint32_t h = vp + 64 * VV * 2;           // [KK][VV] h_c
     static constexpr uint32_t dhn = h + KK * VV * 2;          // [KK][VV] dh_{c+1}
     static constexpr uint32_t misc = dhn + KK * VV * 2;
-    // once h and dh_{c+1} have been read
-    static constexpr uint32_t dg2 = h;                        // fp32 [64][KK]
-    static constexpr uint32_t dakk = dg2 + 64 * KK * 4;       // [64][64]
+    // over h once the first MMAs have read it, and over dh_{c+1} once the second have
+    static constexpr uint32_t dw = h;                         // [64][KK]
+    static constexpr uint32_t dakk = dw + 64 * KK * 2;        // [64][64]
     static constexpr uint32_t xt = dakk + 64 * 64 * 2;        // [64][64] Akk^T dAkk
-    static constexpr uint32_t dw = xt + 64 * 64 * 2;          // [64][KK]
+    static constexpr uint32_t dg2 = dhn;                      // fp32 [64][KK]
     static constexpr uint32_t dap = dout;                     // [128][64]: dP; dA
     static constexpr uint32_t beta = misc;                    // fp32 [64]
     static constexpr uint32_t gl = beta + 64 * 4;             // fp32 [KK]: G
@@ -461,7 +461,7 @@ struct UnitSmem {
     static constexpr uint32_t egl = dbeta + 64 * 4;           // fp32 [KK]: 2^G
     static constexpr uint32_t seg = egl + KK * 4;             // fp32 [4][KK]: cumsum segment totals
     static constexpr uint32_t total = seg + 4 * KK * 4;
-    static_assert(dw + 64 * KK * 2 <= misc, "phase-two tiles fit over h and dh");
+    static_assert(xt + 64 * 64 * 2 <= dhn && dg2 + 64 * KK * 4 <= misc, "tiles over h and dh");
     static_assert(128 * 64 * 2 <= 64 * VV * 2, "[dP; dA] fits over do");
 };
 
@@ -694,7 +694,19 @@ __global__ void __launch_bounds__(kUnitThreads, 1) chunk_bwd_unit_tc_kernel(BwdA
     }
     __syncthreads();
     if (range_bad) {
+        // refused: the chunk's gradients are zero (the status word tells the caller)
         if (tid == 0) report(p.status, KDA_DEVICE_GATE_RANGE);
+        for (int i = tid; i < nr * (KK / 4); i += NT) {
+            const int r = i / (KK / 4), c = (i % (KK / 4)) * 4;
+            const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (p.H == p.HV) {
+                *reinterpret_cast<float4 *>(a.dq + ((rowbase + r) * p.H + hq) * p.K + c) = z;
+                *reinterpret_cast<float4 *>(a.dk + ((rowbase + r) * p.H + hq) * p.K + c) = z;
+            }
+            *reinterpret_cast<float4 *>(a.dg + ((rowbase + r) * p.HV + hv) * p.K + c) = z;
+            *reinterpret_cast<float4 *>(a.dv + ((rowbase + r) * p.HV + hv) * p.V + c) = z;
+        }
+        if (tid < nr) a.dbeta[(rowbase + tid) * p.HV + hv] = 0.f;
         if (tid == 0) mbar_wait(&bar_ld, ld_phase & 1, kWaitNs);  // the copies land first
         ++ld_phase;
         __syncthreads();
@@ -740,15 +752,15 @@ __global__ void __launch_bounds__(kUnitThreads, 1) chunk_bwd_unit_tc_kernel(BwdA
     auto mnmaj = [&](uint32_t off, int C) { return sdesc(s0 + off, C * 16, 128); };
     auto tl = [&](uint32_t col) { return tmem_at(tmem, 32 * quad, col); };
 
-    // ---- P = kp kn^T, do v'^T, [do; dv'] h^T, v' dh^T
+    // ---- P = kp kn^T, dA = do v'^T, Qd = do h^T, Wd = dv' h^T (all M = 64)
     if (tid == 0) {
         mma_bf16_seq<KK / 16, false>(tmem + 0, kmaj(S::kp, KK), 16, kmaj(S::kn, KK), 16,
                                      idesc_bf16(64, 64, false, false));
         mma_bf16_seq<VV / 16, false>(tmem + 64, kmaj(S::dout, VV), 16, kmaj(S::vp, VV), 16,
                                      idesc_bf16(64, 64, false, false));
         mma_bf16_seq<VV / 16, false>(tmem + 128, kmaj(S::dout, VV), 16, kmaj(S::h, VV), 16,
-                                     idesc_bf16(128, KK, false, false));
-        mma_bf16_seq<VV / 16, false>(tmem + 256, kmaj(S::vp, VV), 16, kmaj(S::dhn, VV), 16,
+                                     idesc_bf16(64, KK, false, false));
+        mma_bf16_seq<VV / 16, false>(tmem + 256, kmaj(S::dvp, VV), 16, kmaj(S::h, VV), 16,
                                      idesc_bf16(64, KK, false, false));
         mma_commit(&bar_mma);
     }
@@ -776,43 +788,32 @@ __global__ void __launch_bounds__(kUnitThreads, 1) chunk_bwd_unit_tc_kernel(BwdA
             *d1 = v;
         }
     };
-    // Rows of this thread in an M = 64 result, and in the top / bottom half of an
-    // M = 128 result; the first of its columns in a result N wide.
-    // An M = 64 result is read with the 16x32bx2 shape: the two half-warps hold the
-    // same 16 rows, each half one of two adjacent column blocks.
-    const int r64 = 16 * quad + (lane & 15), r128 = 32 * (quad & 1) + lane, hs = lane >> 4;
-    const bool top = quad < 2;
+    // Every result here is M = 64, read with the 16x32bx2 shape: this thread holds row
+    // r64 and, of a result N wide, the N / 8 columns from c64(N) (the two half-warps
+    // on adjacent column blocks).  Its dq and dk elements (16 each) accumulate in its
+    // own TMEM lane, which no M = 64 result uses, and reach global memory once.
+    const int r64 = 16 * quad + (lane & 15), hs = lane >> 4;
     auto col0 = [&](int N) { return part * (N / 4); };
     auto c64 = [&](int N) { return part * (N / 4) + hs * (N / 8); };
+    const uint32_t acc_dq = tl(384 + part * 16), acc_dk = tl(448 + part * 16);
+    const bool excl = p.H == p.HV;  // no other CTA adds to these q / k rows
 
-    // ---- dqg = scale do h^T (rows 0..63 of the M = 128 result) -> dq, dg2;
-    //      dw = -(dv' h^T) (rows 64..127) -> bf16 tile; dA = scale tril(do v'^T)
-    {
-        const int c0 = col0(KK);
-        float d[KK / 4];
-        tmem_ld32(tl(128 + c0), d);
-        if (top) {
+    // ---- dq <- scale Qd 2^g2 (its dg2 term, ln2 scale Qd . qp = ln2 dq . qp 2^-g2, is
+    // added with the last terms: dg2 lives over dh_{c+1}, which the next MMAs read);
+    // dw = -Wd; dA = scale tril(do v'^T)
 #pragma unroll
-            for (int c8 = 0; c8 < KK / 4; c8 += 8) {
-                float gg[8], qp[8], dq8[8], dg8[8];
-                g2v(r128, c0 + c8, gg);
-                unpack8(sm + S::qp + tile_off(r128, c0 + c8, KK), qp);
+    for (int c8 = 0; c8 < 16; c8 += 8) {
+        const int c0 = c64(KK) + c8;
+        float d[8], gg[8], acc[8];
+        tmem_ld16x2_8<16>(tl(128 + col0(KK) + c8), d);
+        g2v(r64, c0, gg);
 #pragma unroll
-                for (int t = 0; t < 8; ++t) {
-                    const float x = scale * d[c8 + t];
-                    dq8[t] = x * ex2f(gg[t]);
-                    dg8[t] = kLn2 * x * qp[t];
-                }
-                if (r128 < nr && c0 + c8 < p.K) add8(grow(a.dq, r128) + c0 + c8, dq8);
-                dg2_add(r128, c0 + c8, dg8, true);
-            }
-        } else {
+        for (int t = 0; t < 8; ++t) acc[t] = scale * d[t] * ex2f(gg[t]);
+        tmem_st8(acc_dq + c8, acc);
+        tmem_ld16x2_8<16>(tl(256 + col0(KK) + c8), d);
 #pragma unroll
-            for (int t = 0; t < KK / 4; ++t) d[t] = -d[t];
-#pragma unroll
-            for (int c8 = 0; c8 < KK / 4; c8 += 8)
-                *reinterpret_cast<uint4 *>(sm + S::dw + tile_off(r128, c0 + c8, KK)) = pack8_at(d + c8);
-        }
+        for (int t = 0; t < 8; ++t) d[t] = -d[t];
+        *reinterpret_cast<uint4 *>(sm + S::dw + tile_off(r64, c0, KK)) = pack8_at(d);
     }
     {
         const int c0 = c64(64);
@@ -822,40 +823,47 @@ __global__ void __launch_bounds__(kUnitThreads, 1) chunk_bwd_unit_tc_kernel(BwdA
         for (int t = 0; t < 8; ++t) d[t] = (c0 + t <= r64) ? scale * d[t] : 0.f;
         *reinterpret_cast<uint4 *>(sm + S::dap + tile_off(64 + r64, c0, 64)) = pack8_at(d);
     }
-    __syncthreads();
-    // ---- dkg = v' dh^T (M = 64) -> dk, dg2 (kg = kn 2^G)
-    {
-        const int c0 = c64(KK);
-        const float *sEgl = reinterpret_cast<const float *>(sm + S::egl);
-        float d[KK / 8];
-        tmem_ld16x2_16<KK / 8>(tl(256 + col0(KK)), d);
-        {
-#pragma unroll
-            for (int c8 = 0; c8 < KK / 8; c8 += 8) {
-                float gg[8], kn[8], dk8[8], dg8[8];
-                g2v(r64, c0 + c8, gg);
-                unpack8(sm + S::kn + tile_off(r64, c0 + c8, KK), kn);
-#pragma unroll
-                for (int t = 0; t < 8; ++t) {
-                    dk8[t] = d[c8 + t] * ex2f(sGl[c0 + c8 + t] - gg[t]);
-                    dg8[t] = -kLn2 * d[c8 + t] * kn[t] * sEgl[c0 + c8 + t];
-                }
-                if (r64 < nr && c0 + c8 < p.K) add8(grow(a.dk, r64) + c0 + c8, dk8);
-                dg2_add(r64, c0 + c8, dg8, false);
-            }
-        }
-    }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
 
-    // ---- dAkk = dv' v^T + dw kp^T (columns scaled by beta below); Akk^T [dv' | dw]
+    // ---- dkg = v' dh^T; dAkk = dv' v^T + dw kp^T (columns scaled by beta below)
     if (tid == 0) {
-        mma_bf16_seq<VV / 16, false>(tmem + 384, kmaj(S::dvp, VV), 16, kmaj(S::vt, VV), 16,
+        mma_bf16_seq<VV / 16, false>(tmem + 128, kmaj(S::vp, VV), 16, kmaj(S::dhn, VV), 16,
+                                     idesc_bf16(64, KK, false, false));
+        mma_bf16_seq<VV / 16, false>(tmem + 64, kmaj(S::dvp, VV), 16, kmaj(S::vt, VV), 16,
                                      idesc_bf16(64, 64, false, false));
-        mma_bf16_seq<KK / 16, true>(tmem + 384, kmaj(S::dw, KK), 16, kmaj(S::kp, KK), 16,
+        mma_bf16_seq<KK / 16, true>(tmem + 64, kmaj(S::dw, KK), 16, kmaj(S::kp, KK), 16,
                                     idesc_bf16(64, 64, false, false));
+        mma_commit(&bar_mma);
+    }
+    mma_wait();
+    // ---- dk <- dkg 2^(G - g2); dg2 -= ln2 dkg . kg, kg = kn 2^G
+    {
+        const float *sEgl = reinterpret_cast<const float *>(sm + S::egl);
+#pragma unroll
+        for (int c8 = 0; c8 < 16; c8 += 8) {
+            const int c0 = c64(KK) + c8;
+            float d[8], gg[8], kn[8], acc[8], dg8[8];
+            tmem_ld16x2_8<16>(tl(128 + col0(KK) + c8), d);
+            g2v(r64, c0, gg);
+            unpack8(sm + S::kn + tile_off(r64, c0, KK), kn);
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                acc[t] = d[t] * ex2f(sGl[c0 + t] - gg[t]);
+                dg8[t] = -kLn2 * d[t] * kn[t] * sEgl[c0 + t];
+            }
+            tmem_st8(acc_dk + c8, acc);
+            dg2_add(r64, c0, dg8, true);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    // ---- Akk^T [dv' | dw]
+    if (tid == 0) {
         mma_bf16_seq<4, false>(tmem + 128, mnmaj(S::akk, 64), 2 * 64, mnmaj(S::dvp, VV), 2 * VV,
                                idesc_bf16(64, VV, true, true));
         mma_bf16_seq<4, false>(tmem + 256, mnmaj(S::akk, 64), 2 * 64, mnmaj(S::dw, KK), 2 * KK,
@@ -863,57 +871,46 @@ __global__ void __launch_bounds__(kUnitThreads, 1) chunk_bwd_unit_tc_kernel(BwdA
         mma_commit(&bar_mma);
     }
     mma_wait();
-    // ---- dv = diag(beta) Akk^T dv'; dkgate = diag(beta) Akk^T dw; dbeta; dAkk tile
+    // ---- dv = diag(beta) Akk^T dv'; dk += diag(beta) (Akk^T dw) 2^g2; dbeta; dAkk tile
     {
         const float br = sBeta[r64];
         float db = 0.f;
-        {
-            const int c0 = c64(VV);
-            float d[VV / 8];
-            tmem_ld16x2_16<VV / 8>(tl(128 + col0(VV)), d);
-            {
+#pragma unroll
+        for (int c8 = 0; c8 < 16; c8 += 8) {
+            const int c0 = c64(VV) + c8;
+            float d[8], vv[8];
+            tmem_ld16x2_8<16>(tl(128 + col0(VV) + c8), d);
+            unpack8(sm + S::vt + tile_off(r64, c0, VV), vv);
+#pragma unroll
+            for (int t = 0; t < 8; ++t) db = fmaf(d[t], vv[t], db);
+            if (r64 < nr) {
                 float *dvr = a.dv + ((rowbase + r64) * p.HV + hv) * p.V + c0;
-#pragma unroll
-                for (int c8 = 0; c8 < VV / 8; c8 += 8) {
-                    float vv[8];
-                    unpack8(sm + S::vt + tile_off(r64, c0 + c8, VV), vv);
-#pragma unroll
-                    for (int t = 0; t < 8; ++t) db = fmaf(d[c8 + t], vv[t], db);
-                }
-                if (r64 < nr) {
-#pragma unroll
-                    for (int t = 0; t < VV / 8; t += 4)
-                        *reinterpret_cast<float4 *>(dvr + t) =
-                            make_float4(br * d[t], br * d[t + 1], br * d[t + 2], br * d[t + 3]);
-                }
+                *reinterpret_cast<float4 *>(dvr) = make_float4(br * d[0], br * d[1], br * d[2], br * d[3]);
+                *reinterpret_cast<float4 *>(dvr + 4) = make_float4(br * d[4], br * d[5], br * d[6], br * d[7]);
             }
         }
-        {
-            const int c0 = c64(KK);
-            float d[KK / 8];
-            tmem_ld16x2_16<KK / 8>(tl(256 + col0(KK)), d);
-            {
 #pragma unroll
-                for (int c8 = 0; c8 < KK / 8; c8 += 8) {
-                    float gg[8], kp[8], dk8[8], dg8[8];
-                    g2v(r64, c0 + c8, gg);
-                    unpack8(sm + S::kp + tile_off(r64, c0 + c8, KK), kp);
+        for (int c8 = 0; c8 < 16; c8 += 8) {
+            const int c0 = c64(KK) + c8;
+            float d[8], gg[8], kp[8], acc[8], dg8[8];
+            tmem_ld16x2_8<16>(tl(256 + col0(KK) + c8), d);
+            tmem_ld8(acc_dk + c8, acc);
+            g2v(r64, c0, gg);
+            unpack8(sm + S::kp + tile_off(r64, c0, KK), kp);
 #pragma unroll
-                    for (int t = 0; t < 8; ++t) {
-                        db = fmaf(d[c8 + t], kp[t], db);
-                        const float x = br * d[c8 + t];
-                        dk8[t] = x * ex2f(gg[t]);
-                        dg8[t] = kLn2 * x * kp[t];
-                    }
-                    if (r64 < nr && c0 + c8 < p.K) add8(grow(a.dk, r64) + c0 + c8, dk8);
-                    dg2_add(r64, c0 + c8, dg8, false);
-                }
+            for (int t = 0; t < 8; ++t) {
+                db = fmaf(d[t], kp[t], db);
+                const float x = br * d[t];
+                acc[t] = fmaf(x, ex2f(gg[t]), acc[t]);
+                dg8[t] = kLn2 * x * kp[t];
             }
+            tmem_st8(acc_dk + c8, acc);
+            dg2_add(r64, c0, dg8, false);
         }
         {
             const int c0 = c64(64);
             float d[8];
-            tmem_ld16x2_8<8>(tl(384 + col0(64)), d);
+            tmem_ld16x2_8<8>(tl(64 + col0(64)), d);
 #pragma unroll
             for (int t = 0; t < 8; ++t) d[t] *= sBeta[c0 + t];
             *reinterpret_cast<uint4 *>(sm + S::dakk + tile_off(r64, c0, 64)) = pack8_at(d);
@@ -926,7 +923,7 @@ __global__ void __launch_bounds__(kUnitThreads, 1) chunk_bwd_unit_tc_kernel(BwdA
     tc_fence_after();
     // ---- X = Akk^T dAkk
     if (tid == 0) {
-        mma_bf16_seq<4, false>(tmem + 448, mnmaj(S::akk, 64), 2 * 64, mnmaj(S::dakk, 64), 2 * 64,
+        mma_bf16_seq<4, false>(tmem + 128, mnmaj(S::akk, 64), 2 * 64, mnmaj(S::dakk, 64), 2 * 64,
                                idesc_bf16(64, 64, true, true));
         mma_commit(&bar_mma);
     }
@@ -934,7 +931,7 @@ __global__ void __launch_bounds__(kUnitThreads, 1) chunk_bwd_unit_tc_kernel(BwdA
     {
         const int c0 = c64(64);
         float d[8];
-        tmem_ld16x2_8<8>(tl(448 + col0(64)), d);
+        tmem_ld16x2_8<8>(tl(128 + col0(64)), d);
         *reinterpret_cast<uint4 *>(sm + S::xt + tile_off(r64, c0, 64)) = pack8_at(d);
     }
     fence_async_smem();
@@ -943,7 +940,7 @@ __global__ void __launch_bounds__(kUnitThreads, 1) chunk_bwd_unit_tc_kernel(BwdA
     tc_fence_after();
     // ---- Y = X Akk^T
     if (tid == 0) {
-        mma_bf16_seq<4, false>(tmem + 64, kmaj(S::xt, 64), 16, kmaj(S::akk, 64), 16,
+        mma_bf16_seq<4, false>(tmem + 192, kmaj(S::xt, 64), 16, kmaj(S::akk, 64), 16,
                                idesc_bf16(64, 64, false, false));
         mma_commit(&bar_mma);
     }
@@ -952,29 +949,29 @@ __global__ void __launch_bounds__(kUnitThreads, 1) chunk_bwd_unit_tc_kernel(BwdA
     {
         const int c0 = c64(64);
         float y[8], pp[8];
-        tmem_ld16x2_8<8>(tl(64 + col0(64)), y);
+        tmem_ld16x2_8<8>(tl(192 + col0(64)), y);
         tmem_ld16x2_8<8>(tl(0 + col0(64)), pp);
-        {
-            const float br = sBeta[r64];
-            float db = 0.f;
+        const float br = sBeta[r64];
+        float db = 0.f;
 #pragma unroll
-            for (int t = 0; t < 8; ++t) {
-                const float dl = (c0 + t < r64) ? -y[t] : 0.f;
-                db = fmaf(dl, pp[t], db);
-                y[t] = br * dl;
-            }
-            *reinterpret_cast<uint4 *>(sm + S::dap + tile_off(r64, c0, 64)) = pack8_at(y);
-            atomicAdd(&sDbeta[r64], db);
+        for (int t = 0; t < 8; ++t) {
+            const float dl = (c0 + t < r64) ? -y[t] : 0.f;
+            db = fmaf(dl, pp[t], db);
+            y[t] = br * dl;
         }
+        *reinterpret_cast<uint4 *>(sm + S::dap + tile_off(r64, c0, 64)) = pack8_at(y);
+        atomicAdd(&sDbeta[r64], db);
     }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    // ---- [dP; dA] kn and dP^T kp + dA^T qp
+    // ---- dP kn, dA kn, dP^T kp + dA^T qp
     if (tid == 0) {
-        mma_bf16_seq<4, false>(tmem + 128, kmaj(S::dap, 64), 16, mnmaj(S::kn, KK), 2 * KK,
-                               idesc_bf16(128, KK, false, true));
+        mma_bf16_seq<4, false>(tmem + 0, kmaj(S::dap, 64), 16, mnmaj(S::kn, KK), 2 * KK,
+                               idesc_bf16(64, KK, false, true));
+        mma_bf16_seq<4, false>(tmem + 128, kmaj(S::dap + 64 * 64 * 2, 64), 16, mnmaj(S::kn, KK),
+                               2 * KK, idesc_bf16(64, KK, false, true));
         mma_bf16_seq<4, false>(tmem + 256, mnmaj(S::dap, 64), 2 * 64, mnmaj(S::kp, KK), 2 * KK,
                                idesc_bf16(64, KK, true, true));
         mma_bf16_seq<4, true>(tmem + 256, mnmaj(S::dap + 64 * 64 * 2, 64), 2 * 64, mnmaj(S::qp, KK),
@@ -982,52 +979,48 @@ __global__ void __launch_bounds__(kUnitThreads, 1) chunk_bwd_unit_tc_kernel(BwdA
         mma_commit(&bar_mma);
     }
     mma_wait();
-    // ---- (dP kn) 2^g2 -> dk, (dA kn) 2^g2 -> dq, (dP^T kp + dA^T qp) 2^-g2 -> dk, and
-    // their dg2 terms, in three passes so that no two threads share a dg2 element.
-    // Pass 0: rows 0..63 of the M = 128 result (dP kn) -> dk, dg2; rows 64..127
-    // (dA kn) -> dq.  Pass 1: rows 64..127 -> dg2.
-    {
-        const int c0 = col0(KK);
-        float d[KK / 4];
-        tmem_ld32(tl(128 + c0), d);
+    // ---- dk += (dP kn) 2^g2 + (dP^T kp + dA^T qp) 2^-g2, dq += (dA kn) 2^g2, their
+    // dg2 terms; dq and dk to global memory
 #pragma unroll
-        for (int pass = 0; pass < 2; ++pass) {
-            if (pass == 0 || !top) {
-#pragma unroll
-                for (int c8 = 0; c8 < KK / 4; c8 += 8) {
-                    float gg[8], fac[8], g8[8], dg8[8];
-                    g2v(r128, c0 + c8, gg);
-                    unpack8(sm + (top ? S::kp : S::qp) + tile_off(r128, c0 + c8, KK), fac);
-#pragma unroll
-                    for (int t = 0; t < 8; ++t) {
-                        g8[t] = d[c8 + t] * ex2f(gg[t]);
-                        dg8[t] = kLn2 * d[c8 + t] * fac[t];
-                    }
-                    if (pass == 0 && r128 < nr && c0 + c8 < p.K)
-                        add8(grow(top ? a.dk : a.dq, r128) + c0 + c8, g8);
-                    if (pass == 0 ? top : !top) dg2_add(r128, c0 + c8, dg8, false);
-                }
-            }
-            __syncthreads();
-        }
-    }
-    {
-        const int c0 = c64(KK);
-        float d[KK / 8];
-        tmem_ld16x2_16<KK / 8>(tl(256 + col0(KK)), d);
+    for (int c8 = 0; c8 < 16; c8 += 8) {
+        const int c0 = c64(KK) + c8;
+        float t1[8], t3[8], t9[8], ak[8], aq[8], gg[8], dg8[8];
+        tmem_ld16x2_8<16>(tl(0 + col0(KK) + c8), t1);
+        tmem_ld16x2_8<16>(tl(128 + col0(KK) + c8), t3);
+        tmem_ld16x2_8<16>(tl(256 + col0(KK) + c8), t9);
+        tmem_ld8(acc_dk + c8, ak);
+        tmem_ld8(acc_dq + c8, aq);
+        g2v(r64, c0, gg);
         {
+            float f[8];
+            unpack8(sm + S::kp + tile_off(r64, c0, KK), f);
 #pragma unroll
-            for (int c8 = 0; c8 < KK / 8; c8 += 8) {
-                float gg[8], kn[8], dk8[8], dg8[8];
-                g2v(r64, c0 + c8, gg);
-                unpack8(sm + S::kn + tile_off(r64, c0 + c8, KK), kn);
+            for (int t = 0; t < 8; ++t) dg8[t] = t1[t] * f[t];
+            unpack8(sm + S::qp + tile_off(r64, c0, KK), f);
 #pragma unroll
-                for (int t = 0; t < 8; ++t) {
-                    dk8[t] = d[c8 + t] * ex2f(-gg[t]);
-                    dg8[t] = -kLn2 * d[c8 + t] * kn[t];
-                }
-                if (r64 < nr && c0 + c8 < p.K) add8(grow(a.dk, r64) + c0 + c8, dk8);
-                dg2_add(r64, c0 + c8, dg8, false);
+            for (int t = 0; t < 8; ++t)  // (dA kn) . qp, and the first dq term's ln2 dq . qp 2^-g2
+                dg8[t] = fmaf(fmaf(aq[t], ex2f(-gg[t]), t3[t]), f[t], dg8[t]);
+            unpack8(sm + S::kn + tile_off(r64, c0, KK), f);
+#pragma unroll
+            for (int t = 0; t < 8; ++t) dg8[t] = kLn2 * fmaf(-t9[t], f[t], dg8[t]);
+        }
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            const float e = ex2f(gg[t]), ei = ex2f(-gg[t]);
+            ak[t] = fmaf(t1[t], e, fmaf(t9[t], ei, ak[t]));
+            aq[t] = fmaf(t3[t], e, aq[t]);
+        }
+        dg2_add(r64, c0, dg8, false);
+        if (r64 < nr && c0 < p.K) {
+            float *qd = grow(a.dq, r64) + c0, *kd = grow(a.dk, r64) + c0;
+            if (excl) {
+                *reinterpret_cast<float4 *>(qd) = make_float4(aq[0], aq[1], aq[2], aq[3]);
+                *reinterpret_cast<float4 *>(qd + 4) = make_float4(aq[4], aq[5], aq[6], aq[7]);
+                *reinterpret_cast<float4 *>(kd) = make_float4(ak[0], ak[1], ak[2], ak[3]);
+                *reinterpret_cast<float4 *>(kd + 4) = make_float4(ak[4], ak[5], ak[6], ak[7]);
+            } else {
+                add8(qd, aq);
+                add8(kd, ak);
             }
         }
     }

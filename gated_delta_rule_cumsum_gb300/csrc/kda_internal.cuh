@@ -226,7 +226,8 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st);
 // Chunked backward (kda_chunk_bwd), bf16 with K = V = 128: the forward re-run with
 // `c.bwd` and its checkpoints (final states to hend, [N][HV][K][V] fp32), the reverse
 // state scan (dhn, dvp: per-unit tiles; dgs: per unit [V/32][K] fp32 sums of
-// h_{c+1} dh_{c+1}), then the per-chunk gradients.  dq and dk must be zeroed first.
+// h_{c+1} dh_{c+1}), then the per-chunk gradients.  dq and dk must be zeroed first
+// when value heads share q/k heads (HV > H) or with packed sequences.
 bool chunk_bwd_tc_supported(int K, int V);
 cudaError_t launch_chunk_bwd_tc(const ChunkArgs &c, const void *dout, const float *dht, float *dq,
                                 float *dk, float *dv, float *dg, float *dbeta, float *dh0,

@@ -213,6 +213,18 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
     for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// The store counterpart of tmem_ld8: 32 lanes x 8 consecutive 32-bit columns (thread
+// t of the warp writes lane (warp % 4) * 32 + t), then wait for the store.
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const float (&v)[8]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n\t"
+        "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
+        : "memory");
+}
+
 // 16 lanes x N consecutive 32-bit columns for each half of the warp, then wait:
 // thread t < 16 receives lane base + t, columns [c, c + N); thread t >= 16 the same
 // lane base + t - 16, columns [c + OFF, c + OFF + N) (the 16x32bx2 shape).  For an

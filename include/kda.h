@@ -364,9 +364,13 @@ size_t kda_recurrent_bwd_workspace_size(const kda_shape *shape);
  * head) then forms dq, dk, dv, dbeta and dg.  Operands are bf16 (the inputs, the
  * checkpoints and the intermediate gradients), accumulation fp32.
  *   q, k, v, g, beta, h0, cu_seqlens, shape   as for kda_chunk_fwd.
- *   dout, dht, dq, dk, dv, dg, dbeta, dh0     as for kda_recurrent_bwd.  dq and dk
- *                      are summed with atomic adds (their rounding order varies);
- *                      with cu_seqlens, rows outside every sequence are zero.
+ *   dout, dht, dq, dk, dv, dg, dbeta, dh0     as for kda_recurrent_bwd.  With
+ *                      HV > H, dq and dk are summed over the value heads that share
+ *                      a q/k head with atomic adds (their rounding order varies);
+ *                      with HV == H every element is stored once and the result is
+ *                      deterministic.  With cu_seqlens, rows outside every sequence
+ *                      are zero.  A chunk refused for its gate range gets zero
+ *                      gradients (and KDA_DEVICE_GATE_RANGE).
  *   workspace          kda_chunk_bwd_workspace_size() bytes, 256-byte aligned.
  *   flags              KDA_FLAG_SERIAL only (the q/k L2 norm, a cumsummed gate and
  *                      the input activations take kda_recurrent_bwd /
