@@ -145,10 +145,11 @@ ChunkWs chunk_ws_layout(const kda_shape *s, bool packed, bool bwd = false) {
 // kda_chunk_bwd's workspace: the forward's (with the backward's unit tiles),
 // then per unit the checkpoints h_c ([K][V] bf16) and v'_c ([64][V]), and the
 // reverse scan's dL/dh_{c+1} ([K][V]) and dL/dv'_c ([64][V]); the final states
-// ([N][HV][K][V] fp32) and per unit [V/32][K] fp32 sums of h_{c+1} dh_{c+1}.
+// ([N][HV][K][V] fp32), per unit [V/32][K] fp32 sums of h_{c+1} dh_{c+1}, and the
+// state gradient where a pipelined call's two reverse-scan parts meet.
 struct ChunkBwdWs {
     ChunkWs f;
-    size_t ck_h, ck_vp, dhn, dvp, hend, dgs, total;
+    size_t ck_h, ck_vp, dhn, dvp, hend, dgs, dhm, total;
 };
 ChunkBwdWs chunk_bwd_ws_layout(const kda_shape *s, bool packed) {
     ChunkBwdWs W;
@@ -161,7 +162,8 @@ ChunkBwdWs chunk_bwd_ws_layout(const kda_shape *s, bool packed) {
     W.dvp = W.dhn + units * hb;
     W.hend = kda::align_up(W.dvp + units * vb, 256);
     W.dgs = kda::align_up(W.hend + (size_t)s->num_seqs * s->HV * s->K * s->V * 4, 256);
-    W.total = W.dgs + units * (size_t)(s->V / 32) * s->K * 4;
+    W.dhm = kda::align_up(W.dgs + units * (size_t)(s->V / 32) * s->K * 4, 256);
+    W.total = W.dhm + (size_t)s->num_seqs * s->HV * s->K * s->V * 4;
     return W;
 }
 
@@ -561,7 +563,9 @@ kda_status kda_chunk_bwd(const void *q, const void *k, const void *v, const floa
             return cuda_fail(e, op);
     e = kda::launch_chunk_bwd_tc(a, dout, dht, dq, dk, dv, dg, dbeta, dh0, ws + W.dhn, ws + W.dvp,
                                  reinterpret_cast<float *>(ws + W.hend),
-                                 reinterpret_cast<float *>(ws + W.dgs), s);
+                                 reinterpret_cast<float *>(ws + W.dgs),
+                                 reinterpret_cast<float *>(ws + W.dhm),
+                                 (shape->flags & KDA_FLAG_SERIAL) != 0, s);
     if (e != cudaSuccess) return cuda_fail(e, op);
     g_last_error.clear();
     return KDA_OK;

@@ -228,9 +228,14 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st);
 // state scan (dhn, dvp: per-unit tiles; dgs: per unit [V/32][K] fp32 sums of
 // h_{c+1} dh_{c+1}), then the per-chunk gradients.  dq and dk must be zeroed first
 // when value heads share q/k heads (HV > H) or with packed sequences.
+// A dense call of enough chunks pipelines the reverse scan with the gradient kernel
+// (dhm: [N][HV][K][V] fp32, the state gradient where the two scan parts meet) unless
+// `serial`.
 bool chunk_bwd_tc_supported(int K, int V);
+int chunk_bwd_pipe_m(int B, int HV, int V, int T, int sms);
 cudaError_t launch_chunk_bwd_tc(const ChunkArgs &c, const void *dout, const float *dht, float *dq,
                                 float *dk, float *dv, float *dg, float *dbeta, float *dh0,
-                                void *dhn, void *dvp, float *hend, float *dgs, cudaStream_t st);
+                                void *dhn, void *dvp, float *hend, float *dgs, float *dhm,
+                                bool serial, cudaStream_t st);
 
 }  // namespace kda

@@ -143,3 +143,30 @@ def test_autograd_takes_the_chunked_backward(kda_lib, wide_gate):
         got = leaves[name].grad
         err = parity.rel_err(got, ref[key])
         assert err <= TOL, (name, err)
+
+
+def test_pipelined_reverse_scan_matches_serial_and_oracle(kda_lib):
+    """Two sequences of 32 chunks (the last one ragged) over 8 heads: the call pipelines
+    the reverse scan with the gradient kernel (split at chunk 27 on 152 SMs), bit for bit
+    the serial call's result (no atomics when HV == H), and the oracle's on two heads."""
+    inp = _small(1411, B=2, T=2000, H=8, HV=8, K=128, V=128, g_hi=0.3)
+    dout, dht = _grads_in(inp, 1412)
+    q, k, v, g, beta, h0 = (inp[n] for n in ("q", "k", "v", "g", "beta", "h0"))
+    outs = []
+    for flags in (0, kda_lib.KDA_FLAG_SERIAL):
+        shape = kda_lib.make_shape(q, v, None, flags=flags)
+        ws = torch.empty(kda_lib.kda_chunk_bwd_workspace_size(shape), dtype=torch.uint8,
+                         device="cuda")
+        f32 = dict(dtype=torch.float32, device="cuda")
+        gr = dict(dq=torch.empty(q.shape, **f32), dk=torch.empty(k.shape, **f32),
+                  dv=torch.empty(v.shape, **f32), dg=torch.empty(g.shape, **f32),
+                  dbeta=torch.empty(beta.shape, **f32), dh0=torch.empty(h0.shape, **f32))
+        st = kda_lib.new_status()
+        kda_lib.kda_chunk_bwd(q, k, v, g, beta, h0, None, shape, dout, dht, gr["dq"], gr["dk"],
+                              gr["dv"], gr["dg"], gr["dbeta"], gr["dh0"], ws, st)
+        assert kda_lib.kda_read_device_status(st) == (0, 0)
+        outs.append(gr)
+    for name in NAMES:
+        assert torch.equal(outs[0][name], outs[1][name]), name
+    heads = [0, 7]
+    _check(outs[0], _oracle(inp, dout, dht, heads=heads), heads=heads)
