@@ -473,7 +473,7 @@ struct UnitSmem {
     static constexpr uint32_t dw = h;                         // [64][KK]
     static constexpr uint32_t dakk = dw + 64 * KK * 2;        // [64][64]
     static constexpr uint32_t xt = dakk + 64 * 64 * 2;        // [64][64] Akk^T dAkk
-    static constexpr uint32_t dg2 = dhn;                      // fp32 [64][KK]
+    static constexpr uint32_t dg2 = g2;                       // fp32 [64][KK], for the final cumsum
     static constexpr uint32_t dap = dout;                     // [128][64]: dP; dA
     static constexpr uint32_t beta = misc;                    // fp32 [64]
     static constexpr uint32_t gl = beta + 64 * 4;             // fp32 [KK]: G
@@ -481,7 +481,7 @@ struct UnitSmem {
     static constexpr uint32_t egl = dG + KK * 4;              // fp32 [KK]: 2^G
     static constexpr uint32_t seg = egl + KK * 4;             // fp32 [4][KK]: cumsum segment totals
     static constexpr uint32_t total = seg + 4 * KK * 4;
-    static_assert(xt + 64 * 64 * 2 <= dhn && dg2 + 64 * KK * 4 <= misc, "tiles over h and dh");
+    static_assert(xt + 64 * 64 * 2 <= dhn, "tiles over h");
     static_assert(128 * 64 * 2 <= 64 * VV * 2, "[dP; dA] fits over do");
 };
 
@@ -804,20 +804,6 @@ __global__ void __launch_bounds__(kUnitThreads, 1) chunk_bwd_unit_tc_kernel(BwdA
         const float4 y = *reinterpret_cast<const float4 *>(sG + fsw<KK>(r, c + 4));
         o[0] = x.x; o[1] = x.y; o[2] = x.z; o[3] = x.w; o[4] = y.x; o[5] = y.y; o[6] = y.z; o[7] = y.w;
     };
-    auto dg2_add = [&](int r, int c, const float (&x)[8], bool init) {
-        float4 *d0 = reinterpret_cast<float4 *>(sDg2 + fsw<KK>(r, c));
-        float4 *d1 = reinterpret_cast<float4 *>(sDg2 + fsw<KK>(r, c + 4));
-        if (init) {
-            *d0 = make_float4(x[0], x[1], x[2], x[3]);
-            *d1 = make_float4(x[4], x[5], x[6], x[7]);
-        } else {
-            float4 u = *d0, v = *d1;
-            u.x += x[0]; u.y += x[1]; u.z += x[2]; u.w += x[3];
-            v.x += x[4]; v.y += x[5]; v.z += x[6]; v.w += x[7];
-            *d0 = u;
-            *d1 = v;
-        }
-    };
     // Every result here is M = 64, read with the 16x32bx2 shape: this thread holds row
     // r64 and, of a result N wide, the N / 8 columns from c64(N) (the two half-warps
     // on adjacent column blocks).  Its dq and dk elements (16 each) accumulate in its
@@ -826,6 +812,9 @@ __global__ void __launch_bounds__(kUnitThreads, 1) chunk_bwd_unit_tc_kernel(BwdA
     auto col0 = [&](int N) { return part * (N / 4); };
     auto c64 = [&](int N) { return part * (N / 4) + hs * (N / 8); };
     const uint32_t acc_dq = tl(384 + part * 16), acc_dk = tl(448 + part * 16);
+    // this thread's 16 elements of dg2 (the gradient with respect to the cumsum), in
+    // registers until the final reverse cumsum
+    float dgr[16];
     const bool excl = p.H == p.HV;  // no other CTA adds to these q / k rows
 
     // ---- dq <- scale Qd 2^g2 (its dg2 term, ln2 scale Qd . qp = ln2 dq . qp 2^-g2, is
@@ -885,7 +874,8 @@ __global__ void __launch_bounds__(kUnitThreads, 1) chunk_bwd_unit_tc_kernel(BwdA
                 dg8[t] = -kLn2 * d[t] * kn[t] * sEgl[c0 + t];
             }
             tmem_st8(acc_dk + c8, acc);
-            dg2_add(r64, c0, dg8, true);
+#pragma unroll
+            for (int t = 0; t < 8; ++t) dgr[c8 + t] = dg8[t];
         }
     }
     tc_fence_before();
@@ -937,7 +927,8 @@ __global__ void __launch_bounds__(kUnitThreads, 1) chunk_bwd_unit_tc_kernel(BwdA
                 dg8[t] = kLn2 * x * kp[t];
             }
             tmem_st8(acc_dk + c8, acc);
-            dg2_add(r64, c0, dg8, false);
+#pragma unroll
+            for (int t = 0; t < 8; ++t) dgr[c8 + t] += dg8[t];
         }
         {
             const int c0 = c64(64);
@@ -1045,7 +1036,8 @@ __global__ void __launch_bounds__(kUnitThreads, 1) chunk_bwd_unit_tc_kernel(BwdA
             ak[t] = fmaf(t1[t], e, fmaf(t9[t], ei, ak[t]));
             aq[t] = fmaf(t3[t], e, aq[t]);
         }
-        dg2_add(r64, c0, dg8, false);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) dgr[c8 + t] += dg8[t];
         if (r64 < nr && c0 < p.K) {
             float *qd = grow(a.dq, r64) + c0, *kd = grow(a.dk, r64) + c0;
             if (excl) {
@@ -1059,6 +1051,12 @@ __global__ void __launch_bounds__(kUnitThreads, 1) chunk_bwd_unit_tc_kernel(BwdA
             }
         }
     }
+    // dg2 over g2, whose last reader was the loop above
+    __syncthreads();
+#pragma unroll
+    for (int c4 = 0; c4 < 16; c4 += 4)
+        *reinterpret_cast<float4 *>(sDg2 + fsw<KK>(r64, c64(KK) + c4)) =
+            make_float4(dgr[c4], dgr[c4 + 1], dgr[c4 + 2], dgr[c4 + 3]);
     tc_fence_before();
     __syncthreads();
     // ---- dg: g_scale x reverse cumsum of dg2 (G's gradient on the last row), per
