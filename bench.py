@@ -371,8 +371,31 @@ def oracle_sample(inp, max_tokens):
 def _oracle_run(part):
     import oracle
 
+    if "dout" in part:  # a backward workload: the fp64 chunk-form gradients
+        from oracle import chunk_backward
+
+        f64 = lambda t: None if t is None else t.double().numpy()
+        chunk_backward.chunk_grads(f64(part["q"]), f64(part["k"]), f64(part["v"]), f64(part["g"]),
+                                   f64(part["beta"]), f64(part["dout"]), f64(part["h0"]),
+                                   f64(part["dht"]),
+                                   cu_seqlens=None if part["cu_seqlens"] is None
+                                   else part["cu_seqlens"].numpy())
+        return
     oracle.recurrent(part["q"], part["k"], part["v"], part["g"], part["beta"], h0=part["h0"],
                      cu_seqlens=part["cu_seqlens"])
+
+
+def _with_grads_in(part):
+    """A backward sample's dL/do and dL/dht, drawn once from a fixed seed."""
+    import torch
+
+    gen = torch.Generator().manual_seed(11)
+    v, q = part["v"], part["q"]
+    n = q.shape[0] if part["cu_seqlens"] is None else part["cu_seqlens"].numel() - 1
+    part = dict(part)
+    part["dout"] = torch.randn(v.shape, generator=gen).to(v.dtype)
+    part["dht"] = torch.randn(n, v.shape[2], q.shape[3], v.shape[3], generator=gen)
+    return part
 
 
 def cpu_oracle_rate(inp, budget_s=10.0, max_runs=3):
@@ -412,14 +435,19 @@ def run_reference(args):
     else:
         inp = _make_inputs(args.workload, "cpu")
     w = inp["workload"]
+    backward = args.workload in BACKWARD
     # Size a step so that warm-up + steps end within ~2 minutes.
     probe, pL, _ = oracle_sample(inp, 256)
+    if backward:
+        probe = _with_grads_in(probe)
     _oracle_run(probe)
     t0 = time.perf_counter()
     _oracle_run(probe)
     probe_rate = pL / max(1e-6, time.perf_counter() - t0)
     per_step_s = max(0.02, 120.0 / max(1, args.steps + args.warmup))
     part, L, text = oracle_sample(inp, int(max(16, probe_rate * per_step_s)))
+    if backward:
+        part = _with_grads_in(part)
     import oracle
 
     for _ in range(args.warmup):
@@ -436,9 +464,11 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
         "config": workload_config(args.workload, args.gpus),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
+        "cpu_baseline": {"value": value, "unit": UNIT,
+                         "cores": 1 if backward else oracle.num_threads(),
                          "kind": "oracle", "sample_tokens_per_step": L,
-                         "sample": f"{text}, all {w.HV} heads, per step"},
+                         "sample": f"{text}, all {w.HV} heads, per step" +
+                                   (" (fp64 chunk-form gradients, numpy)" if backward else "")},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
