@@ -423,7 +423,7 @@ __global__ void __launch_bounds__(256, 2)
     const float neg_a = gate_act ? gate_neg_a(p.act, hv) : 0.f;
     const float gbias = gate_act && (tid & 127) < Kc ? gate_bias(p.act, hv, tid & 127, Kc) : 0.f;
     if (__builtin_expect(halo && !carry, 0)) {
-#pragma unroll
+#pragma unroll 1
         for (int it = 0; it < KK / 32; ++it) {
             const int idx = tid + it * 256, i = idx & 63, c = (idx >> 6) * 8;
             if (c < Kc)
@@ -638,7 +638,7 @@ __global__ void __launch_bounds__(256, 2)
                     aq = fmaf(qi, kj, aq);
                     ak = fmaf(ki, kj, ak);
                 }
-#pragma unroll
+#pragma unroll 1
                 for (int off = 16; off > 0; off >>= 1) {
                     aq += __shfl_xor_sync(0xffffffffu, aq, off);
                     ak += __shfl_xor_sync(0xffffffffu, ak, off);
@@ -661,7 +661,7 @@ __global__ void __launch_bounds__(256, 2)
     // ---- 3. elementwise, in place: 8 channels of one row per thread; lanes 0..7
     // take 8 consecutive rows of one column chunk, which the swizzle spreads over
     // all banks.  qg, kg, kb in place; qg and kg to the workspace.
-#pragma unroll
+#pragma unroll 1
     for (int it = 0; it < KK / 32; ++it) {
         const int idx = tid + it * 256, l = idx & 31, w = idx >> 5;
         const int i = (w & 7) * 8 + (l & 7);
@@ -742,7 +742,7 @@ __global__ void __launch_bounds__(256, 2)
         const uint32_t a0 = smem_addr(sAG), b0 = smem_addr(sKB) + ((fast || !halo) ? 0 : 8192);
         const uint32_t idn = idesc_bf16(128, (fast && halo) ? 128 : 64, false, false);
         if (fast || halo) {
-#pragma unroll
+#pragma unroll 1
             for (int kk = 0; kk < KK / 16; ++kk) {
                 const uint32_t ko = (kk >> 2) * S::kBlk + (kk & 3) * 32;
                 mma_bf16(tmem + (fast ? 0 : 64), sdesc_sw128(a0 + ko, 16, 1024),
@@ -757,33 +757,41 @@ __global__ void __launch_bounds__(256, 2)
     tc_fence_after();
     {
         const int quad = warp & 3, i = (tid & 127) & 63;
+        // 16 columns at a time, the loops kept rolled: code size, not issue slots, is
+        // what this kernel runs short of (its 2 x 256 threads wait on instruction fetch)
         if (warp < 4 && fast) {  // Aqk (rows 0..63) and L (rows 64..127) from columns 0..63
-            float dd[64];
-            tmem_ld64(tmem_at(tmem, quad * 32, 0), dd);
-            if (tid < 64) {
+            const float bi = sBeta[i];
+#pragma unroll 1
+            for (int c0 = 0; c0 < 64; c0 += 16) {
+                float dd[16];
+                tmem_ld16(tmem_at(tmem, quad * 32, c0), dd);
+                if (tid < 64) {
 #pragma unroll
-                for (int c0 = 0; c0 < 64; c0 += 8) {
-                    float a8[8];
+                    for (int h = 0; h < 16; h += 8) {
+                        float a8[8];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) a8[j] = (c0 + j <= i) ? dd[c0 + j] : 0.f;
-                    *reinterpret_cast<uint4 *>(U + Lo.aqk + tile_off(i, c0, 64)) = pack8(a8);
+                        for (int j = 0; j < 8; ++j) a8[j] = (c0 + h + j <= i) ? dd[h + j] : 0.f;
+                        *reinterpret_cast<uint4 *>(U + Lo.aqk + tile_off(i, c0 + h, 64)) = pack8(a8);
+                    }
+                } else {
+#pragma unroll
+                    for (int h = 0; h < 16; h += 4)
+                        sta4<kSplitA>(sL, i, c0 + h,
+                                make_float4(c0 + h < i ? bi * dd[h] : 0.f,
+                                            c0 + h + 1 < i ? bi * dd[h + 1] : 0.f,
+                                            c0 + h + 2 < i ? bi * dd[h + 2] : 0.f,
+                                            c0 + h + 3 < i ? bi * dd[h + 3] : 0.f));
                 }
-            } else {
-                const float bi = sBeta[i];
-#pragma unroll
-                for (int c0 = 0; c0 < 64; c0 += 4)
-                    sta4<kSplitA>(sL, i, c0,
-                            make_float4(c0 < i ? bi * dd[c0] : 0.f, c0 + 1 < i ? bi * dd[c0 + 1] : 0.f,
-                                        c0 + 2 < i ? bi * dd[c0 + 2] : 0.f,
-                                        c0 + 3 < i ? bi * dd[c0 + 3] : 0.f));
             }
         }
         if (warp >= 6 && halo) {  // P = kg_c kgp^T from rows 64..127, columns 64..127
-            float dd[64];
-            tmem_ld64(tmem_at(tmem, quad * 32, 64), dd);
-#pragma unroll
-            for (int c0 = 0; c0 < 64; c0 += 8)
-                *reinterpret_cast<uint4 *>(sPB + tile_off(i, c0, 64)) = pack8_at(dd + c0);
+#pragma unroll 1
+            for (int c0 = 0; c0 < 64; c0 += 16) {
+                float dd[16];
+                tmem_ld16(tmem_at(tmem, quad * 32, 64 + c0), dd);
+                *reinterpret_cast<uint4 *>(sPB + tile_off(i, c0, 64)) = pack8_at(dd);
+                *reinterpret_cast<uint4 *>(sPB + tile_off(i, c0 + 8, 64)) = pack8_at(dd + 8);
+            }
         }
     }
     tc_fence_before();
@@ -850,7 +858,7 @@ __global__ void __launch_bounds__(256, 2)
     __syncthreads();
     // Akk diag(beta) as a bf16 operand tile (Akk is lower triangular), stored twice so
     // that the MMAs below give every result row in both TMEM lane halves.
-#pragma unroll
+#pragma unroll 1
     for (int it = 0; it < 2; ++it) {
         const int idx = tid + it * 256, l = idx & 31, w = idx >> 5;
         const int i = (w & 7) * 8 + (l & 7);
@@ -881,7 +889,7 @@ __global__ void __launch_bounds__(256, 2)
     const uint64_t adesc = sdesc(smem_addr(sAB), 128, 1024);  // [Akk diag(beta); the same]
     if (tid == 0) {
         const uint32_t kg0 = smem_addr(sAG) + 8192;
-#pragma unroll
+#pragma unroll 1
         for (int kk = 0; kk < 4; ++kk)
             mma_bf16(tmem, adesc + (uint64_t)(kk * 16), sdesc_sw128(kg0 + kk * 2048, S::kBlk, 1024),
                      idesc_bf16(128, KK, false, true), kk > 0);
@@ -958,7 +966,7 @@ __global__ void __launch_bounds__(256, 2)
                          idesc_bf16(128, VV, false, true), kk > 0);
         } else {
             // K step kk: v rows 16 kk .. 16 kk + 15 (the second half v_half further on)
-#pragma unroll
+#pragma unroll 1
             for (int kk = 0; kk < 4; ++kk)
                 mma_bf16(tmem, adesc + (uint64_t)(kk * 16),
                          sdesc(smem_addr(sV) + kk * 2 * VV * 16 + (kk >= 2 ? v_half : 0), VV * 16, 128),
@@ -977,7 +985,7 @@ __global__ void __launch_bounds__(256, 2)
     if (nxt->unit < uend) {
         if (tid == 0) issue(nxt, !pref, true, true, !pref);
         if (nxt->hv == hv && nxt->gc == gc + 1 && continues(p, nxt->cl, nxt->ncs)) {
-#pragma unroll
+#pragma unroll 1
             for (int it = 0; it < KK / 32; ++it) {
                 const int idx = tid + it * 256, i = idx & 63, c = (idx >> 6) * 8;
                 cp_async16(sKB + qk_off(64 + i, c), U + Lo.kgt + tile_off(i, c, KK));
@@ -989,16 +997,14 @@ __global__ void __launch_bounds__(256, 2)
         // u: the same row split as W, a quarter of the dv columns per warp
         const int quad = warp & 3, i = (tid & 127) & 63, part = (warp >> 2) + 2 * (quad >> 1);
         const int per = VV / 4, cbeg = part * per;  // per: a multiple of 8
-        if (per % 32 == 0) {
-            for (int c0 = cbeg; c0 < cbeg + per; c0 += 32) {
-                float dd[32];
-                tmem_ld32(tmem_at(tmem, quad * 32, c0), dd);
-#pragma unroll
-                for (int c = 0; c < 32; c += 16) {
-                    unsigned char *ub = U + Lo.u + ((size_t)((c0 + c) / kUB) * 64 + i) * kUB * 2;
-                    *reinterpret_cast<uint4 *>(ub) = pack8_at(dd + c);
-                    *reinterpret_cast<uint4 *>(ub + 16) = pack8_at(dd + c + 8);
-                }
+        if (per % 16 == 0) {
+#pragma unroll 1
+            for (int c0 = cbeg; c0 < cbeg + per; c0 += 16) {
+                float dd[16];
+                tmem_ld16(tmem_at(tmem, quad * 32, c0), dd);
+                unsigned char *ub = U + Lo.u + ((size_t)(c0 / kUB) * 64 + i) * kUB * 2;
+                *reinterpret_cast<uint4 *>(ub) = pack8_at(dd);
+                *reinterpret_cast<uint4 *>(ub + 16) = pack8_at(dd + 8);
             }
         } else {
             for (int c0 = cbeg; c0 < cbeg + per; c0 += 8) {
