@@ -136,6 +136,13 @@ def chunk_grads(q, k, v, g, beta, do, h0=None, dht=None, cu_seqlens=None, scale=
     chain rules.  Adds dA_log [HV] and ddt_bias [HV, K] (None when not given)."""
     f64 = lambda x: None if x is None else np.asarray(x, dtype=np.float64)
     q, k, g, beta = f64(q), f64(k), f64(g), f64(beta)
+    if cu_seqlens is not None:
+        # rows past the last offset belong to no sequence and are never read: they
+        # enter neither the core nor the options' sums over tokens
+        end = int(np.asarray(cu_seqlens)[-1])
+        q, k, g, beta = (x.copy() for x in (q, k, g, beta))
+        for x in (q, k, g, beta):
+            x[:, end:] = 0.0
     if l2norm:
         qh, rq = _l2norm_rows(q)
         kh, rk = _l2norm_rows(k)

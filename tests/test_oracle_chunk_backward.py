@@ -125,3 +125,27 @@ def test_activation_options(bias, beta_scale):
     assert max(err.values()) < 1e-12, err
     if not bias:
         assert got["ddt_bias"] is None
+
+
+def test_options_ignore_rows_past_the_last_offset():
+    """NaN in every input row past the last offset changes no gradient (the rows belong
+    to no sequence), with the norm and both activations on."""
+    p = _problem(9, T=14)
+    r = np.random.default_rng(10)
+    g_raw = r.standard_normal(p["g"].shape) - 1.0
+    b_raw = r.standard_normal(p["beta"].shape)
+    for x in (p["q"], p["k"], g_raw, b_raw):
+        x[:, 11:] = np.nan
+    args = (p["q"], p["k"], p["v"], g_raw, b_raw, p["do"], p["h0"], p["dht"])
+    kw = dict(cu_seqlens=p["cu"], g_scale=1.0 / math.log(2.0), l2norm=True,
+              A_log=r.uniform(-0.5, 0.8, 2), dt_bias=0.5 * r.standard_normal((2, 3)),
+              beta_scale=1.0)
+    ref = ob.recurrent_grads(*args, **kw)
+    got = cb.chunk_grads(*args, chunk_size=4, **kw)
+    names = NAMES + ("dA_log", "ddt_bias")
+    err = {n: float(np.abs(got[n][:, :11] - ref[n][:, :11]).max() / np.abs(ref[n]).max())
+           if n not in ("dh0", "dA_log", "ddt_bias") else
+           float(np.abs(got[n] - ref[n]).max() / np.abs(ref[n]).max()) for n in names}
+    assert max(err.values()) < 1e-12, err
+    for n in ("dq", "dk", "dv", "dg", "dbeta"):
+        assert np.all(got[n][:, 11:] == 0), n
