@@ -31,7 +31,7 @@ __all__ = [
     "kda_gate_cumsum", "kda_chunk_fwd", "kda_recurrent_fwd", "kda_chunk_workspace_size",
     "kda_workspace_size",
     "kda_recurrent_bwd", "kda_recurrent_bwd_workspace_size", "recurrent_kda_backward", "kda_autograd",
-    "kda_chunk_bwd", "kda_chunk_bwd_workspace_size", "chunk_kda_backward",
+    "kda_chunk_bwd", "kda_chunk_bwd_act", "kda_chunk_bwd_workspace_size", "chunk_kda_backward",
     "kda_gate_cumsum_act", "kda_chunk_fwd_act", "kda_recurrent_fwd_act", "kda_recurrent_bwd_act",
     "kda_chunk_fwd_noalloc", "KDA_NOALLOC_SCRATCH_BYTES",
     "kda_read_device_status", "kda_clear_device_status", "kda_status_string",
@@ -118,6 +118,9 @@ _SIGNATURES = {
     "kda_chunk_bwd": (_ST, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.POINTER(KdaShape),
                             _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP]),
     "kda_chunk_bwd_workspace_size": (_SZ, [ctypes.POINTER(KdaShape)]),
+    "kda_chunk_bwd_act": (_ST, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.POINTER(KdaShape),
+                                ctypes.POINTER(KdaActivation), _VP, _VP, _VP, _VP, _VP, _VP,
+                                _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP]),
     "kda_chunk_fwd_noalloc": (_ST, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.POINTER(KdaShape),
                                     _VP, _VP, _VP, _VP]),
     "kda_recurrent_fwd": (_ST, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.POINTER(KdaShape),
@@ -267,6 +270,18 @@ def kda_chunk_bwd(q, k, v, g, beta, h0, cu_seqlens, shape: KdaShape, dout, dht, 
                                 _ptr(cu_seqlens), ctypes.byref(shape), _ptr(dout), _ptr(dht),
                                 _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg), _ptr(dbeta), _ptr(dh0),
                                 _ptr(workspace), ws, _ptr(dev_status), _stream(stream)))
+
+
+def kda_chunk_bwd_act(q, k, v, g, beta, h0, cu_seqlens, shape: KdaShape, act: KdaActivation,
+                      dout, dht, dq, dk, dv, dg, dbeta, dh0, dA_log, ddt_bias, workspace,
+                      dev_status=None, stream=None):
+    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().kda_chunk_bwd_act(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0),
+                                    _ptr(cu_seqlens), ctypes.byref(shape), ctypes.byref(act),
+                                    _ptr(dout), _ptr(dht), _ptr(dq), _ptr(dk), _ptr(dv),
+                                    _ptr(dg), _ptr(dbeta), _ptr(dh0), _ptr(dA_log),
+                                    _ptr(ddt_bias), _ptr(workspace), ws, _ptr(dev_status),
+                                    _stream(stream)))
 
 
 def kda_recurrent_bwd_act(q, k, v, g, beta, h0, cu_seqlens, shape: KdaShape, act: KdaActivation,
@@ -470,17 +485,20 @@ def recurrent_kda_backward(q, k, v, gate, beta, dout, initial_state=None, dht=No
 
 
 def chunk_kda_backward(q, k, v, gate, beta, dout, initial_state=None, dht=None, *,
-                       cu_seqlens=None, scale=None, g_scale=1.0, want_dh0=True, dev_status=None,
-                       stream=None, workspace=None):
-    """The gradients recurrent_kda_backward returns (dq, dk, dv, dg, dbeta, dh0 as fp32),
-    computed by kda_chunk_bwd in the chunked form on the tensor cores (bf16 inputs,
-    K = V = 128).  `workspace`, if given, is a uint8 device tensor of at least
-    kda_chunk_bwd_workspace_size bytes."""
-    ts = [q, k, v, gate, beta, dout, initial_state, dht, cu_seqlens, dev_status, workspace]
+                       cu_seqlens=None, scale=None, g_scale=1.0, want_dh0=True,
+                       use_qk_l2norm_in_kernel=False, A_log=None, dt_bias=None,
+                       beta_sigmoid_scale=0.0, dev_status=None, stream=None, workspace=None):
+    """The gradients recurrent_kda_backward returns (dq, dk, dv, dg, dbeta, dh0 as fp32,
+    and with the activations dA_log and ddt_bias), computed by kda_chunk_bwd in the
+    chunked form on the tensor cores (bf16 inputs, K = V = 128).  `workspace`, if
+    given, is a uint8 device tensor of at least kda_chunk_bwd_workspace_size bytes."""
+    ts = [q, k, v, gate, beta, dout, initial_state, dht, cu_seqlens, A_log, dt_bias, dev_status,
+          workspace]
     _one_device(*ts)
-    q, k, v, g, beta, dout, h0, dht, cu = [
-        None if t is None else t.detach().contiguous() for t in ts[:9]]
-    shape = make_shape(q, v, cu, scale, g_scale, 0)
+    q, k, v, g, beta, dout, h0, dht, cu, A_log, dt_bias = [
+        None if t is None else t.detach().contiguous() for t in ts[:11]]
+    shape = make_shape(q, v, cu, scale, g_scale,
+                       KDA_FLAG_QK_L2NORM if use_qk_l2norm_in_kernel else 0)
     f32 = dict(dtype=torch.float32, device=q.device)
     out = dict(dq=torch.empty(q.shape, **f32), dk=torch.empty(k.shape, **f32),
                dv=torch.empty(v.shape, **f32), dg=torch.empty(g.shape, **f32),
@@ -490,8 +508,17 @@ def chunk_kda_backward(q, k, v, gate, beta, dout, initial_state=None, dht=None, 
     if workspace is None:
         workspace = torch.empty(max(kda_chunk_bwd_workspace_size(shape), 256), dtype=torch.uint8,
                                 device=q.device)
-    kda_chunk_bwd(q, k, v, g, beta, h0, cu, shape, dout, dht, out["dq"], out["dk"], out["dv"],
-                  out["dg"], out["dbeta"], out["dh0"], workspace, dev_status, stream)
+    if A_log is not None or beta_sigmoid_scale:
+        out["dA_log"] = None if A_log is None else torch.empty(A_log.shape, **f32)
+        out["ddt_bias"] = None if dt_bias is None else torch.empty(dt_bias.shape, **f32)
+        kda_chunk_bwd_act(q, k, v, g, beta, h0, cu, shape,
+                          make_activation(A_log, dt_bias, beta_sigmoid_scale), dout, dht,
+                          out["dq"], out["dk"], out["dv"], out["dg"], out["dbeta"], out["dh0"],
+                          out["dA_log"], out["ddt_bias"], workspace, dev_status, stream)
+    else:
+        kda_chunk_bwd(q, k, v, g, beta, h0, cu, shape, dout, dht, out["dq"], out["dk"],
+                      out["dv"], out["dg"], out["dbeta"], out["dh0"], workspace, dev_status,
+                      stream)
     return out
 
 
@@ -529,15 +556,16 @@ class _KdaFunction(torch.autograd.Function):
         # 2^-9 per element) before the fp32 backward uses it.
         do = torch.zeros_like(v) if do is None else do.to(q.dtype)
         gr = None
-        if (q.dtype == torch.bfloat16 and q.shape[3] == 128 and v.shape[3] == 128
-                and not ctx.l2norm and A_log is None and not ctx.beta_sigmoid_scale):
+        if q.dtype == torch.bfloat16 and q.shape[3] == 128 and v.shape[3] == 128:
             # the chunked backward on the tensor cores; a chunk whose gate range it
             # does not take is reported on the status word, and then the token
             # recurrence's backward runs instead (this reads the word: one sync)
             st = new_status(q.device)
             gr = chunk_kda_backward(q, k, v, g, beta, do, h0, dht, cu_seqlens=cu,
                                     scale=ctx.scale, g_scale=ctx.g_scale,
-                                    want_dh0=h0 is not None, dev_status=st)
+                                    want_dh0=h0 is not None, use_qk_l2norm_in_kernel=ctx.l2norm,
+                                    A_log=A_log, dt_bias=dt_bias,
+                                    beta_sigmoid_scale=ctx.beta_sigmoid_scale, dev_status=st)
             if kda_read_device_status(st)[1] & KDA_DEVICE_GATE_RANGE:
                 gr = None
         if gr is None:
@@ -559,8 +587,8 @@ def kda_autograd(q, k, v, g, beta, initial_state=None, *, cu_seqlens=None, scale
                  g_scale=1.0, chunked=True, use_qk_l2norm_in_kernel=False, A_log=None,
                  dt_bias=None, beta_sigmoid_scale=0.0):
     """(o, ht) with gradients: forward by chunk_kda (or recurrent_kda when `chunked` is
-    False), backward by kda_chunk_bwd where it applies (bf16, K = V = 128, no in-op
-    L2 norm or activations), else kda_recurrent_bwd; `g` is the per-token log2 gate,
+    False), backward by kda_chunk_bwd where it applies (bf16, K = V = 128), else
+    kda_recurrent_bwd; `g` is the per-token log2 gate,
     or with `A_log` the raw gate (A_log and dt_bias then receive gradients too)."""
     _one_device(q, k, v, g, beta, initial_state, cu_seqlens, A_log, dt_bias)
     return _KdaFunction.apply(q, k, v, g, beta, initial_state, cu_seqlens, scale, g_scale, chunked,

@@ -487,16 +487,33 @@ kda_status kda_chunk_bwd(const void *q, const void *k, const void *v, const floa
                          float *dk, float *dv, float *dg, float *dbeta, float *dh0,
                          void *workspace, size_t workspace_bytes, int32_t *dev_status,
                          kda_stream_t stream) {
+    return kda_chunk_bwd_act(q, k, v, g, beta, h0, cu_seqlens, shape, nullptr, dout, dht, dq, dk,
+                             dv, dg, dbeta, dh0, nullptr, nullptr, workspace, workspace_bytes,
+                             dev_status, stream);
+}
+
+kda_status kda_chunk_bwd_act(const void *q, const void *k, const void *v, const float *g,
+                             const void *beta, const float *h0, const int32_t *cu_seqlens,
+                             const kda_shape *shape, const kda_activation *act, const void *dout,
+                             const float *dht, float *dq, float *dk, float *dv, float *dg,
+                             float *dbeta, float *dh0, float *dA_log, float *ddt_bias,
+                             void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                             kda_stream_t stream) {
     const char *op = "kda_chunk_bwd";
     kda_status st = check_common(op, shape, cu_seqlens);
     if (st != KDA_OK) return st;
+    kda::GateAct ga;
+    if ((st = resolve_act(op, shape, act, &ga)) != KDA_OK) return st;
+    if ((ga.A_log && !dA_log) || (ga.dt_bias && !ddt_bias))
+        return fail(KDA_ERR_INVALID_ARG, "%s: dA_log (and ddt_bias with dt_bias) must be non-NULL "
+                    "with the gate activation", op);
     if (shape->dtype != KDA_DTYPE_BF16 || !kda::chunk_bwd_tc_supported(shape->K, shape->V))
         return fail(KDA_ERR_UNSUPPORTED, "%s: bf16 inputs with K = V = 128 only (got dtype %d, "
                     "K=%d, V=%d); kda_recurrent_bwd takes the rest", op, (int)shape->dtype,
                     shape->K, shape->V);
-    if (shape->flags & ~(uint32_t)KDA_FLAG_SERIAL)
-        return fail(KDA_ERR_UNSUPPORTED, "%s: flags 0x%x (only KDA_FLAG_SERIAL is taken; the "
-                    "q/k L2 norm and a cumsummed gate go through kda_recurrent_bwd)", op,
+    if (shape->flags & ~(uint32_t)(KDA_FLAG_SERIAL | KDA_FLAG_QK_L2NORM))
+        return fail(KDA_ERR_UNSUPPORTED, "%s: flags 0x%x (KDA_FLAG_QK_L2NORM and KDA_FLAG_SERIAL "
+                    "are taken; a cumsummed gate goes through kda_recurrent_bwd)", op,
                     shape->flags);
     const bool has_rows = (int64_t)shape->B * shape->T > 0;
     if (has_rows && (!q || !k || !v || !g || !beta || !dout || !dq || !dk || !dv || !dg || !dbeta))
@@ -524,10 +541,10 @@ kda_status kda_chunk_bwd(const void *q, const void *k, const void *v, const floa
     a.V = shape->V; a.N = shape->num_seqs;
     a.scale = resolve_scale(shape);
     a.g_scale = shape->g_scale;
-    a.l2norm = 0;
+    a.l2norm = (shape->flags & KDA_FLAG_QK_L2NORM) ? 1 : 0;
     a.g_is_cumsum = 0;
     a.test_timeout = 0;
-    a.act = kda::GateAct();
+    a.act = ga;
     a.ctrl = reinterpret_cast<kda::ChunkCtrl *>(ws + W.f.ctrl);
     a.chunk_start = reinterpret_cast<int32_t *>(ws + W.f.chunk_start);
     a.units = ws + W.f.units;
@@ -561,12 +578,34 @@ kda_status kda_chunk_bwd(const void *q, const void *k, const void *v, const floa
     for (const auto &z : zero)
         if (z[1] && (e = cudaMemsetAsync(reinterpret_cast<void *>(z[0]), 0, z[1], s)) != cudaSuccess)
             return cuda_fail(e, op);
+    if (ga.A_log && (e = cudaMemsetAsync(dA_log, 0, (size_t)shape->HV * 4, s)) != cudaSuccess)
+        return cuda_fail(e, op);
+    if (ga.dt_bias &&
+        (e = cudaMemsetAsync(ddt_bias, 0, (size_t)shape->HV * shape->K * 4, s)) != cudaSuccess)
+        return cuda_fail(e, op);
     e = kda::launch_chunk_bwd_tc(a, dout, dht, dq, dk, dv, dg, dbeta, dh0, ws + W.dhn, ws + W.dvp,
                                  reinterpret_cast<float *>(ws + W.hend),
                                  reinterpret_cast<float *>(ws + W.dgs),
                                  reinterpret_cast<float *>(ws + W.dhm),
                                  (shape->flags & KDA_FLAG_SERIAL) != 0, s);
     if (e != cudaSuccess) return cuda_fail(e, op);
+    if (a.l2norm || ga.A_log || ga.beta_scale > 0.f) {
+        // the kernels formed the gradients of the normalised rows and of the activated
+        // gate and beta: the options' chain rules, as in kda_recurrent_bwd
+        kda::RecurrentBwdArgs r{};
+        r.q = q; r.k = k; r.v = v; r.g = g; r.beta = beta; r.h0 = h0; r.cu = cu_seqlens;
+        r.dq = dq; r.dk = dk; r.dv = dv; r.dg = dg; r.dbeta = dbeta; r.dh0 = dh0;
+        r.status = dev_status;
+        r.B = shape->B; r.T = shape->T; r.H = shape->H; r.HV = shape->HV; r.K = shape->K;
+        r.V = shape->V; r.N = shape->num_seqs;
+        r.scale = a.scale;
+        r.g_scale = a.g_scale;
+        r.l2norm = a.l2norm;
+        r.act = ga;
+        r.dA_log = dA_log;
+        r.ddt_bias = ddt_bias;
+        if ((e = kda::launch_bwd_chain(r, KDA_DTYPE_BF16, s)) != cudaSuccess) return cuda_fail(e, op);
+    }
     g_last_error.clear();
     return KDA_OK;
 }

@@ -655,6 +655,18 @@ __global__ void __launch_bounds__(kUnitThreads, 1) chunk_bwd_unit_tc_kernel(BwdA
             if (r < nr && c < p.K)
                 x[it] = *reinterpret_cast<const float4 *>(p.g + ((rowbase + r) * p.HV + hv) * p.K + c);
         }
+        if (p.act.A_log) {  // the activated gate -exp(A_log) softplus(g + dt_bias), as the forward
+            const float na = gate_neg_a(p.act, hv);
+#pragma unroll
+            for (int it = 0; it < kGIt; ++it) {
+                const int pc = tid + it * NT, r = pc / (KK / 4), c = (pc % (KK / 4)) * 4;
+                if (r < nr && c < p.K) {
+                    float *e = reinterpret_cast<float *>(&x[it]);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) e[j] = na * softplus_f(e[j] + gate_bias(p.act, hv, c + j, p.K));
+                }
+            }
+        }
 #pragma unroll
         for (int it = 0; it < kVIt; ++it) {
             const int pc = tid + it * NT, r = pc / (VV / 8), c = (pc % (VV / 8)) * 8;
@@ -667,8 +679,10 @@ __global__ void __launch_bounds__(kUnitThreads, 1) chunk_bwd_unit_tc_kernel(BwdA
         }
         if (tid < 64) {
             float bt = 0.f;
-            if (tid < nr)
+            if (tid < nr) {
                 bt = to_f32(static_cast<const __nv_bfloat16 *>(p.beta)[(rowbase + tid) * p.HV + hv]);
+                if (p.act.beta_scale > 0.f) bt = beta_activate<__nv_bfloat16>(bt, p.act.beta_scale);
+            }
             sBeta[tid] = bt;
         }
 #pragma unroll
@@ -749,6 +763,25 @@ __global__ void __launch_bounds__(kUnitThreads, 1) chunk_bwd_unit_tc_kernel(BwdA
         float fq[8], fk[8];
         unpack8(qraw[it], fq);
         unpack8(kraw[it], fk);
+        if (p.l2norm) {  // q / sqrt(sum q^2 + 1e-6) per row, as the forward: 16 threads a row
+            float sq = 0.f, sk = 0.f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                sq = fmaf(fq[j], fq[j], sq);
+                sk = fmaf(fk[j], fk[j], sk);
+            }
+#pragma unroll
+            for (int o = 1; o < 16; o <<= 1) {
+                sq += __shfl_xor_sync(0xffffffffu, sq, o);
+                sk += __shfl_xor_sync(0xffffffffu, sk, o);
+            }
+            const float rq = 1.f / sqrtf(sq + 1e-6f), rk = 1.f / sqrtf(sk + 1e-6f);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                fq[j] *= rq;
+                fk[j] *= rk;
+            }
+        }
         const float4 g0 = *reinterpret_cast<const float4 *>(sG + fsw<KK>(r, c));
         const float4 g1 = *reinterpret_cast<const float4 *>(sG + fsw<KK>(r, c + 4));
         const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};

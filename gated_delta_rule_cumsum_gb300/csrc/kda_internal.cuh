@@ -167,6 +167,10 @@ struct RecurrentBwdArgs {
 // Workspace of kda_recurrent_bwd: the checkpoints of every 8 tokens.
 size_t recurrent_bwd_ckpt_bytes(int B, int T, int N, int HV, int K, int V);
 cudaError_t launch_recurrent_bwd(const RecurrentBwdArgs &a, kda_dtype dt, cudaStream_t st);
+// Only the options' chain rules (q/k L2 norm when a.l2norm, the input activations
+// when a.act sets them) on gradients already summed with respect to the normalised
+// rows and the activated gate and beta (the chunked backward's last step).
+cudaError_t launch_bwd_chain(const RecurrentBwdArgs &a, kda_dtype dt, cudaStream_t st);
 
 struct ChunkArgs {
     const void *q, *k, *v;

@@ -501,6 +501,9 @@ __global__ void __launch_bounds__(256) act_bwd_kernel(RecurrentBwdArgs p, int64_
 }
 
 template <typename T>
+cudaError_t launch_chain_typed(const RecurrentBwdArgs &a, cudaStream_t st);
+
+template <typename T>
 cudaError_t launch_bwd_typed(const RecurrentBwdArgs &a, cudaStream_t st) {
     const int64_t blocks = (int64_t)a.N * a.HV * ((a.V + kBWarps - 1) / kBWarps);
     if (blocks == 0) return cudaSuccess;
@@ -523,6 +526,14 @@ cudaError_t launch_bwd_typed(const RecurrentBwdArgs &a, cudaStream_t st) {
     recurrent_bwd_kernel<T><<<(unsigned)blocks, kBThreads, smem, st>>>(a);
     prof_end(st);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    return launch_chain_typed<T>(a, st);
+}
+
+// The options' chain rules on summed gradients (the q/k L2 norm, then the input
+// activations), shared with the chunked backward.
+template <typename T>
+cudaError_t launch_chain_typed(const RecurrentBwdArgs &a, cudaStream_t st) {
+    cudaError_t e = cudaSuccess;
     const int64_t rows = (int64_t)a.B * a.T;
     if (rows == 0) return cudaSuccess;
     if (a.l2norm) {
@@ -562,6 +573,11 @@ size_t recurrent_bwd_ckpt_bytes(int B, int T, int N, int HV, int K, int V) {
 cudaError_t launch_recurrent_bwd(const RecurrentBwdArgs &a, kda_dtype dt, cudaStream_t st) {
     if (dt == KDA_DTYPE_BF16) return launch_bwd_typed<__nv_bfloat16>(a, st);
     return launch_bwd_typed<float>(a, st);
+}
+
+cudaError_t launch_bwd_chain(const RecurrentBwdArgs &a, kda_dtype dt, cudaStream_t st) {
+    if (dt == KDA_DTYPE_BF16) return launch_chain_typed<__nv_bfloat16>(a, st);
+    return launch_chain_typed<float>(a, st);
 }
 
 }  // namespace kda

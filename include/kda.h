@@ -372,9 +372,9 @@ size_t kda_recurrent_bwd_workspace_size(const kda_shape *shape);
  *                      are zero.  A chunk refused for its gate range gets zero
  *                      gradients (and KDA_DEVICE_GATE_RANGE).
  *   workspace          kda_chunk_bwd_workspace_size() bytes, 256-byte aligned.
- *   flags              KDA_FLAG_SERIAL only (the q/k L2 norm, a cumsummed gate and
- *                      the input activations take kda_recurrent_bwd /
- *                      kda_recurrent_bwd_act).
+ *   flags              KDA_FLAG_QK_L2NORM (q, k normalised inside the op; dq, dk
+ *                      are the raw rows' gradients) and KDA_FLAG_SERIAL; a cumsummed
+ *                      gate takes kda_recurrent_bwd.
  * Supported: bf16, K = V = 128.  A chunk whose gate range is too wide raises
  * KDA_DEVICE_GATE_RANGE in *dev_status.  Tensors 16-byte aligned.
  */
@@ -384,6 +384,21 @@ kda_status kda_chunk_bwd(const void *q, const void *k, const void *v, const floa
                          float *dk, float *dv, float *dg, float *dbeta, float *dh0,
                          void *workspace, size_t workspace_bytes, int32_t *dev_status,
                          kda_stream_t stream);
+/*
+ * kda_chunk_bwd on raw g / beta with the activations of *act (see kda_activation), the
+ * forward being kda_chunk_fwd_act's: the gradients of the raw inputs, dA_log and
+ * ddt_bias as for kda_recurrent_bwd_act.  With KDA_FLAG_QK_L2NORM (either entry point)
+ * the rows are normalised inside the op and dq, dk are the raw rows' gradients.  The
+ * kernels form the gradients of the normalised rows and the activated gate and beta;
+ * the chain rules follow in two elementwise passes (the ones kda_recurrent_bwd uses).
+ */
+kda_status kda_chunk_bwd_act(const void *q, const void *k, const void *v, const float *g,
+                             const void *beta, const float *h0, const int32_t *cu_seqlens,
+                             const kda_shape *shape, const kda_activation *act, const void *dout,
+                             const float *dht, float *dq, float *dk, float *dv, float *dg,
+                             float *dbeta, float *dh0, float *dA_log, float *ddt_bias,
+                             void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                             kda_stream_t stream);
 /* Bytes of workspace kda_chunk_bwd needs for *shape (0 on invalid shapes).  As for
  * kda_chunk_workspace_size, a shape that may be packed (B == 1) is sized for packed
  * input, which covers a dense call of the same shape too. */

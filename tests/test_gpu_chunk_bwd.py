@@ -170,3 +170,131 @@ def test_pipelined_reverse_scan_matches_serial_and_oracle(kda_lib):
         assert torch.equal(outs[0][name], outs[1][name]), name
     heads = [0, 7]
     _check(outs[0], _oracle(inp, dout, dht, heads=heads), heads=heads)
+
+
+RCP_LN2 = 1.0 / np.log(2.0)
+
+
+def _raw_gate(inp, seed, tail=None):
+    """Raw gate and beta logits (NaN from row `tail` on), A_log and dt_bias; the raw gate
+    sits low enough that a chunk's activated gate range stays inside the split grams'."""
+    gen = torch.Generator().manual_seed(seed)
+    B, T, HV, K = inp["g"].shape
+    g_raw = torch.randn(B, T, HV, K, generator=gen) - 4.0
+    b_raw = torch.randn(B, T, HV, generator=gen)
+    if tail is not None:
+        g_raw[:, tail:] = float("nan")
+        b_raw[:, tail:] = float("nan")
+    A_log = torch.log(1.0 + 3.0 * torch.rand(HV, generator=gen))
+    dt_bias = 0.5 * torch.randn(HV, K, generator=gen)
+    return (g_raw.cuda(), b_raw.to(torch.bfloat16).cuda(), A_log.cuda(), dt_bias.cuda())
+
+
+def _oracle_opts(inp, g, beta, dout, dht, **kw):
+    cu = inp["cu_seqlens"]
+    g = g if isinstance(g, np.ndarray) else _np(g)
+    return ocb.chunk_grads(_np(inp["q"]), _np(inp["k"]), _np(inp["v"]), g, _np(beta),
+                           _np(dout), _np(inp["h0"]), _np(dht),
+                           cu_seqlens=None if cu is None else cu.cpu().numpy(), **kw)
+
+
+def _gate_errors(inp, dg, dA_log, ddt_bias, g_raw, A_log, dt_bias, dout, dht, end, b_raw=None,
+                 **kw):
+    """Errors of the raw gate's gradients, each on the scale the core's bound carries to it.
+
+    The raw gate's gradient is the core gate's (dga) times -exp(A_log) sigmoid(g + dt_bias),
+    a factor that spans two orders of magnitude here: it reweights the rows, so the
+    core's bound is checked on dga, recovered by dividing the factor out.  dA_log and
+    dt_bias's gradient are sums over tokens of dga times ga and times the factor; those
+    sums cancel, so their errors are taken relative to the bound TOL max|dga| carried
+    through the sums (error / that bound, TOL when at the bound); that bound is loose, so
+    the sums are also checked as sums: the op's dA_log and dt_bias's gradient against the
+    same sums over its own dga and raw-gate gradient ("_sum", fp32 reductions: 1e-5; measured below 1e-6)."""
+    x = _np(g_raw)[:, :end] + _np(dt_bias)[None, None]
+    a = np.exp(_np(A_log))[None, None, :, None]
+    fac = -a * 0.5 * (1.0 + np.tanh(0.5 * x))
+    ga = np.zeros(_np(g_raw).shape)
+    ga[:, :end] = -a * np.logaddexp(0.0, x)
+    core = _oracle_opts(inp, ga, inp["beta"] if b_raw is None else b_raw, dout, dht,
+                        g_scale=RCP_LN2, l2norm=True, **kw)
+    dga = core["dg"][:, :end]
+    dmax = np.abs(dga).max()
+    ref_dA = np.sum(dga * ga[:, :end], axis=(0, 1, 3))
+    ref_ddt = np.sum(dga * fac, axis=(0, 1))
+    got_dga = _np(dg)[:, :end] / fac
+    return {"dg_core": parity.rel_err(got_dga, dga),
+            "dA_log_sum": parity.rel_err(_np(dA_log),
+                                         np.sum(got_dga * ga[:, :end], axis=(0, 1, 3))),
+            "ddt_bias_sum": parity.rel_err(_np(ddt_bias), np.sum(_np(dg)[:, :end], axis=(0, 1))),
+            "dA_log": TOL * float((np.abs(_np(dA_log) - ref_dA)
+                                   / (dmax * np.abs(ga).sum(axis=(0, 1, 3)))).max()),
+            "ddt_bias": TOL * float((np.abs(_np(ddt_bias) - ref_ddt)
+                                     / (dmax * np.abs(fac).sum(axis=(0, 1)))).max())}
+
+
+@pytest.mark.parametrize("H,HV", [(2, 2), (1, 2)])
+def test_qk_l2norm_option(kda_lib, H, HV):
+    """Rows of norm 3 (q) and 0.5 (k) normalised inside the op: the raw rows' gradients
+    (with HV > H the normalised rows' gradients are summed before the norm's chain rule)."""
+    inp = _small(1421 + HV, B=2, T=150, H=H, HV=HV, K=128, V=128, g_hi=0.3)
+    inp["q"] = (inp["q"].float() * 3.0).to(torch.bfloat16)
+    inp["k"] = (inp["k"].float() * 0.5).to(torch.bfloat16)
+    dout, dht = _grads_in(inp, 1422)
+    got = _run(kda_lib, inp, dout, dht, use_qk_l2norm_in_kernel=True)
+    _check(got, _oracle_opts(inp, inp["g"], inp["beta"], dout, dht, l2norm=True))
+
+
+def test_input_activations_and_l2norm_packed(kda_lib):
+    """Raw gate through -exp(A_log) softplus(g + dt_bias), beta logits through the sigmoid
+    and the q/k norm, packed with an empty slot and a NaN tail: the raw inputs' gradients,
+    dA_log and dt_bias's."""
+    lens = [70, 0, 130, 9]
+    inp = _packed(1431, lens, HV=2, H=2, K=128, V=128)
+    end = sum(lens)
+    g_raw, b_raw, A_log, dt_bias = _raw_gate(inp, 1432, tail=end)
+    dout, dht = _grads_in(inp, 1433)
+    st = kda_lib.new_status()
+    got = kda_lib.chunk_kda_backward(inp["q"], inp["k"], inp["v"], g_raw, b_raw, dout, inp["h0"],
+                                     dht, cu_seqlens=inp["cu_seqlens"], g_scale=RCP_LN2,
+                                     use_qk_l2norm_in_kernel=True, A_log=A_log, dt_bias=dt_bias,
+                                     beta_sigmoid_scale=1.0, dev_status=st)
+    assert kda_lib.kda_read_device_status(st) == (0, 0)
+    ref = _oracle_opts(inp, g_raw, b_raw, dout, dht, g_scale=RCP_LN2, l2norm=True,
+                       A_log=_np(A_log), dt_bias=_np(dt_bias), beta_scale=1.0, beta_bf16=True)
+    errs = _errors(got, ref, rows=end)
+    errs.update(_gate_errors(inp, got["dg"], got["dA_log"], got["ddt_bias"], g_raw, A_log,
+                             dt_bias, dout, dht, end, b_raw=b_raw, beta_scale=1.0,
+                             beta_bf16=True))
+    print(errs)
+    bad = {n: e for n, e in errs.items()
+           if n != "dg" and not e <= (1e-5 if n.endswith("_sum") else TOL)}
+    assert not bad, errs
+    for name in ("dq", "dk", "dv", "dg", "dbeta"):
+        assert torch.all(got[name][:, end:] == 0), name
+
+
+def test_autograd_with_options_takes_the_chunked_backward(kda_lib):
+    """loss.backward() through kda_autograd with the q/k norm and the gate activation."""
+    inp = _small(1441, B=1, T=140, H=1, HV=1, K=128, V=128)
+    g_raw, _, A_log, dt_bias = _raw_gate(inp, 1442)
+    dout, dht = _grads_in(inp, 1443)
+    leaves = {n: t.clone().requires_grad_(True)
+              for n, t in (("q", inp["q"]), ("k", inp["k"]), ("v", inp["v"]), ("g", g_raw),
+                           ("beta", inp["beta"]), ("h0", inp["h0"]), ("A_log", A_log),
+                           ("dt_bias", dt_bias))}
+    o, ht = kda_lib.kda_autograd(leaves["q"], leaves["k"], leaves["v"], leaves["g"],
+                                 leaves["beta"], leaves["h0"], g_scale=RCP_LN2,
+                                 use_qk_l2norm_in_kernel=True, A_log=leaves["A_log"],
+                                 dt_bias=leaves["dt_bias"])
+    ((o.float() * dout.float()).sum() + (ht * dht).sum()).backward()
+    ref = _oracle_opts(inp, g_raw, inp["beta"], dout, dht, g_scale=RCP_LN2, l2norm=True,
+                       A_log=_np(A_log), dt_bias=_np(dt_bias))
+    errs = {key: parity.rel_err(leaves[name].grad, ref[key])
+            for name, key in (("q", "dq"), ("k", "dk"), ("v", "dv"), ("beta", "dbeta"),
+                              ("h0", "dh0"))}
+    errs.update(_gate_errors(inp, leaves["g"].grad, leaves["A_log"].grad,
+                             leaves["dt_bias"].grad, g_raw, A_log, dt_bias, dout, dht,
+                             inp["q"].shape[1]))
+    print(errs)
+    bad = {n: e for n, e in errs.items() if not e <= (1e-5 if n.endswith("_sum") else TOL)}
+    assert not bad, errs
