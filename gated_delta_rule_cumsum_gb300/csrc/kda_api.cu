@@ -83,7 +83,7 @@ struct ChunkWs {
     int64_t slots;
     bool split;
     size_t qc, e0, e1, pm, e0b;  // split launches (e0 also pipelined ones)
-    int pipe_m;                  // > 0: a dense call is pipelined at this chunk
+    kda::PipePlan pipe;          // parts > 0: a dense call is pipelined in these parts
 };
 
 // The tensor-core path serves bf16 inputs whose K and V it supports; fp32
@@ -119,13 +119,13 @@ ChunkWs chunk_ws_layout(const kda_shape *s, bool packed, bool bwd = false) {
     L.split = !bwd && (s->flags & KDA_FLAG_SPLIT_SCAN) && use_tc(s) &&
               kda::chunk_tc_split(s->num_seqs, s->HV, s->K, s->V, s->T);
     L.qc = L.e0 = L.e1 = L.pm = L.e0b = 0;
-    L.pipe_m = 0;
+    L.pipe = kda::PipePlan{};
     if (!L.split && use_tc(s) && !(s->flags & KDA_FLAG_SERIAL)) {
         // Sized the same for dense and packed shapes (only dense calls pipeline;
         // the workspace size cannot tell a B = 1 dense call from a packed one).
         int sms = 0;
-        if (device_sm_count(&sms)) L.pipe_m = kda::chunk_tc_pipe_m(s->B, s->HV, s->K, s->V, s->T, sms);
-        if (L.pipe_m > 0) {
+        if (device_sm_count(&sms)) L.pipe = kda::chunk_tc_pipe_plan(s->B, s->HV, s->K, s->V, s->T, sms);
+        if (L.pipe.parts > 0) {
             L.e0 = kda::align_up(L.total, 256);
             L.total = L.e0 + (size_t)s->B * s->HV * s->K * s->V * 4;
         }
@@ -445,11 +445,10 @@ kda_status kda_chunk_fwd_act(const void *q, const void *k, const void *v, const 
     a.e1 = L.split ? reinterpret_cast<float *>(ws + L.e1) : nullptr;
     a.pm = L.split ? reinterpret_cast<float *>(ws + L.pm) : nullptr;
     a.e0b = L.split ? ws + L.e0b : nullptr;
-    a.pipe = (!packed && L.pipe_m > 0) ? 1 : 0;
-    a.pipe_m = a.pipe ? L.pipe_m : 0;
+    a.pipe = packed ? kda::PipePlan{} : L.pipe;
     a.prep_c0 = a.prep_c1 = 0;
-    a.scan_seg = 0;
-    if (a.pipe) a.e0 = reinterpret_cast<float *>(ws + L.e0);
+    a.scan_c0 = a.scan_c1 = 0;
+    if (a.pipe.parts > 0) a.e0 = reinterpret_cast<float *>(ws + L.e0);
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e;
@@ -551,11 +550,10 @@ kda_status kda_chunk_bwd_act(const void *q, const void *k, const void *v, const 
     a.slots = W.f.slots;
     a.split = 0;
     a.qc = nullptr; a.e1 = nullptr; a.pm = nullptr; a.e0b = nullptr;
-    a.pipe = (!packed && W.f.pipe_m > 0) ? 1 : 0;
-    a.pipe_m = a.pipe ? W.f.pipe_m : 0;
-    a.e0 = a.pipe ? reinterpret_cast<float *>(ws + W.f.e0) : nullptr;
+    a.pipe = packed ? kda::PipePlan{} : W.f.pipe;
+    a.e0 = a.pipe.parts > 0 ? reinterpret_cast<float *>(ws + W.f.e0) : nullptr;
     a.prep_c0 = a.prep_c1 = 0;
-    a.scan_seg = 0;
+    a.scan_c0 = a.scan_c1 = 0;
     a.bwd = 1;
     a.ck_h = ws + W.ck_h;
     a.ck_vp = ws + W.ck_vp;

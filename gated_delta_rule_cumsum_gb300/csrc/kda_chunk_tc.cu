@@ -33,6 +33,7 @@
 #include "kda_tc.cuh"
 #include "kda_chunk_layout.cuh"
 
+#include <algorithm>
 #include <mutex>
 
 #include <cuda.h>
@@ -45,9 +46,11 @@ using namespace tc;
 
 // Whether a chunk continues the scan of the chunk before it: not a sequence's
 // first chunk, nor the first chunk of the second segment of a split launch or of
-// the second part of a pipelined one (those scans start from a given state).
+// a pipelined launch's part (those scans start from a given state).  A prep
+// launch of a pipelined call covers one part, which starts at prep_c0.
 __device__ __forceinline__ bool continues(const ChunkArgs &p, int cl, int seq_chunks) {
-    return cl > 0 && !(p.split && cl == (seq_chunks + 1) / 2) && !(p.pipe && cl == p.pipe_m);
+    return cl > 0 && !(p.split && cl == (seq_chunks + 1) / 2) &&
+           !(p.pipe.parts > 0 && cl == p.prep_c0);
 }
 
 // A prep launch's units: every chunk slot of every value head, or (a pipelined
@@ -1123,7 +1126,7 @@ __device__ __forceinline__ ScanItem scan_item(const ChunkArgs &p, int64_t bid) {
     const int j = (int)(bid % bpp);
     it.hv = (int)((bid / bpp) % p.HV);
     it.n = (int)(bid / ((int64_t)bpp * p.HV));
-    it.seg = p.pipe ? p.scan_seg : (j < nreal ? 0 : 1);
+    it.seg = p.pipe.parts > 0 ? (p.scan_c0 > 0 ? 1 : 0) : (j < nreal ? 0 : 1);
     it.ident = j >= 2 * nreal;
     it.vb = j < nreal ? j : (j < 2 * nreal ? j - nreal : j - 2 * nreal);
     return it;
@@ -1169,8 +1172,9 @@ __global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
     if (p.split) {
         const int m = (nc + 1) / 2;
         if (item.seg == 0) c1 = m; else c0 = m;
-    } else if (p.pipe) {
-        if (item.seg == 0) c1 = min(p.pipe_m, nc); else c0 = min(p.pipe_m, nc);
+    } else if (p.pipe.parts > 0) {
+        c0 = min(p.scan_c0, nc);
+        c1 = min(p.scan_c1, nc);
     }
     const int ncs = c1 - c0;
     const int R = ncs > 0 ? ncs + 1 : 0;  // rounds
@@ -1318,8 +1322,8 @@ __global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
         if (ident) {
 #pragma unroll
             for (int j = 0; j < SBV; ++j) h[j] = (row == vb * SBV + j) ? 1.f : 0.f;
-        } else if (glob_row && (item.seg == 0 ? p.h0 : (p.pipe ? p.e0 : nullptr))) {
-            // a pipelined launch's second part starts from the first part's final state
+        } else if (glob_row && (item.seg == 0 ? p.h0 : (p.pipe.parts > 0 ? p.e0 : nullptr))) {
+            // a pipelined launch's later parts start from the previous part's final state
             const float *h_init = item.seg == 0 ? p.h0 : p.e0;
             const float4 *src = reinterpret_cast<const float4 *>(
                 h_init + (((size_t)n * p.HV + hv) * p.K + row) * (size_t)p.V + (size_t)vb * SBV);
@@ -1392,8 +1396,8 @@ __global__ void __launch_bounds__(320, 1) chunk_scan_tc_kernel(ChunkArgs p) {
         // final state: ht, or for a split sequence E0 / E1 / P
         float *dst_base = nullptr;
         int width = p.V;
-        if (p.pipe) {
-            dst_base = item.seg == 0 ? p.e0 : p.ht;
+        if (p.pipe.parts > 0) {
+            dst_base = c1 >= nc ? p.ht : p.e0;
         } else if (!p.split) {
             dst_base = p.ht;
         } else if (ident) {
@@ -1895,12 +1899,13 @@ cudaError_t launch_scan_any(const ChunkArgs &a, cudaStream_t st, int sms) {
     return launch_scan<KK, 32>(a, st);
 }
 
-// The library's own stream for a pipelined launch's second prep (lowest
-// priority) and the events that fork it from the caller's stream and join it
-// back, one set per device.
+// The library's own stream for a pipelined launch's later preps (lowest
+// priority), the event that forks it from the caller's stream and one event per
+// later part that joins it back, one set per device.
 struct PipeStreams {
     cudaStream_t side = nullptr;
-    cudaEvent_t fork = nullptr, join = nullptr;
+    cudaEvent_t fork = nullptr;
+    cudaEvent_t join[kMaxPipeParts] = {};
 };
 std::mutex g_pipe_mu;
 
@@ -1915,7 +1920,9 @@ cudaError_t pipe_streams(PipeStreams **out) {
         int least = 0, greatest = 0;
         if ((e = cudaDeviceGetStreamPriorityRange(&least, &greatest)) != cudaSuccess) return e;
         if ((e = cudaEventCreateWithFlags(&ps.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
-        if ((e = cudaEventCreateWithFlags(&ps.join, cudaEventDisableTiming)) != cudaSuccess) return e;
+        for (int i = 0; i < kMaxPipeParts; ++i)
+            if ((e = cudaEventCreateWithFlags(&ps.join[i], cudaEventDisableTiming)) != cudaSuccess)
+                return e;
         if ((e = cudaStreamCreateWithPriority(&ps.side, cudaStreamNonBlocking, least)) != cudaSuccess)
             return e;
     }
@@ -1923,35 +1930,48 @@ cudaError_t pipe_streams(PipeStreams **out) {
     return cudaSuccess;
 }
 
-// Pipelined: prep of chunks [0, m), then on the caller's stream the scan of
-// [0, m) (final state to e0) and, once the side stream's prep of [m, nc) on the
-// SMs the scan leaves free is done, the scan of [m, nc) from e0.  The first
-// scan follows the first prep in stream order, so its CTAs are placed as soon
-// as that prep ends, ahead of the second prep, which waits on an event.  No
-// kernel waits for another: the streams and events order whole launches.
+// Pipelined: the prep of part 0 on every SM, then on the caller's stream the
+// scans of parts 0, 1, ... in order, each from the state the one before left in
+// e0 (the last one to ht).  The preps of parts 1, 2, ... run one after another
+// on the side stream, on the SMs the scans leave free, from the moment part 0's
+// prep ends; part i's scan also waits on the event recorded after its prep.
+// Part 0's scan follows its prep in stream order, so its CTAs are placed as soon
+// as that prep ends, ahead of the side stream's prep, which waits on an event.
+// No kernel waits for another: the streams and events order whole launches.
 template <int KK, int VV>
 cudaError_t launch_pipelined(const ChunkArgs &a, cudaStream_t st, int sms) {
     std::lock_guard<std::mutex> lock(g_pipe_mu);
     PipeStreams *ps = nullptr;
     cudaError_t e = pipe_streams(&ps);
     if (e != cudaSuccess) return e;
-    const int nc = (a.T + kBT - 1) / kBT;
+    const PipePlan &pl = a.pipe;
+    if (pl.parts < 2 || pl.parts > kMaxPipeParts) return cudaErrorInvalidValue;
     const int64_t scan_ctas = (int64_t)a.N * a.HV * (a.V / (scan_wide(a.N, a.HV, a.V, sms) ? 64 : 32));
-    ChunkArgs pa = a, pb = a, s0 = a, s1 = a;
-    pa.prep_c0 = 0;
-    pa.prep_c1 = a.pipe_m;
-    pb.prep_c0 = a.pipe_m;
-    pb.prep_c1 = nc;
-    s0.scan_seg = 0;
-    s1.scan_seg = 1;
-    if ((e = launch_prep<KK>(pa, st)) != cudaSuccess) return e;
+    auto part = [&](int i, bool prep) {
+        ChunkArgs x = a;
+        if (prep) {
+            x.prep_c0 = pl.cut[i];
+            x.prep_c1 = pl.cut[i + 1];
+        } else {
+            x.scan_c0 = pl.cut[i];
+            x.scan_c1 = pl.cut[i + 1];
+        }
+        return x;
+    };
+    if ((e = launch_prep<KK>(part(0, true), st)) != cudaSuccess) return e;
     if ((e = cudaEventRecord(ps->fork, st)) != cudaSuccess) return e;
-    if ((e = launch_scan_any<KK, VV>(s0, st, sms)) != cudaSuccess) return e;
+    if ((e = launch_scan_any<KK, VV>(part(0, false), st, sms)) != cudaSuccess) return e;
     if ((e = cudaStreamWaitEvent(ps->side, ps->fork, 0)) != cudaSuccess) return e;
-    if ((e = launch_prep<KK>(pb, ps->side, 2 * (sms - scan_ctas))) != cudaSuccess) return e;
-    if ((e = cudaEventRecord(ps->join, ps->side)) != cudaSuccess) return e;
-    if ((e = cudaStreamWaitEvent(st, ps->join, 0)) != cudaSuccess) return e;
-    return launch_scan_any<KK, VV>(s1, st, sms);
+    for (int i = 1; i < pl.parts; ++i) {
+        if ((e = launch_prep<KK>(part(i, true), ps->side, 2 * (sms - scan_ctas))) != cudaSuccess)
+            return e;
+        if ((e = cudaEventRecord(ps->join[i], ps->side)) != cudaSuccess) return e;
+    }
+    for (int i = 1; i < pl.parts; ++i) {
+        if ((e = cudaStreamWaitEvent(st, ps->join[i], 0)) != cudaSuccess) return e;
+        if ((e = launch_scan_any<KK, VV>(part(i, false), st, sms)) != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 template <int KK, int VV>
@@ -1959,7 +1979,7 @@ cudaError_t launch_kv(const ChunkArgs &a, cudaStream_t st) {
     cudaError_t e = cudaSuccess;
     int sms = 0;
     if ((e = sm_count(&sms)) != cudaSuccess) return e;
-    if (a.pipe) return launch_pipelined<KK, VV>(a, st, sms);
+    if (a.pipe.parts > 0) return launch_pipelined<KK, VV>(a, st, sms);
     if (a.slots > 0 && (e = launch_prep<KK>(a, st)) != cudaSuccess) return e;
     if (!a.split) return launch_scan_any<KK, VV>(a, st, sms);
     if ((e = launch_scan<KK, 64>(a, st)) != cudaSuccess) return e;
@@ -1992,32 +2012,83 @@ size_t chunk_tc_unit_bytes(int K, int V, bool bwd) {
     return tc_layout(K <= 64 ? 64 : 128, V, bwd).stride;
 }
 
-int chunk_tc_pipe_m(int B, int HV, int K, int V, int T, int sms) {
-    // Cost model in scan rounds: at two prep CTAs per SM a prep unit takes about
-    // 23 scan rounds (17.8 us against 0.78 us at K = V = 128, measured).  Serial:
-    // every unit, then 1 + nc rounds.  Pipelined at m: the units of [0, m) on all
-    // SMs, then the longer of (1 + m rounds) and (the units of [m, nc) on the
-    // SMs the scan leaves free), then 1 + nc - m rounds.
-    constexpr int64_t kUnit = 23;
-    if (!chunk_tc_supported(K, V) || B <= 0 || HV <= 0 || T <= 0 || sms <= 0) return 0;
+namespace {
+PipePlan pipe_plan_search(int B, int HV, int K, int V, int T, int sms) {
+    // Cost model in scan rounds.  At two prep CTAs per SM a wave of prep units
+    // takes about 19 scan rounds (14.3 us against 0.78 us at K = V = 128, measured
+    // on the whole GPU).  Serial: every unit, then 1 + nc rounds.  Pipelined: part
+    // 0's units on every SM; part i's scan starts when part i - 1's scan has ended
+    // and the side stream has prepped parts 1..i (on the SMs the scans leave
+    // free), and takes 1 + its chunks rounds.  Each middle part (with more than
+    // two parts) is the largest whose prep, started when the previous one ends,
+    // is done by the time the previous part's scan is; the last part takes the
+    // rest.  Every first cut and part count is tried.  At the training shape the
+    // model picks chunk 76, the best of a measured sweep (181 us; 189 us at the
+    // earlier cost of 23 rounds a wave, which picked chunk 91).
+    constexpr int64_t kUnit = 19;
+    PipePlan best_plan;
+    if (!chunk_tc_supported(K, V) || B <= 0 || HV <= 0 || T <= 0 || sms <= 0) return best_plan;
     const int64_t nc = (T + kBT - 1) / kBT;
     const int64_t scan_ctas = (int64_t)B * HV * (V / (scan_wide(B, HV, V, sms) ? 64 : 32));
-    if (2 * scan_ctas > sms || nc < 16) return 0;
+    if (2 * scan_ctas > sms || nc < 16) return best_plan;
     const int64_t free_ctas = 2 * (sms - scan_ctas), all_ctas = 2 * (int64_t)sms;
-    auto waves = [](int64_t units, int64_t ctas) { return (units + ctas - 1) / ctas; };
     const int64_t hb = (int64_t)B * HV;
+    auto waves = [](int64_t units, int64_t ctas) { return (units + ctas - 1) / ctas; };
     int64_t best = waves(hb * nc, all_ctas) * kUnit + nc + 1;
-    int best_m = 0;
-    for (int64_t m = nc / 4; m + 4 <= nc; ++m) {
-        const int64_t second = waves(hb * (nc - m), free_ctas) * kUnit;
-        const int64_t cost = waves(hb * m, all_ctas) * kUnit + (m + 1 > second ? m + 1 : second) +
-                             nc - m + 1;
-        if (cost < best) {
-            best = cost;
-            best_m = (int)m;
+    for (int parts = 2; parts <= kMaxPipeParts; ++parts) {
+        for (int64_t m = 1; m + 1 <= nc; ++m) {
+            PipePlan pl;
+            pl.parts = parts;
+            pl.cut[0] = 0;
+            pl.cut[1] = (int)m;
+            int64_t prep = waves(hb * m, all_ctas) * kUnit;  // side stream's clock
+            int64_t scan_end = prep + m + 1;
+            int64_t done = m;
+            bool ok = true;
+            for (int i = 1; i < parts; ++i) {
+                int64_t n = nc - done;
+                if (i + 1 < parts) {
+                    // the largest part whose prep ends by scan_end (at least one chunk,
+                    // and one chunk left for every later part)
+                    const int64_t w = (scan_end - prep) / kUnit;
+                    n = std::min(w * free_ctas / hb, nc - done - (parts - 1 - i));
+                    if (n < 1) n = 1;
+                }
+                if (n < 1) { ok = false; break; }
+                prep += waves(hb * n, free_ctas) * kUnit;
+                scan_end = std::max(scan_end, prep) + n + 1;
+                done += n;
+                pl.cut[i + 1] = (int)done;
+            }
+            if (ok && done == nc && scan_end < best) {
+                best = scan_end;
+                best_plan = pl;
+            }
         }
     }
-    return best_m;
+    return best_plan;
+}
+}  // namespace
+
+PipePlan chunk_tc_pipe_plan(int B, int HV, int K, int V, int T, int sms) {
+    // The search costs O(nc) per part count: remembered for the last 16 shapes.
+    struct Entry {
+        int key[6];
+        PipePlan plan;
+    };
+    static std::mutex mu;
+    static Entry cache[16];
+    static int used = 0, next = 0;
+    const int key[6] = {B, HV, K, V, T, sms};
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i)
+        if (std::equal(key, key + 6, cache[i].key)) return cache[i].plan;
+    Entry &e = cache[next];
+    std::copy(key, key + 6, e.key);
+    e.plan = pipe_plan_search(B, HV, K, V, T, sms);
+    next = (next + 1) % 16;
+    if (used < 16) ++used;
+    return e.plan;
 }
 
 bool chunk_tc_split(int N, int HV, int K, int V, int T) {

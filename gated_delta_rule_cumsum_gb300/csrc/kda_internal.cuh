@@ -172,6 +172,17 @@ cudaError_t launch_recurrent_bwd(const RecurrentBwdArgs &a, kda_dtype dt, cudaSt
 // rows and the activated gate and beta (the chunked backward's last step).
 cudaError_t launch_bwd_chain(const RecurrentBwdArgs &a, kda_dtype dt, cudaStream_t st);
 
+// How a dense tensor-core forward is cut into pipelined parts: chunks
+// [cut[i], cut[i + 1]) of every sequence form part i, cut[0] = 0, cut[parts] = nc.
+// Two parts at most: at the training shape three and four parts measured slower
+// than two (187-210 us against 181 us), each extra part adding a launch's start-up
+// and more of the scans' time beside a prep than the model credits.
+constexpr int kMaxPipeParts = 2;
+struct PipePlan {
+    int parts = 0;
+    int cut[kMaxPipeParts + 1] = {};
+};
+
 struct ChunkArgs {
     const void *q, *k, *v;
     const float *g;
@@ -198,14 +209,14 @@ struct ChunkArgs {
     float *e0, *e1;        // [N][HV][K][V] fp32: the segments' final states from zero / h0
     void *e0b;             // [N][HV] bf16 [K][V] operand tiles of e0
     float *pm;             // [N][HV][K][K] fp32: segment 1's state transition
-    // Pipelined launches (tensor-core path, dense input): chunks [0, pipe_m) of
-    // every sequence are prepped and scanned first, and the scan of that part
-    // runs while the prep of [pipe_m, nc) occupies the SMs it leaves free; the
-    // second part's scan starts from the first part's final state (in e0).
-    int pipe;              // 1: pipelined launch
-    int pipe_m;            // first chunk of the second part
+    // Pipelined launches (tensor-core path, dense input): every sequence's chunks
+    // run in parts [pipe.cut[i], pipe.cut[i + 1]).  Part 0 is prepped on every SM;
+    // each later part's prep fills the SMs the scans leave free, and each part's
+    // scan starts from the state the previous part's scan left in e0 (read, then
+    // overwritten, by the same threads).
+    PipePlan pipe;         // pipe.parts == 0: not pipelined
     int prep_c0, prep_c1;  // a prep launch's chunks within every sequence (c1 <= c0: all slots)
-    int scan_seg;          // a pipelined scan launch's part: 0 from h0, 1 from e0
+    int scan_c0, scan_c1;  // a pipelined scan launch's chunks within every sequence
     // The chunked backward's re-run of the forward: the prep also stores W_c and
     // Akk_c in each unit (tc_layout with bwd), the scan stores the state at the
     // start of every chunk (ck_h, a [dk][V] bf16 operand tile per unit) and v'_c
@@ -218,10 +229,10 @@ cudaError_t launch_chunk_simt(const ChunkArgs &a, kda_dtype dt, cudaStream_t st)
 
 // Tensor-core path (bf16 inputs): K in {64, 128}, V a multiple of 32 up to 256.
 bool chunk_tc_supported(int K, int V);
-// The first chunk of a pipelined launch's second part for a dense input of B
-// sequences of T rows on a GPU of `sms` SMs, or 0 when running the prep and the
-// scan one after the other is expected to be as fast.
-int chunk_tc_pipe_m(int B, int HV, int K, int V, int T, int sms);
+// The parts a dense input of B sequences of T rows is pipelined in on a GPU of
+// `sms` SMs; parts == 0 when running the prep and then the scan, each over every
+// chunk, is expected to be as fast.
+PipePlan chunk_tc_pipe_plan(int B, int HV, int K, int V, int T, int sms);
 // Whether a launch splits each sequence's scan into two segments run at once.
 bool chunk_tc_split(int N, int HV, int K, int V, int T);
 size_t chunk_tc_unit_bytes(int K, int V, bool bwd = false);

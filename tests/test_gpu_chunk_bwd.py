@@ -147,8 +147,10 @@ def test_autograd_takes_the_chunked_backward(kda_lib, wide_gate):
 
 def test_pipelined_reverse_scan_matches_serial_and_oracle(kda_lib):
     """Two sequences of 32 chunks (the last one ragged) over 8 heads: the call pipelines
-    the reverse scan with the gradient kernel (split at chunk 27 on 152 SMs), bit for bit
-    the serial call's result (no atomics when HV == H), and the oracle's on two heads."""
+    the reverse scan with the gradient kernel (split at chunk 27 on 152 SMs) and the
+    forward's re-run in parts (a part's first chunk forms v' from its start state rather
+    than from the previous chunk's state and v', which rounds differently): within a few
+    bf16 roundings of the serial call's result, and the oracle's on two heads."""
     inp = _small(1411, B=2, T=2000, H=8, HV=8, K=128, V=128, g_hi=0.3)
     dout, dht = _grads_in(inp, 1412)
     q, k, v, g, beta, h0 = (inp[n] for n in ("q", "k", "v", "g", "beta", "h0"))
@@ -167,7 +169,8 @@ def test_pipelined_reverse_scan_matches_serial_and_oracle(kda_lib):
         assert kda_lib.kda_read_device_status(st) == (0, 0)
         outs.append(gr)
     for name in NAMES:
-        assert torch.equal(outs[0][name], outs[1][name]), name
+        err = parity.rel_err(outs[0][name], outs[1][name])
+        assert err <= 2e-3, (name, err)
     heads = [0, 7]
     _check(outs[0], _oracle(inp, dout, dht, heads=heads), heads=heads)
 

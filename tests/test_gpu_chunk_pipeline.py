@@ -2,9 +2,9 @@
 leaves most SMs idle runs in two parts: the prep of every sequence's first
 chunks, then that part's scan (final state to the workspace) while the prep of
 the remaining chunks fills the other SMs from the library's side stream, then
-the second part's scan from that state.  Each case here is a shape the split
-point rule pipelines; the profile report must show two prep and two scan
-launches, so a change of the rule cannot turn these into serial runs unseen."""
+the second part's scan from that state.  Each case here is a shape the plan
+pipelines; the profile report must show two prep and two scan launches, so a
+change of the plan cannot turn these into serial runs unseen."""
 import pytest
 import torch
 
