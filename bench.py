@@ -10,7 +10,7 @@ to flush the 129 MB L2.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload train|gva|packed|decode|decode_small|prefill|prefill_small|
-                              train_bwd|train_bwd_recurrent]
+                              train_bwd|train_bwd_recurrent|train_step]
 
 `--workload` picks one of the other synthetic workloads instead (grouped value
 heads B4 T4096 HV32; packed varlen H=HV=32; decode 4096 x 1 token; its
@@ -18,7 +18,10 @@ heads B4 T4096 HV32; packed varlen H=HV=32; decode 4096 x 1 token; its
 `kda_recurrent_fwd` call, a train_bwd step is one `kda_chunk_bwd` call (the
 gradients of the training shape for dL/do and dL/dht drawn once, in the chunked
 form on the tensor cores) and a train_bwd_recurrent step one `kda_recurrent_bwd`
-call (the same gradients by the token recurrence).  `--impl reference` times the fp64 CPU oracle
+call (the same gradients by the token recurrence); a train_step step is the
+forward that keeps the backward's state (`kda_chunk_fwd_save`: o and ht) followed
+by the backward from it (`kda_chunk_bwd` with KDA_FLAG_BWD_SAVED), a training
+step's work on this layer.  `--impl reference` times the fp64 CPU oracle
 instead, on the host cores, each step a bounded sample of the same workload.
 Under torchrun (N > 1) every rank runs its own replica of the workload (weak
 scaling, no collective on the data path); rank 0 prints the line with the
@@ -58,8 +61,11 @@ WORKLOADS = {
     # by the token recurrence (kda_recurrent_bwd)
     "train_bwd": (1, {}, 50, 5),
     "train_bwd_recurrent": (1, {}, 10, 3),
+    # forward (keeping the backward's state) + backward from it, the training shape
+    "train_step": (1, {}, 50, 5),
 }
-BACKWARD = ("train_bwd", "train_bwd_recurrent")
+BACKWARD = ("train_bwd", "train_bwd_recurrent", "train_step")
+CHUNK_BWD = ("train_bwd", "train_step")
 BWD_FLOPS_PER_ELEMENT = 26   # one forward pass (7) + the reverse sweep (19) per state element
 RECURRENT = ("decode", "decode_small", "prefill", "prefill_small")
 FP32_LANES_PER_SM = 128      # fp32 FMA lanes per SM (4 partitions x 32)
@@ -71,6 +77,8 @@ def _metric(name, w):
         return METRIC
     if name == "train_bwd":
         return f"chunk_kda bwd tokens/s ({w.name}) on 1 GB300"
+    if name == "train_step":
+        return f"chunk_kda fwd+bwd tokens/s ({w.name}) on 1 GB300"
     if name == "train_bwd_recurrent":
         return f"recurrent_kda bwd tokens/s ({w.name}) on 1 GB300"
     op = "recurrent_kda" if name in RECURRENT else "chunk_kda"
@@ -178,17 +186,23 @@ def chunk_bwd_flops(inp):
     return units * (64 * 1.41e5 + 7.3e6 + 1.78e7)
 
 
-def chunk_bwd_roofline(inp, per_kernel, prof_steps, ms, peaks, name):
+def chunk_bwd_roofline(inp, per_kernel, prof_steps, ms, peaks, name, with_forward_outputs=False):
     """The whole call against the tighter of HBM (its compulsory bytes) and the bf16
     tensor peak (its useful flops); the per-chunk gradient kernel, which reads and
-    writes almost all of those bytes, reported beside it."""
+    writes almost all of those bytes, reported beside it.  `with_forward_outputs`: a
+    training step, which also writes the forward's o and ht (its flops, the forward's
+    once, are already counted: the backward's own recompute is skipped)."""
     r, wr = chunk_bwd_bytes(inp)
+    if with_forward_outputs:
+        w = inp["workload"]
+        wr += _nbytes(inp["v"]) + inp["N"] * w.HV * w.K * w.V * 4
     flops = chunk_bwd_flops(inp)
     t_hbm = (r + wr) / (peaks["hbm_gbs"] * 1e9)
     t_tc = flops / (peaks["bf16_tflops"] * 1e12)
     sec = ms / 1e3
     unit_ms = sum(t for n, (t, _) in per_kernel.items() if n.startswith("chunk_bwd_unit")) / prof_steps
-    out = {"kernel": "kda_chunk_bwd (all launches)", "kernel_ms": ms,
+    out = {"kernel": ("kda_chunk_fwd_save + kda_chunk_bwd (all launches)" if with_forward_outputs
+                      else "kda_chunk_bwd (all launches)"), "kernel_ms": ms,
            "hbm": {"achieved": (r + wr) / sec / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                    "frac": (r + wr) / sec / 1e9 / peaks["hbm_gbs"], "algorithmic_bytes": r + wr},
            "tensor": {"achieved": flops / sec / 1e12, "peak": peaks["bf16_tflops"],
@@ -512,7 +526,7 @@ def run_ours(args):
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     backward = args.workload in BACKWARD
-    chunk_bwd = args.workload == "train_bwd"
+    chunk_bwd = args.workload in CHUNK_BWD
     if backward:
         # dL/do and dL/dht drawn once; the gradients land in preallocated fp32 buffers.
         gen = torch.Generator(device=dev).manual_seed(11)
@@ -524,9 +538,20 @@ def run_ours(args):
         grads = [torch.empty(t.shape, dtype=torch.float32, device=dev) for t in (q, k, v, g, beta)]
         dh0 = torch.empty(inp["N"], w.HV, w.K, w.V, dtype=torch.float32, device=dev)
         bwd_call = kda.kda_chunk_bwd if chunk_bwd else kda.kda_recurrent_bwd
+        if args.workload == "train_step":
+            o_fwd = torch.empty_like(v)
+            ht_fwd = torch.empty(inp["N"], w.HV, w.K, w.V, dtype=torch.float32, device=dev)
+            shape_saved = kda.make_shape(q, v, cu, flags=kda.KDA_FLAG_BWD_SAVED)
 
-        def call(q_, k_, v_, g_, beta_, h0_, o_, ht_, st):
-            bwd_call(q_, k_, v_, g_, beta_, h0_, cu, shape, o_, ht_, *grads, dh0, ws, status, st)
+            def call(q_, k_, v_, g_, beta_, h0_, o_, ht_, st):
+                kda.kda_chunk_fwd_save(q_, k_, v_, g_, beta_, h0_, cu, shape, None, o_fwd, ht_fwd,
+                                       ws, status, st)
+                kda.kda_chunk_bwd(q_, k_, v_, g_, beta_, h0_, cu, shape_saved, o_, ht_, *grads,
+                                  dh0, ws, status, st)
+        else:
+            def call(q_, k_, v_, g_, beta_, h0_, o_, ht_, st):
+                bwd_call(q_, k_, v_, g_, beta_, h0_, cu, shape, o_, ht_, *grads, dh0, ws, status,
+                         st)
         o = dout
     elif recurrent:
         # Decode keeps the state resident and updates it in place (ht == h0).
@@ -604,7 +629,8 @@ def run_ours(args):
         peak_source = ("measured in this run: FMA-loop microbenchmark "
                        "(kda_measure_fp32_fma_peak, 16 chains x 8x256 threads per SM)")
     if chunk_bwd:
-        roofline = chunk_bwd_roofline(inp, per_kernel, prof_steps, ms, peaks, args.workload)
+        roofline = chunk_bwd_roofline(inp, per_kernel, prof_steps, ms, peaks, args.workload,
+                                      with_forward_outputs=args.workload == "train_step")
     elif backward:
         flops = BWD_FLOPS_PER_ELEMENT * inp["tokens"] * w.HV * w.K * w.V
         step_ms = sum(t for t, _ in per_kernel.values()) / prof_steps

@@ -32,6 +32,7 @@ __all__ = [
     "kda_workspace_size",
     "kda_recurrent_bwd", "kda_recurrent_bwd_workspace_size", "recurrent_kda_backward", "kda_autograd",
     "kda_chunk_bwd", "kda_chunk_bwd_act", "kda_chunk_bwd_workspace_size", "chunk_kda_backward",
+    "kda_chunk_fwd_save", "chunk_kda_forward_save", "KDA_FLAG_BWD_SAVED",
     "kda_gate_cumsum_act", "kda_chunk_fwd_act", "kda_recurrent_fwd_act", "kda_recurrent_bwd_act",
     "kda_chunk_fwd_noalloc", "KDA_NOALLOC_SCRATCH_BYTES",
     "kda_read_device_status", "kda_clear_device_status", "kda_status_string",
@@ -45,6 +46,7 @@ KDA_ERR_BAD_CU_SEQLENS, KDA_ERR_CUDA, KDA_ERR_TIMEOUT = 3, 4, 5
 KDA_DTYPE_F32, KDA_DTYPE_BF16 = 0, 1
 KDA_FLAG_QK_L2NORM, KDA_FLAG_G_IS_CUMSUM, KDA_FLAG_SPLIT_SCAN = 1 << 0, 1 << 1, 1 << 2
 KDA_FLAG_SERIAL = 1 << 3
+KDA_FLAG_BWD_SAVED = 1 << 4
 KDA_FLAG_TEST_WAIT_TIMEOUT = 1 << 31
 KDA_DEVICE_BAD_CU_SEQLENS, KDA_DEVICE_TIMEOUT, KDA_DEVICE_INTERNAL = 1 << 0, 1 << 1, 1 << 2
 KDA_DEVICE_GATE_RANGE = 1 << 3
@@ -118,6 +120,8 @@ _SIGNATURES = {
     "kda_chunk_bwd": (_ST, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.POINTER(KdaShape),
                             _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP]),
     "kda_chunk_bwd_workspace_size": (_SZ, [ctypes.POINTER(KdaShape)]),
+    "kda_chunk_fwd_save": (_ST, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.POINTER(KdaShape),
+                                 ctypes.POINTER(KdaActivation), _VP, _VP, _VP, _SZ, _VP, _VP]),
     "kda_chunk_bwd_act": (_ST, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.POINTER(KdaShape),
                                 ctypes.POINTER(KdaActivation), _VP, _VP, _VP, _VP, _VP, _VP,
                                 _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP]),
@@ -270,6 +274,16 @@ def kda_chunk_bwd(q, k, v, g, beta, h0, cu_seqlens, shape: KdaShape, dout, dht, 
                                 _ptr(cu_seqlens), ctypes.byref(shape), _ptr(dout), _ptr(dht),
                                 _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg), _ptr(dbeta), _ptr(dh0),
                                 _ptr(workspace), ws, _ptr(dev_status), _stream(stream)))
+
+
+def kda_chunk_fwd_save(q, k, v, g, beta, h0, cu_seqlens, shape: KdaShape, act, o, ht, workspace,
+                       dev_status=None, stream=None):
+    """`act`: a KdaActivation or None."""
+    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().kda_chunk_fwd_save(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0),
+                                     _ptr(cu_seqlens), ctypes.byref(shape),
+                                     None if act is None else ctypes.byref(act), _ptr(o), _ptr(ht),
+                                     _ptr(workspace), ws, _ptr(dev_status), _stream(stream)))
 
 
 def kda_chunk_bwd_act(q, k, v, g, beta, h0, cu_seqlens, shape: KdaShape, act: KdaActivation,
@@ -484,21 +498,55 @@ def recurrent_kda_backward(q, k, v, gate, beta, dout, initial_state=None, dht=No
     return out
 
 
+@_on_tensor_device
+def chunk_kda_forward_save(q, k, v, g, beta, scale=None, initial_state=None,
+                           output_final_state=False, cu_seqlens=None,
+                           use_qk_l2norm_in_kernel=False, g_scale=1.0, A_log=None, dt_bias=None,
+                           beta_sigmoid_scale=0.0, workspace=None, dev_status=None, stream=None,
+                           serial=False):
+    """chunk_kda (the same o and ht) by kda_chunk_fwd_save: returns (o, ht or None,
+    saved), `saved` the uint8 workspace that a later chunk_kda_backward(..., saved=saved)
+    of the same inputs and options reads instead of running the forward again
+    (bf16 inputs, K = V = 128)."""
+    q, k, v, g, beta, h0, cu = _prep(q, k, v, g, beta, initial_state, cu_seqlens)
+    _one_device(q, workspace, dev_status, A_log, dt_bias)
+    flags = (KDA_FLAG_QK_L2NORM if use_qk_l2norm_in_kernel else 0) | (
+        KDA_FLAG_SERIAL if serial else 0)
+    shape = make_shape(q, v, cu, scale, g_scale, flags)
+    o = torch.empty(v.shape, dtype=q.dtype, device=q.device)
+    ht = (torch.empty(shape.num_seqs, shape.HV, shape.K, shape.V, dtype=torch.float32,
+                      device=q.device) if output_final_state else None)
+    if workspace is None:
+        workspace = torch.empty(max(kda_chunk_bwd_workspace_size(shape), 256), dtype=torch.uint8,
+                                device=q.device)
+    act = (make_activation(A_log, dt_bias, beta_sigmoid_scale)
+           if A_log is not None or beta_sigmoid_scale else None)
+    kda_chunk_fwd_save(q, k, v, g, beta, h0, cu, shape, act, o, ht, workspace, dev_status, stream)
+    return o, ht, workspace
+
+
+@_on_tensor_device
 def chunk_kda_backward(q, k, v, gate, beta, dout, initial_state=None, dht=None, *,
                        cu_seqlens=None, scale=None, g_scale=1.0, want_dh0=True,
                        use_qk_l2norm_in_kernel=False, A_log=None, dt_bias=None,
-                       beta_sigmoid_scale=0.0, dev_status=None, stream=None, workspace=None):
+                       beta_sigmoid_scale=0.0, dev_status=None, stream=None, workspace=None,
+                       saved=None):
     """The gradients recurrent_kda_backward returns (dq, dk, dv, dg, dbeta, dh0 as fp32,
     and with the activations dA_log and ddt_bias), computed by kda_chunk_bwd in the
     chunked form on the tensor cores (bf16 inputs, K = V = 128).  `workspace`, if
-    given, is a uint8 device tensor of at least kda_chunk_bwd_workspace_size bytes."""
+    given, is a uint8 device tensor of at least kda_chunk_bwd_workspace_size bytes;
+    `saved`, chunk_kda_forward_save's workspace for the same inputs and options: the
+    backward then starts from what it holds (KDA_FLAG_BWD_SAVED)."""
+    if saved is not None:
+        workspace = saved
     ts = [q, k, v, gate, beta, dout, initial_state, dht, cu_seqlens, A_log, dt_bias, dev_status,
           workspace]
     _one_device(*ts)
     q, k, v, g, beta, dout, h0, dht, cu, A_log, dt_bias = [
         None if t is None else t.detach().contiguous() for t in ts[:11]]
     shape = make_shape(q, v, cu, scale, g_scale,
-                       KDA_FLAG_QK_L2NORM if use_qk_l2norm_in_kernel else 0)
+                       (KDA_FLAG_QK_L2NORM if use_qk_l2norm_in_kernel else 0) |
+                       (KDA_FLAG_BWD_SAVED if saved is not None else 0))
     f32 = dict(dtype=torch.float32, device=q.device)
     out = dict(dq=torch.empty(q.shape, **f32), dk=torch.empty(k.shape, **f32),
                dv=torch.empty(v.shape, **f32), dg=torch.empty(g.shape, **f32),
@@ -529,14 +577,20 @@ class _KdaFunction(torch.autograd.Function):
 
     @staticmethod
     def forward(ctx, q, k, v, g, beta, h0, cu, scale, g_scale, chunked, l2norm, A_log, dt_bias,
-                beta_sigmoid_scale):
+                beta_sigmoid_scale, save):
+        ctx.saved = None
         with torch.no_grad():
             kw = dict(cu_seqlens=cu, output_final_state=True, scale=scale, g_scale=g_scale,
                       use_qk_l2norm_in_kernel=l2norm,
                       A_log=None if A_log is None else A_log.detach(),
                       dt_bias=None if dt_bias is None else dt_bias.detach(),
                       beta_sigmoid_scale=beta_sigmoid_scale)
-            if chunked:
+            if chunked and save and _chunk_bwd_applies(q, v):
+                # the forward that keeps what the chunked backward would recompute
+                o, ht, ctx.saved = chunk_kda_forward_save(
+                    q.detach(), k.detach(), v.detach(), g.detach(), beta.detach(),
+                    initial_state=None if h0 is None else h0.detach(), **kw)
+            elif chunked:
                 o, ht = chunk_kda(q.detach(), k.detach(), v.detach(), g.detach(), beta.detach(),
                                   initial_state=None if h0 is None else h0.detach(), **kw)
             else:
@@ -556,7 +610,7 @@ class _KdaFunction(torch.autograd.Function):
         # 2^-9 per element) before the fp32 backward uses it.
         do = torch.zeros_like(v) if do is None else do.to(q.dtype)
         gr = None
-        if q.dtype == torch.bfloat16 and q.shape[3] == 128 and v.shape[3] == 128:
+        if _chunk_bwd_applies(q, v):
             # the chunked backward on the tensor cores; a chunk whose gate range it
             # does not take is reported on the status word, and then the token
             # recurrence's backward runs instead (this reads the word: one sync)
@@ -565,7 +619,9 @@ class _KdaFunction(torch.autograd.Function):
                                     scale=ctx.scale, g_scale=ctx.g_scale,
                                     want_dh0=h0 is not None, use_qk_l2norm_in_kernel=ctx.l2norm,
                                     A_log=A_log, dt_bias=dt_bias,
-                                    beta_sigmoid_scale=ctx.beta_sigmoid_scale, dev_status=st)
+                                    beta_sigmoid_scale=ctx.beta_sigmoid_scale, dev_status=st,
+                                    saved=ctx.saved)
+            ctx.saved = None
             if kda_read_device_status(st)[1] & KDA_DEVICE_GATE_RANGE:
                 gr = None
         if gr is None:
@@ -579,21 +635,29 @@ class _KdaFunction(torch.autograd.Function):
         ddt = None if dt_bias is None else gr["ddt_bias"].to(dt_bias.dtype)
         return (gr["dq"].to(q.dtype), gr["dk"].to(k.dtype), gr["dv"].to(v.dtype),
                 gr["dg"].to(g.dtype), gr["dbeta"].to(beta.dtype), dh0, None, None, None, None,
-                None, dA, ddt, None)
+                None, dA, ddt, None, None)
 
 
 @_on_tensor_device
+def _chunk_bwd_applies(q, v):
+    return q.dtype == torch.bfloat16 and q.shape[3] == 128 and v.shape[3] == 128
+
+
 def kda_autograd(q, k, v, g, beta, initial_state=None, *, cu_seqlens=None, scale=None,
                  g_scale=1.0, chunked=True, use_qk_l2norm_in_kernel=False, A_log=None,
-                 dt_bias=None, beta_sigmoid_scale=0.0):
+                 dt_bias=None, beta_sigmoid_scale=0.0, save_for_backward=True):
     """(o, ht) with gradients: forward by chunk_kda (or recurrent_kda when `chunked` is
     False), backward by kda_chunk_bwd where it applies (bf16, K = V = 128), else
     kda_recurrent_bwd; `g` is the per-token log2 gate,
-    or with `A_log` the raw gate (A_log and dt_bias then receive gradients too)."""
+    or with `A_log` the raw gate (A_log and dt_bias then receive gradients too).
+    With `save_for_backward` (and the chunked backward applying) the forward keeps
+    the backward's recomputed state (kda_chunk_fwd_save: kda_chunk_bwd_workspace_size
+    bytes held until the backward) and the backward does not run the forward again;
+    False recomputes it in the backward."""
     _one_device(q, k, v, g, beta, initial_state, cu_seqlens, A_log, dt_bias)
     return _KdaFunction.apply(q, k, v, g, beta, initial_state, cu_seqlens, scale, g_scale, chunked,
                               bool(use_qk_l2norm_in_kernel), A_log, dt_bias,
-                              float(beta_sigmoid_scale))
+                              float(beta_sigmoid_scale), bool(save_for_backward))
 
 
 @_on_tensor_device

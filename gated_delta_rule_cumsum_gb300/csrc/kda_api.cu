@@ -27,7 +27,7 @@ kda_status cuda_fail(cudaError_t e, const char *where) {
 }
 
 constexpr uint32_t kKnownFlags = KDA_FLAG_QK_L2NORM | KDA_FLAG_G_IS_CUMSUM |
-                                  KDA_FLAG_SPLIT_SCAN | KDA_FLAG_SERIAL |
+                                  KDA_FLAG_SPLIT_SCAN | KDA_FLAG_SERIAL | KDA_FLAG_BWD_SAVED |
                                   KDA_FLAG_TEST_WAIT_TIMEOUT;
 
 // Checks shared by the three operations.  `need_h` also checks H and HV % H.
@@ -151,9 +151,14 @@ struct ChunkBwdWs {
     ChunkWs f;
     size_t ck_h, ck_vp, dhn, dvp, hend, dgs, dhm, total;
 };
+// The same for every flag a kda_chunk_fwd_save / kda_chunk_bwd pair may differ in
+// (KDA_FLAG_SERIAL, KDA_FLAG_BWD_SAVED): the backward reads the forward's tiles where
+// the forward put them.
 ChunkBwdWs chunk_bwd_ws_layout(const kda_shape *s, bool packed) {
     ChunkBwdWs W;
-    W.f = chunk_ws_layout(s, packed, true);
+    kda_shape sp = *s;
+    sp.flags &= ~(uint32_t)(KDA_FLAG_SERIAL | KDA_FLAG_BWD_SAVED);
+    W.f = chunk_ws_layout(&sp, packed, true);
     const size_t units = (size_t)W.f.slots * s->HV;
     const size_t hb = (size_t)s->K * s->V * 2, vb = (size_t)64 * s->V * 2;
     W.ck_h = kda::align_up(W.f.total, 256);
@@ -491,6 +496,107 @@ kda_status kda_chunk_bwd(const void *q, const void *k, const void *v, const floa
                              dev_status, stream);
 }
 
+namespace {
+
+// The checks and the forward's ChunkArgs (with the backward's stores) shared by
+// kda_chunk_fwd_save and kda_chunk_bwd_act.
+kda_status chunk_bwd_setup(const char *op, const void *q, const void *k, const void *v,
+                           const float *g, const void *beta, const float *h0,
+                           const int32_t *cu_seqlens, const kda_shape *shape,
+                           const kda_activation *act, uint32_t flags_ok, void *workspace,
+                           size_t workspace_bytes, int32_t *dev_status, kda::GateAct *ga,
+                           ChunkBwdWs *W, kda::ChunkArgs *a) {
+    kda_status st = check_common(op, shape, cu_seqlens);
+    if (st != KDA_OK) return st;
+    if ((st = resolve_act(op, shape, act, ga)) != KDA_OK) return st;
+    if (shape->dtype != KDA_DTYPE_BF16 || !kda::chunk_bwd_tc_supported(shape->K, shape->V))
+        return fail(KDA_ERR_UNSUPPORTED, "%s: bf16 inputs with K = V = 128 only (got dtype %d, "
+                    "K=%d, V=%d); kda_recurrent_bwd takes the rest", op, (int)shape->dtype,
+                    shape->K, shape->V);
+    if (shape->flags & ~flags_ok)
+        return fail(KDA_ERR_UNSUPPORTED, "%s: flags 0x%x (taken: 0x%x; a cumsummed gate goes "
+                    "through kda_recurrent_bwd)", op, shape->flags, flags_ok);
+    const bool has_rows = (int64_t)shape->B * shape->T > 0;
+    if (has_rows && (!q || !k || !v || !g || !beta))
+        return fail(KDA_ERR_INVALID_ARG, "%s: q, k, v, g and beta must be non-NULL", op);
+    const bool packed = cu_seqlens != nullptr;
+    *W = chunk_bwd_ws_layout(shape, packed);
+    if (W->f.slots > INT_MAX) return fail(KDA_ERR_UNSUPPORTED, "%s: too many chunks", op);
+    const size_t need = kda_chunk_bwd_workspace_size(shape);
+    if (!workspace || workspace_bytes < need)
+        return fail(KDA_ERR_INVALID_ARG, "%s: workspace of %zu bytes needed, %zu given", op, need,
+                    workspace_bytes);
+    if ((uintptr_t)workspace % 256 != 0)
+        return fail(KDA_ERR_INVALID_ARG, "%s: workspace must be 256-byte aligned", op);
+    const void *ptrs[] = {q, k, v, g, h0};
+    for (const void *ptr : ptrs)
+        if ((uintptr_t)ptr % 16 != 0)
+            return fail(KDA_ERR_INVALID_ARG, "%s: tensors must be 16-byte aligned", op);
+
+    char *ws = static_cast<char *>(workspace);
+    a->q = q; a->k = k; a->v = v; a->g = g; a->beta = beta; a->h0 = h0; a->cu = cu_seqlens;
+    a->o = nullptr; a->ht = nullptr; a->status = dev_status;
+    a->B = shape->B; a->T = shape->T; a->H = shape->H; a->HV = shape->HV; a->K = shape->K;
+    a->V = shape->V; a->N = shape->num_seqs;
+    a->scale = resolve_scale(shape);
+    a->g_scale = shape->g_scale;
+    a->l2norm = (shape->flags & KDA_FLAG_QK_L2NORM) ? 1 : 0;
+    a->g_is_cumsum = 0;
+    a->test_timeout = 0;
+    a->act = *ga;
+    a->ctrl = reinterpret_cast<kda::ChunkCtrl *>(ws + W->f.ctrl);
+    a->chunk_start = reinterpret_cast<int32_t *>(ws + W->f.chunk_start);
+    a->units = ws + W->f.units;
+    a->slots = W->f.slots;
+    a->split = 0;
+    a->qc = nullptr; a->e1 = nullptr; a->pm = nullptr; a->e0b = nullptr;
+    a->pipe = (packed || (shape->flags & KDA_FLAG_SERIAL)) ? kda::PipePlan{} : W->f.pipe;
+    a->e0 = a->pipe.parts > 0 ? reinterpret_cast<float *>(ws + W->f.e0) : nullptr;
+    a->prep_c0 = a->prep_c1 = 0;
+    a->scan_c0 = a->scan_c1 = 0;
+    a->bwd = 1;
+    a->ck_h = ws + W->ck_h;
+    a->ck_vp = ws + W->ck_vp;
+    return KDA_OK;
+}
+
+}  // namespace
+
+kda_status kda_chunk_fwd_save(const void *q, const void *k, const void *v, const float *g,
+                              const void *beta, const float *h0, const int32_t *cu_seqlens,
+                              const kda_shape *shape, const kda_activation *act, void *o,
+                              float *ht, void *workspace, size_t workspace_bytes,
+                              int32_t *dev_status, kda_stream_t stream) {
+    const char *op = "kda_chunk_fwd_save";
+    kda::GateAct ga;
+    ChunkBwdWs W;
+    kda::ChunkArgs a;
+    kda_status st = chunk_bwd_setup(op, q, k, v, g, beta, h0, cu_seqlens, shape, act,
+                                    KDA_FLAG_SERIAL | KDA_FLAG_QK_L2NORM, workspace,
+                                    workspace_bytes, dev_status, &ga, &W, &a);
+    if (st != KDA_OK) return st;
+    if ((st = check_fwd_pointers(op, shape, q, k, v, g, beta, o, cu_seqlens)) != KDA_OK) return st;
+    if ((uintptr_t)o % 16 != 0 || (uintptr_t)ht % 16 != 0)
+        return fail(KDA_ERR_INVALID_ARG, "%s: tensors must be 16-byte aligned", op);
+    char *ws = static_cast<char *>(workspace);
+    float *hend = reinterpret_cast<float *>(ws + W.hend);
+    a.o = o;
+    a.ht = hend;  // every sequence's final state, for the backward (and copied to ht)
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaSuccess;
+    if (cu_seqlens) {
+        e = kda::launch_validate_offsets(cu_seqlens, a.N, a.T, dev_status, a.ctrl, a.chunk_start, s);
+        if (e != cudaSuccess) return cuda_fail(e, op);
+    }
+    if ((e = kda::launch_chunk_tc(a, s)) != cudaSuccess) return cuda_fail(e, op);
+    if (ht && (e = cudaMemcpyAsync(ht, hend, (size_t)shape->num_seqs * shape->HV * shape->K *
+                                                 shape->V * sizeof(float),
+                                   cudaMemcpyDeviceToDevice, s)) != cudaSuccess)
+        return cuda_fail(e, op);
+    g_last_error.clear();
+    return KDA_OK;
+}
+
 kda_status kda_chunk_bwd_act(const void *q, const void *k, const void *v, const float *g,
                              const void *beta, const float *h0, const int32_t *cu_seqlens,
                              const kda_shape *shape, const kda_activation *act, const void *dout,
@@ -499,64 +605,25 @@ kda_status kda_chunk_bwd_act(const void *q, const void *k, const void *v, const 
                              void *workspace, size_t workspace_bytes, int32_t *dev_status,
                              kda_stream_t stream) {
     const char *op = "kda_chunk_bwd";
-    kda_status st = check_common(op, shape, cu_seqlens);
-    if (st != KDA_OK) return st;
     kda::GateAct ga;
-    if ((st = resolve_act(op, shape, act, &ga)) != KDA_OK) return st;
+    ChunkBwdWs W;
+    kda::ChunkArgs a;
+    kda_status st = chunk_bwd_setup(op, q, k, v, g, beta, h0, cu_seqlens, shape, act,
+                                    KDA_FLAG_SERIAL | KDA_FLAG_QK_L2NORM | KDA_FLAG_BWD_SAVED,
+                                    workspace, workspace_bytes, dev_status, &ga, &W, &a);
+    if (st != KDA_OK) return st;
     if ((ga.A_log && !dA_log) || (ga.dt_bias && !ddt_bias))
         return fail(KDA_ERR_INVALID_ARG, "%s: dA_log (and ddt_bias with dt_bias) must be non-NULL "
                     "with the gate activation", op);
-    if (shape->dtype != KDA_DTYPE_BF16 || !kda::chunk_bwd_tc_supported(shape->K, shape->V))
-        return fail(KDA_ERR_UNSUPPORTED, "%s: bf16 inputs with K = V = 128 only (got dtype %d, "
-                    "K=%d, V=%d); kda_recurrent_bwd takes the rest", op, (int)shape->dtype,
-                    shape->K, shape->V);
-    if (shape->flags & ~(uint32_t)(KDA_FLAG_SERIAL | KDA_FLAG_QK_L2NORM))
-        return fail(KDA_ERR_UNSUPPORTED, "%s: flags 0x%x (KDA_FLAG_QK_L2NORM and KDA_FLAG_SERIAL "
-                    "are taken; a cumsummed gate goes through kda_recurrent_bwd)", op,
-                    shape->flags);
     const bool has_rows = (int64_t)shape->B * shape->T > 0;
-    if (has_rows && (!q || !k || !v || !g || !beta || !dout || !dq || !dk || !dv || !dg || !dbeta))
-        return fail(KDA_ERR_INVALID_ARG, "%s: inputs, dout and dq, dk, dv, dg, dbeta must be "
-                    "non-NULL", op);
-    const bool packed = cu_seqlens != nullptr;
-    const ChunkBwdWs W = chunk_bwd_ws_layout(shape, packed);
-    if (W.f.slots > INT_MAX) return fail(KDA_ERR_UNSUPPORTED, "%s: too many chunks", op);
-    const size_t need = kda_chunk_bwd_workspace_size(shape);
-    if (!workspace || workspace_bytes < need)
-        return fail(KDA_ERR_INVALID_ARG, "%s: workspace of %zu bytes needed, %zu given", op, need,
-                    workspace_bytes);
-    if ((uintptr_t)workspace % 256 != 0)
-        return fail(KDA_ERR_INVALID_ARG, "%s: workspace must be 256-byte aligned", op);
-    const void *ptrs[] = {q, k, v, g, h0, dout, dht, dq, dk, dv, dg, dh0};
+    if (has_rows && (!dout || !dq || !dk || !dv || !dg || !dbeta))
+        return fail(KDA_ERR_INVALID_ARG, "%s: dout and dq, dk, dv, dg, dbeta must be non-NULL", op);
+    const void *ptrs[] = {dout, dht, dq, dk, dv, dg, dh0};
     for (const void *ptr : ptrs)
         if ((uintptr_t)ptr % 16 != 0)
             return fail(KDA_ERR_INVALID_ARG, "%s: tensors must be 16-byte aligned", op);
-
+    const bool packed = cu_seqlens != nullptr;
     char *ws = static_cast<char *>(workspace);
-    kda::ChunkArgs a;
-    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.h0 = h0; a.cu = cu_seqlens;
-    a.o = nullptr; a.ht = nullptr; a.status = dev_status;
-    a.B = shape->B; a.T = shape->T; a.H = shape->H; a.HV = shape->HV; a.K = shape->K;
-    a.V = shape->V; a.N = shape->num_seqs;
-    a.scale = resolve_scale(shape);
-    a.g_scale = shape->g_scale;
-    a.l2norm = (shape->flags & KDA_FLAG_QK_L2NORM) ? 1 : 0;
-    a.g_is_cumsum = 0;
-    a.test_timeout = 0;
-    a.act = ga;
-    a.ctrl = reinterpret_cast<kda::ChunkCtrl *>(ws + W.f.ctrl);
-    a.chunk_start = reinterpret_cast<int32_t *>(ws + W.f.chunk_start);
-    a.units = ws + W.f.units;
-    a.slots = W.f.slots;
-    a.split = 0;
-    a.qc = nullptr; a.e1 = nullptr; a.pm = nullptr; a.e0b = nullptr;
-    a.pipe = packed ? kda::PipePlan{} : W.f.pipe;
-    a.e0 = a.pipe.parts > 0 ? reinterpret_cast<float *>(ws + W.f.e0) : nullptr;
-    a.prep_c0 = a.prep_c1 = 0;
-    a.scan_c0 = a.scan_c1 = 0;
-    a.bwd = 1;
-    a.ck_h = ws + W.ck_h;
-    a.ck_vp = ws + W.ck_vp;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;
@@ -585,7 +652,8 @@ kda_status kda_chunk_bwd_act(const void *q, const void *k, const void *v, const 
                                  reinterpret_cast<float *>(ws + W.hend),
                                  reinterpret_cast<float *>(ws + W.dgs),
                                  reinterpret_cast<float *>(ws + W.dhm),
-                                 (shape->flags & KDA_FLAG_SERIAL) != 0, s);
+                                 (shape->flags & KDA_FLAG_SERIAL) != 0,
+                                 (shape->flags & KDA_FLAG_BWD_SAVED) == 0, s);
     if (e != cudaSuccess) return cuda_fail(e, op);
     if (a.l2norm || ga.A_log || ga.beta_scale > 0.f) {
         // the kernels formed the gradients of the normalised rows and of the activated

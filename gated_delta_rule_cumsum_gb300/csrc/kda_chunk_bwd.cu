@@ -1231,7 +1231,7 @@ int chunk_bwd_pipe_m(int B, int HV, int V, int T, int sms) {
 cudaError_t launch_chunk_bwd_tc(const ChunkArgs &c, const void *dout, const float *dht, float *dq,
                                 float *dk, float *dv, float *dg, float *dbeta, float *dh0,
                                 void *dhn, void *dvp, float *hend, float *dgs, float *dhm,
-                                bool serial, cudaStream_t st) {
+                                bool serial, bool rerun, cudaStream_t st) {
     if (!chunk_bwd_tc_supported(c.K, c.V)) return cudaErrorInvalidValue;
     BwdArgs a;
     a.c = c;
@@ -1252,8 +1252,9 @@ cudaError_t launch_chunk_bwd_tc(const ChunkArgs &c, const void *dout, const floa
     a.pipe_m = 0;
     a.dhm = dhm;
     a.unit_c0 = a.unit_c1 = 0;
-    cudaError_t e = launch_chunk_tc(a.c, st);  // recompute and re-scan, with checkpoints
-    if (e != cudaSuccess) return e;
+    cudaError_t e = cudaSuccess;
+    if (rerun && (e = launch_chunk_tc(a.c, st)) != cudaSuccess)  // recompute and re-scan
+        return e;
     static DeviceOnce once;
     static int sms[64];
     int dev = 0;

@@ -245,12 +245,13 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st);
 // when value heads share q/k heads (HV > H) or with packed sequences.
 // A dense call of enough chunks pipelines the reverse scan with the gradient kernel
 // (dhm: [N][HV][K][V] fp32, the state gradient where the two scan parts meet) unless
-// `serial`.
+// `serial`.  Without `rerun` the forward's tiles, checkpoints and final states are
+// already in place (kda_chunk_fwd_save) and the forward is not launched.
 bool chunk_bwd_tc_supported(int K, int V);
 int chunk_bwd_pipe_m(int B, int HV, int V, int T, int sms);
 cudaError_t launch_chunk_bwd_tc(const ChunkArgs &c, const void *dout, const float *dht, float *dq,
                                 float *dk, float *dv, float *dg, float *dbeta, float *dh0,
                                 void *dhn, void *dvp, float *hend, float *dgs, float *dhm,
-                                bool serial, cudaStream_t st);
+                                bool serial, bool rerun, cudaStream_t st);
 
 }  // namespace kda

@@ -22,7 +22,10 @@
  *   kda_recurrent_bwd  the gradients of the recurrence (ALGORITHM.md, Backward),
  *                      also as kda_recurrent_bwd_act (gradients of the raw inputs)
  *   kda_chunk_bwd      the same gradients in the chunked form on the tensor cores
- *                      (ALGORITHM.md, Backward, the seven launches)
+ *                      (ALGORITHM.md, Backward, the seven launches), also as
+ *                      kda_chunk_bwd_act, and after kda_chunk_fwd_save (a forward
+ *                      that keeps the backward's recomputed state) without the
+ *                      recompute
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -117,6 +120,15 @@ typedef enum {
                                            and joined back to the caller's stream
                                            with events, so graph capture sees one
                                            fork and one join) on the other SMs.    */
+
+#define KDA_FLAG_BWD_SAVED   (1u << 4)  /* kda_chunk_bwd: the workspace holds what
+                                           kda_chunk_fwd_save stored for the same
+                                           inputs, shape and options, so the
+                                           forward is not run again (the saved
+                                           per-chunk tiles and states are read as
+                                           they are; h0 is not read).  Refused by
+                                           kda_chunk_fwd_save, ignored by the
+                                           other entry points.                     */
 
 #define KDA_FLAG_TEST_WAIT_TIMEOUT (1u << 31)
                                         /* Test hook, kda_chunk_fwd on the bf16
@@ -373,8 +385,10 @@ size_t kda_recurrent_bwd_workspace_size(const kda_shape *shape);
  *                      gradients (and KDA_DEVICE_GATE_RANGE).
  *   workspace          kda_chunk_bwd_workspace_size() bytes, 256-byte aligned.
  *   flags              KDA_FLAG_QK_L2NORM (q, k normalised inside the op; dq, dk
- *                      are the raw rows' gradients) and KDA_FLAG_SERIAL; a cumsummed
- *                      gate takes kda_recurrent_bwd.
+ *                      are the raw rows' gradients), KDA_FLAG_SERIAL and
+ *                      KDA_FLAG_BWD_SAVED (the workspace holds kda_chunk_fwd_save's
+ *                      stores for these inputs: the recompute and re-scan are
+ *                      skipped); a cumsummed gate takes kda_recurrent_bwd.
  * Supported: bf16, K = V = 128.  A chunk whose gate range is too wide raises
  * KDA_DEVICE_GATE_RANGE in *dev_status.  Tensors 16-byte aligned.
  */
@@ -399,6 +413,28 @@ kda_status kda_chunk_bwd_act(const void *q, const void *k, const void *v, const 
                              float *dbeta, float *dh0, float *dA_log, float *ddt_bias,
                              void *workspace, size_t workspace_bytes, int32_t *dev_status,
                              kda_stream_t stream);
+/*
+ * kda_chunk_fwd_save -- the chunked forward of kda_chunk_fwd_act (act may be NULL:
+ * kda_chunk_fwd), the same o and ht bit for bit, that also leaves in `workspace`
+ * what kda_chunk_bwd re-derives in its first two stages (recompute and re-scan of
+ * kernel-fun 0.2.0.dev1 sdist, ALGORITHM.md, "Backward"): per (chunk, value head)
+ * the operand tiles, w, Akk, the state at the chunk's start and v', and every
+ * sequence's final state.  A later kda_chunk_bwd (or _act) of the same inputs,
+ * shape, options and workspace with KDA_FLAG_BWD_SAVED then starts at the reverse
+ * scan: memory (kda_chunk_bwd_workspace_size bytes held from the forward to the
+ * backward) for the forward's second run.
+ *   arguments          as for kda_chunk_fwd_act; ht may be NULL.
+ *   workspace          kda_chunk_bwd_workspace_size() bytes, 256-byte aligned,
+ *                      owned by the caller and left untouched until the backward.
+ *   flags              KDA_FLAG_QK_L2NORM and KDA_FLAG_SERIAL.
+ * Supported: bf16, K = V = 128 (as kda_chunk_bwd).
+ */
+kda_status kda_chunk_fwd_save(const void *q, const void *k, const void *v, const float *g,
+                              const void *beta, const float *h0, const int32_t *cu_seqlens,
+                              const kda_shape *shape, const kda_activation *act, void *o,
+                              float *ht, void *workspace, size_t workspace_bytes,
+                              int32_t *dev_status, kda_stream_t stream);
+
 /* Bytes of workspace kda_chunk_bwd needs for *shape (0 on invalid shapes).  As for
  * kda_chunk_workspace_size, a shape that may be packed (B == 1) is sized for packed
  * input, which covers a dense call of the same shape too. */

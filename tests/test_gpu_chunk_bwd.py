@@ -301,3 +301,99 @@ def test_autograd_with_options_takes_the_chunked_backward(kda_lib):
     print(errs)
     bad = {n: e for n, e in errs.items() if not e <= (1e-5 if n.endswith("_sum") else TOL)}
     assert not bad, errs
+
+
+def _save_fwd(kda, inp, **kw):
+    return kda.chunk_kda_forward_save(inp["q"], inp["k"], inp["v"], kw.pop("g", inp["g"]),
+                                      kw.pop("beta", inp["beta"]), initial_state=inp["h0"],
+                                      output_final_state=True, cu_seqlens=inp["cu_seqlens"], **kw)
+
+
+@pytest.mark.parametrize("packed", [False, True])
+def test_forward_save_matches_the_forward_bitwise(kda_lib, packed):
+    """kda_chunk_fwd_save returns kda_chunk_fwd's o and ht bit for bit (the backward's
+    stores change no arithmetic), dense (pipelined) and packed."""
+    if packed:
+        inp = _packed(1451, [70, 0, 1300, 9], HV=4, H=2, K=128, V=128)
+    else:
+        inp = _small(1451, B=1, T=4100, H=4, HV=4, K=128, V=128)
+    o, ht = kda_lib.chunk_kda(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                              initial_state=inp["h0"], output_final_state=True,
+                              cu_seqlens=inp["cu_seqlens"])
+    o2, ht2, _ = _save_fwd(kda_lib, inp)
+    end = o.shape[1] if inp["cu_seqlens"] is None else int(inp["cu_seqlens"][-1])
+    assert torch.equal(o[:, :end], o2[:, :end]) and torch.equal(ht, ht2)
+
+
+@pytest.mark.parametrize("case", ["dense", "packed", "options"])
+def test_saved_backward_matches_the_recomputing_one_bitwise(kda_lib, case):
+    """chunk_kda_backward from chunk_kda_forward_save's workspace (KDA_FLAG_BWD_SAVED,
+    no recompute) gives the recomputing call's gradients bit for bit (HV == H: no
+    atomics), and the oracle's; dA_log and dt_bias's gradient are sums over tokens by
+    fp32 atomics, equal to rounding."""
+    kw = {}
+    if case == "packed":
+        inp = _packed(1461, [70, 0, 1300, 9], HV=2, H=2, K=128, V=128)
+    else:
+        inp = _small(1461, B=2, T=2100, H=4, HV=4, K=128, V=128, g_hi=0.3)
+    dout, dht = _grads_in(inp, 1462)
+    if case == "options":
+        g_raw, b_raw, A_log, dt_bias = _raw_gate(inp, 1463)
+        kw = dict(g=g_raw, beta=b_raw, g_scale=RCP_LN2, use_qk_l2norm_in_kernel=True,
+                  A_log=A_log, dt_bias=dt_bias, beta_sigmoid_scale=1.0)
+    g = kw.get("g", inp["g"])
+    beta = kw.get("beta", inp["beta"])
+    bkw = {n: kw[n] for n in kw if n not in ("g", "beta")}
+    ref = kda_lib.chunk_kda_backward(inp["q"], inp["k"], inp["v"], g, beta, dout, inp["h0"], dht,
+                                     cu_seqlens=inp["cu_seqlens"], **bkw)
+    _, _, saved = _save_fwd(kda_lib, inp, **dict(kw))
+    st = kda_lib.new_status()
+    got = kda_lib.chunk_kda_backward(inp["q"], inp["k"], inp["v"], g, beta, dout, None, dht,
+                                     cu_seqlens=inp["cu_seqlens"], saved=saved, dev_status=st,
+                                     want_dh0=True, **bkw)
+    assert kda_lib.kda_read_device_status(st) == (0, 0)
+    for name, t in ref.items():
+        if t is None:
+            continue
+        if name in ("dA_log", "ddt_bias"):
+            assert parity.rel_err(got[name], t) <= 1e-5, name
+        else:
+            assert torch.equal(t, got[name]), name
+    if case != "options":
+        end = None if inp["cu_seqlens"] is None else int(inp["cu_seqlens"][-1])
+        _check(got, _oracle(inp, dout, dht), rows=end)
+
+
+def test_saved_backward_with_a_serial_call_reads_the_same_layout(kda_lib):
+    """A pipelined kda_chunk_fwd_save then kda_chunk_bwd with KDA_FLAG_SERIAL |
+    KDA_FLAG_BWD_SAVED through the C ABI: the workspace layout does not depend on
+    KDA_FLAG_SERIAL, so the serial backward reads the pipelined forward's tiles."""
+    inp = _small(1471, B=1, T=4100, H=4, HV=4, K=128, V=128, g_hi=0.3)
+    dout, dht = _grads_in(inp, 1472)
+    _, _, saved = _save_fwd(kda_lib, inp)
+    q, k, v, g, beta = (inp[n] for n in ("q", "k", "v", "g", "beta"))
+    shape = kda_lib.make_shape(q, v, None, flags=kda_lib.KDA_FLAG_SERIAL | kda_lib.KDA_FLAG_BWD_SAVED)
+    f32 = dict(dtype=torch.float32, device="cuda")
+    gr = dict(dq=torch.empty(q.shape, **f32), dk=torch.empty(k.shape, **f32),
+              dv=torch.empty(v.shape, **f32), dg=torch.empty(g.shape, **f32),
+              dbeta=torch.empty(beta.shape, **f32), dh0=torch.empty(inp["h0"].shape, **f32))
+    st = kda_lib.new_status()
+    kda_lib.kda_chunk_bwd(q, k, v, g, beta, None, None, shape, dout, dht, gr["dq"], gr["dk"],
+                          gr["dv"], gr["dg"], gr["dbeta"], gr["dh0"], saved, st)
+    assert kda_lib.kda_read_device_status(st) == (0, 0)
+    _check(gr, _oracle(inp, dout, dht))
+
+
+def test_autograd_recomputing_backward(kda_lib):
+    """kda_autograd(save_for_backward=False): the backward runs the forward again."""
+    inp = _small(1481, B=1, T=150, H=1, HV=1, K=128, V=128, g_hi=0.3)
+    dout, dht = _grads_in(inp, 1482)
+    leaves = {n: inp[n].clone().requires_grad_(True) for n in ("q", "k", "v", "g", "beta", "h0")}
+    o, ht = kda_lib.kda_autograd(leaves["q"], leaves["k"], leaves["v"], leaves["g"],
+                                 leaves["beta"], leaves["h0"], save_for_backward=False)
+    ((o.float() * dout.float()).sum() + (ht * dht).sum()).backward()
+    ref = _oracle(inp, dout, dht)
+    for name, key in (("q", "dq"), ("k", "dk"), ("v", "dv"), ("g", "dg"), ("beta", "dbeta"),
+                      ("h0", "dh0")):
+        err = parity.rel_err(leaves[name].grad, ref[key])
+        assert err <= TOL, (name, err)
