@@ -10,7 +10,9 @@ namespace kda {
 namespace {
 
 constexpr int kUB = 16;               // column block of u in the workspace
-constexpr float kSafeRange = 60.f;    // max |g2| (log2) for the split grams
+constexpr float kSafeRange = 100.f;   // max |g2| (log2) for the split grams: factors
+                                      // 2^-100..2^100 stay normal bf16, and the masked
+                                      // upper triangle's sums stay finite in fp32
 constexpr uint64_t kWaitNs = 1000000000ull;
 
 // Byte layout of one workspace unit (chunk c, value head).

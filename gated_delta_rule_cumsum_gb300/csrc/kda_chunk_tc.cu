@@ -11,8 +11,8 @@
 //                 2^(g2_i - g2_j) split through the chunk start, one tcgen05 MMA
 //                 (M = 128: [Qg; Kg] stacked, N = 64, K = dk).  This split keeps
 //                 every factor at most 2^R with R = max |g2| over the chunk; when R
-//                 exceeds kSafeRange the grams are formed exactly in fp32 SIMT with
-//                 one exp2 per (i, j, d), exponent g2_i - g2_j <= 0 (ALGORITHM.md,
+//                 exceeds kSafeRange (100) the grams are formed exactly in fp32 SIMT
+//                 with one exp2 per (i, j, d), exponent g2_i - g2_j <= 0 (ALGORITHM.md,
 //                 "The numerics law").
 //                 Akk = (I + L)^-1: blocked unit-lower-triangular inverse in fp32
 //                 (16 x 16 diagonal blocks by substitution, then two doubling
@@ -625,31 +625,63 @@ __global__ void __launch_bounds__(256, 2)
     }
     const bool fast = __int_as_float(sRangeBits) <= kSafeRange;
 
-    // ---- exact grams for chunks whose gate range is too wide to split
+    // ---- exact grams for chunks whose gate range is too wide to split: per channel
+    // 2^(g2_i - g2_j) itself.  Warp w takes rows i = w, w + 8, ...; a lane keeps its
+    // dk / 32 channels of row i (q, k, g2) in registers and forms four columns j at a
+    // time; the eight sums (Aqk and the k gram of the four columns) are reduced over
+    // the warp by halving exchanges (nine shuffles), lane 4 o ending with sum o.
     if (__builtin_expect(!fast, 0)) {
-        for (int i = warp; i < 64; i += 8) {
-            for (int j = 0; j <= i; ++j) {
-                float aq = 0.f, ak = 0.f;
-                for (int dd = lane; dd < KK; dd += 32) {
-                    const float e = exp2f(sG2[gsw(i, dd)] - sG2[gsw(j, dd)]);
-                    const float qi = __bfloat162float(
-                        *reinterpret_cast<const __nv_bfloat16 *>(sAG + qk_off(i, dd)));
-                    const float ki = __bfloat162float(
-                        *reinterpret_cast<const __nv_bfloat16 *>(sAG + qk_off(64 + i, dd)));
-                    const float kj = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
-                        sAG + qk_off(64 + j, dd))) * e;
-                    aq = fmaf(qi, kj, aq);
-                    ak = fmaf(ki, kj, ak);
-                }
+        constexpr int CH = KK / 32;
+        const auto bf = [&](int r, int c) {
+            return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(sAG + qk_off(r, c)));
+        };
 #pragma unroll 1
-                for (int off = 16; off > 0; off >>= 1) {
-                    aq += __shfl_xor_sync(0xffffffffu, aq, off);
-                    ak += __shfl_xor_sync(0xffffffffu, ak, off);
+        for (int i = warp; i < 64; i += 8) {
+            float qi[CH], ki[CH], gi[CH];
+#pragma unroll
+            for (int m = 0; m < CH; ++m) {
+                qi[m] = bf(i, lane + 32 * m);
+                ki[m] = bf(64 + i, lane + 32 * m);
+                gi[m] = sG2[gsw(i, lane + 32 * m)];
+            }
+            const float bi = sBeta[i];
+#pragma unroll 1
+            for (int j0 = 0; j0 <= i; j0 += 4) {  // j0 + 3 <= 63
+                float v[8];
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    float aq = 0.f, ak = 0.f;
+#pragma unroll
+                    for (int m = 0; m < CH; ++m) {
+                        const int dd = lane + 32 * m;
+                        // columns past i may overflow here; their sums are never stored
+                        const float kj = bf(64 + j0 + jj, dd) * ex2_ftz(gi[m] - sG2[gsw(j0 + jj, dd)]);
+                        aq = fmaf(qi[m], kj, aq);
+                        ak = fmaf(ki[m], kj, ak);
+                    }
+                    v[jj] = aq;
+                    v[4 + jj] = ak;
                 }
-                if (lane == 0) {
-                    *reinterpret_cast<__nv_bfloat16 *>(U + Lo.aqk + tile_off(i, j, 64)) =
-                        __float2bfloat16_rn(aq);
-                    sL[akk_idx<kSplitA>(i, j)] = (i > j) ? sBeta[i] * ak : 0.f;
+                const bool b4 = (lane >> 4) & 1, b3 = (lane >> 3) & 1, b2 = (lane >> 2) & 1;
+                float w[4], x[2];
+#pragma unroll
+                for (int t = 0; t < 4; ++t)
+                    w[t] = (b4 ? v[4 + t] : v[t]) +
+                           __shfl_xor_sync(0xffffffffu, b4 ? v[t] : v[4 + t], 16);
+#pragma unroll
+                for (int t = 0; t < 2; ++t)
+                    x[t] = (b3 ? w[2 + t] : w[t]) +
+                           __shfl_xor_sync(0xffffffffu, b3 ? w[t] : w[2 + t], 8);
+                float y = (b2 ? x[1] : x[0]) + __shfl_xor_sync(0xffffffffu, b2 ? x[0] : x[1], 4);
+                y += __shfl_xor_sync(0xffffffffu, y, 2);
+                y += __shfl_xor_sync(0xffffffffu, y, 1);
+                if ((lane & 3) == 0) {
+                    const int j = j0 + 2 * b3 + b2;  // sum 4 b4 + 2 b3 + b2
+                    if (!b4)
+                        *reinterpret_cast<__nv_bfloat16 *>(U + Lo.aqk + tile_off(i, j, 64)) =
+                            __float2bfloat16_rn(j <= i ? y : 0.f);
+                    else
+                        sL[akk_idx<kSplitA>(i, j)] = j < i ? bi * y : 0.f;
                 }
             }
             for (int j = i + 1 + lane; j < 64; j += 32) {

@@ -172,6 +172,18 @@ def test_extreme_decay(kda_lib):
     _check(inp, o, ht, 1e-4)
 
 
+@pytest.mark.parametrize("lo,hi", [(0.8, 1.6), (1.5, 3.0)])
+def test_wide_gate_range_chunks(kda_lib, lo, hi):
+    """Per-token gates of -U(lo, hi) (log2): chunk gate ranges of about 77 and 144, past
+    the split grams' limit, so every chunk's grams are formed exactly; several chunks,
+    a ragged tail, two value heads per q/k head."""
+    inp = _small(31, B=1, T=300, H=1, HV=2, K=128, V=128, dtype=torch.bfloat16)
+    gen = torch.Generator().manual_seed(32)
+    inp["g"] = -(lo + (hi - lo) * torch.rand(inp["g"].shape, generator=gen)).cuda()
+    o, ht = _run(kda_lib, inp)
+    _check(inp, o, ht, 2e-2)
+
+
 def test_mixed_extreme_and_mild_channels(kda_lib):
     inp = _small(8, T=128, K=128, V=64, dtype=torch.bfloat16)
     inp["g"][..., ::3] = -20.0
