@@ -625,16 +625,75 @@ __global__ void __launch_bounds__(256, 2)
     }
     const bool fast = __int_as_float(sRangeBits) <= kSafeRange;
 
-    // ---- exact grams for chunks whose gate range is too wide to split: per channel
-    // 2^(g2_i - g2_j) itself.  Warp w takes rows i = w, w + 8, ...; a lane keeps its
-    // dk / 32 channels of row i (q, k, g2) in registers and forms four columns j at a
-    // time; the eight sums (Aqk and the k gram of the four columns) are reduced over
-    // the warp by halving exchanges (nine shuffles), lane 4 o ending with sum o.
+    // ---- exact grams for chunks whose gate range is too wide to split.  A column j
+    // of a 16-row block before row i's (j < e = 16 floor(i / 16) <= i) takes the gate
+    // through the block boundary, 2^(g2_i - g2_e) 2^(g2_e - g2_j), both exponents <= 0
+    // (ALGORITHM.md, "The numerics law": a boundary between the blocks separates the
+    // pair); the diagonal blocks take 2^(g2_i - g2_j) itself.  Lanes run over channels
+    // (dk / 32 each); a warp forms four columns at a time for one row, and the eight
+    // sums (Aqk and the k gram of the four columns) are reduced over the warp by
+    // halving exchanges (nine shuffles), lane 4 o ending with sum o.
     if (__builtin_expect(!fast, 0)) {
         constexpr int CH = KK / 32;
         const auto bf = [&](int r, int c) {
             return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(sAG + qk_off(r, c)));
         };
+        // the reduction and the store of row i, columns j0 .. j0 + 3
+        const auto emit = [&](int i, int j0, const float (&v)[8]) {
+            const bool b4 = (lane >> 4) & 1, b3 = (lane >> 3) & 1, b2 = (lane >> 2) & 1;
+            float w[4], x[2];
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+                w[t] = (b4 ? v[4 + t] : v[t]) + __shfl_xor_sync(0xffffffffu, b4 ? v[t] : v[4 + t], 16);
+#pragma unroll
+            for (int t = 0; t < 2; ++t)
+                x[t] = (b3 ? w[2 + t] : w[t]) + __shfl_xor_sync(0xffffffffu, b3 ? w[t] : w[2 + t], 8);
+            float y = (b2 ? x[1] : x[0]) + __shfl_xor_sync(0xffffffffu, b2 ? x[0] : x[1], 4);
+            y += __shfl_xor_sync(0xffffffffu, y, 2);
+            y += __shfl_xor_sync(0xffffffffu, y, 1);
+            if ((lane & 3) == 0) {
+                const int j = j0 + 2 * b3 + b2;  // sum 4 b4 + 2 b3 + b2
+                if (!b4)
+                    *reinterpret_cast<__nv_bfloat16 *>(U + Lo.aqk + tile_off(i, j, 64)) =
+                        __float2bfloat16_rn(j <= i ? y : 0.f);
+                else
+                    sL[akk_idx<kSplitA>(i, j)] = j < i ? sBeta[i] * y : 0.f;
+            }
+        };
+        // off-diagonal blocks: item (block row I, four columns j0 < 16 I), 24 items;
+        // the columns' factors once per item, each of the block's 16 rows after it
+#pragma unroll 1
+        for (int it = warp; it < 24; it += 8) {
+            const int I = it < 4 ? 1 : (it < 12 ? 2 : 3);
+            const int e = 16 * I, j0 = 4 * (it - (I == 1 ? 0 : (I == 2 ? 4 : 12)));
+            float ge[CH], kb[4][CH];
+#pragma unroll
+            for (int m = 0; m < CH; ++m) {
+                const int dd = lane + 32 * m;
+                ge[m] = sG2[gsw(e, dd)];
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj)
+                    kb[jj][m] = bf(64 + j0 + jj, dd) * ex2_ftz(ge[m] - sG2[gsw(j0 + jj, dd)]);
+            }
+#pragma unroll 1
+            for (int i = e; i < e + 16; ++i) {
+                float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int m = 0; m < CH; ++m) {
+                    const int dd = lane + 32 * m;
+                    const float a = ex2_ftz(sG2[gsw(i, dd)] - ge[m]);
+                    const float qa = bf(i, dd) * a, ka = bf(64 + i, dd) * a;
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) {
+                        v[jj] = fmaf(qa, kb[jj][m], v[jj]);
+                        v[4 + jj] = fmaf(ka, kb[jj][m], v[4 + jj]);
+                    }
+                }
+                emit(i, j0, v);
+            }
+        }
+        // diagonal blocks: warp w takes rows i = w, w + 8, ..., the row's channels in
+        // registers, columns 16 floor(i / 16) .. i; zeros above the diagonal
 #pragma unroll 1
         for (int i = warp; i < 64; i += 8) {
             float qi[CH], ki[CH], gi[CH];
@@ -644,9 +703,8 @@ __global__ void __launch_bounds__(256, 2)
                 ki[m] = bf(64 + i, lane + 32 * m);
                 gi[m] = sG2[gsw(i, lane + 32 * m)];
             }
-            const float bi = sBeta[i];
 #pragma unroll 1
-            for (int j0 = 0; j0 <= i; j0 += 4) {  // j0 + 3 <= 63
+            for (int j0 = i & ~15; j0 <= i; j0 += 4) {  // j0 + 3 <= 63
                 float v[8];
 #pragma unroll
                 for (int jj = 0; jj < 4; ++jj) {
@@ -662,27 +720,7 @@ __global__ void __launch_bounds__(256, 2)
                     v[jj] = aq;
                     v[4 + jj] = ak;
                 }
-                const bool b4 = (lane >> 4) & 1, b3 = (lane >> 3) & 1, b2 = (lane >> 2) & 1;
-                float w[4], x[2];
-#pragma unroll
-                for (int t = 0; t < 4; ++t)
-                    w[t] = (b4 ? v[4 + t] : v[t]) +
-                           __shfl_xor_sync(0xffffffffu, b4 ? v[t] : v[4 + t], 16);
-#pragma unroll
-                for (int t = 0; t < 2; ++t)
-                    x[t] = (b3 ? w[2 + t] : w[t]) +
-                           __shfl_xor_sync(0xffffffffu, b3 ? w[t] : w[2 + t], 8);
-                float y = (b2 ? x[1] : x[0]) + __shfl_xor_sync(0xffffffffu, b2 ? x[0] : x[1], 4);
-                y += __shfl_xor_sync(0xffffffffu, y, 2);
-                y += __shfl_xor_sync(0xffffffffu, y, 1);
-                if ((lane & 3) == 0) {
-                    const int j = j0 + 2 * b3 + b2;  // sum 4 b4 + 2 b3 + b2
-                    if (!b4)
-                        *reinterpret_cast<__nv_bfloat16 *>(U + Lo.aqk + tile_off(i, j, 64)) =
-                            __float2bfloat16_rn(j <= i ? y : 0.f);
-                    else
-                        sL[akk_idx<kSplitA>(i, j)] = j < i ? bi * y : 0.f;
-                }
+                emit(i, j0, v);
             }
             for (int j = i + 1 + lane; j < 64; j += 32) {
                 *reinterpret_cast<__nv_bfloat16 *>(U + Lo.aqk + tile_off(i, j, 64)) =
