@@ -629,14 +629,18 @@ __global__ void __launch_bounds__(256, 2)
     // of a 16-row block before row i's (j < e = 16 floor(i / 16) <= i) takes the gate
     // through the block boundary, 2^(g2_i - g2_e) 2^(g2_e - g2_j), both exponents <= 0
     // (ALGORITHM.md, "The numerics law": a boundary between the blocks separates the
-    // pair); the diagonal blocks take 2^(g2_i - g2_j) itself.  Lanes run over channels
-    // (dk / 32 each); a warp forms four columns at a time for one row, and the eight
-    // sums (Aqk and the k gram of the four columns) are reduced over the warp by
-    // halving exchanges (nine shuffles), lane 4 o ending with sum o.
+    // pair); the diagonal blocks take 2^(g2_i - g2_j) itself.  Lanes run over channel
+    // pairs (dk / 32 channels each); a warp forms four columns at a time for one row,
+    // and the eight sums (Aqk and the k gram of the four columns) are reduced over the
+    // warp by halving exchanges (nine shuffles), lane 4 o ending with sum o.
     if (__builtin_expect(!fast, 0)) {
-        constexpr int CH = KK / 32;
-        const auto bf = [&](int r, int c) {
-            return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(sAG + qk_off(r, c)));
+        // lane l holds the channel pairs (2 l + 64 m, 2 l + 64 m + 1), m < dk / 64
+        constexpr int CP = KK / 64;
+        const auto bf2 = [&](int r, int c) {
+            return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(sAG + qk_off(r, c)));
+        };
+        const auto g2p = [&](int r, int c) {
+            return *reinterpret_cast<const float2 *>(sG2 + gsw(r, c));
         };
         // the reduction and the store of row i, columns j0 .. j0 + 3
         const auto emit = [&](int i, int j0, const float (&v)[8]) {
@@ -666,27 +670,30 @@ __global__ void __launch_bounds__(256, 2)
         for (int it = warp; it < 24; it += 8) {
             const int I = it < 4 ? 1 : (it < 12 ? 2 : 3);
             const int e = 16 * I, j0 = 4 * (it - (I == 1 ? 0 : (I == 2 ? 4 : 12)));
-            float ge[CH], kb[4][CH];
+            float2 ge[CP], kb[4][CP];
 #pragma unroll
-            for (int m = 0; m < CH; ++m) {
-                const int dd = lane + 32 * m;
-                ge[m] = sG2[gsw(e, dd)];
+            for (int m = 0; m < CP; ++m) {
+                const int c = 2 * lane + 64 * m;
+                ge[m] = g2p(e, c);
 #pragma unroll
-                for (int jj = 0; jj < 4; ++jj)
-                    kb[jj][m] = bf(64 + j0 + jj, dd) * ex2_ftz(ge[m] - sG2[gsw(j0 + jj, dd)]);
+                for (int jj = 0; jj < 4; ++jj) {
+                    const float2 k2 = bf2(64 + j0 + jj, c), g2 = g2p(j0 + jj, c);
+                    kb[jj][m] = make_float2(k2.x * ex2_ftz(ge[m].x - g2.x), k2.y * ex2_ftz(ge[m].y - g2.y));
+                }
             }
 #pragma unroll 1
             for (int i = e; i < e + 16; ++i) {
                 float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int m = 0; m < CH; ++m) {
-                    const int dd = lane + 32 * m;
-                    const float a = ex2_ftz(sG2[gsw(i, dd)] - ge[m]);
-                    const float qa = bf(i, dd) * a, ka = bf(64 + i, dd) * a;
+                for (int m = 0; m < CP; ++m) {
+                    const int c = 2 * lane + 64 * m;
+                    const float2 gi = g2p(i, c), q2 = bf2(i, c), k2 = bf2(64 + i, c);
+                    const float ax = ex2_ftz(gi.x - ge[m].x), ay = ex2_ftz(gi.y - ge[m].y);
+                    const float qx = q2.x * ax, qy = q2.y * ay, kx = k2.x * ax, ky = k2.y * ay;
 #pragma unroll
                     for (int jj = 0; jj < 4; ++jj) {
-                        v[jj] = fmaf(qa, kb[jj][m], v[jj]);
-                        v[4 + jj] = fmaf(ka, kb[jj][m], v[4 + jj]);
+                        v[jj] = fmaf(qy, kb[jj][m].y, fmaf(qx, kb[jj][m].x, v[jj]));
+                        v[4 + jj] = fmaf(ky, kb[jj][m].y, fmaf(kx, kb[jj][m].x, v[4 + jj]));
                     }
                 }
                 emit(i, j0, v);
@@ -696,12 +703,13 @@ __global__ void __launch_bounds__(256, 2)
         // registers, columns 16 floor(i / 16) .. i; zeros above the diagonal
 #pragma unroll 1
         for (int i = warp; i < 64; i += 8) {
-            float qi[CH], ki[CH], gi[CH];
+            float2 qi[CP], ki[CP], gi[CP];
 #pragma unroll
-            for (int m = 0; m < CH; ++m) {
-                qi[m] = bf(i, lane + 32 * m);
-                ki[m] = bf(64 + i, lane + 32 * m);
-                gi[m] = sG2[gsw(i, lane + 32 * m)];
+            for (int m = 0; m < CP; ++m) {
+                const int c = 2 * lane + 64 * m;
+                qi[m] = bf2(i, c);
+                ki[m] = bf2(64 + i, c);
+                gi[m] = g2p(i, c);
             }
 #pragma unroll 1
             for (int j0 = i & ~15; j0 <= i; j0 += 4) {  // j0 + 3 <= 63
@@ -710,12 +718,14 @@ __global__ void __launch_bounds__(256, 2)
                 for (int jj = 0; jj < 4; ++jj) {
                     float aq = 0.f, ak = 0.f;
 #pragma unroll
-                    for (int m = 0; m < CH; ++m) {
-                        const int dd = lane + 32 * m;
+                    for (int m = 0; m < CP; ++m) {
+                        const int c = 2 * lane + 64 * m;
                         // columns past i may overflow here; their sums are never stored
-                        const float kj = bf(64 + j0 + jj, dd) * ex2_ftz(gi[m] - sG2[gsw(j0 + jj, dd)]);
-                        aq = fmaf(qi[m], kj, aq);
-                        ak = fmaf(ki[m], kj, ak);
+                        const float2 k2 = bf2(64 + j0 + jj, c), g2 = g2p(j0 + jj, c);
+                        const float kx = k2.x * ex2_ftz(gi[m].x - g2.x);
+                        const float ky = k2.y * ex2_ftz(gi[m].y - g2.y);
+                        aq = fmaf(qi[m].y, ky, fmaf(qi[m].x, kx, aq));
+                        ak = fmaf(ki[m].y, ky, fmaf(ki[m].x, kx, ak));
                     }
                     v[jj] = aq;
                     v[4 + jj] = ak;
