@@ -244,6 +244,119 @@ __device__ __forceinline__ void strip_at(float4 &s, const float *A, int pr, int 
     }
 }
 
+// The exact gated grams of a chunk whose gate range is too wide to split (the comment
+// above its call site), out of line: cold code kept away from the prep's hot path.
+// aqk: the unit's Aqk tile; sL: L (fp32, akk_idx layout); warp, lane: the caller's.
+template <int KK, bool kSplitA>
+__device__ __noinline__ void exact_grams(const unsigned char *sAG, const float *sG2,
+                                         const float *sBeta, float *sL, unsigned char *aqk,
+                                         const int warp, const int lane) {
+    // lane l holds the channel pairs (2 l + 64 m, 2 l + 64 m + 1), m < dk / 64
+    constexpr int CP = KK / 64;
+    const auto bf2 = [&](int r, int c) {
+        return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(sAG + qk_off(r, c)));
+    };
+    const auto g2p = [&](int r, int c) {
+        return *reinterpret_cast<const float2 *>(sG2 + gsw(r, c));
+    };
+    // the reduction and the store of row i, columns j0 .. j0 + 3
+    const auto emit = [&](int i, int j0, const float (&v)[8]) {
+        const bool b4 = (lane >> 4) & 1, b3 = (lane >> 3) & 1, b2 = (lane >> 2) & 1;
+        float w[4], x[2];
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+            w[t] = (b4 ? v[4 + t] : v[t]) + __shfl_xor_sync(0xffffffffu, b4 ? v[t] : v[4 + t], 16);
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+            x[t] = (b3 ? w[2 + t] : w[t]) + __shfl_xor_sync(0xffffffffu, b3 ? w[t] : w[2 + t], 8);
+        float y = (b2 ? x[1] : x[0]) + __shfl_xor_sync(0xffffffffu, b2 ? x[0] : x[1], 4);
+        y += __shfl_xor_sync(0xffffffffu, y, 2);
+        y += __shfl_xor_sync(0xffffffffu, y, 1);
+        if ((lane & 3) == 0) {
+            const int j = j0 + 2 * b3 + b2;  // sum 4 b4 + 2 b3 + b2
+            if (!b4)
+                *reinterpret_cast<__nv_bfloat16 *>(aqk + tile_off(i, j, 64)) =
+                    __float2bfloat16_rn(j <= i ? y : 0.f);
+            else
+                sL[akk_idx<kSplitA>(i, j)] = j < i ? sBeta[i] * y : 0.f;
+        }
+    };
+    // off-diagonal blocks: item (block row I, four columns j0 < 16 I), 24 items;
+    // the columns' factors once per item, each of the block's 16 rows after it
+#pragma unroll 1
+    for (int it = warp; it < 24; it += 8) {
+        const int I = it < 4 ? 1 : (it < 12 ? 2 : 3);
+        const int e = 16 * I, j0 = 4 * (it - (I == 1 ? 0 : (I == 2 ? 4 : 12)));
+        float2 ge[CP], kb[4][CP];
+#pragma unroll
+        for (int m = 0; m < CP; ++m) {
+            const int c = 2 * lane + 64 * m;
+            ge[m] = g2p(e, c);
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                const float2 k2 = bf2(64 + j0 + jj, c), g2 = g2p(j0 + jj, c);
+                kb[jj][m] = make_float2(k2.x * ex2_ftz(ge[m].x - g2.x), k2.y * ex2_ftz(ge[m].y - g2.y));
+            }
+        }
+#pragma unroll 1
+        for (int i = e; i < e + 16; ++i) {
+            float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int m = 0; m < CP; ++m) {
+                const int c = 2 * lane + 64 * m;
+                const float2 gi = g2p(i, c), q2 = bf2(i, c), k2 = bf2(64 + i, c);
+                const float ax = ex2_ftz(gi.x - ge[m].x), ay = ex2_ftz(gi.y - ge[m].y);
+                const float qx = q2.x * ax, qy = q2.y * ay, kx = k2.x * ax, ky = k2.y * ay;
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    v[jj] = fmaf(qy, kb[jj][m].y, fmaf(qx, kb[jj][m].x, v[jj]));
+                    v[4 + jj] = fmaf(ky, kb[jj][m].y, fmaf(kx, kb[jj][m].x, v[4 + jj]));
+                }
+            }
+            emit(i, j0, v);
+        }
+    }
+    // diagonal blocks: warp w takes rows i = w, w + 8, ..., the row's channels in
+    // registers, columns 16 floor(i / 16) .. i; zeros above the diagonal
+#pragma unroll 1
+    for (int i = warp; i < 64; i += 8) {
+        float2 qi[CP], ki[CP], gi[CP];
+#pragma unroll
+        for (int m = 0; m < CP; ++m) {
+            const int c = 2 * lane + 64 * m;
+            qi[m] = bf2(i, c);
+            ki[m] = bf2(64 + i, c);
+            gi[m] = g2p(i, c);
+        }
+#pragma unroll 1
+        for (int j0 = i & ~15; j0 <= i; j0 += 4) {  // j0 + 3 <= 63
+            float v[8];
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                float aq = 0.f, ak = 0.f;
+#pragma unroll
+                for (int m = 0; m < CP; ++m) {
+                    const int c = 2 * lane + 64 * m;
+                    // columns past i may overflow here; their sums are never stored
+                    const float2 k2 = bf2(64 + j0 + jj, c), g2 = g2p(j0 + jj, c);
+                    const float kx = k2.x * ex2_ftz(gi[m].x - g2.x);
+                    const float ky = k2.y * ex2_ftz(gi[m].y - g2.y);
+                    aq = fmaf(qi[m].y, ky, fmaf(qi[m].x, kx, aq));
+                    ak = fmaf(ki[m].y, ky, fmaf(ki[m].x, kx, ak));
+                }
+                v[jj] = aq;
+                v[4 + jj] = ak;
+            }
+            emit(i, j0, v);
+        }
+        for (int j = i + 1 + lane; j < 64; j += 32) {
+            *reinterpret_cast<__nv_bfloat16 *>(aqk + tile_off(i, j, 64)) =
+                __float2bfloat16_rn(0.f);
+            sL[akk_idx<kSplitA>(i, j)] = 0.f;
+        }
+    }
+}
+
 // ACT: the gate activation (kda_activation.A_log) is compiled in.
 // PADK: K < dk, the channels past K are zero (TMA fills them; otherwise K == dk
 // and the channel count is a compile-time constant).
@@ -634,110 +747,7 @@ __global__ void __launch_bounds__(256, 2)
     // and the eight sums (Aqk and the k gram of the four columns) are reduced over the
     // warp by halving exchanges (nine shuffles), lane 4 o ending with sum o.
     if (__builtin_expect(!fast, 0)) {
-        // lane l holds the channel pairs (2 l + 64 m, 2 l + 64 m + 1), m < dk / 64
-        constexpr int CP = KK / 64;
-        const auto bf2 = [&](int r, int c) {
-            return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(sAG + qk_off(r, c)));
-        };
-        const auto g2p = [&](int r, int c) {
-            return *reinterpret_cast<const float2 *>(sG2 + gsw(r, c));
-        };
-        // the reduction and the store of row i, columns j0 .. j0 + 3
-        const auto emit = [&](int i, int j0, const float (&v)[8]) {
-            const bool b4 = (lane >> 4) & 1, b3 = (lane >> 3) & 1, b2 = (lane >> 2) & 1;
-            float w[4], x[2];
-#pragma unroll
-            for (int t = 0; t < 4; ++t)
-                w[t] = (b4 ? v[4 + t] : v[t]) + __shfl_xor_sync(0xffffffffu, b4 ? v[t] : v[4 + t], 16);
-#pragma unroll
-            for (int t = 0; t < 2; ++t)
-                x[t] = (b3 ? w[2 + t] : w[t]) + __shfl_xor_sync(0xffffffffu, b3 ? w[t] : w[2 + t], 8);
-            float y = (b2 ? x[1] : x[0]) + __shfl_xor_sync(0xffffffffu, b2 ? x[0] : x[1], 4);
-            y += __shfl_xor_sync(0xffffffffu, y, 2);
-            y += __shfl_xor_sync(0xffffffffu, y, 1);
-            if ((lane & 3) == 0) {
-                const int j = j0 + 2 * b3 + b2;  // sum 4 b4 + 2 b3 + b2
-                if (!b4)
-                    *reinterpret_cast<__nv_bfloat16 *>(U + Lo.aqk + tile_off(i, j, 64)) =
-                        __float2bfloat16_rn(j <= i ? y : 0.f);
-                else
-                    sL[akk_idx<kSplitA>(i, j)] = j < i ? sBeta[i] * y : 0.f;
-            }
-        };
-        // off-diagonal blocks: item (block row I, four columns j0 < 16 I), 24 items;
-        // the columns' factors once per item, each of the block's 16 rows after it
-#pragma unroll 1
-        for (int it = warp; it < 24; it += 8) {
-            const int I = it < 4 ? 1 : (it < 12 ? 2 : 3);
-            const int e = 16 * I, j0 = 4 * (it - (I == 1 ? 0 : (I == 2 ? 4 : 12)));
-            float2 ge[CP], kb[4][CP];
-#pragma unroll
-            for (int m = 0; m < CP; ++m) {
-                const int c = 2 * lane + 64 * m;
-                ge[m] = g2p(e, c);
-#pragma unroll
-                for (int jj = 0; jj < 4; ++jj) {
-                    const float2 k2 = bf2(64 + j0 + jj, c), g2 = g2p(j0 + jj, c);
-                    kb[jj][m] = make_float2(k2.x * ex2_ftz(ge[m].x - g2.x), k2.y * ex2_ftz(ge[m].y - g2.y));
-                }
-            }
-#pragma unroll 1
-            for (int i = e; i < e + 16; ++i) {
-                float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int m = 0; m < CP; ++m) {
-                    const int c = 2 * lane + 64 * m;
-                    const float2 gi = g2p(i, c), q2 = bf2(i, c), k2 = bf2(64 + i, c);
-                    const float ax = ex2_ftz(gi.x - ge[m].x), ay = ex2_ftz(gi.y - ge[m].y);
-                    const float qx = q2.x * ax, qy = q2.y * ay, kx = k2.x * ax, ky = k2.y * ay;
-#pragma unroll
-                    for (int jj = 0; jj < 4; ++jj) {
-                        v[jj] = fmaf(qy, kb[jj][m].y, fmaf(qx, kb[jj][m].x, v[jj]));
-                        v[4 + jj] = fmaf(ky, kb[jj][m].y, fmaf(kx, kb[jj][m].x, v[4 + jj]));
-                    }
-                }
-                emit(i, j0, v);
-            }
-        }
-        // diagonal blocks: warp w takes rows i = w, w + 8, ..., the row's channels in
-        // registers, columns 16 floor(i / 16) .. i; zeros above the diagonal
-#pragma unroll 1
-        for (int i = warp; i < 64; i += 8) {
-            float2 qi[CP], ki[CP], gi[CP];
-#pragma unroll
-            for (int m = 0; m < CP; ++m) {
-                const int c = 2 * lane + 64 * m;
-                qi[m] = bf2(i, c);
-                ki[m] = bf2(64 + i, c);
-                gi[m] = g2p(i, c);
-            }
-#pragma unroll 1
-            for (int j0 = i & ~15; j0 <= i; j0 += 4) {  // j0 + 3 <= 63
-                float v[8];
-#pragma unroll
-                for (int jj = 0; jj < 4; ++jj) {
-                    float aq = 0.f, ak = 0.f;
-#pragma unroll
-                    for (int m = 0; m < CP; ++m) {
-                        const int c = 2 * lane + 64 * m;
-                        // columns past i may overflow here; their sums are never stored
-                        const float2 k2 = bf2(64 + j0 + jj, c), g2 = g2p(j0 + jj, c);
-                        const float kx = k2.x * ex2_ftz(gi[m].x - g2.x);
-                        const float ky = k2.y * ex2_ftz(gi[m].y - g2.y);
-                        aq = fmaf(qi[m].y, ky, fmaf(qi[m].x, kx, aq));
-                        ak = fmaf(ki[m].y, ky, fmaf(ki[m].x, kx, ak));
-                    }
-                    v[jj] = aq;
-                    v[4 + jj] = ak;
-                }
-                emit(i, j0, v);
-            }
-            for (int j = i + 1 + lane; j < 64; j += 32) {
-                *reinterpret_cast<__nv_bfloat16 *>(U + Lo.aqk + tile_off(i, j, 64)) =
-                    __float2bfloat16_rn(0.f);
-                sL[akk_idx<kSplitA>(i, j)] = 0.f;
-            }
-        }
+        exact_grams<KK, kSplitA>(sAG, sG2, sBeta, sL, U + Lo.aqk, warp, lane);
         __syncthreads();
     }
 
