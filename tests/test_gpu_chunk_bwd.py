@@ -397,3 +397,33 @@ def test_autograd_recomputing_backward(kda_lib):
                       ("h0", "dh0")):
         err = parity.rel_err(leaves[name].grad, ref[key])
         assert err <= TOL, (name, err)
+
+
+def test_saved_backward_grouped_value_heads(kda_lib):
+    """Two value heads per q/k head: the saved backward's dq and dk are summed over the
+    heads by atomics (order varies), so they match the recomputing call to rounding; the
+    rest bit for bit."""
+    inp = _small(1491, B=1, T=700, H=2, HV=4, K=128, V=128, g_hi=0.3)
+    dout, dht = _grads_in(inp, 1492)
+    ref = _run(kda_lib, inp, dout, dht)
+    _, _, saved = _save_fwd(kda_lib, inp)
+    got = kda_lib.chunk_kda_backward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], dout,
+                                     None, dht, saved=saved, want_dh0=True)
+    for name in NAMES:
+        if name in ("dq", "dk"):
+            assert parity.rel_err(got[name], ref[name]) <= 1e-5, name
+        else:
+            assert torch.equal(got[name], ref[name]), name
+    _check(got, _oracle(inp, dout, dht))
+
+
+def test_forward_save_refuses_the_saved_flag(kda_lib):
+    """KDA_FLAG_BWD_SAVED belongs to the backward: the saving forward refuses it."""
+    inp = _small(1495, B=1, T=64, H=1, HV=1, K=128, V=128)
+    q, k, v, g, beta = (inp[n] for n in ("q", "k", "v", "g", "beta"))
+    shape = kda_lib.make_shape(q, v, None, flags=kda_lib.KDA_FLAG_BWD_SAVED)
+    ws = torch.empty(kda_lib.kda_chunk_bwd_workspace_size(shape), dtype=torch.uint8, device="cuda")
+    o = torch.empty_like(v)
+    with pytest.raises(kda_lib.KdaError) as err:
+        kda_lib.kda_chunk_fwd_save(q, k, v, g, beta, None, None, shape, None, o, None, ws)
+    assert err.value.status == kda_lib.KDA_ERR_UNSUPPORTED
