@@ -9,7 +9,7 @@ HBM before the timed region; a 512 MiB buffer is written between timed steps
 to flush the 129 MB L2.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload train|gva|packed|decode|decode_small|prefill|prefill_small|
+                  [--workload train|train_wide_gate|gva|packed|decode|decode_small|prefill|prefill_small|
                               train_bwd|train_bwd_recurrent|train_step]
 
 `--workload` picks one of the other synthetic workloads instead (grouped value
@@ -49,6 +49,9 @@ FLUSH_BYTES = 512 << 20
 # name -> (kda_synth workload, overrides, default steps, default warm-up)
 WORKLOADS = {
     "train": (1, {}, 2000, 20),
+    # the training shape with per-token gates of -U(1.5, 3) (log2): every chunk's gate
+    # range (~144) past the split grams', so every chunk takes the exact-gram path
+    "train_wide_gate": (1, {"g_lo": 1.5, "g_hi": 3.0}, 500, 10),
     "gva": (2, {}, 500, 10),
     "packed": (3, {}, 300, 10),
     "decode": (4, {}, 100, 5),
@@ -75,6 +78,8 @@ E2E_MAX_H2D = 8 << 30        # larger inputs are not staged through pinned host 
 def _metric(name, w):
     if name == "train":
         return METRIC
+    if name == "train_wide_gate":
+        return f"chunk_kda fwd tokens/s ({w.name}, gates -U(1.5,3) log2 per token) on 1 GB300"
     if name == "train_bwd":
         return f"chunk_kda bwd tokens/s ({w.name}) on 1 GB300"
     if name == "train_step":
@@ -340,6 +345,7 @@ def workload_config(name, world=1):
         seqs, tokens = w.B, w.B * w.T
     return {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "HV": w.HV, "K": w.K, "V": w.V,
             "input_dtype": "bf16" if w.dtype == _bf16() else "f32", "gate_dtype": "f32",
+            "gate": f"-U({w.g_lo:g},{w.g_hi:g}) log2 per token",
             "h0": "N(0,0.1) fp32" if w.has_h0 else "none",
             "ht": "in place (ht == h0)" if recurrent else "stored",
             "pass": "backward" if name in BACKWARD else "forward",

@@ -251,13 +251,27 @@ template <int KK, bool kSplitA>
 __device__ __noinline__ void exact_grams(const unsigned char *sAG, const float *sG2,
                                          const float *sBeta, float *sL, unsigned char *aqk,
                                          const int warp, const int lane) {
-    // lane l holds the channel pairs (2 l + 64 m, 2 l + 64 m + 1), m < dk / 64
+    // lane l holds the channel pairs (2 l + 64 m, 2 l + 64 m + 1), m < dk / 64.  Its
+    // shared-memory offsets, from the swizzles: the q/k tile (qk_off) at
+    // m * 16 KB + r * 128 + ((((l / 4) % 8) ^ (r % 8)) << 4) + 4 (l % 4), the k rows 8 KB
+    // further; g2 (gsw) at (l / 16 + 2 m) * 8 KB + 4 r (32 r floats) + the 16-byte chunk
+    // ((l / 2) % 8) ^ (r % 8) + 8 (l % 2) bytes.  Addressed in the shared window.
     constexpr int CP = KK / 64;
-    const auto bf2 = [&](int r, int c) {
-        return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(sAG + qk_off(r, c)));
+    const uint32_t ag = (uint32_t)__cvta_generic_to_shared(sAG);
+    const uint32_t g2b = (uint32_t)__cvta_generic_to_shared(sG2);
+    const int L1 = (lane >> 2) & 7, L0 = (lane & 3) * 4;
+    const int G1 = (lane >> 1) & 7, G0 = (lane & 1) * 8 + (lane >> 4) * 8192;
+    const auto qrow = [&](int r) { return ag + (uint32_t)(r * 128 + ((L1 ^ (r & 7)) << 4) + L0); };
+    const auto grow = [&](int r) { return g2b + (uint32_t)(r * 128 + ((G1 ^ (r & 7)) << 4) + G0); };
+    const auto bf2 = [](uint32_t a) {
+        uint32_t x;
+        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(x) : "r"(a));
+        return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&x));
     };
-    const auto g2p = [&](int r, int c) {
-        return *reinterpret_cast<const float2 *>(sG2 + gsw(r, c));
+    const auto f2 = [](uint32_t a) {
+        float2 x;
+        asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(x.x), "=f"(x.y) : "r"(a));
+        return x;
     };
     // the reduction and the store of row i, columns j0 .. j0 + 3
     const auto emit = [&](int i, int j0, const float (&v)[8]) {
@@ -290,21 +304,22 @@ __device__ __noinline__ void exact_grams(const unsigned char *sAG, const float *
         float2 ge[CP], kb[4][CP];
 #pragma unroll
         for (int m = 0; m < CP; ++m) {
-            const int c = 2 * lane + 64 * m;
-            ge[m] = g2p(e, c);
+            ge[m] = f2(grow(e) + m * 16384);
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj) {
-                const float2 k2 = bf2(64 + j0 + jj, c), g2 = g2p(j0 + jj, c);
+                const float2 k2 = bf2(qrow(j0 + jj) + 8192 + m * 16384);
+                const float2 g2 = f2(grow(j0 + jj) + m * 16384);
                 kb[jj][m] = make_float2(k2.x * ex2_ftz(ge[m].x - g2.x), k2.y * ex2_ftz(ge[m].y - g2.y));
             }
         }
 #pragma unroll 1
         for (int i = e; i < e + 16; ++i) {
             float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            const uint32_t qa = qrow(i), ga = grow(i);
 #pragma unroll
             for (int m = 0; m < CP; ++m) {
-                const int c = 2 * lane + 64 * m;
-                const float2 gi = g2p(i, c), q2 = bf2(i, c), k2 = bf2(64 + i, c);
+                const float2 gi = f2(ga + m * 16384), q2 = bf2(qa + m * 16384),
+                             k2 = bf2(qa + 8192 + m * 16384);
                 const float ax = ex2_ftz(gi.x - ge[m].x), ay = ex2_ftz(gi.y - ge[m].y);
                 const float qx = q2.x * ax, qy = q2.y * ay, kx = k2.x * ax, ky = k2.y * ay;
 #pragma unroll
@@ -321,12 +336,12 @@ __device__ __noinline__ void exact_grams(const unsigned char *sAG, const float *
 #pragma unroll 1
     for (int i = warp; i < 64; i += 8) {
         float2 qi[CP], ki[CP], gi[CP];
+        const uint32_t qa = qrow(i), ga = grow(i);
 #pragma unroll
         for (int m = 0; m < CP; ++m) {
-            const int c = 2 * lane + 64 * m;
-            qi[m] = bf2(i, c);
-            ki[m] = bf2(64 + i, c);
-            gi[m] = g2p(i, c);
+            qi[m] = bf2(qa + m * 16384);
+            ki[m] = bf2(qa + 8192 + m * 16384);
+            gi[m] = f2(ga + m * 16384);
         }
 #pragma unroll 1
         for (int j0 = i & ~15; j0 <= i; j0 += 4) {  // j0 + 3 <= 63
@@ -334,11 +349,11 @@ __device__ __noinline__ void exact_grams(const unsigned char *sAG, const float *
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj) {
                 float aq = 0.f, ak = 0.f;
+                const uint32_t kja = qrow(j0 + jj) + 8192, gja = grow(j0 + jj);
 #pragma unroll
                 for (int m = 0; m < CP; ++m) {
-                    const int c = 2 * lane + 64 * m;
                     // columns past i may overflow here; their sums are never stored
-                    const float2 k2 = bf2(64 + j0 + jj, c), g2 = g2p(j0 + jj, c);
+                    const float2 k2 = bf2(kja + m * 16384), g2 = f2(gja + m * 16384);
                     const float kx = k2.x * ex2_ftz(gi[m].x - g2.x);
                     const float ky = k2.y * ex2_ftz(gi[m].y - g2.y);
                     aq = fmaf(qi[m].y, ky, fmaf(qi[m].x, kx, aq));
@@ -350,8 +365,7 @@ __device__ __noinline__ void exact_grams(const unsigned char *sAG, const float *
             emit(i, j0, v);
         }
         for (int j = i + 1 + lane; j < 64; j += 32) {
-            *reinterpret_cast<__nv_bfloat16 *>(aqk + tile_off(i, j, 64)) =
-                __float2bfloat16_rn(0.f);
+            *reinterpret_cast<__nv_bfloat16 *>(aqk + tile_off(i, j, 64)) = __float2bfloat16_rn(0.f);
             sL[akk_idx<kSplitA>(i, j)] = 0.f;
         }
     }
