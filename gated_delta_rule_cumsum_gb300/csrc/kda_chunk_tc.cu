@@ -115,7 +115,12 @@ struct PrepSmem {
     static constexpr uint32_t kbx = ag + (KK / 64) * kBlk;      // [kb; previous kg] tile
     static constexpr uint32_t g = kbx + (KK / 64) * kBlk;       // fp32 [64][KK] g2 (swizzled); later v + AB
     static constexpr uint32_t g_need0 = 64 * KK * 4;
-    static_assert(misc + 8 <= cur && cur + 96 <= ag && g % 1024 == 0, "prep layout");
+    // the exact grams' B operand (32 k rows, 128-byte swizzled), right after g2: dead
+    // space then (v and the tiles after g2 are written later in the unit)
+    static constexpr uint32_t khat = g + g_need0;
+    static constexpr uint32_t khat_end = khat + 32 * KK * 2;
+    static_assert(misc + 8 <= cur && cur + 96 <= ag && g % 1024 == 0 && khat % 1024 == 0,
+                  "prep layout");
     __host__ __device__ static constexpr uint32_t g_bytes(int VV) {
         return g_need0 > 64u * VV * 2 + 64 * 64 * 2 ? g_need0 : 64u * VV * 2 + 64 * 64 * 2;
     }
@@ -135,7 +140,8 @@ struct PrepSmem {
         return big ? ag : pbuf(VV) + 64 * 64 * 2;
     }
     __host__ __device__ static constexpr uint32_t used(int VV) {
-        return big ? extra(VV) : abuf(VV) + 64 * 64 * 4;
+        return big ? (extra(VV) > khat_end ? extra(VV) : khat_end)
+                   : (abuf(VV) + 64 * 64 * 4 > khat_end ? abuf(VV) + 64 * 64 * 4 : khat_end);
     }
     // Floor so that at most two CTAs (256 TMEM columns each) share an SM.
     __host__ __device__ static constexpr uint32_t total(int VV) {
@@ -246,16 +252,128 @@ __device__ __forceinline__ void strip_at(float4 &s, const float *A, int pr, int 
 
 // The exact gated grams of a chunk whose gate range is too wide to split (the comment
 // above its call site), out of line: cold code kept away from the prep's hot path.
-// aqk: the unit's Aqk tile; sL: L (fp32, akk_idx layout); warp, lane: the caller's.
+// Off-diagonal 16-row blocks: the gate of a pair i > j in different blocks is split
+// at a block boundary e between them, 2^(g2_i - g2_e) 2^(g2_e - g2_j), both exponents
+// <= 0, so the pair is the product of two bounded operands and the blocks go to the
+// tensor cores.  Two M = 64, N = 32 MMAs cover the six blocks: the boundary 32 serves
+// the four pairs of blocks {2, 3} x {0, 1}, the boundaries 16 and 48 the pairs (1, 0)
+// and (3, 2).  A operand (rows 0..63 of kbx, free in this path until L is written
+// there): the q rows of the later blocks scaled to e, then their k rows; B operand
+// (khat, 32 rows): the earlier blocks' k rows scaled from e.  Products of rows and
+// columns with different boundaries are formed too and discarded (every factor is
+// at most 1, so they stay finite).  The diagonal blocks take 2^(g2_i - g2_j) itself
+// per channel on the CUDA cores.
+// aqk: the unit's Aqk tile; sL: L (fp32, akk_idx layout); sKB: kbx; sKH: khat;
+// tmem: the CTA's accumulator (columns 0..63 used here); bar, phase: the MMA barrier
+// and its phase (two completions consumed).
 template <int KK, bool kSplitA>
 __device__ __noinline__ void exact_grams(const unsigned char *sAG, const float *sG2,
-                                         const float *sBeta, float *sL, unsigned char *aqk,
-                                         const int warp, const int lane) {
-    // lane l holds the channel pairs (2 l + 64 m, 2 l + 64 m + 1), m < dk / 64.  Its
-    // shared-memory offsets, from the swizzles: the q/k tile (qk_off) at
-    // m * 16 KB + r * 128 + ((((l / 4) % 8) ^ (r % 8)) << 4) + 4 (l % 4), the k rows 8 KB
-    // further; g2 (gsw) at (l / 16 + 2 m) * 8 KB + 4 r (32 r floats) + the 16-byte chunk
-    // ((l / 2) % 8) ^ (r % 8) + 8 (l % 2) bytes.  Addressed in the shared window.
+                                         const float *sBeta, float *sL, unsigned char *sKB,
+                                         unsigned char *sKH, unsigned char *aqk,
+                                         const uint32_t tmem, uint64_t *bar, uint32_t phase,
+                                         int32_t *status, const int tid) {
+    const int warp = tid >> 5, lane = tid & 31;
+    // ---- the off-diagonal blocks, one MMA group per boundary set
+#pragma unroll 1
+    for (int grp = 0; grp < 2; ++grp) {
+        // A rows r: side r / 32 (q, then k), row i of the chunk, boundary e
+#pragma unroll 1
+        for (int it = 0; it < KK / 32; ++it) {
+            const int idx = tid + it * 256, l = idx & 31, w = idx >> 5;
+            const int r = (w & 7) * 8 + (l & 7), c = ((w >> 3) * 4 + (l >> 3)) * 8;
+            const int rr = r & 31;
+            const int i = grp == 0 ? 32 + rr : 16 + rr + (rr & 16);
+            const int e = grp == 0 ? 32 : 16 + 2 * (rr & 16);
+            float f[8];
+            unpack8(*reinterpret_cast<const uint4 *>(sAG + qk_off((r >> 5) * 64 + i, c)), f);
+            const float4 gi0 = *reinterpret_cast<const float4 *>(sG2 + gsw(i, c));
+            const float4 gi1 = *reinterpret_cast<const float4 *>(sG2 + gsw(i, c + 4));
+            const float4 ge0 = *reinterpret_cast<const float4 *>(sG2 + gsw(e, c));
+            const float4 ge1 = *reinterpret_cast<const float4 *>(sG2 + gsw(e, c + 4));
+            f[0] *= ex2_ftz(gi0.x - ge0.x); f[1] *= ex2_ftz(gi0.y - ge0.y);
+            f[2] *= ex2_ftz(gi0.z - ge0.z); f[3] *= ex2_ftz(gi0.w - ge0.w);
+            f[4] *= ex2_ftz(gi1.x - ge1.x); f[5] *= ex2_ftz(gi1.y - ge1.y);
+            f[6] *= ex2_ftz(gi1.z - ge1.z); f[7] *= ex2_ftz(gi1.w - ge1.w);
+            *reinterpret_cast<uint4 *>(sKB + qk_off(r, c)) = pack8(f);
+        }
+        // B rows n: k row j of an earlier block, boundary e after it
+#pragma unroll 1
+        for (int it = 0; it < KK / 64; ++it) {
+            const int idx = tid + it * 256, l = idx & 31, w = idx >> 5;
+            const int n = (w & 3) * 8 + (l & 7), c = ((w >> 2) * 4 + (l >> 3)) * 8;
+            const int j = grp == 0 ? n : n + (n & 16);
+            const int e = grp == 0 ? 32 : 16 + 2 * (n & 16);
+            float f[8];
+            unpack8(*reinterpret_cast<const uint4 *>(sAG + qk_off(64 + j, c)), f);
+            const float4 gj0 = *reinterpret_cast<const float4 *>(sG2 + gsw(j, c));
+            const float4 gj1 = *reinterpret_cast<const float4 *>(sG2 + gsw(j, c + 4));
+            const float4 ge0 = *reinterpret_cast<const float4 *>(sG2 + gsw(e, c));
+            const float4 ge1 = *reinterpret_cast<const float4 *>(sG2 + gsw(e, c + 4));
+            f[0] *= ex2_ftz(ge0.x - gj0.x); f[1] *= ex2_ftz(ge0.y - gj0.y);
+            f[2] *= ex2_ftz(ge0.z - gj0.z); f[3] *= ex2_ftz(ge0.w - gj0.w);
+            f[4] *= ex2_ftz(ge1.x - gj1.x); f[5] *= ex2_ftz(ge1.y - gj1.y);
+            f[6] *= ex2_ftz(ge1.z - gj1.z); f[7] *= ex2_ftz(ge1.w - gj1.w);
+            *reinterpret_cast<uint4 *>(sKH + sw128_off(n, c, 32 * 128)) = pack8(f);
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (tid == 0) {
+            const uint32_t a0 = smem_addr(sKB), b0 = smem_addr(sKH);
+            const uint32_t idn = idesc_bf16(64, 32, false, false);
+#pragma unroll 1
+            for (int kk = 0; kk < KK / 16; ++kk) {
+                const uint32_t ko = (kk & 3) * 32;
+                mma_bf16(tmem + 32 * grp, sdesc_sw128(a0 + (kk >> 2) * 16384 + ko, 16, 1024),
+                         sdesc_sw128(b0 + (kk >> 2) * (32 * 128) + ko, 16, 1024), idn, kk > 0);
+            }
+            mma_commit(bar);
+            if (!mbar_wait(bar, phase & 1, kWaitNs)) report(status, KDA_DEVICE_TIMEOUT);
+        }
+        ++phase;
+        __syncthreads();
+        tc_fence_after();
+    }
+    // ---- their results (L's place in kbx is free now): an M = 64 result's row r sits
+    // in TMEM lane 32 (r / 16) + r % 16; this thread holds row r, columns 16 hs .. + 15
+    {
+        const int quad = warp & 3, grp = warp >> 2, hs = lane >> 4;
+        const int r = 16 * quad + (lane & 15);
+        float d[16];
+        tmem_ld16x2_16<16>(tmem_at(tmem, 32 * quad, 32 * grp), d);
+        int i = -1, j0 = 0;
+        if (grp == 0) {
+            i = quad < 2 ? 32 + r : r;
+            j0 = 16 * hs;
+        } else if (hs == (quad & 1)) {  // the pairs of the boundaries 16 and 48 only
+            i = quad == 0 ? 16 + r : (quad == 1 ? 32 + r : (quad == 2 ? r - 16 : r));
+            j0 = 32 * (quad & 1);
+        }
+        if (i >= 0) {
+            if (quad < 2) {
+#pragma unroll
+                for (int h = 0; h < 16; h += 8) {
+                    float a8[8];
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) a8[t] = d[h + t];
+                    *reinterpret_cast<uint4 *>(aqk + tile_off(i, j0 + h, 64)) = pack8(a8);
+                }
+            } else {
+                const float bi = sBeta[i];
+#pragma unroll
+                for (int h = 0; h < 16; h += 4)
+                    sta4<kSplitA>(sL, i, j0 + h,
+                                  make_float4(bi * d[h], bi * d[h + 1], bi * d[h + 2], bi * d[h + 3]));
+            }
+        }
+    }
+    // ---- the diagonal blocks.  lane l holds the channel pairs (2 l + 64 m, 2 l + 64 m
+    // + 1), m < dk / 64.  Its shared-memory offsets, from the swizzles: the q/k tile
+    // (qk_off) at m * 16 KB + r * 128 + ((((l / 4) % 8) ^ (r % 8)) << 4) + 4 (l % 4), the
+    // k rows 8 KB further; g2 (gsw) at (l / 16 + 2 m) * 8 KB + 4 r (32 r floats) + the
+    // 16-byte chunk ((l / 2) % 8) ^ (r % 8) + 8 (l % 2) bytes.  Addressed in the shared
+    // window.
     constexpr int CP = KK / 64;
     const uint32_t ag = (uint32_t)__cvta_generic_to_shared(sAG);
     const uint32_t g2b = (uint32_t)__cvta_generic_to_shared(sG2);
@@ -273,7 +391,9 @@ __device__ __noinline__ void exact_grams(const unsigned char *sAG, const float *
         asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(x.x), "=f"(x.y) : "r"(a));
         return x;
     };
-    // the reduction and the store of row i, columns j0 .. j0 + 3
+    // the reduction and the store of row i, columns j0 .. j0 + 3: the eight sums (Aqk
+    // and the k gram of the four columns) reduced over the warp by halving exchanges
+    // (nine shuffles), lane 4 o ending with sum o
     const auto emit = [&](int i, int j0, const float (&v)[8]) {
         const bool b4 = (lane >> 4) & 1, b3 = (lane >> 3) & 1, b2 = (lane >> 2) & 1;
         float w[4], x[2];
@@ -295,46 +415,12 @@ __device__ __noinline__ void exact_grams(const unsigned char *sAG, const float *
                 sL[akk_idx<kSplitA>(i, j)] = j < i ? sBeta[i] * y : 0.f;
         }
     };
-    // off-diagonal blocks: item (block row I, four columns j0 < 16 I), 24 items;
-    // the columns' factors once per item, each of the block's 16 rows after it
+    // warp w takes rows 16 b + w and 16 b + 15 - w of every block b (five column
+    // steps of four per block for every warp), the row's channels in registers,
+    // columns 16 b .. i; zeros above the diagonal
 #pragma unroll 1
-    for (int it = warp; it < 24; it += 8) {
-        const int I = it < 4 ? 1 : (it < 12 ? 2 : 3);
-        const int e = 16 * I, j0 = 4 * (it - (I == 1 ? 0 : (I == 2 ? 4 : 12)));
-        float2 ge[CP], kb[4][CP];
-#pragma unroll
-        for (int m = 0; m < CP; ++m) {
-            ge[m] = f2(grow(e) + m * 16384);
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-                const float2 k2 = bf2(qrow(j0 + jj) + 8192 + m * 16384);
-                const float2 g2 = f2(grow(j0 + jj) + m * 16384);
-                kb[jj][m] = make_float2(k2.x * ex2_ftz(ge[m].x - g2.x), k2.y * ex2_ftz(ge[m].y - g2.y));
-            }
-        }
-#pragma unroll 1
-        for (int i = e; i < e + 16; ++i) {
-            float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            const uint32_t qa = qrow(i), ga = grow(i);
-#pragma unroll
-            for (int m = 0; m < CP; ++m) {
-                const float2 gi = f2(ga + m * 16384), q2 = bf2(qa + m * 16384),
-                             k2 = bf2(qa + 8192 + m * 16384);
-                const float ax = ex2_ftz(gi.x - ge[m].x), ay = ex2_ftz(gi.y - ge[m].y);
-                const float qx = q2.x * ax, qy = q2.y * ay, kx = k2.x * ax, ky = k2.y * ay;
-#pragma unroll
-                for (int jj = 0; jj < 4; ++jj) {
-                    v[jj] = fmaf(qy, kb[jj][m].y, fmaf(qx, kb[jj][m].x, v[jj]));
-                    v[4 + jj] = fmaf(ky, kb[jj][m].y, fmaf(kx, kb[jj][m].x, v[4 + jj]));
-                }
-            }
-            emit(i, j0, v);
-        }
-    }
-    // diagonal blocks: warp w takes rows i = w, w + 8, ..., the row's channels in
-    // registers, columns 16 floor(i / 16) .. i; zeros above the diagonal
-#pragma unroll 1
-    for (int i = warp; i < 64; i += 8) {
+    for (int s = 0; s < 8; ++s) {
+        const int i = 16 * (s >> 1) + ((s & 1) ? 15 - warp : warp);
         float2 qi[CP], ki[CP], gi[CP];
         const uint32_t qa = qrow(i), ga = grow(i);
 #pragma unroll
@@ -752,16 +838,16 @@ __global__ void __launch_bounds__(256, 2)
     }
     const bool fast = __int_as_float(sRangeBits) <= kSafeRange;
 
-    // ---- exact grams for chunks whose gate range is too wide to split.  A column j
-    // of a 16-row block before row i's (j < e = 16 floor(i / 16) <= i) takes the gate
-    // through the block boundary, 2^(g2_i - g2_e) 2^(g2_e - g2_j), both exponents <= 0
-    // (ALGORITHM.md, "The numerics law": a boundary between the blocks separates the
-    // pair); the diagonal blocks take 2^(g2_i - g2_j) itself.  Lanes run over channel
-    // pairs (dk / 32 channels each); a warp forms four columns at a time for one row,
-    // and the eight sums (Aqk and the k gram of the four columns) are reduced over the
-    // warp by halving exchanges (nine shuffles), lane 4 o ending with sum o.
+    // ---- exact grams for chunks whose gate range is too wide to split.  A pair j < i
+    // in different 16-row blocks takes the gate through a block boundary e between
+    // them, 2^(g2_i - g2_e) 2^(g2_e - g2_j), both exponents <= 0 (ALGORITHM.md, "The
+    // numerics law": a boundary between the blocks separates the pair): two small
+    // tensor-core products of operands scaled to the boundaries.  The diagonal blocks
+    // take 2^(g2_i - g2_j) itself on the CUDA cores.
     if (__builtin_expect(!fast, 0)) {
-        exact_grams<KK, kSplitA>(sAG, sG2, sBeta, sL, U + Lo.aqk, warp, lane);
+        exact_grams<KK, kSplitA>(sAG, sG2, sBeta, sL, sKB, sm + S::khat, U + Lo.aqk, tmem, &bar,
+                                 phase, p.status, tid);
+        phase += 2;
         __syncthreads();
     }
 
