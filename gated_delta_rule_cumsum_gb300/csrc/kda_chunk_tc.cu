@@ -252,20 +252,20 @@ __device__ __forceinline__ void strip_at(float4 &s, const float *A, int pr, int 
 
 // The exact gated grams of a chunk whose gate range is too wide to split (the comment
 // above its call site), out of line: cold code kept away from the prep's hot path.
-// Off-diagonal 16-row blocks: the gate of a pair i > j in different blocks is split
-// at a block boundary e between them, 2^(g2_i - g2_e) 2^(g2_e - g2_j), both exponents
-// <= 0, so the pair is the product of two bounded operands and the blocks go to the
-// tensor cores.  Two M = 64, N = 32 MMAs cover the six blocks: the boundary 32 serves
-// the four pairs of blocks {2, 3} x {0, 1}, the boundaries 16 and 48 the pairs (1, 0)
-// and (3, 2).  A operand (rows 0..63 of kbx, free in this path until L is written
-// there): the q rows of the later blocks scaled to e, then their k rows; B operand
-// (khat, 32 rows): the earlier blocks' k rows scaled from e.  Products of rows and
-// columns with different boundaries are formed too and discarded (every factor is
-// at most 1, so they stay finite).  The diagonal blocks take 2^(g2_i - g2_j) itself
-// per channel on the CUDA cores.
+// Pairs j < i in different 4-row blocks: the gate is split at a block boundary e
+// between them, 2^(g2_i - g2_e) 2^(g2_e - g2_j), both exponents <= 0, so the pair is
+// the product of two bounded operands and goes to the tensor cores.  Four M = 64,
+// N = 32 MMAs, one per level of a halving of the chunk: level s (32, 16, 8, 4) pairs
+// the rows of the second half of every 2s-row block (A: their q rows, then their k
+// rows, scaled to the block's midpoint e) with the rows of its first half (B: k rows
+// scaled from e).  A lives in rows 0..63 of kbx (free in this path until L is written
+// there), B in khat.  Products of rows and columns of different blocks are formed
+// too and discarded (every factor is at most 1, so they stay finite).  What is left,
+// the 4 x 4 diagonal blocks, takes 2^(g2_i - g2_j) itself per channel on the CUDA
+// cores.
 // aqk: the unit's Aqk tile; sL: L (fp32, akk_idx layout); sKB: kbx; sKH: khat;
-// tmem: the CTA's accumulator (columns 0..63 used here); bar, phase: the MMA barrier
-// and its phase (two completions consumed).
+// tmem: the CTA's accumulator (columns 0..127 used here); bar, phase: the MMA
+// barrier and its phase (four completions consumed).
 template <int KK, bool kSplitA>
 __device__ __noinline__ void exact_grams(const unsigned char *sAG, const float *sG2,
                                          const float *sBeta, float *sL, unsigned char *sKB,
@@ -273,17 +273,18 @@ __device__ __noinline__ void exact_grams(const unsigned char *sAG, const float *
                                          const uint32_t tmem, uint64_t *bar, uint32_t phase,
                                          int32_t *status, const int tid) {
     const int warp = tid >> 5, lane = tid & 31;
-    // ---- the off-diagonal blocks, one MMA group per boundary set
+    // ---- the pairs in different 4-row blocks, one MMA per level
 #pragma unroll 1
-    for (int grp = 0; grp < 2; ++grp) {
-        // A rows r: side r / 32 (q, then k), row i of the chunk, boundary e
+    for (int grp = 0; grp < 4; ++grp) {
+        const int lg = 5 - grp, hsz = 1 << lg;  // level: half-blocks of hsz rows
+        // A rows r: side r / 32 (q, then k); row i of the chunk: the second half of
+        // block rr / hsz; boundary e: that block's midpoint
 #pragma unroll 1
         for (int it = 0; it < KK / 32; ++it) {
             const int idx = tid + it * 256, l = idx & 31, w = idx >> 5;
             const int r = (w & 7) * 8 + (l & 7), c = ((w >> 3) * 4 + (l >> 3)) * 8;
             const int rr = r & 31;
-            const int i = grp == 0 ? 32 + rr : 16 + rr + (rr & 16);
-            const int e = grp == 0 ? 32 : 16 + 2 * (rr & 16);
+            const int e = ((rr >> lg) << (lg + 1)) + hsz, i = e + (rr & (hsz - 1));
             float f[8];
             unpack8(*reinterpret_cast<const uint4 *>(sAG + qk_off((r >> 5) * 64 + i, c)), f);
             const float4 gi0 = *reinterpret_cast<const float4 *>(sG2 + gsw(i, c));
@@ -296,13 +297,12 @@ __device__ __noinline__ void exact_grams(const unsigned char *sAG, const float *
             f[6] *= ex2_ftz(gi1.z - ge1.z); f[7] *= ex2_ftz(gi1.w - ge1.w);
             *reinterpret_cast<uint4 *>(sKB + qk_off(r, c)) = pack8(f);
         }
-        // B rows n: k row j of an earlier block, boundary e after it
+        // B rows n: k row j of the first half of block n / hsz, boundary e its midpoint
 #pragma unroll 1
         for (int it = 0; it < KK / 64; ++it) {
             const int idx = tid + it * 256, l = idx & 31, w = idx >> 5;
             const int n = (w & 3) * 8 + (l & 7), c = ((w >> 2) * 4 + (l >> 3)) * 8;
-            const int j = grp == 0 ? n : n + (n & 16);
-            const int e = grp == 0 ? 32 : 16 + 2 * (n & 16);
+            const int e = ((n >> lg) << (lg + 1)) + hsz, j = e - hsz + (n & (hsz - 1));
             float f[8];
             unpack8(*reinterpret_cast<const uint4 *>(sAG + qk_off(64 + j, c)), f);
             const float4 gj0 = *reinterpret_cast<const float4 *>(sG2 + gsw(j, c));
@@ -335,36 +335,33 @@ __device__ __noinline__ void exact_grams(const unsigned char *sAG, const float *
         __syncthreads();
         tc_fence_after();
     }
-    // ---- their results (L's place in kbx is free now): an M = 64 result's row r sits
+    // ---- their results (L's place in kbx is free now).  An M = 64 result's row r sits
     // in TMEM lane 32 (r / 16) + r % 16; this thread holds row r, columns 16 hs .. + 15
+    // of levels w / 4 and w / 4 + 2, and stores the columns of its own block, four at
+    // a time (contiguous in j)
     {
-        const int quad = warp & 3, grp = warp >> 2, hs = lane >> 4;
-        const int r = 16 * quad + (lane & 15);
-        float d[16];
-        tmem_ld16x2_16<16>(tmem_at(tmem, 32 * quad, 32 * grp), d);
-        int i = -1, j0 = 0;
-        if (grp == 0) {
-            i = quad < 2 ? 32 + r : r;
-            j0 = 16 * hs;
-        } else if (hs == (quad & 1)) {  // the pairs of the boundaries 16 and 48 only
-            i = quad == 0 ? 16 + r : (quad == 1 ? 32 + r : (quad == 2 ? r - 16 : r));
-            j0 = 32 * (quad & 1);
-        }
-        if (i >= 0) {
-            if (quad < 2) {
+        const int quad = warp & 3, hs = lane >> 4;
+        const int r = 16 * quad + (lane & 15), rr = r & 31;
+#pragma unroll 1
+        for (int g2 = 0; g2 < 2; ++g2) {
+            const int grp = (warp >> 2) + 2 * g2, lg = 5 - grp, hsz = 1 << lg;
+            float d[16];
+            tmem_ld16x2_16<16>(tmem_at(tmem, 32 * quad, 32 * grp), d);
+            const int e = ((rr >> lg) << (lg + 1)) + hsz, i = e + (rr & (hsz - 1));
 #pragma unroll
-                for (int h = 0; h < 16; h += 8) {
-                    float a8[8];
-#pragma unroll
-                    for (int t = 0; t < 8; ++t) a8[t] = d[h + t];
-                    *reinterpret_cast<uint4 *>(aqk + tile_off(i, j0 + h, 64)) = pack8(a8);
+            for (int t = 0; t < 16; t += 4) {
+                const int n = 16 * hs + t;
+                if ((n >> lg) != (rr >> lg)) continue;
+                const int j = e - hsz + (n & (hsz - 1));
+                if (quad < 2) {
+                    __nv_bfloat162 h2[2] = {__floats2bfloat162_rn(d[t], d[t + 1]),
+                                            __floats2bfloat162_rn(d[t + 2], d[t + 3])};
+                    *reinterpret_cast<uint2 *>(aqk + tile_off(i, j, 64)) =
+                        *reinterpret_cast<const uint2 *>(h2);
+                } else {
+                    const float b = sBeta[i];
+                    sta4<kSplitA>(sL, i, j, make_float4(b * d[t], b * d[t + 1], b * d[t + 2], b * d[t + 3]));
                 }
-            } else {
-                const float bi = sBeta[i];
-#pragma unroll
-                for (int h = 0; h < 16; h += 4)
-                    sta4<kSplitA>(sL, i, j0 + h,
-                                  make_float4(bi * d[h], bi * d[h + 1], bi * d[h + 2], bi * d[h + 3]));
             }
         }
     }
@@ -415,12 +412,11 @@ __device__ __noinline__ void exact_grams(const unsigned char *sAG, const float *
                 sL[akk_idx<kSplitA>(i, j)] = j < i ? sBeta[i] * y : 0.f;
         }
     };
-    // warp w takes rows 16 b + w and 16 b + 15 - w of every block b (five column
-    // steps of four per block for every warp), the row's channels in registers,
-    // columns 16 b .. i; zeros above the diagonal
+    // warp w takes rows 8 b + w, b < 8, the row's channels in registers, columns
+    // 4 floor(i / 4) .. i of its 4-row block; zeros above the diagonal
 #pragma unroll 1
     for (int s = 0; s < 8; ++s) {
-        const int i = 16 * (s >> 1) + ((s & 1) ? 15 - warp : warp);
+        const int i = 8 * s + warp;
         float2 qi[CP], ki[CP], gi[CP];
         const uint32_t qa = qrow(i), ga = grow(i);
 #pragma unroll
@@ -430,7 +426,8 @@ __device__ __noinline__ void exact_grams(const unsigned char *sAG, const float *
             gi[m] = f2(ga + m * 16384);
         }
 #pragma unroll 1
-        for (int j0 = i & ~15; j0 <= i; j0 += 4) {  // j0 + 3 <= 63
+        {
+            const int j0 = i & ~3;
             float v[8];
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj) {
@@ -841,13 +838,13 @@ __global__ void __launch_bounds__(256, 2)
     // ---- exact grams for chunks whose gate range is too wide to split.  A pair j < i
     // in different 16-row blocks takes the gate through a block boundary e between
     // them, 2^(g2_i - g2_e) 2^(g2_e - g2_j), both exponents <= 0 (ALGORITHM.md, "The
-    // numerics law": a boundary between the blocks separates the pair): two small
-    // tensor-core products of operands scaled to the boundaries.  The diagonal blocks
-    // take 2^(g2_i - g2_j) itself on the CUDA cores.
+    // numerics law": a boundary between the blocks separates the pair): four small
+    // tensor-core products of operands scaled to the boundaries.  The 4 x 4 diagonal
+    // blocks take 2^(g2_i - g2_j) itself on the CUDA cores.
     if (__builtin_expect(!fast, 0)) {
         exact_grams<KK, kSplitA>(sAG, sG2, sBeta, sL, sKB, sm + S::khat, U + Lo.aqk, tmem, &bar,
                                  phase, p.status, tid);
-        phase += 2;
+        phase += 4;
         __syncthreads();
     }
 
