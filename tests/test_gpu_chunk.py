@@ -184,6 +184,47 @@ def test_wide_gate_range_chunks(kda_lib, lo, hi):
     _check(inp, o, ht, 2e-2)
 
 
+def _wide_gates(inp, seed, rows=None):
+    """-U(1.5, 3) log2 per token and channel (a chunk's range about 144) in the first
+    `rows` rows (all by default); the rest keep what they hold."""
+    g = inp["g"]
+    rows = g.shape[1] if rows is None else rows
+    gen = torch.Generator().manual_seed(seed)
+    w = -(1.5 + 1.5 * torch.rand((g.shape[0], rows) + tuple(g.shape[2:]), generator=gen))
+    g[:, :rows] = w.to(g.device)
+
+
+@pytest.mark.parametrize("K,V", [(64, 64), (64, 128), (128, 256)])
+def test_wide_gate_other_tile_sizes(kda_lib, K, V):
+    """Every chunk on the exact grams with 64-channel tiles (their tensor-core operand
+    then sits where L is later written) and with 256 value columns (inside v's region):
+    several chunks, a ragged tail, two value heads per q/k head."""
+    inp = _small(33, B=1, T=200, H=1, HV=2, K=K, V=V, dtype=torch.bfloat16)
+    _wide_gates(inp, 34)
+    o, ht = _run(kda_lib, inp)
+    _check(inp, o, ht, 2e-2)
+
+
+def test_wide_gate_packed(kda_lib):
+    """The exact grams on packed sequences: short and empty slots, chunks that end
+    inside a sequence's last rows, a NaN tail past the last offset."""
+    lens = [1, 0, 63, 64, 65, 0, 130, 7]
+    inp = _packed(35, lens, HV=2, H=1, K=128, V=128, dtype=torch.bfloat16)
+    _wide_gates(inp, 36, rows=sum(lens))
+    o, ht = _run(kda_lib, inp)
+    _check(inp, o, ht, 2e-2)
+
+
+def test_extreme_decay_bf16(kda_lib):
+    """g = -16 per step on the bf16 tensor-core path: every boundary factor past a few
+    rows underflows to zero, and the result is still the oracle's."""
+    inp = _small(37, B=1, T=130, H=1, HV=2, K=128, V=128, dtype=torch.bfloat16)
+    inp["g"].fill_(-16.0)
+    o, ht = _run(kda_lib, inp)
+    assert torch.isfinite(o).all() and torch.isfinite(ht).all()
+    _check(inp, o, ht, 2e-2)
+
+
 def test_mixed_extreme_and_mild_channels(kda_lib):
     inp = _small(8, T=128, K=128, V=64, dtype=torch.bfloat16)
     inp["g"][..., ::3] = -20.0
